@@ -1,0 +1,424 @@
+#!/usr/bin/env python
+"""Benchmark of the paged, quantized MoE expert layer on one GB300.
+
+Workload: the decode-shaped paged layer -- E=256 experts, H=2048, I=512 (3 MiB
+of FP8 weights per expert), top-8, CACHE_SLOTS=32 per layer with the LRU page
+table, router logits Zipf(1.1)-skewed with 0.7 reuse of a token slot's
+previous experts, refills of missed experts from pinned host memory on a side
+stream. A stack of L layers (each its own slot pool; one shared working
+buffer) is stepped round-robin, so the weights read per step come from HBM,
+not L2 (L * 32 slots * 3.16 MB > 129 MB L2).
+
+A step is one layer step: route -> permute -> LRU page table -> refills ->
+paged expert FFN -> combine, at T tokens (64 by default; T=1 and T=8 are
+reported too). `value` = tokens/s over K timed steps with inputs resident in
+HBM; `e2e` = the same through pqe_layer_step_host with pinned host x/logits/y
+copied inside every step.
+
+--impl reference times the CPU oracle on the same workload (bounded samples).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+CFG = synth.CONFIGS[2]
+METRIC = "MoE-layer tokens/s; % of HBM BW (decode) and FP8 tensor peak (batched)"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=512)
+    ap.add_argument("--warmup", type=int, default=16)
+    ap.add_argument("--impl", default="pqe", choices=["pqe", "reference"])
+    ap.add_argument("--T", type=int, default=64)
+    ap.add_argument("--layers", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the T=1 and T=8 lines")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---- distributed (replicas only: no data-path collective) -------------------------
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(ws, v: float, device) -> float:
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---- clocks ------------------------------------------------------------------------
+
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.idx), "-lms", "100"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---- workload ----------------------------------------------------------------------
+
+def expert_pages_host(pqe, torch, device):
+    """All E experts' FP8 pages (synthetic N(0,0.02) weights, quantised by the
+    library), pinned on the host: the host tier every layer refills from."""
+    E, H, I = CFG.E, CFG.H, CFG.I
+    stride = pqe.slot_stride(H, I)
+    host = torch.empty((E, stride), dtype=torch.uint8).pin_memory()
+    page = torch.zeros(stride, dtype=torch.uint8, device=device)
+    for e in range(E):
+        w13, w2 = synth.expert_weights(CFG, e)
+        pqe.pqe_pack_fp8_page(torch.from_numpy(w13).to(device), torch.from_numpy(w2).to(device), H, I, page)
+        host[e].copy_(page)
+    torch.cuda.synchronize()
+    return host
+
+
+def make_traces(T, L, n_steps):
+    """logits[i] for step i (layer i % L, that layer's trace step i // L)."""
+    traces = [synth.RoutingTrace(CFG, T, layer=l) for l in range(L)]
+    out = []
+    for i in range(n_steps):
+        out.append(traces[i % L].step(i // L))
+    return out
+
+
+class Runner:
+    def __init__(self, pqe, torch, device, host, L, max_T):
+        E, H, I, k, S = CFG.E, CFG.H, CFG.I, CFG.k, CFG.S
+        self.pqe, self.torch, self.device = pqe, torch, device
+        self.wb = pqe.alloc_working_buffer(E, H, I, device)
+        nbytes = [pqe.page_bytes(pqe.PQE_FMT_FP8, H, I)] * E
+        self.layers = [pqe.PagedMoELayer(E, H, I, k, S, E, max_T, host, nbytes, working_buffer=self.wb,
+                                         device=device) for _ in range(L)]
+        self.stream = torch.cuda.current_stream(device)
+        self.side = torch.cuda.Stream(device)
+
+    def close(self):
+        for l in self.layers:
+            l.close()
+
+
+def run_timed(r: Runner, T, logits_dev, xs_dev, y, warmup, K, ws, want_ffn=True):
+    torch, pqe = r.torch, r.pqe
+    L = len(r.layers)
+    total = warmup + K
+    assert len(logits_dev) >= total
+    infos = []
+    evs = []
+    if want_ffn:
+        for _ in range(K):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(r.stream)
+            b.record(r.stream)  # creates the events; the library records them again
+            evs.append((a, b))
+    for i in range(warmup):
+        layer = r.layers[i % L]
+        layer.set_ffn_events(None, None)
+        layer.step(xs_dev[i % len(xs_dev)], y, T, logits=logits_dev[i], stream=r.stream, side_stream=r.side)
+    torch.cuda.synchronize()
+    barrier(ws)
+    launches0 = pqe.kernel_launches()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(r.stream)
+    wall0 = time.perf_counter()
+    for j in range(K):
+        i = warmup + j
+        layer = r.layers[i % L]
+        if want_ffn:
+            layer.set_ffn_events(*evs[j])
+        info = layer.step(xs_dev[i % len(xs_dev)], y, T, logits=logits_dev[i], stream=r.stream, side_stream=r.side)
+        infos.append((info.n_routed, info.n_miss, info.working_buffer, info.h2d_bytes))
+    e1.record(r.stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier(ws)
+    launches = pqe.kernel_launches() - launches0
+    ms = e0.elapsed_time(e1)
+    for l in r.layers:
+        l.set_ffn_events(None, None)
+    ffn_ms = [a.elapsed_time(b) for a, b in evs] if want_ffn else []
+    return ms, wall, infos, ffn_ms, launches
+
+
+def ffn_bytes(n_routed, T):
+    """Algorithmic bytes of one moe_paged_ffn call: the routed experts' pages,
+    x once, out_perm once."""
+    return n_routed * CFG.page_bytes_fp8_with_scales + T * CFG.H * 2 + T * CFG.k * CFG.H * 2
+
+
+# page bytes incl. fp32 scales (3*H*I + 4*(2I+H))
+synth.LayerConfig.page_bytes_fp8_with_scales = property(lambda c: 3 * c.H * c.I + 4 * (2 * c.I + c.H))
+
+
+def cpu_oracle_sample(host_np, T, logits_list, budget_s=10.0, max_steps=16):
+    """The oracle (as it stands) on layer 0's trace steps: routing of all T
+    tokens, permutation, LRU step and the FFN of all T tokens; steps are run
+    until `budget_s` is spent. Returns (tokens, seconds, threads, steps)."""
+    import oracle
+    E, H, I, k = CFG.E, CFG.H, CFG.I, CFG.k
+    lay = {"w13": 0, "w2": 2 * I * H, "s13": 3 * I * H, "s2": 3 * I * H + 8 * I}
+    ex = oracle.ExpertSet(E)
+    for e in range(E):
+        p = host_np[e]
+        ex.set(e, 0, p[lay["w13"]:lay["w13"] + 2 * I * H].reshape(2 * I, H),
+               p[lay["s13"]:lay["s13"] + 8 * I].view(np.float32),
+               p[lay["w2"]:lay["w2"] + H * I].reshape(H, I), p[lay["s2"]:lay["s2"] + 4 * H].view(np.float32))
+    lru = oracle.LRU(E, CFG.S)
+    x = synth.activations(CFG, T, 0)
+    tokens, t_used, steps = 0, 0.0, 0
+    for s, lg in enumerate(logits_list[:max_steps]):
+        t0 = time.perf_counter()
+        ids, g = oracle.topk_gates(lg, k)
+        counts, offsets, perm_src, inv = oracle.permute(ids, E)
+        lru.step(counts)
+        oracle.moe_ffn(x, ids, g, ex, I)
+        t_used += time.perf_counter() - t0
+        tokens += T
+        steps += 1
+        if t_used >= budget_s:
+            break
+    return tokens, t_used, oracle.num_threads(), steps
+
+
+# ---- reference arm (the oracle) ----------------------------------------------------------
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    T, L = args.T, args.layers
+    E, H, I = CFG.E, CFG.H, CFG.I
+    # pages from the oracle's own quantiser (same bytes as the library's)
+    host = np.zeros((E, 3 * H * I + 4 * (2 * I + H)), np.uint8)
+    for e in range(E):
+        w13, w2 = synth.expert_weights(CFG, e)
+        q13, s13 = oracle.quant_e4m3_rows(w13)
+        q2, s2 = oracle.quant_e4m3_rows(w2)
+        host[e, :2 * I * H] = q13.reshape(-1)
+        host[e, 2 * I * H:3 * I * H] = q2.reshape(-1)
+        host[e, 3 * I * H:3 * I * H + 8 * I] = s13.view(np.uint8)
+        host[e, 3 * I * H + 8 * I:] = s2.view(np.uint8)
+    traces = make_traces(T, 1, args.warmup + args.steps)
+    # each step: one layer step of the oracle on a bounded token sample
+    n_tok = max(1, min(T, 8))
+    sub = [lg[:n_tok] for lg in traces]
+    _, _, threads, _ = cpu_oracle_sample(host, n_tok, sub[:args.warmup], budget_s=1e9, max_steps=args.warmup)
+    tok, secs, threads, steps = cpu_oracle_sample(host, n_tok, sub[args.warmup:], budget_s=1e9,
+                                                  max_steps=args.steps)
+    v = tok / secs
+    line = {"metric": METRIC, "value": v, "unit": "tokens/s", "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"decode-shaped paged MoE layer E=256 H=2048 I=512 top-8 CACHE_SLOTS=32, "
+                                   f"T={T}; oracle step on {n_tok} tokens", "T": T},
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": f"{steps} layer steps of {n_tok} tokens each"},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---- main arm ------------------------------------------------------------------------------
+
+def main():
+    args = parse_args()
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+    import torch
+    import paged_quantized_expert_gb300 as pqe
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pqe.load()
+    T, L, K, W = args.T, args.layers, args.steps, max(3, args.warmup)
+    host = expert_pages_host(pqe, torch, device)
+    r = Runner(pqe, torch, device, host, L, max(T, 64))
+    xs_dev = [torch.from_numpy(synth.activations(CFG, T, s).view(np.int16)).to(device) for s in range(4)]
+    logits_np = make_traces(T, L, W + K)
+    logits_dev = [torch.from_numpy(l).to(device) for l in logits_np]
+    y = torch.zeros((T, CFG.H), dtype=torch.bfloat16, device=device)
+
+    clocks = Clocks(local)
+    clocks.start()
+    ms, wall, infos, ffn_ms, launches = run_timed(r, T, logits_dev, xs_dev, y, W, K, ws)
+    clk = clocks.stop()
+    ms = max_over_ranks(ws, ms, device)
+    value = ws * T * K / (ms / 1e3)
+
+    # roofline of the FFN call (w13 + SwiGLU, w2; HBM-bound weight stream)
+    peak, peak_kind = peaks()
+    byts = [ffn_bytes(n, T) for (n, _, _, _) in infos]
+    ffn_total_ms = sum(ffn_ms)
+    achieved = sum(byts) / (ffn_total_ms / 1e3) / 1e9 if ffn_total_ms > 0 else None
+
+    # e2e: host buffers through pqe_layer_step_host
+    x_h = torch.from_numpy(synth.activations(CFG, T, 0).view(np.int16)).pin_memory()
+    y_h = torch.zeros((T, CFG.H), dtype=torch.bfloat16).pin_memory()
+    lg_h = [torch.from_numpy(l).pin_memory() for l in logits_np]
+    Ke = min(K, 128)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(r.stream)
+    for j in range(Ke):
+        i = W + j
+        r.layers[i % L].step_host(x_h, y_h, T, logits_host=lg_h[i], stream=r.stream, side_stream=r.side)
+    e1.record(r.stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(ws, e0.elapsed_time(e1), device)
+    e2e_value = ws * T * Ke / (e2e_ms / 1e3)
+
+    sweep = {}
+    if not args.no_sweep:
+        for Ts in (1, 8):
+            if Ts == T:
+                continue
+            lg_s = [torch.from_numpy(l).to(device) for l in make_traces(Ts, L, W + K)]
+            xs_s = [torch.from_numpy(synth.activations(CFG, Ts, s).view(np.int16)).to(device) for s in range(4)]
+            ys = torch.zeros((Ts, CFG.H), dtype=torch.bfloat16, device=device)
+            ms_s, _, inf_s, ffn_s, _ = run_timed(r, Ts, lg_s, xs_s, ys, W, K, ws)
+            b_s = [ffn_bytes(n, Ts) for (n, _, _, _) in inf_s]
+            sweep[f"T={Ts}"] = {"tokens_per_s": ws * Ts * K / (max_over_ranks(ws, ms_s, device) / 1e3),
+                                "ms_per_step": ms_s / K,
+                                "ffn_hbm_gbs": sum(b_s) / (sum(ffn_s) / 1e3) / 1e9 if sum(ffn_s) > 0 else None,
+                                "misses_per_step": float(np.mean([m for (_, m, _, _) in inf_s]))}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        tok, secs, threads, steps = cpu_oracle_sample(host.numpy(), T, make_traces(T, 1, 16), budget_s=10.0)
+        cpu = {"value": tok / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{steps} layer-0 trace steps x {T} tokens (route, permute, LRU, FFN of every token)"}
+
+    n_routed = [n for (n, _, _, _) in infos]
+    misses = [m for (_, m, _, _) in infos]
+    h2d = [b for (_, _, _, b) in infos]
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": W,
+            "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "fp8(e4m3) weights, bf16 activations, fp32 accumulate", "data": "synthetic",
+            "config": {"workload": "decode-shaped paged MoE layer (E=256, H=2048, I=512, top-8, "
+                                   "CACHE_SLOTS=32 LRU per layer, Zipf(1.1) routing with 0.7 reuse, "
+                                   "pinned-host refills)",
+                       "T": T, "layers_round_robin": L,
+                       "l2": f"inputs larger than L2: {L} layers x 32 slots x 3.16 MB of weights",
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                       "mean_routed_experts": float(np.mean(n_routed)), "mean_misses": float(np.mean(misses)),
+                       "working_buffer_steps": int(sum(w for (_, _, w, _) in infos)),
+                       "h2d_gb_per_s": (sum(h2d) / (ms / 1e3) / 1e9), "by_T": sweep},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": (achieved / peak) if achieved else None, "traffic": None,
+                         "kernel": "moe_paged_ffn (w13+SwiGLU and w2 weight streams)",
+                         "peak_kind": peak_kind,
+                         "ffn_ms_per_step": ffn_total_ms / K,
+                         "algorithmic_bytes_per_step": float(np.mean(byts))},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * CFG.H * 2 + T * CFG.E * 4,
+                    "d2h_bytes_per_step": T * CFG.H * 2},
+            "gpu_launches": int(launches),
+            "clocks": clk,
+        }
+        print(json.dumps(line))
+    r.close()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,436 @@
+/*
+ * pqe.h -- C ABI of libpqe.so: the MoE expert layer over paged, quantized
+ * expert weights, on one NVIDIA GB300 (sm_103a).
+ *
+ * The layer: top-k routing; a token-to-expert permutation that builds one
+ * contiguous batch per expert; a SwiGLU expert FFN that reads FP8 (or 4-bit)
+ * weights through an expert-to-slot page table into a fixed VRAM slot pool
+ * managed LRU per layer; a weighted combine; and GPU decode of host-tier
+ * pages whose FP8 exponents are Huffman-coded per row.
+ *
+ * Sources, cited by page and section:
+ *   [EP] vllm-expert-pager article (rand.pepabo.com, 2026-09-18):
+ *        "エキスパート重みの階層ページング" (per-layer slot pools, LRU,
+ *        working buffer), "重みの圧縮" (per-row exponent Huffman, GPU decode
+ *        after the copy), "評価"/表4 (code table resident in VRAM), and the
+ *        "w13_weight"/"w2_weight" names of vLLM's FP8 MoE weights.
+ *   [MG] MoE-Gen summary (aibr.jp), "3.中核となる技術的要素": module-based
+ *        batching (large per-expert batches) and overlap of host-to-device
+ *        transfer with compute.
+ *   [PW] PagedWeight commentary (spectral-agent.com), "技術的に面白い点":
+ *        page-unit weight management, per-expert bit-width from importance.
+ *
+ * Conventions for every call:
+ *   - Return value: PQE_OK (0) or a negative PQE_ERR_* code.
+ *   - Pointers marked "device" point to GPU memory owned by the caller
+ *     (allocated with any CUDA allocator); the library never frees them and
+ *     keeps no reference after the call returns. "host" pointers are CPU
+ *     memory; "pinned" means page-locked host memory (cudaHostAlloc).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Device calls are asynchronous on it unless stated otherwise.
+ *   - Arguments are checked on the host before any launch; a bad argument
+ *     returns PQE_ERR_INVALID_ARG and launches nothing.
+ *   - Errors found on the device (an out-of-range expert id, a corrupt
+ *     compressed stream, a page whose format tag is unknown) are OR-ed into a
+ *     caller-owned device int32 `status` word as PQE_STATUS_* bits; kernels
+ *     never trap. The caller clears the word and reads it after the stream
+ *     is synchronised.
+ *   - bf16 tensors are row-major with the innermost dimension contiguous.
+ *   - Shape limits: 1 <= k <= 32, k <= E <= 1024; H % 64 == 0, I % 64 == 0;
+ *     64 <= H <= 16384, 64 <= I <= 8192; T >= 0 (T == 0 is a no-op).
+ */
+#ifndef PQE_H
+#define PQE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PQE_API __attribute__((visibility("default")))
+#else
+#define PQE_API
+#endif
+
+#define PQE_OK 0
+#define PQE_ERR_INVALID_ARG (-1)
+#define PQE_ERR_CUDA (-2)
+#define PQE_ERR_CAPACITY (-3)
+#define PQE_ERR_CORRUPT (-4)
+#define PQE_ERR_TIMEOUT (-5)
+#define PQE_ERR_UNSUPPORTED (-6)
+
+/* bits OR-ed into the device status word */
+#define PQE_STATUS_BAD_EXPERT_ID 0x1  /* a routed id outside [0, E) */
+#define PQE_STATUS_CORRUPT_STREAM 0x2 /* a compressed row that does not decode */
+#define PQE_STATUS_BAD_PAGE 0x4       /* page table entry outside the pool, or unknown format */
+#define PQE_STATUS_TIMEOUT 0x8        /* a bounded device wait gave up */
+
+/* page formats (per expert page) */
+#define PQE_FMT_FP8 0   /* E4M3 weights, one fp32 scale per output row */
+#define PQE_FMT_MXFP4 1 /* E2M1 weights, one E8M0 scale per 32 weights along a row */
+
+/* Message for a PQE_* code; never NULL. */
+PQE_API const char *pqe_strerror(int code);
+
+/* Library ABI version (this header: 1). */
+PQE_API int pqe_abi_version(void);
+
+/* The cudaError_t of the last PQE_ERR_CUDA returned on this thread. */
+PQE_API int pqe_last_cuda_error(void);
+
+/* Kernels this library has launched in this process (all threads). */
+PQE_API uint64_t pqe_kernel_launches(void);
+
+/* ------------------------------------------------------------------------
+ * Expert pages and the slot pool  ([EP] 階層ページング; [PW] page-unit weights)
+ *
+ * One expert's weights form one page of contiguous bytes; the same byte
+ * layout is used in a VRAM slot and in a host-tier buffer, so a refill is one
+ * copy. FP8 page (offsets in bytes):
+ *   w13 [2I, H] E4M3 at 0        (rows 0..I-1 gate projection, I..2I-1 up)
+ *   w2  [H, I]  E4M3 at 2*I*H
+ *   s13 [2I]    fp32 at 3*I*H    (per-row scales; weight = e4m3(code) * s)
+ *   s2  [H]     fp32 at 3*I*H + 8*I
+ * MXFP4 page:
+ *   w13 [2I, H/2] E2M1 pairs at 0 (low nibble = even column)
+ *   w2  [H, I/2]  E2M1 pairs at I*H
+ *   x13 [2I, H/32] E8M0 at 3*I*H/2 (weight = e2m1 * 2^(x - 127))
+ *   x2  [H, I/32]  E8M0 at 3*I*H/2 + I*H/16
+ * A slot pool is n_slots cache slots of `slot_stride` bytes each (the LRU
+ * cache of one layer) plus n_wb working-buffer entries, used when one step
+ * needs more than n_slots experts. Page-table entry s < n_slots addresses
+ * base + s * slot_stride, entry n_slots + w addresses wb_base + w *
+ * slot_stride. The working buffer holds pages for one step only, so layers
+ * that run one after another on one stream may share it.
+ * ------------------------------------------------------------------------ */
+
+/* Bytes of one page in format fmt; 0 for bad arguments. */
+PQE_API size_t pqe_page_bytes(int fmt, int H, int I);
+
+/* Slot stride for (H, I): the FP8 page size rounded up to 4096 bytes. */
+PQE_API size_t pqe_slot_stride(int H, int I);
+
+typedef struct pqe_pool {
+    void *base;         /* device: n_slots * slot_stride bytes, 256-byte aligned */
+    void *wb_base;      /* device: n_wb * slot_stride bytes, 256-byte aligned (NULL if n_wb == 0) */
+    size_t slot_stride; /* == pqe_slot_stride(H, I) */
+    int32_t n_slots;    /* cache slots */
+    int32_t n_wb;       /* working-buffer entries */
+    int32_t H, I;
+} pqe_pool;
+
+/* Device address of page-table entry `dest` of the pool; NULL if outside it. */
+PQE_API void *pqe_pool_slot_addr(const pqe_pool *pool, int dest);
+
+/* Quantise fp32 weights [rows, cols] (device) to E4M3 codes (device, [rows,
+ * cols]) with one fp32 scale per row (device, [rows]): s = amax/448 in fp32
+ * (1 for an all-zero row), code = RNE_e4m3(w / s) with the quotient in fp32,
+ * saturating at 448. This is the configs' "quantized to FP8 e4m3 with per-row
+ * fp32 scales"; it prepares pages and is not on the per-step path. */
+PQE_API int pqe_quantize_fp8_rows(const float *w, int rows, int cols, uint8_t *q, float *scale, void *stream);
+
+/* 4-bit copy of an FP8 matrix ([PW]: lower-bit pages; the FP8 master copy is
+ * kept, [EP] 位置づけ). From v = fp32(e4m3(q)) * s (fp32 product), per block
+ * of 32 along a row: X = 2^(floor(log2 amax) - 2) as E8M0 (byte 0 for an
+ * all-zero block), element RNE_e2m1(v / X) saturating at 6 (OCP MX v1.0).
+ * q8 [rows, cols] and s8 [rows] device in; q4 [rows, cols/2] and x8
+ * [rows, cols/32] device out. cols % 32 == 0. */
+PQE_API int pqe_quantize_mxfp4_rows(const uint8_t *q8, const float *s8, int rows, int cols, uint8_t *q4,
+                            uint8_t *x8, void *stream);
+
+/* Pack one FP8 page (device) from fp32 weights w13 [2I, H] and w2 [H, I]
+ * (device): both matrices quantised with pqe_quantize_fp8_rows into the
+ * page's sections. */
+PQE_API int pqe_pack_fp8_page(const float *w13, const float *w2, int H, int I, uint8_t *page, void *stream);
+
+/* Pack the 4-bit page (device) of an FP8 page (device) with
+ * pqe_quantize_mxfp4_rows on both matrices. */
+PQE_API int pqe_pack_mxfp4_page(const uint8_t *fp8_page, int H, int I, uint8_t *fp4_page, void *stream);
+
+/* ------------------------------------------------------------------------
+ * moe_route -- top-k routing ([EP] 階層ページング: each token uses a few
+ * experts; [MG] §3). The pages give no formula; the plain MoE reading is used.
+ *   logits[t,e] = sum_h x[t,h] * w_router[e,h] in fp32 when w_router is not
+ *     NULL; the reduction order is fixed (32 strided partial sums with fused
+ *     multiply-add, h = l, l+32, ..., then a pairwise tree over offsets 16, 8,
+ *     4, 2, 1), so the logits, and with them the top-k choice, are
+ *     reproducible bit for bit.
+ *   top-k: the k largest logits, the lower expert id on an exact tie; ids are
+ *     ordered by logit descending, then id ascending.
+ *   gates: softmax over the k picked (the full softmax renormalised to them).
+ * x_bf16   device bf16 [T, H] (read only when w_router != NULL)
+ * w_router device fp32 [E, H] or NULL
+ * logits   device fp32 [T, E]: output when w_router != NULL (may then be NULL
+ *          to skip storing), input otherwise. Inputs must be finite.
+ * topk_ids device int32 [T, k] out; topk_w device fp32 [T, k] out.
+ * ------------------------------------------------------------------------ */
+PQE_API int moe_route(const void *x_bf16, const float *w_router, float *logits, int T, int H, int E, int k,
+              int32_t *topk_ids, float *topk_w, void *stream);
+
+/* ------------------------------------------------------------------------
+ * moe_permute -- token-to-expert permutation: one contiguous batch per expert
+ * ([MG] §3, module-based batching). Stable counting sort of the assignments
+ * f = t*k + j by expert id:
+ *   counts[e] = #{f : topk_ids[f] == e}; offsets = exclusive prefix sum, E+1;
+ *   within an expert, assignments keep ascending f;
+ *   perm_src[p] = the f at batch position p; inv[f] = p.
+ * The result is unique and deterministic.
+ * topk_ids device int32 [T*k]; counts device int32 [E]; offsets device int32
+ * [E+1]; perm_src, inv device int32 [T*k]. ws: device scratch of at least
+ * moe_permute_workspace_size(T, k, E) bytes, 256-byte aligned. status: device
+ * int32; an id outside [0, E) sets PQE_STATUS_BAD_EXPERT_ID and that
+ * assignment is dropped from the counts (perm_src/inv then hold -1 for it).
+ * ------------------------------------------------------------------------ */
+PQE_API size_t moe_permute_workspace_size(int T, int k, int E);
+PQE_API int moe_permute(const int32_t *topk_ids, int T, int k, int E, int32_t *counts, int32_t *offsets,
+                int32_t *perm_src, int32_t *inv, void *ws, size_t ws_bytes, int32_t *status,
+                void *stream);
+
+/* ------------------------------------------------------------------------
+ * moe_paged_ffn -- grouped SwiGLU expert FFN over the slot pool ([EP]
+ * 階層ページング for the paging, 評価 for w13/w2; [PW] for 4-bit pages).
+ * For each expert e with a non-empty batch, its page is read from slot
+ * page_table[e] of the pool, and for each batch position p in
+ * [offsets[e], offsets[e+1]), with token t = perm_src[p] / k:
+ *   u = W13_e x_t;  h = SiLU(u[0:I]) * u[I:2I];  out_perm[p] = W2_e h.
+ * x_bf16     device bf16 [T, H]
+ * perm_src, offsets: from moe_permute (device)
+ * page_table device int32 [E]: slot of each routed expert, -1 if unrouted
+ * expert_fmt device uint8 [E]: PQE_FMT_* of each expert's page, or NULL for
+ *            all FP8
+ * pool       host struct describing the device slot pool
+ * out_perm   device bf16 [T*k, H] out
+ * ws         device scratch, >= moe_paged_ffn_workspace_size(...) bytes
+ * status     device int32; a routed expert whose slot is outside the pool or
+ *            whose format is unknown sets PQE_STATUS_BAD_PAGE and its rows of
+ *            out_perm are zero.
+ * Work is dispatched on the device per expert batch: small batches take a
+ * weight-streaming CUDA-core path, large ones the tensor-core path.
+ * ------------------------------------------------------------------------ */
+PQE_API size_t moe_paged_ffn_workspace_size(int T, int k, int E, int H, int I);
+PQE_API int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *offsets,
+                  const int32_t *page_table, const uint8_t *expert_fmt, const pqe_pool *pool, int T,
+                  int k, int E, void *out_perm, void *ws, size_t ws_bytes, int32_t *status,
+                  void *stream);
+
+/* ------------------------------------------------------------------------
+ * moe_combine -- y[t] = sum_j topk_w[t,j] * out_perm[inv[t*k+j]] with fp32
+ * accumulation in ascending j, bf16 output (the weighted sum that closes a
+ * MoE layer; the pages do not spell it out).
+ * out_perm device bf16 [T*k, H]; inv device int32 [T*k]; topk_w device fp32
+ * [T, k]; y device bf16 [T, H] out. An inv entry of -1 contributes nothing.
+ * ------------------------------------------------------------------------ */
+PQE_API int moe_combine(const void *out_perm, const int32_t *inv, const float *topk_w, int T, int k, int H,
+                void *y_bf16, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Per-layer LRU slot pool on the host ([EP] 階層ページング: each MoE layer owns
+ * its slots, one expert per slot, managed LRU; a miss is copied in; a step
+ * that needs more experts than slots switches to a working buffer).
+ * Rules (the pages say only "LRU"):
+ *   U = {e : counts[e] > 0}.
+ *   |U| > S: working-buffer step; slot state untouched (no eviction, no
+ *     recency update); resident experts are read in place; every
+ *     non-resident e in U gets entry S + w, w its rank among them by id.
+ *   |U| <= S: hits refresh last_use = step; misses in ascending id take the
+ *     lowest empty slot, else the slot with the smallest last_use whose expert
+ *     is not in U (ties: lowest slot index).
+ *   page_table[e] = slot or S + w for e in U, -1 otherwise; the step counter
+ *   advances by one per call.
+ * ------------------------------------------------------------------------ */
+typedef struct pqe_lru pqe_lru;
+
+/* New state with S empty slots for E experts; NULL on bad arguments. */
+PQE_API pqe_lru *pqe_lru_create(int E, int S);
+PQE_API void pqe_lru_destroy(pqe_lru *st);
+
+/* Copy out slot->expert [S] (-1 empty), last_use [S] and the step counter. */
+PQE_API int pqe_lru_state(const pqe_lru *st, int32_t *slot_expert, int64_t *last_use, int64_t *step);
+
+/* Forget expert e's resident copy (its slot becomes empty), e.g. after its
+ * page changed format. */
+PQE_API int pqe_lru_invalidate(pqe_lru *st, int expert);
+
+/* One step (host only, no CUDA call). counts_host [E] in; page_table_host
+ * [E] out; miss_expert / miss_dest [E] out: the n_miss experts to copy and
+ * their destination (slot, or S + w); working_buffer_mode out (0/1). */
+PQE_API int page_table_update(pqe_lru *st, const int32_t *counts_host, int32_t *page_table_host,
+                      int32_t *miss_expert, int32_t *miss_dest, int32_t *n_miss,
+                      int32_t *working_buffer_mode);
+
+/* ------------------------------------------------------------------------
+ * slot_fill -- refill one slot from the host tier ([EP] 階層ページング: a
+ * missing expert is copied from its RAM slot; [MG] §3: transfers overlap
+ * compute). One cudaMemcpyAsync of `bytes` from pinned_src (pinned host, one
+ * page in the layout above) to slot `dest` of the pool, on `stream` (a side
+ * stream), then cudaEventRecord(done_event) if done_event is not NULL.
+ * bytes <= pool->slot_stride.
+ * ------------------------------------------------------------------------ */
+PQE_API int slot_fill(const pqe_pool *pool, int dest, const void *pinned_src, size_t bytes, void *stream,
+              void *done_event);
+
+/* ------------------------------------------------------------------------
+ * Compressed host tier ([EP] 重みの圧縮: per row of each expert weight matrix
+ * the FP8 exponent field is Huffman-coded, the rest kept raw; decoded on the
+ * GPU right after the copy to VRAM; 表4: the code table stays in VRAM).
+ * Format (the pages fix only the above):
+ *   symbol = (byte >> 3) & 15; raw nibble = (byte >> 7) << 3 | (byte & 7);
+ *   one canonical prefix code per matrix (w13 and w2 of each expert), lengths
+ *   <= 12, optimal for the matrix's symbol histogram (package-merge; at equal
+ *   weight a symbol item precedes a package, symbols by id, packages by
+ *   creation order); canonical code values in (length, symbol) order;
+ *   each row its own MSB-first bitstream of uint32 words starting on a word
+ *   boundary; rows cut into chunks of 64 symbols with a uint16 bit offset per
+ *   chunk; raw nibbles two per byte, low nibble = even column.
+ * Compressed page: a 256-byte header then 256-byte aligned sections:
+ *   scales (s13 then s2, fp32), w13 {row_word [2I+1] u32, chunk_bit
+ *   [2I*H/64] u16, nibbles [2I*H/2], words}, w2 {row_word [H+1], chunk_bit
+ *   [H*I/64], nibbles [H*I/2], words}.
+ * Code table: 4096 bytes per matrix, entry for a 12-bit window w = (symbol
+ * << 4) | length of the code that prefixes w, 0 if none.
+ * ------------------------------------------------------------------------ */
+
+#define PQE_HUFF_LUT_BYTES 4096
+
+/* Upper bound of a compressed FP8 page for (H, I). */
+PQE_API size_t pqe_huff_page_bound(int H, int I);
+
+/* Host: compress one FP8 page (host bytes, layout above) into out (host,
+ * out_cap bytes). Writes the page size to *out_bytes and the two code tables
+ * to lut13 / lut2 (host, PQE_HUFF_LUT_BYTES each). */
+PQE_API int pqe_huff_encode_page(const uint8_t *fp8_page, int H, int I, void *out, size_t out_cap,
+                         size_t *out_bytes, uint8_t *lut13, uint8_t *lut2);
+
+/* Code lengths [16] of a compressed page's two matrices (host page). */
+PQE_API int pqe_huff_page_lengths(const void *comp_page, uint8_t *len13, uint8_t *len2);
+
+/* Host: the code table (PQE_HUFF_LUT_BYTES) of canonical code lengths [16]. */
+PQE_API int pqe_huff_build_lut(const uint8_t *lengths, uint8_t *lut);
+
+/* fp8_exp_huff_decode -- GPU decode of one compressed page (device) into an
+ * FP8 page (device, e.g. a slot). lut13 / lut2: resident device code tables
+ * of that expert. A row that does not decode sets PQE_STATUS_CORRUPT_STREAM;
+ * its bytes are then unspecified. comp_bytes bounds every read. */
+PQE_API int fp8_exp_huff_decode(const void *comp_page, size_t comp_bytes, const uint8_t *lut13,
+                        const uint8_t *lut2, int H, int I, uint8_t *fp8_page, int32_t *status,
+                        void *stream);
+
+/* slot_fill_compressed -- H2D copy of a compressed page (pinned) into a device
+ * staging buffer, then fp8_exp_huff_decode into slot `dest`, both on
+ * `stream`; done_event recorded after the decode. */
+PQE_API int slot_fill_compressed(const pqe_pool *pool, int dest, const void *pinned_comp, size_t comp_bytes,
+                         void *staging, size_t staging_bytes, const uint8_t *lut13,
+                         const uint8_t *lut2, int32_t *status, void *stream, void *done_event);
+
+/* ------------------------------------------------------------------------
+ * Per-expert bit-width from importance ([PW] 技術的に面白い点: the router's
+ * choices estimate each expert's importance; important experts keep more
+ * bits). Importance m_e is an exponential moving average of the gate mass
+ * per token: m_e <- alpha*m_e + (1-alpha) * (sum_{t,j: ids=e} g[t,j]) / T,
+ * summed in ascending (t, j) in fp64. After steps every-1, 2*every-1, ... the
+ * experts are ranked (m descending, ties to the lower id); the top n_hi get
+ * PQE_FMT_FP8, the rest PQE_FMT_MXFP4. Host only.
+ * m host fp64 [E] in/out; ids host int32 [T*k]; gates host fp32 [T*k];
+ * fmt host uint8 [E] in/out; *reranked set to 1 when the formats were
+ * re-ranked at this step.
+ * ------------------------------------------------------------------------ */
+PQE_API int pqe_importance_step(double *m, const int32_t *ids, const float *gates, int T, int k, int E,
+                        double alpha, int64_t step, int every, int n_hi, uint8_t *fmt,
+                        int32_t *reranked);
+
+/* Rank without an update: the top n_hi of m get FP8, the rest MXFP4. */
+PQE_API int pqe_rank_formats(const double *m, int E, int n_hi, uint8_t *fmt);
+
+/* ------------------------------------------------------------------------
+ * Layer runtime -- one MoE layer over its own slot pool, one call per step.
+ * A step: moe_route -> moe_permute -> per-expert counts to the host (the one
+ * host synchronisation of a step; the LRU state lives on the host) ->
+ * page_table_update -> for each miss slot_fill (or slot_fill_compressed) on
+ * the side stream -> the compute stream waits for the refills -> page table
+ * to the device -> moe_paged_ffn -> moe_combine. Sources: [EP]
+ * 階層ページング and 重みの圧縮; [MG] §3 (transfers on their own stream).
+ * ------------------------------------------------------------------------ */
+typedef struct pqe_layer_config {
+    int32_t E, H, I, k;
+    int32_t S;          /* cache slots */
+    int32_t W;          /* working-buffer entries; pool->n_slots == S, pool->n_wb == W */
+    int32_t max_T;      /* largest token count of a step */
+    int32_t compressed; /* host pages are compressed pages (decoded after the copy) */
+} pqe_layer_config;
+
+typedef struct pqe_step_info {
+    int32_t n_routed;       /* |U|: experts with a non-empty batch */
+    int32_t n_miss;         /* pages copied in by this step */
+    int32_t working_buffer; /* 1 when |U| > S */
+    int32_t pad;
+    int64_t h2d_bytes;      /* bytes of host pages copied by this step */
+} pqe_step_info;
+
+typedef struct pqe_layer_buffers_t {
+    int32_t *status;   /* device status word of the layer's kernels */
+    int32_t *topk_ids; /* [max_T*k] of the last step */
+    float *topk_w;
+    int32_t *counts, *offsets, *perm_src, *inv, *page_table;
+    void *out_perm;    /* bf16 [max_T*k, H] */
+    void *x_in;        /* bf16 [max_T, H] staging used by pqe_layer_step_host */
+    float *logits_in;  /* fp32 [max_T, E] staging used by pqe_layer_step_host */
+    void *y_out;       /* bf16 [max_T, H] staging used by pqe_layer_step_host */
+} pqe_layer_buffers_t;
+
+typedef struct pqe_layer pqe_layer;
+
+/* Device scratch a layer needs (0 for a bad config). */
+PQE_API size_t pqe_layer_scratch_bytes(const pqe_layer_config *cfg);
+
+/* host_pages [E]: pinned pointer of each expert's page (compressed page when
+ * cfg->compressed), host_page_bytes [E] its size; luts_dev: device code tables
+ * [E][2][PQE_HUFF_LUT_BYTES] (w13 then w2), required when compressed;
+ * expert_fmt_dev: device [E] PQE_FMT_* or NULL (all FP8); scratch_dev:
+ * device, 256-byte aligned, >= pqe_layer_scratch_bytes(cfg). The layer keeps
+ * these pointers (caller-owned) and allocates only small pinned host buffers
+ * and two CUDA events of its own. NULL on bad arguments or allocation failure. */
+PQE_API pqe_layer *pqe_layer_create(const pqe_layer_config *cfg, const pqe_pool *pool,
+                                    const void *const *host_pages, const size_t *host_page_bytes,
+                                    const uint8_t *luts_dev, const uint8_t *expert_fmt_dev,
+                                    void *scratch_dev, size_t scratch_bytes);
+PQE_API void pqe_layer_destroy(pqe_layer *L);
+
+/* Point expert e at a new host page (e.g. after its format changed) and
+ * forget its resident copy, so its next use refills the slot. */
+PQE_API int pqe_layer_set_host_page(pqe_layer *L, int expert, const void *pinned_page, size_t bytes);
+
+/* Device pointers of the layer's internal buffers. */
+PQE_API int pqe_layer_buffers(pqe_layer *L, pqe_layer_buffers_t *out);
+
+/* Optional CUDA events (timing-enabled, created by the caller) recorded on
+ * the compute stream right before and right after the FFN of the next step;
+ * NULL, NULL to stop. For measuring the FFN inside whole steps. */
+PQE_API int pqe_layer_set_ffn_events(pqe_layer *L, void *ev_begin, void *ev_end);
+
+/* The layer's LRU state (see pqe_lru_state). */
+PQE_API int pqe_layer_lru_state(const pqe_layer *L, int32_t *slot_expert, int64_t *last_use, int64_t *step);
+
+/* One step on device inputs: x_dev bf16 [T, H]; either w_router_dev fp32
+ * [E, H] (logits computed, written to logits_dev if not NULL) or logits_dev
+ * fp32 [T, E] given; y_dev bf16 [T, H] out. Blocks the host once, until the
+ * routing counts are known. side_stream NULL = refills on `stream`. A working-
+ * buffer step with more misses than W returns PQE_ERR_CAPACITY. */
+PQE_API int pqe_layer_step(pqe_layer *L, const void *x_dev, const float *w_router_dev, float *logits_dev,
+                           int T, void *y_dev, void *stream, void *side_stream, pqe_step_info *info);
+
+/* The same step on host buffers (pinned for asynchronous copies): x_host bf16
+ * [T, H] and logits_host fp32 [T, E] are copied in, y_host bf16 [T, H] is
+ * copied out; returns after the stream is synchronised. */
+PQE_API int pqe_layer_step_host(pqe_layer *L, const void *x_host, const float *w_router_dev,
+                                const float *logits_host, int T, void *y_host, void *stream,
+                                void *side_stream, pqe_step_info *info);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PQE_H */

@@ -51,21 +51,39 @@ EXPORT double orc_e4m3_value(uint8_t b)
     return s ? -v : v;
 }
 
+/* the 256 decoded values, filled once from orc_e4m3_value (a cache, same values) */
+static double e4m3_table[256];
+static int e4m3_table_ready = 0;
+
+static double e4m3_cached(uint8_t b)
+{
+    if (!e4m3_table_ready) {
+#pragma omp critical(orc_e4m3_table)
+        {
+            if (!e4m3_table_ready) {
+                for (int i = 0; i < 256; ++i) e4m3_table[i] = orc_e4m3_value((uint8_t)i);
+                e4m3_table_ready = 1;
+            }
+        }
+    }
+    return e4m3_table[b];
+}
+
 /* Codes 0x00..0x7E hold the non-negative finite values in increasing order.
  * Round |v| to the nearest of them; on an exact tie take the even code (its
  * mantissa LSB is 0: round half to even); beyond 448 saturate to 448. */
 static uint8_t e4m3_magnitude_code(double a)
 {
     int lo = 0, hi = 0x7E;
-    if (a >= orc_e4m3_value(0x7E)) return 0x7E;
+    if (a >= e4m3_cached(0x7E)) return 0x7E;
     /* largest code with value <= a */
     while (lo < hi) {
         int mid = (lo + hi + 1) / 2;
-        if (orc_e4m3_value((uint8_t)mid) <= a) lo = mid; else hi = mid - 1;
+        if (e4m3_cached((uint8_t)mid) <= a) lo = mid; else hi = mid - 1;
     }
     {
-        double below = orc_e4m3_value((uint8_t)lo);
-        double above = orc_e4m3_value((uint8_t)(lo + 1));
+        double below = e4m3_cached((uint8_t)lo);
+        double above = e4m3_cached((uint8_t)(lo + 1));
         double dlo = a - below, dhi = above - a;
         if (dlo < dhi) return (uint8_t)lo;
         if (dhi < dlo) return (uint8_t)(lo + 1);
@@ -426,7 +444,7 @@ typedef struct {
 static double weight_at(int fmt, const uint8_t *w, const void *s, int cols, int r, int c)
 {
     size_t idx = (size_t)r * cols + c;
-    if (fmt == 0) return orc_e4m3_value(w[idx]) * (double)((const float *)s)[r];
+    if (fmt == 0) return e4m3_cached(w[idx]) * (double)((const float *)s)[r];
     {
         uint8_t byte = w[idx / 2];
         uint8_t nib = (idx & 1) ? (byte >> 4) : (byte & 15);

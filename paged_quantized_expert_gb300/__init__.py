@@ -1,0 +1,478 @@
+"""Python binding of libpqe: the MoE expert layer over paged, quantized expert
+weights on one GB300 (sm_103a).
+
+Each function below has the name of a C entry point in include/pqe.h and only
+marshals arguments: tensors become device (or host) pointers, streams become
+cudaStream_t handles, non-zero return codes become PqeError. All compute
+happens in the CUDA library; there is no other implementation, and loading
+fails loudly when the library cannot be built or loaded.
+
+PyTorch is used for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+PQE_OK = 0
+PQE_ERR_INVALID_ARG = -1
+PQE_ERR_CUDA = -2
+PQE_ERR_CAPACITY = -3
+PQE_ERR_CORRUPT = -4
+PQE_ERR_TIMEOUT = -5
+PQE_ERR_UNSUPPORTED = -6
+
+PQE_STATUS_BAD_EXPERT_ID = 0x1
+PQE_STATUS_CORRUPT_STREAM = 0x2
+PQE_STATUS_BAD_PAGE = 0x4
+PQE_STATUS_TIMEOUT = 0x8
+
+PQE_FMT_FP8 = 0
+PQE_FMT_MXFP4 = 1
+PQE_HUFF_LUT_BYTES = 4096
+
+LIB_PATH = _build.LIB
+
+
+class PqeError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        msg = _lib.pqe_strerror(code).decode() if _lib else str(code)
+        extra = ""
+        if code == PQE_ERR_CUDA and _lib:
+            extra = f" (cudaError {_lib.pqe_last_cuda_error()})"
+        super().__init__(f"{fn}: {msg} [{code}]{extra}")
+        self.code = code
+
+
+class pqe_layer_config(C.Structure):
+    _fields_ = [(n, C.c_int32) for n in ("E", "H", "I", "k", "S", "W", "max_T", "compressed")]
+
+
+class pqe_step_info(C.Structure):
+    _fields_ = [("n_routed", C.c_int32), ("n_miss", C.c_int32), ("working_buffer", C.c_int32),
+                ("pad", C.c_int32), ("h2d_bytes", C.c_int64)]
+
+
+class pqe_layer_buffers_t(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("status", "topk_ids", "topk_w", "counts", "offsets", "perm_src", "inv",
+                                          "page_table", "out_perm", "x_in", "logits_in", "y_out")]
+
+
+class pqe_pool(C.Structure):
+    _fields_ = [("base", C.c_void_p), ("wb_base", C.c_void_p), ("slot_stride", C.c_size_t),
+                ("n_slots", C.c_int32), ("n_wb", C.c_int32), ("H", C.c_int32), ("I", C.c_int32)]
+
+
+_lib: Optional[C.CDLL] = None
+P = C.c_void_p
+I32 = C.c_int
+SZ = C.c_size_t
+
+_SIGS = {
+    "pqe_strerror": (C.c_char_p, [I32]),
+    "pqe_abi_version": (I32, []),
+    "pqe_last_cuda_error": (I32, []),
+    "pqe_kernel_launches": (C.c_uint64, []),
+    "pqe_layer_set_ffn_events": (I32, [P, P, P]),
+    "pqe_page_bytes": (SZ, [I32, I32, I32]),
+    "pqe_slot_stride": (SZ, [I32, I32]),
+    "pqe_quantize_fp8_rows": (I32, [P, I32, I32, P, P, P]),
+    "pqe_quantize_mxfp4_rows": (I32, [P, P, I32, I32, P, P, P]),
+    "moe_route": (I32, [P, P, P, I32, I32, I32, I32, P, P, P]),
+    "moe_permute_workspace_size": (SZ, [I32, I32, I32]),
+    "moe_permute": (I32, [P, I32, I32, I32, P, P, P, P, P, SZ, P, P]),
+    "moe_paged_ffn_workspace_size": (SZ, [I32, I32, I32, I32, I32]),
+    "moe_paged_ffn": (I32, [P, P, P, P, P, C.POINTER(pqe_pool), I32, I32, I32, P, P, SZ, P, P]),
+    "moe_combine": (I32, [P, P, P, I32, I32, I32, P, P]),
+    "pqe_lru_create": (P, [I32, I32]),
+    "pqe_lru_destroy": (None, [P]),
+    "pqe_lru_state": (I32, [P, P, P, P]),
+    "pqe_lru_invalidate": (I32, [P, I32]),
+    "page_table_update": (I32, [P, P, P, P, P, P, P]),
+    "slot_fill": (I32, [C.POINTER(pqe_pool), I32, P, SZ, P, P]),
+    "pqe_huff_page_bound": (SZ, [I32, I32]),
+    "pqe_huff_encode_page": (I32, [P, I32, I32, P, SZ, C.POINTER(C.c_size_t), P, P]),
+    "pqe_huff_page_lengths": (I32, [P, P, P]),
+    "pqe_huff_build_lut": (I32, [P, P]),
+    "fp8_exp_huff_decode": (I32, [P, SZ, P, P, I32, I32, P, P, P]),
+    "slot_fill_compressed": (I32, [C.POINTER(pqe_pool), I32, P, SZ, P, SZ, P, P, P, P, P]),
+    "pqe_importance_step": (I32, [P, P, P, I32, I32, I32, C.c_double, C.c_int64, I32, I32, P, P]),
+    "pqe_rank_formats": (I32, [P, I32, I32, P]),
+    "pqe_pool_slot_addr": (P, [C.POINTER(pqe_pool), I32]),
+    "pqe_pack_fp8_page": (I32, [P, P, I32, I32, P, P]),
+    "pqe_pack_mxfp4_page": (I32, [P, I32, I32, P, P]),
+    "pqe_layer_scratch_bytes": (SZ, [P]),
+    "pqe_layer_create": (P, [P, C.POINTER(pqe_pool), P, P, P, P, P, SZ]),
+    "pqe_layer_destroy": (None, [P]),
+    "pqe_layer_set_host_page": (I32, [P, I32, P, SZ]),
+    "pqe_layer_buffers": (I32, [P, P]),
+    "pqe_layer_lru_state": (I32, [P, P, P, P]),
+    "pqe_layer_step": (I32, [P, P, P, P, I32, P, P, P, P]),
+    "pqe_layer_step_host": (I32, [P, P, P, P, I32, P, P, P, P]),
+}
+
+# every entry point of include/pqe.h
+ABI_SYMBOLS = tuple(_SIGS)
+
+
+def load(build_if_needed: bool = True) -> C.CDLL:
+    """Load libpqe.so (building it first when its sources are newer)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if build_if_needed:
+        _build.build()
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libpqe.so is missing at {LIB_PATH}; build it with paged_quantized_expert_gb300.build")
+    lib = C.CDLL(LIB_PATH)
+    for name, (res, args) in _SIGS.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def lib() -> C.CDLL:
+    return _lib if _lib is not None else load()
+
+
+def _check(fn: str, rc: int):
+    if rc != PQE_OK:
+        raise PqeError(fn, rc)
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if isinstance(t, torch.Tensor):
+        if not t.is_contiguous():
+            raise ValueError("tensors passed to libpqe must be contiguous")
+        return t.data_ptr()
+    raise TypeError(f"cannot pass {type(t)} as a pointer")
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream if torch.cuda.is_available() else None
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _event(ev) -> Optional[int]:
+    if ev is None:
+        return None
+    if isinstance(ev, torch.cuda.Event):
+        return ev.cuda_event
+    return int(ev)
+
+
+# ---- page layout ---------------------------------------------------------------
+
+def page_bytes(fmt: int, H: int, I: int) -> int:
+    return lib().pqe_page_bytes(fmt, H, I)
+
+
+def slot_stride(H: int, I: int) -> int:
+    return lib().pqe_slot_stride(H, I)
+
+
+def page_layout(fmt: int, H: int, I: int) -> dict:
+    """Byte offsets of the page sections (pqe.h, "Expert pages and the slot pool")."""
+    ih = H * I
+    if fmt == PQE_FMT_FP8:
+        return {"w13": 0, "w2": 2 * ih, "s13": 3 * ih, "s2": 3 * ih + 8 * I, "bytes": page_bytes(fmt, H, I)}
+    return {"w13": 0, "w2": ih, "s13": 3 * ih // 2, "s2": 3 * ih // 2 + ih // 16, "bytes": page_bytes(fmt, H, I)}
+
+
+def make_pool(base: Optional[torch.Tensor], n_slots: int, H: int, I: int, wb: Optional[torch.Tensor] = None,
+              n_wb: int = 0) -> pqe_pool:
+    """Describe cache slots (``base``) and working-buffer entries (``wb``) for the library."""
+    stride = slot_stride(H, I)
+    if n_slots and (base is None or base.numel() * base.element_size() < n_slots * stride):
+        raise ValueError("pool tensor too small")
+    if n_wb and (wb is None or wb.numel() * wb.element_size() < n_wb * stride):
+        raise ValueError("working-buffer tensor too small")
+    return pqe_pool(base.data_ptr() if n_slots else None, wb.data_ptr() if n_wb else None, stride, n_slots, n_wb,
+                    H, I)
+
+
+def alloc_pool(n_slots: int, H: int, I: int, device="cuda") -> tuple[torch.Tensor, pqe_pool]:
+    """A pool of n_slots cache slots and no working buffer."""
+    t = torch.zeros(max(n_slots, 1) * slot_stride(H, I), dtype=torch.uint8, device=device)
+    return t, make_pool(t, n_slots, H, I)
+
+
+def alloc_working_buffer(n_wb: int, H: int, I: int, device="cuda") -> torch.Tensor:
+    return torch.zeros(max(n_wb, 1) * slot_stride(H, I), dtype=torch.uint8, device=device)
+
+
+def pqe_pool_slot_addr(pool: pqe_pool, dest: int) -> Optional[int]:
+    return lib().pqe_pool_slot_addr(C.byref(pool), dest)
+
+
+# ---- quantisers ----------------------------------------------------------------
+
+def pqe_quantize_fp8_rows(w, q, scale, stream=None):
+    rows, cols = w.shape
+    _check("pqe_quantize_fp8_rows", lib().pqe_quantize_fp8_rows(_ptr(w), rows, cols, _ptr(q), _ptr(scale),
+                                                                _stream(stream)))
+
+
+def pqe_quantize_mxfp4_rows(q8, s8, q4, x8, stream=None):
+    rows, cols = q8.shape
+    _check("pqe_quantize_mxfp4_rows", lib().pqe_quantize_mxfp4_rows(_ptr(q8), _ptr(s8), rows, cols, _ptr(q4),
+                                                                    _ptr(x8), _stream(stream)))
+
+
+# ---- hot path ------------------------------------------------------------------
+
+def moe_route(x, w_router, logits, T, H, E, k, topk_ids, topk_w, stream=None):
+    _check("moe_route", lib().moe_route(_ptr(x), _ptr(w_router), _ptr(logits), T, H, E, k, _ptr(topk_ids),
+                                        _ptr(topk_w), _stream(stream)))
+
+
+def moe_permute_workspace_size(T, k, E) -> int:
+    return lib().moe_permute_workspace_size(T, k, E)
+
+
+def moe_permute(topk_ids, T, k, E, counts, offsets, perm_src, inv, ws, status, stream=None):
+    nbytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check("moe_permute", lib().moe_permute(_ptr(topk_ids), T, k, E, _ptr(counts), _ptr(offsets), _ptr(perm_src),
+                                            _ptr(inv), _ptr(ws), nbytes, _ptr(status), _stream(stream)))
+
+
+def moe_paged_ffn_workspace_size(T, k, E, H, I) -> int:
+    return lib().moe_paged_ffn_workspace_size(T, k, E, H, I)
+
+
+def moe_paged_ffn(x, perm_src, offsets, page_table, expert_fmt, pool: pqe_pool, T, k, E, out_perm, ws, status,
+                  stream=None):
+    nbytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check("moe_paged_ffn", lib().moe_paged_ffn(_ptr(x), _ptr(perm_src), _ptr(offsets), _ptr(page_table),
+                                                _ptr(expert_fmt), C.byref(pool), T, k, E, _ptr(out_perm),
+                                                _ptr(ws), nbytes, _ptr(status), _stream(stream)))
+
+
+def moe_combine(out_perm, inv, topk_w, T, k, H, y, stream=None):
+    _check("moe_combine", lib().moe_combine(_ptr(out_perm), _ptr(inv), _ptr(topk_w), T, k, H, _ptr(y),
+                                            _stream(stream)))
+
+
+# ---- pager ---------------------------------------------------------------------
+
+class LRU:
+    """Host LRU state of one layer's slot pool (pqe_lru)."""
+
+    def __init__(self, E: int, S: int):
+        self.E, self.S = E, S
+        self._h = lib().pqe_lru_create(E, S)
+        if not self._h:
+            raise PqeError("pqe_lru_create", PQE_ERR_INVALID_ARG)
+        self._pt = torch.empty(E, dtype=torch.int32)
+        self._me = torch.empty(E, dtype=torch.int32)
+        self._md = torch.empty(E, dtype=torch.int32)
+        self._n = torch.zeros(2, dtype=torch.int32)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h and _lib is not None:
+            _lib.pqe_lru_destroy(h)
+            self._h = None
+
+    def page_table_update(self, counts_host: torch.Tensor, page_table_host: torch.Tensor = None):
+        """-> (page_table [E], miss_expert [n], miss_dest [n], working_buffer_mode)"""
+        pt = self._pt if page_table_host is None else page_table_host
+        nm = self._n[0:1]
+        wb = self._n[1:2]
+        _check("page_table_update", lib().page_table_update(self._h, _ptr(counts_host), _ptr(pt), _ptr(self._me),
+                                                            _ptr(self._md), _ptr(nm), _ptr(wb)))
+        n = int(nm.item())
+        return pt, self._me[:n], self._md[:n], bool(wb.item())
+
+    def state(self):
+        se = torch.empty(self.S, dtype=torch.int32)
+        lu = torch.empty(self.S, dtype=torch.int64)
+        st = torch.zeros(1, dtype=torch.int64)
+        _check("pqe_lru_state", lib().pqe_lru_state(self._h, _ptr(se), _ptr(lu), _ptr(st)))
+        return se, lu, int(st.item())
+
+    def invalidate(self, expert: int):
+        _check("pqe_lru_invalidate", lib().pqe_lru_invalidate(self._h, expert))
+
+
+def page_table_update(lru: LRU, counts_host, page_table_host=None):
+    return lru.page_table_update(counts_host, page_table_host)
+
+
+def slot_fill(pool: pqe_pool, dest: int, pinned_src, nbytes: int, stream=None, done_event=None):
+    _check("slot_fill", lib().slot_fill(C.byref(pool), dest, _ptr(pinned_src), nbytes, _stream(stream),
+                                        _event(done_event)))
+
+
+# ---- compressed host tier ---------------------------------------------------------
+
+def pqe_huff_page_bound(H: int, I: int) -> int:
+    return lib().pqe_huff_page_bound(H, I)
+
+
+def pqe_huff_encode_page(fp8_page: torch.Tensor, H: int, I: int, out: torch.Tensor, lut13: torch.Tensor,
+                         lut2: torch.Tensor) -> int:
+    """Host tensors. Returns the compressed size in bytes."""
+    n = C.c_size_t(0)
+    _check("pqe_huff_encode_page", lib().pqe_huff_encode_page(_ptr(fp8_page), H, I, _ptr(out), out.numel(),
+                                                              C.byref(n), _ptr(lut13), _ptr(lut2)))
+    return n.value
+
+
+def pqe_huff_page_lengths(comp_page: torch.Tensor):
+    l13 = torch.zeros(16, dtype=torch.uint8)
+    l2 = torch.zeros(16, dtype=torch.uint8)
+    _check("pqe_huff_page_lengths", lib().pqe_huff_page_lengths(_ptr(comp_page), _ptr(l13), _ptr(l2)))
+    return l13, l2
+
+
+def pqe_huff_build_lut(lengths: torch.Tensor, lut: torch.Tensor):
+    _check("pqe_huff_build_lut", lib().pqe_huff_build_lut(_ptr(lengths), _ptr(lut)))
+
+
+def fp8_exp_huff_decode(comp_page, comp_bytes, lut13, lut2, H, I, fp8_page, status, stream=None):
+    _check("fp8_exp_huff_decode", lib().fp8_exp_huff_decode(_ptr(comp_page), comp_bytes, _ptr(lut13), _ptr(lut2),
+                                                            H, I, _ptr(fp8_page), _ptr(status), _stream(stream)))
+
+
+def slot_fill_compressed(pool: pqe_pool, dest, pinned_comp, comp_bytes, staging, lut13, lut2, status, stream=None,
+                         done_event=None):
+    _check("slot_fill_compressed", lib().slot_fill_compressed(
+        C.byref(pool), dest, _ptr(pinned_comp), comp_bytes, _ptr(staging), staging.numel(), _ptr(lut13),
+        _ptr(lut2), _ptr(status), _stream(stream), _event(done_event)))
+
+
+# ---- bit-width assignment ---------------------------------------------------------
+
+def pqe_importance_step(m: torch.Tensor, ids: torch.Tensor, gates: torch.Tensor, T, k, E, alpha, step, every,
+                        n_hi, fmt: torch.Tensor) -> bool:
+    rr = torch.zeros(1, dtype=torch.int32)
+    _check("pqe_importance_step", lib().pqe_importance_step(_ptr(m), _ptr(ids), _ptr(gates), T, k, E, alpha, step,
+                                                            every, n_hi, _ptr(fmt), _ptr(rr)))
+    return bool(rr.item())
+
+
+def pqe_rank_formats(m: torch.Tensor, n_hi: int, fmt: torch.Tensor):
+    _check("pqe_rank_formats", lib().pqe_rank_formats(_ptr(m), m.numel(), n_hi, _ptr(fmt)))
+
+
+def pqe_pack_fp8_page(w13, w2, H, I, page, stream=None):
+    _check("pqe_pack_fp8_page", lib().pqe_pack_fp8_page(_ptr(w13), _ptr(w2), H, I, _ptr(page), _stream(stream)))
+
+
+def pqe_pack_mxfp4_page(fp8_page, H, I, fp4_page, stream=None):
+    _check("pqe_pack_mxfp4_page", lib().pqe_pack_mxfp4_page(_ptr(fp8_page), H, I, _ptr(fp4_page),
+                                                            _stream(stream)))
+
+
+# ---- layer runtime ---------------------------------------------------------------
+
+class PagedMoELayer:
+    """One MoE layer over its own slot pool (pqe_layer): the public per-step API.
+
+    The caller owns the host tier: ``host_pages`` is a pinned uint8 tensor
+    [E, page_stride] (or a list of pinned tensors, one page each) holding each
+    expert's page in the library's page layout (compressed pages when
+    ``compressed``). Device memory (pool, scratch, code tables, format tags) is
+    allocated here with PyTorch and handed to the library.
+    """
+
+    def __init__(self, E, H, I, k, S, W, max_T, host_pages, host_page_bytes, compressed=False, luts=None,
+                 expert_fmt=None, device="cuda", working_buffer: Optional[torch.Tensor] = None):
+        self.cfg = pqe_layer_config(E, H, I, k, S, W, max_T, int(bool(compressed)))
+        self.E, self.H, self.I, self.k, self.S, self.W, self.max_T = E, H, I, k, S, W, max_T
+        self.pool_mem = torch.zeros(max(S, 1) * slot_stride(H, I), dtype=torch.uint8, device=device)
+        # the working buffer holds one step's pages; layers on one stream may share it
+        self.wb_mem = working_buffer if working_buffer is not None else alloc_working_buffer(W, H, I, device)
+        self.pool = make_pool(self.pool_mem, S, H, I, self.wb_mem, W)
+        nbytes = lib().pqe_layer_scratch_bytes(C.byref(self.cfg))
+        if nbytes == 0:
+            raise PqeError("pqe_layer_scratch_bytes", PQE_ERR_INVALID_ARG)
+        self.scratch = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+        off = (-self.scratch.data_ptr()) % 256
+        self._scratch_ptr = self.scratch.data_ptr() + off
+        if isinstance(host_pages, torch.Tensor):
+            ptrs = [host_pages[e].data_ptr() for e in range(E)]
+        else:
+            ptrs = [p.data_ptr() for p in host_pages]
+        self._host_keep = host_pages
+        self._ptrs = (C.c_void_p * E)(*ptrs)
+        self._bytes = (C.c_size_t * E)(*[int(b) for b in host_page_bytes])
+        self.luts = luts
+        self.expert_fmt = expert_fmt
+        self._h = lib().pqe_layer_create(C.byref(self.cfg), C.byref(self.pool), C.cast(self._ptrs, C.c_void_p),
+                                         C.cast(self._bytes, C.c_void_p), _ptr(luts), _ptr(expert_fmt),
+                                         self._scratch_ptr, nbytes)
+        if not self._h:
+            raise PqeError("pqe_layer_create", PQE_ERR_INVALID_ARG)
+        b = pqe_layer_buffers_t()
+        _check("pqe_layer_buffers", lib().pqe_layer_buffers(self._h, C.byref(b)))
+        self.buffers = b
+        self.info = pqe_step_info()
+
+    def close(self):
+        if getattr(self, "_h", None) and _lib is not None:
+            _lib.pqe_layer_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    def set_host_page(self, expert: int, pinned_page: torch.Tensor, nbytes: int):
+        self._host_keep = (self._host_keep, pinned_page) if not isinstance(self._host_keep, list) else \
+            self._host_keep + [pinned_page]
+        _check("pqe_layer_set_host_page", lib().pqe_layer_set_host_page(self._h, expert, pinned_page.data_ptr(),
+                                                                        nbytes))
+
+    def step(self, x, y, T, logits=None, w_router=None, stream=None, side_stream=None) -> pqe_step_info:
+        _check("pqe_layer_step", lib().pqe_layer_step(self._h, _ptr(x), _ptr(w_router), _ptr(logits), T, _ptr(y),
+                                                      _stream(stream), _stream(side_stream) if side_stream
+                                                      is not None else None, C.byref(self.info)))
+        return self.info
+
+    def step_host(self, x_host, y_host, T, logits_host=None, w_router=None, stream=None, side_stream=None):
+        _check("pqe_layer_step_host", lib().pqe_layer_step_host(
+            self._h, _ptr(x_host), _ptr(w_router), _ptr(logits_host), T, _ptr(y_host), _stream(stream),
+            _stream(side_stream) if side_stream is not None else None, C.byref(self.info)))
+        return self.info
+
+    def set_ffn_events(self, ev_begin, ev_end):
+        _check("pqe_layer_set_ffn_events", lib().pqe_layer_set_ffn_events(self._h, _event(ev_begin),
+                                                                          _event(ev_end)))
+
+    def lru_state(self):
+        se = torch.empty(self.S, dtype=torch.int32)
+        lu = torch.empty(self.S, dtype=torch.int64)
+        st = torch.zeros(1, dtype=torch.int64)
+        _check("pqe_layer_lru_state", lib().pqe_layer_lru_state(self._h, _ptr(se), _ptr(lu), _ptr(st)))
+        return se, lu, int(st.item())
+
+    def device_view(self, name: str, dtype, shape):
+        """A torch view of one of the layer's device buffers (no copy)."""
+        ptr = getattr(self.buffers, name)
+        n = 1
+        for d in shape:
+            n *= d
+        esize = torch.empty(0, dtype=dtype).element_size()
+        base = self.scratch.data_ptr()
+        off = ptr - base
+        return self.scratch[off:off + n * esize].view(dtype).view(*shape)
+
+
+def kernel_launches() -> int:
+    """Kernels libpqe has launched in this process."""
+    return int(lib().pqe_kernel_launches())

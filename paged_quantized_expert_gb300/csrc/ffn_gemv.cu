@@ -1,0 +1,391 @@
+// ffn_gemv.cu -- expert FFN over the slot pool, weight-streaming CUDA-core path.
+//
+// For each routed expert e (its page in slot page_table[e]) and each batch
+// position p of e: u = W13_e x_t, h = SiLU(u[:I]) * u[I:], out_perm[p] = W2_e h.
+// Paging per layer and the w13/w2 weight names: expert-pager article
+// (rand.pepabo.com), "エキスパート重みの階層ページング" and "評価"; 4-bit pages:
+// PagedWeight commentary (spectral-agent.com), "技術的に面白い点".
+//
+// This path serves small per-expert batches (decode), where the layer is bound
+// by streaming the weights from HBM: every weight byte is read once per group
+// of up to NT tokens with 128-bit loads, converted exactly to fp32 and
+// multiplied with bf16 activations in fp32. h stays fp32.
+#include "pqe_common.cuh"
+#include "ffn_internal.cuh"
+
+namespace pqe {
+
+// ---------------------------------------------------------------------------
+// schedule: the list of experts with a non-empty batch, ascending id.
+// sched[0] = count, sched[1 + a] = expert id. One CTA of 1024 threads.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) ffn_schedule_kernel(const int32_t *__restrict__ offsets, int E,
+                                                            int32_t *__restrict__ sched) {
+    __shared__ int32_t warp_cnt[32];
+    const int e = threadIdx.x, lane = e & 31, w = e >> 5;
+    const bool act = e < E && (offsets[e + 1] - offsets[e]) > 0;
+    const unsigned b = __ballot_sync(0xffffffffu, act);
+    if (lane == 0) warp_cnt[w] = __popc(b);
+    __syncthreads();
+    if (w == 0) {
+        int c = warp_cnt[lane], incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        warp_cnt[lane] = incl - c;
+        if (lane == 31) sched[0] = incl;
+    }
+    __syncthreads();
+    if (act) sched[1 + warp_cnt[w] + __popc(b & ((1u << lane) - 1u))] = e;
+}
+
+__device__ __forceinline__ bool page_ok(const FfnArgs &a, int e, int &slot, int &fmt) {
+    slot = a.page_table[e];
+    fmt = a.expert_fmt ? (int)a.expert_fmt[e] : PQE_FMT_FP8;
+    return slot >= 0 && slot < a.n_slots + a.n_wb && (fmt == PQE_FMT_FP8 || fmt == PQE_FMT_MXFP4);
+}
+
+// 16 bf16 activations (two uint4 in shared memory) dotted with 16 fp32 weights
+__device__ __forceinline__ float dot16_bf16(const float (&w)[16], const uint4 &x0, const uint4 &x1, float acc) {
+    const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        acc = __fmaf_rn(w[2 * i], __uint_as_float(xs[i] << 16), acc);
+        acc = __fmaf_rn(w[2 * i + 1], __uint_as_float(xs[i] & 0xffff0000u), acc);
+    }
+    return acc;
+}
+
+__device__ __forceinline__ void cvt16_e4m3(const uint4 &v, float (&f)[16]) {
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 a = e4m3x2_to_f32x2((uint16_t)(u[i] & 0xffff));
+        float2 b = e4m3x2_to_f32x2((uint16_t)(u[i] >> 16));
+        f[4 * i] = a.x;
+        f[4 * i + 1] = a.y;
+        f[4 * i + 2] = b.x;
+        f[4 * i + 3] = b.y;
+    }
+}
+
+// 8 bytes of E2M1 pairs -> 16 fp32
+__device__ __forceinline__ void cvt16_e2m1(uint32_t lo, uint32_t hi, float (&f)[16]) {
+    const uint32_t u[2] = {lo, hi};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            float2 v = e2m1x2_to_f32x2((uint8_t)(u[i] >> (8 * b)));
+            f[8 * i + 2 * b] = v.x;
+            f[8 * i + 2 * b + 1] = v.y;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// w13 + SwiGLU. Unit = (active expert a, block of 8 gate/up row pairs); one
+// warp per pair (gate row j, up row I + j). Tokens in groups of NT, their x
+// rows staged in shared memory as bf16.
+// ---------------------------------------------------------------------------
+template <int NT>
+__global__ void __launch_bounds__(256) ffn_w13_gemv_kernel(FfnArgs a) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw);  // [NT][H]
+    const int H = a.H, I = a.I;
+    const int rblocks = I / 8;
+    const int act_i = blockIdx.x / rblocks, rb = blockIdx.x % rblocks;
+    if (act_i >= a.sched[0]) return;
+    const int e = a.sched[1 + act_i];
+    const int p0 = a.offsets[e], n = a.offsets[e + 1] - p0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int j = rb * 8 + warp;
+    int slot, fmt;
+    if (!page_ok(a, e, slot, fmt)) {
+        if (threadIdx.x == 0) atomicOr(a.status, PQE_STATUS_BAD_PAGE);
+        if (lane == 0)
+            for (int p = p0; p < p0 + n; ++p) a.h[(size_t)p * I + j] = 0.0f;
+        return;
+    }
+    const uint8_t *page = page_addr(a, slot);
+    for (int g0 = 0; g0 < n; g0 += NT) {
+        const int nt = min(NT, n - g0);
+        __syncthreads();
+        for (int i = threadIdx.x; i < nt * (H / 8); i += blockDim.x) {
+            const int tt = i / (H / 8), c = i % (H / 8);
+            const int tok = a.perm_src[p0 + g0 + tt] / a.k;
+            reinterpret_cast<uint4 *>(xs + (size_t)tt * H)[c] =
+                __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)tok * H) + c);
+        }
+        __syncthreads();
+        float ag[NT], au[NT];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) ag[t] = au[t] = 0.0f;
+        if (fmt == PQE_FMT_FP8) {
+            const uint4 *gr = reinterpret_cast<const uint4 *>(page + (size_t)j * H);
+            const uint4 *ur = reinterpret_cast<const uint4 *>(page + (size_t)(I + j) * H);
+            for (int c = lane; c < H / 16; c += 32) {
+                float wg[16], wu[16];
+                cvt16_e4m3(__ldg(gr + c), wg);
+                cvt16_e4m3(__ldg(ur + c), wu);
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    if (t < nt) {
+                        const uint4 *xr = reinterpret_cast<const uint4 *>(xs + (size_t)t * H + 16 * c);
+                        const uint4 x0 = xr[0], x1 = xr[1];
+                        ag[t] = dot16_bf16(wg, x0, x1, ag[t]);
+                        au[t] = dot16_bf16(wu, x0, x1, au[t]);
+                    }
+                }
+            }
+        } else {
+            const PageLayout L = mxfp4_layout(H, I);
+            const uint4 *gr = reinterpret_cast<const uint4 *>(page + (size_t)j * (H / 2));
+            const uint4 *ur = reinterpret_cast<const uint4 *>(page + (size_t)(I + j) * (H / 2));
+            const uint8_t *xg = page + L.s13 + (size_t)j * (H / 32);
+            const uint8_t *xu = page + L.s13 + (size_t)(I + j) * (H / 32);
+            for (int c = lane; c < H / 32; c += 32) {  // 16 bytes = 32 weights = one scale block
+                const uint4 vg = __ldg(gr + c), vu = __ldg(ur + c);
+                const float sg = e8m0_to_f32(__ldg(xg + c)), su = e8m0_to_f32(__ldg(xu + c));
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float wg[16], wu[16];
+                    cvt16_e2m1(half ? vg.z : vg.x, half ? vg.w : vg.y, wg);
+                    cvt16_e2m1(half ? vu.z : vu.x, half ? vu.w : vu.y, wu);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        wg[q] *= sg;
+                        wu[q] *= su;
+                    }
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        if (t < nt) {
+                            const uint4 *xr =
+                                reinterpret_cast<const uint4 *>(xs + (size_t)t * H + 32 * c + 16 * half);
+                            const uint4 x0 = xr[0], x1 = xr[1];
+                            ag[t] = dot16_bf16(wg, x0, x1, ag[t]);
+                            au[t] = dot16_bf16(wu, x0, x1, au[t]);
+                        }
+                    }
+                }
+            }
+        }
+        float sg = 1.0f, su = 1.0f;
+        if (fmt == PQE_FMT_FP8) {
+            const PageLayout L = fp8_layout(H, I);
+            sg = __ldg(reinterpret_cast<const float *>(page + L.s13) + j);
+            su = __ldg(reinterpret_cast<const float *>(page + L.s13) + I + j);
+        }
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            if (t < nt) {
+                const float g = warp_sum(ag[t]) * sg;
+                const float u = warp_sum(au[t]) * su;
+                if (lane == 0) a.h[(size_t)(p0 + g0 + t) * I + j] = silu(g) * u;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// w2. Unit = (active expert a, block of 32 output rows); each warp 4 rows.
+// h rows of a token group staged in shared memory (fp32); the CTA's 32
+// outputs per token are written as one 64-byte bf16 segment.
+// ---------------------------------------------------------------------------
+template <int NT>
+__global__ void __launch_bounds__(256) ffn_w2_gemv_kernel(FfnArgs a) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    float *hs = reinterpret_cast<float *>(smem_raw);  // [NT][I]
+    __shared__ float outs[NT][32];
+    const int H = a.H, I = a.I;
+    const int rblocks = H / 32;
+    const int act_i = blockIdx.x / rblocks, rb = blockIdx.x % rblocks;
+    if (act_i >= a.sched[0]) return;
+    const int e = a.sched[1 + act_i];
+    const int p0 = a.offsets[e], n = a.offsets[e + 1] - p0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int r0 = rb * 32 + warp * 4;
+    int slot, fmt;
+    const bool ok = page_ok(a, e, slot, fmt);
+    const uint8_t *page = page_addr(a, ok ? slot : 0);
+    for (int g0 = 0; g0 < n; g0 += NT) {
+        const int nt = min(NT, n - g0);
+        __syncthreads();
+        if (ok) {
+            for (int i = threadIdx.x; i < nt * (I / 4); i += blockDim.x) {
+                const int tt = i / (I / 4), c = i % (I / 4);
+                reinterpret_cast<float4 *>(hs + (size_t)tt * I)[c] =
+                    reinterpret_cast<const float4 *>(a.h + (size_t)(p0 + g0 + tt) * I)[c];
+            }
+        }
+        __syncthreads();
+        float acc[4][NT];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int t = 0; t < NT; ++t) acc[r][t] = 0.0f;
+        if (ok && fmt == PQE_FMT_FP8) {
+            const PageLayout L = fp8_layout(H, I);
+            for (int c = lane; c < I / 16; c += 32) {
+                float w[4][16];
+#pragma unroll
+                for (int r = 0; r < 4; ++r)
+                    cvt16_e4m3(__ldg(reinterpret_cast<const uint4 *>(page + L.w2 + (size_t)(r0 + r) * I) + c), w[r]);
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    if (t < nt) {
+                        const float4 *hr = reinterpret_cast<const float4 *>(hs + (size_t)t * I + 16 * c);
+                        float hv[16];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            float4 v = hr[q];
+                            hv[4 * q] = v.x;
+                            hv[4 * q + 1] = v.y;
+                            hv[4 * q + 2] = v.z;
+                            hv[4 * q + 3] = v.w;
+                        }
+#pragma unroll
+                        for (int r = 0; r < 4; ++r)
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) acc[r][t] = __fmaf_rn(w[r][q], hv[q], acc[r][t]);
+                    }
+                }
+            }
+        } else if (ok) {
+            const PageLayout L = mxfp4_layout(H, I);
+            for (int c = lane; c < I / 32; c += 32) {
+                uint4 v[4];
+                float sc[4];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    v[r] = __ldg(reinterpret_cast<const uint4 *>(page + L.w2 + (size_t)(r0 + r) * (I / 2)) + c);
+                    sc[r] = e8m0_to_f32(__ldg(page + L.s2 + (size_t)(r0 + r) * (I / 32) + c));
+                }
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float w[4][16];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        cvt16_e2m1(half ? v[r].z : v[r].x, half ? v[r].w : v[r].y, w[r]);
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) w[r][q] *= sc[r];
+                    }
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) {
+                        if (t < nt) {
+                            const float4 *hr = reinterpret_cast<const float4 *>(hs + (size_t)t * I + 32 * c + 16 * half);
+                            float hv[16];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                float4 x4 = hr[q];
+                                hv[4 * q] = x4.x;
+                                hv[4 * q + 1] = x4.y;
+                                hv[4 * q + 2] = x4.z;
+                                hv[4 * q + 3] = x4.w;
+                            }
+#pragma unroll
+                            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                                for (int q = 0; q < 16; ++q) acc[r][t] = __fmaf_rn(w[r][q], hv[q], acc[r][t]);
+                        }
+                    }
+                }
+            }
+        }
+        float s2[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+        if (ok && fmt == PQE_FMT_FP8) {
+            const PageLayout L = fp8_layout(H, I);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) s2[r] = __ldg(reinterpret_cast<const float *>(page + L.s2) + r0 + r);
+        }
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float v = warp_sum(acc[r][t]) * s2[r];
+                if (lane == 0 && t < nt) outs[t][warp * 4 + r] = v;
+            }
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < nt * 32; i += blockDim.x) {
+            const int t = i / 32, c = i % 32;
+            a.out_perm[(size_t)(p0 + g0 + t) * H + rb * 32 + c] = f32_to_bf16_rn(outs[t][c]);
+        }
+    }
+    if (!ok && threadIdx.x == 0 && n > 0) atomicOr(a.status, PQE_STATUS_BAD_PAGE);
+}
+
+int launch_ffn_gemv(const FfnArgs &args, int max_active, cudaStream_t s) {
+    constexpr int NT = 4;
+    const int E = args.E;
+    ffn_schedule_kernel<<<1, 1024, 0, s>>>(args.offsets, E, args.sched);
+    PQE_LAUNCH_CHECK();
+    const size_t smem13 = (size_t)NT * args.H * sizeof(uint16_t);
+    const size_t smem2 = (size_t)NT * args.I * sizeof(float);
+    if (smem13 > 48 * 1024)
+        PQE_CUDA_TRY(cudaFuncSetAttribute(ffn_w13_gemv_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)smem13));
+    if (smem2 > 48 * 1024)
+        PQE_CUDA_TRY(cudaFuncSetAttribute(ffn_w2_gemv_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)smem2));
+    const long g13 = (long)max_active * (args.I / 8);
+    const long g2 = (long)max_active * (args.H / 32);
+    ffn_w13_gemv_kernel<NT><<<(unsigned)g13, 256, smem13, s>>>(args);
+    PQE_LAUNCH_CHECK();
+    ffn_w2_gemv_kernel<NT><<<(unsigned)g2, 256, smem2, s>>>(args);
+    PQE_LAUNCH_CHECK();
+    return PQE_OK;
+}
+
+}  // namespace pqe
+
+using namespace pqe;
+
+extern "C" {
+
+size_t moe_paged_ffn_workspace_size(int T, int k, int E, int H, int I) {
+    if (T < 0 || k < 1 || E < 1 || !shape_ok(H, I)) return 0;
+    const size_t A = (size_t)T * k;
+    return round_up(sizeof(int32_t) * (E + 1), 256) + round_up(A * I * sizeof(float), 256);
+}
+
+int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *offsets, const int32_t *page_table,
+                  const uint8_t *expert_fmt, const pqe_pool *pool, int T, int k, int E, void *out_perm, void *ws,
+                  size_t ws_bytes, int32_t *status, void *stream) {
+    PQE_CHECK_ARG(pool && T >= 0 && k >= 1 && k <= 32 && E >= 1 && E <= 1024 && k <= E);
+    PQE_CHECK_ARG(shape_ok(pool->H, pool->I));
+    if (T == 0) return PQE_OK;
+    PQE_CHECK_ARG(x_bf16 && perm_src && offsets && page_table && out_perm && ws && status);
+    PQE_CHECK_ARG(pool->n_slots >= 0 && pool->n_wb >= 0 && pool->n_slots + pool->n_wb >= 1);
+    PQE_CHECK_ARG(pool->slot_stride == pqe_slot_stride(pool->H, pool->I));
+    PQE_CHECK_ARG(pool->n_slots == 0 || (pool->base && aligned(pool->base, 256)));
+    PQE_CHECK_ARG(pool->n_wb == 0 || (pool->wb_base && aligned(pool->wb_base, 256)));
+    PQE_CHECK_ARG(aligned(x_bf16, 16) && aligned(out_perm, 16) && aligned(ws, 256));
+    PQE_CHECK_ARG(ws_bytes >= moe_paged_ffn_workspace_size(T, k, E, pool->H, pool->I));
+    FfnArgs args{};
+    args.x = static_cast<const uint16_t *>(x_bf16);
+    args.perm_src = perm_src;
+    args.offsets = offsets;
+    args.page_table = page_table;
+    args.expert_fmt = expert_fmt;
+    args.pool_base = static_cast<const uint8_t *>(pool->base);
+    args.wb_base = static_cast<const uint8_t *>(pool->wb_base);
+    args.slot_stride = pool->slot_stride;
+    args.n_slots = pool->n_slots;
+    args.n_wb = pool->n_wb;
+    args.k = k;
+    args.E = E;
+    args.H = pool->H;
+    args.I = pool->I;
+    args.sched = static_cast<int32_t *>(ws);
+    args.h = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + round_up(sizeof(int32_t) * (E + 1), 256));
+    args.out_perm = static_cast<uint16_t *>(out_perm);
+    args.status = status;
+    const long A = (long)T * k;
+    const int max_active = (int)(A < E ? A : E);
+    return launch_ffn_gemv(args, max_active, as_stream(stream));
+}
+
+}  // extern "C"

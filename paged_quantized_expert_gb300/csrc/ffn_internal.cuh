@@ -1,0 +1,34 @@
+// ffn_internal.cuh -- argument block shared by the expert-FFN kernels (internal).
+#pragma once
+
+#include <stdint.h>
+
+namespace pqe {
+
+struct FfnArgs {
+    const uint16_t *x;           // bf16 [T, H]
+    const int32_t *perm_src;     // [T*k]
+    const int32_t *offsets;      // [E+1]
+    const int32_t *page_table;   // [E]
+    const uint8_t *expert_fmt;   // [E] or null (all FP8)
+    const uint8_t *pool_base;    // cache slots
+    const uint8_t *wb_base;      // working-buffer entries
+    size_t slot_stride;
+    int n_slots;                 // cache slots
+    int n_wb;                    // working-buffer entries
+    int k, E, H, I;
+    int32_t *sched;              // [E+1]: count, then active expert ids
+    float *h;                    // fp32 [T*k, I]
+    uint16_t *out_perm;          // bf16 [T*k, H]
+    int32_t *status;
+};
+
+// address of page-table entry `slot` (valid: 0 <= slot < n_slots + n_wb)
+__device__ __forceinline__ const uint8_t *page_addr(const FfnArgs &a, int slot) {
+    return slot < a.n_slots ? a.pool_base + (size_t)slot * a.slot_stride
+                            : a.wb_base + (size_t)(slot - a.n_slots) * a.slot_stride;
+}
+
+int launch_ffn_gemv(const FfnArgs &args, int max_active, cudaStream_t s);
+
+}  // namespace pqe

@@ -1,0 +1,303 @@
+// layer.cpp -- native runtime of one paged MoE layer: a step is
+//   route -> permute -> counts to the host (the one sync of a step) ->
+//   page_table_update -> refills of the misses on a side stream ->
+//   page table to the device -> (compute stream waits for the refills) ->
+//   expert FFN over the slot pool -> combine.
+//
+// Expert-pager article (rand.pepabo.com), "エキスパート重みの階層ページング":
+// per-layer VRAM slots managed LRU, copy-in of a missing expert, working buffer
+// when a step needs more experts than slots; "重みの圧縮": compressed host pages
+// decoded on the GPU after the copy. MoE-Gen summary (aibr.jp), "3.中核となる
+// 技術的要素": host-to-device transfers overlap compute (side stream).
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "pqe.h"
+
+namespace pqe {
+void set_last_cuda_error(cudaError_t e);
+}
+
+namespace {
+
+size_t up256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct ScratchMap {
+    size_t status, topk_ids, topk_w, counts, offsets, perm_src, inv, page_table, perm_ws, ffn_ws, out_perm, x_in,
+        logits_in, y_out, staging, total;
+    size_t perm_ws_bytes, ffn_ws_bytes, staging_bytes;
+};
+
+ScratchMap scratch_map(const pqe_layer_config &c) {
+    ScratchMap m{};
+    const size_t A = (size_t)c.max_T * c.k;
+    size_t off = 0;
+    auto take = [&off](size_t bytes) {
+        size_t at = off;
+        off += up256(bytes == 0 ? 1 : bytes);
+        return at;
+    };
+    m.status = take(sizeof(int32_t));
+    m.topk_ids = take(sizeof(int32_t) * A);
+    m.topk_w = take(sizeof(float) * A);
+    m.counts = take(sizeof(int32_t) * c.E);
+    m.offsets = take(sizeof(int32_t) * (c.E + 1));
+    m.perm_src = take(sizeof(int32_t) * A);
+    m.inv = take(sizeof(int32_t) * A);
+    m.page_table = take(sizeof(int32_t) * c.E);
+    m.perm_ws_bytes = moe_permute_workspace_size(c.max_T, c.k, c.E);
+    m.perm_ws = take(m.perm_ws_bytes);
+    m.ffn_ws_bytes = moe_paged_ffn_workspace_size(c.max_T, c.k, c.E, c.H, c.I);
+    m.ffn_ws = take(m.ffn_ws_bytes);
+    m.out_perm = take(sizeof(uint16_t) * A * c.H);
+    m.x_in = take(sizeof(uint16_t) * (size_t)c.max_T * c.H);
+    m.logits_in = take(sizeof(float) * (size_t)c.max_T * c.E);
+    m.y_out = take(sizeof(uint16_t) * (size_t)c.max_T * c.H);
+    m.staging_bytes = c.compressed ? pqe_huff_page_bound(c.H, c.I) : 0;
+    m.staging = take(m.staging_bytes);
+    m.total = off;
+    return m;
+}
+
+bool config_ok(const pqe_layer_config *c) {
+    return c && c->E >= 1 && c->E <= 1024 && c->k >= 1 && c->k <= 32 && c->k <= c->E && c->S >= 0 && c->W >= 0 &&
+           c->max_T >= 1 && (size_t)c->max_T * c->k < (1u << 30) && pqe_page_bytes(PQE_FMT_FP8, c->H, c->I) > 0;
+}
+
+}  // namespace
+
+struct pqe_layer {
+    pqe_layer_config cfg{};
+    pqe_pool pool{};
+    std::vector<const void *> host_pages;
+    std::vector<size_t> host_bytes;
+    const uint8_t *luts = nullptr;
+    const uint8_t *expert_fmt = nullptr;
+    uint8_t *scratch = nullptr;
+    ScratchMap map{};
+    pqe_lru *lru = nullptr;
+    int32_t *pinned = nullptr;  // counts [E], page table [E], miss expert [E], miss dest [E]
+    cudaEvent_t ev_counts = nullptr, ev_fill = nullptr;
+    cudaEvent_t ev_ffn_begin = nullptr, ev_ffn_end = nullptr;  // caller's, optional
+
+    template <class T>
+    T *at(size_t off) const {
+        return reinterpret_cast<T *>(scratch + off);
+    }
+};
+
+extern "C" {
+
+size_t pqe_layer_scratch_bytes(const pqe_layer_config *cfg) {
+    if (!config_ok(cfg)) return 0;
+    return scratch_map(*cfg).total;
+}
+
+pqe_layer *pqe_layer_create(const pqe_layer_config *cfg, const pqe_pool *pool, const void *const *host_pages,
+                            const size_t *host_page_bytes, const uint8_t *luts_dev, const uint8_t *expert_fmt_dev,
+                            void *scratch_dev, size_t scratch_bytes) {
+    if (!config_ok(cfg) || !pool || !host_pages || !host_page_bytes || !scratch_dev) return nullptr;
+    if ((cfg->S > 0 && !pool->base) || (cfg->W > 0 && !pool->wb_base)) return nullptr;
+    if (pool->H != cfg->H || pool->I != cfg->I || pool->n_slots != cfg->S || pool->n_wb != cfg->W) return nullptr;
+    if (pool->slot_stride != pqe_slot_stride(cfg->H, cfg->I)) return nullptr;
+    if (cfg->compressed && !luts_dev) return nullptr;
+    if (reinterpret_cast<uintptr_t>(scratch_dev) % 256) return nullptr;
+    ScratchMap m = scratch_map(*cfg);
+    if (scratch_bytes < m.total) return nullptr;
+    for (int e = 0; e < cfg->E; ++e) {
+        if (!host_pages[e] || host_page_bytes[e] == 0) return nullptr;
+        if (!cfg->compressed && host_page_bytes[e] > pool->slot_stride) return nullptr;
+        if (cfg->compressed && host_page_bytes[e] > m.staging_bytes) return nullptr;
+    }
+    pqe_layer *L = new (std::nothrow) pqe_layer();
+    if (!L) return nullptr;
+    L->cfg = *cfg;
+    L->pool = *pool;
+    L->host_pages.assign(host_pages, host_pages + cfg->E);
+    L->host_bytes.assign(host_page_bytes, host_page_bytes + cfg->E);
+    L->luts = luts_dev;
+    L->expert_fmt = expert_fmt_dev;
+    L->scratch = static_cast<uint8_t *>(scratch_dev);
+    L->map = m;
+    L->lru = pqe_lru_create(cfg->E, cfg->S);
+    cudaError_t e1 = cudaHostAlloc(reinterpret_cast<void **>(&L->pinned), sizeof(int32_t) * 4 * cfg->E,
+                                   cudaHostAllocDefault);
+    cudaError_t e2 = cudaEventCreateWithFlags(&L->ev_counts, cudaEventDisableTiming);
+    cudaError_t e3 = cudaEventCreateWithFlags(&L->ev_fill, cudaEventDisableTiming);
+    if (!L->lru || e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) {
+        pqe::set_last_cuda_error(e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3));
+        pqe_layer_destroy(L);
+        return nullptr;
+    }
+    if (cudaMemset(L->at<int32_t>(m.status), 0, sizeof(int32_t)) != cudaSuccess) {
+        pqe_layer_destroy(L);
+        return nullptr;
+    }
+    return L;
+}
+
+void pqe_layer_destroy(pqe_layer *L) {
+    if (!L) return;
+    if (L->ev_counts) cudaEventDestroy(L->ev_counts);
+    if (L->ev_fill) cudaEventDestroy(L->ev_fill);
+    if (L->pinned) cudaFreeHost(L->pinned);
+    pqe_lru_destroy(L->lru);
+    delete L;
+}
+
+int pqe_layer_set_host_page(pqe_layer *L, int expert, const void *pinned_page, size_t bytes) {
+    if (!L || expert < 0 || expert >= L->cfg.E || !pinned_page || bytes == 0) return PQE_ERR_INVALID_ARG;
+    if (!L->cfg.compressed && bytes > L->pool.slot_stride) return PQE_ERR_INVALID_ARG;
+    if (L->cfg.compressed && bytes > L->map.staging_bytes) return PQE_ERR_INVALID_ARG;
+    L->host_pages[expert] = pinned_page;
+    L->host_bytes[expert] = bytes;
+    return pqe_lru_invalidate(L->lru, expert);
+}
+
+int pqe_layer_buffers(pqe_layer *L, pqe_layer_buffers_t *out) {
+    if (!L || !out) return PQE_ERR_INVALID_ARG;
+    out->status = L->at<int32_t>(L->map.status);
+    out->topk_ids = L->at<int32_t>(L->map.topk_ids);
+    out->topk_w = L->at<float>(L->map.topk_w);
+    out->counts = L->at<int32_t>(L->map.counts);
+    out->offsets = L->at<int32_t>(L->map.offsets);
+    out->perm_src = L->at<int32_t>(L->map.perm_src);
+    out->inv = L->at<int32_t>(L->map.inv);
+    out->page_table = L->at<int32_t>(L->map.page_table);
+    out->out_perm = L->at<void>(L->map.out_perm);
+    out->x_in = L->at<void>(L->map.x_in);
+    out->logits_in = L->at<float>(L->map.logits_in);
+    out->y_out = L->at<void>(L->map.y_out);
+    return PQE_OK;
+}
+
+int pqe_layer_set_ffn_events(pqe_layer *L, void *ev_begin, void *ev_end) {
+    if (!L || (!ev_begin) != (!ev_end)) return PQE_ERR_INVALID_ARG;
+    L->ev_ffn_begin = reinterpret_cast<cudaEvent_t>(ev_begin);
+    L->ev_ffn_end = reinterpret_cast<cudaEvent_t>(ev_end);
+    return PQE_OK;
+}
+
+int pqe_layer_lru_state(const pqe_layer *L, int32_t *slot_expert, int64_t *last_use, int64_t *step) {
+    if (!L) return PQE_ERR_INVALID_ARG;
+    return pqe_lru_state(L->lru, slot_expert, last_use, step);
+}
+
+int pqe_layer_step(pqe_layer *L, const void *x_dev, const float *w_router_dev, float *logits_dev, int T, void *y_dev,
+                   void *stream, void *side_stream, pqe_step_info *info) {
+    if (!L || T < 0 || T > L->cfg.max_T || !y_dev || !x_dev || (!w_router_dev && !logits_dev))
+        return PQE_ERR_INVALID_ARG;
+    const pqe_layer_config &c = L->cfg;
+    const ScratchMap &m = L->map;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaStream_t side = side_stream ? reinterpret_cast<cudaStream_t>(side_stream) : s;
+    pqe_step_info local{};
+    if (T == 0) {
+        if (info) *info = local;
+        return PQE_OK;
+    }
+    int32_t *status = L->at<int32_t>(m.status);
+    int32_t *ids = L->at<int32_t>(m.topk_ids);
+    float *gates = L->at<float>(m.topk_w);
+    int32_t *counts = L->at<int32_t>(m.counts);
+    int32_t *offsets = L->at<int32_t>(m.offsets);
+    int32_t *perm_src = L->at<int32_t>(m.perm_src);
+    int32_t *inv = L->at<int32_t>(m.inv);
+    int32_t *page_table = L->at<int32_t>(m.page_table);
+    void *out_perm = L->at<void>(m.out_perm);
+    int rc = moe_route(x_dev, w_router_dev, logits_dev, T, c.H, c.E, c.k, ids, gates, stream);
+    if (rc) return rc;
+    rc = moe_permute(ids, T, c.k, c.E, counts, offsets, perm_src, inv, L->at<void>(m.perm_ws), m.perm_ws_bytes,
+                     status, stream);
+    if (rc) return rc;
+    int32_t *counts_h = L->pinned, *pt_h = L->pinned + c.E, *miss_e = L->pinned + 2 * c.E,
+            *miss_d = L->pinned + 3 * c.E;
+    cudaError_t ce = cudaMemcpyAsync(counts_h, counts, sizeof(int32_t) * c.E, cudaMemcpyDeviceToHost, s);
+    if (ce == cudaSuccess) ce = cudaEventRecord(L->ev_counts, s);
+    if (ce == cudaSuccess) ce = cudaEventSynchronize(L->ev_counts);
+    if (ce != cudaSuccess) {
+        pqe::set_last_cuda_error(ce);
+        return PQE_ERR_CUDA;
+    }
+    int32_t nm = 0, wb = 0;
+    rc = page_table_update(L->lru, counts_h, pt_h, miss_e, miss_d, &nm, &wb);
+    if (rc) return rc;
+    for (int e = 0; e < c.E; ++e) local.n_routed += counts_h[e] > 0;
+    local.n_miss = nm;
+    local.working_buffer = wb;
+    for (int i = 0; i < nm; ++i)
+        if (miss_d[i] >= L->pool.n_slots + L->pool.n_wb) return PQE_ERR_CAPACITY;
+    for (int i = 0; i < nm; ++i) {
+        const int e = miss_e[i];
+        if (c.compressed) {
+            const uint8_t *l13 = L->luts + (size_t)e * 2 * PQE_HUFF_LUT_BYTES;
+            rc = slot_fill_compressed(&L->pool, miss_d[i], L->host_pages[e], L->host_bytes[e],
+                                      L->at<void>(m.staging), m.staging_bytes, l13, l13 + PQE_HUFF_LUT_BYTES, status,
+                                      side, nullptr);
+        } else {
+            rc = slot_fill(&L->pool, miss_d[i], L->host_pages[e], L->host_bytes[e], side, nullptr);
+        }
+        if (rc) return rc;
+        local.h2d_bytes += (int64_t)L->host_bytes[e];
+    }
+    if (nm > 0 && side != s) {
+        ce = cudaEventRecord(L->ev_fill, side);
+        if (ce == cudaSuccess) ce = cudaStreamWaitEvent(s, L->ev_fill, 0);
+        if (ce != cudaSuccess) {
+            pqe::set_last_cuda_error(ce);
+            return PQE_ERR_CUDA;
+        }
+    }
+    ce = cudaMemcpyAsync(page_table, pt_h, sizeof(int32_t) * c.E, cudaMemcpyHostToDevice, s);
+    if (ce != cudaSuccess) {
+        pqe::set_last_cuda_error(ce);
+        return PQE_ERR_CUDA;
+    }
+    if (L->ev_ffn_begin && (ce = cudaEventRecord(L->ev_ffn_begin, s)) != cudaSuccess) {
+        pqe::set_last_cuda_error(ce);
+        return PQE_ERR_CUDA;
+    }
+    rc = moe_paged_ffn(x_dev, perm_src, offsets, page_table, L->expert_fmt, &L->pool, T, c.k, c.E, out_perm,
+                       L->at<void>(m.ffn_ws), m.ffn_ws_bytes, status, stream);
+    if (rc) return rc;
+    if (L->ev_ffn_end && (ce = cudaEventRecord(L->ev_ffn_end, s)) != cudaSuccess) {
+        pqe::set_last_cuda_error(ce);
+        return PQE_ERR_CUDA;
+    }
+    rc = moe_combine(out_perm, inv, gates, T, c.k, c.H, y_dev, stream);
+    if (rc) return rc;
+    if (info) *info = local;
+    return PQE_OK;
+}
+
+int pqe_layer_step_host(pqe_layer *L, const void *x_host, const float *w_router_dev, const float *logits_host, int T,
+                        void *y_host, void *stream, void *side_stream, pqe_step_info *info) {
+    if (!L || T < 0 || T > L->cfg.max_T || !x_host || !y_host || (!w_router_dev && !logits_host))
+        return PQE_ERR_INVALID_ARG;
+    const pqe_layer_config &c = L->cfg;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    void *x_in = L->at<void>(L->map.x_in);
+    float *lg = L->at<float>(L->map.logits_in);
+    void *y = L->at<void>(L->map.y_out);
+    cudaError_t ce = cudaMemcpyAsync(x_in, x_host, sizeof(uint16_t) * (size_t)T * c.H, cudaMemcpyHostToDevice, s);
+    if (ce == cudaSuccess && !w_router_dev)
+        ce = cudaMemcpyAsync(lg, logits_host, sizeof(float) * (size_t)T * c.E, cudaMemcpyHostToDevice, s);
+    if (ce != cudaSuccess) {
+        pqe::set_last_cuda_error(ce);
+        return PQE_ERR_CUDA;
+    }
+    int rc = pqe_layer_step(L, x_in, w_router_dev, w_router_dev ? nullptr : lg, T, y, stream, side_stream, info);
+    if (rc) return rc;
+    ce = cudaMemcpyAsync(y_host, y, sizeof(uint16_t) * (size_t)T * c.H, cudaMemcpyDeviceToHost, s);
+    if (ce == cudaSuccess) ce = cudaStreamSynchronize(s);
+    if (ce != cudaSuccess) {
+        pqe::set_last_cuda_error(ce);
+        return PQE_ERR_CUDA;
+    }
+    return PQE_OK;
+}
+
+}  // extern "C"

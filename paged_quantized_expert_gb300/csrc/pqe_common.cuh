@@ -1,0 +1,126 @@
+// pqe_common.cuh -- shared device/host helpers of libpqe (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pqe.h"
+
+namespace pqe {
+
+// ---- host-side error plumbing ----------------------------------------------
+
+void set_last_cuda_error(cudaError_t e);
+
+#define PQE_CUDA_TRY(expr)                                                                     \
+    do {                                                                                       \
+        cudaError_t pqe_e_ = (expr);                                                           \
+        if (pqe_e_ != cudaSuccess) {                                                           \
+            ::pqe::set_last_cuda_error(pqe_e_);                                                \
+            return PQE_ERR_CUDA;                                                               \
+        }                                                                                      \
+    } while (0)
+
+#define PQE_CHECK_ARG(cond)                                                                    \
+    do {                                                                                       \
+        if (!(cond)) return PQE_ERR_INVALID_ARG;                                               \
+    } while (0)
+
+// every kernel launch of the library is counted (pqe_kernel_launches)
+void count_launch();
+
+#define PQE_LAUNCH_CHECK()                                                                     \
+    do {                                                                                       \
+        ::pqe::count_launch();                                                                 \
+        PQE_CUDA_TRY(cudaGetLastError());                                                      \
+    } while (0)
+
+inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+__host__ __device__ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline bool shape_ok(int H, int I) {
+    return H >= 64 && H <= 16384 && H % 64 == 0 && I >= 64 && I <= 8192 && I % 64 == 0;
+}
+
+// ---- page layout (bytes) ---------------------------------------------------
+
+struct PageLayout {
+    size_t w13, w2, s13, s2, bytes;
+};
+
+__host__ __device__ inline PageLayout fp8_layout(int H, int I) {
+    size_t ih = (size_t)I * H;
+    return {0, 2 * ih, 3 * ih, 3 * ih + 8 * (size_t)I, 3 * ih + 8 * (size_t)I + 4 * (size_t)H};
+}
+
+__host__ __device__ inline PageLayout mxfp4_layout(int H, int I) {
+    size_t ih = (size_t)I * H;
+    return {0, ih, 3 * ih / 2, 3 * ih / 2 + ih / 16, 3 * ih / 2 + ih / 16 + ih / 32};
+}
+
+// ---- device helpers --------------------------------------------------------
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+    uint16_t r;
+    asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+    return r;
+}
+
+// two E4M3 codes (lo byte -> .x, hi byte -> .y) to fp32, exact
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t v) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+    float2 r;
+    asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(h2));
+    return r;
+}
+
+// two E2M1 codes (low nibble -> .x, high nibble -> .y) to fp32, exact
+__device__ __forceinline__ float2 e2m1x2_to_f32x2(uint8_t v) {
+    uint32_t h2;
+    uint16_t w = v;
+    asm("{\n\t.reg .b8 b;\n\tcvt.u8.u16 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(h2) : "h"(w));
+    float2 r;
+    asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tcvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(h2));
+    return r;
+}
+
+// fp32 pair -> two E4M3 codes, round to nearest even, saturating (lo <- a, hi <- b)
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float a, float b) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+    return r;
+}
+
+// fp32 pair -> two E2M1 codes in one byte (low nibble <- a, high nibble <- b)
+__device__ __forceinline__ uint8_t f32x2_to_e2m1x2(float a, float b) {
+    uint16_t r;
+    asm("{\n\t.reg .b8 d;\n\tcvt.rn.satfinite.e2m1x2.f32 d, %1, %2;\n\tcvt.u16.u8 %0, d;\n\t}"
+        : "=h"(r)
+        : "f"(b), "f"(a));
+    return (uint8_t)r;
+}
+
+// 2^(b - 127) for an E8M0 byte b in [0, 254], as fp32
+__device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
+    return b == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+}  // namespace pqe

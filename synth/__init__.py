@@ -151,9 +151,9 @@ class RoutingTrace:
     their k-th and (k+1)-th largest logits, to exercise the lower-id rule.
     """
 
-    def __init__(self, cfg: LayerConfig, T: int):
-        self.cfg, self.T = cfg, T
-        self._perm = _rng(cfg, 0, _TAG_PERM).permutation(cfg.E)
+    def __init__(self, cfg: LayerConfig, T: int, layer: int = 0):
+        self.cfg, self.T, self.layer = cfg, T, layer
+        self._perm = _rng(cfg, 0, _TAG_PERM, layer).permutation(cfg.E)
         self._p = _zipf_probs(cfg.E, cfg.zipf_s) if cfg.zipf_s > 0 else np.full(cfg.E, 1.0 / cfg.E)
         self._prev = None
 
@@ -163,7 +163,7 @@ class RoutingTrace:
 
     def step(self, s: int) -> np.ndarray:
         cfg, T = self.cfg, self.T
-        g = _rng(cfg, s, _TAG_TRACE, T)
+        g = _rng(cfg, s, _TAG_TRACE, T + (self.layer << 20))
         sets = np.empty((T, cfg.k), dtype=np.int64)
         for t in range(T):
             if self._prev is not None and g.random() < cfg.reuse_p:

@@ -1,0 +1,181 @@
+"""GPU parity of the expert FFN + combine over the slot pool, called through the
+C-ABI one step at a time (moe_route -> moe_permute -> moe_paged_ffn ->
+moe_combine), against the oracle.
+
+Tolerance per token t: max_i |y - ref| / ||ref_t||_2 <= 2e-2 (stated bound);
+the CUDA-core path is also held to a relative L2 error of 5e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from tests import helpers
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+class Pages:
+    """Expert pages on the device, in slots 0..E-1 of one pool (identity table),
+    plus the oracle's copy of the experts the checked tokens use."""
+
+    def __init__(self, pqe, orc, cfg, needed, fp4=(), seed=0):
+        self.pqe, self.cfg = pqe, cfg
+        E, H, I = cfg.E, cfg.H, cfg.I
+        self.pool_mem, self.pool = pqe.alloc_pool(E, H, I)
+        stride = pqe.slot_stride(H, I)
+        self.fmt = torch.zeros(E, dtype=torch.uint8)
+        self.experts = orc.ExpertSet(E)
+        gen = torch.Generator(device=DEV)
+        gen.manual_seed(1000 + seed)
+        lay8 = pqe.page_layout(pqe.PQE_FMT_FP8, H, I)
+        for e in range(E):
+            if e in needed:
+                w13, w2 = synth.expert_weights(cfg, e)
+                w13d, w2d = torch.from_numpy(w13).to(DEV), torch.from_numpy(w2).to(DEV)
+            else:
+                w13d = torch.randn(2 * I, H, device=DEV, generator=gen) * 0.02
+                w2d = torch.randn(H, I, device=DEV, generator=gen) * 0.02
+            slot = self.pool_mem[e * stride:(e + 1) * stride]
+            pqe.pqe_pack_fp8_page(w13d, w2d, H, I, slot)
+            if e in fp4:
+                tmp = torch.zeros(pqe.page_bytes(pqe.PQE_FMT_MXFP4, H, I), dtype=torch.uint8, device=DEV)
+                pqe.pqe_pack_mxfp4_page(slot, H, I, tmp)
+                slot.zero_()
+                slot[:tmp.numel()].copy_(tmp)
+                self.fmt[e] = pqe.PQE_FMT_MXFP4
+            if e in needed:
+                q13, s13 = orc.quant_e4m3_rows(w13)
+                q2, s2 = orc.quant_e4m3_rows(w2)
+                if e in fp4:
+                    a13, x13 = orc.quant_mxfp4_rows(q13, s13)
+                    a2, x2 = orc.quant_mxfp4_rows(q2, s2)
+                    self.experts.set(e, 1, a13, x13, a2, x2)
+                else:
+                    self.experts.set(e, 0, q13, s13, q2, s2)
+        torch.cuda.synchronize()
+        # the library's pages of the needed experts are the oracle's bytes
+        for e in sorted(needed)[:2]:
+            if e in fp4:
+                continue
+            got = self.pool_mem[e * stride:e * stride + lay8["bytes"]].cpu().numpy()
+            q13, s13, q2, s2 = helpers.split_fp8_page(got, lay8, H, I)
+            w13, w2 = synth.expert_weights(cfg, e)
+            assert np.array_equal(q13, orc.quant_e4m3_rows(w13)[0])
+        self.fmt_dev = self.fmt.to(DEV)
+
+
+def run_layer(pqe, cfg, T, x_np, logits_np=None, w_r_np=None, page_table=None, fmt_dev=None, pool=None):
+    E, H, k = cfg.E, cfg.H, cfg.k
+    A = T * k
+    x = torch.from_numpy(x_np.view(np.int16)).to(DEV)
+    ids = torch.zeros((T, k), dtype=torch.int32, device=DEV)
+    gw = torch.zeros((T, k), dtype=torch.float32, device=DEV)
+    if w_r_np is not None:
+        lg = torch.zeros((T, E), dtype=torch.float32, device=DEV)
+        pqe.moe_route(x, torch.from_numpy(w_r_np).to(DEV), lg, T, H, E, k, ids, gw)
+    else:
+        pqe.moe_route(None, None, torch.from_numpy(logits_np).to(DEV), T, H, E, k, ids, gw)
+    counts = torch.zeros(E, dtype=torch.int32, device=DEV)
+    offsets = torch.zeros(E + 1, dtype=torch.int32, device=DEV)
+    perm_src = torch.zeros(A, dtype=torch.int32, device=DEV)
+    inv = torch.zeros(A, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ws = torch.zeros(pqe.moe_permute_workspace_size(T, k, E), dtype=torch.uint8, device=DEV)
+    pqe.moe_permute(ids, T, k, E, counts, offsets, perm_src, inv, ws, status)
+    pt = page_table if page_table is not None else torch.arange(E, dtype=torch.int32, device=DEV)
+    out_perm = torch.zeros((A, H), dtype=torch.bfloat16, device=DEV)
+    fws = torch.zeros(pqe.moe_paged_ffn_workspace_size(T, k, E, H, cfg.I), dtype=torch.uint8, device=DEV)
+    pqe.moe_paged_ffn(x, perm_src, offsets, pt, fmt_dev, pool, T, k, E, out_perm, fws, status)
+    y = torch.zeros((T, H), dtype=torch.bfloat16, device=DEV)
+    pqe.moe_combine(out_perm, inv, gw, T, k, H, y)
+    torch.cuda.synchronize()
+    return {"y": y, "ids": ids.cpu().numpy(), "gates": gw.cpu().numpy(), "status": int(status.item()),
+            "out_perm": out_perm}
+
+
+def check_tokens(orc, pages, cfg, x_np, ids, gates_ref, res, tokens, l2_bound=helpers.TOL_L2_GEMV):
+    ref = orc.moe_ffn(x_np, ids, gates_ref, pages.experts, cfg.I, tokens=tokens)
+    y = helpers.bf16_to_f64(res["y"])[tokens]
+    st = helpers.error_stats(y, ref)
+    assert st["max_over_l2"] <= helpers.TOL_MAX_OVER_L2, st
+    assert st["l2"] <= l2_bound, st
+    return st
+
+
+def test_config1_end_to_end(cuda_lib, orc):
+    pqe = cuda_lib
+    cfg = synth.CONFIGS[1]
+    pages = Pages(pqe, orc, cfg, needed=set(range(cfg.E)))
+    x = synth.activations(cfg, 64)
+    w_r = synth.router_weights(cfg)
+    res = run_layer(pqe, cfg, 64, x, w_r_np=w_r, fmt_dev=pages.fmt_dev, pool=pages.pool)
+    ids, g = orc.topk_gates(orc.router_logits(x, w_r), cfg.k)
+    assert np.array_equal(res["ids"], ids) and res["status"] == 0
+    check_tokens(orc, pages, cfg, x, ids, g, res, np.arange(64, dtype=np.int32))
+
+
+@pytest.mark.parametrize("E,H,I,k,T,fp4", [
+    (5, 192, 64, 3, 37, ()),
+    (5, 192, 64, 3, 37, (1, 3)),
+    (9, 256, 128, 2, 129, (0, 1, 2, 3, 4, 5, 6, 7, 8)),
+    (3, 64, 192, 1, 11, (2,)),
+])
+def test_small_ragged_layers(cuda_lib, orc, E, H, I, k, T, fp4):
+    pqe = cuda_lib
+    cfg = synth.small_config(E=E, H=H, I=I, k=k, T=T, cid=92)
+    pages = Pages(pqe, orc, cfg, needed=set(range(E)), fp4=set(fp4))
+    x = synth.activations(cfg, T)
+    g = np.random.default_rng(T)
+    logits = g.standard_normal((T, E)).astype(np.float32)
+    res = run_layer(pqe, cfg, T, x, logits_np=logits, fmt_dev=pages.fmt_dev, pool=pages.pool)
+    ids, gates = orc.topk_gates(logits, k)
+    assert np.array_equal(res["ids"], ids) and res["status"] == 0
+    check_tokens(orc, pages, cfg, x, ids, gates, res, np.arange(T, dtype=np.int32))
+
+
+@pytest.mark.parametrize("T,n_check", [(1, 1), (8, 4), (64, 3)])
+def test_config2_decode_shapes(cuda_lib, orc, T, n_check):
+    pqe = cuda_lib
+    cfg = synth.CONFIGS[2]
+    logits = synth.routing_logits(cfg, T, 2)
+    ids, gates = orc.topk_gates(logits, cfg.k)
+    tokens = helpers.sample_tokens(T, n_check, seed=T)
+    needed = set(ids[tokens].reshape(-1).tolist())
+    pages = Pages(pqe, orc, cfg, needed=needed, seed=T)
+    x = synth.activations(cfg, T, 2)
+    res = run_layer(pqe, cfg, T, x, logits_np=logits, fmt_dev=pages.fmt_dev, pool=pages.pool)
+    assert np.array_equal(res["ids"], ids) and res["status"] == 0
+    check_tokens(orc, pages, cfg, x, ids, gates, res, tokens)
+
+
+def test_slot_indirection_and_bad_page(cuda_lib, orc):
+    # experts live in permuted slots; one routed expert points outside the pool
+    pqe = cuda_lib
+    cfg = synth.small_config(E=6, H=128, I=64, k=2, T=40, cid=93)
+    pages = Pages(pqe, orc, cfg, needed=set(range(6)))
+    stride = pqe.slot_stride(cfg.H, cfg.I)
+    perm = np.array([4, 0, 5, 2, 1, 3])
+    pool2 = torch.zeros(8 * stride, dtype=torch.uint8, device=DEV)
+    for e in range(6):
+        pool2[perm[e] * stride:(perm[e] + 1) * stride].copy_(pages.pool_mem[e * stride:(e + 1) * stride])
+    p2 = pqe.make_pool(pool2, 8, cfg.H, cfg.I)
+    x = synth.activations(cfg, 40)
+    logits = np.random.default_rng(1).standard_normal((40, 6)).astype(np.float32)
+    pt = torch.from_numpy(perm.astype(np.int32)).to(DEV)
+    res = run_layer(pqe, cfg, 40, x, logits_np=logits, page_table=pt, fmt_dev=pages.fmt_dev, pool=p2)
+    ids, gates = orc.topk_gates(logits, 2)
+    assert res["status"] == 0
+    check_tokens(orc, pages, cfg, x, ids, gates, res, np.arange(40, dtype=np.int32))
+    # expert 3 -> slot 9 (outside the 8-slot pool): flagged, its rows are zero
+    bad = perm.copy()
+    bad[3] = 9
+    res = run_layer(pqe, cfg, 40, x, logits_np=logits, page_table=torch.from_numpy(bad.astype(np.int32)).to(DEV),
+                    fmt_dev=pages.fmt_dev, pool=p2)
+    assert res["status"] & pqe.PQE_STATUS_BAD_PAGE
+    op = res["out_perm"].float().cpu().numpy()
+    flat = ids.reshape(-1)
+    _, offsets, perm_src, _ = orc.permute(ids, 6)
+    rows3 = np.arange(offsets[3], offsets[4])
+    assert np.all(op[rows3] == 0) and np.any(op[np.arange(offsets[0], offsets[1])] != 0)
