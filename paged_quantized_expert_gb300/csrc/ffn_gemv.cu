@@ -16,29 +16,69 @@
 namespace pqe {
 
 // ---------------------------------------------------------------------------
-// schedule: the list of experts with a non-empty batch, ascending id.
-// sched[0] = count, sched[1 + a] = expert id. One CTA of 1024 threads.
+// schedule (one CTA of 1024 threads, one thread per expert, ascending id):
+//   sched[0] = count, sched[1 + a] = experts for the CUDA-core path;
+//   tiles[i] = {expert, first batch row, valid rows, page entry} of the
+//   128-row tiles of experts on the tensor-core path, *n_tiles their count.
+// An expert goes to the tensor cores when tc_min > 0, its batch has at least
+// tc_min rows, its page is FP8 and its page-table entry is inside the pool.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) ffn_schedule_kernel(const int32_t *__restrict__ offsets, int E,
-                                                            int32_t *__restrict__ sched) {
-    __shared__ int32_t warp_cnt[32];
-    const int e = threadIdx.x, lane = e & 31, w = e >> 5;
-    const bool act = e < E && (offsets[e + 1] - offsets[e]) > 0;
-    const unsigned b = __ballot_sync(0xffffffffu, act);
-    if (lane == 0) warp_cnt[w] = __popc(b);
+__device__ __forceinline__ int block_excl_scan(int v, int *warp_tot, int &total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) warp_tot[w] = incl;
     __syncthreads();
     if (w == 0) {
-        int c = warp_cnt[lane], incl = c;
+        const int c = warp_tot[lane];
+        int ci = c;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            int n = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += n;
+            const int n = __shfl_up_sync(0xffffffffu, ci, o);
+            if (lane >= o) ci += n;
         }
-        warp_cnt[lane] = incl - c;
-        if (lane == 31) sched[0] = incl;
+        warp_tot[lane] = ci - c;
+        if (lane == 31) warp_tot[32] = ci;
     }
     __syncthreads();
-    if (act) sched[1 + warp_cnt[w] + __popc(b & ((1u << lane) - 1u))] = e;
+    const int r = warp_tot[w] + incl - v;
+    total = warp_tot[32];
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(1024) ffn_schedule_kernel(FfnArgs a, int tc_min, int32_t *__restrict__ tiles,
+                                                            int32_t *__restrict__ n_tiles) {
+    __shared__ int warp_tot[33];
+    const int e = threadIdx.x;
+    int n = 0, slot = -1, fmt = PQE_FMT_FP8;
+    if (e < a.E) {
+        n = a.offsets[e + 1] - a.offsets[e];
+        slot = a.page_table[e];
+        fmt = a.expert_fmt ? (int)a.expert_fmt[e] : PQE_FMT_FP8;
+    }
+    const bool valid_page = slot >= 0 && slot < a.n_slots + a.n_wb;
+    const bool tc = n > 0 && tc_min > 0 && n >= tc_min && fmt == PQE_FMT_FP8 && valid_page;
+    const bool gemv = n > 0 && !tc;
+    int total;
+    const int gpos = block_excl_scan(gemv ? 1 : 0, warp_tot, total);
+    if (gemv) a.sched[1 + gpos] = e;
+    if (threadIdx.x == 0) a.sched[0] = total;
+    const int nt = tc ? (n + 127) / 128 : 0;
+    const int tpos = block_excl_scan(nt, warp_tot, total);
+    for (int i = 0; i < nt; ++i) {
+        int4 t;
+        t.x = e;
+        t.y = a.offsets[e] + 128 * i;
+        t.z = min(128, n - 128 * i);
+        t.w = slot;
+        reinterpret_cast<int4 *>(tiles)[tpos + i] = t;
+    }
+    if (threadIdx.x == 0) *n_tiles = total;
 }
 
 __device__ __forceinline__ bool page_ok(const FfnArgs &a, int e, int &slot, int &fmt) {
@@ -96,18 +136,19 @@ __global__ void __launch_bounds__(256) ffn_w13_gemv_kernel(FfnArgs a) {
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw);  // [NT][H]
     const int H = a.H, I = a.I;
     const int rblocks = I / 8;
-    const int act_i = blockIdx.x / rblocks, rb = blockIdx.x % rblocks;
-    if (act_i >= a.sched[0]) return;
+    const int units = a.sched[0] * rblocks;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
+    const int act_i = unit / rblocks, rb = unit % rblocks;
     const int e = a.sched[1 + act_i];
     const int p0 = a.offsets[e], n = a.offsets[e + 1] - p0;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int j = rb * 8 + warp;
     int slot, fmt;
     if (!page_ok(a, e, slot, fmt)) {
         if (threadIdx.x == 0) atomicOr(a.status, PQE_STATUS_BAD_PAGE);
         if (lane == 0)
             for (int p = p0; p < p0 + n; ++p) a.h[(size_t)p * I + j] = 0.0f;
-        return;
+        continue;
     }
     const uint8_t *page = page_addr(a, slot);
     for (int g0 = 0; g0 < n; g0 += NT) {
@@ -187,6 +228,8 @@ __global__ void __launch_bounds__(256) ffn_w13_gemv_kernel(FfnArgs a) {
             }
         }
     }
+    __syncthreads();  // x staging is reused by the next unit
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -201,11 +244,12 @@ __global__ void __launch_bounds__(256) ffn_w2_gemv_kernel(FfnArgs a) {
     __shared__ float outs[NT][32];
     const int H = a.H, I = a.I;
     const int rblocks = H / 32;
-    const int act_i = blockIdx.x / rblocks, rb = blockIdx.x % rblocks;
-    if (act_i >= a.sched[0]) return;
+    const int units = a.sched[0] * rblocks;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
+    const int act_i = unit / rblocks, rb = unit % rblocks;
     const int e = a.sched[1 + act_i];
     const int p0 = a.offsets[e], n = a.offsets[e + 1] - p0;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int r0 = rb * 32 + warp * 4;
     int slot, fmt;
     const bool ok = page_ok(a, e, slot, fmt);
@@ -315,13 +359,12 @@ __global__ void __launch_bounds__(256) ffn_w2_gemv_kernel(FfnArgs a) {
         }
     }
     if (!ok && threadIdx.x == 0 && n > 0) atomicOr(a.status, PQE_STATUS_BAD_PAGE);
+    __syncthreads();  // h staging and outs are reused by the next unit
+    }
 }
 
 int launch_ffn_gemv(const FfnArgs &args, int max_active, cudaStream_t s) {
     constexpr int NT = 4;
-    const int E = args.E;
-    ffn_schedule_kernel<<<1, 1024, 0, s>>>(args.offsets, E, args.sched);
-    PQE_LAUNCH_CHECK();
     const size_t smem13 = (size_t)NT * args.H * sizeof(uint16_t);
     const size_t smem2 = (size_t)NT * args.I * sizeof(float);
     if (smem13 > 48 * 1024)
@@ -330,13 +373,48 @@ int launch_ffn_gemv(const FfnArgs &args, int max_active, cudaStream_t s) {
     if (smem2 > 48 * 1024)
         PQE_CUDA_TRY(cudaFuncSetAttribute(ffn_w2_gemv_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)smem2));
-    const long g13 = (long)max_active * (args.I / 8);
-    const long g2 = (long)max_active * (args.H / 32);
-    ffn_w13_gemv_kernel<NT><<<(unsigned)g13, 256, smem13, s>>>(args);
+    // grid-stride over (expert, row block) units; the unit count is known on the device
+    const long cap = 148L * 8;
+    const long u13 = (long)max_active * (args.I / 8), u2 = (long)max_active * (args.H / 32);
+    ffn_w13_gemv_kernel<NT><<<(unsigned)(u13 < cap ? u13 : cap), 256, smem13, s>>>(args);
     PQE_LAUNCH_CHECK();
-    ffn_w2_gemv_kernel<NT><<<(unsigned)g2, 256, smem2, s>>>(args);
+    ffn_w2_gemv_kernel<NT><<<(unsigned)(u2 < cap ? u2 : cap), 256, smem2, s>>>(args);
     PQE_LAUNCH_CHECK();
     return PQE_OK;
+}
+
+// workspace carve-up shared by the size query and the call
+struct FfnWs {
+    size_t sched, tiles, n_tiles, h, xq, sx, hbf, hmax, hq, sh, total;
+    int max_tiles;
+    bool tc;
+};
+
+static FfnWs ffn_ws_layout(int T, int k, int E, int H, int I) {
+    FfnWs w{};
+    const size_t A = (size_t)T * k;
+    w.tc = tc_shape_ok(H, I) && A >= (size_t)TC_MIN_ROWS;
+    w.max_tiles = w.tc ? (int)((A + 127) / 128 + (size_t)E) : 0;
+    size_t off = 0;
+    auto take = [&off](size_t b) {
+        const size_t at = off;
+        off += round_up(b ? b : 1, 256);
+        return at;
+    };
+    w.sched = take(sizeof(int32_t) * (E + 1));
+    w.tiles = take(sizeof(int32_t) * 4 * (size_t)(w.max_tiles ? w.max_tiles : 1));
+    w.n_tiles = take(sizeof(int32_t));
+    w.h = take(A * I * sizeof(float));
+    if (w.tc) {
+        w.xq = take(A * H);
+        w.sx = take(A * sizeof(float));
+        w.hbf = take(A * I * sizeof(uint16_t));
+        w.hmax = take(A * sizeof(uint32_t));
+        w.hq = take(A * I);
+        w.sh = take(A * sizeof(float));
+    }
+    w.total = off;
+    return w;
 }
 
 }  // namespace pqe
@@ -347,8 +425,7 @@ extern "C" {
 
 size_t moe_paged_ffn_workspace_size(int T, int k, int E, int H, int I) {
     if (T < 0 || k < 1 || E < 1 || !shape_ok(H, I)) return 0;
-    const size_t A = (size_t)T * k;
-    return round_up(sizeof(int32_t) * (E + 1), 256) + round_up(A * I * sizeof(float), 256);
+    return ffn_ws_layout(T, k, E, H, I).total;
 }
 
 int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *offsets, const int32_t *page_table,
@@ -379,13 +456,32 @@ int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *of
     args.E = E;
     args.H = pool->H;
     args.I = pool->I;
-    args.sched = static_cast<int32_t *>(ws);
-    args.h = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + round_up(sizeof(int32_t) * (E + 1), 256));
+    const FfnWs w = ffn_ws_layout(T, k, E, pool->H, pool->I);
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    args.sched = reinterpret_cast<int32_t *>(wsb + w.sched);
+    args.h = reinterpret_cast<float *>(wsb + w.h);
     args.out_perm = static_cast<uint16_t *>(out_perm);
     args.status = status;
     const long A = (long)T * k;
     const int max_active = (int)(A < E ? A : E);
-    return launch_ffn_gemv(args, max_active, as_stream(stream));
+    cudaStream_t s = as_stream(stream);
+    int32_t *tiles = reinterpret_cast<int32_t *>(wsb + w.tiles);
+    int32_t *n_tiles = reinterpret_cast<int32_t *>(wsb + w.n_tiles);
+    ffn_schedule_kernel<<<1, 1024, 0, s>>>(args, w.tc ? TC_MIN_ROWS : 0, tiles, n_tiles);
+    PQE_LAUNCH_CHECK();
+    int rc = launch_ffn_gemv(args, max_active, s);
+    if (rc != PQE_OK || !w.tc) return rc;
+    TcBuffers b{};
+    b.A = A;
+    b.tiles = tiles;
+    b.n_tiles = n_tiles;
+    b.xq = wsb + w.xq;
+    b.sx = reinterpret_cast<float *>(wsb + w.sx);
+    b.h = reinterpret_cast<uint16_t *>(wsb + w.hbf);
+    b.hmax = reinterpret_cast<uint32_t *>(wsb + w.hmax);
+    b.hq = wsb + w.hq;
+    b.sh = reinterpret_cast<float *>(wsb + w.sh);
+    return launch_ffn_tc(args, b, w.max_tiles, s);
 }
 
 }  // extern "C"

@@ -29,6 +29,24 @@ __device__ __forceinline__ const uint8_t *page_addr(const FfnArgs &a, int slot) 
                             : a.wb_base + (size_t)(slot - a.n_slots) * a.slot_stride;
 }
 
+// scratch of the tensor-core path (all device, inside the FFN workspace)
+struct TcBuffers {
+    long A;
+    int32_t *tiles;      // [max_tiles][4]: expert, first batch row, valid rows, page-table entry
+    int32_t *n_tiles;    // [1]
+    uint8_t *xq;         // E4M3 [A, H] activations in batch order
+    float *sx;           // [A] their row scales
+    uint16_t *h;         // bf16 [A, I]
+    uint32_t *hmax;      // [A] row amax of h (fp32 bits)
+    uint8_t *hq;         // E4M3 [A, I]
+    float *sh;           // [A]
+};
+
+// batches of at least this many rows (FP8 pages) take the tensor-core path
+constexpr int TC_MIN_ROWS = 64;
+
+bool tc_shape_ok(int H, int I);
 int launch_ffn_gemv(const FfnArgs &args, int max_active, cudaStream_t s);
+int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaStream_t s);
 
 }  // namespace pqe

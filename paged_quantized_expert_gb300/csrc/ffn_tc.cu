@@ -1,0 +1,522 @@
+// ffn_tc.cu -- expert FFN for large per-expert batches on the 5th-generation
+// tensor cores (tcgen05, FP8 E4M3 x E4M3 -> fp32 in TMEM), fed by TMA from
+// the slot pool through the page table.
+//
+// Module-based batching (MoE-Gen summary, aibr.jp, "3.中核となる技術的要素")
+// gives each expert a batch of hundreds of tokens; the FFN is then a grouped
+// GEMM over ragged per-expert segments. The weights are read from the slot
+// each expert's page occupies (expert-pager article, rand.pepabo.com,
+// "エキスパート重みの階層ページング"): one 3-D TMA tensor map per pool region
+// [slot, row, k] with the slot as the outer coordinate.
+//
+// Per segment of expert e (rows p of the permuted batch, tiles of 128):
+//   GEMM1  D[128 x 256] = Xq[p, :] . [W13 gate rows j..j+127 ; up rows I+j..]^T
+//          epilogue: u = D * sx[p] * s13[row]; h = SiLU(u_gate) * u_up -> bf16,
+//          row amax of h -> hmax[p]
+//   hquant hq[p, :] = E4M3(h[p, :] / sh[p]), sh[p] = hmax[p] / 448
+//   GEMM2  D[128 x 256] = hq[p, :] . W2[n..n+255, :]^T
+//          epilogue: out_perm[p, n..] = D * sh[p] * s2[n] -> bf16
+// Activations are quantised per row to E4M3 (scale amax / 448) by a gather
+// kernel that also lays the rows out in batch order for TMA.
+//
+// CTA = 6 warps: warp 0 issues TMA (one thread), warp 1 owns TMEM and issues
+// the MMAs (one thread), warps 2-5 read the accumulator from TMEM (each warp
+// its 32-lane quarter) and run the epilogue. 4-stage smem ring of
+// A [128 x 128 B] + B [256 x 128 B] tiles, 128-byte swizzle, K-major.
+// Every mbarrier wait is bounded: on expiry the CTA sets PQE_STATUS_TIMEOUT,
+// drains what it issued (bounded), frees its TMEM and returns.
+#include <cuda.h>
+
+#include "ffn_internal.cuh"
+#include "pqe_common.cuh"
+
+namespace pqe {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 128;  // bytes of K per stage (FP8)
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK;
+constexpr int B_BYTES = BN * BK;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t WAIT_LIMIT = 1u << 22;
+// smem: stages | full[S] empty[S] tmem_full (8 B each) | tmem base | column scales [256]
+constexpr int SMEM_BAR_OFF = STAGES * STAGE_BYTES;
+constexpr int SMEM_TMEM_OFF = SMEM_BAR_OFF + 8 * (2 * STAGES + 1);
+constexpr int SMEM_SCALE_OFF = (SMEM_TMEM_OFF + 4 + 15) / 16 * 16;
+constexpr int SMEM_BYTES = SMEM_SCALE_OFF + 4 * BN + 1024;  // + alignment slack
+
+// instruction descriptor, kind::f8f6f4: D f32, A/B E4M3, both K-major, N, M
+constexpr uint32_t IDESC = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                           ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// bounded wait; false after WAIT_LIMIT polls
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (i > 32) __nanosleep(128);
+    }
+    return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+        "%4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+// shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;             // leading byte offset (unused for this layout)
+    d |= (uint64_t)(1024 >> 4) << 32;   // stride byte offset
+    d |= (uint64_t)1 << 46;             // descriptor version
+    d |= (uint64_t)2 << 61;             // 128-byte swizzle
+    return d;
+}
+
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\ttcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, "
+        "p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accum)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+struct GemmArgs {
+    const int32_t *tiles;    // [n][4]: expert, first row p0, valid rows, page-table entry
+    const int32_t *n_tiles;  // device count
+    int n_slots;             // entries below this use the cache map, others the working-buffer map
+    int K;                   // reduction length in bytes (H for GEMM1, I for GEMM2)
+    int I;                   // GEMM1: up rows start at I
+    int out_cols;            // row length of the output (I for h, H for out_perm)
+    int swiglu;              // 1: GEMM1 epilogue, 0: GEMM2 epilogue
+    const float *row_scale;  // sx or sh [A]
+    const uint8_t *pool_base, *wb_base;
+    size_t slot_stride;
+    size_t wscale_off;       // byte offset of the weight row scales in a page (s13 or s2)
+    uint16_t *out;           // bf16 h [A, I] or out_perm [A, H]
+    uint32_t *hmax;          // [A] (GEMM1)
+    int32_t *status;
+};
+
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB_cache,
+                   const __grid_constant__ CUtensorMap tmB_wb, const GemmArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    if ((int)blockIdx.x >= *a.n_tiles) return;
+    // 1024-byte alignment for the 128-byte swizzle atoms
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar_full = sbase + SMEM_BAR_OFF;
+    const uint32_t bar_empty = bar_full + 8 * STAGES;
+    const uint32_t bar_tmem = bar_empty + 8 * STAGES;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SMEM_TMEM_OFF);
+    float *col_scale = reinterpret_cast<float *>(smem + SMEM_SCALE_OFF);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int4 tile = reinterpret_cast<const int4 *>(a.tiles)[blockIdx.x];
+    const int p0 = tile.y, nv = tile.z, slot = tile.w;
+    const int nt = blockIdx.y;
+    // B rows of this N tile: two halves of 128 rows
+    const int r0 = a.swiglu ? nt * 128 : nt * 256;
+    const int r1 = a.swiglu ? a.I + nt * 128 : nt * 256 + 128;
+    const bool in_cache = slot < a.n_slots;
+    const CUtensorMap *tmB = in_cache ? &tmB_cache : &tmB_wb;
+    const int zc = in_cache ? slot : slot - a.n_slots;
+    const uint8_t *page = in_cache ? a.pool_base + (size_t)slot * a.slot_stride
+                                   : a.wb_base + (size_t)(slot - a.n_slots) * a.slot_stride;
+    const int nk = a.K / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        mbar_init(bar_tmem, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmB)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    if (warp >= 2) {
+        // weight row scales of the 256 output columns
+        const float *ws = reinterpret_cast<const float *>(page + a.wscale_off);
+        for (int c = threadIdx.x - 64; c < BN; c += 128) col_scale[c] = ws[c < 128 ? r0 + c : r1 + (c - 128)];
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int issued = 0;
+            bool ok = true;
+            for (int kb = 0; kb < nk && ok; ++kb) {
+                const int s = kb % STAGES;
+                const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
+                if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sa = sbase + s * STAGE_BYTES, sb = sa + A_BYTES;
+                mbar_expect_tx(bar_full + 8 * s, STAGE_BYTES);
+                tma_load_2d(sa, &tmA, kb * BK, p0, bar_full + 8 * s);
+                tma_load_3d(sb, tmB, kb * BK, r0, zc, bar_full + 8 * s);
+                tma_load_3d(sb + B_BYTES / 2, tmB, kb * BK, r1, zc, bar_full + 8 * s);
+                ++issued;
+            }
+            if (!ok) atomicOr(a.status, PQE_STATUS_TIMEOUT);
+            // drain: every stage issued has landed before the CTA may exit
+            for (int kb = (issued > STAGES ? issued - STAGES : 0); kb < issued; ++kb)
+                mbar_wait(bar_full + 8 * (kb % STAGES), (uint32_t)(kb / STAGES) & 1u);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            bool ok = true;
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % STAGES;
+                const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
+                if (!mbar_wait(bar_full + 8 * s, ph)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sa = sbase + s * STAGE_BYTES, sb = sa + A_BYTES;
+#pragma unroll
+                for (int k = 0; k < BK / 32; ++k)
+                    umma_f8(tmem, sw128_desc(sa + 32 * k), sw128_desc(sb + 32 * k), (kb | k) != 0);
+                umma_commit(bar_empty + 8 * s);
+            }
+            if (!ok) atomicOr(a.status, PQE_STATUS_TIMEOUT);
+            umma_commit(bar_tmem);
+        }
+    } else {
+        // epilogue: this warp's TMEM lane quarter
+        const int q = warp & 3;
+        const int m = 32 * q + lane;
+        const int p = p0 + m;
+        const bool valid = m < nv;
+        const bool ok = mbar_wait(bar_tmem, 0);
+        tc_fence_after();
+        if (!ok) {
+            if (lane == 0) atomicOr(a.status, PQE_STATUS_TIMEOUT);
+        } else {
+            const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+            const float rs = valid ? a.row_scale[p] : 0.0f;
+            if (a.swiglu) {
+                float amax = 0.0f;
+                uint16_t *dst = a.out + (size_t)p * a.out_cols + nt * 128;
+                for (int c0 = 0; c0 < 128; c0 += 32) {
+                    uint32_t g[32], u[32];
+                    tmem_ld32(trow + c0, g);
+                    tmem_ld32(trow + 128 + c0, u);
+                    tmem_ld_wait();
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        float h2[2];
+#pragma unroll
+                        for (int t = 0; t < 2; ++t) {
+                            const float gv = __uint_as_float(g[i + t]) * rs * col_scale[c0 + i + t];
+                            const float uv = __uint_as_float(u[i + t]) * rs * col_scale[128 + c0 + i + t];
+                            h2[t] = silu(gv) * uv;
+                        }
+                        const uint16_t b0 = f32_to_bf16_rn(h2[0]), b1 = f32_to_bf16_rn(h2[1]);
+                        amax = fmaxf(amax, fmaxf(fabsf(bf16_to_f32(b0)), fabsf(bf16_to_f32(b1))));
+                        packed[i / 2] = (uint32_t)b0 | ((uint32_t)b1 << 16);
+                    }
+                    if (valid) {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            d4[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+                    }
+                }
+                if (valid) atomicMax(a.hmax + p, __float_as_uint(amax));
+            } else {
+                uint16_t *dst = a.out + (size_t)p * a.out_cols + nt * 256;
+                for (int c0 = 0; c0 < 256; c0 += 32) {
+                    uint32_t d[32];
+                    tmem_ld32(trow + c0, d);
+                    tmem_ld_wait();
+                    uint32_t packed[16];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {
+                        const float v0 = __uint_as_float(d[i]) * rs * col_scale[c0 + i];
+                        const float v1 = __uint_as_float(d[i + 1]) * rs * col_scale[c0 + i + 1];
+                        packed[i / 2] = (uint32_t)f32_to_bf16_rn(v0) | ((uint32_t)f32_to_bf16_rn(v1) << 16);
+                    }
+                    if (valid) {
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            d4[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
+// gather + quantise: row p of the batch <- E4M3(x[perm_src[p] / k] / sx[p]),
+// sx[p] = amax / 448 (1 for a zero row); one warp per row, rows of TC tiles.
+// Also clears hmax for the rows.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) tc_gather_quant_kernel(const uint16_t *__restrict__ x,
+                                                              const int32_t *__restrict__ perm_src, int k, int H,
+                                                              const int32_t *__restrict__ tiles,
+                                                              const int32_t *__restrict__ n_tiles,
+                                                              uint8_t *__restrict__ xq, float *__restrict__ sx,
+                                                              uint32_t *__restrict__ hmax) {
+    if ((int)blockIdx.x >= *n_tiles) return;
+    const int4 tile = reinterpret_cast<const int4 *>(tiles)[blockIdx.x];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int m = warp; m < tile.z; m += blockDim.x >> 5) {
+        const int p = tile.y + m;
+        const int t = perm_src[p] / k;
+        const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
+        float amax = 0.0f;
+        for (int c = lane; c < H / 8; c += 32) {
+            const uint4 v = __ldg(xr + c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xffff0000u))));
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+        const float inv = __fdiv_rn(1.0f, s);
+        for (int c = lane; c < H / 8; c += 32) {
+            const uint4 v = __ldg(xr + c);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t q[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const uint16_t lo = f32x2_to_e4m3x2(__uint_as_float(w[2 * i] << 16) * inv,
+                                                    __uint_as_float(w[2 * i] & 0xffff0000u) * inv);
+                const uint16_t hi = f32x2_to_e4m3x2(__uint_as_float(w[2 * i + 1] << 16) * inv,
+                                                    __uint_as_float(w[2 * i + 1] & 0xffff0000u) * inv);
+                q[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+            }
+            reinterpret_cast<uint2 *>(xq + (size_t)p * H)[c] = make_uint2(q[0], q[1]);
+        }
+        if (lane == 0) {
+            sx[p] = s;
+            hmax[p] = 0u;
+        }
+    }
+}
+
+// hq[p, :] = E4M3(h[p, :] / sh[p]), sh[p] = hmax[p] / 448; one warp per row
+__global__ void __launch_bounds__(256) tc_hquant_kernel(const uint16_t *__restrict__ h, int I,
+                                                        const int32_t *__restrict__ tiles,
+                                                        const int32_t *__restrict__ n_tiles,
+                                                        const uint32_t *__restrict__ hmax, uint8_t *__restrict__ hq,
+                                                        float *__restrict__ sh) {
+    if ((int)blockIdx.x >= *n_tiles) return;
+    const int4 tile = reinterpret_cast<const int4 *>(tiles)[blockIdx.x];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int m = warp; m < tile.z; m += blockDim.x >> 5) {
+        const int p = tile.y + m;
+        const float amax = __uint_as_float(hmax[p]);
+        const float s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+        const float inv = __fdiv_rn(1.0f, s);
+        const uint4 *hr = reinterpret_cast<const uint4 *>(h + (size_t)p * I);
+        for (int c = lane; c < I / 8; c += 32) {
+            const uint4 v = hr[c];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t q[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const uint16_t lo = f32x2_to_e4m3x2(__uint_as_float(w[2 * i] << 16) * inv,
+                                                    __uint_as_float(w[2 * i] & 0xffff0000u) * inv);
+                const uint16_t hi = f32x2_to_e4m3x2(__uint_as_float(w[2 * i + 1] << 16) * inv,
+                                                    __uint_as_float(w[2 * i + 1] & 0xffff0000u) * inv);
+                q[i] = (uint32_t)lo | ((uint32_t)hi << 16);
+            }
+            reinterpret_cast<uint2 *>(hq + (size_t)p * I)[c] = make_uint2(q[0], q[1]);
+        }
+        if (lane == 0) sh[p] = s;
+    }
+}
+
+// ---- host: tensor maps -------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D [rows, cols] uint8, box [128 rows, 128 cols], 128-byte swizzle
+static bool map_2d(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols};
+    cuuint32_t box[2] = {128, 128};
+    cuuint32_t es[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D [slots, rows, cols] uint8 with a slot stride, box [1, 128, 128]
+static bool map_3d(CUtensorMap *m, const void *base, uint64_t slots, uint64_t rows, uint64_t cols,
+                   uint64_t slot_stride) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    cuuint64_t dims[3] = {cols, rows, slots};
+    cuuint64_t strides[2] = {cols, slot_stride};
+    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace tc
+
+bool tc_shape_ok(int H, int I) { return H % 256 == 0 && I % 128 == 0 && H >= 256 && I >= 128; }
+
+int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaStream_t s) {
+    using namespace tc;
+    const int H = args.H, I = args.I;
+    const long A = b.A;
+    CUtensorMap mx, mh, m13c, m13w, m2c, m2w;
+    const PageLayout L = fp8_layout(H, I);
+    // the working-buffer / cache maps need a non-empty region to encode; an
+    // absent region gets a one-slot map over the other base (never selected)
+    const uint8_t *cache = args.n_slots ? args.pool_base : args.wb_base;
+    const uint8_t *wb = args.n_wb ? args.wb_base : args.pool_base;
+    const uint64_t ns = args.n_slots ? args.n_slots : 1, nw = args.n_wb ? args.n_wb : 1;
+    bool ok = map_2d(&mx, b.xq, (uint64_t)A, (uint64_t)H) && map_2d(&mh, b.hq, (uint64_t)A, (uint64_t)I) &&
+              map_3d(&m13c, cache + L.w13, ns, 2 * (uint64_t)I, H, args.slot_stride) &&
+              map_3d(&m13w, wb + L.w13, nw, 2 * (uint64_t)I, H, args.slot_stride) &&
+              map_3d(&m2c, cache + L.w2, ns, (uint64_t)H, I, args.slot_stride) &&
+              map_3d(&m2w, wb + L.w2, nw, (uint64_t)H, I, args.slot_stride);
+    if (!ok) return PQE_ERR_UNSUPPORTED;
+    static bool attr_set = false;
+    if (!attr_set) {
+        PQE_CUDA_TRY(cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
+        attr_set = true;
+    }
+    tc_gather_quant_kernel<<<max_tiles, 256, 0, s>>>(args.x, args.perm_src, args.k, H, b.tiles, b.n_tiles, b.xq,
+                                                     b.sx, b.hmax);
+    PQE_LAUNCH_CHECK();
+    GemmArgs g1{};
+    g1.tiles = b.tiles;
+    g1.n_tiles = b.n_tiles;
+    g1.n_slots = args.n_slots;
+    g1.K = H;
+    g1.I = I;
+    g1.out_cols = I;
+    g1.swiglu = 1;
+    g1.row_scale = b.sx;
+    g1.pool_base = args.pool_base;
+    g1.wb_base = args.wb_base;
+    g1.slot_stride = args.slot_stride;
+    g1.wscale_off = L.s13;
+    g1.out = b.h;
+    g1.hmax = b.hmax;
+    g1.status = args.status;
+    tc_gemm_kernel<<<dim3(max_tiles, I / 128), THREADS, SMEM_BYTES, s>>>(mx, m13c, m13w, g1);
+    PQE_LAUNCH_CHECK();
+    tc_hquant_kernel<<<max_tiles, 256, 0, s>>>(b.h, I, b.tiles, b.n_tiles, b.hmax, b.hq, b.sh);
+    PQE_LAUNCH_CHECK();
+    GemmArgs g2 = g1;
+    g2.K = I;
+    g2.out_cols = H;
+    g2.swiglu = 0;
+    g2.row_scale = b.sh;
+    g2.wscale_off = L.s2;
+    g2.out = args.out_perm;
+    g2.hmax = nullptr;
+    tc_gemm_kernel<<<dim3(max_tiles, H / 256), THREADS, SMEM_BYTES, s>>>(mh, m2c, m2w, g2);
+    PQE_LAUNCH_CHECK();
+    return PQE_OK;
+}
+
+}  // namespace pqe
