@@ -190,6 +190,25 @@ PQE_API int moe_permute(const int32_t *topk_ids, int T, int k, int E, int32_t *c
                 int32_t *perm_src, int32_t *inv, void *ws, size_t ws_bytes, int32_t *status,
                 void *stream);
 
+/* moe_permute_static -- moe_permute without a caller-provided workspace.
+ * The pages have no counterpart of this call. It exists for callers that
+ * cannot hand the library scratch memory: a plugin inside a framework that
+ * owns all device memory and exposes no allocator to it, or a steady-state
+ * serving loop that must not call cudaMalloc/cudaFree because those
+ * synchronise the device. Its scratch is one file-scope device array of
+ * moe_permute_static_max_words() int32 (4 MiB), held on every GPU that loads
+ * the library until the process exits; calls with T*k*E beyond it (more
+ * than 1M chunk-histogram words, i.e. ceil(T*k/2048)*E > 1048576) return
+ * PQE_ERR_CAPACITY. The call allocates nothing. The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture. All calls share
+ * the one array, so calls that overlap on the GPU (other streams, other host
+ * threads) race and corrupt each other's results; issue them in one stream
+ * order. Results are identical to moe_permute's. */
+PQE_API size_t moe_permute_static_max_words(void);
+PQE_API int moe_permute_static(const int32_t *topk_ids, int T, int k, int E, int32_t *counts, int32_t *offsets,
+                               int32_t *perm_src, int32_t *inv, int32_t *status, void *stream);
+
 /* ------------------------------------------------------------------------
  * moe_paged_ffn -- grouped SwiGLU expert FFN over the slot pool ([EP]
  * 階層ページング for the paging, 評価 for w13/w2; [PW] for 4-bit pages).

@@ -86,6 +86,8 @@ _SIGS = {
     "moe_route": (I32, [P, P, P, I32, I32, I32, I32, P, P, P]),
     "moe_permute_workspace_size": (SZ, [I32, I32, I32]),
     "moe_permute": (I32, [P, I32, I32, I32, P, P, P, P, P, SZ, P, P]),
+    "moe_permute_static_max_words": (SZ, []),
+    "moe_permute_static": (I32, [P, I32, I32, I32, P, P, P, P, P, P]),
     "moe_paged_ffn_workspace_size": (SZ, [I32, I32, I32, I32, I32]),
     "moe_paged_ffn": (I32, [P, P, P, P, P, C.POINTER(pqe_pool), I32, I32, I32, P, P, SZ, P, P]),
     "moe_combine": (I32, [P, P, P, I32, I32, I32, P, P]),
@@ -248,6 +250,12 @@ def moe_permute(topk_ids, T, k, E, counts, offsets, perm_src, inv, ws, status, s
     nbytes = ws.numel() * ws.element_size() if ws is not None else 0
     _check("moe_permute", lib().moe_permute(_ptr(topk_ids), T, k, E, _ptr(counts), _ptr(offsets), _ptr(perm_src),
                                             _ptr(inv), _ptr(ws), nbytes, _ptr(status), _stream(stream)))
+
+
+def moe_permute_static(topk_ids, T, k, E, counts, offsets, perm_src, inv, status, stream=None):
+    """moe_permute with the library's own fixed device scratch (no workspace argument)."""
+    _check("moe_permute_static", lib().moe_permute_static(_ptr(topk_ids), T, k, E, _ptr(counts), _ptr(offsets),
+                                                          _ptr(perm_src), _ptr(inv), _ptr(status), _stream(stream)))
 
 
 def moe_paged_ffn_workspace_size(T, k, E, H, I) -> int:

@@ -323,6 +323,32 @@ __global__ void __launch_bounds__(256) quant_mxfp4_kernel(const uint8_t *__restr
     if (lane == 0) x8[(size_t)r * nblk + b] = (uint8_t)sb;
 }
 
+// ---------------------------------------------------------------------------
+// Scratch of moe_permute_static: a file-scope device array, so that call needs
+// no workspace from the caller. Every GPU that loads the library holds it
+// until the process exits. Only device code may name it; host code reaches it
+// through the per-device address from cudaGetSymbolAddress.
+// ---------------------------------------------------------------------------
+constexpr size_t PERM_STATIC_WORDS = (size_t)1 << 20;  // 4 MiB of int32 chunk histograms
+static __device__ __align__(256) int32_t g_perm_scratch[PERM_STATIC_WORDS];
+
+constexpr int MAX_DEVICES = 64;
+static int32_t *g_perm_scratch_addr[MAX_DEVICES];
+
+// address of g_perm_scratch on the current device, looked up once per device
+static int perm_static_scratch(int32_t **out) {
+    int dev = 0;
+    PQE_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= MAX_DEVICES) return PQE_ERR_UNSUPPORTED;
+    if (!g_perm_scratch_addr[dev]) {
+        void *p = nullptr;
+        PQE_CUDA_TRY(cudaGetSymbolAddress(&p, g_perm_scratch));
+        g_perm_scratch_addr[dev] = static_cast<int32_t *>(p);
+    }
+    *out = g_perm_scratch_addr[dev];
+    return PQE_OK;
+}
+
 }  // namespace pqe
 
 using namespace pqe;
@@ -385,6 +411,22 @@ int moe_permute(const int32_t *topk_ids, int T, int k, int E, int32_t *counts, i
     perm_scatter_kernel<<<nchunk, PERM_THREADS, smem, s>>>(topk_ids, (int)A, E, hist, perm_src, inv);
     PQE_LAUNCH_CHECK();
     return PQE_OK;
+}
+
+size_t moe_permute_static_max_words(void) { return PERM_STATIC_WORDS; }
+
+int moe_permute_static(const int32_t *topk_ids, int T, int k, int E, int32_t *counts, int32_t *offsets,
+                       int32_t *perm_src, int32_t *inv, int32_t *status, void *stream) {
+    PQE_CHECK_ARG(T >= 0 && k >= 1 && k <= 32 && E >= 1 && E <= 1024);
+    PQE_CHECK_ARG(counts && offsets && status);
+    const size_t need = moe_permute_workspace_size(T, k, E);
+    if (need > PERM_STATIC_WORDS * sizeof(int32_t)) return PQE_ERR_CAPACITY;
+    int32_t *scratch = nullptr;
+    int rc = perm_static_scratch(&scratch);
+    if (rc != PQE_OK) return rc;
+    // the chunk histograms are written in full by every call before they are
+    // read, so nothing has to be cleared between calls
+    return moe_permute(topk_ids, T, k, E, counts, offsets, perm_src, inv, scratch, need, status, stream);
 }
 
 int moe_combine(const void *out_perm, const int32_t *inv, const float *topk_w, int T, int k, int H, void *y_bf16,
