@@ -50,6 +50,13 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="skip the T=1 and T=8 lines")
+    ap.add_argument("--no-batched", action="store_true", help="skip the module-batched (T=16384) measurement")
+    ap.add_argument("--batched-steps", type=int, default=6)
+    ap.add_argument("--workload", default="decode", choices=["decode", "batched"],
+                    help="batched: only the module-batched measurement (for profiling)")
+    ap.add_argument("--pager", default="both", choices=["host", "device", "both"],
+                    help="host: LRU on the host (one read-back per step); device: LRU on the GPU, each layer's step "
+                         "replayed from a CUDA graph; both: measure both, the faster is the headline")
     return ap.parse_args()
 
 
@@ -60,6 +67,17 @@ def peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def fp8_peak_tflops():
+    """Dense FP8 peak: the measured bf16 cuBLAS rate x the nominal FP8/bf16
+    ratio of 2 (4.5 / 2.25 PFLOP/s), as no FP8 rate is measured."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return 2.0 * float(d["bf16_tflops"]), "measured bf16 x 2 (nominal fp8/bf16 ratio)"
+    return 2.0 * 1900.0, "fallback bf16 x 2"
 
 
 # ---- distributed (replicas only: no data-path collective) -------------------------
@@ -183,6 +201,80 @@ class Runner:
     def close(self):
         for l in self.layers:
             l.close()
+
+
+class GraphRunner:
+    """Device-pager layers, each step captured once into a CUDA graph: a timed
+    step is a copy of that step's logits and x into the graph's input buffers
+    (device to device, 64 KB / 256 KB at T=64) plus one graph replay."""
+
+    def __init__(self, pqe, torch, device, host, L, T):
+        E, H, I, k, S = CFG.E, CFG.H, CFG.I, CFG.k, CFG.S
+        self.pqe, self.torch, self.T = pqe, torch, T
+        self.wb = pqe.alloc_working_buffer(E, H, I, device)
+        nbytes = [pqe.page_bytes(pqe.PQE_FMT_FP8, H, I)] * E
+        self.layers = [pqe.PagedMoELayer(E, H, I, k, S, E, T, host, nbytes, working_buffer=self.wb, device=device,
+                                         device_pager=True) for _ in range(L)]
+        self.stream = torch.cuda.Stream(device)
+        self.x = [torch.zeros((T, H), dtype=torch.int16, device=device) for _ in range(L)]
+        self.lg = [torch.zeros((T, E), dtype=torch.float32, device=device) for _ in range(L)]
+        self.y = [torch.zeros((T, H), dtype=torch.bfloat16, device=device) for _ in range(L)]
+        self.graphs = []
+        self.nodes = []
+
+    def capture(self, logits0, x0):
+        torch = self.torch
+        with torch.cuda.stream(self.stream):
+            for l, layer in enumerate(self.layers):
+                self.x[l].copy_(x0)
+                self.lg[l].copy_(logits0[l])
+                layer.step(self.x[l], self.y[l], self.T, logits=self.lg[l], stream=self.stream)  # eager warm-up
+            torch.cuda.synchronize()
+            for l, layer in enumerate(self.layers):
+                g = torch.cuda.CUDAGraph()
+                n0 = self.pqe.kernel_launches()
+                with torch.cuda.graph(g, stream=self.stream):
+                    layer.step(self.x[l], self.y[l], self.T, logits=self.lg[l], stream=self.stream)
+                # launches recorded during the capture = kernel nodes run by each replay
+                self.nodes.append(self.pqe.kernel_launches() - n0)
+                self.graphs.append(g)
+        torch.cuda.synchronize()
+
+    def step(self, i, logits_dev, x_dev):
+        l = i % len(self.layers)
+        with self.torch.cuda.stream(self.stream):
+            self.lg[l].copy_(logits_dev, non_blocking=True)
+            self.x[l].copy_(x_dev, non_blocking=True)
+            self.graphs[l].replay()
+
+    def close(self):
+        for l in self.layers:
+            l.close()
+
+
+def run_graph(pqe, torch, device, host, T, L, logits_dev, xs_dev, warmup, K, ws):
+    gr = GraphRunner(pqe, torch, device, host, L, T)
+    gr.capture(logits_dev[:L], xs_dev[0])
+    for i in range(L, L + warmup):
+        gr.step(i, logits_dev[i], xs_dev[i % len(xs_dev)])
+    torch.cuda.synchronize()
+    barrier(ws)
+    stats0 = [l.device_stats() for l in gr.layers]
+    launches = sum(gr.nodes[(L + warmup + j) % L] for j in range(K))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(gr.stream)
+    for j in range(K):
+        i = L + warmup + j
+        gr.step(i, logits_dev[i], xs_dev[i % len(xs_dev)])
+    e1.record(gr.stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    ms = e0.elapsed_time(e1)
+    stats1 = [l.device_stats() for l in gr.layers]
+    d = {k: sum(b[k] - a[k] for a, b in zip(stats0, stats1)) for k in stats0[0]}
+    gr.close()
+    return ms, d, launches
 
 
 def run_timed(r: Runner, T, logits_dev, xs_dev, y, warmup, K, ws, want_ffn=True):
@@ -309,6 +401,58 @@ def run_reference(args, ws, rank):
     return 0
 
 
+def run_batched(pqe, torch, device, host, steps, ws):
+    """Module-batched prefill layer: T=16384 tokens in one step, per-expert
+    batches of ~512 rows (Zipf-skewed); |U| > CACHE_SLOTS, so every step stages
+    the needed non-resident experts into the working buffer. Reports whole
+    steps and the FFN alone (FP8 tensor path) against the FP8 peak."""
+    cfg3 = synth.CONFIGS[3]
+    E, H, I, k, S, T = cfg3.E, cfg3.H, cfg3.I, cfg3.k, cfg3.S, cfg3.T[0]
+    nbytes = [pqe.page_bytes(pqe.PQE_FMT_FP8, H, I)] * E
+    layer = pqe.PagedMoELayer(E, H, I, k, S, E, T, host, nbytes, device=device)
+    stream = torch.cuda.current_stream(device)
+    side = torch.cuda.Stream(device)
+    tr = synth.RoutingTrace(cfg3, T)
+    logits = [torch.from_numpy(tr.step(s)).to(device) for s in range(2)]
+    x = torch.from_numpy(synth.activations(cfg3, T, 0).view(np.int16)).to(device)
+    y = torch.zeros((T, H), dtype=torch.bfloat16, device=device)
+    evs = []
+    for _ in range(steps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        b.record(stream)
+        evs.append((a, b))
+    for i in range(2):  # warm-up
+        layer.step(x, y, T, logits=logits[i % 2], stream=stream, side_stream=side)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    misses = []
+    for i in range(steps):
+        layer.set_ffn_events(*evs[i])
+        info = layer.step(x, y, T, logits=logits[i % 2], stream=stream, side_stream=side)
+        misses.append(info.n_miss)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    layer.set_ffn_events(None, None)
+    ms = e0.elapsed_time(e1)
+    ffn = [a.elapsed_time(b) for a, b in evs]
+    flops = 6.0 * T * k * H * I
+    peak, kind = fp8_peak_tflops()
+    ffn_ms = float(np.mean(ffn))
+    tflops = flops / (ffn_ms / 1e3) / 1e12
+    layer.close()
+    return {"workload": "module-batched prefill layer (E=256, H=2048, I=512, top-8, T=16384, CACHE_SLOTS=32, "
+                        "working buffer)",
+            "tokens_per_s": T * steps / (ms / 1e3), "ms_per_step": ms / steps,
+            "mean_staged_experts": float(np.mean(misses)),
+            "ffn": {"ms": ffn_ms, "tflops": tflops, "peak_tflops": peak, "peak_kind": kind, "frac": tflops / peak,
+                    "bound": "tensor", "flops_per_step": flops}}
+
+
 # ---- main arm ------------------------------------------------------------------------------
 
 def main():
@@ -325,9 +469,15 @@ def main():
     pqe.load()
     T, L, K, W = args.T, args.layers, args.steps, max(3, args.warmup)
     host = expert_pages_host(pqe, torch, device)
+    graph_extra = L if args.pager != "host" else 0
+    if args.workload == "batched":
+        res = run_batched(pqe, torch, device, host, args.batched_steps, ws)
+        if rank == 0:
+            print(json.dumps({"batched": res}))
+        return 0
     r = Runner(pqe, torch, device, host, L, max(T, 64))
     xs_dev = [torch.from_numpy(synth.activations(CFG, T, s).view(np.int16)).to(device) for s in range(4)]
-    logits_np = make_traces(T, L, W + K)
+    logits_np = make_traces(T, L, W + K + graph_extra)
     logits_dev = [torch.from_numpy(l).to(device) for l in logits_np]
     y = torch.zeros((T, CFG.H), dtype=torch.bfloat16, device=device)
 
@@ -336,7 +486,23 @@ def main():
     ms, wall, infos, ffn_ms, launches = run_timed(r, T, logits_dev, xs_dev, y, W, K, ws)
     clk = clocks.stop()
     ms = max_over_ranks(ws, ms, device)
-    value = ws * T * K / (ms / 1e3)
+    host_value, host_ms = ws * T * K / (ms / 1e3), ms / K
+    value, pager_used, graph = host_value, "host", None
+    if args.pager != "host":
+        r.close()
+        clocks_g = Clocks(local)
+        clocks_g.start()
+        gms, gstats, glaunch = run_graph(pqe, torch, device, host, T, L, logits_dev, xs_dev, W, K, ws)
+        clk_g = clocks_g.stop()
+        gms = max_over_ranks(ws, gms, device)
+        gval = ws * T * K / (gms / 1e3)
+        graph = {"tokens_per_s": gval, "ms_per_step": gms / K, "gpu_launches": int(glaunch),
+                 "mean_routed_experts": gstats["routed"] / K, "mean_misses": gstats["misses"] / K,
+                 "working_buffer_steps": gstats["working_buffer_steps"],
+                 "h2d_gb_per_s": gstats["refill_bytes"] / (gms / 1e3) / 1e9, "clocks": clk_g}
+        if args.pager == "device" or gval > host_value:
+            value, pager_used, ms, launches, clk = gval, "device", gms, glaunch, clk_g
+        r = Runner(pqe, torch, device, host, L, max(T, 64))
 
     # roofline of the FFN call (w13 + SwiGLU, w2; HBM-bound weight stream)
     peak, peak_kind = peaks()
@@ -377,6 +543,11 @@ def main():
                                 "ffn_hbm_gbs": sum(b_s) / (sum(ffn_s) / 1e3) / 1e9 if sum(ffn_s) > 0 else None,
                                 "misses_per_step": float(np.mean([m for (_, m, _, _) in inf_s]))}
 
+    batched = None
+    if not args.no_batched:
+        r.close()
+        batched = run_batched(pqe, torch, device, host, args.batched_steps, ws)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         tok, secs, threads, steps = cpu_oracle_sample(host.numpy(), T, make_traces(T, 1, 16), budget_s=10.0)
@@ -395,6 +566,10 @@ def main():
                                    "CACHE_SLOTS=32 LRU per layer, Zipf(1.1) routing with 0.7 reuse, "
                                    "pinned-host refills)",
                        "T": T, "layers_round_robin": L,
+                       "pager": pager_used + (" (LRU on the GPU, each step a CUDA graph replay)"
+                                              if pager_used == "device" else " (LRU on the host, eager launches)"),
+                       "host_pager": {"tokens_per_s": host_value, "ms_per_step": host_ms},
+                       "device_pager_graph": graph,
                        "l2": f"inputs larger than L2: {L} layers x 32 slots x 3.16 MB of weights",
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                        "mean_routed_experts": float(np.mean(n_routed)), "mean_misses": float(np.mean(misses)),
@@ -411,6 +586,7 @@ def main():
                     "d2h_bytes_per_step": T * CFG.H * 2},
             "gpu_launches": int(launches),
             "clocks": clk,
+            "batched": batched,
         }
         print(json.dumps(line))
     r.close()

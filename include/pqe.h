@@ -292,6 +292,51 @@ PQE_API int page_table_update(pqe_lru *st, const int32_t *counts_host, int32_t *
 PQE_API int slot_fill(const pqe_pool *pool, int dest, const void *pinned_src, size_t bytes, void *stream,
               void *done_event);
 
+/* slot_fill_batch -- refill n entries of the pool with one kernel launch per
+ * 128 pages: page i is read from host_src[i] (pinned host memory, which
+ * kernels can address directly under unified addressing) and written to
+ * entry dest[i]; bytes[i] <= slot_stride, a multiple of 16, both addresses
+ * 16-byte aligned. dest, host_src, bytes are host arrays. Asynchronous on
+ * `stream`; done_event recorded after the last launch if not NULL. The SMs
+ * pull the pages over the host link, so one launch (per 128 pages) covers
+ * every miss of a step at the link's bandwidth. */
+PQE_API int slot_fill_batch(const pqe_pool *pool, int n, const int32_t *dest, const void *const *host_src,
+                            const size_t *bytes, void *stream, void *done_event);
+
+/* ------------------------------------------------------------------------
+ * GPU-resident pager: the same LRU rules with the state in device memory, so
+ * a step needs no host round trip (the counts, page table, miss list and
+ * refill stay on the GPU). State: pqe_lru_device_bytes(E, S) bytes of device
+ * memory, 16-byte aligned, owned by the caller; E <= 1024, S <= 1024.
+ * ------------------------------------------------------------------------ */
+PQE_API size_t pqe_lru_device_bytes(int E, int S);
+
+/* All slots empty, step 0, counters 0 (asynchronous on stream). */
+PQE_API int pqe_lru_device_init(void *state, int E, int S, void *stream);
+
+/* Forget expert e's resident copy (asynchronous on stream). */
+PQE_API int pqe_lru_device_invalidate(void *state, int E, int S, int expert, void *stream);
+
+/* Copy the state to the host (synchronises the stream): slot_expert [S],
+ * last_use [S], step, and running totals stats[4] = routed experts, misses,
+ * working-buffer steps, refill bytes. Any output may be NULL. */
+PQE_API int pqe_lru_device_state(const void *state, int E, int S, int32_t *slot_expert, int64_t *last_use,
+                                 int64_t *step, int64_t *stats, void *stream);
+
+/* page_table_update on the device, one CTA: counts [E] (device) ->
+ * page_table [E] (device) and miss (device int32 [3E + 3]): [0] number of
+ * misses, [1] working-buffer flag, [2, 2+E) missed experts in ascending id,
+ * [2+E, 2+2E) their destinations, [2+2E, 3+3E) prefix of their refill
+ * segments. page_bytes [E] (device): bytes of each expert's host page. */
+PQE_API int page_table_update_device(void *state, int E, int S, const int32_t *counts, const size_t *page_bytes,
+                                     int32_t *page_table, int32_t *miss, void *stream);
+
+/* Refill every page of a device miss list from pinned host memory:
+ * host_pages [E] (device array of the pinned page addresses), page_bytes [E]
+ * (device). One persistent kernel; no host involvement. */
+PQE_API int slot_fill_device(const pqe_pool *pool, const int32_t *miss, int E, const uint64_t *host_pages,
+                             const size_t *page_bytes, void *stream);
+
 /* ------------------------------------------------------------------------
  * Compressed host tier ([EP] 重みの圧縮: per row of each expert weight matrix
  * the FP8 exponent field is Huffman-coded, the rest kept raw; decoded on the
@@ -379,6 +424,8 @@ typedef struct pqe_layer_config {
     int32_t W;          /* working-buffer entries; pool->n_slots == S, pool->n_wb == W */
     int32_t max_T;      /* largest token count of a step */
     int32_t compressed; /* host pages are compressed pages (decoded after the copy) */
+    int32_t device_pager; /* 1: LRU state and refills on the GPU, no host synchronisation in a step
+                             (uncompressed host pages only) */
 } pqe_layer_config;
 
 typedef struct pqe_step_info {
@@ -435,11 +482,19 @@ PQE_API int pqe_layer_lru_state(const pqe_layer *L, int32_t *slot_expert, int64_
 
 /* One step on device inputs: x_dev bf16 [T, H]; either w_router_dev fp32
  * [E, H] (logits computed, written to logits_dev if not NULL) or logits_dev
- * fp32 [T, E] given; y_dev bf16 [T, H] out. Blocks the host once, until the
- * routing counts are known. side_stream NULL = refills on `stream`. A working-
- * buffer step with more misses than W returns PQE_ERR_CAPACITY. */
+ * fp32 [T, E] given; y_dev bf16 [T, H] out. With the host pager it blocks the
+ * host once, until the routing counts are known, and a working-buffer step
+ * with more misses than W returns PQE_ERR_CAPACITY; side_stream NULL = refills
+ * on `stream`. With the device pager nothing blocks, every launch is on
+ * `stream` (the step may be captured in a CUDA graph), W must be >= E, and
+ * *info is left zero (the totals are in pqe_layer_device_stats). */
 PQE_API int pqe_layer_step(pqe_layer *L, const void *x_dev, const float *w_router_dev, float *logits_dev,
                            int T, void *y_dev, void *stream, void *side_stream, pqe_step_info *info);
+
+/* Device-pager layers: the running totals (routed experts, misses,
+ * working-buffer steps, refill bytes) and the LRU state; synchronises. */
+PQE_API int pqe_layer_device_stats(pqe_layer *L, int64_t *stats, int32_t *slot_expert, int64_t *last_use,
+                                   int64_t *step, void *stream);
 
 /* The same step on host buffers (pinned for asynchronous copies): x_host bf16
  * [T, H] and logits_host fp32 [T, E] are copied in, y_host bf16 [T, H] is

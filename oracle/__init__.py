@@ -65,6 +65,7 @@ def _declare(L):
         "orc_lru_destroy": (None, [P]),
         "orc_lru_state": (None, [P, P, P, P]),
         "orc_lru_step": (C.c_int, [P, P, P, P, P, P]),
+        "orc_lru_invalidate": (None, [P, C.c_int]),
         "orc_moe_ffn": (None, [P, C.c_int, C.c_int, C.c_int, C.c_int, P, P, P, P, C.c_int, P]),
         "orc_num_threads": (C.c_int, []),
         "orc_set_num_threads": (None, [C.c_int]),
@@ -204,6 +205,9 @@ class LRU:
         n = np.zeros(1, np.int32)
         wb = lib().orc_lru_step(self._h, _p(counts), _p(table), _p(me), _p(md), _p(n))
         return table, me[: n[0]].copy(), md[: n[0]].copy(), bool(wb)
+
+    def invalidate(self, e: int):
+        lib().orc_lru_invalidate(self._h, int(e))
 
     def state(self):
         se = np.empty(self.S, np.int32)

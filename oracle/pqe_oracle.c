@@ -346,6 +346,18 @@ EXPORT void orc_lru_state(const orc_lru *st, int32_t *slot_expert, int64_t *last
     *step = st->step;
 }
 
+/* Forgetting an expert's resident copy (its page changed, e.g. a new bit
+ * width): its slot becomes empty, as at the start. */
+EXPORT void orc_lru_invalidate(orc_lru *st, int e)
+{
+    for (int s = 0; s < st->S; ++s) {
+        if (st->slot_expert[s] == e) {
+            st->slot_expert[s] = -1;
+            st->last_use[s] = -1;
+        }
+    }
+}
+
 static int lru_slot_of(const orc_lru *st, int e)
 {
     for (int s = 0; s < st->S; ++s)

@@ -50,7 +50,7 @@ class PqeError(RuntimeError):
 
 
 class pqe_layer_config(C.Structure):
-    _fields_ = [(n, C.c_int32) for n in ("E", "H", "I", "k", "S", "W", "max_T", "compressed")]
+    _fields_ = [(n, C.c_int32) for n in ("E", "H", "I", "k", "S", "W", "max_T", "compressed", "device_pager")]
 
 
 class pqe_step_info(C.Structure):
@@ -97,6 +97,7 @@ _SIGS = {
     "pqe_lru_invalidate": (I32, [P, I32]),
     "page_table_update": (I32, [P, P, P, P, P, P, P]),
     "slot_fill": (I32, [C.POINTER(pqe_pool), I32, P, SZ, P, P]),
+    "slot_fill_batch": (I32, [C.POINTER(pqe_pool), I32, P, P, P, P, P]),
     "pqe_huff_page_bound": (SZ, [I32, I32]),
     "pqe_huff_encode_page": (I32, [P, I32, I32, P, SZ, C.POINTER(C.c_size_t), P, P]),
     "pqe_huff_page_lengths": (I32, [P, P, P]),
@@ -106,6 +107,13 @@ _SIGS = {
     "pqe_importance_step": (I32, [P, P, P, I32, I32, I32, C.c_double, C.c_int64, I32, I32, P, P]),
     "pqe_rank_formats": (I32, [P, I32, I32, P]),
     "pqe_pool_slot_addr": (P, [C.POINTER(pqe_pool), I32]),
+    "pqe_lru_device_bytes": (SZ, [I32, I32]),
+    "pqe_lru_device_init": (I32, [P, I32, I32, P]),
+    "pqe_lru_device_invalidate": (I32, [P, I32, I32, I32, P]),
+    "pqe_lru_device_state": (I32, [P, I32, I32, P, P, P, P, P]),
+    "page_table_update_device": (I32, [P, I32, I32, P, P, P, P, P]),
+    "slot_fill_device": (I32, [C.POINTER(pqe_pool), P, I32, P, P, P]),
+    "pqe_layer_device_stats": (I32, [P, P, P, P, P, P]),
     "pqe_pack_fp8_page": (I32, [P, P, I32, I32, P, P]),
     "pqe_pack_mxfp4_page": (I32, [P, I32, I32, P, P]),
     "pqe_layer_scratch_bytes": (SZ, [P]),
@@ -321,6 +329,16 @@ def page_table_update(lru: LRU, counts_host, page_table_host=None):
     return lru.page_table_update(counts_host, page_table_host)
 
 
+def slot_fill_batch(pool: pqe_pool, dests, pinned_srcs, nbytes, stream=None, done_event=None):
+    """dests: entries; pinned_srcs: pinned tensors (or addresses); nbytes: bytes per page."""
+    n = len(dests)
+    d = (C.c_int32 * n)(*[int(x) for x in dests])
+    s = (C.c_void_p * n)(*[_ptr(x) for x in pinned_srcs])
+    b = (C.c_size_t * n)(*[int(x) for x in nbytes])
+    _check("slot_fill_batch", lib().slot_fill_batch(C.byref(pool), n, C.cast(d, C.c_void_p), C.cast(s, C.c_void_p),
+                                                    C.cast(b, C.c_void_p), _stream(stream), _event(done_event)))
+
+
 def slot_fill(pool: pqe_pool, dest: int, pinned_src, nbytes: int, stream=None, done_event=None):
     _check("slot_fill", lib().slot_fill(C.byref(pool), dest, _ptr(pinned_src), nbytes, _stream(stream),
                                         _event(done_event)))
@@ -400,8 +418,10 @@ class PagedMoELayer:
     """
 
     def __init__(self, E, H, I, k, S, W, max_T, host_pages, host_page_bytes, compressed=False, luts=None,
-                 expert_fmt=None, device="cuda", working_buffer: Optional[torch.Tensor] = None):
-        self.cfg = pqe_layer_config(E, H, I, k, S, W, max_T, int(bool(compressed)))
+                 expert_fmt=None, device="cuda", working_buffer: Optional[torch.Tensor] = None,
+                 device_pager=False):
+        self.cfg = pqe_layer_config(E, H, I, k, S, W, max_T, int(bool(compressed)), int(bool(device_pager)))
+        self.device_pager = bool(device_pager)
         self.E, self.H, self.I, self.k, self.S, self.W, self.max_T = E, H, I, k, S, W, max_T
         self.pool_mem = torch.zeros(max(S, 1) * slot_stride(H, I), dtype=torch.uint8, device=device)
         # the working buffer holds one step's pages; layers on one stream may share it
@@ -466,8 +486,21 @@ class PagedMoELayer:
         se = torch.empty(self.S, dtype=torch.int32)
         lu = torch.empty(self.S, dtype=torch.int64)
         st = torch.zeros(1, dtype=torch.int64)
-        _check("pqe_layer_lru_state", lib().pqe_layer_lru_state(self._h, _ptr(se), _ptr(lu), _ptr(st)))
+        if self.device_pager:
+            stats = torch.zeros(4, dtype=torch.int64)
+            _check("pqe_layer_device_stats", lib().pqe_layer_device_stats(self._h, _ptr(stats), _ptr(se), _ptr(lu),
+                                                                          _ptr(st), _stream(None)))
+        else:
+            _check("pqe_layer_lru_state", lib().pqe_layer_lru_state(self._h, _ptr(se), _ptr(lu), _ptr(st)))
         return se, lu, int(st.item())
+
+    def device_stats(self, stream=None) -> dict:
+        """Device-pager totals since creation (synchronises)."""
+        stats = torch.zeros(4, dtype=torch.int64)
+        _check("pqe_layer_device_stats", lib().pqe_layer_device_stats(self._h, _ptr(stats), None, None, None,
+                                                                      _stream(stream)))
+        r, m, w, b = stats.tolist()
+        return {"routed": r, "misses": m, "working_buffer_steps": w, "refill_bytes": b}
 
     def device_view(self, name: str, dtype, shape):
         """A torch view of one of the layer's device buffers (no copy)."""
@@ -484,3 +517,38 @@ class PagedMoELayer:
 def kernel_launches() -> int:
     """Kernels libpqe has launched in this process."""
     return int(lib().pqe_kernel_launches())
+
+
+# ---- GPU-resident pager -------------------------------------------------------------
+
+def pqe_lru_device_bytes(E: int, S: int) -> int:
+    return lib().pqe_lru_device_bytes(E, S)
+
+
+def pqe_lru_device_init(state, E, S, stream=None):
+    _check("pqe_lru_device_init", lib().pqe_lru_device_init(_ptr(state), E, S, _stream(stream)))
+
+
+def pqe_lru_device_invalidate(state, E, S, expert, stream=None):
+    _check("pqe_lru_device_invalidate", lib().pqe_lru_device_invalidate(_ptr(state), E, S, expert, _stream(stream)))
+
+
+def pqe_lru_device_state(state, E, S, stream=None):
+    se = torch.empty(max(S, 1), dtype=torch.int32)
+    lu = torch.empty(max(S, 1), dtype=torch.int64)
+    st = torch.zeros(1, dtype=torch.int64)
+    stats = torch.zeros(4, dtype=torch.int64)
+    _check("pqe_lru_device_state", lib().pqe_lru_device_state(_ptr(state), E, S, _ptr(se), _ptr(lu), _ptr(st),
+                                                              _ptr(stats), _stream(stream)))
+    return se[:S], lu[:S], int(st.item()), stats
+
+
+def page_table_update_device(state, E, S, counts, page_bytes, page_table, miss, stream=None):
+    _check("page_table_update_device", lib().page_table_update_device(_ptr(state), E, S, _ptr(counts),
+                                                                      _ptr(page_bytes), _ptr(page_table), _ptr(miss),
+                                                                      _stream(stream)))
+
+
+def slot_fill_device(pool: pqe_pool, miss, E, host_pages, page_bytes, stream=None):
+    _check("slot_fill_device", lib().slot_fill_device(C.byref(pool), _ptr(miss), E, _ptr(host_pages),
+                                                      _ptr(page_bytes), _stream(stream)))

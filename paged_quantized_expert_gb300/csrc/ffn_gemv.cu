@@ -68,6 +68,11 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(FfnArgs a, int tc_mi
     const int gpos = block_excl_scan(gemv ? 1 : 0, warp_tot, total);
     if (gemv) a.sched[1 + gpos] = e;
     if (threadIdx.x == 0) a.sched[0] = total;
+    // work weight of a CUDA-core expert: its weight stream (~2 rows' worth) plus its rows
+    int wtot;
+    const int wpos = block_excl_scan(gemv ? n + 2 : 0, warp_tot, wtot);
+    if (gemv) a.wpre[gpos] = wpos;
+    if (threadIdx.x == 0) a.wpre[total] = wtot;
     const int nt = tc ? (n + 127) / 128 : 0;
     const int tpos = block_excl_scan(nt, warp_tot, total);
     for (int i = 0; i < nt; ++i) {
@@ -78,7 +83,10 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(FfnArgs a, int tc_mi
         t.w = slot;
         reinterpret_cast<int4 *>(tiles)[tpos + i] = t;
     }
-    if (threadIdx.x == 0) *n_tiles = total;
+    if (threadIdx.x == 0) {
+        *n_tiles = total;
+        if (a.grid_bar) *a.grid_bar = 0u;
+    }
 }
 
 __device__ __forceinline__ bool page_ok(const FfnArgs &a, int e, int &slot, int &fmt) {
@@ -385,7 +393,7 @@ int launch_ffn_gemv(const FfnArgs &args, int max_active, cudaStream_t s) {
 
 // workspace carve-up shared by the size query and the call
 struct FfnWs {
-    size_t sched, tiles, n_tiles, h, xq, sx, hbf, hmax, hq, sh, total;
+    size_t sched, wpre, tiles, n_tiles, grid_bar, h, xq, sx, hbf, hmax, hq, sh, total;
     int max_tiles;
     bool tc;
 };
@@ -402,8 +410,10 @@ static FfnWs ffn_ws_layout(int T, int k, int E, int H, int I) {
         return at;
     };
     w.sched = take(sizeof(int32_t) * (E + 1));
+    w.wpre = take(sizeof(int32_t) * (E + 1));
     w.tiles = take(sizeof(int32_t) * 4 * (size_t)(w.max_tiles ? w.max_tiles : 1));
     w.n_tiles = take(sizeof(int32_t));
+    w.grid_bar = take(sizeof(uint32_t));
     w.h = take(A * I * sizeof(float));
     if (w.tc) {
         w.xq = take(A * H);
@@ -459,9 +469,11 @@ int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *of
     const FfnWs w = ffn_ws_layout(T, k, E, pool->H, pool->I);
     uint8_t *wsb = static_cast<uint8_t *>(ws);
     args.sched = reinterpret_cast<int32_t *>(wsb + w.sched);
+    args.wpre = reinterpret_cast<int32_t *>(wsb + w.wpre);
     args.h = reinterpret_cast<float *>(wsb + w.h);
     args.out_perm = static_cast<uint16_t *>(out_perm);
     args.status = status;
+    args.grid_bar = reinterpret_cast<uint32_t *>(wsb + w.grid_bar);
     const long A = (long)T * k;
     const int max_active = (int)(A < E ? A : E);
     cudaStream_t s = as_stream(stream);
@@ -469,7 +481,7 @@ int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *of
     int32_t *n_tiles = reinterpret_cast<int32_t *>(wsb + w.n_tiles);
     ffn_schedule_kernel<<<1, 1024, 0, s>>>(args, w.tc ? TC_MIN_ROWS : 0, tiles, n_tiles);
     PQE_LAUNCH_CHECK();
-    int rc = launch_ffn_gemv(args, max_active, s);
+    int rc = stream_shape_ok(pool->H, pool->I) ? launch_ffn_stream(args, s) : launch_ffn_gemv(args, max_active, s);
     if (rc != PQE_OK || !w.tc) return rc;
     TcBuffers b{};
     b.A = A;

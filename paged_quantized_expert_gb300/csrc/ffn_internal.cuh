@@ -18,9 +18,11 @@ struct FfnArgs {
     int n_wb;                    // working-buffer entries
     int k, E, H, I;
     int32_t *sched;              // [E+1]: count, then active expert ids
+    int32_t *wpre;               // [E+1]: prefix of per-expert work weights over sched (stream kernel)
     float *h;                    // fp32 [T*k, I]
     uint16_t *out_perm;          // bf16 [T*k, H]
     int32_t *status;
+    uint32_t *grid_bar;          // grid barrier counter of the stream kernel (zeroed by the schedule)
 };
 
 // address of page-table entry `slot` (valid: 0 <= slot < n_slots + n_wb)
@@ -42,10 +44,13 @@ struct TcBuffers {
     float *sh;           // [A]
 };
 
-// batches of at least this many rows (FP8 pages) take the tensor-core path
-constexpr int TC_MIN_ROWS = 64;
+// batches of at least this many rows (FP8 pages) take the tensor-core path;
+// below it the CUDA-core weight stream is bound by HBM, above it by its FMAs
+constexpr int TC_MIN_ROWS = 5;
 
 bool tc_shape_ok(int H, int I);
+bool stream_shape_ok(int H, int I);
+int launch_ffn_stream(const FfnArgs &args, cudaStream_t s);
 int launch_ffn_gemv(const FfnArgs &args, int max_active, cudaStream_t s);
 int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaStream_t s);
 

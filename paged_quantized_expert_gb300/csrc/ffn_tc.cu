@@ -19,10 +19,12 @@
 // Activations are quantised per row to E4M3 (scale amax / 448) by a gather
 // kernel that also lays the rows out in batch order for TMA.
 //
-// CTA = 6 warps: warp 0 issues TMA (one thread), warp 1 owns TMEM and issues
-// the MMAs (one thread), warps 2-5 read the accumulator from TMEM (each warp
-// its 32-lane quarter) and run the epilogue. 4-stage smem ring of
-// A [128 x 128 B] + B [256 x 128 B] tiles, 128-byte swizzle, K-major.
+// Persistent CTA (one per SM) over (M tile, N tile) work items, 6 warps:
+// warp 0 issues TMA (one thread), warp 1 owns TMEM and issues the MMAs (one
+// thread), warps 2-5 read the accumulator from TMEM (each warp its 32-lane
+// quarter) and run the epilogue. 4-stage smem ring of A [128 x 128 B] +
+// B [256 x 128 B] tiles, 128-byte swizzle, K-major; two TMEM accumulators so
+// the epilogue of one item overlaps the MMAs of the next.
 // Every mbarrier wait is bounded: on expiry the CTA sets PQE_STATUS_TIMEOUT,
 // drains what it issued (bounded), frees its TMEM and returns.
 #include <cuda.h>
@@ -40,12 +42,14 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int THREADS = 192;
-constexpr uint32_t TMEM_COLS = 256;
+constexpr int EPI_WARPS = 4;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr uint32_t ACC_COLS = 256;       // one fp32 accumulator of BM x BN
+constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;  // two: the epilogue of item i overlaps the MMAs of item i+1
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
-// smem: stages | full[S] empty[S] tmem_full (8 B each) | tmem base | column scales [256]
+// smem: stages | full[S] empty[S] tfull[2] tempty[2] | tmem base | column scales [BN]
 constexpr int SMEM_BAR_OFF = STAGES * STAGE_BYTES;
-constexpr int SMEM_TMEM_OFF = SMEM_BAR_OFF + 8 * (2 * STAGES + 1);
+constexpr int SMEM_TMEM_OFF = SMEM_BAR_OFF + 8 * (2 * STAGES + 4);
 constexpr int SMEM_SCALE_OFF = (SMEM_TMEM_OFF + 4 + 15) / 16 * 16;
 constexpr int SMEM_BYTES = SMEM_SCALE_OFF + 4 * BN + 1024;  // + alignment slack
 
@@ -61,6 +65,10 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_plain(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
@@ -142,6 +150,7 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 struct GemmArgs {
     const int32_t *tiles;    // [n][4]: expert, first row p0, valid rows, page-table entry
     const int32_t *n_tiles;  // device count
+    int n_nt;                // N tiles per M tile
     int n_slots;             // entries below this use the cache map, others the working-buffer map
     int K;                   // reduction length in bytes (H for GEMM1, I for GEMM2)
     int I;                   // GEMM1: up rows start at I
@@ -156,32 +165,57 @@ struct GemmArgs {
     int32_t *status;
 };
 
+struct Item {
+    int p0, nv, slot, nt, r0, r1;
+};
+
+__device__ __forceinline__ Item item_of(const GemmArgs &a, int i) {
+    const int4 t = reinterpret_cast<const int4 *>(a.tiles)[i / a.n_nt];
+    Item it;
+    it.p0 = t.y;
+    it.nv = t.z;
+    it.slot = t.w;
+    it.nt = i % a.n_nt;
+    // B rows of this N tile: two halves of 128 rows
+    it.r0 = a.swiglu ? it.nt * 128 : it.nt * 256;
+    it.r1 = a.swiglu ? a.I + it.nt * 128 : it.nt * 256 + 128;
+    return it;
+}
+
+// barrier among the epilogue warps only (named barrier 1)
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(EPI_WARPS * 32) : "memory"); }
+
+// the same barrier with an AND vote: every epilogue warp takes the same branch
+__device__ __forceinline__ bool epi_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, "
+        "q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(EPI_WARPS * 32)
+        : "memory");
+    return r != 0;
+}
+
+// Persistent: CTA b takes work items b, b + G, b + 2G, ... (item = M tile x N
+// tile; neighbouring CTAs share an M tile, so its activations stay in L2).
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB_cache,
                    const __grid_constant__ CUtensorMap tmB_wb, const GemmArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    if ((int)blockIdx.x >= *a.n_tiles) return;
+    const int n_items = *a.n_tiles * a.n_nt;
+    if ((int)blockIdx.x >= n_items) return;
     // 1024-byte alignment for the 128-byte swizzle atoms
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar_full = sbase + SMEM_BAR_OFF;
     const uint32_t bar_empty = bar_full + 8 * STAGES;
-    const uint32_t bar_tmem = bar_empty + 8 * STAGES;
+    const uint32_t bar_tfull = bar_empty + 8 * STAGES;
+    const uint32_t bar_tempty = bar_tfull + 16;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SMEM_TMEM_OFF);
     float *col_scale = reinterpret_cast<float *>(smem + SMEM_SCALE_OFF);
-
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int4 tile = reinterpret_cast<const int4 *>(a.tiles)[blockIdx.x];
-    const int p0 = tile.y, nv = tile.z, slot = tile.w;
-    const int nt = blockIdx.y;
-    // B rows of this N tile: two halves of 128 rows
-    const int r0 = a.swiglu ? nt * 128 : nt * 256;
-    const int r1 = a.swiglu ? a.I + nt * 128 : nt * 256 + 128;
-    const bool in_cache = slot < a.n_slots;
-    const CUtensorMap *tmB = in_cache ? &tmB_cache : &tmB_wb;
-    const int zc = in_cache ? slot : slot - a.n_slots;
-    const uint8_t *page = in_cache ? a.pool_base + (size_t)slot * a.slot_stride
-                                   : a.wb_base + (size_t)(slot - a.n_slots) * a.slot_stride;
+    const int G = gridDim.x;
     const int nk = a.K / BK;
 
     if (threadIdx.x == 0) {
@@ -189,10 +223,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
         }
-        mbar_init(bar_tmem, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_tfull + 8 * b, 1);
+            mbar_init(bar_tempty + 8 * b, EPI_WARPS * 32);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmB)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB_cache)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB_wb)) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -200,75 +238,101 @@ __global__ void __launch_bounds__(THREADS, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    if (warp >= 2) {
-        // weight row scales of the 256 output columns
-        const float *ws = reinterpret_cast<const float *>(page + a.wscale_off);
-        for (int c = threadIdx.x - 64; c < BN; c += 128) col_scale[c] = ws[c < 128 ? r0 + c : r1 + (c - 128)];
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
+        // ---------------- TMA producer ----------------
         if (lane == 0) {
-            int issued = 0;
+            int it = 0;
             bool ok = true;
-            for (int kb = 0; kb < nk && ok; ++kb) {
-                const int s = kb % STAGES;
-                const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-                if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u)) {
-                    ok = false;
-                    break;
+            for (int i = blockIdx.x; i < n_items && ok; i += G) {
+                const Item w = item_of(a, i);
+                const bool in_cache = w.slot < a.n_slots;
+                const CUtensorMap *tmB = in_cache ? &tmB_cache : &tmB_wb;
+                const int zc = in_cache ? w.slot : w.slot - a.n_slots;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    if (!mbar_wait(bar_empty + 8 * s, ((uint32_t)(it / STAGES) & 1u) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = sbase + s * STAGE_BYTES, sb = sa + A_BYTES;
+                    mbar_expect_tx(bar_full + 8 * s, STAGE_BYTES);
+                    tma_load_2d(sa, &tmA, kb * BK, w.p0, bar_full + 8 * s);
+                    tma_load_3d(sb, tmB, kb * BK, w.r0, zc, bar_full + 8 * s);
+                    tma_load_3d(sb + B_BYTES / 2, tmB, kb * BK, w.r1, zc, bar_full + 8 * s);
                 }
-                const uint32_t sa = sbase + s * STAGE_BYTES, sb = sa + A_BYTES;
-                mbar_expect_tx(bar_full + 8 * s, STAGE_BYTES);
-                tma_load_2d(sa, &tmA, kb * BK, p0, bar_full + 8 * s);
-                tma_load_3d(sb, tmB, kb * BK, r0, zc, bar_full + 8 * s);
-                tma_load_3d(sb + B_BYTES / 2, tmB, kb * BK, r1, zc, bar_full + 8 * s);
-                ++issued;
             }
             if (!ok) atomicOr(a.status, PQE_STATUS_TIMEOUT);
-            // drain: every stage issued has landed before the CTA may exit
-            for (int kb = (issued > STAGES ? issued - STAGES : 0); kb < issued; ++kb)
-                mbar_wait(bar_full + 8 * (kb % STAGES), (uint32_t)(kb / STAGES) & 1u);
+            // drain: the stages issued last have landed before the CTA may exit
+            for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+                mbar_wait(bar_full + 8 * (j % STAGES), (uint32_t)(j / STAGES) & 1u);
         }
     } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
         if (lane == 0) {
+            int it = 0, local = 0;
             bool ok = true;
-            for (int kb = 0; kb < nk; ++kb) {
-                const int s = kb % STAGES;
-                const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
-                if (!mbar_wait(bar_full + 8 * s, ph)) {
+            for (int i = blockIdx.x; i < n_items && ok; i += G, ++local) {
+                const int b = local & 1;
+                if (!mbar_wait(bar_tempty + 8 * b, ((uint32_t)(local >> 1) & 1u) ^ 1u)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sa = sbase + s * STAGE_BYTES, sb = sa + A_BYTES;
+                const uint32_t d = tmem + (uint32_t)b * ACC_COLS;
+                for (int kb = 0; kb < nk; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    if (!mbar_wait(bar_full + 8 * s, (uint32_t)(it / STAGES) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = sbase + s * STAGE_BYTES, sb = sa + A_BYTES;
 #pragma unroll
-                for (int k = 0; k < BK / 32; ++k)
-                    umma_f8(tmem, sw128_desc(sa + 32 * k), sw128_desc(sb + 32 * k), (kb | k) != 0);
-                umma_commit(bar_empty + 8 * s);
+                    for (int k = 0; k < BK / 32; ++k)
+                        umma_f8(d, sw128_desc(sa + 32 * k), sw128_desc(sb + 32 * k), (kb | k) != 0);
+                    umma_commit(bar_empty + 8 * s);
+                }
+                umma_commit(bar_tfull + 8 * b);
             }
             if (!ok) atomicOr(a.status, PQE_STATUS_TIMEOUT);
-            umma_commit(bar_tmem);
+            // every issued MMA has finished before TMEM is released
+            if (local > 0) mbar_wait(bar_tfull + 8 * ((local - 1) & 1), (uint32_t)((local - 1) >> 1) & 1u);
         }
     } else {
-        // epilogue: this warp's TMEM lane quarter
-        const int q = warp & 3;
+        // ---------------- epilogue: TMEM -> registers -> global ----------------
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
         const int m = 32 * q + lane;
-        const int p = p0 + m;
-        const bool valid = m < nv;
-        const bool ok = mbar_wait(bar_tmem, 0);
-        tc_fence_after();
-        if (!ok) {
-            if (lane == 0) atomicOr(a.status, PQE_STATUS_TIMEOUT);
-        } else {
-            const uint32_t trow = tmem + ((uint32_t)(32 * q) << 16);
+        const int et = threadIdx.x - 64;
+        int local = 0;
+        bool ok = true;
+        for (int i = blockIdx.x; i < n_items && ok; i += G, ++local) {
+            const Item w = item_of(a, i);
+            const int b = local & 1;
+            const uint8_t *page = w.slot < a.n_slots ? a.pool_base + (size_t)w.slot * a.slot_stride
+                                                     : a.wb_base + (size_t)(w.slot - a.n_slots) * a.slot_stride;
+            // weight row scales of the 256 output columns
+            epi_sync();
+            const float *ws = reinterpret_cast<const float *>(page + a.wscale_off);
+            for (int c = et; c < BN; c += EPI_WARPS * 32) col_scale[c] = ws[c < 128 ? w.r0 + c : w.r1 + (c - 128)];
+            epi_sync();
+            if (!epi_all(mbar_wait(bar_tfull + 8 * b, (uint32_t)(local >> 1) & 1u))) {
+                ok = false;
+                if (et == 0) atomicOr(a.status, PQE_STATUS_TIMEOUT);
+                break;
+            }
+            tc_fence_after();
+            const int p = w.p0 + m;
+            const bool valid = m < w.nv;
+            const uint32_t trow = tmem + (uint32_t)b * ACC_COLS + ((uint32_t)(32 * q) << 16);
             const float rs = valid ? a.row_scale[p] : 0.0f;
             if (a.swiglu) {
                 float amax = 0.0f;
-                uint16_t *dst = a.out + (size_t)p * a.out_cols + nt * 128;
+                uint16_t *dst = a.out + (size_t)p * a.out_cols + w.nt * 128;
                 for (int c0 = 0; c0 < 128; c0 += 32) {
                     uint32_t g[32], u[32];
                     tmem_ld32(trow + c0, g);
@@ -276,17 +340,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tmem_ld_wait();
                     uint32_t packed[16];
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
+                    for (int j = 0; j < 32; j += 2) {
                         float h2[2];
 #pragma unroll
                         for (int t = 0; t < 2; ++t) {
-                            const float gv = __uint_as_float(g[i + t]) * rs * col_scale[c0 + i + t];
-                            const float uv = __uint_as_float(u[i + t]) * rs * col_scale[128 + c0 + i + t];
+                            const float gv = __uint_as_float(g[j + t]) * rs * col_scale[c0 + j + t];
+                            const float uv = __uint_as_float(u[j + t]) * rs * col_scale[128 + c0 + j + t];
                             h2[t] = silu(gv) * uv;
                         }
                         const uint16_t b0 = f32_to_bf16_rn(h2[0]), b1 = f32_to_bf16_rn(h2[1]);
                         amax = fmaxf(amax, fmaxf(fabsf(bf16_to_f32(b0)), fabsf(bf16_to_f32(b1))));
-                        packed[i / 2] = (uint32_t)b0 | ((uint32_t)b1 << 16);
+                        packed[j / 2] = (uint32_t)b0 | ((uint32_t)b1 << 16);
                     }
                     if (valid) {
                         uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
@@ -297,17 +361,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 if (valid) atomicMax(a.hmax + p, __float_as_uint(amax));
             } else {
-                uint16_t *dst = a.out + (size_t)p * a.out_cols + nt * 256;
+                uint16_t *dst = a.out + (size_t)p * a.out_cols + w.nt * 256;
                 for (int c0 = 0; c0 < 256; c0 += 32) {
                     uint32_t d[32];
                     tmem_ld32(trow + c0, d);
                     tmem_ld_wait();
                     uint32_t packed[16];
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const float v0 = __uint_as_float(d[i]) * rs * col_scale[c0 + i];
-                        const float v1 = __uint_as_float(d[i + 1]) * rs * col_scale[c0 + i + 1];
-                        packed[i / 2] = (uint32_t)f32_to_bf16_rn(v0) | ((uint32_t)f32_to_bf16_rn(v1) << 16);
+                    for (int j = 0; j < 32; j += 2) {
+                        const float v0 = __uint_as_float(d[j]) * rs * col_scale[c0 + j];
+                        const float v1 = __uint_as_float(d[j + 1]) * rs * col_scale[c0 + j + 1];
+                        packed[j / 2] = (uint32_t)f32_to_bf16_rn(v0) | ((uint32_t)f32_to_bf16_rn(v1) << 16);
                     }
                     if (valid) {
                         uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
@@ -317,6 +381,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             }
+            // this accumulator may be overwritten by the MMAs of item i + 2G
+            tc_fence_before();
+            mbar_arrive_plain(bar_tempty + 8 * b);
         }
     }
     tc_fence_before();
@@ -479,16 +546,24 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
               map_3d(&m2w, wb + L.w2, nw, (uint64_t)H, I, args.slot_stride);
     if (!ok) return PQE_ERR_UNSUPPORTED;
     static bool attr_set = false;
+    static int sms = 0;
     if (!attr_set) {
         PQE_CUDA_TRY(cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
+        int dev = 0;
+        PQE_CUDA_TRY(cudaGetDevice(&dev));
+        PQE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
         attr_set = true;
     }
+    // persistent grids: one CTA per SM, at most one per work item
+    const int items1 = max_tiles * (I / 128), items2 = max_tiles * (H / 256);
+    const int grid1 = items1 < sms ? items1 : sms, grid2 = items2 < sms ? items2 : sms;
     tc_gather_quant_kernel<<<max_tiles, 256, 0, s>>>(args.x, args.perm_src, args.k, H, b.tiles, b.n_tiles, b.xq,
                                                      b.sx, b.hmax);
     PQE_LAUNCH_CHECK();
     GemmArgs g1{};
     g1.tiles = b.tiles;
     g1.n_tiles = b.n_tiles;
+    g1.n_nt = I / 128;
     g1.n_slots = args.n_slots;
     g1.K = H;
     g1.I = I;
@@ -502,11 +577,12 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     g1.out = b.h;
     g1.hmax = b.hmax;
     g1.status = args.status;
-    tc_gemm_kernel<<<dim3(max_tiles, I / 128), THREADS, SMEM_BYTES, s>>>(mx, m13c, m13w, g1);
+    tc_gemm_kernel<<<grid1, THREADS, SMEM_BYTES, s>>>(mx, m13c, m13w, g1);
     PQE_LAUNCH_CHECK();
     tc_hquant_kernel<<<max_tiles, 256, 0, s>>>(b.h, I, b.tiles, b.n_tiles, b.hmax, b.hq, b.sh);
     PQE_LAUNCH_CHECK();
     GemmArgs g2 = g1;
+    g2.n_nt = H / 256;
     g2.K = I;
     g2.out_cols = H;
     g2.swiglu = 0;
@@ -514,7 +590,7 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     g2.wscale_off = L.s2;
     g2.out = args.out_perm;
     g2.hmax = nullptr;
-    tc_gemm_kernel<<<dim3(max_tiles, H / 256), THREADS, SMEM_BYTES, s>>>(mh, m2c, m2w, g2);
+    tc_gemm_kernel<<<grid2, THREADS, SMEM_BYTES, s>>>(mh, m2c, m2w, g2);
     PQE_LAUNCH_CHECK();
     return PQE_OK;
 }

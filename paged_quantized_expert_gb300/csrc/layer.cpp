@@ -27,7 +27,7 @@ size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct ScratchMap {
     size_t status, topk_ids, topk_w, counts, offsets, perm_src, inv, page_table, perm_ws, ffn_ws, out_perm, x_in,
-        logits_in, y_out, staging, total;
+        logits_in, y_out, staging, lru, miss, host_pages, page_bytes, total;
     size_t perm_ws_bytes, ffn_ws_bytes, staging_bytes;
 };
 
@@ -58,13 +58,23 @@ ScratchMap scratch_map(const pqe_layer_config &c) {
     m.y_out = take(sizeof(uint16_t) * (size_t)c.max_T * c.H);
     m.staging_bytes = c.compressed ? pqe_huff_page_bound(c.H, c.I) : 0;
     m.staging = take(m.staging_bytes);
+    if (c.device_pager) {
+        m.lru = take(pqe_lru_device_bytes(c.E, c.S));
+        m.miss = take(sizeof(int32_t) * (3 * (size_t)c.E + 3));
+        m.host_pages = take(sizeof(uint64_t) * c.E);
+        m.page_bytes = take(sizeof(size_t) * c.E);
+    }
     m.total = off;
     return m;
 }
 
 bool config_ok(const pqe_layer_config *c) {
-    return c && c->E >= 1 && c->E <= 1024 && c->k >= 1 && c->k <= 32 && c->k <= c->E && c->S >= 0 && c->W >= 0 &&
-           c->max_T >= 1 && (size_t)c->max_T * c->k < (1u << 30) && pqe_page_bytes(PQE_FMT_FP8, c->H, c->I) > 0;
+    if (!c || c->E < 1 || c->E > 1024 || c->k < 1 || c->k > 32 || c->k > c->E || c->S < 0 || c->W < 0 ||
+        c->max_T < 1 || (size_t)c->max_T * c->k >= (1u << 30) || pqe_page_bytes(PQE_FMT_FP8, c->H, c->I) == 0)
+        return false;
+    // the device pager: uncompressed pages, at most 1024 slots, a working buffer for any step
+    if (c->device_pager && (c->compressed || c->S > 1024 || c->W < c->E)) return false;
+    return true;
 }
 
 }  // namespace
@@ -82,6 +92,8 @@ struct pqe_layer {
     int32_t *pinned = nullptr;  // counts [E], page table [E], miss expert [E], miss dest [E]
     cudaEvent_t ev_counts = nullptr, ev_fill = nullptr;
     cudaEvent_t ev_ffn_begin = nullptr, ev_ffn_end = nullptr;  // caller's, optional
+    std::vector<const void *> fill_src;  // [E] scratch for slot_fill_batch
+    std::vector<size_t> fill_bytes;
 
     template <class T>
     T *at(size_t off) const {
@@ -109,6 +121,8 @@ pqe_layer *pqe_layer_create(const pqe_layer_config *cfg, const pqe_pool *pool, c
     if (scratch_bytes < m.total) return nullptr;
     for (int e = 0; e < cfg->E; ++e) {
         if (!host_pages[e] || host_page_bytes[e] == 0) return nullptr;
+        if (!cfg->compressed && (reinterpret_cast<uintptr_t>(host_pages[e]) % 16 || host_page_bytes[e] % 16))
+            return nullptr;
         if (!cfg->compressed && host_page_bytes[e] > pool->slot_stride) return nullptr;
         if (cfg->compressed && host_page_bytes[e] > m.staging_bytes) return nullptr;
     }
@@ -118,6 +132,8 @@ pqe_layer *pqe_layer_create(const pqe_layer_config *cfg, const pqe_pool *pool, c
     L->pool = *pool;
     L->host_pages.assign(host_pages, host_pages + cfg->E);
     L->host_bytes.assign(host_page_bytes, host_page_bytes + cfg->E);
+    L->fill_src.assign(cfg->E, nullptr);
+    L->fill_bytes.assign(cfg->E, 0);
     L->luts = luts_dev;
     L->expert_fmt = expert_fmt_dev;
     L->scratch = static_cast<uint8_t *>(scratch_dev);
@@ -136,6 +152,19 @@ pqe_layer *pqe_layer_create(const pqe_layer_config *cfg, const pqe_pool *pool, c
         pqe_layer_destroy(L);
         return nullptr;
     }
+    if (cfg->device_pager) {
+        std::vector<uint64_t> ptrs(cfg->E);
+        for (int e = 0; e < cfg->E; ++e) ptrs[e] = reinterpret_cast<uint64_t>(host_pages[e]);
+        if (cudaMemcpy(L->at<void>(m.host_pages), ptrs.data(), sizeof(uint64_t) * cfg->E, cudaMemcpyHostToDevice) !=
+                cudaSuccess ||
+            cudaMemcpy(L->at<void>(m.page_bytes), host_page_bytes, sizeof(size_t) * cfg->E,
+                       cudaMemcpyHostToDevice) != cudaSuccess ||
+            pqe_lru_device_init(L->at<void>(m.lru), cfg->E, cfg->S, nullptr) != PQE_OK ||
+            cudaDeviceSynchronize() != cudaSuccess) {
+            pqe_layer_destroy(L);
+            return nullptr;
+        }
+    }
     return L;
 }
 
@@ -150,11 +179,38 @@ void pqe_layer_destroy(pqe_layer *L) {
 
 int pqe_layer_set_host_page(pqe_layer *L, int expert, const void *pinned_page, size_t bytes) {
     if (!L || expert < 0 || expert >= L->cfg.E || !pinned_page || bytes == 0) return PQE_ERR_INVALID_ARG;
-    if (!L->cfg.compressed && bytes > L->pool.slot_stride) return PQE_ERR_INVALID_ARG;
+    if (!L->cfg.compressed && (bytes > L->pool.slot_stride || bytes % 16 ||
+                               reinterpret_cast<uintptr_t>(pinned_page) % 16))
+        return PQE_ERR_INVALID_ARG;
     if (L->cfg.compressed && bytes > L->map.staging_bytes) return PQE_ERR_INVALID_ARG;
     L->host_pages[expert] = pinned_page;
     L->host_bytes[expert] = bytes;
+    if (L->cfg.device_pager) {
+        const uint64_t ptr = reinterpret_cast<uint64_t>(pinned_page);
+        cudaError_t ce = cudaMemcpy(L->at<uint64_t>(L->map.host_pages) + expert, &ptr, sizeof(ptr),
+                                    cudaMemcpyHostToDevice);
+        if (ce == cudaSuccess)
+            ce = cudaMemcpy(L->at<size_t>(L->map.page_bytes) + expert, &bytes, sizeof(bytes), cudaMemcpyHostToDevice);
+        if (ce != cudaSuccess) {
+            pqe::set_last_cuda_error(ce);
+            return PQE_ERR_CUDA;
+        }
+        int rc = pqe_lru_device_invalidate(L->at<void>(L->map.lru), L->cfg.E, L->cfg.S, expert, nullptr);
+        if (rc) return rc;
+        ce = cudaDeviceSynchronize();
+        if (ce != cudaSuccess) {
+            pqe::set_last_cuda_error(ce);
+            return PQE_ERR_CUDA;
+        }
+    }
     return pqe_lru_invalidate(L->lru, expert);
+}
+
+int pqe_layer_device_stats(pqe_layer *L, int64_t *stats, int32_t *slot_expert, int64_t *last_use, int64_t *step,
+                           void *stream) {
+    if (!L || !L->cfg.device_pager) return PQE_ERR_INVALID_ARG;
+    return pqe_lru_device_state(L->at<void>(L->map.lru), L->cfg.E, L->cfg.S, slot_expert, last_use, step, stats,
+                                stream);
 }
 
 int pqe_layer_buffers(pqe_layer *L, pqe_layer_buffers_t *out) {
@@ -213,6 +269,24 @@ int pqe_layer_step(pqe_layer *L, const void *x_dev, const float *w_router_dev, f
     rc = moe_permute(ids, T, c.k, c.E, counts, offsets, perm_src, inv, L->at<void>(m.perm_ws), m.perm_ws_bytes,
                      status, stream);
     if (rc) return rc;
+    if (c.device_pager) {
+        // page table, misses and refills stay on the device: nothing blocks the host
+        int32_t *miss = L->at<int32_t>(m.miss);
+        const size_t *pbytes = L->at<size_t>(m.page_bytes);
+        rc = page_table_update_device(L->at<void>(m.lru), c.E, c.S, counts, pbytes, page_table, miss, stream);
+        if (rc) return rc;
+        rc = slot_fill_device(&L->pool, miss, c.E, L->at<uint64_t>(m.host_pages), pbytes, stream);
+        if (rc) return rc;
+        if (L->ev_ffn_begin && (rc = (cudaEventRecord(L->ev_ffn_begin, s) == cudaSuccess ? 0 : PQE_ERR_CUDA))) return rc;
+        rc = moe_paged_ffn(x_dev, perm_src, offsets, page_table, L->expert_fmt, &L->pool, T, c.k, c.E, out_perm,
+                           L->at<void>(m.ffn_ws), m.ffn_ws_bytes, status, stream);
+        if (rc) return rc;
+        if (L->ev_ffn_end && (rc = (cudaEventRecord(L->ev_ffn_end, s) == cudaSuccess ? 0 : PQE_ERR_CUDA))) return rc;
+        rc = moe_combine(out_perm, inv, gates, T, c.k, c.H, y_dev, stream);
+        if (rc) return rc;
+        if (info) *info = local;
+        return PQE_OK;
+    }
     int32_t *counts_h = L->pinned, *pt_h = L->pinned + c.E, *miss_e = L->pinned + 2 * c.E,
             *miss_d = L->pinned + 3 * c.E;
     cudaError_t ce = cudaMemcpyAsync(counts_h, counts, sizeof(int32_t) * c.E, cudaMemcpyDeviceToHost, s);
@@ -230,18 +304,25 @@ int pqe_layer_step(pqe_layer *L, const void *x_dev, const float *w_router_dev, f
     local.working_buffer = wb;
     for (int i = 0; i < nm; ++i)
         if (miss_d[i] >= L->pool.n_slots + L->pool.n_wb) return PQE_ERR_CAPACITY;
-    for (int i = 0; i < nm; ++i) {
-        const int e = miss_e[i];
-        if (c.compressed) {
+    if (c.compressed) {
+        for (int i = 0; i < nm; ++i) {
+            const int e = miss_e[i];
             const uint8_t *l13 = L->luts + (size_t)e * 2 * PQE_HUFF_LUT_BYTES;
             rc = slot_fill_compressed(&L->pool, miss_d[i], L->host_pages[e], L->host_bytes[e],
                                       L->at<void>(m.staging), m.staging_bytes, l13, l13 + PQE_HUFF_LUT_BYTES, status,
                                       side, nullptr);
-        } else {
-            rc = slot_fill(&L->pool, miss_d[i], L->host_pages[e], L->host_bytes[e], side, nullptr);
+            if (rc) return rc;
+            local.h2d_bytes += (int64_t)L->host_bytes[e];
         }
+    } else if (nm > 0) {
+        // every miss of the step in one kernel launch over the host link
+        for (int i = 0; i < nm; ++i) {
+            L->fill_src[i] = L->host_pages[miss_e[i]];
+            L->fill_bytes[i] = L->host_bytes[miss_e[i]];
+            local.h2d_bytes += (int64_t)L->host_bytes[miss_e[i]];
+        }
+        rc = slot_fill_batch(&L->pool, nm, miss_d, L->fill_src.data(), L->fill_bytes.data(), side, nullptr);
         if (rc) return rc;
-        local.h2d_bytes += (int64_t)L->host_bytes[e];
     }
     if (nm > 0 && side != s) {
         ce = cudaEventRecord(L->ev_fill, side);

@@ -22,7 +22,7 @@ TOL_L2_GEMV = 5e-3
 # pages) rounds x and h per row to E4M3 (about 2-3% RMS each); its relative L2
 # error per token stays below 0.1, which a dropped expert term (~1/k) breaks.
 TOL_L2_TC = 0.1
-TC_MIN_ROWS = 64
+TC_MIN_ROWS = 5
 
 
 def l2_bounds(ids: np.ndarray, tokens, E: int, fp4=(), H: int = 0, I: int = 0) -> np.ndarray:

@@ -183,7 +183,7 @@ def test_slot_indirection_and_bad_page(cuda_lib, orc):
     assert np.all(op[rows3] == 0) and np.any(op[np.arange(offsets[0], offsets[1])] != 0)
 
 
-# ---- tensor-core path (batches of >= 64 rows on FP8 pages) -------------------------------
+# ---- tensor-core path (batches of >= TC_MIN_ROWS rows on FP8 pages) ----------------------
 # the per-token L2 bound follows the path (helpers.l2_bounds)
 
 
@@ -199,7 +199,7 @@ def test_tensor_core_path_small(cuda_lib, orc, E, H, I, k, T):
     ids, gates = orc.topk_gates(logits, k)
     assert np.array_equal(res["ids"], ids) and res["status"] == 0
     counts = np.bincount(ids.reshape(-1), minlength=E)
-    assert counts.max() >= 64          # at least one expert on the tensor-core path
+    assert counts.max() >= helpers.TC_MIN_ROWS  # at least one expert on the tensor-core path
     check_tokens(orc, pages, cfg, x, ids, gates, res, np.arange(T, dtype=np.int32))
 
 
@@ -217,7 +217,7 @@ def test_mixed_paths_one_call(cuda_lib, orc):
     res = run_layer(pqe, cfg, T, x, logits_np=logits, fmt_dev=pages.fmt_dev, pool=pages.pool)
     ids, gates = orc.topk_gates(logits, k)
     counts = np.bincount(ids.reshape(-1), minlength=E)
-    assert counts[0] >= 64 and counts[5] >= 64 and counts.min() < 64
+    assert counts[0] >= helpers.TC_MIN_ROWS and counts[5] >= helpers.TC_MIN_ROWS
     assert res["status"] == 0
     check_tokens(orc, pages, cfg, x, ids, gates, res, np.arange(T, dtype=np.int32))
 
@@ -235,3 +235,18 @@ def test_full_size_batched(cuda_lib, orc, cid, T, n_check):
     res = run_layer(pqe, cfg, T, x, logits_np=logits, fmt_dev=pages.fmt_dev, pool=pages.pool)
     assert np.array_equal(res["ids"], ids) and res["status"] == 0
     check_tokens(orc, pages, cfg, x, ids, gates, res, tokens)
+
+
+def test_wide_hidden_fallback_path(cuda_lib, orc):
+    # H = 8192: 8 gate/up row pairs (128 KiB) do not fit two stages of the
+    # streaming kernel's ring, so the grid-stride CUDA-core kernels run
+    pqe = cuda_lib
+    E, H, I, k, T = 2, 8192, 64, 2, 5
+    cfg = synth.small_config(E=E, H=H, I=I, k=k, T=T, cid=99)
+    pages = Pages(pqe, orc, cfg, needed=set(range(E)), fp4={1})
+    x = synth.activations(cfg, T)
+    logits = np.random.default_rng(3).standard_normal((T, E)).astype(np.float32)
+    res = run_layer(pqe, cfg, T, x, logits_np=logits, fmt_dev=pages.fmt_dev, pool=pages.pool)
+    ids, gates = orc.topk_gates(logits, k)
+    assert res["status"] == 0
+    check_tokens(orc, pages, cfg, x, ids, gates, res, np.arange(T, dtype=np.int32))

@@ -24,7 +24,7 @@ def _host_tier(pqe, pages: Pages):
     return host, nbytes
 
 
-def _run_trace(pqe, orc, cfg, T, steps, S, W, check_every, n_check, side=True, host_api=False):
+def _run_trace(pqe, orc, cfg, T, steps, S, W, check_every, n_check, side=True, host_api=False, device_pager=False):
     # experts the checked tokens of the checked steps use get oracle weights
     tr = synth.RoutingTrace(cfg, T)
     logits_all = [tr.step(s) for s in range(steps)]
@@ -37,7 +37,8 @@ def _run_trace(pqe, orc, cfg, T, steps, S, W, check_every, n_check, side=True, h
         needed |= set(ids[tok].reshape(-1).tolist())
     pages = Pages(pqe, orc, cfg, needed=needed, seed=7)
     host, nbytes = _host_tier(pqe, pages)
-    layer = pqe.PagedMoELayer(cfg.E, cfg.H, cfg.I, cfg.k, S, W, T, host, nbytes, expert_fmt=pages.fmt_dev)
+    layer = pqe.PagedMoELayer(cfg.E, cfg.H, cfg.I, cfg.k, S, W, T, host, nbytes, expert_fmt=pages.fmt_dev,
+                              device_pager=device_pager)
     ref_lru = orc.LRU(cfg.E, S)
     stream = torch.cuda.current_stream()
     side_stream = torch.cuda.Stream() if side else None
@@ -63,7 +64,8 @@ def _run_trace(pqe, orc, cfg, T, steps, S, W, check_every, n_check, side=True, h
         se, lu, st = layer.lru_state()
         se2, lu2, st2 = ref_lru.state()
         assert np.array_equal(se.numpy(), se2) and np.array_equal(lu.numpy(), lu2) and st == st2
-        assert info.n_miss == len(me) and info.working_buffer == int(wb)
+        if not device_pager:
+            assert info.n_miss == len(me) and info.working_buffer == int(wb)
         n_wb += int(wb)
         torch.cuda.synchronize()
         if s in checks:
@@ -163,4 +165,199 @@ def test_layer_capacity_error(cuda_lib, orc):
         layer.step(x, y, 4, logits=torch.from_numpy(logits).to(DEV))
     assert ei.value.code == pqe.PQE_ERR_CAPACITY
     torch.cuda.synchronize()
+    layer.close()
+
+
+def test_layer_device_pager_trace(cuda_lib, orc):
+    # LRU state, misses and refills on the GPU: same slot states as the oracle
+    cfg = synth.CONFIGS[2]
+    _run_trace(cuda_lib, orc, cfg, T=8, steps=30, S=cfg.S, W=cfg.E, check_every=7, n_check=3, device_pager=True)
+
+
+def test_layer_device_pager_working_buffer(cuda_lib, orc):
+    cfg = synth.CONFIGS[2]
+    _run_trace(cuda_lib, orc, cfg, T=64, steps=5, S=cfg.S, W=cfg.E, check_every=4, n_check=2, device_pager=True)
+
+
+def test_layer_device_pager_graph_replay(cuda_lib, orc):
+    # with the device pager a whole step has no host synchronisation: capture it
+    # once in a CUDA graph and replay it on new inputs copied into its buffers
+    pqe = cuda_lib
+    cfg = synth.small_config(E=16, H=256, I=128, k=2, T=8, S=4, cid=80, reuse_p=0.5, zipf_s=1.1,
+                             router_gemm=False, steps=8)
+    T = 8
+    pages = Pages(pqe, orc, cfg, needed=set(range(cfg.E)), seed=11)
+    host, nbytes = _host_tier(pqe, pages)
+    layer = pqe.PagedMoELayer(cfg.E, cfg.H, cfg.I, cfg.k, cfg.S, cfg.E, T, host, nbytes, expert_fmt=pages.fmt_dev,
+                              device_pager=True)
+    tr = synth.RoutingTrace(cfg, T)
+    logits_all = [tr.step(s) for s in range(8)]
+    x_buf = torch.zeros((T, cfg.H), dtype=torch.int16, device=DEV)
+    lg_buf = torch.zeros((T, cfg.E), dtype=torch.float32, device=DEV)
+    y = torch.zeros((T, cfg.H), dtype=torch.bfloat16, device=DEV)
+    # step 0 eagerly (also warms up the launch paths), then capture step 1
+    x_buf.copy_(torch.from_numpy(synth.activations(cfg, T, 0).view(np.int16)))
+    lg_buf.copy_(torch.from_numpy(logits_all[0]))
+    layer.step(x_buf, y, T, logits=lg_buf)
+    torch.cuda.synchronize()
+    ref_lru = orc.LRU(cfg.E, cfg.S)
+    ref_lru.step(np.bincount(orc.topk_gates(logits_all[0], cfg.k)[0].reshape(-1), minlength=cfg.E).astype(np.int32))
+    g = torch.cuda.CUDAGraph()
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            layer.step(x_buf, y, T, logits=lg_buf, stream=stream)
+    torch.cuda.synchronize()
+    # capture did not run the step: the LRU state is still after step 0
+    assert layer.lru_state()[2] == 1
+    for s in range(1, 8):
+        x_np = synth.activations(cfg, T, s)
+        x_buf.copy_(torch.from_numpy(x_np.view(np.int16)))
+        lg_buf.copy_(torch.from_numpy(logits_all[s]))
+        g.replay()
+        torch.cuda.synchronize()
+        ids, gates = orc.topk_gates(logits_all[s], cfg.k)
+        ref_lru.step(np.bincount(ids.reshape(-1), minlength=cfg.E).astype(np.int32))
+        se, lu, st = layer.lru_state()
+        se2, lu2, st2 = ref_lru.state()
+        assert np.array_equal(se.numpy(), se2) and np.array_equal(lu.numpy(), lu2) and st == st2, s
+        ref = orc.moe_ffn(x_np, ids, gates, pages.experts, cfg.I)
+        st_ = helpers.error_stats(helpers.bf16_to_f64(y), ref)
+        bound = helpers.l2_bounds(ids, np.arange(T), cfg.E, (), cfg.H, cfg.I)
+        assert st_["max_over_l2"] <= helpers.TOL_MAX_OVER_L2 and np.all(st_["l2_per_token"] <= bound), (s, st_)
+    assert layer.device_view("status", torch.int32, (1,)).item() == 0
+    layer.close()
+
+
+def test_layer_mixed_precision_reranking(cuda_lib, orc):
+    # config-5 behaviour at a small size: every `every` steps the experts are
+    # re-ranked by the EMA of their gate mass; the top quarter keep FP8 pages,
+    # the rest get 4-bit pages; a changed expert's page is swapped on the host
+    # and its resident copy forgotten, so its next use refills the new page
+    pqe = cuda_lib
+    E, H, I, k, T, every, n_hi = 32, 256, 128, 4, 48, 6, 8
+    cfg = synth.small_config(E=E, H=H, I=I, k=k, T=T, S=E, cid=81, reuse_p=0.7, zipf_s=1.1, router_gemm=False,
+                             steps=24)
+    stride = pqe.slot_stride(H, I)
+    lay8 = pqe.page_layout(pqe.PQE_FMT_FP8, H, I)
+    n8, n4 = pqe.page_bytes(pqe.PQE_FMT_FP8, H, I), pqe.page_bytes(pqe.PQE_FMT_MXFP4, H, I)
+    fp8_pages = torch.zeros((E, stride), dtype=torch.uint8)
+    fp4_pages = torch.zeros((E, stride), dtype=torch.uint8)
+    ex8, ex4 = {}, {}
+    dev_page = torch.zeros(stride, dtype=torch.uint8, device=DEV)
+    dev_p4 = torch.zeros(n4, dtype=torch.uint8, device=DEV)
+    for e in range(E):
+        w13, w2 = synth.expert_weights(cfg, e)
+        pqe.pqe_pack_fp8_page(torch.from_numpy(w13).to(DEV), torch.from_numpy(w2).to(DEV), H, I, dev_page)
+        pqe.pqe_pack_mxfp4_page(dev_page, H, I, dev_p4)
+        fp8_pages[e] = dev_page.cpu()
+        fp4_pages[e, :n4] = dev_p4.cpu()
+        q13, s13 = orc.quant_e4m3_rows(w13)
+        q2, s2 = orc.quant_e4m3_rows(w2)
+        ex8[e] = (q13, s13, q2, s2)
+        ex4[e] = orc.quant_mxfp4_rows(q13, s13) + orc.quant_mxfp4_rows(q2, s2)
+    fp8_pages, fp4_pages = fp8_pages.pin_memory(), fp4_pages.pin_memory()
+    m_lib = synth.importance_init(cfg)
+    m_orc = m_lib.copy()
+    fmt = np.zeros(E, np.uint8)
+    pqe.pqe_rank_formats(torch.from_numpy(m_lib), n_hi, torch.from_numpy(fmt))
+    fmt_orc = orc.rank_formats(m_orc, n_hi)
+    assert np.array_equal(fmt, fmt_orc)
+    host = [fp8_pages[e] if fmt[e] == 0 else fp4_pages[e] for e in range(E)]
+    sizes = [n8 if fmt[e] == 0 else n4 for e in range(E)]
+    fmt_dev = torch.from_numpy(fmt.copy()).to(DEV)
+    layer = pqe.PagedMoELayer(E, H, I, k, E, 0, T, host, sizes, expert_fmt=fmt_dev)
+    ref_lru = orc.LRU(E, E)
+    tr = synth.RoutingTrace(cfg, T)
+    y = torch.zeros((T, H), dtype=torch.bfloat16, device=DEV)
+    n_changes = 0
+    for s in range(24):
+        logits = tr.step(s)
+        x_np = synth.activations(cfg, T, s)
+        layer.step(torch.from_numpy(x_np.view(np.int16)).to(DEV), y, T, logits=torch.from_numpy(logits).to(DEV))
+        torch.cuda.synchronize()
+        ids = layer.device_view("topk_ids", torch.int32, (T, k)).cpu().numpy()
+        gates32 = layer.device_view("topk_w", torch.float32, (T, k)).cpu().numpy()
+        ids_ref, gates_ref = orc.topk_gates(logits, k)
+        assert np.array_equal(ids, ids_ref)
+        ref_lru.step(np.bincount(ids.reshape(-1), minlength=E).astype(np.int32))
+        assert np.array_equal(layer.lru_state()[0].numpy(), ref_lru.state()[0])
+        experts = orc.ExpertSet(E)
+        for e in range(E):
+            experts.set(e, int(fmt[e]), *(ex8[e] if fmt[e] == 0 else ex4[e]))
+        ref = orc.moe_ffn(x_np, ids_ref, gates_ref, experts, I)
+        st = helpers.error_stats(helpers.bf16_to_f64(y), ref)
+        bound = helpers.l2_bounds(ids_ref, np.arange(T), E, set(np.nonzero(fmt == 1)[0].tolist()), H, I)
+        assert st["max_over_l2"] <= helpers.TOL_MAX_OVER_L2 and np.all(st["l2_per_token"] <= bound), (s, st)
+        # importance and re-ranking: library (host) and oracle bit for bit
+        old = fmt.copy()
+        r1 = pqe.pqe_importance_step(torch.from_numpy(m_lib), torch.from_numpy(ids), torch.from_numpy(gates32),
+                                     T, k, E, 0.9, s, every, n_hi, torch.from_numpy(fmt))
+        r2 = orc.importance_step(m_orc, ids, gates32, E, s, fmt_orc, alpha=0.9, every=every, n_hi=n_hi)
+        assert r1 == r2 and np.array_equal(m_lib, m_orc) and np.array_equal(fmt, fmt_orc)
+        for e in np.nonzero(fmt != old)[0]:
+            page = fp8_pages[e] if fmt[e] == 0 else fp4_pages[e]
+            layer.set_host_page(int(e), page, n8 if fmt[e] == 0 else n4)
+            ref_lru.invalidate(int(e))
+            n_changes += 1
+        if (fmt != old).any():
+            fmt_dev.copy_(torch.from_numpy(fmt))
+    assert n_changes > 0
+    assert int((fmt == 0).sum()) == n_hi
+    assert layer.device_view("status", torch.int32, (1,)).item() == 0
+    layer.close()
+
+
+def test_layer_config4_shapes_compressed(cuda_lib, orc):
+    # E=512, H=2560, I=640, 46 slots, Huffman-compressed host tier decoded on the
+    # GPU after every refill. 16 distinct pages, expert e uses page e % 16.
+    pqe = cuda_lib
+    cfg = synth.CONFIGS[4]
+    E, H, I, k, S, T = cfg.E, cfg.H, cfg.I, cfg.k, cfg.S, 1
+    n_src = 16
+    stride = pqe.slot_stride(H, I)
+    nb = pqe.page_bytes(pqe.PQE_FMT_FP8, H, I)
+    bound = pqe.pqe_huff_page_bound(H, I)
+    comp = torch.zeros((n_src, bound), dtype=torch.uint8)
+    luts_src = torch.zeros((n_src, 2 * 4096), dtype=torch.uint8)
+    sizes_src, src_w = [], []
+    dev_page = torch.zeros(stride, dtype=torch.uint8, device=DEV)
+    for j in range(n_src):
+        w13, w2 = synth.expert_weights(cfg, j)
+        pqe.pqe_pack_fp8_page(torch.from_numpy(w13).to(DEV), torch.from_numpy(w2).to(DEV), H, I, dev_page)
+        page = dev_page[:nb].cpu().contiguous()
+        sizes_src.append(pqe.pqe_huff_encode_page(page, H, I, comp[j], luts_src[j, :4096], luts_src[j, 4096:]))
+        q13, s13 = orc.quant_e4m3_rows(w13)
+        q2, s2 = orc.quant_e4m3_rows(w2)
+        src_w.append((q13, s13, q2, s2))
+        assert sizes_src[-1] < 0.9 * nb
+    comp = comp.pin_memory()
+    host = [comp[e % n_src] for e in range(E)]
+    sizes = [sizes_src[e % n_src] for e in range(E)]
+    luts = luts_src[torch.arange(E) % n_src].contiguous().to(DEV)
+    experts = orc.ExpertSet(E)
+    for e in range(E):
+        experts.set(e, 0, *src_w[e % n_src])
+    layer = pqe.PagedMoELayer(E, H, I, k, S, E, T, host, sizes, compressed=True, luts=luts)
+    ref_lru = orc.LRU(E, S)
+    tr = synth.RoutingTrace(cfg, T)
+    y = torch.zeros((T, H), dtype=torch.bfloat16, device=DEV)
+    side = torch.cuda.Stream()
+    misses = 0
+    for s in range(12):
+        logits = tr.step(s)
+        x_np = synth.activations(cfg, T, s)
+        info = layer.step(torch.from_numpy(x_np.view(np.int16)).to(DEV), y, T,
+                          logits=torch.from_numpy(logits).to(DEV), side_stream=side)
+        misses += info.n_miss
+        ids, g = orc.topk_gates(logits, k)
+        _, me, _, _ = ref_lru.step(np.bincount(ids.reshape(-1), minlength=E).astype(np.int32))
+        assert info.n_miss == len(me)
+        torch.cuda.synchronize()
+        assert np.array_equal(layer.lru_state()[0].numpy(), ref_lru.state()[0])
+        ref = orc.moe_ffn(x_np, ids, g, experts, I)
+        st = helpers.error_stats(helpers.bf16_to_f64(y), ref)
+        assert st["max_over_l2"] <= helpers.TOL_MAX_OVER_L2 and st["l2"] <= helpers.TOL_L2_GEMV, (s, st)
+    assert misses >= 8
+    assert layer.device_view("status", torch.int32, (1,)).item() == 0
     layer.close()

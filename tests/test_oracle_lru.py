@@ -119,3 +119,17 @@ def test_lru_all_resident_gives_identity(orc):
     assert np.array_equal(pt, np.arange(E)) and not wb
     pt, me, md, wb = lru.step(np.ones(E, np.int32))
     assert np.array_equal(pt, np.arange(E)) and len(me) == 0
+
+
+def test_lru_invalidate_hand(orc):
+    # invalidation empties the slot; the next miss takes the lowest empty slot
+    E, S = 6, 3
+    lru = orc.LRU(E, S)
+    lru.step(_counts(E, [0, 1, 2]))            # slots: 0 1 2
+    lru.invalidate(1)
+    se, lu, _ = lru.state()
+    assert se.tolist() == [0, -1, 2] and lu.tolist() == [0, -1, 0]
+    pt, me, md, wb = lru.step(_counts(E, [5]))
+    assert list(zip(me.tolist(), md.tolist())) == [(5, 1)]
+    lru.invalidate(4)                           # not resident: no change
+    assert lru.state()[0].tolist() == [0, 5, 2]
