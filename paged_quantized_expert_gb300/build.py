@@ -16,7 +16,10 @@ LIB = os.path.join(OUT_DIR, "libpqe.so")
 OBJ_DIR = os.path.join(PKG, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
+# host code: no floating-point contraction, so host arithmetic that must match
+# the specification bit for bit (the importance EMA) rounds every operation on
+# every host architecture
+NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden,-ffp-contract=off",
               "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
 
 

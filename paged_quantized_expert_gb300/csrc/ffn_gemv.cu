@@ -68,9 +68,11 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(FfnArgs a, int tc_mi
     const int gpos = block_excl_scan(gemv ? 1 : 0, warp_tot, total);
     if (gemv) a.sched[1 + gpos] = e;
     if (threadIdx.x == 0) a.sched[0] = total;
-    // work weight of a CUDA-core expert: its weight stream (~2 rows' worth) plus its rows
+    // work weight of a weight-stream expert: its bytes (FP8 4, E2M1 2) plus 3 per
+    // further group of 8 tokens (each repeats the conversion and the mma)
     int wtot;
-    const int wpos = block_excl_scan(gemv ? n + 2 : 0, warp_tot, wtot);
+    const int wgt = (fmt == PQE_FMT_FP8 ? 4 : 2) + 3 * ((n > 0 ? n - 1 : 0) / 8);
+    const int wpos = block_excl_scan(gemv ? wgt : 0, warp_tot, wtot);
     if (gemv) a.wpre[gpos] = wpos;
     if (threadIdx.x == 0) a.wpre[total] = wtot;
     const int nt = tc ? (n + 127) / 128 : 0;

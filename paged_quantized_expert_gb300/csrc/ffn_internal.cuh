@@ -44,9 +44,10 @@ struct TcBuffers {
     float *sh;           // [A]
 };
 
-// batches of at least this many rows (FP8 pages) take the tensor-core path;
-// below it the CUDA-core weight stream is bound by HBM, above it by its FMAs
-constexpr int TC_MIN_ROWS = 5;
+// batches of at least this many rows (FP8 pages) take the tcgen05 path; the
+// weight stream handles up to 8 tokens in one mma column group, so its cost up
+// to here is that of reading the weights once
+constexpr int TC_MIN_ROWS = 9;
 
 bool tc_shape_ok(int H, int I);
 bool stream_shape_ok(int H, int I);

@@ -4,17 +4,29 @@
 // The weights of a routed expert are read once from its slot (expert-pager
 // article, rand.pepabo.com, "エキスパート重みの階層ページング"); for a handful of
 // tokens per expert the layer is bound by that stream from HBM. One CTA per SM
-// (cooperative launch); warp 0 is the producer: one thread pulls whole
-// contiguous row blocks of the pages into a ring of shared-memory stages with
-// cp.async.bulk and mbarrier transaction counts (8 gate/up row pairs of w13, or
-// 64 rows of w2, plus their scales). Warps 1-8 consume: exact FP8 (or E2M1 with
-// E8M0 block scale) -> fp32 conversion, fp32 FMA against x / h staged in shared
-// memory as fp32 once per expert (four tokens at a time), shuffle
-// reduce-scatter, SwiGLU, bf16 out. Each CTA takes a contiguous range of units
-// holding an equal share of the work, weighting each expert by its rows.
-// Phase 1 (w13 + SwiGLU -> h) and phase 2 (w2 -> out_perm) are separated by a
-// grid barrier among the consumer warps; the producer keeps streaming, so
-// phase-2 weights are in flight while the last phase-1 units finish.
+// (cooperative launch). Warp 0 is the producer: its lanes pull the weight rows
+// of a unit (8 gate/up row pairs of w13, or 64 rows of w2, plus their scales)
+// into a ring of shared-memory stages with one cp.async.bulk per row, completing
+// on an mbarrier transaction count. Rows land with a small pad so that the
+// consumers' fragment loads are free of bank conflicts.
+//
+// Warps 1-8 consume with mma.sync m16n8k16 (f16 inputs, fp32 accumulate): 16
+// weight rows are the M side and up to 8 tokens the N side. FP8 E4M3 weights
+// convert exactly to f16 (one cvt per two weights); E2M1 weights too, with their
+// E8M0 block scale applied to each 32-column block's partial sum. Activations
+// (bf16 x, fp32 h) are brought to f16 with a power-of-two factor per token and
+// per warp slice of K, so products of bf16 x are exact (h is rounded to 11
+// bits) and all sums are fp32. Inside a warp's slice the K order is permuted
+// identically for weights and activations, which a dot product allows: each
+// lane reads contiguous weight bytes of its rows.
+// Phase 1 (w13 + SwiGLU -> h): the 8 warps split K of a 16-row unit; their
+// partial sums meet in shared memory and one warp applies the row scales and
+// SwiGLU. Phase 2 (w2 -> out_perm): warp w takes 16 of the unit's 64 rows and
+// half of K; the halves meet in shared memory. Each CTA takes a contiguous range
+// of units holding an equal share of the work, weighting each expert by its
+// bytes and token groups. The phases are separated by a grid barrier among the
+// consumer warps; the producer keeps streaming, so phase-2 weights are in
+// flight while the last phase-1 units finish.
 // Every wait is bounded: on expiry PQE_STATUS_TIMEOUT is set and the waiter
 // moves on.
 #include "ffn_internal.cuh"
@@ -25,16 +37,29 @@ namespace st {
 
 constexpr int CONS = 8;                   // consumer warps
 constexpr int THREADS = 32 * (CONS + 1);  // + producer warp
-constexpr int PAIRS = 8;                  // w13 gate/up row pairs per unit (one per consumer warp)
-constexpr int ROWS2 = 64;                 // w2 rows per unit (eight per consumer warp)
-constexpr int NTS = 4;                    // tokens staged in shared memory at once (fp32)
-constexpr int NTG = 4;                    // tokens per register group
+constexpr int PAIRS = 8;                  // w13 gate/up row pairs per unit (16 weight rows)
+constexpr int ROWS2 = 64;                 // w2 rows per unit
+constexpr int NT = 8;                     // tokens per mma column group
+constexpr int NCH_MAX = 5;                // 64-column chunks of K a warp holds at most (H <= 2560, I <= 640)
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
+
+// shared-memory pitch of a weight row of `len` bytes: FP8 rows are read as
+// 16-byte pieces (pitch = 64 mod 128), E2M1 rows as 4-byte pieces (pitch = 16
+// mod 128); either way a warp's loads fall on distinct banks
+__host__ __device__ inline uint32_t pitch8(int len) { return (uint32_t)round_up((size_t)len, 128) + 64; }
+__host__ __device__ inline uint32_t pitch4(int len) { return (uint32_t)round_up((size_t)len, 128) + 16; }
+// w2 units land as 2-KiB-class pieces (single-row copies of I bytes stream
+// poorly): FP8 as 16 pieces of 4 rows, E2M1 as 8 pieces of 8 rows, each piece
+// padded like a row above. An mma row then takes one row from each piece:
+// FP8 m-tile mt, mma row g <- unit row 4g + mt; E2M1 m-tile mt, mma rows g and
+// g+8 <- unit rows 8g + 2mt and 8g + 2mt + 1.
+__host__ __device__ inline uint32_t piece8(int I) { return pitch8(4 * I); }
+__host__ __device__ inline uint32_t piece4(int I) { return pitch4(4 * I); }
 
 struct Geo {
     int stages;
     uint32_t stage_bytes;  // multiple of 128
-    uint32_t stage_off, bar_off, act_off, out_off, sched_off, smem_bytes;
+    uint32_t red_off, sched_off, bar_off, smem_bytes;
 };
 
 // per active expert, staged in shared memory once per launch
@@ -80,80 +105,214 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
 // barrier among the consumer warps only (named barrier 1)
 __device__ __forceinline__ void cons_sync() { asm volatile("bar.sync 1, %0;" ::"n"(CONS * 32) : "memory"); }
 
-__device__ __forceinline__ void cvt16_e4m3(const uint4 &v, float (&f)[16]) {
-    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 a = e4m3x2_to_f32x2((uint16_t)(u[i] & 0xffff));
-        const float2 b = e4m3x2_to_f32x2((uint16_t)(u[i] >> 16));
-        f[4 * i] = a.x;
-        f[4 * i + 1] = a.y;
-        f[4 * i + 2] = b.x;
-        f[4 * i + 3] = b.y;
-    }
+// two E4M3 codes (low / high 16 bits of w) -> f16x2, exact
+__device__ __forceinline__ uint32_t f16x2_e4m3_lo(uint32_t w) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, l;\n\t}" : "=r"(r) : "r"(w));
+    return r;
 }
-
-__device__ __forceinline__ void cvt16_e2m1(uint32_t lo, uint32_t hi, float s, float (&f)[16]) {
-    const uint32_t u[2] = {lo, hi};
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const float2 v = e2m1x2_to_f32x2((uint8_t)(u[i] >> (8 * b)));
-            f[8 * i + 2 * b] = v.x * s;
-            f[8 * i + 2 * b + 1] = v.y * s;
-        }
-}
-
-// 16 weights . 16 fp32 activations from shared memory
-__device__ __forceinline__ float dot16_f32(const float (&w)[16], const float *x, float acc) {
-    const float4 *x4 = reinterpret_cast<const float4 *>(x);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float4 v = x4[q];
-        acc = __fmaf_rn(w[4 * q], v.x, acc);
-        acc = __fmaf_rn(w[4 * q + 1], v.y, acc);
-        acc = __fmaf_rn(w[4 * q + 2], v.z, acc);
-        acc = __fmaf_rn(w[4 * q + 3], v.w, acc);
-    }
-    return acc;
-}
-
-// 8 partial sums per lane -> lane l holds the warp total of index (l >> 2) & 7
-__device__ __forceinline__ float reduce_scatter8(float (&v)[8], int lane) {
-#pragma unroll
-    for (int o = 16, n = 4; o >= 4; o >>= 1, n >>= 1) {
-        const bool up = (lane & o) != 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if (i < n) {
-                const float send = up ? v[i] : v[i + n];
-                const float keep = up ? v[i + n] : v[i];
-                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-            }
-        }
-    }
-    float r = v[0];
-    r += __shfl_xor_sync(0xffffffffu, r, 2);
-    r += __shfl_xor_sync(0xffffffffu, r, 1);
+__device__ __forceinline__ uint32_t f16x2_e4m3_hi(uint32_t w) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, h;\n\t}" : "=r"(r) : "r"(w));
     return r;
 }
 
-// 32 partial sums per lane -> lane l holds the warp total of index l
-__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+// four bytes of E2M1 pairs -> four f16x2 (byte i -> d[i], low nibble in the low half), exact
+__device__ __forceinline__ void f16x2_e2m1x4(uint32_t w, uint32_t (&d)[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\tcvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3])
+        : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// D[16 x 8] += A[16 x 16] . B[16 x 8], f16 inputs, fp32 accumulate. Lane (g, c):
+// a0/a2 = row g, k pairs (2c, 2c+1) / (2c+8, 2c+9); a1/a3 = row g+8, same k;
+// b0/b1 = column g, same k as a0/a2; d = rows g, g+8 x columns 2c, 2c+1.
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// power of two s with amax * s in [2^14, 2^15) (inside f16's range), and 1/s
+__device__ __forceinline__ void pow2_scale(float amax, float &s, float &inv) {
+    int sh = 14 - ((int)((__float_as_uint(amax) >> 23) & 0xffu) - 127);
+    if (amax == 0.0f) sh = 0;
+    sh = max(-126, min(126, sh));
+    s = __uint_as_float((uint32_t)(127 + sh) << 23);
+    inv = __uint_as_float((uint32_t)(127 - sh) << 23);
+}
+
+// Activation fragments of one token group for a warp's K slice (chunks c0 ..
+// c0+nch-1 of 64 columns): lane (g, c) holds token g; v[j][i] is its column
+// pair i of chunk j as f16x2. Column order inside a chunk: for FP8 weights lane
+// c takes columns 16c .. 16c+15; for E2M1 weights columns 8c .. 8c+7 of each of
+// the chunk's two 32-column blocks.
+template <int NCH>
+struct BFrag {
+    uint32_t v[NCH][8];
+};
+
+// Column offset (elements) of piece q (0..1 for bf16 x as 8-element pieces,
+// 0..3 for fp32 h as 4-element pieces) of chunk `ch` for lane c.
+__device__ __forceinline__ int bf16_piece(int ch, int q, int c, bool fp8map) {
+    const int base = 64 * ch;
+    return fp8map ? base + 16 * c + 8 * q : base + 32 * q + 8 * c;
+}
+__device__ __forceinline__ int f32_piece(int ch, int q, int c, bool fp8map) {
+    const int base = 64 * ch;
+    return fp8map ? base + 16 * c + 4 * q : base + (q >> 1) * 32 + 8 * c + 4 * (q & 1);
+}
+
+// The token's amax over the warp slice (its four lanes hold it). With amax in
+// [2^-4, 2^15) the values convert with factor 1: bf16 x is then exact in f16
+// down to amax * 2^-10 and below that off by at most 2^-25 absolute, far
+// inside the tolerance; only other amax take a second, scaled pass.
+__device__ __forceinline__ bool unit_factor_ok(float amax) {
+    return amax == 0.0f || (amax >= 0.0625f && amax < 32768.0f);
+}
+
+__device__ __forceinline__ float token_amax(float amax) {
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    return fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+}
+
+// from a bf16 row (x); row == nullptr -> zeros. inv = 1/s of this lane's token.
+template <int NCH>
+__device__ __forceinline__ void load_bfrag_bf16(const uint16_t *row, int c0, int nch, int c, bool fp8map, BFrag<NCH> &b,
+                                                float &inv) {
+    float amax = 0.0f;
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-        const bool up = (lane & o) != 0;
+    for (int j = 0; j < NCH; ++j) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            if (i < o) {
-                const float send = up ? v[i] : v[i + o];
-                const float keep = up ? v[i + o] : v[i];
-                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        for (int q = 0; q < 2; ++q) {
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (j < nch && row != nullptr)
+                v = __ldg(reinterpret_cast<const uint4 *>(row + bf16_piece(c0 + j, q, c, fp8map)));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
+                amax = fmaxf(amax, fmaxf(fabsf(lo), fabsf(hi)));
+                b.v[j][4 * q + i] = pack_f16x2(lo, hi);
             }
         }
     }
-    return v[0];
+    amax = token_amax(amax);
+    inv = 1.0f;
+    if (unit_factor_ok(amax)) return;
+    float s;
+    pow2_scale(amax, s, inv);
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            if (j < nch && row != nullptr) {
+                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(row + bf16_piece(c0 + j, q, c, fp8map)));
+                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    b.v[j][4 * q + i] =
+                        pack_f16x2(__uint_as_float(w[i] << 16) * s, __uint_as_float(w[i] & 0xffff0000u) * s);
+            }
+        }
+    }
+}
+
+// from an fp32 row (h, written earlier in this launch by other CTAs: read at L2)
+template <int NCH>
+__device__ __forceinline__ void load_bfrag_f32(const float *row, int c0, int nch, int c, bool fp8map, BFrag<NCH> &b,
+                                               float &inv) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j < nch && row != nullptr)
+                v = __ldcg(reinterpret_cast<const float4 *>(row + f32_piece(c0 + j, q, c, fp8map)));
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+            b.v[j][2 * q] = pack_f16x2(v.x, v.y);
+            b.v[j][2 * q + 1] = pack_f16x2(v.z, v.w);
+        }
+    }
+    amax = token_amax(amax);
+    inv = 1.0f;
+    if (unit_factor_ok(amax)) return;
+    float s;
+    pow2_scale(amax, s, inv);
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (j < nch && row != nullptr) {
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(row + f32_piece(c0 + j, q, c, fp8map)));
+                b.v[j][2 * q] = pack_f16x2(v.x * s, v.y * s);
+                b.v[j][2 * q + 1] = pack_f16x2(v.z * s, v.w * s);
+            }
+        }
+    }
+}
+
+// acc[mma rows g, g+8 x tokens 2c, 2c+1] += W . B over the warp's chunks.
+// FP8: mma row g at rows + g * pitch, row g+8 `off8` bytes after it; lane c
+// reads bytes 16c .. 16c+15 of each chunk.
+template <int NCH>
+__device__ __forceinline__ void mma_rows_fp8(const uint8_t *rows, uint32_t pitch, uint32_t off8, int c0, int nch,
+                                             int g, int c, const BFrag<NCH> &b, float (&acc)[4]) {
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+        if (j < nch) {
+            const uint8_t *pa = rows + (size_t)g * pitch + 64 * (c0 + j) + 16 * c;
+            const uint4 wa = *reinterpret_cast<const uint4 *>(pa);
+            const uint4 wb = *reinterpret_cast<const uint4 *>(pa + off8);
+            const uint32_t ua[4] = {wa.x, wa.y, wa.z, wa.w}, ub[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                mma_f16(acc, f16x2_e4m3_lo(ua[q]), f16x2_e4m3_lo(ub[q]), f16x2_e4m3_hi(ua[q]), f16x2_e4m3_hi(ub[q]),
+                        b.v[j][2 * q], b.v[j][2 * q + 1]);
+        }
+    }
+}
+
+// E2M1: rows placed as for FP8; lane c reads bytes 4c .. 4c+3 of each 16-byte
+// (32-column) block. E8M0 scales of mma row g at scales + g * spitch, of row
+// g+8 `soff8` bytes after them, one byte per block.
+template <int NCH>
+__device__ __forceinline__ void mma_rows_fp4(const uint8_t *rows, uint32_t pitch, uint32_t off8,
+                                             const uint8_t *scales, int spitch, int soff8, int c0, int nch, int g,
+                                             int c, const BFrag<NCH> &b, float (&acc)[4]) {
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+        if (j < nch) {
+#pragma unroll
+            for (int lb = 0; lb < 2; ++lb) {
+                const int blk = 2 * (c0 + j) + lb;
+                const uint8_t *pa = rows + (size_t)g * pitch + 16 * blk + 4 * c;
+                uint32_t fa[4], fb[4];
+                f16x2_e2m1x4(*reinterpret_cast<const uint32_t *>(pa), fa);
+                f16x2_e2m1x4(*reinterpret_cast<const uint32_t *>(pa + off8), fb);
+                float t[4] = {0.f, 0.f, 0.f, 0.f};
+                mma_f16(t, fa[0], fb[0], fa[1], fb[1], b.v[j][4 * lb], b.v[j][4 * lb + 1]);
+                mma_f16(t, fa[2], fb[2], fa[3], fb[3], b.v[j][4 * lb + 2], b.v[j][4 * lb + 3]);
+                const float sa = e8m0_to_f32(scales[(size_t)g * spitch + blk]);
+                const float sb = e8m0_to_f32(scales[(size_t)g * spitch + soff8 + blk]);
+                acc[0] = __fmaf_rn(sa, t[0], acc[0]);
+                acc[1] = __fmaf_rn(sa, t[1], acc[1]);
+                acc[2] = __fmaf_rn(sb, t[2], acc[2]);
+                acc[3] = __fmaf_rn(sb, t[3], acc[3]);
+            }
+        }
+    }
 }
 
 __device__ __forceinline__ bool page_ok(const FfnArgs &a, int e, int &slot, int &fmt) {
@@ -186,6 +345,7 @@ __device__ __forceinline__ void unit_range(const int32_t *wpre, int n, int per, 
     u1 = unit_at(wpre, n, per, total * (blockIdx.x + 1) / gridDim.x);
 }
 
+template <int NCH>
 __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a, const Geo g) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int H = a.H, I = a.I;
@@ -193,6 +353,8 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar_full = sbase + g.bar_off, bar_empty = bar_full + 8 * g.stages;
     const PageLayout L8 = fp8_layout(H, I), L4 = mxfp4_layout(H, I);
+    // row pitches of the four stage layouts
+    const uint32_t p13_8 = pitch8(H), p13_4 = pitch4(H / 2), q2_8 = piece8(I), q2_4 = piece4(I);
     // the expert list, its work-weight prefix and each expert's batch and page,
     // loaded once by all threads in parallel (no dependent global loads later)
     const int n_act = __ldg(a.sched);
@@ -221,160 +383,147 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
     unit_range(s_wpre, n_act, per2, u2a, u2b);
 
     if (warp == 0) {
-        // ---------------- producer ----------------
-        if (lane == 0) {
-            int it = 0;
-            bool ok = true;
-            for (int phase = 1; phase <= 2 && ok; ++phase) {
-                const int ua = phase == 1 ? u13a : u2a, ub = phase == 1 ? u13b : u2b;
-                const int per = phase == 1 ? per13 : per2;
-                for (int u = ua; u < ub; ++u, ++it) {
-                    const int s = it % g.stages;
-                    if (!mbar_wait(bar_empty + 8 * s, ((uint32_t)(it / g.stages) & 1u) ^ 1u)) {
-                        ok = false;
-                        break;
+        // ---------------- producer: one bulk copy per weight row ----------------
+        int it = 0;
+        bool ok = true;
+        for (int phase = 1; phase <= 2 && ok; ++phase) {
+            const int ua = phase == 1 ? u13a : u2a, ub = phase == 1 ? u13b : u2b;
+            const int per = phase == 1 ? per13 : per2;
+            for (int u = ua; u < ub; ++u, ++it) {
+                const int s = it % g.stages;
+                int w_ok = 1;
+                if (lane == 0) w_ok = mbar_wait(bar_empty + 8 * s, ((uint32_t)(it / g.stages) & 1u) ^ 1u) ? 1 : 0;
+                if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+                    ok = false;
+                    break;
+                }
+                const ExpertInfo f = s_info[u / per];
+                const int rb = u % per;
+                const uint32_t dst = sbase + (uint32_t)s * g.stage_bytes;
+                const uint32_t fb = bar_full + 8 * s;
+                if (!f.valid) {
+                    if (lane == 0) mbar_arrive(fb);  // no data: consumers write zeros
+                    continue;
+                }
+                const uint8_t *page = page_addr(a, f.slot);
+                if (phase == 1) {
+                    // stage rows 0..7: gate rows rb*8 .. +7; rows 8..15: the matching up rows
+                    // then the rows' scales: FP8 8 + 8 fp32, E2M1 [16][H/32] E8M0
+                    const bool fp8 = f.fmt == PQE_FMT_FP8;
+                    const uint32_t rowb = fp8 ? (uint32_t)H : (uint32_t)H / 2, pitch = fp8 ? p13_8 : p13_4;
+                    const uint32_t scb = fp8 ? 4u * PAIRS : (uint32_t)PAIRS * (H / 32);
+                    const size_t scrow = fp8 ? 4 : (size_t)(H / 32);
+                    if (lane == 0) mbar_expect_tx(fb, 2u * PAIRS * rowb + 2u * scb);
+                    __syncwarp();
+                    if (lane < 2 * PAIRS) {
+                        const size_t wr = lane < PAIRS ? (size_t)rb * PAIRS + lane : (size_t)I + rb * PAIRS + (lane - PAIRS);
+                        bulk_g2s(dst + (uint32_t)lane * pitch, page + (fp8 ? L8.w13 : L4.w13) + wr * rowb, rowb, fb);
+                    } else if (lane < 2 * PAIRS + 2) {
+                        const int hf = lane - 2 * PAIRS;  // 0: the gate rows' scales, 1: the up rows'
+                        const size_t sr = (size_t)(hf ? I : 0) + (size_t)rb * PAIRS;
+                        bulk_g2s(dst + 2 * PAIRS * pitch + (uint32_t)hf * scb, page + (fp8 ? L8.s13 : L4.s13) + sr * scrow,
+                                 scb, fb);
                     }
-                    const ExpertInfo f = s_info[u / per];
-                    const int rb = u % per, fmt = f.fmt;
-                    const uint32_t dst = sbase + g.stage_off + (uint32_t)s * g.stage_bytes;
-                    const uint32_t fb = bar_full + 8 * s;
-                    if (!f.valid) {
-                        mbar_arrive(fb);  // no data: consumers write zeros
-                        continue;
-                    }
-                    const uint8_t *page = page_addr(a, f.slot);
-                    if (phase == 1 && fmt == PQE_FMT_FP8) {
-                        const uint32_t rows = (uint32_t)PAIRS * H;
-                        mbar_expect_tx(fb, 2 * rows);
-                        bulk_g2s(dst, page + L8.w13 + (size_t)rb * PAIRS * H, rows, fb);
-                        bulk_g2s(dst + rows, page + L8.w13 + (size_t)(I + rb * PAIRS) * H, rows, fb);
-                    } else if (phase == 1) {
-                        const uint32_t rows = (uint32_t)PAIRS * H / 2, sc = (uint32_t)PAIRS * H / 32;
-                        mbar_expect_tx(fb, 2 * rows + 2 * sc);
-                        bulk_g2s(dst, page + L4.w13 + (size_t)rb * PAIRS * (H / 2), rows, fb);
-                        bulk_g2s(dst + rows, page + L4.w13 + (size_t)(I + rb * PAIRS) * (H / 2), rows, fb);
-                        bulk_g2s(dst + 2 * rows, page + L4.s13 + (size_t)rb * PAIRS * (H / 32), sc, fb);
-                        bulk_g2s(dst + 2 * rows + sc, page + L4.s13 + (size_t)(I + rb * PAIRS) * (H / 32), sc, fb);
-                    } else if (fmt == PQE_FMT_FP8) {
-                        const uint32_t rows = (uint32_t)ROWS2 * I;
-                        mbar_expect_tx(fb, rows + 4 * ROWS2);
-                        bulk_g2s(dst, page + L8.w2 + (size_t)rb * ROWS2 * I, rows, fb);
-                        bulk_g2s(dst + rows, page + L8.s2 + (size_t)rb * ROWS2 * 4, 4 * ROWS2, fb);
-                    } else {
-                        const uint32_t rows = (uint32_t)ROWS2 * I / 2, sc = (uint32_t)ROWS2 * I / 32;
-                        mbar_expect_tx(fb, rows + sc);
-                        bulk_g2s(dst, page + L4.w2 + (size_t)rb * ROWS2 * (I / 2), rows, fb);
-                        bulk_g2s(dst + rows, page + L4.s2 + (size_t)rb * ROWS2 * (I / 32), sc, fb);
-                    }
+                } else {
+                    // pieces of 4 (FP8) or 8 (E2M1) contiguous rows, 4*I bytes each; then the scales
+                    const bool fp8 = f.fmt == PQE_FMT_FP8;
+                    const int np = fp8 ? 16 : 8;
+                    const uint32_t pb = 4u * I, pitch = fp8 ? q2_8 : q2_4;
+                    const uint32_t scb = fp8 ? 4u * ROWS2 : (uint32_t)ROWS2 * (I / 32);
+                    const uint8_t *w2 = page + (fp8 ? L8.w2 : L4.w2) + (size_t)rb * ROWS2 * (fp8 ? I : I / 2);
+                    if (lane == 0) mbar_expect_tx(fb, (uint32_t)np * pb + scb);
+                    __syncwarp();
+                    if (lane < np) bulk_g2s(dst + (uint32_t)lane * pitch, w2 + (size_t)lane * pb, pb, fb);
+                    else if (lane == np)
+                        bulk_g2s(dst + (uint32_t)np * pitch,
+                                 page + (fp8 ? L8.s2 + (size_t)rb * ROWS2 * 4 : L4.s2 + (size_t)rb * ROWS2 * (I / 32)),
+                                 scb, fb);
                 }
             }
+        }
+        if (lane == 0) {
             if (!ok) atomicOr(a.status, PQE_STATUS_TIMEOUT);
+            // the copies issued last have landed before the CTA may exit
+            for (int j = (it > g.stages ? it - g.stages : 0); j < it; ++j)
+                mbar_wait(bar_full + 8 * (j % g.stages), (uint32_t)(j / g.stages) & 1u);
         }
         return;  // the producer warp takes no part in the consumer barriers
     }
 
     // ---------------- consumers ----------------
     const int cw = warp - 1;
-    float *xs = reinterpret_cast<float *>(smem + g.act_off);        // [NTS][H] fp32 (phase 1)
-    float *hs = reinterpret_cast<float *>(smem + g.act_off);        // [NTS][I] fp32 (phase 2)
-    float *outs = reinterpret_cast<float *>(smem + g.out_off);      // [NTS][ROWS2]
-    int it = 0;
+    const int gq = lane >> 2, cq = lane & 3;                      // mma fragment coordinates
+    float4 *red = reinterpret_cast<float4 *>(smem + g.red_off);  // [2][CONS][32] partial sums
+    int it = 0, rc = 0;
     bool timed_out = false;
-    int cur_e = -1, cur_g = -1;
+    BFrag<NCH> bf;
+    float inv = 1.0f;
+    int b_a = -1, b_tg = -1;  // expert and token group bf holds
 
-    // ---- phase 1: h[p, j] = SiLU(gate_j . x_t) * (up_j . x_t)
-    for (int u = u13a; u < u13b; ++u, ++it) {
-        const int s = it % g.stages;
-        const ExpertInfo f = s_info[u / per13];
-        const int e = f.e, rb = u % per13, p0 = f.p0, n = f.n, slot = f.slot, fmt = f.fmt;
-        const int j = rb * PAIRS + cw;
-        bool valid = f.valid != 0;
-        if (!mbar_wait(bar_full + 8 * s, (uint32_t)(it / g.stages) & 1u)) {
-            valid = false;
-            timed_out = true;
-        }
-        const uint8_t *stg = smem + g.stage_off + (size_t)s * g.stage_bytes;
-        float sg = 1.0f, su = 1.0f;
-        if (valid && fmt == PQE_FMT_FP8) {
-            const float *s13 = reinterpret_cast<const float *>(page_addr(a, slot) + L8.s13);
-            sg = __ldg(s13 + j);
-            su = __ldg(s13 + I + j);
-        }
-        for (int g0 = 0; g0 < n; g0 += NTS) {
-            const int nts = min(NTS, n - g0);
-            if (cur_e != e || cur_g != g0) {
-                cons_sync();
-                for (int i = threadIdx.x - 32; i < nts * (H / 8); i += CONS * 32) {
-                    const int t = i / (H / 8), c = i % (H / 8);
-                    const int tok = a.perm_src[p0 + g0 + t] / a.k;
-                    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)tok * H) + c);
-                    float4 *d = reinterpret_cast<float4 *>(xs + (size_t)t * H + 8 * c);
-                    d[0] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
-                                       __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
-                    d[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u),
-                                       __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
-                }
-                cons_sync();
-                cur_e = e;
-                cur_g = g0;
+    // ---- phase 1: h[p, j] = SiLU(gate_j . x_t) * (up_j . x_t); warp cw owns chunks [c0, c0 + nch) of K
+    {
+        const int NC = H / 64, c0 = cw * NC / CONS, nch = (cw + 1) * NC / CONS - c0;
+        for (int u = u13a; u < u13b; ++u, ++it) {
+            const int s = it % g.stages;
+            const int ua = u / per13;
+            const ExpertInfo f = s_info[ua];
+            const int rb = u % per13, p0 = f.p0, n = f.n;
+            const bool fp8 = f.fmt == PQE_FMT_FP8;
+            bool valid = f.valid != 0 && !timed_out;
+            if (!timed_out && !mbar_wait(bar_full + 8 * s, (uint32_t)(it / g.stages) & 1u)) {
+                valid = false;
+                timed_out = true;
             }
-            for (int tg = 0; tg < nts; tg += NTG) {
-                float v[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = 0.0f;
-                if (valid && fmt == PQE_FMT_FP8) {
-                    const uint4 *gr = reinterpret_cast<const uint4 *>(stg + (size_t)cw * H);
-                    const uint4 *ur = reinterpret_cast<const uint4 *>(stg + (size_t)(PAIRS + cw) * H);
-                    for (int c = lane; c < H / 16; c += 32) {
-                        float wg[16], wu[16];
-                        cvt16_e4m3(gr[c], wg);
-                        cvt16_e4m3(ur[c], wu);
-#pragma unroll
-                        for (int t = 0; t < NTG; ++t) {
-                            if (tg + t < nts) {
-                                const float *xr = xs + (size_t)(tg + t) * H + 16 * c;
-                                v[2 * t] = dot16_f32(wg, xr, v[2 * t]);
-                                v[2 * t + 1] = dot16_f32(wu, xr, v[2 * t + 1]);
-                            }
-                        }
+            const uint8_t *stg = smem + (size_t)s * g.stage_bytes;
+            for (int tg = 0; tg < n; tg += NT) {
+                const int nt = min(NT, n - tg);
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                if (valid) {
+                    if (b_a != ua || b_tg != tg) {
+                        const uint16_t *row = nullptr;
+                        if (gq < nt) row = a.x + (size_t)(__ldg(a.perm_src + p0 + tg + gq) / a.k) * H;
+                        load_bfrag_bf16(row, c0, nch, cq, fp8, bf, inv);
+                        b_a = ua;
+                        b_tg = tg;
                     }
-                } else if (valid) {
-                    const uint32_t rows = (uint32_t)PAIRS * H / 2;
-                    const uint4 *gr = reinterpret_cast<const uint4 *>(stg + (size_t)cw * (H / 2));
-                    const uint4 *ur = reinterpret_cast<const uint4 *>(stg + rows + (size_t)cw * (H / 2));
-                    const uint8_t *gs = stg + 2 * rows + (size_t)cw * (H / 32);
-                    const uint8_t *us = stg + 2 * rows + (uint32_t)PAIRS * H / 32 + (size_t)cw * (H / 32);
-                    for (int c = lane; c < H / 32; c += 32) {
-                        const uint4 vg = gr[c], vu = ur[c];
-                        const float xg = e8m0_to_f32(gs[c]), xu = e8m0_to_f32(us[c]);
+                    if (fp8) mma_rows_fp8(stg, p13_8, 8 * p13_8, c0, nch, gq, cq, bf, acc);
+                    else
+                        mma_rows_fp4(stg, p13_4, 8 * p13_4, stg + 2 * PAIRS * p13_4, H / 32, 8 * (H / 32), c0, nch, gq,
+                                     cq, bf, acc);
+                }
+                // undo this warp's activation factors (tokens 2cq, 2cq+1 sit in lanes 8cq, 8cq+4)
+                const float i0 = __shfl_sync(0xffffffffu, inv, 8 * cq), i1 = __shfl_sync(0xffffffffu, inv, 8 * cq + 4);
+                float4 *rbuf = red + (rc & 1) * CONS * 32;
+                rbuf[cw * 32 + lane] = make_float4(acc[0] * i0, acc[1] * i1, acc[2] * i0, acc[3] * i1);
+                cons_sync();
+                if (cw == rc % CONS) {
+                    // lane (gq, cq): gate row j = rb*8 + gq and up row j, tokens 2cq, 2cq+1
+                    float4 v = rbuf[lane];
 #pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            float wg[16], wu[16];
-                            cvt16_e2m1(half ? vg.z : vg.x, half ? vg.w : vg.y, xg, wg);
-                            cvt16_e2m1(half ? vu.z : vu.x, half ? vu.w : vu.y, xu, wu);
-#pragma unroll
-                            for (int t = 0; t < NTG; ++t) {
-                                if (tg + t < nts) {
-                                    const float *xr = xs + (size_t)(tg + t) * H + 32 * c + 16 * half;
-                                    v[2 * t] = dot16_f32(wg, xr, v[2 * t]);
-                                    v[2 * t + 1] = dot16_f32(wu, xr, v[2 * t + 1]);
-                                }
-                            }
-                        }
+                    for (int w2 = 1; w2 < CONS; ++w2) {
+                        const float4 t = rbuf[w2 * 32 + lane];
+                        v.x += t.x;
+                        v.y += t.y;
+                        v.z += t.z;
+                        v.w += t.w;
                     }
+                    const int j = rb * PAIRS + gq;
+                    float sg = 1.0f, su = 1.0f;
+                    if (valid && fp8) {
+                        const float *s13 = reinterpret_cast<const float *>(stg + 2 * PAIRS * p13_8);
+                        sg = s13[gq];
+                        su = s13[PAIRS + gq];
+                    }
+                    const int t0 = 2 * cq;
+                    if (t0 < nt) a.h[(size_t)(p0 + tg + t0) * I + j] = valid ? silu(v.x * sg) * (v.z * su) : 0.0f;
+                    if (t0 + 1 < nt)
+                        a.h[(size_t)(p0 + tg + t0 + 1) * I + j] = valid ? silu(v.y * sg) * (v.w * su) : 0.0f;
                 }
-                // lane l: index q = (l >> 2) & 7 = 2 t + {0 gate, 1 up}
-                const float r = reduce_scatter8(v, lane);
-                const float up = __shfl_down_sync(0xffffffffu, r, 4);
-                const int q = (lane >> 2) & 7, t = q >> 1;
-                if ((lane & 3) == 0 && (q & 1) == 0 && tg + t < nts) {
-                    const float hv = valid ? silu(r * sg) * (up * su) : 0.0f;
-                    a.h[(size_t)(p0 + g0 + tg + t) * I + j] = hv;
-                }
+                ++rc;
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
     }
 
     // ---- grid barrier among consumers: every h row is written before phase 2 reads it
@@ -393,141 +542,107 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
         __threadfence();
     }
     cons_sync();
-    cur_e = -1;
-    cur_g = -1;
+    b_a = -1;
+    b_tg = -1;
 
-    // ---- phase 2: out_perm[p, r] = w2_r . h_p
-    for (int u = u2a; u < u2b; ++u, ++it) {
-        const int s = it % g.stages;
-        const ExpertInfo f = s_info[u / per2];
-        const int e = f.e, rb = u % per2, p0 = f.p0, n = f.n, fmt = f.fmt;
-        const int r0 = rb * ROWS2;
-        bool valid = f.valid != 0;
-        if (!mbar_wait(bar_full + 8 * s, (uint32_t)(it / g.stages) & 1u)) {
-            valid = false;
-            timed_out = true;
-        }
-        const uint8_t *stg = smem + g.stage_off + (size_t)s * g.stage_bytes;
-        for (int g0 = 0; g0 < n; g0 += NTS) {
-            const int nts = min(NTS, n - g0);
-            if (cur_e != e || cur_g != g0) {
-                cons_sync();
-                for (int i = threadIdx.x - 32; i < nts * (I / 4); i += CONS * 32) {
-                    const int t = i / (I / 4), c = i % (I / 4);
-                    reinterpret_cast<float4 *>(hs + (size_t)t * I)[c] =
-                        reinterpret_cast<const float4 *>(a.h + (size_t)(p0 + g0 + t) * I)[c];
-                }
-                cons_sync();
-                cur_e = e;
-                cur_g = g0;
+    // ---- phase 2: out_perm[p, r] = w2_r . h_p; warp cw: rows 16 mt .. 16 mt + 15 of the unit, half kh of K
+    {
+        const int mt = cw & 3, kh = cw >> 2;
+        const int NC = I / 64, c0 = kh * NC / 2, nch = (kh + 1) * NC / 2 - c0;
+        for (int u = u2a; u < u2b; ++u, ++it) {
+            const int s = it % g.stages;
+            const int ua = u / per2;
+            const ExpertInfo f = s_info[ua];
+            const int rb = u % per2, p0 = f.p0, n = f.n;
+            const int r0 = rb * ROWS2;
+            const bool fp8 = f.fmt == PQE_FMT_FP8;
+            bool valid = f.valid != 0 && !timed_out;
+            if (!timed_out && !mbar_wait(bar_full + 8 * s, (uint32_t)(it / g.stages) & 1u)) {
+                valid = false;
+                timed_out = true;
             }
-            for (int tg = 0; tg < nts; tg += NTG) {
-                float v[32];  // index 4 r + t: row cw*8 + r, token tg + t
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-                if (valid && fmt == PQE_FMT_FP8) {
-                    for (int c = lane; c < I / 16; c += 32) {
-                        float hv[NTG][16];
-#pragma unroll
-                        for (int t = 0; t < NTG; ++t) {
-                            const float4 *hr = reinterpret_cast<const float4 *>(hs + (size_t)(tg + t) * I + 16 * c);
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const float4 f = (tg + t < nts) ? hr[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-                                hv[t][4 * q] = f.x;
-                                hv[t][4 * q + 1] = f.y;
-                                hv[t][4 * q + 2] = f.z;
-                                hv[t][4 * q + 3] = f.w;
-                            }
-                        }
-#pragma unroll
-                        for (int r = 0; r < 8; ++r) {
-                            float w[16];
-                            cvt16_e4m3(reinterpret_cast<const uint4 *>(stg + (size_t)(cw * 8 + r) * I)[c], w);
-#pragma unroll
-                            for (int t = 0; t < NTG; ++t)
-#pragma unroll
-                                for (int q = 0; q < 16; ++q) v[4 * r + t] = __fmaf_rn(w[q], hv[t][q], v[4 * r + t]);
-                        }
+            const uint8_t *stg = smem + (size_t)s * g.stage_bytes;
+            for (int tg = 0; tg < n; tg += NT) {
+                const int nt = min(NT, n - tg);
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                if (valid) {
+                    if (b_a != ua || b_tg != tg) {
+                        const float *row = gq < nt ? a.h + (size_t)(p0 + tg + gq) * I : nullptr;
+                        load_bfrag_f32(row, c0, nch, cq, fp8, bf, inv);
+                        b_a = ua;
+                        b_tg = tg;
                     }
-                } else if (valid) {
-                    const uint32_t rows = (uint32_t)ROWS2 * I / 2;
-                    for (int c = lane; c < I / 32; c += 32) {
+                    if (fp8) mma_rows_fp8(stg + (size_t)mt * I, q2_8, 8 * q2_8, c0, nch, gq, cq, bf, acc);
+                    else
+                        mma_rows_fp4(stg + (size_t)mt * I, q2_4, I / 2, stg + 8 * q2_4 + (size_t)2 * mt * (I / 32),
+                                     8 * (I / 32), I / 32, c0, nch, gq, cq, bf, acc);
+                }
+                const float i0 = __shfl_sync(0xffffffffu, inv, 8 * cq), i1 = __shfl_sync(0xffffffffu, inv, 8 * cq + 4);
+                float4 v = make_float4(acc[0] * i0, acc[1] * i1, acc[2] * i0, acc[3] * i1);
+                float4 *rbuf = red + (rc & 1) * CONS * 32;
+                if (kh == 1) rbuf[mt * 32 + lane] = v;
+                cons_sync();
+                if (kh == 0) {
+                    const float4 t = rbuf[mt * 32 + lane];
+                    v.x += t.x;
+                    v.y += t.y;
+                    v.z += t.z;
+                    v.w += t.w;
+                    // unit rows of mma rows gq and gq + 8
+                    const int ra = fp8 ? 4 * gq + mt : 8 * gq + 2 * mt, rbw = fp8 ? ra + 32 : ra + 1;
+                    float sa = 1.0f, sb = 1.0f;
+                    if (valid && fp8) {
+                        const float *s2 = reinterpret_cast<const float *>(stg + 16 * q2_8);
+                        sa = s2[ra];
+                        sb = s2[rbw];
+                    }
+                    const int t0 = 2 * cq;
 #pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            float hv[NTG][16];
-#pragma unroll
-                            for (int t = 0; t < NTG; ++t) {
-                                const float4 *hr =
-                                    reinterpret_cast<const float4 *>(hs + (size_t)(tg + t) * I + 32 * c + 16 * half);
-#pragma unroll
-                                for (int q = 0; q < 4; ++q) {
-                                    const float4 f = (tg + t < nts) ? hr[q] : make_float4(0.f, 0.f, 0.f, 0.f);
-                                    hv[t][4 * q] = f.x;
-                                    hv[t][4 * q + 1] = f.y;
-                                    hv[t][4 * q + 2] = f.z;
-                                    hv[t][4 * q + 3] = f.w;
-                                }
-                            }
-#pragma unroll
-                            for (int r = 0; r < 8; ++r) {
-                                const uint4 wv = reinterpret_cast<const uint4 *>(stg + (size_t)(cw * 8 + r) * (I / 2))[c];
-                                const float sc = e8m0_to_f32(stg[rows + (size_t)(cw * 8 + r) * (I / 32) + c]);
-                                float w[16];
-                                cvt16_e2m1(half ? wv.z : wv.x, half ? wv.w : wv.y, sc, w);
-#pragma unroll
-                                for (int t = 0; t < NTG; ++t)
-#pragma unroll
-                                    for (int q = 0; q < 16; ++q) v[4 * r + t] = __fmaf_rn(w[q], hv[t][q], v[4 * r + t]);
-                            }
+                    for (int i = 0; i < 2; ++i) {
+                        if (t0 + i < nt) {
+                            uint16_t *o = a.out_perm + (size_t)(p0 + tg + t0 + i) * H + r0;
+                            o[ra] = f32_to_bf16_rn(valid ? (i ? v.y : v.x) * sa : 0.0f);
+                            o[rbw] = f32_to_bf16_rn(valid ? (i ? v.w : v.z) * sb : 0.0f);
                         }
                     }
                 }
-                const float sum = reduce_scatter32(v, lane);  // lane l: row cw*8 + l/4, token tg + l%4
-                const int r = lane >> 2, t = lane & 3;
-                float sc = 1.0f;
-                if (valid && fmt == PQE_FMT_FP8)
-                    sc = reinterpret_cast<const float *>(stg + (size_t)ROWS2 * I)[cw * 8 + r];
-                if (tg + t < nts) outs[(tg + t) * ROWS2 + cw * 8 + r] = valid ? sum * sc : 0.0f;
+                ++rc;
             }
-            cons_sync();
-            for (int i = threadIdx.x - 32; i < nts * (ROWS2 / 2); i += CONS * 32) {
-                const int t = i / (ROWS2 / 2), c2 = i % (ROWS2 / 2);
-                const uint32_t pk = (uint32_t)f32_to_bf16_rn(outs[t * ROWS2 + 2 * c2]) |
-                                    ((uint32_t)f32_to_bf16_rn(outs[t * ROWS2 + 2 * c2 + 1]) << 16);
-                reinterpret_cast<uint32_t *>(a.out_perm + (size_t)(p0 + g0 + t) * H + r0)[c2] = pk;
-            }
-            cons_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+            if (!valid && threadIdx.x == 32 && n > 0 && !timed_out) atomicOr(a.status, PQE_STATUS_BAD_PAGE);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
-        if (!valid && threadIdx.x == 32 && n > 0 && !timed_out) atomicOr(a.status, PQE_STATUS_BAD_PAGE);
     }
     if (timed_out && lane == 0) atomicOr(a.status, PQE_STATUS_TIMEOUT);
 }
 
+// 64-column chunks a consumer warp holds: phase 1 splits H/64 over 8 warps, phase 2 I/64 over 2
+static int chunks_per_warp(int H, int I) {
+    const int c1 = (H / 64 + CONS - 1) / CONS, c2 = (I / 64 + 1) / 2;
+    return c1 > c2 ? c1 : c2;
+}
+
 static bool geometry(int H, int I, Geo &g) {
-    const uint32_t s13_fp8 = 2u * PAIRS * H, s13_fp4 = (uint32_t)PAIRS * H + 2u * PAIRS * H / 32;
-    const uint32_t s2_fp8 = (uint32_t)ROWS2 * I + 4u * ROWS2, s2_fp4 = (uint32_t)ROWS2 * I / 2 + (uint32_t)ROWS2 * I / 32;
-    uint32_t sb = s13_fp8;
-    if (s13_fp4 > sb) sb = s13_fp4;
-    if (s2_fp8 > sb) sb = s2_fp8;
-    if (s2_fp4 > sb) sb = s2_fp4;
+    const uint32_t s13_8 = 2u * PAIRS * pitch8(H) + 8u * PAIRS;
+    const uint32_t s13_4 = 2u * PAIRS * pitch4(H / 2) + 2u * PAIRS * (H / 32);
+    const uint32_t s2_8 = 16u * piece8(I) + 4u * ROWS2;
+    const uint32_t s2_4 = 8u * piece4(I) + (uint32_t)ROWS2 * (I / 32);
+    uint32_t sb = s13_8;
+    if (s13_4 > sb) sb = s13_4;
+    if (s2_8 > sb) sb = s2_8;
+    if (s2_4 > sb) sb = s2_4;
     sb = (sb + 127) / 128 * 128;
-    const uint32_t act = (uint32_t)round_up((size_t)NTS * 4 * (H > I ? (size_t)H : (size_t)I), 128);
-    const uint32_t outb = NTS * ROWS2 * 4;
+    const uint32_t redb = 2u * CONS * 32 * 16;
     const uint32_t schedb = (uint32_t)round_up(4 * 1028 + sizeof(ExpertInfo) * 1024, 128);
     const uint32_t budget = 227 * 1024 - 1024;
-    const uint32_t fixed = act + outb + schedb + 256;
+    const uint32_t fixed = redb + schedb + 256;
     if (fixed + 2 * sb > budget) return false;
     int stages = (int)((budget - fixed) / sb);
     if (stages > 4) stages = 4;
     g.stages = stages;
     g.stage_bytes = sb;
-    g.stage_off = 0;
-    g.act_off = stages * sb;
-    g.out_off = g.act_off + act;
-    g.sched_off = g.out_off + outb;
+    g.red_off = stages * sb;
+    g.sched_off = g.red_off + redb;
     g.bar_off = g.sched_off + schedb;
     g.smem_bytes = g.bar_off + 16 * stages;
     return true;
@@ -537,7 +652,9 @@ static bool geometry(int H, int I, Geo &g) {
 
 bool stream_shape_ok(int H, int I) {
     st::Geo g;
-    return H % st::ROWS2 == 0 && I % st::PAIRS == 0 && st::geometry(H, I, g);
+    // phase 1: the 8 consumer warps split H/64 chunks; phase 2: two warps split I/64 chunks
+    return H % st::ROWS2 == 0 && I % st::PAIRS == 0 && H % 64 == 0 && I % 64 == 0 &&
+           st::chunks_per_warp(H, I) <= st::NCH_MAX && st::geometry(H, I, g);
 }
 
 int launch_ffn_stream(const FfnArgs &args, cudaStream_t s) {
@@ -551,7 +668,9 @@ int launch_ffn_stream(const FfnArgs &args, cudaStream_t s) {
         PQE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
     }
     if (g.smem_bytes > smem_set) {
-        PQE_CUDA_TRY(cudaFuncSetAttribute(st::ffn_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        PQE_CUDA_TRY(cudaFuncSetAttribute(st::ffn_stream_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)g.smem_bytes));
+        PQE_CUDA_TRY(cudaFuncSetAttribute(st::ffn_stream_kernel<5>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)g.smem_bytes));
         smem_set = g.smem_bytes;
     }
@@ -567,7 +686,8 @@ int launch_ffn_stream(const FfnArgs &args, cudaStream_t s) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    PQE_CUDA_TRY(cudaLaunchKernelEx(&cfg, st::ffn_stream_kernel, args, g));
+    if (st::chunks_per_warp(args.H, args.I) <= 4) PQE_CUDA_TRY(cudaLaunchKernelEx(&cfg, st::ffn_stream_kernel<4>, args, g));
+    else PQE_CUDA_TRY(cudaLaunchKernelEx(&cfg, st::ffn_stream_kernel<5>, args, g));
     count_launch();
     return PQE_OK;
 }

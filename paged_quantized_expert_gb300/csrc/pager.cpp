@@ -220,6 +220,7 @@ int pqe_importance_step(double *m, const int32_t *ids, const float *gates, int T
         if (e < 0 || e >= E) return PQE_ERR_INVALID_ARG;
         mass[e] += (double)gates[f];
     }
+    // three separately rounded operations (the library is built without contraction)
     for (int e = 0; e < E; ++e) m[e] = alpha * m[e] + (1.0 - alpha) * (mass[e] / (double)T);
     const bool rr = (step + 1) % every == 0;
     if (reranked) *reranked = rr ? 1 : 0;

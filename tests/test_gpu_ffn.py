@@ -118,6 +118,26 @@ def test_config1_end_to_end(cuda_lib, orc):
     check_tokens(orc, pages, cfg, x, ids, g, res, np.arange(64, dtype=np.int32))
 
 
+@pytest.mark.parametrize("shift,fp4", [(18, ()), (-18, ()), (18, (3,)), (-18, (3,))])
+def test_activation_magnitude_extremes(cuda_lib, orc, shift, fp4):
+    # |x| (and so |h|) far from 1: the weight stream brings its f16 activations
+    # into range with a power-of-two factor per token and K slice; the bound is
+    # relative, so the same tolerance holds at any scale
+    pqe = cuda_lib
+    cfg = synth.CONFIGS[1]
+    T = 6
+    pages = Pages(pqe, orc, cfg, needed=set(range(cfg.E)), fp4=set(fp4))
+    x = synth.activations(cfg, T)
+    xf = (x.astype(np.uint32) << 16).view(np.float32) * np.float32(2.0 ** shift)
+    xs = (xf.view(np.uint32) >> 16).astype(np.uint16)
+    logits = np.random.default_rng(7).standard_normal((T, cfg.E)).astype(np.float32)
+    logits[:, 3] += 2.0  # the 4-bit expert is routed
+    res = run_layer(pqe, cfg, T, xs, logits_np=logits, fmt_dev=pages.fmt_dev, pool=pages.pool)
+    ids, g = orc.topk_gates(logits, cfg.k)
+    assert np.array_equal(res["ids"], ids) and res["status"] == 0
+    check_tokens(orc, pages, cfg, xs, ids, g, res, np.arange(T, dtype=np.int32))
+
+
 @pytest.mark.parametrize("E,H,I,k,T,fp4", [
     (5, 192, 64, 3, 37, ()),
     (5, 192, 64, 3, 37, (1, 3)),
