@@ -269,6 +269,8 @@ __device__ __forceinline__ void load_bfrag_f32(const float *row, int c0, int nch
 template <int NCH>
 __device__ __forceinline__ void mma_rows_fp8(const uint8_t *rows, uint32_t pitch, uint32_t off8, int c0, int nch,
                                              int g, int c, const BFrag<NCH> &b, float (&acc)[4]) {
+    // four independent accumulator chains (one per k-step of a chunk)
+    float part[4][4] = {};
 #pragma unroll
     for (int j = 0; j < NCH; ++j) {
         if (j < nch) {
@@ -278,10 +280,12 @@ __device__ __forceinline__ void mma_rows_fp8(const uint8_t *rows, uint32_t pitch
             const uint32_t ua[4] = {wa.x, wa.y, wa.z, wa.w}, ub[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-                mma_f16(acc, f16x2_e4m3_lo(ua[q]), f16x2_e4m3_lo(ub[q]), f16x2_e4m3_hi(ua[q]), f16x2_e4m3_hi(ub[q]),
-                        b.v[j][2 * q], b.v[j][2 * q + 1]);
+                mma_f16(part[q], f16x2_e4m3_lo(ua[q]), f16x2_e4m3_lo(ub[q]), f16x2_e4m3_hi(ua[q]),
+                        f16x2_e4m3_hi(ub[q]), b.v[j][2 * q], b.v[j][2 * q + 1]);
         }
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] += (part[0][i] + part[1][i]) + (part[2][i] + part[3][i]);
 }
 
 // E2M1: rows placed as for FP8; lane c reads bytes 4c .. 4c+3 of each 16-byte
@@ -638,7 +642,7 @@ static bool geometry(int H, int I, Geo &g) {
     const uint32_t fixed = redb + schedb + 256;
     if (fixed + 2 * sb > budget) return false;
     int stages = (int)((budget - fixed) / sb);
-    if (stages > 4) stages = 4;
+    if (stages > 5) stages = 5;
     g.stages = stages;
     g.stage_bytes = sb;
     g.red_off = stages * sb;

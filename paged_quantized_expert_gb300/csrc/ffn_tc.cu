@@ -47,6 +47,7 @@ constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t ACC_COLS = 256;       // one fp32 accumulator of BM x BN
 constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;  // two: the epilogue of item i overlaps the MMAs of item i+1
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
+constexpr int ROW_CTAS = BM / 8;  // row kernels: CTAs of 8 warps per 128-row tile, one row per warp
 // smem: stages | full[S] empty[S] tfull[2] tempty[2] | tmem base | column scales [BN]
 constexpr int SMEM_BAR_OFF = STAGES * STAGE_BYTES;
 constexpr int SMEM_TMEM_OFF = SMEM_BAR_OFF + 8 * (2 * STAGES + 4);
@@ -405,10 +406,13 @@ __global__ void __launch_bounds__(256) tc_gather_quant_kernel(const uint16_t *__
                                                               const int32_t *__restrict__ n_tiles,
                                                               uint8_t *__restrict__ xq, float *__restrict__ sx,
                                                               uint32_t *__restrict__ hmax) {
-    if ((int)blockIdx.x >= *n_tiles) return;
-    const int4 tile = reinterpret_cast<const int4 *>(tiles)[blockIdx.x];
+    // CTA b: tile b / 16, rows 8 (b % 16) .. +7 of it, one per warp
+    const int ti = (int)blockIdx.x / ROW_CTAS;
+    if (ti >= *n_tiles) return;
+    const int4 tile = reinterpret_cast<const int4 *>(tiles)[ti];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int m = warp; m < tile.z; m += blockDim.x >> 5) {
+    const int m = ((int)blockIdx.x % ROW_CTAS) * 8 + warp;
+    if (m < tile.z) {
         const int p = tile.y + m;
         const int t = perm_src[p] / k;
         const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
@@ -451,10 +455,12 @@ __global__ void __launch_bounds__(256) tc_hquant_kernel(const uint16_t *__restri
                                                         const int32_t *__restrict__ n_tiles,
                                                         const uint32_t *__restrict__ hmax, uint8_t *__restrict__ hq,
                                                         float *__restrict__ sh) {
-    if ((int)blockIdx.x >= *n_tiles) return;
-    const int4 tile = reinterpret_cast<const int4 *>(tiles)[blockIdx.x];
+    const int ti = (int)blockIdx.x / ROW_CTAS;
+    if (ti >= *n_tiles) return;
+    const int4 tile = reinterpret_cast<const int4 *>(tiles)[ti];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int m = warp; m < tile.z; m += blockDim.x >> 5) {
+    const int m = ((int)blockIdx.x % ROW_CTAS) * 8 + warp;
+    if (m < tile.z) {
         const int p = tile.y + m;
         const float amax = __uint_as_float(hmax[p]);
         const float s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
@@ -557,7 +563,7 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     // persistent grids: one CTA per SM, at most one per work item
     const int items1 = max_tiles * (I / 128), items2 = max_tiles * (H / 256);
     const int grid1 = items1 < sms ? items1 : sms, grid2 = items2 < sms ? items2 : sms;
-    tc_gather_quant_kernel<<<max_tiles, 256, 0, s>>>(args.x, args.perm_src, args.k, H, b.tiles, b.n_tiles, b.xq,
+    tc_gather_quant_kernel<<<max_tiles * ROW_CTAS, 256, 0, s>>>(args.x, args.perm_src, args.k, H, b.tiles, b.n_tiles, b.xq,
                                                      b.sx, b.hmax);
     PQE_LAUNCH_CHECK();
     GemmArgs g1{};
@@ -579,7 +585,7 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     g1.status = args.status;
     tc_gemm_kernel<<<grid1, THREADS, SMEM_BYTES, s>>>(mx, m13c, m13w, g1);
     PQE_LAUNCH_CHECK();
-    tc_hquant_kernel<<<max_tiles, 256, 0, s>>>(b.h, I, b.tiles, b.n_tiles, b.hmax, b.hq, b.sh);
+    tc_hquant_kernel<<<max_tiles * ROW_CTAS, 256, 0, s>>>(b.h, I, b.tiles, b.n_tiles, b.hmax, b.hq, b.sh);
     PQE_LAUNCH_CHECK();
     GemmArgs g2 = g1;
     g2.n_nt = H / 256;
