@@ -20,9 +20,11 @@
 // identically for weights and activations, which a dot product allows: each
 // lane reads contiguous weight bytes of its rows.
 // Phase 1 (w13 + SwiGLU -> h): the 8 warps split K of a 16-row unit; their
-// partial sums meet in shared memory and one warp applies the row scales and
-// SwiGLU. Phase 2 (w2 -> out_perm): warp w takes 16 of the unit's 64 rows and
-// half of K; the halves meet in shared memory. Each CTA takes a contiguous range
+// partial sums meet in a double-buffered shared-memory area and one warp (in
+// turn) applies the row scales and SwiGLU. Phase 2 (w2 -> out_perm): warp w
+// takes 16 of the unit's 64 rows and half of K; the halves meet the same way.
+// The hand-offs go through mbarriers, so a warp waits only for the partials it
+// combines or for a buffer two steps back, never for all warps at once. Each CTA takes a contiguous range
 // of units holding an equal share of the work, weighting each expert by its
 // bytes and token groups. The phases are separated by a grid barrier among the
 // consumer warps; the producer keeps streaming, so phase-2 weights are in
@@ -378,6 +380,17 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, CONS);
         }
+        // partial-sum hand-off: phase 1 all warps -> one combining warp, phase 2
+        // pairs of warps (K halves of one m-tile); [buffer][slot]
+        const uint32_t rb = bar_empty + 8 * g.stages;
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(rb + 8 * b, CONS * 32);  // rfull1[b]
+            mbar_init(rb + 16 + 8 * b, 32);    // rfree1[b]
+            for (int m = 0; m < 4; ++m) {
+                mbar_init(rb + 32 + 8 * (4 * b + m), 32);  // rfull2[b][m]
+                mbar_init(rb + 96 + 8 * (4 * b + m), 32);  // rfree2[b][m]
+            }
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -458,6 +471,8 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
     const int cw = warp - 1;
     const int gq = lane >> 2, cq = lane & 3;                      // mma fragment coordinates
     float4 *red = reinterpret_cast<float4 *>(smem + g.red_off);  // [2][CONS][32] partial sums
+    const uint32_t rfull1 = bar_empty + 8 * g.stages, rfree1 = rfull1 + 16, rfull2 = rfull1 + 32,
+                   rfree2 = rfull1 + 96;
     int it = 0, rc = 0;
     bool timed_out = false;
     BFrag<NCH> bf;
@@ -497,10 +512,17 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
                 }
                 // undo this warp's activation factors (tokens 2cq, 2cq+1 sit in lanes 8cq, 8cq+4)
                 const float i0 = __shfl_sync(0xffffffffu, inv, 8 * cq), i1 = __shfl_sync(0xffffffffu, inv, 8 * cq + 4);
-                float4 *rbuf = red + (rc & 1) * CONS * 32;
+                // hand-off through buffer b: wait until the combine of step rc - 2 has
+                // read it, publish this warp's partials; only the combining warp waits
+                // for the others' (no barrier across all warps)
+                const int b = rc & 1;
+                const uint32_t ph = (uint32_t)(rc >> 1) & 1u;
+                float4 *rbuf = red + b * CONS * 32;
+                if (!timed_out && !mbar_wait(rfree1 + 8 * b, ph ^ 1u)) timed_out = true;
                 rbuf[cw * 32 + lane] = make_float4(acc[0] * i0, acc[1] * i1, acc[2] * i0, acc[3] * i1);
-                cons_sync();
+                mbar_arrive(rfull1 + 8 * b);
                 if (cw == rc % CONS) {
+                    if (!timed_out && !mbar_wait(rfull1 + 8 * b, ph)) timed_out = true;
                     // lane (gq, cq): gate row j = rb*8 + gq and up row j, tokens 2cq, 2cq+1
                     float4 v = rbuf[lane];
 #pragma unroll
@@ -518,6 +540,7 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
                         sg = s13[gq];
                         su = s13[PAIRS + gq];
                     }
+                    mbar_arrive(rfree1 + 8 * b);  // buffer b read
                     const int t0 = 2 * cq;
                     if (t0 < nt) a.h[(size_t)(p0 + tg + t0) * I + j] = valid ? silu(v.x * sg) * (v.z * su) : 0.0f;
                     if (t0 + 1 < nt)
@@ -548,6 +571,7 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
     cons_sync();
     b_a = -1;
     b_tg = -1;
+    rc = 0;  // phase 2 hand-off barriers count from their first phase
 
     // ---- phase 2: out_perm[p, r] = w2_r . h_p; warp cw: rows 16 mt .. 16 mt + 15 of the unit, half kh of K
     {
@@ -583,11 +607,18 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
                 }
                 const float i0 = __shfl_sync(0xffffffffu, inv, 8 * cq), i1 = __shfl_sync(0xffffffffu, inv, 8 * cq + 4);
                 float4 v = make_float4(acc[0] * i0, acc[1] * i1, acc[2] * i0, acc[3] * i1);
-                float4 *rbuf = red + (rc & 1) * CONS * 32;
-                if (kh == 1) rbuf[mt * 32 + lane] = v;
-                cons_sync();
-                if (kh == 0) {
+                // the K half 1 warp of m-tile mt hands its partials to the K half 0 warp
+                const int b = rc & 1;
+                const uint32_t ph = (uint32_t)(rc >> 1) & 1u;
+                float4 *rbuf = red + b * CONS * 32;
+                if (kh == 1) {
+                    if (!timed_out && !mbar_wait(rfree2 + 8 * (4 * b + mt), ph ^ 1u)) timed_out = true;
+                    rbuf[mt * 32 + lane] = v;
+                    mbar_arrive(rfull2 + 8 * (4 * b + mt));
+                } else {
+                    if (!timed_out && !mbar_wait(rfull2 + 8 * (4 * b + mt), ph)) timed_out = true;
                     const float4 t = rbuf[mt * 32 + lane];
+                    mbar_arrive(rfree2 + 8 * (4 * b + mt));
                     v.x += t.x;
                     v.y += t.y;
                     v.z += t.z;
@@ -648,7 +679,7 @@ static bool geometry(int H, int I, Geo &g) {
     g.red_off = stages * sb;
     g.sched_off = g.red_off + redb;
     g.bar_off = g.sched_off + schedb;
-    g.smem_bytes = g.bar_off + 16 * stages;
+    g.smem_bytes = g.bar_off + 16 * stages + 160;
     return true;
 }
 

@@ -21,8 +21,8 @@
 //
 // Persistent CTA (one per SM) over (M tile, N tile) work items, 6 warps:
 // warp 0 issues TMA (one thread), warp 1 owns TMEM and issues the MMAs (one
-// thread), warps 2-5 read the accumulator from TMEM (each warp its 32-lane
-// quarter) and run the epilogue. 4-stage smem ring of A [128 x 128 B] +
+// thread), warps 2-9 read the accumulator from TMEM (two warps per 32-lane
+// quarter, each half of the columns) and run the epilogue. 4-stage smem ring of A [128 x 128 B] +
 // B [256 x 128 B] tiles, 128-byte swizzle, K-major; two TMEM accumulators so
 // the epilogue of one item overlaps the MMAs of the next.
 // Every mbarrier wait is bounded: on expiry the CTA sets PQE_STATUS_TIMEOUT,
@@ -42,17 +42,17 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int EPI_WARPS = 4;
+constexpr int EPI_WARPS = 8;  // two per TMEM lane quarter, each taking half the columns
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t ACC_COLS = 256;       // one fp32 accumulator of BM x BN
 constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;  // two: the epilogue of item i overlaps the MMAs of item i+1
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 constexpr int ROW_CTAS = BM / 8;  // row kernels: CTAs of 8 warps per 128-row tile, one row per warp
-// smem: stages | full[S] empty[S] tfull[2] tempty[2] | tmem base | column scales [BN]
+// smem: stages | full[S] empty[S] tfull[2] tempty[2] | tmem base | column scales [2][BN]
 constexpr int SMEM_BAR_OFF = STAGES * STAGE_BYTES;
 constexpr int SMEM_TMEM_OFF = SMEM_BAR_OFF + 8 * (2 * STAGES + 4);
 constexpr int SMEM_SCALE_OFF = (SMEM_TMEM_OFF + 4 + 15) / 16 * 16;
-constexpr int SMEM_BYTES = SMEM_SCALE_OFF + 4 * BN + 1024;  // + alignment slack
+constexpr int SMEM_BYTES = SMEM_SCALE_OFF + 8 * BN + 1024;  // two column-scale buffers + alignment slack
 
 // instruction descriptor, kind::f8f6f4: D f32, A/B E4M3, both K-major, N, M
 constexpr uint32_t IDESC = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(BN >> 3) << 17) |
@@ -144,6 +144,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
+}
+
+// SiLU with the hardware exponential and reciprocal: the activations on this
+// path are rounded to E4M3 (3 mantissa bits), far coarser than their error
+__device__ __forceinline__ float silu_fast(float z) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + __expf(-z)));
+    return z * r;
 }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -306,35 +314,44 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else {
         // ---------------- epilogue: TMEM -> registers -> global ----------------
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int q = warp & 3;            // TMEM lane quarter this warp may access
+        const int half = (warp - 2) >> 2;  // which half of the tile's columns it finishes
         const int m = 32 * q + lane;
-        const int et = threadIdx.x - 64;
+        const int et = threadIdx.x - 64;  // one output column per epilogue thread (BN of them)
+        static_assert(EPI_WARPS * 32 == BN, "one column scale per epilogue thread");
+        // weight row scale of output column et of item i
+        auto col_scale_of = [&](int i) -> float {
+            const Item w = item_of(a, i);
+            const uint8_t *page = w.slot < a.n_slots ? a.pool_base + (size_t)w.slot * a.slot_stride
+                                                     : a.wb_base + (size_t)(w.slot - a.n_slots) * a.slot_stride;
+            const float *ws = reinterpret_cast<const float *>(page + a.wscale_off);
+            return ws[et < 128 ? w.r0 + et : w.r1 + (et - 128)];
+        };
+        // the column scales of item i are staged while item i - G is finished
+        col_scale[et] = col_scale_of(blockIdx.x);
+        epi_sync();
         int local = 0;
         bool ok = true;
         for (int i = blockIdx.x; i < n_items && ok; i += G, ++local) {
             const Item w = item_of(a, i);
             const int b = local & 1;
-            const uint8_t *page = w.slot < a.n_slots ? a.pool_base + (size_t)w.slot * a.slot_stride
-                                                     : a.wb_base + (size_t)(w.slot - a.n_slots) * a.slot_stride;
-            // weight row scales of the 256 output columns
-            epi_sync();
-            const float *ws = reinterpret_cast<const float *>(page + a.wscale_off);
-            for (int c = et; c < BN; c += EPI_WARPS * 32) col_scale[c] = ws[c < 128 ? w.r0 + c : w.r1 + (c - 128)];
-            epi_sync();
+            const float *cs = col_scale + b * BN;
+            const int p = w.p0 + m;
+            const bool valid = m < w.nv;
+            // global loads issued before the accumulator wait: this row's scale, the next item's column scale
+            const float rs = valid ? a.row_scale[p] : 0.0f;
+            const float cs_next = i + G < n_items ? col_scale_of(i + G) : 0.0f;
             if (!epi_all(mbar_wait(bar_tfull + 8 * b, (uint32_t)(local >> 1) & 1u))) {
                 ok = false;
                 if (et == 0) atomicOr(a.status, PQE_STATUS_TIMEOUT);
                 break;
             }
             tc_fence_after();
-            const int p = w.p0 + m;
-            const bool valid = m < w.nv;
             const uint32_t trow = tmem + (uint32_t)b * ACC_COLS + ((uint32_t)(32 * q) << 16);
-            const float rs = valid ? a.row_scale[p] : 0.0f;
             if (a.swiglu) {
                 float amax = 0.0f;
                 uint16_t *dst = a.out + (size_t)p * a.out_cols + w.nt * 128;
-                for (int c0 = 0; c0 < 128; c0 += 32) {
+                for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
                     uint32_t g[32], u[32];
                     tmem_ld32(trow + c0, g);
                     tmem_ld32(trow + 128 + c0, u);
@@ -345,9 +362,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                         float h2[2];
 #pragma unroll
                         for (int t = 0; t < 2; ++t) {
-                            const float gv = __uint_as_float(g[j + t]) * rs * col_scale[c0 + j + t];
-                            const float uv = __uint_as_float(u[j + t]) * rs * col_scale[128 + c0 + j + t];
-                            h2[t] = silu(gv) * uv;
+                            const float gv = __uint_as_float(g[j + t]) * rs * cs[c0 + j + t];
+                            const float uv = __uint_as_float(u[j + t]) * rs * cs[128 + c0 + j + t];
+                            h2[t] = silu_fast(gv) * uv;
                         }
                         const uint16_t b0 = f32_to_bf16_rn(h2[0]), b1 = f32_to_bf16_rn(h2[1]);
                         amax = fmaxf(amax, fmaxf(fabsf(bf16_to_f32(b0)), fabsf(bf16_to_f32(b1))));
@@ -363,15 +380,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (valid) atomicMax(a.hmax + p, __float_as_uint(amax));
             } else {
                 uint16_t *dst = a.out + (size_t)p * a.out_cols + w.nt * 256;
-                for (int c0 = 0; c0 < 256; c0 += 32) {
+                for (int c0 = 128 * half; c0 < 128 * half + 128; c0 += 32) {
                     uint32_t d[32];
                     tmem_ld32(trow + c0, d);
                     tmem_ld_wait();
                     uint32_t packed[16];
 #pragma unroll
                     for (int j = 0; j < 32; j += 2) {
-                        const float v0 = __uint_as_float(d[j]) * rs * col_scale[c0 + j];
-                        const float v1 = __uint_as_float(d[j + 1]) * rs * col_scale[c0 + j + 1];
+                        const float v0 = __uint_as_float(d[j]) * rs * cs[c0 + j];
+                        const float v1 = __uint_as_float(d[j + 1]) * rs * cs[c0 + j + 1];
                         packed[j / 2] = (uint32_t)f32_to_bf16_rn(v0) | ((uint32_t)f32_to_bf16_rn(v1) << 16);
                     }
                     if (valid) {
@@ -385,6 +402,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             // this accumulator may be overwritten by the MMAs of item i + 2G
             tc_fence_before();
             mbar_arrive_plain(bar_tempty + 8 * b);
+            // the other buffer was last read for item i - G, which every thread has finished
+            col_scale[(b ^ 1) * BN + et] = cs_next;
+            epi_sync();
         }
     }
     tc_fence_before();
