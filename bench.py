@@ -52,8 +52,10 @@ def parse_args():
     ap.add_argument("--no-sweep", action="store_true", help="skip the T=1 and T=8 lines")
     ap.add_argument("--no-batched", action="store_true", help="skip the module-batched (T=16384) measurement")
     ap.add_argument("--batched-steps", type=int, default=6)
-    ap.add_argument("--workload", default="decode", choices=["decode", "batched"],
-                    help="batched: only the module-batched measurement (for profiling)")
+    ap.add_argument("--workload", default="decode", choices=["decode", "batched", "large", "mixed"],
+                    help="batched / large / mixed: only that measurement (for profiling)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the compressed large-layer (E=512) and mixed-precision (T=4096) measurements")
     ap.add_argument("--pager", default="both", choices=["host", "device", "both"],
                     help="host: LRU on the host (one read-back per step); device: LRU on the GPU, each layer's step "
                          "replayed from a CUDA graph; both: measure both, the faster is the headline")
@@ -453,6 +455,176 @@ def run_batched(pqe, torch, device, host, steps, ws):
                     "bound": "tensor", "flops_per_step": flops}}
 
 
+def _timed_steps(torch, layer, x, y, T, logits, steps, stream, side):
+    """Whole layer steps with per-step FFN events; returns (ms total, [ffn ms], [step infos])."""
+    evs = []
+    for _ in range(steps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    infos = []
+    for i in range(steps):
+        layer.set_ffn_events(*evs[i])
+        info = layer.step(x[i % len(x)], y, T, logits=logits[i % len(logits)], stream=stream, side_stream=side)
+        infos.append((info.n_routed, info.n_miss, info.working_buffer))
+    e1.record(stream)
+    torch.cuda.synchronize()
+    layer.set_ffn_events(None, None)
+    return e0.elapsed_time(e1), [a.elapsed_time(b) for a, b in evs], infos
+
+
+def run_large(pqe, torch, device, steps_t1=64, steps_big=3, n_src=32):
+    """Large paged layer with a compressed host tier (E=512, H=2560, I=640, top-8,
+    46 LRU slots): every refill copies a Huffman-coded page and decodes it on the
+    GPU. T=1 (decode) and T=4096 whole steps, the FFN against HBM / FP8 peak,
+    and the decoder alone on device-resident compressed pages. The host tier
+    holds n_src distinct encoded pages (expert e uses page e % n_src), so the
+    bytes moved and decoded per step are those of the full layer."""
+    cfg = synth.CONFIGS[4]
+    E, H, I, k, S = cfg.E, cfg.H, cfg.I, cfg.k, cfg.S
+    stride = pqe.slot_stride(H, I)
+    nb = pqe.page_bytes(pqe.PQE_FMT_FP8, H, I)
+    bound = pqe.pqe_huff_page_bound(H, I)
+    comp = torch.zeros((n_src, bound), dtype=torch.uint8)
+    luts_src = torch.zeros((n_src, 2 * 4096), dtype=torch.uint8)
+    sizes_src = []
+    page = torch.zeros(stride, dtype=torch.uint8, device=device)
+    for j in range(n_src):
+        w13, w2 = synth.expert_weights(cfg, j)
+        pqe.pqe_pack_fp8_page(torch.from_numpy(w13).to(device), torch.from_numpy(w2).to(device), H, I, page)
+        sizes_src.append(pqe.pqe_huff_encode_page(page[:nb].cpu().contiguous(), H, I, comp[j], luts_src[j, :4096],
+                                                  luts_src[j, 4096:]))
+    comp = comp.pin_memory()
+    host = [comp[e % n_src] for e in range(E)]
+    sizes = [sizes_src[e % n_src] for e in range(E)]
+    luts = luts_src[torch.arange(E) % n_src].contiguous().to(device)
+    big_T = cfg.T[-1]
+    layer = pqe.PagedMoELayer(E, H, I, k, S, E, big_T, host, sizes, compressed=True, luts=luts, device=device)
+    stream = torch.cuda.current_stream(device)
+    side = torch.cuda.Stream(device)
+    out = {"workload": "large paged layer, compressed host tier (E=512, H=2560, I=640, top-8, CACHE_SLOTS=46, "
+                       "Huffman-coded FP8 exponents decoded on the GPU after each refill)",
+           "mean_compressed_ratio": float(np.mean(sizes_src)) / nb}
+    peak_bw = peaks()[0]
+    for T, steps in ((1, steps_t1), (big_T, steps_big)):
+        tr = synth.RoutingTrace(cfg, T)
+        n_tr = min(steps + 4, 32)
+        logits = [torch.from_numpy(tr.step(s)).to(device) for s in range(n_tr)]
+        xs = [torch.from_numpy(synth.activations(cfg, T, s % 2).view(np.int16)).to(device) for s in range(2)]
+        y = torch.zeros((T, H), dtype=torch.bfloat16, device=device)
+        for i in range(2):  # warm-up
+            layer.step(xs[i % 2], y, T, logits=logits[i % n_tr], stream=stream, side_stream=side)
+        ms, ffn, infos = _timed_steps(torch, layer, xs, y, T, logits, steps, stream, side)
+        ffn_ms = float(np.mean(ffn))
+        routed = float(np.mean([r for r, _, _ in infos]))
+        rec = {"tokens_per_s": T * steps / (ms / 1e3), "ms_per_step": ms / steps, "steps": steps,
+               "mean_routed_experts": routed, "mean_misses": float(np.mean([m for _, m, _ in infos])),
+               "ffn_ms": ffn_ms}
+        if T == 1:
+            gbs = (routed * (nb + 0.0) + T * H * 2 + T * k * H * 2) / (ffn_ms / 1e3) / 1e9
+            rec.update({"ffn_hbm_gbs": gbs, "ffn_frac_of_measured_hbm": gbs / peak_bw})
+        else:
+            tflops = 6.0 * T * k * H * I / (ffn_ms / 1e3) / 1e12
+            pk, kind = fp8_peak_tflops()
+            rec.update({"ffn_tflops": tflops, "ffn_frac_of_fp8_peak": tflops / pk, "fp8_peak_kind": kind})
+        out["T=%d" % T] = rec
+    layer.close()
+    out["huff_decode"] = huff_decode_rate(pqe, torch, device, comp, sizes_src, luts_src, H, I, nb)
+    return out
+
+
+def run_mixed(pqe, torch, device, steps=12):
+    """Mixed per-expert precision layer (E=256, H=2048, I=512, top-8, T=4096):
+    the top 25% of experts by a seeded importance score keep FP8 pages, the
+    rest hold MXFP4 pages; all pages resident (256 slots). Whole steps and the
+    FFN against both HBM (bytes of the routed pages) and the FP8 peak."""
+    cfg = synth.CONFIGS[5]
+    E, H, I, k, T = cfg.E, cfg.H, cfg.I, cfg.k, cfg.T[0]
+    stride = pqe.slot_stride(H, I)
+    n8, n4 = pqe.page_bytes(pqe.PQE_FMT_FP8, H, I), pqe.page_bytes(pqe.PQE_FMT_MXFP4, H, I)
+    m = synth.importance_init(cfg)
+    fmt = np.zeros(E, np.uint8)
+    n_hi = E // 4
+    pqe.pqe_rank_formats(torch.from_numpy(m), n_hi, torch.from_numpy(fmt))
+    host = torch.zeros((E, stride), dtype=torch.uint8)
+    page = torch.zeros(stride, dtype=torch.uint8, device=device)
+    p4 = torch.zeros(n4, dtype=torch.uint8, device=device)
+    for e in range(E):
+        w13, w2 = synth.expert_weights(cfg, e)
+        pqe.pqe_pack_fp8_page(torch.from_numpy(w13).to(device), torch.from_numpy(w2).to(device), H, I, page)
+        if fmt[e] == 0:
+            host[e].copy_(page)
+        else:
+            pqe.pqe_pack_mxfp4_page(page, H, I, p4)
+            host[e, :n4].copy_(p4)
+    host = host.pin_memory()
+    sizes = [n8 if fmt[e] == 0 else n4 for e in range(E)]
+    fmt_dev = torch.from_numpy(fmt.copy()).to(device)
+    layer = pqe.PagedMoELayer(E, H, I, k, E, 0, T, [host[e] for e in range(E)], sizes, expert_fmt=fmt_dev,
+                              device=device)
+    stream = torch.cuda.current_stream(device)
+    side = torch.cuda.Stream(device)
+    tr = synth.RoutingTrace(cfg, T)
+    logits_np = [tr.step(s) for s in range(4)]
+    logits = [torch.from_numpy(l).to(device) for l in logits_np]
+    xs = [torch.from_numpy(synth.activations(cfg, T, s).view(np.int16)).to(device) for s in range(2)]
+    y = torch.zeros((T, H), dtype=torch.bfloat16, device=device)
+    for i in range(3):  # warm-up: the first step loads every routed page
+        layer.step(xs[i % 2], y, T, logits=logits[i % 4], stream=stream, side_stream=side)
+    ms, ffn, infos = _timed_steps(torch, layer, xs, y, T, logits, steps, stream, side)
+    layer.close()
+    ffn_ms = float(np.mean(ffn))
+    # routed bytes per step, from the routing of the logits cycled through
+    byts = []
+    for l in logits_np:
+        ids = np.argsort(-l, axis=1, kind="stable")[:, :k]
+        used = np.unique(ids)
+        byts.append(sum(n8 if fmt[e] == 0 else n4 for e in used) + T * H * 2 + T * k * H * 2)
+    bpstep = float(np.mean([byts[i % 4] for i in range(steps)]))
+    gbs = bpstep / (ffn_ms / 1e3) / 1e9
+    tflops = 6.0 * T * k * H * I / (ffn_ms / 1e3) / 1e12
+    pk, kind = fp8_peak_tflops()
+    return {"workload": "mixed per-expert precision layer (E=256, H=2048, I=512, top-8, T=4096; top 25% by "
+                        "importance FP8, the rest MXFP4; all pages resident)",
+            "n_fp8_experts": int((fmt == 0).sum()), "tokens_per_s": T * steps / (ms / 1e3), "ms_per_step": ms / steps,
+            "steps": steps, "ffn_ms": ffn_ms, "ffn_hbm_gbs": gbs,
+            "ffn_frac_of_measured_hbm": gbs / peaks()[0],
+            "ffn_tflops": tflops, "ffn_frac_of_fp8_peak": tflops / pk, "fp8_peak_kind": kind}
+
+
+def huff_decode_rate(pqe, torch, device, comp_host, sizes, luts_host, H, I, nb, n_pages=8, reps=4):
+    """The GPU decoder alone: compressed pages already in HBM -> FP8 pages."""
+    n = min(n_pages, len(sizes))
+    comp = comp_host[:n].to(device)
+    luts = luts_host[:n].to(device)
+    outp = torch.zeros((n, nb), dtype=torch.uint8, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    for j in range(n):  # warm-up
+        pqe.fp8_exp_huff_decode(comp[j], sizes[j], luts[j, :4096], luts[j, 4096:], H, I, outp[j], status, stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        for j in range(n):
+            pqe.fp8_exp_huff_decode(comp[j], sizes[j], luts[j, :4096], luts[j, 4096:], H, I, outp[j], status,
+                                    stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (reps * n)
+    cb = float(np.mean(sizes[:n]))
+    return {"ms_per_page": ms, "decoded_gb_per_s": nb / (ms / 1e3) / 1e9,
+            "compressed_gb_per_s": cb / (ms / 1e3) / 1e9,
+            "hbm_gb_per_s_in_plus_out": (nb + cb) / (ms / 1e3) / 1e9, "status": int(status.item())}
+
+
 # ---- main arm ------------------------------------------------------------------------------
 
 def main():
@@ -474,6 +646,11 @@ def main():
         res = run_batched(pqe, torch, device, host, args.batched_steps, ws)
         if rank == 0:
             print(json.dumps({"batched": res}))
+        return 0
+    if args.workload in ("large", "mixed"):
+        res = run_large(pqe, torch, device) if args.workload == "large" else run_mixed(pqe, torch, device)
+        if rank == 0:
+            print(json.dumps({args.workload: res}))
         return 0
     r = Runner(pqe, torch, device, host, L, max(T, 64))
     xs_dev = [torch.from_numpy(synth.activations(CFG, T, s).view(np.int16)).to(device) for s in range(4)]
@@ -547,6 +724,11 @@ def main():
     if not args.no_batched:
         r.close()
         batched = run_batched(pqe, torch, device, host, args.batched_steps, ws)
+    large = mixed = None
+    if not args.no_extra:
+        r.close()
+        large = run_large(pqe, torch, device)
+        mixed = run_mixed(pqe, torch, device)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -587,6 +769,8 @@ def main():
             "gpu_launches": int(launches),
             "clocks": clk,
             "batched": batched,
+            "large": large,
+            "mixed": mixed,
         }
         print(json.dumps(line))
     r.close()

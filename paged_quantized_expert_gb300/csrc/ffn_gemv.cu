@@ -61,6 +61,7 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(FfnArgs a, int tc_mi
         slot = a.page_table[e];
         fmt = a.expert_fmt ? (int)a.expert_fmt[e] : PQE_FMT_FP8;
     }
+    if (e < a.E && a.done13) a.done13[e] = 0u;
     const bool valid_page = slot >= 0 && slot < a.n_slots + a.n_wb;
     const bool tc = n > 0 && tc_min > 0 && n >= tc_min && fmt == PQE_FMT_FP8 && valid_page;
     const bool gemv = n > 0 && !tc;
@@ -87,7 +88,6 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(FfnArgs a, int tc_mi
     }
     if (threadIdx.x == 0) {
         *n_tiles = total;
-        if (a.grid_bar) *a.grid_bar = 0u;
     }
 }
 
@@ -395,7 +395,7 @@ int launch_ffn_gemv(const FfnArgs &args, int max_active, cudaStream_t s) {
 
 // workspace carve-up shared by the size query and the call
 struct FfnWs {
-    size_t sched, wpre, tiles, n_tiles, grid_bar, h, xq, sx, hbf, hmax, hq, sh, total;
+    size_t sched, wpre, tiles, n_tiles, done13, h, xq, sx, hbf, hmax, hq, sh, total;
     int max_tiles;
     bool tc;
 };
@@ -415,7 +415,7 @@ static FfnWs ffn_ws_layout(int T, int k, int E, int H, int I) {
     w.wpre = take(sizeof(int32_t) * (E + 1));
     w.tiles = take(sizeof(int32_t) * 4 * (size_t)(w.max_tiles ? w.max_tiles : 1));
     w.n_tiles = take(sizeof(int32_t));
-    w.grid_bar = take(sizeof(uint32_t));
+    w.done13 = take(sizeof(uint32_t) * E);
     w.h = take(A * I * sizeof(float));
     if (w.tc) {
         w.xq = take(A * H);
@@ -475,7 +475,7 @@ int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *of
     args.h = reinterpret_cast<float *>(wsb + w.h);
     args.out_perm = static_cast<uint16_t *>(out_perm);
     args.status = status;
-    args.grid_bar = reinterpret_cast<uint32_t *>(wsb + w.grid_bar);
+    args.done13 = reinterpret_cast<uint32_t *>(wsb + w.done13);
     const long A = (long)T * k;
     const int max_active = (int)(A < E ? A : E);
     cudaStream_t s = as_stream(stream);

@@ -22,7 +22,7 @@ struct FfnArgs {
     float *h;                    // fp32 [T*k, I]
     uint16_t *out_perm;          // bf16 [T*k, H]
     int32_t *status;
-    uint32_t *grid_bar;          // grid barrier counter of the stream kernel (zeroed by the schedule)
+    uint32_t *done13;            // [E] stream kernel: phase-1 units x token groups combined per expert (zeroed by the schedule)
 };
 
 // address of page-table entry `slot` (valid: 0 <= slot < n_slots + n_wb)

@@ -24,11 +24,12 @@
 // turn) applies the row scales and SwiGLU. Phase 2 (w2 -> out_perm): warp w
 // takes 16 of the unit's 64 rows and half of K; the halves meet the same way.
 // The hand-offs go through mbarriers, so a warp waits only for the partials it
-// combines or for a buffer two steps back, never for all warps at once. Each CTA takes a contiguous range
-// of units holding an equal share of the work, weighting each expert by its
-// bytes and token groups. The phases are separated by a grid barrier among the
-// consumer warps; the producer keeps streaming, so phase-2 weights are in
-// flight while the last phase-1 units finish.
+// combines or for a buffer two steps back, never for all warps at once. Each
+// CTA takes a contiguous range of units holding an equal share of the work,
+// weighting each expert by its
+// bytes and token groups. Phase 2 of an expert starts once all of its phase-1
+// work (in any CTA) is counted complete, with no grid-wide barrier; the
+// producer keeps streaming, so phase-2 weights are in flight meanwhile.
 // Every wait is bounded: on expiry PQE_STATUS_TIMEOUT is set and the waiter
 // moves on.
 #include "ffn_internal.cuh"
@@ -102,6 +103,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                  "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
                  : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // barrier among the consumer warps only (named barrier 1)
@@ -494,6 +501,13 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
                 timed_out = true;
             }
             const uint8_t *stg = smem + (size_t)s * g.stage_bytes;
+            // this unit's row scales, read before the stage is handed back
+            float sg = 1.0f, su = 1.0f;
+            if (valid && fp8) {
+                const float *s13 = reinterpret_cast<const float *>(stg + 2 * PAIRS * p13_8);
+                sg = s13[gq];
+                su = s13[PAIRS + gq];
+            }
             for (int tg = 0; tg < n; tg += NT) {
                 const int nt = min(NT, n - tg);
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -509,6 +523,10 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
                     else
                         mma_rows_fp4(stg, p13_4, 8 * p13_4, stg + 2 * PAIRS * p13_4, H / 32, 8 * (H / 32), c0, nch, gq,
                                      cq, bf, acc);
+                }
+                if (tg + NT >= n) {  // last token group: this warp reads the stage no more
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_empty + 8 * s);
                 }
                 // undo this warp's activation factors (tokens 2cq, 2cq+1 sit in lanes 8cq, 8cq+4)
                 const float i0 = __shfl_sync(0xffffffffu, inv, 8 * cq), i1 = __shfl_sync(0xffffffffu, inv, 8 * cq + 4);
@@ -534,12 +552,6 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
                         v.w += t.w;
                     }
                     const int j = rb * PAIRS + gq;
-                    float sg = 1.0f, su = 1.0f;
-                    if (valid && fp8) {
-                        const float *s13 = reinterpret_cast<const float *>(stg + 2 * PAIRS * p13_8);
-                        sg = s13[gq];
-                        su = s13[PAIRS + gq];
-                    }
                     mbar_arrive(rfree1 + 8 * b);  // buffer b read
                     const int t0 = 2 * cq;
                     if (t0 < nt) a.h[(size_t)(p0 + tg + t0) * I + j] = valid ? silu(v.x * sg) * (v.z * su) : 0.0f;
@@ -548,27 +560,23 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
                 }
                 ++rc;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
         }
     }
 
-    // ---- grid barrier among consumers: every h row is written before phase 2 reads it
+    // ---- end of phase 1: this CTA's consumers meet (the partial-sum buffers are
+    // reused), then one thread publishes the CTA's finished phase-1 work per
+    // expert; phase 2 waits per expert for the h rows it reads (done13), not
+    // for the whole grid
     __threadfence();
     cons_sync();
-    if (threadIdx.x == 32) {
-        atomicAdd(a.grid_bar, 1u);
-        uint32_t i = 0;
-        while (*reinterpret_cast<volatile uint32_t *>(a.grid_bar) < gridDim.x) {
-            if (++i > WAIT_LIMIT) {
-                timed_out = true;
-                break;
-            }
-            __nanosleep(100);
+    if (threadIdx.x == 32 && u13b > u13a) {
+        for (int ea = u13a / per13; ea <= (u13b - 1) / per13; ++ea) {
+            const int lo = max(u13a, ea * per13), hi = min(u13b, (ea + 1) * per13);
+            const int groups = (s_info[ea].n + NT - 1) / NT;
+            atomicAdd(a.done13 + s_info[ea].e, (uint32_t)((hi - lo) * groups));
         }
-        __threadfence();
     }
-    cons_sync();
+    int ready_a = -1;  // expert whose h rows this warp has seen complete
     b_a = -1;
     b_tg = -1;
     rc = 0;  // phase 2 hand-off barriers count from their first phase
@@ -590,9 +598,34 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
                 timed_out = true;
             }
             const uint8_t *stg = smem + (size_t)s * g.stage_bytes;
+            // unit rows of mma rows gq and gq + 8, and their scales, read before the stage is handed back
+            const int ra = fp8 ? 4 * gq + mt : 8 * gq + 2 * mt, rbw = fp8 ? ra + 32 : ra + 1;
+            float sa = 1.0f, sb = 1.0f;
+            if (valid && fp8) {
+                const float *s2 = reinterpret_cast<const float *>(stg + 16 * q2_8);
+                sa = s2[ra];
+                sb = s2[rbw];
+            }
             for (int tg = 0; tg < n; tg += NT) {
                 const int nt = min(NT, n - tg);
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                if (valid && ready_a != ua) {
+                    // h of this expert: all per13 units x token groups combined (other CTAs included)
+                    const uint32_t target = (uint32_t)per13 * (uint32_t)((n + NT - 1) / NT);
+                    int ok = 1;
+                    if (lane == 0 && !timed_out) {
+                        uint32_t i = 0;
+                        while (ld_acquire(a.done13 + f.e) < target) {
+                            if (++i > WAIT_LIMIT) {
+                                ok = 0;
+                                break;
+                            }
+                            __nanosleep(64);
+                        }
+                    }
+                    if (!__shfl_sync(0xffffffffu, ok, 0)) timed_out = true;
+                    ready_a = ua;
+                }
                 if (valid) {
                     if (b_a != ua || b_tg != tg) {
                         const float *row = gq < nt ? a.h + (size_t)(p0 + tg + gq) * I : nullptr;
@@ -604,6 +637,10 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
                     else
                         mma_rows_fp4(stg + (size_t)mt * I, q2_4, I / 2, stg + 8 * q2_4 + (size_t)2 * mt * (I / 32),
                                      8 * (I / 32), I / 32, c0, nch, gq, cq, bf, acc);
+                }
+                if (tg + NT >= n) {  // last token group: this warp reads the stage no more
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_empty + 8 * s);
                 }
                 const float i0 = __shfl_sync(0xffffffffu, inv, 8 * cq), i1 = __shfl_sync(0xffffffffu, inv, 8 * cq + 4);
                 float4 v = make_float4(acc[0] * i0, acc[1] * i1, acc[2] * i0, acc[3] * i1);
@@ -623,14 +660,6 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
                     v.y += t.y;
                     v.z += t.z;
                     v.w += t.w;
-                    // unit rows of mma rows gq and gq + 8
-                    const int ra = fp8 ? 4 * gq + mt : 8 * gq + 2 * mt, rbw = fp8 ? ra + 32 : ra + 1;
-                    float sa = 1.0f, sb = 1.0f;
-                    if (valid && fp8) {
-                        const float *s2 = reinterpret_cast<const float *>(stg + 16 * q2_8);
-                        sa = s2[ra];
-                        sb = s2[rbw];
-                    }
                     const int t0 = 2 * cq;
 #pragma unroll
                     for (int i = 0; i < 2; ++i) {
@@ -643,8 +672,6 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
                 }
                 ++rc;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * s);
             if (!valid && threadIdx.x == 32 && n > 0 && !timed_out) atomicOr(a.status, PQE_STATUS_BAD_PAGE);
         }
     }

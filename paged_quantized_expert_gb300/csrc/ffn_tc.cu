@@ -48,11 +48,13 @@ constexpr uint32_t ACC_COLS = 256;       // one fp32 accumulator of BM x BN
 constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;  // two: the epilogue of item i overlaps the MMAs of item i+1
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 constexpr int ROW_CTAS = BM / 8;  // row kernels: CTAs of 8 warps per 128-row tile, one row per warp
-// smem: stages | full[S] empty[S] tfull[2] tempty[2] | tmem base | column scales [2][BN]
+// smem: stages | full[S] empty[S] tfull[2] tempty[2] | tmem base | column scales [2][BN] | store buffers
 constexpr int SMEM_BAR_OFF = STAGES * STAGE_BYTES;
 constexpr int SMEM_TMEM_OFF = SMEM_BAR_OFF + 8 * (2 * STAGES + 4);
 constexpr int SMEM_SCALE_OFF = (SMEM_TMEM_OFF + 4 + 15) / 16 * 16;
-constexpr int SMEM_BYTES = SMEM_SCALE_OFF + 8 * BN + 1024;  // two column-scale buffers + alignment slack
+constexpr int EPI_PITCH = 80;  // bytes per row of an epilogue warp's store buffer (64 + 16: conflict-free)
+constexpr int SMEM_EPI_OFF = SMEM_SCALE_OFF + 8 * BN;  // after two column-scale buffers
+constexpr int SMEM_BYTES = SMEM_EPI_OFF + EPI_WARPS * 32 * EPI_PITCH + 1024;  // + alignment slack
 
 // instruction descriptor, kind::f8f6f4: D f32, A/B E4M3, both K-major, N, M
 constexpr uint32_t IDESC = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(BN >> 3) << 17) |
@@ -191,6 +193,29 @@ __device__ __forceinline__ Item item_of(const GemmArgs &a, int i) {
     return it;
 }
 
+// A warp's 32 output rows x 32 bf16 columns (lane = row, packed = its 64 bytes)
+// go to global memory through the warp's padded shared buffer, so that each
+// store instruction writes 8 rows x 64 contiguous bytes (whole 32-byte sectors)
+// instead of 16 bytes in each of 32 rows. out: row 0 of the 32, ld: row stride
+// in elements; rows >= nrows are not written.
+__device__ __forceinline__ void store_rows32(uint8_t *buf, const uint32_t (&packed)[16], uint16_t *out, size_t ld,
+                                             int nrows, int lane) {
+    uint8_t *mine = buf + lane * EPI_PITCH;
+#pragma unroll
+    for (int v = 0; v < 4; ++v)
+        *reinterpret_cast<uint4 *>(mine + 16 * v) =
+            make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int it = 0; it < 4; ++it) {
+        const int pc = it * 32 + lane, r = pc >> 2, part = pc & 3;
+        if (r < nrows)
+            *reinterpret_cast<uint4 *>(out + (size_t)r * ld + 8 * part) =
+                *reinterpret_cast<const uint4 *>(buf + r * EPI_PITCH + 16 * part);
+    }
+    __syncwarp();
+}
+
 // barrier among the epilogue warps only (named barrier 1)
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(EPI_WARPS * 32) : "memory"); }
 
@@ -318,7 +343,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int half = (warp - 2) >> 2;  // which half of the tile's columns it finishes
         const int m = 32 * q + lane;
         const int et = threadIdx.x - 64;  // one output column per epilogue thread (BN of them)
+        uint8_t *ebuf = smem + SMEM_EPI_OFF + (warp - 2) * 32 * EPI_PITCH;  // this warp's store buffer
         static_assert(EPI_WARPS * 32 == BN, "one column scale per epilogue thread");
+        static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
         // weight row scale of output column et of item i
         auto col_scale_of = [&](int i) -> float {
             const Item w = item_of(a, i);
@@ -348,9 +375,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             tc_fence_after();
             const uint32_t trow = tmem + (uint32_t)b * ACC_COLS + ((uint32_t)(32 * q) << 16);
+            // this warp's 32 rows of the tile: the first, and how many hold batch rows
+            uint16_t *wrow = a.out + (size_t)(w.p0 + 32 * q) * a.out_cols;
+            const int nrows = min(max(w.nv - 32 * q, 0), 32);
             if (a.swiglu) {
                 float amax = 0.0f;
-                uint16_t *dst = a.out + (size_t)p * a.out_cols + w.nt * 128;
                 for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
                     uint32_t g[32], u[32];
                     tmem_ld32(trow + c0, g);
@@ -370,16 +399,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                         amax = fmaxf(amax, fmaxf(fabsf(bf16_to_f32(b0)), fabsf(bf16_to_f32(b1))));
                         packed[j / 2] = (uint32_t)b0 | ((uint32_t)b1 << 16);
                     }
-                    if (valid) {
-                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            d4[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-                    }
+                    store_rows32(ebuf, packed, wrow + w.nt * 128 + c0, a.out_cols, nrows, lane);
                 }
                 if (valid) atomicMax(a.hmax + p, __float_as_uint(amax));
             } else {
-                uint16_t *dst = a.out + (size_t)p * a.out_cols + w.nt * 256;
                 for (int c0 = 128 * half; c0 < 128 * half + 128; c0 += 32) {
                     uint32_t d[32];
                     tmem_ld32(trow + c0, d);
@@ -391,12 +414,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const float v1 = __uint_as_float(d[j + 1]) * rs * cs[c0 + j + 1];
                         packed[j / 2] = (uint32_t)f32_to_bf16_rn(v0) | ((uint32_t)f32_to_bf16_rn(v1) << 16);
                     }
-                    if (valid) {
-                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + c0);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            d4[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-                    }
+                    store_rows32(ebuf, packed, wrow + w.nt * 256 + c0, a.out_cols, nrows, lane);
                 }
             }
             // this accumulator may be overwritten by the MMAs of item i + 2G
