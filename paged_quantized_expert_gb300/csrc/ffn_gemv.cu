@@ -63,9 +63,17 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(FfnArgs a, int tc_mi
     }
     if (e < a.E && a.done13) a.done13[e] = 0u;
     const bool valid_page = slot >= 0 && slot < a.n_slots + a.n_wb;
-    const bool tc = n > 0 && tc_min > 0 && n >= tc_min && fmt == PQE_FMT_FP8 && valid_page;
-    const bool gemv = n > 0 && !tc;
+    const bool big = n > 0 && tc_min > 0 && n >= tc_min && valid_page;
+    // 4-bit experts with a large batch get an FP8 copy (while copies last) and the tcgen05 path
     int total;
+    const bool want_x = big && fmt == PQE_FMT_MXFP4 && a.max_xp > 0;
+    const int xpos = block_excl_scan(want_x ? 1 : 0, warp_tot, total);
+    const bool tcx = want_x && xpos < a.max_xp;
+    if (tcx) a.xp_list[xpos] = slot;
+    if (threadIdx.x == 0 && a.xp_count) *a.xp_count = min(total, a.max_xp);
+    const bool tc = (big && fmt == PQE_FMT_FP8) || tcx;
+    const int tslot = tcx ? a.n_slots + a.n_wb + xpos : slot;
+    const bool gemv = n > 0 && !tc;
     const int gpos = block_excl_scan(gemv ? 1 : 0, warp_tot, total);
     if (gemv) a.sched[1 + gpos] = e;
     if (threadIdx.x == 0) a.sched[0] = total;
@@ -83,7 +91,7 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(FfnArgs a, int tc_mi
         t.x = e;
         t.y = a.offsets[e] + 128 * i;
         t.z = min(128, n - 128 * i);
-        t.w = slot;
+        t.w = tslot;
         reinterpret_cast<int4 *>(tiles)[tpos + i] = t;
     }
     if (threadIdx.x == 0) {
@@ -395,8 +403,8 @@ int launch_ffn_gemv(const FfnArgs &args, int max_active, cudaStream_t s) {
 
 // workspace carve-up shared by the size query and the call
 struct FfnWs {
-    size_t sched, wpre, tiles, n_tiles, done13, h, xq, sx, hbf, hmax, hq, sh, total;
-    int max_tiles;
+    size_t sched, wpre, tiles, n_tiles, done13, h, xq, sx, hbf, hmax, hq, sh, xp_list, xp_count, xp, total;
+    int max_tiles, max_xp;
     bool tc;
 };
 
@@ -424,6 +432,12 @@ static FfnWs ffn_ws_layout(int T, int k, int E, int H, int I) {
         w.hmax = take(A * sizeof(uint32_t));
         w.hq = take(A * I);
         w.sh = take(A * sizeof(float));
+        // FP8 copies for 4-bit experts with >= TC_MIN_ROWS rows: at most one per such expert
+        const size_t cap = A / TC_MIN_ROWS < (size_t)E ? A / TC_MIN_ROWS : (size_t)E;
+        w.max_xp = (int)cap;
+        w.xp_list = take(sizeof(int32_t) * (cap ? cap : 1));
+        w.xp_count = take(sizeof(int32_t));
+        w.xp = take(cap * pqe_slot_stride(H, I));
     }
     w.total = off;
     return w;
@@ -476,6 +490,12 @@ int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *of
     args.out_perm = static_cast<uint16_t *>(out_perm);
     args.status = status;
     args.done13 = reinterpret_cast<uint32_t *>(wsb + w.done13);
+    if (w.tc) {
+        args.xp_base = wsb + w.xp;
+        args.xp_list = reinterpret_cast<int32_t *>(wsb + w.xp_list);
+        args.xp_count = reinterpret_cast<int32_t *>(wsb + w.xp_count);
+        args.max_xp = w.max_xp;
+    }
     const long A = (long)T * k;
     const int max_active = (int)(A < E ? A : E);
     cudaStream_t s = as_stream(stream);

@@ -23,6 +23,13 @@ struct FfnArgs {
     uint16_t *out_perm;          // bf16 [T*k, H]
     int32_t *status;
     uint32_t *done13;            // [E] stream kernel: phase-1 units x token groups combined per expert (zeroed by the schedule)
+    // 4-bit pages whose batch takes the tcgen05 path are first rewritten as FP8
+    // pages (power-of-two row scales) into copy i of this region; page-table
+    // entries n_slots + n_wb + i in the tile list address copy i
+    uint8_t *xp_base;            // [max_xp] x slot_stride
+    int32_t *xp_list;            // [max_xp]: page-table entry of the 4-bit page behind copy i
+    int32_t *xp_count;           // [1]: copies used
+    int max_xp;
 };
 
 // address of page-table entry `slot` (valid: 0 <= slot < n_slots + n_wb)

@@ -162,19 +162,27 @@ struct GemmArgs {
     const int32_t *tiles;    // [n][4]: expert, first row p0, valid rows, page-table entry
     const int32_t *n_tiles;  // device count
     int n_nt;                // N tiles per M tile
-    int n_slots;             // entries below this use the cache map, others the working-buffer map
+    int n_slots;             // entries below this use the cache map,
+    int n_wb;                // then n_wb working-buffer entries, then FP8 copies of 4-bit pages
     int K;                   // reduction length in bytes (H for GEMM1, I for GEMM2)
     int I;                   // GEMM1: up rows start at I
     int out_cols;            // row length of the output (I for h, H for out_perm)
     int swiglu;              // 1: GEMM1 epilogue, 0: GEMM2 epilogue
     const float *row_scale;  // sx or sh [A]
-    const uint8_t *pool_base, *wb_base;
+    const uint8_t *pool_base, *wb_base, *xp_base;
     size_t slot_stride;
     size_t wscale_off;       // byte offset of the weight row scales in a page (s13 or s2)
     uint16_t *out;           // bf16 h [A, I] or out_perm [A, H]
     uint32_t *hmax;          // [A] (GEMM1)
     int32_t *status;
 };
+
+// address of the page behind a tile's page-table entry (cache, working buffer or FP8 copy)
+__device__ __forceinline__ const uint8_t *tile_page(const GemmArgs &a, int slot) {
+    if (slot < a.n_slots) return a.pool_base + (size_t)slot * a.slot_stride;
+    if (slot < a.n_slots + a.n_wb) return a.wb_base + (size_t)(slot - a.n_slots) * a.slot_stride;
+    return a.xp_base + (size_t)(slot - a.n_slots - a.n_wb) * a.slot_stride;
+}
 
 struct Item {
     int p0, nv, slot, nt, r0, r1;
@@ -235,7 +243,8 @@ __device__ __forceinline__ bool epi_all(bool v) {
 // tile; neighbouring CTAs share an M tile, so its activations stay in L2).
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB_cache,
-                   const __grid_constant__ CUtensorMap tmB_wb, const GemmArgs a) {
+                   const __grid_constant__ CUtensorMap tmB_wb, const __grid_constant__ CUtensorMap tmB_xp,
+                   const GemmArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const int n_items = *a.n_tiles * a.n_nt;
     if ((int)blockIdx.x >= n_items) return;
@@ -265,6 +274,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB_cache)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB_wb)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB_xp)) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -284,9 +294,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             bool ok = true;
             for (int i = blockIdx.x; i < n_items && ok; i += G) {
                 const Item w = item_of(a, i);
-                const bool in_cache = w.slot < a.n_slots;
-                const CUtensorMap *tmB = in_cache ? &tmB_cache : &tmB_wb;
-                const int zc = in_cache ? w.slot : w.slot - a.n_slots;
+                // the region the tile's page lies in, and its index there
+                const int reg = w.slot < a.n_slots ? 0 : (w.slot < a.n_slots + a.n_wb ? 1 : 2);
+                const CUtensorMap *tmB = reg == 0 ? &tmB_cache : (reg == 1 ? &tmB_wb : &tmB_xp);
+                const int zc = w.slot - (reg == 0 ? 0 : (reg == 1 ? a.n_slots : a.n_slots + a.n_wb));
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int s = it % STAGES;
                     if (!mbar_wait(bar_empty + 8 * s, ((uint32_t)(it / STAGES) & 1u) ^ 1u)) {
@@ -349,8 +360,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // weight row scale of output column et of item i
         auto col_scale_of = [&](int i) -> float {
             const Item w = item_of(a, i);
-            const uint8_t *page = w.slot < a.n_slots ? a.pool_base + (size_t)w.slot * a.slot_stride
-                                                     : a.wb_base + (size_t)(w.slot - a.n_slots) * a.slot_stride;
+            const uint8_t *page = tile_page(a, w.slot);
             const float *ws = reinterpret_cast<const float *>(page + a.wscale_off);
             return ws[et < 128 ? w.r0 + et : w.r1 + (et - 128)];
         };
@@ -522,6 +532,60 @@ __global__ void __launch_bounds__(256) tc_hquant_kernel(const uint16_t *__restri
     }
 }
 
+// ---------------------------------------------------------------------------
+// FP8 copy of a 4-bit page for the tcgen05 path. Row r of w13 or w2 holds
+// E2M1 codes m with E8M0 block scales x_b (value m * 2^(x_b - 127)). With
+// x_max the row's largest block exponent, the copy stores
+// E4M3(m * 2^(x_b - x_max + 6)) and the row scale 2^(x_max - 133): E2M1 values
+// carry at most two significant bits, so every element whose block lies
+// within 14 binades of the row's largest is exact; smaller ones round toward
+// E4M3's subnormals (below 2^-15 of the row's largest element). One warp per
+// row; copies i < *xp_count, page-table entry xp_list[i].
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) tc_expand_fp4_kernel(const FfnArgs a) {
+    const int n_xp = *a.xp_count;
+    const int H = a.H, I = a.I, rows = 2 * I + H;
+    const PageLayout L8 = fp8_layout(H, I), L4 = mxfp4_layout(H, I);
+    const int lane = threadIdx.x & 31;
+    const long total = (long)n_xp * rows;
+    for (long wi = (long)blockIdx.x * 8 + (threadIdx.x >> 5); wi < total; wi += (long)gridDim.x * 8) {
+        const int x = (int)(wi / rows), r = (int)(wi % rows);
+        const uint8_t *src = page_addr(a, a.xp_list[x]);
+        uint8_t *dst = a.xp_base + (size_t)x * a.slot_stride;
+        const bool w13 = r < 2 * I;
+        const int rr = w13 ? r : r - 2 * I, K = w13 ? H : I, nb = K / 32;
+        const uint8_t *q = src + (w13 ? L4.w13 : L4.w2) + (size_t)rr * (K / 2);
+        const uint8_t *xs = src + (w13 ? L4.s13 : L4.s2) + (size_t)rr * nb;
+        uint8_t *o = dst + (w13 ? L8.w13 : L8.w2) + (size_t)rr * K;
+        int xm = 0;
+        for (int b = lane; b < nb; b += 32) xm = max(xm, (int)xs[b]);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) xm = max(xm, __shfl_xor_sync(0xffffffffu, xm, off));
+        for (int b = lane; b < nb; b += 32) {
+            const float f = ldexpf(1.0f, (int)xs[b] - xm + 6);
+            const uint4 v = *reinterpret_cast<const uint4 *>(q + 16 * b);  // 32 codes
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint32_t out[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint16_t c[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 e = e2m1x2_to_f32x2((uint8_t)(w[i] >> (8 * j)));
+                    c[j] = f32x2_to_e4m3x2(e.x * f, e.y * f);
+                }
+                out[2 * i] = (uint32_t)c[0] | ((uint32_t)c[1] << 16);
+                out[2 * i + 1] = (uint32_t)c[2] | ((uint32_t)c[3] << 16);
+            }
+            uint4 *o4 = reinterpret_cast<uint4 *>(o + 32 * b);
+            o4[0] = make_uint4(out[0], out[1], out[2], out[3]);
+            o4[1] = make_uint4(out[4], out[5], out[6], out[7]);
+        }
+        if (lane == 0)
+            reinterpret_cast<float *>(dst + (w13 ? L8.s13 : L8.s2))[rr] = ldexpf(1.0f, xm - 133);
+    }
+}
+
 // ---- host: tensor maps -------------------------------------------------------
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -576,7 +640,7 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     using namespace tc;
     const int H = args.H, I = args.I;
     const long A = b.A;
-    CUtensorMap mx, mh, m13c, m13w, m2c, m2w;
+    CUtensorMap mx, mh, m13c, m13w, m13x, m2c, m2w, m2x;
     const PageLayout L = fp8_layout(H, I);
     // the working-buffer / cache maps need a non-empty region to encode; an
     // absent region gets a one-slot map over the other base (never selected)
@@ -588,6 +652,11 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
               map_3d(&m13w, wb + L.w13, nw, 2 * (uint64_t)I, H, args.slot_stride) &&
               map_3d(&m2c, cache + L.w2, ns, (uint64_t)H, I, args.slot_stride) &&
               map_3d(&m2w, wb + L.w2, nw, (uint64_t)H, I, args.slot_stride);
+    // FP8 copies of 4-bit pages (a one-entry map over the cache when there is no such region)
+    const uint8_t *xp = args.max_xp > 0 ? args.xp_base : cache;
+    const uint64_t nx = args.max_xp > 0 ? (uint64_t)args.max_xp : ns;
+    ok = ok && map_3d(&m13x, xp + L.w13, nx, 2 * (uint64_t)I, H, args.slot_stride) &&
+         map_3d(&m2x, xp + L.w2, nx, (uint64_t)H, I, args.slot_stride);
     if (!ok) return PQE_ERR_UNSUPPORTED;
     static bool attr_set = false;
     static int sms = 0;
@@ -609,6 +678,8 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     g1.n_tiles = b.n_tiles;
     g1.n_nt = I / 128;
     g1.n_slots = args.n_slots;
+    g1.n_wb = args.n_wb;
+    g1.xp_base = args.xp_base;
     g1.K = H;
     g1.I = I;
     g1.out_cols = I;
@@ -621,7 +692,14 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     g1.out = b.h;
     g1.hmax = b.hmax;
     g1.status = args.status;
-    tc_gemm_kernel<<<grid1, THREADS, SMEM_BYTES, s>>>(mx, m13c, m13w, g1);
+    if (args.max_xp > 0) {
+        // FP8 copies of the 4-bit pages listed by the schedule (count on the device)
+        const long rows = (long)args.max_xp * (2 * I + H);
+        const long want = (rows + 7) / 8;
+        tc_expand_fp4_kernel<<<(unsigned)(want < 8L * sms ? want : 8L * sms), 256, 0, s>>>(args);
+        PQE_LAUNCH_CHECK();
+    }
+    tc_gemm_kernel<<<grid1, THREADS, SMEM_BYTES, s>>>(mx, m13c, m13w, m13x, g1);
     PQE_LAUNCH_CHECK();
     tc_hquant_kernel<<<max_tiles * ROW_CTAS, 256, 0, s>>>(b.h, I, b.tiles, b.n_tiles, b.hmax, b.hq, b.sh);
     PQE_LAUNCH_CHECK();
@@ -634,7 +712,7 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     g2.wscale_off = L.s2;
     g2.out = args.out_perm;
     g2.hmax = nullptr;
-    tc_gemm_kernel<<<grid2, THREADS, SMEM_BYTES, s>>>(mh, m2c, m2w, g2);
+    tc_gemm_kernel<<<grid2, THREADS, SMEM_BYTES, s>>>(mh, m2c, m2w, m2x, g2);
     PQE_LAUNCH_CHECK();
     return PQE_OK;
 }

@@ -233,12 +233,34 @@ def test_mixed_paths_one_call(cuda_lib, orc):
     g = np.random.default_rng(5)
     logits = g.standard_normal((T, E)).astype(np.float32)
     logits[:, 0] += 3.0   # expert 0 in almost every token
-    logits[:, 5] += 3.0   # the 4-bit expert too: it stays on the CUDA-core path
+    logits[:, 5] += 3.0   # the 4-bit expert too: its page is copied to FP8 for the tensor-core path
     res = run_layer(pqe, cfg, T, x, logits_np=logits, fmt_dev=pages.fmt_dev, pool=pages.pool)
     ids, gates = orc.topk_gates(logits, k)
     counts = np.bincount(ids.reshape(-1), minlength=E)
     assert counts[0] >= helpers.TC_MIN_ROWS and counts[5] >= helpers.TC_MIN_ROWS
     assert res["status"] == 0
+    check_tokens(orc, pages, cfg, x, ids, gates, res, np.arange(T, dtype=np.int32))
+
+
+@pytest.mark.parametrize("H,I", [(512, 256), (2048, 512)])
+def test_tensor_core_path_4bit_pages(cuda_lib, orc, H, I):
+    # most experts hold MXFP4 pages and batches of ~75 rows: each such page is
+    # rewritten as an FP8 page (power-of-two row scales) and multiplied on the
+    # tensor cores; one FP8 expert and one small 4-bit batch ride along
+    pqe = cuda_lib
+    E, k, T = 8, 2, 300
+    cfg = synth.small_config(E=E, H=H, I=I, k=k, T=T, cid=96)
+    fp4 = {0, 1, 2, 3, 4, 6, 7}
+    pages = Pages(pqe, orc, cfg, needed=set(range(E)), fp4=fp4)
+    x = synth.activations(cfg, T)
+    g = np.random.default_rng(H)
+    logits = g.standard_normal((T, E)).astype(np.float32)
+    logits[:, 7] -= 4.0  # expert 7: a handful of rows (weight-stream path)
+    res = run_layer(pqe, cfg, T, x, logits_np=logits, fmt_dev=pages.fmt_dev, pool=pages.pool)
+    ids, gates = orc.topk_gates(logits, k)
+    counts = np.bincount(ids.reshape(-1), minlength=E)
+    assert min(counts[e] for e in fp4 if e != 7) >= helpers.TC_MIN_ROWS and counts[7] < helpers.TC_MIN_ROWS
+    assert np.array_equal(res["ids"], ids) and res["status"] == 0
     check_tokens(orc, pages, cfg, x, ids, gates, res, np.arange(T, dtype=np.int32))
 
 
