@@ -490,7 +490,7 @@ int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *of
     args.out_perm = static_cast<uint16_t *>(out_perm);
     args.status = status;
     args.done13 = reinterpret_cast<uint32_t *>(wsb + w.done13);
-    if (w.tc) {
+    if (w.tc && expert_fmt) {  // all-FP8 layers (no format tags) need no copies
         args.xp_base = wsb + w.xp;
         args.xp_list = reinterpret_cast<int32_t *>(wsb + w.xp_list);
         args.xp_count = reinterpret_cast<int32_t *>(wsb + w.xp_count);
