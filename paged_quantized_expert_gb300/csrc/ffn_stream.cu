@@ -63,6 +63,7 @@ struct Geo {
     int stages;
     uint32_t stage_bytes;  // multiple of 128
     uint32_t red_off, sched_off, bar_off, smem_bytes;
+    uint32_t info_off;  // ExpertInfo array, in int32 words after the work-weight prefix
 };
 
 // per active expert, staged in shared memory once per launch
@@ -372,7 +373,7 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
     // loaded once by all threads in parallel (no dependent global loads later)
     const int n_act = __ldg(a.sched);
     int32_t *s_wpre = reinterpret_cast<int32_t *>(smem + g.sched_off);  // [n_act + 1]
-    ExpertInfo *s_info = reinterpret_cast<ExpertInfo *>(s_wpre + 1028);  // [n_act]
+    ExpertInfo *s_info = reinterpret_cast<ExpertInfo *>(s_wpre + g.info_off);  // [n_act]
     for (int i = threadIdx.x; i <= n_act; i += THREADS) s_wpre[i] = __ldg(a.wpre + i);
     for (int i = threadIdx.x; i < n_act; i += THREADS) {
         ExpertInfo f;
@@ -684,7 +685,8 @@ static int chunks_per_warp(int H, int I) {
     return c1 > c2 ? c1 : c2;
 }
 
-static bool geometry(int H, int I, Geo &g) {
+// shared memory of one CTA for experts E (the schedule area is sized by E)
+static bool geometry(int H, int I, int E, Geo &g) {
     const uint32_t s13_8 = 2u * PAIRS * pitch8(H) + 8u * PAIRS;
     const uint32_t s13_4 = 2u * PAIRS * pitch4(H / 2) + 2u * PAIRS * (H / 32);
     const uint32_t s2_8 = 16u * piece8(I) + 4u * ROWS2;
@@ -695,12 +697,13 @@ static bool geometry(int H, int I, Geo &g) {
     if (s2_4 > sb) sb = s2_4;
     sb = (sb + 127) / 128 * 128;
     const uint32_t redb = 2u * CONS * 32 * 16;
-    const uint32_t schedb = (uint32_t)round_up(4 * 1028 + sizeof(ExpertInfo) * 1024, 128);
+    g.info_off = (uint32_t)(E + 4);  // >= n_act + 1 prefix entries
+    const uint32_t schedb = (uint32_t)round_up(4 * (size_t)g.info_off + sizeof(ExpertInfo) * (size_t)E, 128);
     const uint32_t budget = 227 * 1024 - 1024;
     const uint32_t fixed = redb + schedb + 256;
     if (fixed + 2 * sb > budget) return false;
     int stages = (int)((budget - fixed) / sb);
-    if (stages > 5) stages = 5;
+    if (stages > 6) stages = 6;
     g.stages = stages;
     g.stage_bytes = sb;
     g.red_off = stages * sb;
@@ -716,12 +719,12 @@ bool stream_shape_ok(int H, int I) {
     st::Geo g;
     // phase 1: the 8 consumer warps split H/64 chunks; phase 2: two warps split I/64 chunks
     return H % st::ROWS2 == 0 && I % st::PAIRS == 0 && H % 64 == 0 && I % 64 == 0 &&
-           st::chunks_per_warp(H, I) <= st::NCH_MAX && st::geometry(H, I, g);
+           st::chunks_per_warp(H, I) <= st::NCH_MAX && st::geometry(H, I, 1024, g);
 }
 
 int launch_ffn_stream(const FfnArgs &args, cudaStream_t s) {
     st::Geo g;
-    if (!st::geometry(args.H, args.I, g)) return PQE_ERR_UNSUPPORTED;
+    if (!st::geometry(args.H, args.I, args.E, g)) return PQE_ERR_UNSUPPORTED;
     static int sms = 0;
     static uint32_t smem_set = 0;
     if (sms == 0) {
