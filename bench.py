@@ -526,13 +526,14 @@ def run_large(pqe, torch, device, steps_t1=64, steps_big=3, n_src=32):
         rec = {"tokens_per_s": T * steps / (ms / 1e3), "ms_per_step": ms / steps, "steps": steps,
                "mean_routed_experts": routed, "mean_misses": float(np.mean([m for _, m, _ in infos])),
                "ffn_ms": ffn_ms}
-        if T == 1:
-            gbs = (routed * (nb + 0.0) + T * H * 2 + T * k * H * 2) / (ffn_ms / 1e3) / 1e9
-            rec.update({"ffn_hbm_gbs": gbs, "ffn_frac_of_measured_hbm": gbs / peak_bw})
-        else:
-            tflops = 6.0 * T * k * H * I / (ffn_ms / 1e3) / 1e12
-            pk, kind = fp8_peak_tflops()
-            rec.update({"ffn_tflops": tflops, "ffn_frac_of_fp8_peak": tflops / pk, "fp8_peak_kind": kind})
+        # both bounds: the routed pages (plus x and out_perm) against HBM, the FLOPs against
+        # the FP8 peak; at T=4096 a batch is ~64 rows per expert, below the FP8 ridge (~290)
+        gbs = (routed * (nb + 0.0) + T * H * 2 + T * k * H * 2) / (ffn_ms / 1e3) / 1e9
+        tflops = 6.0 * T * k * H * I / (ffn_ms / 1e3) / 1e12
+        pk, kind = fp8_peak_tflops()
+        rec.update({"ffn_hbm_gbs": gbs, "ffn_frac_of_measured_hbm": gbs / peak_bw, "ffn_tflops": tflops,
+                    "ffn_frac_of_fp8_peak": tflops / pk, "fp8_peak_kind": kind,
+                    "bound": "hbm" if T * k / max(routed, 1.0) < 290 else "tensor"})
         out["T=%d" % T] = rec
     layer.close()
     out["huff_decode"] = huff_decode_rate(pqe, torch, device, comp, sizes_src, luts_src, H, I, nb)

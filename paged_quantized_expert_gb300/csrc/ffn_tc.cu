@@ -52,9 +52,11 @@ constexpr int ROW_CTAS = BM / 8;  // row kernels: CTAs of 8 warps per 128-row ti
 constexpr int SMEM_BAR_OFF = STAGES * STAGE_BYTES;
 constexpr int SMEM_TMEM_OFF = SMEM_BAR_OFF + 8 * (2 * STAGES + 4);
 constexpr int SMEM_SCALE_OFF = (SMEM_TMEM_OFF + 4 + 15) / 16 * 16;
-constexpr int EPI_PITCH = 80;  // bytes per row of an epilogue warp's store buffer (64 + 16: conflict-free)
-constexpr int SMEM_EPI_OFF = SMEM_SCALE_OFF + 8 * BN;  // after two column-scale buffers
-constexpr int SMEM_BYTES = SMEM_EPI_OFF + EPI_WARPS * 32 * EPI_PITCH + 1024;  // + alignment slack
+// store buffers: per epilogue warp 32 rows x 64 bytes (32 bf16 columns), laid out
+// with the 64-byte swizzle the output tensor maps use; 1024-byte aligned
+constexpr int EPI_BUF = 32 * 64;
+constexpr int SMEM_EPI_OFF = (SMEM_SCALE_OFF + 8 * BN + 1023) / 1024 * 1024;  // after two column-scale buffers
+constexpr int SMEM_BYTES = SMEM_EPI_OFF + EPI_WARPS * EPI_BUF + 1024;  // + alignment slack
 
 // instruction descriptor, kind::f8f6f4: D f32, A/B E4M3, both K-major, N, M
 constexpr uint32_t IDESC = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(BN >> 3) << 17) |
@@ -202,24 +204,42 @@ __device__ __forceinline__ Item item_of(const GemmArgs &a, int i) {
 }
 
 // A warp's 32 output rows x 32 bf16 columns (lane = row, packed = its 64 bytes)
-// go to global memory through the warp's padded shared buffer, so that each
-// store instruction writes 8 rows x 64 contiguous bytes (whole 32-byte sectors)
-// instead of 16 bytes in each of 32 rows. out: row 0 of the 32, ld: row stride
-// in elements; rows >= nrows are not written.
-__device__ __forceinline__ void store_rows32(uint8_t *buf, const uint32_t (&packed)[16], uint16_t *out, size_t ld,
-                                             int nrows, int lane) {
-    uint8_t *mine = buf + lane * EPI_PITCH;
+// go through the warp's shared buffer, in the 64-byte swizzle of the output
+// tensor map (16-byte piece v of row r at piece v ^ ((r >> 1) & 3)), which
+// also makes the warp's buffer writes conflict-free. A full group of 32 batch
+// rows leaves as one asynchronous TMA store at (col, row0); a partial group
+// (the end of an expert's segment) is stored row by row, 8 rows x 64 bytes per
+// instruction, so that no row of another expert is written.
+__device__ __forceinline__ void store_rows32(uint8_t *buf, const uint32_t (&packed)[16], const CUtensorMap *tm,
+                                             int col, int row0, uint16_t *out, size_t ld, int nrows, int lane) {
+    // the previous TMA store of this buffer has finished reading it
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    __syncwarp();
+    uint8_t *mine = buf + lane * 64;
+    const int sw = (lane >> 1) & 3;
 #pragma unroll
     for (int v = 0; v < 4; ++v)
-        *reinterpret_cast<uint4 *>(mine + 16 * v) =
+        *reinterpret_cast<uint4 *>(mine + 16 * (v ^ sw)) =
             make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+    if (nrows == 32) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // writes visible to the TMA unit
+        __syncwarp();
+        if (lane == 0) {
+            asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                             reinterpret_cast<uint64_t>(tm)),
+                         "r"(col), "r"(row0), "r"(smem_u32(buf))
+                         : "memory");
+            asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        return;
+    }
     __syncwarp();
 #pragma unroll
     for (int it = 0; it < 4; ++it) {
         const int pc = it * 32 + lane, r = pc >> 2, part = pc & 3;
         if (r < nrows)
             *reinterpret_cast<uint4 *>(out + (size_t)r * ld + 8 * part) =
-                *reinterpret_cast<const uint4 *>(buf + r * EPI_PITCH + 16 * part);
+                *reinterpret_cast<const uint4 *>(buf + r * 64 + 16 * (part ^ ((r >> 1) & 3)));
     }
     __syncwarp();
 }
@@ -244,7 +264,7 @@ __device__ __forceinline__ bool epi_all(bool v) {
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB_cache,
                    const __grid_constant__ CUtensorMap tmB_wb, const __grid_constant__ CUtensorMap tmB_xp,
-                   const GemmArgs a) {
+                   const __grid_constant__ CUtensorMap tmOut, const GemmArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const int n_items = *a.n_tiles * a.n_nt;
     if ((int)blockIdx.x >= n_items) return;
@@ -354,7 +374,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int half = (warp - 2) >> 2;  // which half of the tile's columns it finishes
         const int m = 32 * q + lane;
         const int et = threadIdx.x - 64;  // one output column per epilogue thread (BN of them)
-        uint8_t *ebuf = smem + SMEM_EPI_OFF + (warp - 2) * 32 * EPI_PITCH;  // this warp's store buffer
+        uint8_t *ebuf = smem + SMEM_EPI_OFF + (warp - 2) * EPI_BUF;  // this warp's store buffer
         static_assert(EPI_WARPS * 32 == BN, "one column scale per epilogue thread");
         static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
         // weight row scale of output column et of item i
@@ -409,7 +429,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         amax = fmaxf(amax, fmaxf(fabsf(bf16_to_f32(b0)), fabsf(bf16_to_f32(b1))));
                         packed[j / 2] = (uint32_t)b0 | ((uint32_t)b1 << 16);
                     }
-                    store_rows32(ebuf, packed, wrow + w.nt * 128 + c0, a.out_cols, nrows, lane);
+                    store_rows32(ebuf, packed, &tmOut, w.nt * 128 + c0, w.p0 + 32 * q, wrow + w.nt * 128 + c0,
+                                 a.out_cols, nrows, lane);
                 }
                 if (valid) atomicMax(a.hmax + p, __float_as_uint(amax));
             } else {
@@ -424,7 +445,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const float v1 = __uint_as_float(d[j + 1]) * rs * cs[c0 + j + 1];
                         packed[j / 2] = (uint32_t)f32_to_bf16_rn(v0) | ((uint32_t)f32_to_bf16_rn(v1) << 16);
                     }
-                    store_rows32(ebuf, packed, wrow + w.nt * 256 + c0, a.out_cols, nrows, lane);
+                    store_rows32(ebuf, packed, &tmOut, w.nt * 256 + c0, w.p0 + 32 * q, wrow + w.nt * 256 + c0,
+                                 a.out_cols, nrows, lane);
                 }
             }
             // this accumulator may be overwritten by the MMAs of item i + 2G
@@ -435,6 +457,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             epi_sync();
         }
     }
+    // every TMA store of an epilogue warp has completed before the CTA leaves
+    if (warp >= 2 && lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -618,6 +642,19 @@ static bool map_2d(CUtensorMap *m, const void *base, uint64_t rows, uint64_t col
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D [rows, cols] bf16 output, box [32 rows, 32 cols], 64-byte swizzle (epilogue TMA stores)
+static bool map_out(CUtensorMap *m, const void *base, uint64_t rows, uint64_t cols) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t es[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3-D [slots, rows, cols] uint8 with a slot stride, box [1, 128, 128]
 static bool map_3d(CUtensorMap *m, const void *base, uint64_t slots, uint64_t rows, uint64_t cols,
                    uint64_t slot_stride) {
@@ -640,7 +677,7 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     using namespace tc;
     const int H = args.H, I = args.I;
     const long A = b.A;
-    CUtensorMap mx, mh, m13c, m13w, m13x, m2c, m2w, m2x;
+    CUtensorMap mx, mh, m13c, m13w, m13x, m2c, m2w, m2x, mo1, mo2;
     const PageLayout L = fp8_layout(H, I);
     // the working-buffer / cache maps need a non-empty region to encode; an
     // absent region gets a one-slot map over the other base (never selected)
@@ -657,6 +694,7 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     const uint64_t nx = args.max_xp > 0 ? (uint64_t)args.max_xp : ns;
     ok = ok && map_3d(&m13x, xp + L.w13, nx, 2 * (uint64_t)I, H, args.slot_stride) &&
          map_3d(&m2x, xp + L.w2, nx, (uint64_t)H, I, args.slot_stride);
+    ok = ok && map_out(&mo1, b.h, (uint64_t)A, (uint64_t)I) && map_out(&mo2, args.out_perm, (uint64_t)A, (uint64_t)H);
     if (!ok) return PQE_ERR_UNSUPPORTED;
     static bool attr_set = false;
     static int sms = 0;
@@ -699,7 +737,7 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
         tc_expand_fp4_kernel<<<(unsigned)(want < 8L * sms ? want : 8L * sms), 256, 0, s>>>(args);
         PQE_LAUNCH_CHECK();
     }
-    tc_gemm_kernel<<<grid1, THREADS, SMEM_BYTES, s>>>(mx, m13c, m13w, m13x, g1);
+    tc_gemm_kernel<<<grid1, THREADS, SMEM_BYTES, s>>>(mx, m13c, m13w, m13x, mo1, g1);
     PQE_LAUNCH_CHECK();
     tc_hquant_kernel<<<max_tiles * ROW_CTAS, 256, 0, s>>>(b.h, I, b.tiles, b.n_tiles, b.hmax, b.hq, b.sh);
     PQE_LAUNCH_CHECK();
@@ -712,7 +750,7 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     g2.wscale_off = L.s2;
     g2.out = args.out_perm;
     g2.hmax = nullptr;
-    tc_gemm_kernel<<<grid2, THREADS, SMEM_BYTES, s>>>(mh, m2c, m2w, m2x, g2);
+    tc_gemm_kernel<<<grid2, THREADS, SMEM_BYTES, s>>>(mh, m2c, m2w, m2x, mo2, g2);
     PQE_LAUNCH_CHECK();
     return PQE_OK;
 }
