@@ -446,13 +446,44 @@ def run_batched(pqe, torch, device, host, steps, ws):
     peak, kind = fp8_peak_tflops()
     ffn_ms = float(np.mean(ffn))
     tflops = flops / (ffn_ms / 1e3) / 1e12
+    sweep = batch_sweep(pqe, torch, layer, cfg3, x, y, stream, side, peak)
     layer.close()
     return {"workload": "module-batched prefill layer (E=256, H=2048, I=512, top-8, T=16384, CACHE_SLOTS=32, "
                         "working buffer)",
             "tokens_per_s": T * steps / (ms / 1e3), "ms_per_step": ms / steps,
             "mean_staged_experts": float(np.mean(misses)),
             "ffn": {"ms": ffn_ms, "tflops": tflops, "peak_tflops": peak, "peak_kind": kind, "frac": tflops / peak,
-                    "bound": "tensor", "flops_per_step": flops}}
+                    "bound": "tensor", "flops_per_step": flops},
+            "batch_size_sweep": sweep}
+
+
+def batch_sweep(pqe, torch, layer, cfg, x, y, stream, side, peak, Ts=(2048, 4096, 8192, 16384), steps=4):
+    """Module-batch sizing: the FFN of the same layer at several accumulated
+    batch sizes T, beside the knee the library's sizer puts on the roofline."""
+    E, H, I, k = cfg.E, cfg.H, cfg.I, cfg.k
+    bw = peaks()[0]
+    out = {"T": [], "ffn_ms": [], "ffn_tflops": [], "ffn_frac_of_fp8_peak": [], "ffn_hbm_gbs": []}
+    nb = pqe.page_bytes(pqe.PQE_FMT_FP8, H, I)
+    for T in Ts:
+        tr = synth.RoutingTrace(cfg, T)
+        logits = [torch.from_numpy(tr.step(s)).to(x.device) for s in range(2)]
+        xs = [x[:T]]
+        layer.step(x[:T], y[:T], T, logits=logits[0], stream=stream, side_stream=side)  # warm-up
+        _, ffn, infos = _timed_steps(torch, layer, xs, y[:T], T, logits, steps, stream, side)
+        f_ms = float(np.mean(ffn))
+        routed = float(np.mean([r for r, _, _ in infos]))
+        out["T"].append(T)
+        out["ffn_ms"].append(f_ms)
+        tf = 6.0 * T * k * H * I / (f_ms / 1e3) / 1e12
+        out["ffn_tflops"].append(tf)
+        out["ffn_frac_of_fp8_peak"].append(tf / peak)
+        out["ffn_hbm_gbs"].append((routed * nb + T * H * 2 + T * k * H * 2) / (f_ms / 1e3) / 1e9)
+    best = max(out["ffn_tflops"])
+    out["measured_knee_T"] = next(T for T, tf in zip(out["T"], out["ffn_tflops"]) if tf >= 0.9 * best)
+    out["model_knee_T"] = pqe.pqe_module_batch_size(E, k, H, I, bw, peak, 64)
+    out["note"] = ("measured_knee_T: the smallest swept T within 90% of the best FFN TFLOP/s; model_knee_T: "
+                   "pqe_module_batch_size on the measured HBM and derived FP8 ceilings")
+    return out
 
 
 def _timed_steps(torch, layer, x, y, T, logits, steps, stream, side):

@@ -409,6 +409,20 @@ PQE_API int pqe_importance_step(double *m, const int32_t *ids, const float *gate
 /* Rank without an update: the top n_hi of m get FP8, the rest MXFP4. */
 PQE_API int pqe_rank_formats(const double *m, int E, int n_hi, uint8_t *fmt);
 
+/* Module-batch sizer: how many tokens to accumulate before running a layer so
+ * that its expert FFN turns from weight-bound to compute-bound ([MG] 3.中核と
+ * なる技術的要素: tokens are accumulated into large per-expert batches;
+ * 6.今後の調査・学習の方向性: choosing the batch size). On the roofline of the
+ * given ceilings (HBM GB/s, dense FP8 TFLOP/s), an expert with n rows does
+ * 6 n H I FLOP against its FP8 page (pqe_page_bytes) plus a = 2 H (1 + 1/k)
+ * bytes of activations per row (the token's bf16 x read once for its k rows,
+ * the row's bf16 out_perm); it is compute-bound from
+ *   n* = P * page / (6 H I BW - a P)   rows,
+ * so with tokens routed evenly over E experts, k per token, T* = E n* / k.
+ * Returns T* rounded up to a multiple of granule (>= 1), or 0 for invalid
+ * arguments or when no batch reaches the knee (6 H I BW <= a P). Host-only. */
+PQE_API int64_t pqe_module_batch_size(int E, int k, int H, int I, double hbm_gbs, double fp8_tflops, int granule);
+
 /* ------------------------------------------------------------------------
  * Layer runtime -- one MoE layer over its own slot pool, one call per step.
  * A step: moe_route -> moe_permute -> per-expert counts to the host (the one

@@ -106,6 +106,7 @@ _SIGS = {
     "slot_fill_compressed": (I32, [C.POINTER(pqe_pool), I32, P, SZ, P, SZ, P, P, P, P, P]),
     "pqe_importance_step": (I32, [P, P, P, I32, I32, I32, C.c_double, C.c_int64, I32, I32, P, P]),
     "pqe_rank_formats": (I32, [P, I32, I32, P]),
+    "pqe_module_batch_size": (C.c_int64, [I32, I32, I32, I32, C.c_double, C.c_double, I32]),
     "pqe_pool_slot_addr": (P, [C.POINTER(pqe_pool), I32]),
     "pqe_lru_device_bytes": (SZ, [I32, I32]),
     "pqe_lru_device_init": (I32, [P, I32, I32, P]),
@@ -390,6 +391,11 @@ def pqe_importance_step(m: torch.Tensor, ids: torch.Tensor, gates: torch.Tensor,
     _check("pqe_importance_step", lib().pqe_importance_step(_ptr(m), _ptr(ids), _ptr(gates), T, k, E, alpha, step,
                                                             every, n_hi, _ptr(fmt), _ptr(rr)))
     return bool(rr.item())
+
+
+def pqe_module_batch_size(E, k, H, I, hbm_gbs, fp8_tflops, granule=64) -> int:
+    """Tokens to accumulate so that the layer's FFN is compute-bound (0: no knee)."""
+    return int(lib().pqe_module_batch_size(E, k, H, I, float(hbm_gbs), float(fp8_tflops), granule))
 
 
 def pqe_rank_formats(m: torch.Tensor, n_hi: int, fmt: torch.Tensor):

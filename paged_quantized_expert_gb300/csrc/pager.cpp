@@ -6,6 +6,7 @@
 // (rand.pepabo.com), "エキスパート重みの階層ページング". Refills overlap compute:
 // MoE-Gen summary (aibr.jp), "3.中核となる技術的要素". Bit-width from
 // importance: PagedWeight commentary (spectral-agent.com), "技術的に面白い点".
+#include <cmath>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -226,6 +227,23 @@ int pqe_importance_step(double *m, const int32_t *ids, const float *gates, int T
     if (reranked) *reranked = rr ? 1 : 0;
     if (rr) return pqe_rank_formats(m, E, n_hi, fmt);
     return PQE_OK;
+}
+
+int64_t pqe_module_batch_size(int E, int k, int H, int I, double hbm_gbs, double fp8_tflops, int granule) {
+    if (E < 1 || k < 1 || k > E || pqe_page_bytes(PQE_FMT_FP8, H, I) == 0 || !(hbm_gbs > 0.0) ||
+        !(fp8_tflops > 0.0) || granule < 1)
+        return 0;
+    // per expert with n rows: 6 n H I FLOP against its FP8 page plus
+    // 2 H (1 + 1/k) bytes of activations per row (the token's bf16 x, read once
+    // for its k rows, and the row's bf16 out_perm)
+    const double P = fp8_tflops * 1e12, BW = hbm_gbs * 1e9;
+    const double page = (double)pqe_page_bytes(PQE_FMT_FP8, H, I);
+    const double den = 6.0 * H * I * BW - P * 2.0 * H * (1.0 + 1.0 / k);
+    if (!(den > 0.0)) return 0;  // the activations alone outrun the tensor cores: no knee
+    const double n_star = P * page / den;
+    const double t_star = std::ceil(n_star * E / k);
+    const int64_t g = granule;
+    return ((int64_t)t_star + g - 1) / g * g;
 }
 
 }  // extern "C"
