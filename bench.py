@@ -587,9 +587,15 @@ def run_mixed(pqe, torch, device, steps=12):
     host = torch.zeros((E, stride), dtype=torch.uint8)
     page = torch.zeros(stride, dtype=torch.uint8, device=device)
     p4 = torch.zeros(n4, dtype=torch.uint8, device=device)
+    nq = 16  # experts whose two pages feed the quality proxy
+    q8 = torch.zeros((nq, stride), dtype=torch.uint8, device=device)
+    q4 = torch.zeros((nq, n4), dtype=torch.uint8, device=device)
     for e in range(E):
         w13, w2 = synth.expert_weights(cfg, e)
         pqe.pqe_pack_fp8_page(torch.from_numpy(w13).to(device), torch.from_numpy(w2).to(device), H, I, page)
+        if e < nq:
+            q8[e].copy_(page)
+            pqe.pqe_pack_mxfp4_page(page, H, I, q4[e])
         if fmt[e] == 0:
             host[e].copy_(page)
         else:
@@ -622,12 +628,48 @@ def run_mixed(pqe, torch, device, steps=12):
     gbs = bpstep / (ffn_ms / 1e3) / 1e9
     tflops = 6.0 * T * k * H * I / (ffn_ms / 1e3) / 1e12
     pk, kind = fp8_peak_tflops()
+    quality = quality_proxy_rate(pqe, torch, device, cfg, q8, q4, m[:nq])
     return {"workload": "mixed per-expert precision layer (E=256, H=2048, I=512, top-8, T=4096; top 25% by "
                         "importance FP8, the rest MXFP4; all pages resident)",
             "n_fp8_experts": int((fmt == 0).sum()), "tokens_per_s": T * steps / (ms / 1e3), "ms_per_step": ms / steps,
             "steps": steps, "ffn_ms": ffn_ms, "ffn_hbm_gbs": gbs,
             "ffn_frac_of_measured_hbm": gbs / peaks()[0],
-            "ffn_tflops": tflops, "ffn_frac_of_fp8_peak": tflops / pk, "fp8_peak_kind": kind}
+            "ffn_tflops": tflops, "ffn_frac_of_fp8_peak": tflops / pk, "fp8_peak_kind": kind,
+            "quality_proxy": quality}
+
+
+def quality_proxy_rate(pqe, torch, device, cfg, q8, q4, m, n=64, reps=4):
+    """The 4-bit quality proxy on n sampled tokens per expert, timed per expert,
+    and the quality-aware ranking of the sampled experts (score m * q) against
+    the plain importance ranking."""
+    H, I = cfg.H, cfg.I
+    nq = q8.shape[0]
+    x = torch.from_numpy(synth.activations(cfg, n, 7).view(np.int16)).to(device)
+    ws = torch.zeros(pqe.pqe_quality_workspace_size(n, H, I), dtype=torch.uint8, device=device)
+    sums = torch.zeros((nq, 2), dtype=torch.float64, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    for e in range(nq):  # warm-up
+        pqe.pqe_expert_quant_error(x, n, q8[e], q4[e], H, I, sums[e], ws, status, stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        for e in range(nq):
+            pqe.pqe_expert_quant_error(x, n, q8[e], q4[e], H, I, sums[e], ws, status, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    s = sums.cpu().numpy()
+    q = np.sqrt(s[:, 0] / s[:, 1])
+    n_hi = nq // 4
+    f_plain = torch.zeros(nq, dtype=torch.uint8)
+    f_qual = torch.zeros(nq, dtype=torch.uint8)
+    pqe.pqe_rank_formats(torch.from_numpy(np.ascontiguousarray(m)), n_hi, f_plain)
+    pqe.pqe_rank_formats_quality(torch.from_numpy(np.ascontiguousarray(m)), torch.from_numpy(q), n_hi, f_qual)
+    return {"tokens_per_expert": n, "experts": nq, "us_per_expert": e0.elapsed_time(e1) * 1e3 / (reps * nq),
+            "rel_err_mean": float(q.mean()), "rel_err_min": float(q.min()), "rel_err_max": float(q.max()),
+            "fp8_set_changed": int((f_plain != f_qual).sum().item()) // 2, "status": int(status.item())}
 
 
 def huff_decode_rate(pqe, torch, device, comp_host, sizes, luts_host, H, I, nb, n_pages=8, reps=4):

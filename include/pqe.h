@@ -409,6 +409,28 @@ PQE_API int pqe_importance_step(double *m, const int32_t *ids, const float *gate
 /* Rank without an update: the top n_hi of m get FP8, the rest MXFP4. */
 PQE_API int pqe_rank_formats(const double *m, int E, int n_hi, uint8_t *fmt);
 
+/* Quality-aware ranking ([PW] 技術的に面白い点, the feedback loop that tracks
+ * quantisation error and adjusts bit widths; the scoring is a reading): expert
+ * e's score is m[e] * q[e], its importance times q[e], the relative output
+ * error of its 4-bit page measured on sampled tokens (pqe_expert_quant_error:
+ * sqrt(sums[0] / sums[1])); the top n_hi scores keep FP8, the rest MXFP4, ties
+ * to the lower id. m, q host double [E]; fmt host uint8 [E] out. Host-only. */
+PQE_API int pqe_rank_formats_quality(const double *m, const double *q, int E, int n_hi, uint8_t *fmt);
+
+/* The 4-bit quality proxy of one expert ([PW] 技術的に面白い点): runs n
+ * sampled tokens x (device bf16 [n, H], 16-byte aligned) through the expert's
+ * FP8 page and its MXFP4 page (device, in the layouts of pqe_page_layout),
+ * both through moe_paged_ffn exactly as the layer runs them, and writes
+ *   sums[0] = sum_t ||y4(x_t) - y8(x_t)||^2,  sums[1] = sum_t ||y8(x_t)||^2
+ * (device double [2], fp64, deterministic order) computed from the bf16
+ * outputs. Scratch: ws (device, 256-byte aligned) of at least
+ * pqe_quality_workspace_size(n, H, I) bytes; both pages are copied into it.
+ * status: device int32, as for moe_paged_ffn. Asynchronous on stream. */
+PQE_API size_t pqe_quality_workspace_size(int n, int H, int I);
+PQE_API int pqe_expert_quant_error(const void *x_bf16, int n, const uint8_t *page_fp8, const uint8_t *page_fp4,
+                                   int H, int I, double *sums, void *ws, size_t ws_bytes, int32_t *status,
+                                   void *stream);
+
 /* Module-batch sizer: how many tokens to accumulate before running a layer so
  * that its expert FFN turns from weight-bound to compute-bound ([MG] 3.中核と
  * なる技術的要素: tokens are accumulated into large per-expert batches;

@@ -74,6 +74,7 @@ def _declare(L):
         "orc_huff_encode": (C.c_int64, [P, C.c_int, C.c_int, C.c_int, P, P, P, P, P]),
         "orc_huff_decode": (C.c_int, [P, P, P, P, P, C.c_int, C.c_int, P]),
         "orc_rank_formats": (None, [P, C.c_int, C.c_int, P]),
+        "orc_rank_formats_quality": (None, [P, P, C.c_int, C.c_int, P]),
         "orc_importance_step": (C.c_int, [P, P, P, C.c_int, C.c_int, C.c_int, C.c_double,
                                           C.c_int64, C.c_int, C.c_int, P]),
     }
@@ -336,6 +337,30 @@ def rank_formats(m: np.ndarray, n_hi: int) -> np.ndarray:
     fmt = np.empty(m.shape[0], np.uint8)
     lib().orc_rank_formats(_p(m), m.shape[0], n_hi, _p(fmt))
     return fmt
+
+
+def rank_formats_quality(m: np.ndarray, q: np.ndarray, n_hi: int) -> np.ndarray:
+    """Top n_hi of m[e] * q[e] keep FP8 (0), the rest MXFP4 (1); ties to the lower id."""
+    m = _c(m, np.float64)
+    q = _c(q, np.float64)
+    fmt = np.empty(m.shape[0], np.uint8)
+    lib().orc_rank_formats_quality(_p(m), _p(q), m.shape[0], n_hi, _p(fmt))
+    return fmt
+
+
+def quant_error_sums(x_bf16: np.ndarray, w8: tuple, w4: tuple, I: int, fmt8: int = 0, fmt4: int = 1) -> tuple:
+    """The 4-bit quality proxy of one expert on tokens x: (sum ||y4 - y8||^2,
+    sum ||y8||^2) in fp64, y8 / y4 the expert's SwiGLU FFN from its FP8 page
+    (q13, s13, q2, s2) and its MXFP4 page (a13, x13, a2, x2). fmt8 / fmt4 name
+    the formats of the two pages (FP8 0, MXFP4 1)."""
+    n = x_bf16.shape[0]
+    ex = ExpertSet(2)
+    ex.set(0, fmt8, *w8)
+    ex.set(1, fmt4, *w4)
+    ones = np.ones((n, 1), np.float32)
+    y8 = moe_ffn(x_bf16, np.zeros((n, 1), np.int32), ones, ex, I)
+    y4 = moe_ffn(x_bf16, np.ones((n, 1), np.int32), ones, ex, I)
+    return float(np.sum((y4 - y8) ** 2)), float(np.sum(y8 ** 2))
 
 
 def importance_step(m: np.ndarray, ids: np.ndarray, gates_f32: np.ndarray, E: int, step: int,

@@ -755,6 +755,17 @@ EXPORT void orc_rank_formats(const double *m, int E, int n_hi, uint8_t *fmt)
     free(done);
 }
 
+/* Quality-aware ranking (the PagedWeight feedback loop, a reading): expert e's
+ * score is its importance m[e] times q[e], the relative output error its 4-bit
+ * page shows on sampled tokens; the top n_hi scores keep FP8 (ties: lower id). */
+EXPORT void orc_rank_formats_quality(const double *m, const double *q, int E, int n_hi, uint8_t *fmt)
+{
+    double *score = (double *)malloc((size_t)E * sizeof(double));
+    for (int e = 0; e < E; ++e) score[e] = m[e] * q[e];
+    orc_rank_formats(score, E, n_hi, fmt);
+    free(score);
+}
+
 /* returns 1 when the formats were re-ranked at this step */
 EXPORT int orc_importance_step(double *m, const int32_t *ids, const float *gates, int T, int k,
                                int E, double alpha, int64_t step, int every, int n_hi, uint8_t *fmt)

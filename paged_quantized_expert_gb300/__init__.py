@@ -107,6 +107,9 @@ _SIGS = {
     "pqe_importance_step": (I32, [P, P, P, I32, I32, I32, C.c_double, C.c_int64, I32, I32, P, P]),
     "pqe_rank_formats": (I32, [P, I32, I32, P]),
     "pqe_module_batch_size": (C.c_int64, [I32, I32, I32, I32, C.c_double, C.c_double, I32]),
+    "pqe_rank_formats_quality": (I32, [P, P, I32, I32, P]),
+    "pqe_quality_workspace_size": (SZ, [I32, I32, I32]),
+    "pqe_expert_quant_error": (I32, [P, I32, P, P, I32, I32, P, P, SZ, P, P]),
     "pqe_pool_slot_addr": (P, [C.POINTER(pqe_pool), I32]),
     "pqe_lru_device_bytes": (SZ, [I32, I32]),
     "pqe_lru_device_init": (I32, [P, I32, I32, P]),
@@ -391,6 +394,22 @@ def pqe_importance_step(m: torch.Tensor, ids: torch.Tensor, gates: torch.Tensor,
     _check("pqe_importance_step", lib().pqe_importance_step(_ptr(m), _ptr(ids), _ptr(gates), T, k, E, alpha, step,
                                                             every, n_hi, _ptr(fmt), _ptr(rr)))
     return bool(rr.item())
+
+
+def pqe_rank_formats_quality(m: torch.Tensor, q: torch.Tensor, n_hi: int, fmt: torch.Tensor):
+    """Top n_hi of importance x 4-bit error keep FP8 (host double m, q; host uint8 fmt)."""
+    _check("pqe_rank_formats_quality", lib().pqe_rank_formats_quality(_ptr(m), _ptr(q), m.numel(), n_hi, _ptr(fmt)))
+
+
+def pqe_quality_workspace_size(n: int, H: int, I: int) -> int:
+    return int(lib().pqe_quality_workspace_size(n, H, I))
+
+
+def pqe_expert_quant_error(x, n, page_fp8, page_fp4, H, I, sums, ws, status, stream=None):
+    """sums (device float64 [2]) <- (sum ||y4 - y8||^2, sum ||y8||^2) over the n tokens x."""
+    _check("pqe_expert_quant_error", lib().pqe_expert_quant_error(_ptr(x), n, _ptr(page_fp8), _ptr(page_fp4), H, I,
+                                                                  _ptr(sums), _ptr(ws), ws.numel(), _ptr(status),
+                                                                  _stream(stream)))
 
 
 def pqe_module_batch_size(E, k, H, I, hbm_gbs, fp8_tflops, granule=64) -> int:

@@ -211,6 +211,13 @@ int pqe_rank_formats(const double *m, int E, int n_hi, uint8_t *fmt) {
     return PQE_OK;
 }
 
+int pqe_rank_formats_quality(const double *m, const double *q, int E, int n_hi, uint8_t *fmt) {
+    if (!m || !q || !fmt || E < 1 || n_hi < 0) return PQE_ERR_INVALID_ARG;
+    std::vector<double> score(E);
+    for (int e = 0; e < E; ++e) score[e] = m[e] * q[e];
+    return pqe_rank_formats(score.data(), E, n_hi, fmt);
+}
+
 int pqe_importance_step(double *m, const int32_t *ids, const float *gates, int T, int k, int E, double alpha,
                         int64_t step, int every, int n_hi, uint8_t *fmt, int32_t *reranked) {
     if (!m || !fmt || E < 1 || T < 1 || k < 1 || every < 1 || (!ids && T) || (!gates && T))
