@@ -4,13 +4,16 @@
 // The weights of a routed expert are read once from its slot (expert-pager
 // article, rand.pepabo.com, "エキスパート重みの階層ページング"); for a handful of
 // tokens per expert the layer is bound by that stream from HBM. One CTA per SM
-// (cooperative launch). Warp 0 is the producer: its lanes pull the weight rows
-// of a unit (8 gate/up row pairs of w13, or 64 rows of w2, plus their scales)
-// into a ring of shared-memory stages with one cp.async.bulk per row, completing
-// on an mbarrier transaction count. Rows land with a small pad so that the
-// consumers' fragment loads are free of bank conflicts.
+// (cooperative launch). Warps 0-3 are the producers: their lanes pull the
+// weight rows of a unit (8 gate/up row pairs of w13, or 64 rows of w2, plus
+// their scales) into a ring of shared-memory stages with one cp.async.bulk per
+// row (2 KB pieces of w2), completing on an mbarrier transaction count. A
+// single warp issuing a stage's 2 KB copies reaches about 5.1 TB/s on GB300;
+// four warps sharing them reach 7.2 TB/s, above a device-to-device copy. Rows
+// land with a small pad so that the consumers' fragment loads are free of bank
+// conflicts.
 //
-// Warps 1-8 consume with mma.sync m16n8k16 (f16 inputs, fp32 accumulate): 16
+// Warps 4-11 consume with mma.sync m16n8k16 (f16 inputs, fp32 accumulate): 16
 // weight rows are the M side and up to 8 tokens the N side. FP8 E4M3 weights
 // convert exactly to f16 (one cvt per two weights); E2M1 weights too, with their
 // E8M0 block scale applied to each 32-column block's partial sum. Activations
@@ -39,7 +42,9 @@ namespace pqe {
 namespace st {
 
 constexpr int CONS = 8;                   // consumer warps
-constexpr int THREADS = 32 * (CONS + 1);  // + producer warp
+constexpr int PROD = 4;                   // producer warps
+constexpr int THREADS = 32 * (CONS + PROD);
+constexpr int MAX_STAGES = 4;
 constexpr int PAIRS = 8;                  // w13 gate/up row pairs per unit (16 weight rows)
 constexpr int ROWS2 = 64;                 // w2 rows per unit
 constexpr int NT = 8;                     // tokens per mma column group
@@ -385,7 +390,7 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < g.stages; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_full + 8 * s, PROD);
             mbar_init(bar_empty + 8 * s, CONS);
         }
         // partial-sum hand-off: phase 1 all warps -> one combining warp, phase 2
@@ -407,10 +412,15 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
     unit_range(s_wpre, n_act, per13, u13a, u13b);
     unit_range(s_wpre, n_act, per2, u2a, u2b);
 
-    if (warp == 0) {
-        // ---------------- producer: one bulk copy per weight row ----------------
+    if (warp < PROD) {
+        // ---------------- producers: one bulk copy per weight row ----------------
+        // copy c of a unit is issued by warp c % PROD, lane c / PROD: the copies of
+        // a stage leave from several warps at once, which a single warp's lanes
+        // cannot match (one warp's bulk copies are accepted one after another).
+        // Each warp posts the bytes of its own copies on the stage's barrier.
         int it = 0;
         bool ok = true;
+        const int c = warp + PROD * lane;
         for (int phase = 1; phase <= 2 && ok; ++phase) {
             const int ua = phase == 1 ? u13a : u2a, ub = phase == 1 ? u13b : u2b;
             const int per = phase == 1 ? per13 : per2;
@@ -431,39 +441,47 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
                     continue;
                 }
                 const uint8_t *page = page_addr(a, f.slot);
+                const bool fp8 = f.fmt == PQE_FMT_FP8;
+                const uint8_t *src = nullptr;
+                uint32_t doff = 0, bytes = 0;
                 if (phase == 1) {
-                    // stage rows 0..7: gate rows rb*8 .. +7; rows 8..15: the matching up rows
-                    // then the rows' scales: FP8 8 + 8 fp32, E2M1 [16][H/32] E8M0
-                    const bool fp8 = f.fmt == PQE_FMT_FP8;
+                    // copies 0..7: gate rows rb*8 .. +7; 8..15: the matching up rows;
+                    // 16, 17: the gate and the up rows' scales (FP8 8 fp32 each, E2M1 [8][H/32] E8M0)
                     const uint32_t rowb = fp8 ? (uint32_t)H : (uint32_t)H / 2, pitch = fp8 ? p13_8 : p13_4;
                     const uint32_t scb = fp8 ? 4u * PAIRS : (uint32_t)PAIRS * (H / 32);
                     const size_t scrow = fp8 ? 4 : (size_t)(H / 32);
-                    if (lane == 0) mbar_expect_tx(fb, 2u * PAIRS * rowb + 2u * scb);
-                    __syncwarp();
-                    if (lane < 2 * PAIRS) {
-                        const size_t wr = lane < PAIRS ? (size_t)rb * PAIRS + lane : (size_t)I + rb * PAIRS + (lane - PAIRS);
-                        bulk_g2s(dst + (uint32_t)lane * pitch, page + (fp8 ? L8.w13 : L4.w13) + wr * rowb, rowb, fb);
-                    } else if (lane < 2 * PAIRS + 2) {
-                        const int hf = lane - 2 * PAIRS;  // 0: the gate rows' scales, 1: the up rows'
+                    if (c < 2 * PAIRS) {
+                        const size_t wr = c < PAIRS ? (size_t)rb * PAIRS + c : (size_t)I + rb * PAIRS + (c - PAIRS);
+                        src = page + (fp8 ? L8.w13 : L4.w13) + wr * rowb;
+                        doff = (uint32_t)c * pitch;
+                        bytes = rowb;
+                    } else if (c < 2 * PAIRS + 2) {
+                        const int hf = c - 2 * PAIRS;
                         const size_t sr = (size_t)(hf ? I : 0) + (size_t)rb * PAIRS;
-                        bulk_g2s(dst + 2 * PAIRS * pitch + (uint32_t)hf * scb, page + (fp8 ? L8.s13 : L4.s13) + sr * scrow,
-                                 scb, fb);
+                        src = page + (fp8 ? L8.s13 : L4.s13) + sr * scrow;
+                        doff = 2 * PAIRS * pitch + (uint32_t)hf * scb;
+                        bytes = scb;
                     }
                 } else {
                     // pieces of 4 (FP8) or 8 (E2M1) contiguous rows, 4*I bytes each; then the scales
-                    const bool fp8 = f.fmt == PQE_FMT_FP8;
                     const int np = fp8 ? 16 : 8;
                     const uint32_t pb = 4u * I, pitch = fp8 ? q2_8 : q2_4;
                     const uint32_t scb = fp8 ? 4u * ROWS2 : (uint32_t)ROWS2 * (I / 32);
                     const uint8_t *w2 = page + (fp8 ? L8.w2 : L4.w2) + (size_t)rb * ROWS2 * (fp8 ? I : I / 2);
-                    if (lane == 0) mbar_expect_tx(fb, (uint32_t)np * pb + scb);
-                    __syncwarp();
-                    if (lane < np) bulk_g2s(dst + (uint32_t)lane * pitch, w2 + (size_t)lane * pb, pb, fb);
-                    else if (lane == np)
-                        bulk_g2s(dst + (uint32_t)np * pitch,
-                                 page + (fp8 ? L8.s2 + (size_t)rb * ROWS2 * 4 : L4.s2 + (size_t)rb * ROWS2 * (I / 32)),
-                                 scb, fb);
+                    if (c < np) {
+                        src = w2 + (size_t)c * pb;
+                        doff = (uint32_t)c * pitch;
+                        bytes = pb;
+                    } else if (c == np) {
+                        src = page + (fp8 ? L8.s2 + (size_t)rb * ROWS2 * 4 : L4.s2 + (size_t)rb * ROWS2 * (I / 32));
+                        doff = (uint32_t)np * pitch;
+                        bytes = scb;
+                    }
                 }
+                const uint32_t tot = __reduce_add_sync(0xffffffffu, bytes);
+                if (lane == 0) mbar_expect_tx(fb, tot);
+                __syncwarp();
+                if (bytes) bulk_g2s(dst + doff, src, bytes, fb);
             }
         }
         if (lane == 0) {
@@ -472,11 +490,11 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
             for (int j = (it > g.stages ? it - g.stages : 0); j < it; ++j)
                 mbar_wait(bar_full + 8 * (j % g.stages), (uint32_t)(j / g.stages) & 1u);
         }
-        return;  // the producer warp takes no part in the consumer barriers
+        return;  // the producer warps take no part in the consumer barriers
     }
 
     // ---------------- consumers ----------------
-    const int cw = warp - 1;
+    const int cw = warp - PROD;
     const int gq = lane >> 2, cq = lane & 3;                      // mma fragment coordinates
     float4 *red = reinterpret_cast<float4 *>(smem + g.red_off);  // [2][CONS][32] partial sums
     const uint32_t rfull1 = bar_empty + 8 * g.stages, rfree1 = rfull1 + 16, rfull2 = rfull1 + 32,
@@ -570,7 +588,7 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
     // for the whole grid
     __threadfence();
     cons_sync();
-    if (threadIdx.x == 32 && u13b > u13a) {
+    if (threadIdx.x == 32 * PROD && u13b > u13a) {
         for (int ea = u13a / per13; ea <= (u13b - 1) / per13; ++ea) {
             const int lo = max(u13a, ea * per13), hi = min(u13b, (ea + 1) * per13);
             const int groups = (s_info[ea].n + NT - 1) / NT;
@@ -673,7 +691,7 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
                 }
                 ++rc;
             }
-            if (!valid && threadIdx.x == 32 && n > 0 && !timed_out) atomicOr(a.status, PQE_STATUS_BAD_PAGE);
+            if (!valid && threadIdx.x == 32 * PROD && n > 0 && !timed_out) atomicOr(a.status, PQE_STATUS_BAD_PAGE);
         }
     }
     if (timed_out && lane == 0) atomicOr(a.status, PQE_STATUS_TIMEOUT);
@@ -703,7 +721,7 @@ static bool geometry(int H, int I, int E, Geo &g) {
     const uint32_t fixed = redb + schedb + 256;
     if (fixed + 2 * sb > budget) return false;
     int stages = (int)((budget - fixed) / sb);
-    if (stages > 6) stages = 6;
+    if (stages > MAX_STAGES) stages = MAX_STAGES;
     g.stages = stages;
     g.stage_bytes = sb;
     g.red_off = stages * sb;
