@@ -4,35 +4,41 @@
 // The weights of a routed expert are read once from its slot (expert-pager
 // article, rand.pepabo.com, "エキスパート重みの階層ページング"); for a handful of
 // tokens per expert the layer is bound by that stream from HBM. One CTA per SM
-// (cooperative launch). Warps 0-3 are the producers: their lanes pull the
-// weight rows of a unit (8 gate/up row pairs of w13, or 64 rows of w2, plus
-// their scales) into a ring of shared-memory stages with one cp.async.bulk per
-// row (2 KB pieces of w2), completing on an mbarrier transaction count. A
-// single warp issuing a stage's 2 KB copies reaches about 5.1 TB/s on GB300;
-// four warps sharing them reach 7.2 TB/s, above a device-to-device copy. Rows
-// land with a small pad so that the consumers' fragment loads are free of bank
-// conflicts.
+// (cooperative launch), twelve warps: three producers, one combiner, eight
+// consumers.
 //
-// Warps 4-11 consume with mma.sync m16n8k16 (f16 inputs, fp32 accumulate): 16
-// weight rows are the M side and up to 8 tokens the N side. FP8 E4M3 weights
-// convert exactly to f16 (one cvt per two weights); E2M1 weights too, with their
-// E8M0 block scale applied to each 32-column block's partial sum. Activations
-// (bf16 x, fp32 h) are brought to f16 with a power-of-two factor per token and
-// per warp slice of K, so products of bf16 x are exact (h is rounded to 11
-// bits) and all sums are fp32. Inside a warp's slice the K order is permuted
-// identically for weights and activations, which a dot product allows: each
-// lane reads contiguous weight bytes of its rows.
-// Phase 1 (w13 + SwiGLU -> h): the 8 warps split K of a 16-row unit; their
-// partial sums meet in a double-buffered shared-memory area and one warp (in
-// turn) applies the row scales and SwiGLU. Phase 2 (w2 -> out_perm): warp w
-// takes 16 of the unit's 64 rows and half of K; the halves meet the same way.
-// The hand-offs go through mbarriers, so a warp waits only for the partials it
-// combines or for a buffer two steps back, never for all warps at once. Each
-// CTA takes a contiguous range of units holding an equal share of the work,
-// weighting each expert by its
-// bytes and token groups. Phase 2 of an expert starts once all of its phase-1
-// work (in any CTA) is counted complete, with no grid-wide barrier; the
-// producer keeps streaming, so phase-2 weights are in flight meanwhile.
+// Producers (warps 0-2): their lanes pull the weight rows of a unit (8 gate/up
+// row pairs of w13, or 64 rows of w2, plus their scales) into a ring of
+// shared-memory stages with one cp.async.bulk per row (2 KB pieces of w2),
+// completing on an mbarrier transaction count. A single warp issuing a stage's
+// 2 KB copies reaches about 5.1 TB/s on GB300; several warps sharing them
+// reach 7 TB/s and more, above a device-to-device copy. Rows land with a small
+// pad so that the consumers' fragment loads are free of bank conflicts.
+//
+// Consumers (warps 4-11) multiply with mma.sync m16n8k16 (f16 inputs, fp32
+// accumulate): 16 weight rows are the M side and up to 8 tokens the N side.
+// FP8 E4M3 weights convert exactly to f16 (one cvt per two weights); E2M1
+// weights too, with their E8M0 block scale applied to each 32-column block's
+// partial sum. Activations (bf16 x, fp32 h) are brought to f16 with a
+// power-of-two factor per token and per warp slice of K, so products of bf16 x
+// are exact (h is rounded to 11 bits) and all sums are fp32. Inside a warp's
+// slice the K order is permuted identically for weights and activations, which
+// a dot product allows: each lane reads contiguous weight bytes of its rows.
+// Phase 1 (w13 + SwiGLU -> h): the 8 warps split K of a 16-row unit. Phase 2
+// (w2 -> out_perm): warp w takes 16 of the unit's 64 rows and half of K. Each
+// warp hands its partial sums, already multiplied by the rows' scales and the
+// tokens' factors (both linear), to a ring of four shared-memory slots.
+//
+// The combiner (warp 3) reads the slots in the same (unit, token group) order,
+// adds the partials and applies SwiGLU (phase 1) or pairs the K halves (phase
+// 2), and stores h / out_perm. A consumer waits only when the combiner is four
+// steps behind, never for the other consumers.
+//
+// Each CTA takes a contiguous range of units holding an equal share of the
+// work, weighting each expert by its bytes and token groups. Phase 2 of an
+// expert starts once all of its phase-1 work (in any CTA) is counted complete,
+// which each CTA's combiner publishes per expert: no grid-wide barrier, and
+// the producers keep streaming, so phase-2 weights are in flight meanwhile.
 // Every wait is bounded: on expiry PQE_STATUS_TIMEOUT is set and the waiter
 // moves on.
 #include "ffn_internal.cuh"
@@ -42,8 +48,11 @@ namespace pqe {
 namespace st {
 
 constexpr int CONS = 8;                   // consumer warps
-constexpr int PROD = 4;                   // producer warps
-constexpr int THREADS = 32 * (CONS + PROD);
+constexpr int PROD = 3;                   // producer warps 0 .. PROD-1
+constexpr int COMB = PROD;                // the combiner warp
+constexpr int CONS0 = PROD + 1;           // first consumer warp
+constexpr int THREADS = 32 * (CONS + PROD + 1);
+constexpr int RSLOTS = 4;                 // partial-sum slots between the consumers and the combiner
 constexpr int MAX_STAGES = 4;
 constexpr int PAIRS = 8;                  // w13 gate/up row pairs per unit (16 weight rows)
 constexpr int ROWS2 = 64;                 // w2 rows per unit
@@ -116,9 +125,6 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
-
-// barrier among the consumer warps only (named barrier 1)
-__device__ __forceinline__ void cons_sync() { asm volatile("bar.sync 1, %0;" ::"n"(CONS * 32) : "memory"); }
 
 // two E4M3 codes (low / high 16 bits of w) -> f16x2, exact
 __device__ __forceinline__ uint32_t f16x2_e4m3_lo(uint32_t w) {
@@ -393,16 +399,11 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
             mbar_init(bar_full + 8 * s, PROD);
             mbar_init(bar_empty + 8 * s, CONS);
         }
-        // partial-sum hand-off: phase 1 all warps -> one combining warp, phase 2
-        // pairs of warps (K halves of one m-tile); [buffer][slot]
+        // partial-sum slots: rfull[i] takes every consumer lane's arrival, rfree[i] the combiner's lanes
         const uint32_t rb = bar_empty + 8 * g.stages;
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(rb + 8 * b, CONS * 32);  // rfull1[b]
-            mbar_init(rb + 16 + 8 * b, 32);    // rfree1[b]
-            for (int m = 0; m < 4; ++m) {
-                mbar_init(rb + 32 + 8 * (4 * b + m), 32);  // rfull2[b][m]
-                mbar_init(rb + 96 + 8 * (4 * b + m), 32);  // rfree2[b][m]
-            }
+        for (int i = 0; i < RSLOTS; ++i) {
+            mbar_init(rb + 8 * i, CONS * 32);
+            mbar_init(rb + 8 * (RSLOTS + i), 32);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -493,26 +494,114 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
         return;  // the producer warps take no part in the consumer barriers
     }
 
-    // ---------------- consumers ----------------
-    const int cw = warp - PROD;
+    const uint32_t rfull = bar_empty + 8 * g.stages, rfree = rfull + 8 * RSLOTS;
+    float4 *red = reinterpret_cast<float4 *>(smem + g.red_off);  // [RSLOTS][CONS][32] partial sums
     const int gq = lane >> 2, cq = lane & 3;                      // mma fragment coordinates
-    float4 *red = reinterpret_cast<float4 *>(smem + g.red_off);  // [2][CONS][32] partial sums
-    const uint32_t rfull1 = bar_empty + 8 * g.stages, rfree1 = rfull1 + 16, rfull2 = rfull1 + 32,
-                   rfree2 = rfull1 + 96;
+
+    if (warp == COMB) {
+        // ---------------- combiner: partial sums -> h, out_perm ----------------
+        // takes the (unit, token group) steps in the consumers' order; slot rc % RSLOTS
+        int rc = 0;
+        bool timed_out = false;
+        // phase 1: lane (gq, cq) holds gate row j = rb*8 + gq and up row j for tokens 2cq, 2cq+1
+        for (int u = u13a; u < u13b; ++u) {
+            const ExpertInfo f = s_info[u / per13];
+            const int j = (u % per13) * PAIRS + gq;
+            for (int tg = 0; tg < f.n; tg += NT, ++rc) {
+                const int nt = min(NT, f.n - tg), sl = rc % RSLOTS;
+                if (!timed_out && !mbar_wait(rfull + 8 * sl, (uint32_t)(rc / RSLOTS) & 1u)) timed_out = true;
+                const float4 *rs = red + sl * CONS * 32;
+                float4 v = rs[lane];
+#pragma unroll
+                for (int w = 1; w < CONS; ++w) {
+                    const float4 t = rs[w * 32 + lane];
+                    v.x += t.x;
+                    v.y += t.y;
+                    v.z += t.z;
+                    v.w += t.w;
+                }
+                mbar_arrive(rfree + 8 * sl);
+                const int t0 = 2 * cq;
+                if (t0 < nt) a.h[(size_t)(f.p0 + tg + t0) * I + j] = silu(v.x) * v.z;
+                if (t0 + 1 < nt) a.h[(size_t)(f.p0 + tg + t0 + 1) * I + j] = silu(v.y) * v.w;
+            }
+        }
+        // this CTA's h rows are stored: publish its finished phase-1 work per expert;
+        // phase 2 waits per expert for the h rows it reads (done13), not for the whole grid
+        __threadfence();
+        __syncwarp();
+        if (lane == 0 && u13b > u13a) {
+            for (int ea = u13a / per13; ea <= (u13b - 1) / per13; ++ea) {
+                const int lo = max(u13a, ea * per13), hi = min(u13b, (ea + 1) * per13);
+                const int groups = (s_info[ea].n + NT - 1) / NT;
+                atomicAdd(a.done13 + s_info[ea].e, (uint32_t)((hi - lo) * groups));
+            }
+        }
+        // phase 2: warps mt and mt + 4 hold the two K halves of m-tile mt
+        for (int u = u2a; u < u2b; ++u) {
+            const ExpertInfo f = s_info[u / per2];
+            const int r0 = (u % per2) * ROWS2;
+            const bool fp8 = f.fmt == PQE_FMT_FP8;
+            for (int tg = 0; tg < f.n; tg += NT, ++rc) {
+                const int nt = min(NT, f.n - tg), sl = rc % RSLOTS;
+                if (!timed_out && !mbar_wait(rfull + 8 * sl, (uint32_t)(rc / RSLOTS) & 1u)) timed_out = true;
+                const float4 *rs = red + sl * CONS * 32;
+                float4 v[4];
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt) {
+                    const float4 p = rs[mt * 32 + lane], q = rs[(mt + 4) * 32 + lane];
+                    v[mt] = make_float4(p.x + q.x, p.y + q.y, p.z + q.z, p.w + q.w);
+                }
+                mbar_arrive(rfree + 8 * sl);
+                const int t0 = 2 * cq;
+#pragma unroll
+                for (int mt = 0; mt < 4; ++mt) {
+                    // unit rows of mma rows gq and gq + 8 in m-tile mt
+                    const int ra = fp8 ? 4 * gq + mt : 8 * gq + 2 * mt, rbw = fp8 ? ra + 32 : ra + 1;
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        if (t0 + i < nt) {
+                            uint16_t *o = a.out_perm + (size_t)(f.p0 + tg + t0 + i) * H + r0;
+                            o[ra] = f32_to_bf16_rn(i ? v[mt].y : v[mt].x);
+                            o[rbw] = f32_to_bf16_rn(i ? v[mt].w : v[mt].z);
+                        }
+                    }
+                }
+            }
+        }
+        if (timed_out && lane == 0) atomicOr(a.status, PQE_STATUS_TIMEOUT);
+        return;
+    }
+
+    // ---------------- consumers ----------------
+    // each (unit, token group) step ends with this warp's partials, already
+    // multiplied by the rows' scales and the tokens' activation factors, in slot
+    // rc % RSLOTS; only a slot the combiner has not yet read makes a warp wait
+    const int cw = warp - CONS0;
     int it = 0, rc = 0;
     bool timed_out = false;
     BFrag<NCH> bf;
     float inv = 1.0f;
     int b_a = -1, b_tg = -1;  // expert and token group bf holds
+    auto hand_off = [&](float s_lo, float s_hi, const float (&acc)[4]) {
+        // tokens 2cq, 2cq+1 sit in lanes 8cq, 8cq+4 of the fragment
+        const float i0 = __shfl_sync(0xffffffffu, inv, 8 * cq), i1 = __shfl_sync(0xffffffffu, inv, 8 * cq + 4);
+        const int sl = rc % RSLOTS;
+        if (!timed_out && !mbar_wait(rfree + 8 * sl, ((uint32_t)(rc / RSLOTS) & 1u) ^ 1u)) timed_out = true;
+        red[(sl * CONS + cw) * 32 + lane] =
+            make_float4(acc[0] * i0 * s_lo, acc[1] * i1 * s_lo, acc[2] * i0 * s_hi, acc[3] * i1 * s_hi);
+        mbar_arrive(rfull + 8 * sl);
+        ++rc;
+    };
 
-    // ---- phase 1: h[p, j] = SiLU(gate_j . x_t) * (up_j . x_t); warp cw owns chunks [c0, c0 + nch) of K
+    // ---- phase 1: gate_j . x_t and up_j . x_t over this warp's chunks [c0, c0 + nch) of K
     {
         const int NC = H / 64, c0 = cw * NC / CONS, nch = (cw + 1) * NC / CONS - c0;
         for (int u = u13a; u < u13b; ++u, ++it) {
             const int s = it % g.stages;
             const int ua = u / per13;
             const ExpertInfo f = s_info[ua];
-            const int rb = u % per13, p0 = f.p0, n = f.n;
+            const int p0 = f.p0, n = f.n;
             const bool fp8 = f.fmt == PQE_FMT_FP8;
             bool valid = f.valid != 0 && !timed_out;
             if (!timed_out && !mbar_wait(bar_full + 8 * s, (uint32_t)(it / g.stages) & 1u)) {
@@ -547,58 +636,14 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_empty + 8 * s);
                 }
-                // undo this warp's activation factors (tokens 2cq, 2cq+1 sit in lanes 8cq, 8cq+4)
-                const float i0 = __shfl_sync(0xffffffffu, inv, 8 * cq), i1 = __shfl_sync(0xffffffffu, inv, 8 * cq + 4);
-                // hand-off through buffer b: wait until the combine of step rc - 2 has
-                // read it, publish this warp's partials; only the combining warp waits
-                // for the others' (no barrier across all warps)
-                const int b = rc & 1;
-                const uint32_t ph = (uint32_t)(rc >> 1) & 1u;
-                float4 *rbuf = red + b * CONS * 32;
-                if (!timed_out && !mbar_wait(rfree1 + 8 * b, ph ^ 1u)) timed_out = true;
-                rbuf[cw * 32 + lane] = make_float4(acc[0] * i0, acc[1] * i1, acc[2] * i0, acc[3] * i1);
-                mbar_arrive(rfull1 + 8 * b);
-                if (cw == rc % CONS) {
-                    if (!timed_out && !mbar_wait(rfull1 + 8 * b, ph)) timed_out = true;
-                    // lane (gq, cq): gate row j = rb*8 + gq and up row j, tokens 2cq, 2cq+1
-                    float4 v = rbuf[lane];
-#pragma unroll
-                    for (int w2 = 1; w2 < CONS; ++w2) {
-                        const float4 t = rbuf[w2 * 32 + lane];
-                        v.x += t.x;
-                        v.y += t.y;
-                        v.z += t.z;
-                        v.w += t.w;
-                    }
-                    const int j = rb * PAIRS + gq;
-                    mbar_arrive(rfree1 + 8 * b);  // buffer b read
-                    const int t0 = 2 * cq;
-                    if (t0 < nt) a.h[(size_t)(p0 + tg + t0) * I + j] = valid ? silu(v.x * sg) * (v.z * su) : 0.0f;
-                    if (t0 + 1 < nt)
-                        a.h[(size_t)(p0 + tg + t0 + 1) * I + j] = valid ? silu(v.y * sg) * (v.w * su) : 0.0f;
-                }
-                ++rc;
+                hand_off(sg, su, acc);
             }
         }
     }
 
-    // ---- end of phase 1: this CTA's consumers meet (the partial-sum buffers are
-    // reused), then one thread publishes the CTA's finished phase-1 work per
-    // expert; phase 2 waits per expert for the h rows it reads (done13), not
-    // for the whole grid
-    __threadfence();
-    cons_sync();
-    if (threadIdx.x == 32 * PROD && u13b > u13a) {
-        for (int ea = u13a / per13; ea <= (u13b - 1) / per13; ++ea) {
-            const int lo = max(u13a, ea * per13), hi = min(u13b, (ea + 1) * per13);
-            const int groups = (s_info[ea].n + NT - 1) / NT;
-            atomicAdd(a.done13 + s_info[ea].e, (uint32_t)((hi - lo) * groups));
-        }
-    }
     int ready_a = -1;  // expert whose h rows this warp has seen complete
     b_a = -1;
     b_tg = -1;
-    rc = 0;  // phase 2 hand-off barriers count from their first phase
 
     // ---- phase 2: out_perm[p, r] = w2_r . h_p; warp cw: rows 16 mt .. 16 mt + 15 of the unit, half kh of K
     {
@@ -608,8 +653,7 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
             const int s = it % g.stages;
             const int ua = u / per2;
             const ExpertInfo f = s_info[ua];
-            const int rb = u % per2, p0 = f.p0, n = f.n;
-            const int r0 = rb * ROWS2;
+            const int p0 = f.p0, n = f.n;
             const bool fp8 = f.fmt == PQE_FMT_FP8;
             bool valid = f.valid != 0 && !timed_out;
             if (!timed_out && !mbar_wait(bar_full + 8 * s, (uint32_t)(it / g.stages) & 1u)) {
@@ -661,37 +705,9 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_empty + 8 * s);
                 }
-                const float i0 = __shfl_sync(0xffffffffu, inv, 8 * cq), i1 = __shfl_sync(0xffffffffu, inv, 8 * cq + 4);
-                float4 v = make_float4(acc[0] * i0, acc[1] * i1, acc[2] * i0, acc[3] * i1);
-                // the K half 1 warp of m-tile mt hands its partials to the K half 0 warp
-                const int b = rc & 1;
-                const uint32_t ph = (uint32_t)(rc >> 1) & 1u;
-                float4 *rbuf = red + b * CONS * 32;
-                if (kh == 1) {
-                    if (!timed_out && !mbar_wait(rfree2 + 8 * (4 * b + mt), ph ^ 1u)) timed_out = true;
-                    rbuf[mt * 32 + lane] = v;
-                    mbar_arrive(rfull2 + 8 * (4 * b + mt));
-                } else {
-                    if (!timed_out && !mbar_wait(rfull2 + 8 * (4 * b + mt), ph)) timed_out = true;
-                    const float4 t = rbuf[mt * 32 + lane];
-                    mbar_arrive(rfree2 + 8 * (4 * b + mt));
-                    v.x += t.x;
-                    v.y += t.y;
-                    v.z += t.z;
-                    v.w += t.w;
-                    const int t0 = 2 * cq;
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        if (t0 + i < nt) {
-                            uint16_t *o = a.out_perm + (size_t)(p0 + tg + t0 + i) * H + r0;
-                            o[ra] = f32_to_bf16_rn(valid ? (i ? v.y : v.x) * sa : 0.0f);
-                            o[rbw] = f32_to_bf16_rn(valid ? (i ? v.w : v.z) * sb : 0.0f);
-                        }
-                    }
-                }
-                ++rc;
+                hand_off(sa, sb, acc);
             }
-            if (!valid && threadIdx.x == 32 * PROD && n > 0 && !timed_out) atomicOr(a.status, PQE_STATUS_BAD_PAGE);
+            if (!valid && threadIdx.x == 32 * CONS0 && n > 0 && !timed_out) atomicOr(a.status, PQE_STATUS_BAD_PAGE);
         }
     }
     if (timed_out && lane == 0) atomicOr(a.status, PQE_STATUS_TIMEOUT);
@@ -714,7 +730,7 @@ static bool geometry(int H, int I, int E, Geo &g) {
     if (s2_8 > sb) sb = s2_8;
     if (s2_4 > sb) sb = s2_4;
     sb = (sb + 127) / 128 * 128;
-    const uint32_t redb = 2u * CONS * 32 * 16;
+    const uint32_t redb = (uint32_t)RSLOTS * CONS * 32 * 16;
     g.info_off = (uint32_t)(E + 4);  // >= n_act + 1 prefix entries
     const uint32_t schedb = (uint32_t)round_up(4 * (size_t)g.info_off + sizeof(ExpertInfo) * (size_t)E, 128);
     const uint32_t budget = 227 * 1024 - 1024;
@@ -727,7 +743,7 @@ static bool geometry(int H, int I, int E, Geo &g) {
     g.red_off = stages * sb;
     g.sched_off = g.red_off + redb;
     g.bar_off = g.sched_off + schedb;
-    g.smem_bytes = g.bar_off + 16 * stages + 160;
+    g.smem_bytes = g.bar_off + 16 * stages + 16 * RSLOTS;
     return true;
 }
 
