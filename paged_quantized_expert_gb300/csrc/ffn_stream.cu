@@ -85,6 +85,31 @@ struct ExpertInfo {
     int e, p0, n, slot, fmt, valid;
 };
 
+// position in the stage ring: stage s and the parity of its current fill
+struct RingPos {
+    int s = 0;
+    uint32_t ph = 0;
+    __device__ __forceinline__ void next(int stages) {
+        if (++s == stages) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
+// position in a range of units: schedule entry ea and unit rb of its `per`
+// (one division at the start, none per unit)
+struct UnitPos {
+    int ea, rb;
+    __device__ __forceinline__ UnitPos(int u, int per) : ea(u / per), rb(u % per) {}
+    __device__ __forceinline__ void next(int per) {
+        if (++rb == per) {
+            rb = 0;
+            ++ea;
+        }
+    }
+};
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -420,21 +445,23 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
         // cannot match (one warp's bulk copies are accepted one after another).
         // Each warp posts the bytes of its own copies on the stage's barrier.
         int it = 0;
+        RingPos rp;
         bool ok = true;
         const int c = warp + PROD * lane;
         for (int phase = 1; phase <= 2 && ok; ++phase) {
             const int ua = phase == 1 ? u13a : u2a, ub = phase == 1 ? u13b : u2b;
             const int per = phase == 1 ? per13 : per2;
-            for (int u = ua; u < ub; ++u, ++it) {
-                const int s = it % g.stages;
+            UnitPos up(ua, per);
+            for (int u = ua; u < ub; ++u, ++it, rp.next(g.stages), up.next(per)) {
+                const int s = rp.s;
                 int w_ok = 1;
-                if (lane == 0) w_ok = mbar_wait(bar_empty + 8 * s, ((uint32_t)(it / g.stages) & 1u) ^ 1u) ? 1 : 0;
+                if (lane == 0) w_ok = mbar_wait(bar_empty + 8 * s, rp.ph ^ 1u) ? 1 : 0;
                 if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
                     ok = false;
                     break;
                 }
-                const ExpertInfo f = s_info[u / per];
-                const int rb = u % per;
+                const ExpertInfo f = s_info[up.ea];
+                const int rb = up.rb;
                 const uint32_t dst = sbase + (uint32_t)s * g.stage_bytes;
                 const uint32_t fb = bar_full + 8 * s;
                 if (!f.valid) {
@@ -504,9 +531,10 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
         int rc = 0;
         bool timed_out = false;
         // phase 1: lane (gq, cq) holds gate row j = rb*8 + gq and up row j for tokens 2cq, 2cq+1
-        for (int u = u13a; u < u13b; ++u) {
-            const ExpertInfo f = s_info[u / per13];
-            const int j = (u % per13) * PAIRS + gq;
+        UnitPos up1(u13a, per13);
+        for (int u = u13a; u < u13b; ++u, up1.next(per13)) {
+            const ExpertInfo f = s_info[up1.ea];
+            const int j = up1.rb * PAIRS + gq;
             for (int tg = 0; tg < f.n; tg += NT, ++rc) {
                 const int nt = min(NT, f.n - tg), sl = rc % RSLOTS;
                 if (!timed_out && !mbar_wait(rfull + 8 * sl, (uint32_t)(rc / RSLOTS) & 1u)) timed_out = true;
@@ -538,9 +566,10 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
             }
         }
         // phase 2: warps mt and mt + 4 hold the two K halves of m-tile mt
-        for (int u = u2a; u < u2b; ++u) {
-            const ExpertInfo f = s_info[u / per2];
-            const int r0 = (u % per2) * ROWS2;
+        UnitPos up2(u2a, per2);
+        for (int u = u2a; u < u2b; ++u, up2.next(per2)) {
+            const ExpertInfo f = s_info[up2.ea];
+            const int r0 = up2.rb * ROWS2;
             const bool fp8 = f.fmt == PQE_FMT_FP8;
             for (int tg = 0; tg < f.n; tg += NT, ++rc) {
                 const int nt = min(NT, f.n - tg), sl = rc % RSLOTS;
@@ -578,7 +607,8 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
     // multiplied by the rows' scales and the tokens' activation factors, in slot
     // rc % RSLOTS; only a slot the combiner has not yet read makes a warp wait
     const int cw = warp - CONS0;
-    int it = 0, rc = 0;
+    RingPos rp;
+    int rc = 0;
     bool timed_out = false;
     BFrag<NCH> bf;
     float inv = 1.0f;
@@ -597,14 +627,15 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
     // ---- phase 1: gate_j . x_t and up_j . x_t over this warp's chunks [c0, c0 + nch) of K
     {
         const int NC = H / 64, c0 = cw * NC / CONS, nch = (cw + 1) * NC / CONS - c0;
-        for (int u = u13a; u < u13b; ++u, ++it) {
-            const int s = it % g.stages;
-            const int ua = u / per13;
+        UnitPos up(u13a, per13);
+        for (int u = u13a; u < u13b; ++u, rp.next(g.stages), up.next(per13)) {
+            const int s = rp.s;
+            const int ua = up.ea;
             const ExpertInfo f = s_info[ua];
             const int p0 = f.p0, n = f.n;
             const bool fp8 = f.fmt == PQE_FMT_FP8;
             bool valid = f.valid != 0 && !timed_out;
-            if (!timed_out && !mbar_wait(bar_full + 8 * s, (uint32_t)(it / g.stages) & 1u)) {
+            if (!timed_out && !mbar_wait(bar_full + 8 * s, rp.ph)) {
                 valid = false;
                 timed_out = true;
             }
@@ -649,14 +680,15 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
     {
         const int mt = cw & 3, kh = cw >> 2;
         const int NC = I / 64, c0 = kh * NC / 2, nch = (kh + 1) * NC / 2 - c0;
-        for (int u = u2a; u < u2b; ++u, ++it) {
-            const int s = it % g.stages;
-            const int ua = u / per2;
+        UnitPos up(u2a, per2);
+        for (int u = u2a; u < u2b; ++u, rp.next(g.stages), up.next(per2)) {
+            const int s = rp.s;
+            const int ua = up.ea;
             const ExpertInfo f = s_info[ua];
             const int p0 = f.p0, n = f.n;
             const bool fp8 = f.fmt == PQE_FMT_FP8;
             bool valid = f.valid != 0 && !timed_out;
-            if (!timed_out && !mbar_wait(bar_full + 8 * s, (uint32_t)(it / g.stages) & 1u)) {
+            if (!timed_out && !mbar_wait(bar_full + 8 * s, rp.ph)) {
                 valid = false;
                 timed_out = true;
             }
