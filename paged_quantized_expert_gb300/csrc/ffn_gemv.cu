@@ -443,6 +443,41 @@ static FfnWs ffn_ws_layout(int T, int k, int E, int H, int I) {
     return w;
 }
 
+// The side stream of this host thread on the current device, with its fork and
+// join events (created on first use; one set per thread, so calls from several
+// host threads never share them).
+struct SideStream {
+    int dev = -1;
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+
+static int side_stream(SideStream *&out) {
+    thread_local SideStream ss[16];
+    int dev = 0;
+    PQE_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 16) return PQE_ERR_UNSUPPORTED;
+    SideStream &x = ss[dev];
+    if (x.s == nullptr) {
+        PQE_CUDA_TRY(cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking));
+        PQE_CUDA_TRY(cudaEventCreateWithFlags(&x.fork, cudaEventDisableTiming));
+        PQE_CUDA_TRY(cudaEventCreateWithFlags(&x.join, cudaEventDisableTiming));
+        x.dev = dev;
+    }
+    out = &x;
+    return PQE_OK;
+}
+
+static int sm_count() {
+    static int sms = 0;
+    if (sms == 0) {
+        int dev = 0;
+        PQE_CUDA_TRY(cudaGetDevice(&dev));
+        PQE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    }
+    return sms;
+}
+
 }  // namespace pqe
 
 using namespace pqe;
@@ -503,7 +538,19 @@ int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *of
     int32_t *n_tiles = reinterpret_cast<int32_t *>(wsb + w.n_tiles);
     ffn_schedule_kernel<<<1, 1024, 0, s>>>(args, w.tc ? TC_MIN_ROWS : 0, tiles, n_tiles);
     PQE_LAUNCH_CHECK();
-    int rc = stream_shape_ok(pool->H, pool->I) ? launch_ffn_stream(args, s) : launch_ffn_gemv(args, max_active, s);
+    const bool stream_path = stream_shape_ok(pool->H, pool->I);
+    // decode-sized step: the tensor-core batches run beside the weight stream
+    const bool side = stream_path && w.tc && A >= TC_MIN_ROWS && A <= (long)DECODE_ROWS_PER_EXPERT * E &&
+                      sm_count() > 2 * TC_SIDE_SMS;
+    SideStream *ss = nullptr;
+    if (side) {
+        const int r = side_stream(ss);
+        if (r != PQE_OK) return r;
+        PQE_CUDA_TRY(cudaEventRecord(ss->fork, s));
+        PQE_CUDA_TRY(cudaStreamWaitEvent(ss->s, ss->fork, 0));
+    }
+    int rc = stream_path ? launch_ffn_stream(args, s, side ? sm_count() - TC_SIDE_SMS : 0)
+                         : launch_ffn_gemv(args, max_active, s);
     if (rc != PQE_OK || !w.tc) return rc;
     TcBuffers b{};
     b.A = A;
@@ -515,7 +562,13 @@ int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *of
     b.hmax = reinterpret_cast<uint32_t *>(wsb + w.hmax);
     b.hq = wsb + w.hq;
     b.sh = reinterpret_cast<float *>(wsb + w.sh);
-    return launch_ffn_tc(args, b, w.max_tiles, s);
+    if (!side) return launch_ffn_tc(args, b, w.max_tiles, s);
+    rc = launch_ffn_tc(args, b, w.max_tiles, ss->s, TC_SIDE_SMS);
+    // the join is recorded even after a failed launch, so the caller's stream never
+    // waits on a fork that was left open
+    PQE_CUDA_TRY(cudaEventRecord(ss->join, ss->s));
+    PQE_CUDA_TRY(cudaStreamWaitEvent(s, ss->join, 0));
+    return rc;
 }
 
 }  // extern "C"

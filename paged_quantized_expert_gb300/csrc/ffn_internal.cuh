@@ -56,10 +56,22 @@ struct TcBuffers {
 // to here is that of reading the weights once
 constexpr int TC_MIN_ROWS = 9;
 
+// Decode-sized steps (at most DECODE_ROWS_PER_EXPERT rows per routed expert on
+// average) run the tensor-core batches beside the weight stream: the stream
+// kernel leaves TC_SIDE_SMS SMs free and the tensor-core kernels, on a side
+// stream, use at most that many persistent CTAs. The weight stream is bound
+// per SM by its consumers, so it gives up about TC_SIDE_SMS / SMs of its rate,
+// while the tensor-core chain (a few latency-bound launches) no longer adds to
+// the step.
+constexpr int TC_SIDE_SMS = 16;
+constexpr int DECODE_ROWS_PER_EXPERT = 4;
+
 bool tc_shape_ok(int H, int I);
 bool stream_shape_ok(int H, int I);
-int launch_ffn_stream(const FfnArgs &args, cudaStream_t s);
+// grid: CTAs of the persistent stream kernel, 0 = one per SM
+int launch_ffn_stream(const FfnArgs &args, cudaStream_t s, int grid = 0);
 int launch_ffn_gemv(const FfnArgs &args, int max_active, cudaStream_t s);
-int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaStream_t s);
+// sm_cap: at most this many persistent GEMM CTAs, 0 = one per SM
+int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaStream_t s, int sm_cap = 0);
 
 }  // namespace pqe

@@ -788,7 +788,7 @@ bool stream_shape_ok(int H, int I) {
            st::chunks_per_warp(H, I) <= st::NCH_MAX && st::geometry(H, I, 1024, g);
 }
 
-int launch_ffn_stream(const FfnArgs &args, cudaStream_t s) {
+int launch_ffn_stream(const FfnArgs &args, cudaStream_t s, int grid) {
     st::Geo g;
     if (!st::geometry(args.H, args.I, args.E, g)) return PQE_ERR_UNSUPPORTED;
     static int sms = 0;
@@ -805,10 +805,11 @@ int launch_ffn_stream(const FfnArgs &args, cudaStream_t s) {
                                           (int)g.smem_bytes));
         smem_set = g.smem_bytes;
     }
-    // cooperative: all CTAs resident at once (the grid barrier between the phases);
-    // the attribute also holds when the launch is captured into a graph
+    // cooperative: all CTAs resident at once (phase 2 of an expert waits for
+    // phase-1 work of other CTAs); the attribute also holds when the launch is
+    // captured into a graph
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(sms);
+    cfg.gridDim = dim3(grid > 0 && grid < sms ? grid : sms);
     cfg.blockDim = dim3(st::THREADS);
     cfg.dynamicSmemBytes = g.smem_bytes;
     cfg.stream = s;

@@ -673,7 +673,7 @@ static bool map_3d(CUtensorMap *m, const void *base, uint64_t slots, uint64_t ro
 
 bool tc_shape_ok(int H, int I) { return H % 256 == 0 && I % 128 == 0 && H >= 256 && I >= 128; }
 
-int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaStream_t s) {
+int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaStream_t s, int sm_cap) {
     using namespace tc;
     const int H = args.H, I = args.I;
     const long A = b.A;
@@ -705,9 +705,10 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
         PQE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
         attr_set = true;
     }
-    // persistent grids: one CTA per SM, at most one per work item
+    // persistent grids: one CTA per SM (or per SM of the share given), at most one per work item
+    const int cap = sm_cap > 0 && sm_cap < sms ? sm_cap : sms;
     const int items1 = max_tiles * (I / 128), items2 = max_tiles * (H / 256);
-    const int grid1 = items1 < sms ? items1 : sms, grid2 = items2 < sms ? items2 : sms;
+    const int grid1 = items1 < cap ? items1 : cap, grid2 = items2 < cap ? items2 : cap;
     tc_gather_quant_kernel<<<max_tiles * ROW_CTAS, 256, 0, s>>>(args.x, args.perm_src, args.k, H, b.tiles, b.n_tiles, b.xq,
                                                      b.sx, b.hmax);
     PQE_LAUNCH_CHECK();
