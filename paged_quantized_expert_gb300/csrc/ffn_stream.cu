@@ -108,6 +108,12 @@ struct UnitPos {
             ++ea;
         }
     }
+    __device__ __forceinline__ void prev(int per) {
+        if (rb-- == 0) {
+            rb = per - 1;
+            --ea;
+        }
+    }
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -451,8 +457,10 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
         for (int phase = 1; phase <= 2 && ok; ++phase) {
             const int ua = phase == 1 ? u13a : u2a, ub = phase == 1 ? u13b : u2b;
             const int per = phase == 1 ? per13 : per2;
-            UnitPos up(ua, per);
-            for (int u = ua; u < ub; ++u, ++it, rp.next(g.stages), up.next(per)) {
+            // phase 2 runs backwards (see the consumers)
+            const bool fwd = phase == 1;
+            UnitPos up(fwd ? ua : ub - 1, per);
+            for (int i = ua; i < ub; ++i, ++it, rp.next(g.stages), fwd ? up.next(per) : up.prev(per)) {
                 const int s = rp.s;
                 int w_ok = 1;
                 if (lane == 0) w_ok = mbar_wait(bar_empty + 8 * s, rp.ph ^ 1u) ? 1 : 0;
@@ -530,8 +538,12 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
         // takes the (unit, token group) steps in the consumers' order; slot rc % RSLOTS
         int rc = 0;
         bool timed_out = false;
-        // phase 1: lane (gq, cq) holds gate row j = rb*8 + gq and up row j for tokens 2cq, 2cq+1
+        // phase 1: lane (gq, cq) holds gate row j = rb*8 + gq and up row j for tokens 2cq, 2cq+1.
+        // Once this CTA's units of an expert are combined, their count is published
+        // (after the h stores are visible); phase 2 of the expert waits for the
+        // counts of all CTAs (done13), not for the whole grid
         UnitPos up1(u13a, per13);
+        int run = 0;  // units of the current expert combined here
         for (int u = u13a; u < u13b; ++u, up1.next(per13)) {
             const ExpertInfo f = s_info[up1.ea];
             const int j = up1.rb * PAIRS + gq;
@@ -553,21 +565,17 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
                 if (t0 < nt) a.h[(size_t)(f.p0 + tg + t0) * I + j] = silu(v.x) * v.z;
                 if (t0 + 1 < nt) a.h[(size_t)(f.p0 + tg + t0 + 1) * I + j] = silu(v.y) * v.w;
             }
-        }
-        // this CTA's h rows are stored: publish its finished phase-1 work per expert;
-        // phase 2 waits per expert for the h rows it reads (done13), not for the whole grid
-        __threadfence();
-        __syncwarp();
-        if (lane == 0 && u13b > u13a) {
-            for (int ea = u13a / per13; ea <= (u13b - 1) / per13; ++ea) {
-                const int lo = max(u13a, ea * per13), hi = min(u13b, (ea + 1) * per13);
-                const int groups = (s_info[ea].n + NT - 1) / NT;
-                atomicAdd(a.done13 + s_info[ea].e, (uint32_t)((hi - lo) * groups));
+            ++run;
+            if (u + 1 == u13b || up1.rb + 1 == per13) {
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atomicAdd(a.done13 + f.e, (uint32_t)(run * ((f.n + NT - 1) / NT)));
+                run = 0;
             }
         }
         // phase 2: warps mt and mt + 4 hold the two K halves of m-tile mt
-        UnitPos up2(u2a, per2);
-        for (int u = u2a; u < u2b; ++u, up2.next(per2)) {
+        UnitPos up2(u2b - 1, per2);
+        for (int u = u2b - 1; u >= u2a; --u, up2.prev(per2)) {
             const ExpertInfo f = s_info[up2.ea];
             const int r0 = up2.rb * ROWS2;
             const bool fp8 = f.fmt == PQE_FMT_FP8;
@@ -680,8 +688,11 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
     {
         const int mt = cw & 3, kh = cw >> 2;
         const int NC = I / 64, c0 = kh * NC / 2, nch = (kh + 1) * NC / 2 - c0;
-        UnitPos up(u2a, per2);
-        for (int u = u2a; u < u2b; ++u, rp.next(g.stages), up.next(per2)) {
+        // backwards through this CTA's units: it starts with the expert it shares
+        // with the next CTA, whose phase-1 share of it that CTA did first, and ends
+        // with the one it shares with the previous CTA, whose share came last there
+        UnitPos up(u2b - 1, per2);
+        for (int u = u2b - 1; u >= u2a; --u, rp.next(g.stages), up.prev(per2)) {
             const int s = rp.s;
             const int ua = up.ea;
             const ExpertInfo f = s_info[ua];
