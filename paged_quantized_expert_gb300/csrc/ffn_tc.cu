@@ -51,12 +51,12 @@ constexpr int ROW_CTAS = BM / 8;  // row kernels: CTAs of 8 warps per 128-row ti
 // smem: stages | full[S] empty[S] tfull[2] tempty[2] | tmem base | column scales [2][BN] | store buffers
 constexpr int SMEM_BAR_OFF = STAGES * STAGE_BYTES;
 constexpr int SMEM_TMEM_OFF = SMEM_BAR_OFF + 8 * (2 * STAGES + 4);
-constexpr int SMEM_SCALE_OFF = (SMEM_TMEM_OFF + 4 + 15) / 16 * 16;
 // store buffers: per epilogue warp 32 rows x 64 bytes (32 bf16 columns), laid out
 // with the 64-byte swizzle the output tensor maps use; 1024-byte aligned
 constexpr int EPI_BUF = 32 * 64;
-constexpr int SMEM_EPI_OFF = (SMEM_SCALE_OFF + 8 * BN + 1023) / 1024 * 1024;  // after two column-scale buffers
-constexpr int SMEM_BYTES = SMEM_EPI_OFF + EPI_WARPS * EPI_BUF + 1024;  // + alignment slack
+constexpr int EPI_NBUF = 2;  // store buffers per epilogue warp (32-column chunks flushed together)
+constexpr int SMEM_EPI_OFF = (SMEM_TMEM_OFF + 4 + 1023) / 1024 * 1024;
+constexpr int SMEM_BYTES = SMEM_EPI_OFF + EPI_WARPS * EPI_NBUF * EPI_BUF + 1024;  // + alignment slack
 
 // instruction descriptor, kind::f8f6f4: D f32, A/B E4M3, both K-major, N, M
 constexpr uint32_t IDESC = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(BN >> 3) << 17) |
@@ -203,51 +203,73 @@ __device__ __forceinline__ Item item_of(const GemmArgs &a, int i) {
     return it;
 }
 
+// a * b for two fp32 pairs in one instruction (sm_100+ packed fp32)
+__device__ __forceinline__ float2 mul2(float2 x, float2 y) {
+    uint64_t rx, ry, rd;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rx) : "f"(x.x), "f"(x.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ry) : "f"(y.x), "f"(y.y));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(rx), "l"(ry));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(rd));
+    return r;
+}
+
+// two floats -> bf16x2 (lo in the low half), round to nearest even
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // A warp's 32 output rows x 32 bf16 columns (lane = row, packed = its 64 bytes)
-// go through the warp's shared buffer, in the 64-byte swizzle of the output
-// tensor map (16-byte piece v of row r at piece v ^ ((r >> 1) & 3)), which
-// also makes the warp's buffer writes conflict-free. A full group of 32 batch
-// rows leaves as one asynchronous TMA store at (col, row0); a partial group
-// (the end of an expert's segment) is stored row by row, 8 rows x 64 bytes per
-// instruction, so that no row of another expert is written.
-__device__ __forceinline__ void store_rows32(uint8_t *buf, const uint32_t (&packed)[16], const CUtensorMap *tm,
-                                             int col, int row0, uint16_t *out, size_t ld, int nrows, int lane) {
-    // the previous TMA store of this buffer has finished reading it
-    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-    __syncwarp();
+// into one of its shared buffers, in the 64-byte swizzle of the output tensor
+// map (16-byte piece v of row r at piece v ^ ((r >> 1) & 3)), which also makes
+// the writes conflict-free.
+__device__ __forceinline__ void stage_rows32(uint8_t *buf, const uint32_t (&packed)[16], int lane) {
     uint8_t *mine = buf + lane * 64;
     const int sw = (lane >> 1) & 3;
 #pragma unroll
     for (int v = 0; v < 4; ++v)
         *reinterpret_cast<uint4 *>(mine + 16 * (v ^ sw)) =
             make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+}
+
+// The n chunks a warp staged for an item (buffers 0..n-1, 32 columns each from
+// column col) leave together: a full group of 32 batch rows as n TMA stores in
+// one bulk group behind one proxy fence; a partial group (the end of an
+// expert's segment) row by row, 8 rows x 64 bytes per instruction, so that no
+// row of another expert is written.
+__device__ __forceinline__ void flush_rows32(const uint8_t *buf0, int n, const CUtensorMap *tm, int col, int row0,
+                                             uint16_t *out, size_t ld, int nrows, int lane) {
     if (nrows == 32) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // writes visible to the TMA unit
         __syncwarp();
         if (lane == 0) {
-            asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                             reinterpret_cast<uint64_t>(tm)),
-                         "r"(col), "r"(row0), "r"(smem_u32(buf))
-                         : "memory");
+            for (int c = 0; c < n; ++c)
+                asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                                 reinterpret_cast<uint64_t>(tm)),
+                             "r"(col + 32 * c), "r"(row0), "r"(smem_u32(buf0 + c * EPI_BUF))
+                             : "memory");
             asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
         return;
     }
     __syncwarp();
+    for (int c = 0; c < n; ++c) {
+        const uint8_t *buf = buf0 + c * EPI_BUF;
 #pragma unroll
-    for (int it = 0; it < 4; ++it) {
-        const int pc = it * 32 + lane, r = pc >> 2, part = pc & 3;
-        if (r < nrows)
-            *reinterpret_cast<uint4 *>(out + (size_t)r * ld + 8 * part) =
-                *reinterpret_cast<const uint4 *>(buf + r * 64 + 16 * (part ^ ((r >> 1) & 3)));
+        for (int it = 0; it < 4; ++it) {
+            const int pc = it * 32 + lane, r = pc >> 2, part = pc & 3;
+            if (r < nrows)
+                *reinterpret_cast<uint4 *>(out + (size_t)r * ld + 32 * c + 8 * part) =
+                    *reinterpret_cast<const uint4 *>(buf + r * 64 + 16 * (part ^ ((r >> 1) & 3)));
+        }
     }
     __syncwarp();
 }
 
-// barrier among the epilogue warps only (named barrier 1)
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(EPI_WARPS * 32) : "memory"); }
-
-// the same barrier with an AND vote: every epilogue warp takes the same branch
+// barrier among the epilogue warps only (named barrier 1) with an AND vote:
+// every epilogue warp takes the same branch
 __device__ __forceinline__ bool epi_all(bool v) {
     uint32_t r;
     asm volatile(
@@ -276,7 +298,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t bar_tfull = bar_empty + 8 * STAGES;
     const uint32_t bar_tempty = bar_tfull + 16;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + SMEM_TMEM_OFF);
-    float *col_scale = reinterpret_cast<float *>(smem + SMEM_SCALE_OFF);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x;
     const int nk = a.K / BK;
@@ -374,30 +395,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int half = (warp - 2) >> 2;  // which half of the tile's columns it finishes
         const int m = 32 * q + lane;
         const int et = threadIdx.x - 64;  // one output column per epilogue thread (BN of them)
-        uint8_t *ebuf = smem + SMEM_EPI_OFF + (warp - 2) * EPI_BUF;  // this warp's store buffer
-        static_assert(EPI_WARPS * 32 == BN, "one column scale per epilogue thread");
+        uint8_t *ebuf = smem + SMEM_EPI_OFF + (warp - 2) * EPI_NBUF * EPI_BUF;  // this warp's store buffers
         static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
-        // weight row scale of output column et of item i
-        auto col_scale_of = [&](int i) -> float {
-            const Item w = item_of(a, i);
-            const uint8_t *page = tile_page(a, w.slot);
-            const float *ws = reinterpret_cast<const float *>(page + a.wscale_off);
-            return ws[et < 128 ? w.r0 + et : w.r1 + (et - 128)];
-        };
-        // the column scales of item i are staged while item i - G is finished
-        col_scale[et] = col_scale_of(blockIdx.x);
-        epi_sync();
         int local = 0;
         bool ok = true;
         for (int i = blockIdx.x; i < n_items && ok; i += G, ++local) {
             const Item w = item_of(a, i);
             const int b = local & 1;
-            const float *cs = col_scale + b * BN;
             const int p = w.p0 + m;
             const bool valid = m < w.nv;
-            // global loads issued before the accumulator wait: this row's scale, the next item's column scale
+            // the weight-row (output column) scales of this warp's columns: output
+            // column c < 128 is weight row r0 + c, c >= 128 row r1 + c - 128. They are
+            // read with broadcast vector loads; fetched to L1 before the accumulator
+            // wait, like this lane's row scale
+            const float *wsc = reinterpret_cast<const float *>(tile_page(a, w.slot) + a.wscale_off);
+            const float *cs_lo = wsc + w.r0, *cs_hi = wsc + w.r1 - 128;
+            if (lane < 4) {
+                const float *pf = a.swiglu ? (lane < 2 ? cs_lo + 64 * half + 32 * lane : cs_hi + 128 + 64 * half + 32 * (lane - 2))
+                                           : (half ? cs_hi + 128 : cs_lo) + 32 * lane;
+                asm volatile("prefetch.global.L1 [%0];" ::"l"(pf));
+            }
             const float rs = valid ? a.row_scale[p] : 0.0f;
-            const float cs_next = i + G < n_items ? col_scale_of(i + G) : 0.0f;
             if (!epi_all(mbar_wait(bar_tfull + 8 * b, (uint32_t)(local >> 1) & 1u))) {
                 ok = false;
                 if (et == 0) atomicOr(a.status, PQE_STATUS_TIMEOUT);
@@ -408,53 +426,82 @@ __global__ void __launch_bounds__(THREADS, 1)
             // this warp's 32 rows of the tile: the first, and how many hold batch rows
             uint16_t *wrow = a.out + (size_t)(w.p0 + 32 * q) * a.out_cols;
             const int nrows = min(max(w.nv - 32 * q, 0), 32);
+            // the previous item's stores have finished reading this warp's buffers
+            if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+            __syncwarp();
+            const float2 rs2 = make_float2(rs, rs);
             if (a.swiglu) {
+                // h columns 64 half .. 64 half + 63 of the item's 128: gate in accumulator
+                // columns c, up in c + 128
                 float amax = 0.0f;
-                for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
+#pragma unroll 1
+                for (int ci = 0; ci < 2; ++ci) {
+                    const int c0 = 64 * half + 32 * ci;
                     uint32_t g[32], u[32];
                     tmem_ld32(trow + c0, g);
                     tmem_ld32(trow + 128 + c0, u);
                     tmem_ld_wait();
+                    const float4 *cg = reinterpret_cast<const float4 *>(cs_lo + c0);
+                    const float4 *cu = reinterpret_cast<const float4 *>(cs_hi + 128 + c0);
                     uint32_t packed[16];
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        float h2[2];
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 sg = __ldg(cg + j4), su = __ldg(cu + j4);
 #pragma unroll
                         for (int t = 0; t < 2; ++t) {
-                            const float gv = __uint_as_float(g[j + t]) * rs * cs[c0 + j + t];
-                            const float uv = __uint_as_float(u[j + t]) * rs * cs[128 + c0 + j + t];
-                            h2[t] = silu_fast(gv) * uv;
+                            const int j = 4 * j4 + 2 * t;
+                            const float2 gs = mul2(t ? make_float2(sg.z, sg.w) : make_float2(sg.x, sg.y), rs2);
+                            const float2 us = mul2(t ? make_float2(su.z, su.w) : make_float2(su.x, su.y), rs2);
+                            const float2 gv = mul2(make_float2(__uint_as_float(g[j]), __uint_as_float(g[j + 1])), gs);
+                            const float2 uv = mul2(make_float2(__uint_as_float(u[j]), __uint_as_float(u[j + 1])), us);
+                            const float2 hv = mul2(make_float2(silu_fast(gv.x), silu_fast(gv.y)), uv);
+                            const uint32_t hb = bf16x2_rn(hv.x, hv.y);
+                            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(hb << 16)),
+                                                     fabsf(__uint_as_float(hb & 0xffff0000u))));
+                            packed[j / 2] = hb;
                         }
-                        const uint16_t b0 = f32_to_bf16_rn(h2[0]), b1 = f32_to_bf16_rn(h2[1]);
-                        amax = fmaxf(amax, fmaxf(fabsf(bf16_to_f32(b0)), fabsf(bf16_to_f32(b1))));
-                        packed[j / 2] = (uint32_t)b0 | ((uint32_t)b1 << 16);
                     }
-                    store_rows32(ebuf, packed, &tmOut, w.nt * 128 + c0, w.p0 + 32 * q, wrow + w.nt * 128 + c0,
-                                 a.out_cols, nrows, lane);
+                    stage_rows32(ebuf + ci * EPI_BUF, packed, lane);
                 }
+                flush_rows32(ebuf, 2, &tmOut, w.nt * 128 + 64 * half, w.p0 + 32 * q, wrow + w.nt * 128 + 64 * half,
+                             a.out_cols, nrows, lane);
                 if (valid) atomicMax(a.hmax + p, __float_as_uint(amax));
             } else {
-                for (int c0 = 128 * half; c0 < 128 * half + 128; c0 += 32) {
-                    uint32_t d[32];
-                    tmem_ld32(trow + c0, d);
-                    tmem_ld_wait();
-                    uint32_t packed[16];
-#pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        const float v0 = __uint_as_float(d[j]) * rs * cs[c0 + j];
-                        const float v1 = __uint_as_float(d[j + 1]) * rs * cs[c0 + j + 1];
-                        packed[j / 2] = (uint32_t)f32_to_bf16_rn(v0) | ((uint32_t)f32_to_bf16_rn(v1) << 16);
+                // output columns 128 half .. 128 half + 127 of the item's 256, two chunks per flush
+                const float *csw = half ? cs_hi : cs_lo;
+#pragma unroll 1
+                for (int hp = 0; hp < 2; ++hp) {
+                    if (hp) {  // the first pair's stores have finished reading the buffers
+                        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                        __syncwarp();
                     }
-                    store_rows32(ebuf, packed, &tmOut, w.nt * 256 + c0, w.p0 + 32 * q, wrow + w.nt * 256 + c0,
-                                 a.out_cols, nrows, lane);
+#pragma unroll 1
+                    for (int ci = 0; ci < 2; ++ci) {
+                        const int c0 = 128 * half + 64 * hp + 32 * ci;
+                        uint32_t d[32];
+                        tmem_ld32(trow + c0, d);
+                        tmem_ld_wait();
+                        const float4 *c4 = reinterpret_cast<const float4 *>(csw + c0);
+                        uint32_t packed[16];
+#pragma unroll
+                        for (int j4 = 0; j4 < 8; ++j4) {
+                            const float4 sc = __ldg(c4 + j4);
+                            const float2 s01 = mul2(make_float2(sc.x, sc.y), rs2), s23 = mul2(make_float2(sc.z, sc.w), rs2);
+                            const int j = 4 * j4;
+                            const float2 v01 = mul2(make_float2(__uint_as_float(d[j]), __uint_as_float(d[j + 1])), s01);
+                            const float2 v23 = mul2(make_float2(__uint_as_float(d[j + 2]), __uint_as_float(d[j + 3])), s23);
+                            packed[2 * j4] = bf16x2_rn(v01.x, v01.y);
+                            packed[2 * j4 + 1] = bf16x2_rn(v23.x, v23.y);
+                        }
+                        stage_rows32(ebuf + ci * EPI_BUF, packed, lane);
+                    }
+                    flush_rows32(ebuf, 2, &tmOut, w.nt * 256 + 128 * half + 64 * hp, w.p0 + 32 * q,
+                                 wrow + w.nt * 256 + 128 * half + 64 * hp, a.out_cols, nrows, lane);
                 }
             }
             // this accumulator may be overwritten by the MMAs of item i + 2G
             tc_fence_before();
             mbar_arrive_plain(bar_tempty + 8 * b);
-            // the other buffer was last read for item i - G, which every thread has finished
-            col_scale[(b ^ 1) * BN + et] = cs_next;
-            epi_sync();
         }
     }
     // every TMA store of an epilogue warp has completed before the CTA leaves
