@@ -323,6 +323,12 @@ def run_timed(r: Runner, T, logits_dev, xs_dev, y, warmup, K, ws, want_ffn=True)
     return ms, wall, infos, ffn_ms, launches
 
 
+# ncu (dram__bytes_read.sum + dram__bytes_write.sum) of every kernel of 10 FFN
+# calls at T=64 (schedule, weight stream, the tensor-core chain), divided by the
+# calls' mean routed experts (142.56): 454.0 MB per call
+FFN_DRAM_BYTES_PER_EXPERT_T64 = 454.0e6 / 142.56
+
+
 def ffn_bytes(n_routed, T):
     """Algorithmic bytes of one moe_paged_ffn call: the routed experts' pages,
     x once, out_perm once."""
@@ -760,6 +766,10 @@ def main():
     byts = [ffn_bytes(n, T) for (n, _, _, _) in infos]
     ffn_total_ms = sum(ffn_ms)
     achieved = sum(byts) / (ffn_total_ms / 1e3) / 1e9 if ffn_total_ms > 0 else None
+    # DRAM bytes of one FFN call, from an ncu capture of its kernels at T=64
+    # (profiles/launches_decode_T64.md), per routed expert, times this run's experts
+    traffic = (FFN_DRAM_BYTES_PER_EXPERT_T64 * float(np.mean([n for (n, _, _, _) in infos]))
+               if T == 64 else None)
 
     # e2e: host buffers through pqe_layer_step_host
     x_h = torch.from_numpy(synth.activations(CFG, T, 0).view(np.int16)).pin_memory()
@@ -832,7 +842,7 @@ def main():
                        "working_buffer_steps": int(sum(w for (_, _, w, _) in infos)),
                        "h2d_gb_per_s": (sum(h2d) / (ms / 1e3) / 1e9), "by_T": sweep},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": (achieved / peak) if achieved else None, "traffic": None,
+                         "frac": (achieved / peak) if achieved else None, "traffic": traffic,
                          "kernel": "moe_paged_ffn (w13+SwiGLU and w2 weight streams)",
                          "peak_kind": peak_kind,
                          "ffn_ms_per_step": ffn_total_ms / K,

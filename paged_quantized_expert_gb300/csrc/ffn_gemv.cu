@@ -547,11 +547,19 @@ int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *of
         const int r = side_stream(ss);
         if (r != PQE_OK) return r;
         PQE_CUDA_TRY(cudaEventRecord(ss->fork, s));
-        PQE_CUDA_TRY(cudaStreamWaitEvent(ss->s, ss->fork, 0));
     }
+    // the stream kernel goes out first: from an idle GPU every host step before it
+    // is a gap after the schedule kernel
     int rc = stream_path ? launch_ffn_stream(args, s, side ? sm_count() - TC_SIDE_SMS : 0)
                          : launch_ffn_gemv(args, max_active, s);
-    if (rc != PQE_OK || !w.tc) return rc;
+    if (side) PQE_CUDA_TRY(cudaStreamWaitEvent(ss->s, ss->fork, 0));
+    if (rc != PQE_OK || !w.tc) {
+        if (side) {  // close the fork
+            PQE_CUDA_TRY(cudaEventRecord(ss->join, ss->s));
+            PQE_CUDA_TRY(cudaStreamWaitEvent(s, ss->join, 0));
+        }
+        return rc;
+    }
     TcBuffers b{};
     b.A = A;
     b.tiles = tiles;

@@ -467,37 +467,43 @@ __global__ void __launch_bounds__(THREADS, 1)
                              a.out_cols, nrows, lane);
                 if (valid) atomicMax(a.hmax + p, __float_as_uint(amax));
             } else {
-                // output columns 128 half .. 128 half + 127 of the item's 256, two chunks per flush
+                // output columns 128 half .. 128 half + 127 of the item's 256, in four
+                // 32-column chunks flushed in pairs; the third chunk is computed before
+                // the wait for the first pair's stores, which then have its math to finish
+                // reading the buffers
                 const float *csw = half ? cs_hi : cs_lo;
-#pragma unroll 1
-                for (int hp = 0; hp < 2; ++hp) {
-                    if (hp) {  // the first pair's stores have finished reading the buffers
-                        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                        __syncwarp();
-                    }
-#pragma unroll 1
-                    for (int ci = 0; ci < 2; ++ci) {
-                        const int c0 = 128 * half + 64 * hp + 32 * ci;
-                        uint32_t d[32];
-                        tmem_ld32(trow + c0, d);
-                        tmem_ld_wait();
-                        const float4 *c4 = reinterpret_cast<const float4 *>(csw + c0);
-                        uint32_t packed[16];
+                auto chunk = [&](int ci, uint32_t (&packed)[16]) {
+                    const int c0 = 128 * half + 32 * ci;
+                    uint32_t d[32];
+                    tmem_ld32(trow + c0, d);
+                    tmem_ld_wait();
+                    const float4 *c4 = reinterpret_cast<const float4 *>(csw + c0);
 #pragma unroll
-                        for (int j4 = 0; j4 < 8; ++j4) {
-                            const float4 sc = __ldg(c4 + j4);
-                            const float2 s01 = mul2(make_float2(sc.x, sc.y), rs2), s23 = mul2(make_float2(sc.z, sc.w), rs2);
-                            const int j = 4 * j4;
-                            const float2 v01 = mul2(make_float2(__uint_as_float(d[j]), __uint_as_float(d[j + 1])), s01);
-                            const float2 v23 = mul2(make_float2(__uint_as_float(d[j + 2]), __uint_as_float(d[j + 3])), s23);
-                            packed[2 * j4] = bf16x2_rn(v01.x, v01.y);
-                            packed[2 * j4 + 1] = bf16x2_rn(v23.x, v23.y);
-                        }
-                        stage_rows32(ebuf + ci * EPI_BUF, packed, lane);
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 sc = __ldg(c4 + j4);
+                        const float2 s01 = mul2(make_float2(sc.x, sc.y), rs2), s23 = mul2(make_float2(sc.z, sc.w), rs2);
+                        const int j = 4 * j4;
+                        const float2 v01 = mul2(make_float2(__uint_as_float(d[j]), __uint_as_float(d[j + 1])), s01);
+                        const float2 v23 = mul2(make_float2(__uint_as_float(d[j + 2]), __uint_as_float(d[j + 3])), s23);
+                        packed[2 * j4] = bf16x2_rn(v01.x, v01.y);
+                        packed[2 * j4 + 1] = bf16x2_rn(v23.x, v23.y);
                     }
-                    flush_rows32(ebuf, 2, &tmOut, w.nt * 256 + 128 * half + 64 * hp, w.p0 + 32 * q,
-                                 wrow + w.nt * 256 + 128 * half + 64 * hp, a.out_cols, nrows, lane);
-                }
+                };
+                uint32_t packed[16];
+                chunk(0, packed);
+                stage_rows32(ebuf, packed, lane);
+                chunk(1, packed);
+                stage_rows32(ebuf + EPI_BUF, packed, lane);
+                flush_rows32(ebuf, 2, &tmOut, w.nt * 256 + 128 * half, w.p0 + 32 * q, wrow + w.nt * 256 + 128 * half,
+                             a.out_cols, nrows, lane);
+                chunk(2, packed);
+                if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                __syncwarp();
+                stage_rows32(ebuf, packed, lane);
+                chunk(3, packed);
+                stage_rows32(ebuf + EPI_BUF, packed, lane);
+                flush_rows32(ebuf, 2, &tmOut, w.nt * 256 + 128 * half + 64, w.p0 + 32 * q,
+                             wrow + w.nt * 256 + 128 * half + 64, a.out_cols, nrows, lane);
             }
             // this accumulator may be overwritten by the MMAs of item i + 2G
             tc_fence_before();
