@@ -318,23 +318,32 @@ __device__ __forceinline__ void load_bfrag_f32(const float *row, int c0, int nch
 // acc[mma rows g, g+8 x tokens 2c, 2c+1] += W . B over the warp's chunks.
 // FP8: mma row g at rows + g * pitch, row g+8 `off8` bytes after it; lane c
 // reads bytes 16c .. 16c+15 of each chunk.
+// one 64-column chunk of FP8 rows: pa = row g's 16 bytes of the chunk for lane c
+template <int NCH>
+__device__ __forceinline__ void mma_chunk_fp8(const uint8_t *pa, uint32_t off8, const uint32_t (&bv)[8],
+                                              float (&part)[4][4]) {
+    const uint4 wa = *reinterpret_cast<const uint4 *>(pa);
+    const uint4 wb = *reinterpret_cast<const uint4 *>(pa + off8);
+    const uint32_t ua[4] = {wa.x, wa.y, wa.z, wa.w}, ub[4] = {wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        mma_f16(part[q], f16x2_e4m3_lo(ua[q]), f16x2_e4m3_lo(ub[q]), f16x2_e4m3_hi(ua[q]), f16x2_e4m3_hi(ub[q]),
+                bv[2 * q], bv[2 * q + 1]);
+}
+
 template <int NCH>
 __device__ __forceinline__ void mma_rows_fp8(const uint8_t *rows, uint32_t pitch, uint32_t off8, int c0, int nch,
                                              int g, int c, const BFrag<NCH> &b, float (&acc)[4]) {
     // four independent accumulator chains (one per k-step of a chunk)
     float part[4][4] = {};
+    const uint8_t *base = rows + (size_t)g * pitch + 64 * c0 + 16 * c;
+    if (nch == NCH) {  // every warp's slice on the standard shapes: no per-chunk guard
 #pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-        if (j < nch) {
-            const uint8_t *pa = rows + (size_t)g * pitch + 64 * (c0 + j) + 16 * c;
-            const uint4 wa = *reinterpret_cast<const uint4 *>(pa);
-            const uint4 wb = *reinterpret_cast<const uint4 *>(pa + off8);
-            const uint32_t ua[4] = {wa.x, wa.y, wa.z, wa.w}, ub[4] = {wb.x, wb.y, wb.z, wb.w};
+        for (int j = 0; j < NCH; ++j) mma_chunk_fp8<NCH>(base + 64 * j, off8, b.v[j], part);
+    } else {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                mma_f16(part[q], f16x2_e4m3_lo(ua[q]), f16x2_e4m3_lo(ub[q]), f16x2_e4m3_hi(ua[q]),
-                        f16x2_e4m3_hi(ub[q]), b.v[j][2 * q], b.v[j][2 * q + 1]);
-        }
+        for (int j = 0; j < NCH; ++j)
+            if (j < nch) mma_chunk_fp8<NCH>(base + 64 * j, off8, b.v[j], part);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] += (part[0][i] + part[1][i]) + (part[2][i] + part[3][i]);
@@ -343,31 +352,41 @@ __device__ __forceinline__ void mma_rows_fp8(const uint8_t *rows, uint32_t pitch
 // E2M1: rows placed as for FP8; lane c reads bytes 4c .. 4c+3 of each 16-byte
 // (32-column) block. E8M0 scales of mma row g at scales + g * spitch, of row
 // g+8 `soff8` bytes after them, one byte per block.
+// one 64-column chunk (two 32-column blocks) of E2M1 rows; pa = row g's bytes
+// of the chunk for lane c, sc = row g's scale of the chunk's first block
+template <int NCH>
+__device__ __forceinline__ void mma_chunk_fp4(const uint8_t *pa, uint32_t off8, const uint8_t *sc, int soff8,
+                                              const uint32_t (&bv)[8], float (&acc)[4]) {
+#pragma unroll
+    for (int lb = 0; lb < 2; ++lb) {
+        uint32_t fa[4], fb[4];
+        f16x2_e2m1x4(*reinterpret_cast<const uint32_t *>(pa + 16 * lb), fa);
+        f16x2_e2m1x4(*reinterpret_cast<const uint32_t *>(pa + 16 * lb + off8), fb);
+        float t[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_f16(t, fa[0], fb[0], fa[1], fb[1], bv[4 * lb], bv[4 * lb + 1]);
+        mma_f16(t, fa[2], fb[2], fa[3], fb[3], bv[4 * lb + 2], bv[4 * lb + 3]);
+        const float sa = e8m0_to_f32(sc[lb]);
+        const float sb = e8m0_to_f32(sc[soff8 + lb]);
+        acc[0] = __fmaf_rn(sa, t[0], acc[0]);
+        acc[1] = __fmaf_rn(sa, t[1], acc[1]);
+        acc[2] = __fmaf_rn(sb, t[2], acc[2]);
+        acc[3] = __fmaf_rn(sb, t[3], acc[3]);
+    }
+}
+
 template <int NCH>
 __device__ __forceinline__ void mma_rows_fp4(const uint8_t *rows, uint32_t pitch, uint32_t off8,
                                              const uint8_t *scales, int spitch, int soff8, int c0, int nch, int g,
                                              int c, const BFrag<NCH> &b, float (&acc)[4]) {
+    const uint8_t *base = rows + (size_t)g * pitch + 32 * c0 + 4 * c;
+    const uint8_t *sbase = scales + (size_t)g * spitch + 2 * c0;
+    if (nch == NCH) {  // every warp's slice on the standard shapes: no per-chunk guard
 #pragma unroll
-    for (int j = 0; j < NCH; ++j) {
-        if (j < nch) {
+        for (int j = 0; j < NCH; ++j) mma_chunk_fp4<NCH>(base + 32 * j, off8, sbase + 2 * j, soff8, b.v[j], acc);
+    } else {
 #pragma unroll
-            for (int lb = 0; lb < 2; ++lb) {
-                const int blk = 2 * (c0 + j) + lb;
-                const uint8_t *pa = rows + (size_t)g * pitch + 16 * blk + 4 * c;
-                uint32_t fa[4], fb[4];
-                f16x2_e2m1x4(*reinterpret_cast<const uint32_t *>(pa), fa);
-                f16x2_e2m1x4(*reinterpret_cast<const uint32_t *>(pa + off8), fb);
-                float t[4] = {0.f, 0.f, 0.f, 0.f};
-                mma_f16(t, fa[0], fb[0], fa[1], fb[1], b.v[j][4 * lb], b.v[j][4 * lb + 1]);
-                mma_f16(t, fa[2], fb[2], fa[3], fb[3], b.v[j][4 * lb + 2], b.v[j][4 * lb + 3]);
-                const float sa = e8m0_to_f32(scales[(size_t)g * spitch + blk]);
-                const float sb = e8m0_to_f32(scales[(size_t)g * spitch + soff8 + blk]);
-                acc[0] = __fmaf_rn(sa, t[0], acc[0]);
-                acc[1] = __fmaf_rn(sa, t[1], acc[1]);
-                acc[2] = __fmaf_rn(sb, t[2], acc[2]);
-                acc[3] = __fmaf_rn(sb, t[3], acc[3]);
-            }
-        }
+        for (int j = 0; j < NCH; ++j)
+            if (j < nch) mma_chunk_fp4<NCH>(base + 32 * j, off8, sbase + 2 * j, soff8, b.v[j], acc);
     }
 }
 
