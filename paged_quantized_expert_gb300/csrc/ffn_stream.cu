@@ -640,9 +640,16 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
     BFrag<NCH> bf;
     float inv = 1.0f;
     int b_a = -1, b_tg = -1;  // expert and token group bf holds
+    int f_a = -1;             // schedule entry f holds
+    ExpertInfo f{};
+    // the activation factors of this lane's output tokens 2cq, 2cq+1 (they sit in
+    // lanes 8cq, 8cq+4 of the fragment), taken when the fragment is loaded
+    float i0 = 1.0f, i1 = 1.0f;
+    auto take_factors = [&]() {
+        i0 = __shfl_sync(0xffffffffu, inv, 8 * cq);
+        i1 = __shfl_sync(0xffffffffu, inv, 8 * cq + 4);
+    };
     auto hand_off = [&](float s_lo, float s_hi, const float (&acc)[4]) {
-        // tokens 2cq, 2cq+1 sit in lanes 8cq, 8cq+4 of the fragment
-        const float i0 = __shfl_sync(0xffffffffu, inv, 8 * cq), i1 = __shfl_sync(0xffffffffu, inv, 8 * cq + 4);
         const int sl = rc % RSLOTS;
         if (!timed_out && !mbar_wait(rfree + 8 * sl, ((uint32_t)(rc / RSLOTS) & 1u) ^ 1u)) timed_out = true;
         red[(sl * CONS + cw) * 32 + lane] =
@@ -658,7 +665,10 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
         for (int u = u13a; u < u13b; ++u, rp.next(g.stages), up.next(per13)) {
             const int s = rp.s;
             const int ua = up.ea;
-            const ExpertInfo f = s_info[ua];
+            if (ua != f_a) {  // the schedule entry changes only at expert boundaries
+                f = s_info[ua];
+                f_a = ua;
+            }
             const int p0 = f.p0, n = f.n;
             const bool fp8 = f.fmt == PQE_FMT_FP8;
             bool valid = f.valid != 0 && !timed_out;
@@ -682,6 +692,7 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
                         const uint16_t *row = nullptr;
                         if (gq < nt) row = a.x + (size_t)(__ldg(a.perm_src + p0 + tg + gq) / a.k) * H;
                         load_bfrag_bf16(row, c0, nch, cq, fp8, bf, inv);
+                        take_factors();
                         b_a = ua;
                         b_tg = tg;
                     }
@@ -714,7 +725,10 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
         for (int u = u2b - 1; u >= u2a; --u, rp.next(g.stages), up.prev(per2)) {
             const int s = rp.s;
             const int ua = up.ea;
-            const ExpertInfo f = s_info[ua];
+            if (ua != f_a) {  // the schedule entry changes only at expert boundaries
+                f = s_info[ua];
+                f_a = ua;
+            }
             const int p0 = f.p0, n = f.n;
             const bool fp8 = f.fmt == PQE_FMT_FP8;
             bool valid = f.valid != 0 && !timed_out;
@@ -755,6 +769,7 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
                     if (b_a != ua || b_tg != tg) {
                         const float *row = gq < nt ? a.h + (size_t)(p0 + tg + gq) * I : nullptr;
                         load_bfrag_f32(row, c0, nch, cq, fp8, bf, inv);
+                        take_factors();
                         b_a = ua;
                         b_tg = tg;
                     }
