@@ -325,8 +325,8 @@ def run_timed(r: Runner, T, logits_dev, xs_dev, y, warmup, K, ws, want_ffn=True)
 
 # ncu (dram__bytes_read.sum + dram__bytes_write.sum) of every kernel of 10 FFN
 # calls at T=64 (schedule, weight stream, the tensor-core chain), divided by the
-# calls' mean routed experts (142.56): 454.0 MB per call
-FFN_DRAM_BYTES_PER_EXPERT_T64 = 454.0e6 / 142.56
+# calls' mean routed experts (142.56): 454.17 MB per call
+FFN_DRAM_BYTES_PER_EXPERT_T64 = 454.17e6 / 142.5625
 
 
 def ffn_bytes(n_routed, T):
