@@ -292,3 +292,58 @@ def test_wide_hidden_fallback_path(cuda_lib, orc):
     ids, gates = orc.topk_gates(logits, k)
     assert res["status"] == 0
     check_tokens(orc, pages, cfg, x, ids, gates, res, np.arange(T, dtype=np.int32))
+
+
+def test_decode_step_tensor_core_batches_beside_stream(cuda_lib, orc):
+    # a decode-sized step (at most 4 rows per routed expert on average) in which
+    # two experts have 14 rows: their batches take the tensor-core path on the
+    # side stream while the weight stream takes the rest. Every token is checked
+    # against the oracle, and a CUDA-graph replay of the same FFN call (fork and
+    # join captured) gives the eager out_perm bit for bit.
+    pqe = cuda_lib
+    E, H, I, k, T = 64, 256, 128, 4, 32
+    cfg = synth.small_config(E=E, H=H, I=I, k=k, T=T, cid=89)
+    g = np.random.default_rng(5)
+    logits = g.standard_normal((T, E)).astype(np.float32)
+    logits[:14, 0] += 8.0
+    logits[14:28, 1] += 8.0
+    ids, gates = orc.topk_gates(logits, k)
+    counts = np.bincount(ids.reshape(-1), minlength=E)
+    assert counts[0] >= helpers.TC_MIN_ROWS and counts[1] >= helpers.TC_MIN_ROWS
+    assert helpers.TC_MIN_ROWS <= T * k <= 4 * E
+    pages = Pages(pqe, orc, cfg, needed=set(range(E)))
+    x = synth.activations(cfg, T)
+    res = run_layer(pqe, cfg, T, x, logits_np=logits, fmt_dev=pages.fmt_dev, pool=pages.pool)
+    assert np.array_equal(res["ids"], ids) and res["status"] == 0
+    check_tokens(orc, pages, cfg, x, ids, gates, res, np.arange(T, dtype=np.int32))
+
+    # the FFN call alone, eager and then replayed from a graph
+    A = T * k
+    xd = torch.from_numpy(x.view(np.int16)).to(DEV)
+    idsd = torch.from_numpy(ids.astype(np.int32)).to(DEV)
+    counts_d = torch.zeros(E, dtype=torch.int32, device=DEV)
+    offsets = torch.zeros(E + 1, dtype=torch.int32, device=DEV)
+    perm_src = torch.zeros(A, dtype=torch.int32, device=DEV)
+    inv = torch.zeros(A, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pws = torch.zeros(pqe.moe_permute_workspace_size(T, k, E), dtype=torch.uint8, device=DEV)
+    pqe.moe_permute(idsd, T, k, E, counts_d, offsets, perm_src, inv, pws, status)
+    pt = torch.arange(E, dtype=torch.int32, device=DEV)
+    fws = torch.zeros(pqe.moe_paged_ffn_workspace_size(T, k, E, H, I), dtype=torch.uint8, device=DEV)
+    eager = torch.zeros((A, H), dtype=torch.bfloat16, device=DEV)
+    pqe.moe_paged_ffn(xd, perm_src, offsets, pt, pages.fmt_dev, pages.pool, T, k, E, eager, fws, status)
+    torch.cuda.synchronize()
+    replay = torch.zeros((A, H), dtype=torch.bfloat16, device=DEV)
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            pqe.moe_paged_ffn(xd, perm_src, offsets, pt, pages.fmt_dev, pages.pool, T, k, E, replay, fws, status,
+                              stream=s)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        replay.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(replay.view(torch.int16), eager.view(torch.int16))
+    assert status.item() == 0
