@@ -227,8 +227,18 @@ PQE_API int moe_permute_static(const int32_t *topk_ids, int T, int k, int E, int
  * status     device int32; a routed expert whose slot is outside the pool or
  *            whose format is unknown sets PQE_STATUS_BAD_PAGE and its rows of
  *            out_perm are zero.
- * Work is dispatched on the device per expert batch: small batches take a
- * weight-streaming CUDA-core path, large ones the tensor-core path.
+ * Work is dispatched on the device per expert batch: batches of at most 8
+ * rows take the weight stream (mma.sync on the SMs' tensor pipe as a
+ * dot-product engine), larger ones the tcgen05 tensor-core path.
+ * Streams: all work is ordered after earlier work on `stream`, and later work
+ * on `stream` is ordered after all of it. For decode-sized steps (T*k at most
+ * 4*E) the tensor-core batches run on a side stream that the library creates
+ * once per host thread and device (non-blocking, never destroyed). It is
+ * forked from `stream` with an event after the call's first kernel and joined
+ * back with another before the call returns. The call can be captured into a
+ * CUDA graph (the fork and join become graph edges). Make one call before the
+ * first capture on a host thread, so that the side stream and its events
+ * exist.
  * ------------------------------------------------------------------------ */
 PQE_API size_t moe_paged_ffn_workspace_size(int T, int k, int E, int H, int I);
 PQE_API int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *offsets,
