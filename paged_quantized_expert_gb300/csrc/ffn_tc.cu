@@ -19,12 +19,17 @@
 // Activations are quantised per row to E4M3 (scale amax / 448) by a gather
 // kernel that also lays the rows out in batch order for TMA.
 //
-// Persistent CTA (one per SM) over (M tile, N tile) work items, 6 warps:
-// warp 0 issues TMA (one thread), warp 1 owns TMEM and issues the MMAs (one
-// thread), warps 2-9 read the accumulator from TMEM (two warps per 32-lane
-// quarter, each half of the columns) and run the epilogue. 4-stage smem ring of A [128 x 128 B] +
-// B [256 x 128 B] tiles, 128-byte swizzle, K-major; two TMEM accumulators so
-// the epilogue of one item overlaps the MMAs of the next.
+// Persistent CTA (one per SM, or per SM of a given share) over (M tile,
+// N tile) work items, 10 warps: warp 0 issues TMA (one thread), warp 1 owns
+// TMEM and issues the MMAs (one thread), warps 2-9 read the accumulator from
+// TMEM (two warps per 32-lane quarter, each half of the columns) and run the
+// epilogue. 4-stage smem ring of A [128 x 128 B] + B [256 x 128 B] tiles,
+// 128-byte swizzle, K-major; two TMEM accumulators so the epilogue of one item
+// overlaps the MMAs of the next. The epilogue scales with packed fp32
+// multiplies, converts two values per instruction to bf16 and stages 32-column
+// chunks in two per-warp shared buffers (the output map's 64-byte swizzle),
+// which leave in pairs as TMA stores; rows past an expert's segment are never
+// written.
 // Every mbarrier wait is bounded: on expiry the CTA sets PQE_STATUS_TIMEOUT,
 // drains what it issued (bounded), frees its TMEM and returns.
 #include <cuda.h>
