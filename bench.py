@@ -36,7 +36,7 @@ sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
 
-CFG = synth.CONFIGS[2]
+CFG = synth.WORKLOADS["decode"]
 METRIC = "MoE-layer tokens/s; % of HBM BW (decode) and FP8 tensor peak (batched)"
 
 
@@ -414,7 +414,7 @@ def run_batched(pqe, torch, device, host, steps, ws):
     batches of ~512 rows (Zipf-skewed); |U| > CACHE_SLOTS, so every step stages
     the needed non-resident experts into the working buffer. Reports whole
     steps and the FFN alone (FP8 tensor path) against the FP8 peak."""
-    cfg3 = synth.CONFIGS[3]
+    cfg3 = synth.WORKLOADS["batched"]
     E, H, I, k, S, T = cfg3.E, cfg3.H, cfg3.I, cfg3.k, cfg3.S, cfg3.T[0]
     nbytes = [pqe.page_bytes(pqe.PQE_FMT_FP8, H, I)] * E
     layer = pqe.PagedMoELayer(E, H, I, k, S, E, T, host, nbytes, device=device)
@@ -523,7 +523,7 @@ def run_large(pqe, torch, device, steps_t1=64, steps_big=3, n_src=32):
     and the decoder alone on device-resident compressed pages. The host tier
     holds n_src distinct encoded pages (expert e uses page e % n_src), so the
     bytes moved and decoded per step are those of the full layer."""
-    cfg = synth.CONFIGS[4]
+    cfg = synth.WORKLOADS["large"]
     E, H, I, k, S = cfg.E, cfg.H, cfg.I, cfg.k, cfg.S
     stride = pqe.slot_stride(H, I)
     nb = pqe.page_bytes(pqe.PQE_FMT_FP8, H, I)
@@ -582,7 +582,7 @@ def run_mixed(pqe, torch, device, steps=12):
     the top 25% of experts by a seeded importance score keep FP8 pages, the
     rest hold MXFP4 pages; all pages resident (256 slots). Whole steps and the
     FFN against both HBM (bytes of the routed pages) and the FP8 peak."""
-    cfg = synth.CONFIGS[5]
+    cfg = synth.WORKLOADS["mixed"]
     E, H, I, k, T = cfg.E, cfg.H, cfg.I, cfg.k, cfg.T[0]
     stride = pqe.slot_stride(H, I)
     n8, n4 = pqe.page_bytes(pqe.PQE_FMT_FP8, H, I), pqe.page_bytes(pqe.PQE_FMT_MXFP4, H, I)

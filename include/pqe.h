@@ -129,8 +129,8 @@ PQE_API void *pqe_pool_slot_addr(const pqe_pool *pool, int dest);
 /* Quantise fp32 weights [rows, cols] (device) to E4M3 codes (device, [rows,
  * cols]) with one fp32 scale per row (device, [rows]): s = amax/448 in fp32
  * (1 for an all-zero row), code = RNE_e4m3(w / s) with the quotient in fp32,
- * saturating at 448. This is the configs' "quantized to FP8 e4m3 with per-row
- * fp32 scales"; it prepares pages and is not on the per-step path. */
+ * saturating at 448: FP8 E4M3 weights with one fp32 scale per row, as the
+ * workloads' experts are stored; it prepares pages and is not on the per-step path. */
 PQE_API int pqe_quantize_fp8_rows(const float *w, int rows, int cols, uint8_t *q, float *scale, void *stream);
 
 /* 4-bit copy of an FP8 matrix ([PW]: lower-bit pages; the FP8 master copy is

@@ -97,8 +97,8 @@ EXPORT uint8_t orc_e4m3_encode(float v)
     return sign | e4m3_magnitude_code(fabs((double)v));
 }
 
-/* Per-row FP8 weight quantisation (the configs' "quantized to FP8 e4m3 with
- * per-row fp32 scales"). Reading: s = amax/448 in fp32 (s = 1 for an all-zero
+/* Per-row FP8 weight quantisation: E4M3 codes with one fp32 scale per row.
+ * Reading: s = amax/448 in fp32 (s = 1 for an all-zero
  * row); code = RNE_e4m3(w / s) with the quotient taken in fp32; dequant is
  * e4m3(code) * s. */
 EXPORT void orc_quant_e4m3_rows(const float *w, int rows, int cols, uint8_t *q, float *scale)

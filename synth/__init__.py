@@ -62,20 +62,22 @@ class LayerConfig:
         return 3 * self.H * self.I
 
 
-CONFIGS = {
-    1: LayerConfig(1, "tiny layer, all experts resident", E=8, H=256, I=128, k=2,
+# The layer workloads, by what they are. The first field of each is its seed
+# namespace (inputs drawn for a workload depend on it, not on the name).
+WORKLOADS = {
+    "tiny": LayerConfig(1, "tiny layer, all experts resident", E=8, H=256, I=128, k=2,
                    T=(64,), S=8, steps=1, reuse_p=0.0, zipf_s=0.0,
                    router_gemm=True, compressed=False, mixed=False, tie_frac=0.0),
-    2: LayerConfig(2, "decode-shaped paged layer", E=256, H=2048, I=512, k=8,
+    "decode": LayerConfig(2, "decode-shaped paged layer", E=256, H=2048, I=512, k=8,
                    T=(1, 8, 64), S=32, steps=256, reuse_p=0.7, zipf_s=1.1,
                    router_gemm=False, compressed=False, mixed=False),
-    3: LayerConfig(3, "module-batched prefill layer", E=256, H=2048, I=512, k=8,
+    "batched": LayerConfig(3, "module-batched prefill layer", E=256, H=2048, I=512, k=8,
                    T=(16384,), S=32, steps=1, reuse_p=0.0, zipf_s=1.1,
                    router_gemm=False, compressed=False, mixed=False),
-    4: LayerConfig(4, "large paged layer, compressed host tier", E=512, H=2560, I=640, k=8,
+    "large": LayerConfig(4, "large paged layer, compressed host tier", E=512, H=2560, I=640, k=8,
                    T=(1, 4096), S=46, steps=256, reuse_p=0.7, zipf_s=1.1,
                    router_gemm=False, compressed=True, mixed=False),
-    5: LayerConfig(5, "mixed per-expert precision layer", E=256, H=2048, I=512, k=8,
+    "mixed": LayerConfig(5, "mixed per-expert precision layer", E=256, H=2048, I=512, k=8,
                    T=(4096,), S=256, steps=256, reuse_p=0.7, zipf_s=1.1,
                    router_gemm=False, compressed=False, mixed=True),
 }

@@ -106,9 +106,9 @@ def check_tokens(orc, pages, cfg, x_np, ids, gates_ref, res, tokens, l2_bound=No
     return st
 
 
-def test_config1_end_to_end(cuda_lib, orc):
+def test_tiny_layer_end_to_end(cuda_lib, orc):
     pqe = cuda_lib
-    cfg = synth.CONFIGS[1]
+    cfg = synth.WORKLOADS["tiny"]
     pages = Pages(pqe, orc, cfg, needed=set(range(cfg.E)))
     x = synth.activations(cfg, 64)
     w_r = synth.router_weights(cfg)
@@ -124,7 +124,7 @@ def test_activation_magnitude_extremes(cuda_lib, orc, shift, fp4):
     # into range with a power-of-two factor per token and K slice; the bound is
     # relative, so the same tolerance holds at any scale
     pqe = cuda_lib
-    cfg = synth.CONFIGS[1]
+    cfg = synth.WORKLOADS["tiny"]
     T = 6
     pages = Pages(pqe, orc, cfg, needed=set(range(cfg.E)), fp4=set(fp4))
     x = synth.activations(cfg, T)
@@ -158,9 +158,9 @@ def test_small_ragged_layers(cuda_lib, orc, E, H, I, k, T, fp4):
 
 
 @pytest.mark.parametrize("T,n_check", [(1, 1), (8, 4), (64, 3)])
-def test_config2_decode_shapes(cuda_lib, orc, T, n_check):
+def test_decode_layer_shapes(cuda_lib, orc, T, n_check):
     pqe = cuda_lib
-    cfg = synth.CONFIGS[2]
+    cfg = synth.WORKLOADS["decode"]
     logits = synth.routing_logits(cfg, T, 2)
     ids, gates = orc.topk_gates(logits, cfg.k)
     tokens = helpers.sample_tokens(T, n_check, seed=T)
@@ -264,15 +264,15 @@ def test_tensor_core_path_4bit_pages(cuda_lib, orc, H, I):
     check_tokens(orc, pages, cfg, x, ids, gates, res, np.arange(T, dtype=np.int32))
 
 
-@pytest.mark.parametrize("cid,T,n_check", [(3, 16384, 6), (4, 4096, 4)])
-def test_full_size_batched(cuda_lib, orc, cid, T, n_check):
+@pytest.mark.parametrize("wl,T,n_check", [("batched", 16384, 6), ("large", 4096, 4)])
+def test_full_size_batched(cuda_lib, orc, wl, T, n_check):
     pqe = cuda_lib
-    cfg = synth.CONFIGS[cid]
+    cfg = synth.WORKLOADS[wl]
     logits = synth.routing_logits(cfg, T, 0)
     ids, gates = orc.topk_gates(logits, cfg.k)
-    tokens = helpers.sample_tokens(T, n_check, seed=cid)
+    tokens = helpers.sample_tokens(T, n_check, seed=cfg.cid)
     needed = set(ids[tokens].reshape(-1).tolist())
-    pages = Pages(pqe, orc, cfg, needed=needed, seed=cid)
+    pages = Pages(pqe, orc, cfg, needed=needed, seed=cfg.cid)
     x = synth.activations(cfg, T, 0)
     res = run_layer(pqe, cfg, T, x, logits_np=logits, fmt_dev=pages.fmt_dev, pool=pages.pool)
     assert np.array_equal(res["ids"], ids) and res["status"] == 0

@@ -39,10 +39,10 @@ def _decode(pqe, comp, luts, H, I, comp_bytes=None):
     return out.cpu().numpy(), int(status.item())
 
 
-@pytest.mark.parametrize("cid,e", [(1, 1), (2, 0), (2, 200), (4, 511)])
-def test_decode_bit_exact(cuda_lib, orc, cid, e):
+@pytest.mark.parametrize("wl,e", [("tiny", 1), ("decode", 0), ("decode", 200), ("large", 511)])
+def test_decode_bit_exact(cuda_lib, orc, wl, e):
     pqe = cuda_lib
-    cfg = synth.CONFIGS[cid]
+    cfg = synth.WORKLOADS[wl]
     page = _fp8_page(pqe, orc, cfg, e)
     comp, luts = _encode(pqe, page, cfg.H, cfg.I)
     assert comp.numel() < page.size
@@ -73,7 +73,7 @@ def test_decode_adversarial(cuda_lib, kind):
 
 def test_corrupt_pages_flagged(cuda_lib, orc):
     pqe = cuda_lib
-    cfg = synth.CONFIGS[1]
+    cfg = synth.WORKLOADS["tiny"]
     page = _fp8_page(pqe, orc, cfg, 2)
     comp, luts = _encode(pqe, page, cfg.H, cfg.I)
     # truncated page: the header's sections no longer fit
@@ -108,7 +108,7 @@ def test_corrupt_pages_flagged(cuda_lib, orc):
 
 def test_slot_fill_compressed(cuda_lib, orc):
     pqe = cuda_lib
-    cfg = synth.CONFIGS[1]
+    cfg = synth.WORKLOADS["tiny"]
     page = _fp8_page(pqe, orc, cfg, 4)
     comp, luts = _encode(pqe, page, cfg.H, cfg.I)
     pinned = comp.pin_memory()

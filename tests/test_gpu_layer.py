@@ -83,18 +83,18 @@ def _run_trace(pqe, orc, cfg, T, steps, S, W, check_every, n_check, side=True, h
     return worst, n_wb
 
 
-def test_layer_trace_config2_T1(cuda_lib, orc):
-    cfg = synth.CONFIGS[2]
+def test_layer_trace_decode_T1(cuda_lib, orc):
+    cfg = synth.WORKLOADS["decode"]
     _run_trace(cuda_lib, orc, cfg, T=1, steps=40, S=cfg.S, W=cfg.k, check_every=13, n_check=1)
 
 
-def test_layer_trace_config2_T8_same_stream(cuda_lib, orc):
-    cfg = synth.CONFIGS[2]
+def test_layer_trace_decode_T8_same_stream(cuda_lib, orc):
+    cfg = synth.WORKLOADS["decode"]
     _run_trace(cuda_lib, orc, cfg, T=8, steps=24, S=cfg.S, W=64, check_every=11, n_check=2, side=False)
 
 
-def test_layer_trace_config2_T64_working_buffer(cuda_lib, orc):
-    cfg = synth.CONFIGS[2]
+def test_layer_trace_decode_T64_working_buffer(cuda_lib, orc):
+    cfg = synth.WORKLOADS["decode"]
     worst, n_wb = _run_trace(cuda_lib, orc, cfg, T=64, steps=6, S=cfg.S, W=cfg.E, check_every=5, n_check=2)
     assert n_wb == 6   # |U| > 32 at T=64 every step
 
@@ -170,12 +170,12 @@ def test_layer_capacity_error(cuda_lib, orc):
 
 def test_layer_device_pager_trace(cuda_lib, orc):
     # LRU state, misses and refills on the GPU: same slot states as the oracle
-    cfg = synth.CONFIGS[2]
+    cfg = synth.WORKLOADS["decode"]
     _run_trace(cuda_lib, orc, cfg, T=8, steps=30, S=cfg.S, W=cfg.E, check_every=7, n_check=3, device_pager=True)
 
 
 def test_layer_device_pager_working_buffer(cuda_lib, orc):
-    cfg = synth.CONFIGS[2]
+    cfg = synth.WORKLOADS["decode"]
     _run_trace(cuda_lib, orc, cfg, T=64, steps=5, S=cfg.S, W=cfg.E, check_every=4, n_check=2, device_pager=True)
 
 
@@ -308,11 +308,11 @@ def test_layer_mixed_precision_reranking(cuda_lib, orc):
     layer.close()
 
 
-def test_layer_config4_shapes_compressed(cuda_lib, orc):
+def test_layer_large_shapes_compressed(cuda_lib, orc):
     # E=512, H=2560, I=640, 46 slots, Huffman-compressed host tier decoded on the
     # GPU after every refill. 16 distinct pages, expert e uses page e % 16.
     pqe = cuda_lib
-    cfg = synth.CONFIGS[4]
+    cfg = synth.WORKLOADS["large"]
     E, H, I, k, S, T = cfg.E, cfg.H, cfg.I, cfg.k, cfg.S, 1
     n_src = 16
     stride = pqe.slot_stride(H, I)

@@ -20,10 +20,10 @@ def _sync():
 
 # ---- quantisers ---------------------------------------------------------------
 
-@pytest.mark.parametrize("cid,e", [(1, 0), (1, 7), (2, 11), (4, 300)])
-def test_fp8_page_pack_bit_exact(cuda_lib, orc, cid, e):
+@pytest.mark.parametrize("wl,e", [("tiny", 0), ("tiny", 7), ("decode", 11), ("large", 300)])
+def test_fp8_page_pack_bit_exact(cuda_lib, orc, wl, e):
     pqe = cuda_lib
-    cfg = synth.CONFIGS[cid]
+    cfg = synth.WORKLOADS[wl]
     H, I = cfg.H, cfg.I
     w13, w2 = synth.expert_weights(cfg, e)
     page = torch.zeros(pqe.page_bytes(pqe.PQE_FMT_FP8, H, I), dtype=torch.uint8, device=DEV)
@@ -63,10 +63,10 @@ def test_fp8_quant_ties_subnormals_zeros(cuda_lib, orc):
     assert np.array_equal(q.cpu().numpy(), qr)
 
 
-@pytest.mark.parametrize("cid,e", [(1, 2), (5, 40)])
-def test_mxfp4_page_pack_bit_exact(cuda_lib, orc, cid, e):
+@pytest.mark.parametrize("wl,e", [("tiny", 2), ("mixed", 40)])
+def test_mxfp4_page_pack_bit_exact(cuda_lib, orc, wl, e):
     pqe = cuda_lib
-    cfg = synth.CONFIGS[cid]
+    cfg = synth.WORKLOADS[wl]
     H, I = cfg.H, cfg.I
     w13, w2 = synth.expert_weights(cfg, e)
     q13, s13 = orc.quant_e4m3_rows(w13)
@@ -111,9 +111,9 @@ def _route(pqe, T, H, E, k, x=None, w_r=None, logits=None):
     return ids.cpu().numpy(), gw.cpu().numpy(), lg.cpu().numpy()
 
 
-def test_route_router_gemm_config1_bit_exact(cuda_lib, orc):
+def test_route_router_gemm_tiny_bit_exact(cuda_lib, orc):
     pqe = cuda_lib
-    cfg = synth.CONFIGS[1]
+    cfg = synth.WORKLOADS["tiny"]
     x = synth.activations(cfg, 64)
     w_r = synth.router_weights(cfg)
     ids, gw, lg = _route(pqe, 64, cfg.H, cfg.E, cfg.k, torch.from_numpy(x.view(np.int16)).to(DEV),
@@ -137,10 +137,10 @@ def test_route_router_gemm_other_shapes(cuda_lib, orc, H, E, k, T):
     assert np.array_equal(ids, orc.topk_gates(ref_lg, k)[0])
 
 
-@pytest.mark.parametrize("cid,T,step", [(2, 64, 0), (2, 64, 5), (2, 1, 3), (3, 16384, 0), (4, 4096, 0)])
-def test_route_trace_logits(cuda_lib, orc, cid, T, step):
+@pytest.mark.parametrize("wl,T,step", [("decode", 64, 0), ("decode", 64, 5), ("decode", 1, 3), ("batched", 16384, 0), ("large", 4096, 0)])
+def test_route_trace_logits(cuda_lib, orc, wl, T, step):
     pqe = cuda_lib
-    cfg = synth.CONFIGS[cid]
+    cfg = synth.WORKLOADS[wl]
     logits = synth.routing_logits(cfg, T, step)
     ids, gw, _ = _route(pqe, T, cfg.H, cfg.E, cfg.k, logits=torch.from_numpy(logits).to(DEV))
     ref_ids, ref_g = orc.topk_gates(logits, cfg.k)
@@ -186,10 +186,10 @@ def _permute(pqe, ids_np, E):
         int(status.item())
 
 
-@pytest.mark.parametrize("cid,T", [(1, 64), (2, 1), (2, 64), (3, 16384), (4, 4096)])
-def test_permute_bit_exact_on_traces(cuda_lib, orc, cid, T):
+@pytest.mark.parametrize("wl,T", [("tiny", 64), ("decode", 1), ("decode", 64), ("batched", 16384), ("large", 4096)])
+def test_permute_bit_exact_on_traces(cuda_lib, orc, wl, T):
     pqe = cuda_lib
-    cfg = synth.CONFIGS[cid]
+    cfg = synth.WORKLOADS[wl]
     if cfg.router_gemm:
         ids, _ = orc.topk_gates(orc.router_logits(synth.activations(cfg, T), synth.router_weights(cfg)), cfg.k)
     else:

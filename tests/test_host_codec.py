@@ -69,10 +69,10 @@ def _check_page(orc, pqe, page, H, I):
     return comp
 
 
-@pytest.mark.parametrize("cid,e", [(1, 0), (1, 5), (2, 17)])
-def test_encoder_matches_oracle_on_synthetic_pages(orc, cid, e):
+@pytest.mark.parametrize("wl,e", [("tiny", 0), ("tiny", 5), ("decode", 17)])
+def test_encoder_matches_oracle_on_synthetic_pages(orc, wl, e):
     pqe = _pqe()
-    cfg = synth.CONFIGS[cid]
+    cfg = synth.WORKLOADS[wl]
     w13, w2 = synth.expert_weights(cfg, e)
     q13, s13 = orc.quant_e4m3_rows(w13)
     q2, s2 = orc.quant_e4m3_rows(w2)

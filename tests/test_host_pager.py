@@ -51,9 +51,9 @@ def test_lru_random_traces_match_oracle(orc, E, S, maxk, steps):
 
 
 def test_lru_trace_of_config_2(orc):
-    # the decode trace of config 2 at T=8 through both pools
+    # the decode layer's trace at T=8 through both pools
     pqe = _pqe()
-    cfg = synth.CONFIGS[2]
+    cfg = synth.WORKLOADS["decode"]
     tr = synth.RoutingTrace(cfg, 8)
     a, b = pqe.LRU(cfg.E, cfg.S), orc.LRU(cfg.E, cfg.S)
     for s in range(64):
@@ -77,7 +77,7 @@ def test_lru_invalidate(orc):
 
 def test_importance_matches_oracle(orc):
     pqe = _pqe()
-    cfg = synth.CONFIGS[5]
+    cfg = synth.WORKLOADS["mixed"]
     T, k, E = 256, cfg.k, cfg.E
     m_a = synth.importance_init(cfg)
     m_b = m_a.copy()

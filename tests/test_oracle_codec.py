@@ -105,8 +105,8 @@ def _synthetic_fp8(orc, cfg, e):
 
 
 def test_roundtrip_synthetic_pages(orc):
-    for cid in (1, 2):
-        cfg = synth.CONFIGS[cid]
+    for wl in ("tiny", "decode"):
+        cfg = synth.WORKLOADS[wl]
         for q in _synthetic_fp8(orc, cfg, 3):
             enc = orc.huff_encode(q)
             dec, rc = orc.huff_decode(enc)
@@ -149,7 +149,7 @@ def test_roundtrip_adversarial(orc, kind):
 
 
 def test_corrupt_streams_are_reported(orc):
-    cfg = synth.CONFIGS[1]
+    cfg = synth.WORKLOADS["tiny"]
     q = _synthetic_fp8(orc, cfg, 0)[1]
     enc = orc.huff_encode(q)
     short = dict(enc)
@@ -178,8 +178,8 @@ def test_page_sizes_match_pages(orc):
     for layers, experts, H, I, gib in rows:
         cfg = synth.LayerConfig(0, "", int(experts), int(H), int(I), 8, (1,), 0, 0, 0, 0, False, False, False)
         assert cfg.page_bytes_fp8 * int(experts) * int(layers) == float(gib) * 2 ** 30
-    assert synth.CONFIGS[2].page_bytes_fp8 == 3 * 2 ** 20
-    assert synth.CONFIGS[4].page_bytes_fp8 == int(4.6875 * 2 ** 20)
+    assert synth.WORKLOADS["decode"].page_bytes_fp8 == 3 * 2 ** 20
+    assert synth.WORKLOADS["large"].page_bytes_fp8 == int(4.6875 * 2 ** 20)
 
 
 def test_compression_ratio_plausible(orc):
@@ -190,7 +190,7 @@ def test_compression_ratio_plausible(orc):
         rows = [l.split() for l in f if l.strip() and not l.startswith("#")]
     page_ratios = [float(c) / float(u) for _, _, u, c in rows]
     assert all(0.85 <= r <= 0.9 for r in page_ratios)
-    cfg = synth.CONFIGS[2]
+    cfg = synth.WORKLOADS["decode"]
     tot = comp = 0
     for q in _synthetic_fp8(orc, cfg, 5):
         enc = orc.huff_encode(q)

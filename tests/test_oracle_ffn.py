@@ -95,7 +95,7 @@ def test_single_expert_matches_torch(orc):
 
 def test_all_experts_is_dense_mixture(orc):
     # k = E: every expert is picked and the gates are the full softmax
-    cfg = synth.CONFIGS[1]
+    cfg = synth.WORKLOADS["tiny"]
     ex, deq = _fp8_experts(orc, cfg, cfg.E)
     x = synth.activations(cfg, 64)
     xt = torch.from_numpy(synth.bf16_bits_to_f32(x).astype(np.float64))
@@ -130,7 +130,7 @@ def test_fp4_experts_match_torch(orc):
 
 
 def test_token_subset_equals_full(orc):
-    cfg = synth.CONFIGS[1]
+    cfg = synth.WORKLOADS["tiny"]
     ex, _ = _fp8_experts(orc, cfg, cfg.E)
     x = synth.activations(cfg, 64)
     lg = orc.router_logits(x, synth.router_weights(cfg))

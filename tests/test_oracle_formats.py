@@ -77,7 +77,7 @@ def test_quant_rows_amax_and_zero_row(orc):
 
 def test_quant_rows_error_bound(orc):
     # RNE error bound: half a step of the code grid at the value's binade
-    cfg = synth.CONFIGS[1]
+    cfg = synth.WORKLOADS["tiny"]
     w13, _ = synth.expert_weights(cfg, 0)
     q, s = orc.quant_e4m3_rows(w13)
     deq = orc.dequant_e4m3_rows(q, s)
@@ -152,7 +152,7 @@ def test_mxfp4_hand_groups_exact(orc):
 
 
 def test_mxfp4_error_bound(orc):
-    cfg = synth.CONFIGS[1]
+    cfg = synth.WORKLOADS["tiny"]
     w13, _ = synth.expert_weights(cfg, 1)
     q8, s8 = orc.quant_e4m3_rows(w13)
     v = orc.dequant_e4m3_rows(q8, s8)

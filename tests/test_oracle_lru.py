@@ -112,7 +112,7 @@ def test_lru_invariants_random(orc, E, S, maxk):
 
 
 def test_lru_all_resident_gives_identity(orc):
-    # config 1: slots = experts and every expert used at the first step
+    # the tiny layer: slots = experts and every expert used at the first step
     E = 8
     lru = orc.LRU(E, E)
     pt, me, md, wb = lru.step(np.ones(E, np.int32))

@@ -26,7 +26,7 @@ def test_logits_exact_on_powers_of_two(orc):
 
 
 def test_logits_within_summation_bound(orc):
-    cfg = synth.CONFIGS[1]
+    cfg = synth.WORKLOADS["tiny"]
     x = synth.activations(cfg, 64)
     w = synth.router_weights(cfg)
     lg = orc.router_logits(x, w).astype(np.float64)
@@ -58,7 +58,7 @@ def test_topk_matches_stable_sort_with_ties(orc, E, k):
 
 
 def test_topk_on_trace_ties(orc):
-    cfg = synth.CONFIGS[2]
+    cfg = synth.WORKLOADS["decode"]
     logits = synth.routing_logits(cfg, 64, 0)
     ids, _ = orc.topk_gates(logits, cfg.k)
     assert np.array_equal(ids, _stable_topk(logits, cfg.k))

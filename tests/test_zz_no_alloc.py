@@ -42,7 +42,7 @@ def test_static_scratch_matches_workspace_version(cuda_lib, T, k, E):
 
 def test_static_scratch_on_a_trace_and_capacity(cuda_lib):
     pqe = cuda_lib
-    cfg = synth.CONFIGS[2]
+    cfg = synth.WORKLOADS["decode"]
     import oracle
     logits = synth.routing_logits(cfg, 64, 1)
     ids_np, _ = oracle.topk_gates(logits, cfg.k)
