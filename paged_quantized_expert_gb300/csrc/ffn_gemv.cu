@@ -10,6 +10,8 @@
 // by streaming the weights from HBM: every weight byte is read once per group
 // of up to NT tokens with 128-bit loads, converted exactly to fp32 and
 // multiplied with bf16 activations in fp32. h stays fp32.
+#include <atomic>
+
 #include "pqe_common.cuh"
 #include "ffn_internal.cuh"
 
@@ -392,7 +394,10 @@ int launch_ffn_gemv(const FfnArgs &args, int max_active, cudaStream_t s) {
         PQE_CUDA_TRY(cudaFuncSetAttribute(ffn_w2_gemv_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)smem2));
     // grid-stride over (expert, row block) units; the unit count is known on the device
-    const long cap = 148L * 8;
+    int dev = 0, sms = 0;
+    const int di = device_info(dev, sms);
+    if (di != PQE_OK) return di;
+    const long cap = 8L * sms;
     const long u13 = (long)max_active * (args.I / 8), u2 = (long)max_active * (args.H / 32);
     ffn_w13_gemv_kernel<NT><<<(unsigned)(u13 < cap ? u13 : cap), 256, smem13, s>>>(args);
     PQE_LAUNCH_CHECK();
@@ -452,11 +457,9 @@ struct SideStream {
     cudaEvent_t fork = nullptr, join = nullptr;
 };
 
-static int side_stream(SideStream *&out) {
-    thread_local SideStream ss[16];
-    int dev = 0;
-    PQE_CUDA_TRY(cudaGetDevice(&dev));
-    if (dev < 0 || dev >= 16) return PQE_ERR_UNSUPPORTED;
+static int side_stream(int dev, SideStream *&out) {
+    thread_local SideStream ss[PQE_MAX_DEVICES];
+    if (dev < 0 || dev >= PQE_MAX_DEVICES) return PQE_ERR_UNSUPPORTED;
     SideStream &x = ss[dev];
     if (x.s == nullptr) {
         PQE_CUDA_TRY(cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking));
@@ -468,14 +471,17 @@ static int side_stream(SideStream *&out) {
     return PQE_OK;
 }
 
-static int sm_count() {
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        PQE_CUDA_TRY(cudaGetDevice(&dev));
-        PQE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+int device_info(int &dev, int &sms) {
+    static std::atomic<int> cache[PQE_MAX_DEVICES];
+    PQE_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= PQE_MAX_DEVICES) return PQE_ERR_UNSUPPORTED;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        PQE_CUDA_TRY(cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev));
+        cache[dev].store(v, std::memory_order_relaxed);
     }
-    return sms;
+    sms = v;
+    return PQE_OK;
 }
 
 }  // namespace pqe
@@ -539,18 +545,21 @@ int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *of
     ffn_schedule_kernel<<<1, 1024, 0, s>>>(args, w.tc ? TC_MIN_ROWS : 0, tiles, n_tiles);
     PQE_LAUNCH_CHECK();
     const bool stream_path = stream_shape_ok(pool->H, pool->I);
+    int dev = 0, sms = 0;
+    const int di = device_info(dev, sms);
+    if (di != PQE_OK) return di;
     // decode-sized step: the tensor-core batches run beside the weight stream
     const bool side = stream_path && w.tc && A >= TC_MIN_ROWS && A <= (long)DECODE_ROWS_PER_EXPERT * E &&
-                      sm_count() > 2 * TC_SIDE_SMS;
+                      sms > 2 * TC_SIDE_SMS;
     SideStream *ss = nullptr;
     if (side) {
-        const int r = side_stream(ss);
+        const int r = side_stream(dev, ss);
         if (r != PQE_OK) return r;
         PQE_CUDA_TRY(cudaEventRecord(ss->fork, s));
     }
     // the stream kernel goes out first: from an idle GPU every host step before it
     // is a gap after the schedule kernel
-    int rc = stream_path ? launch_ffn_stream(args, s, side ? sm_count() - TC_SIDE_SMS : 0)
+    int rc = stream_path ? launch_ffn_stream(args, s, side ? sms - TC_SIDE_SMS : 0)
                          : launch_ffn_gemv(args, max_active, s);
     if (side) PQE_CUDA_TRY(cudaStreamWaitEvent(ss->s, ss->fork, 0));
     if (rc != PQE_OK || !w.tc) {

@@ -836,19 +836,17 @@ bool stream_shape_ok(int H, int I) {
 int launch_ffn_stream(const FfnArgs &args, cudaStream_t s, int grid) {
     st::Geo g;
     if (!st::geometry(args.H, args.I, args.E, g)) return PQE_ERR_UNSUPPORTED;
-    static int sms = 0;
-    static uint32_t smem_set = 0;
-    if (sms == 0) {
-        int dev = 0;
-        PQE_CUDA_TRY(cudaGetDevice(&dev));
-        PQE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    }
-    if (g.smem_bytes > smem_set) {
+    // the shared-memory opt-in is per device
+    static uint32_t smem_set[PQE_MAX_DEVICES] = {};
+    int dev = 0, sms = 0;
+    const int di = device_info(dev, sms);
+    if (di != PQE_OK) return di;
+    if (g.smem_bytes > smem_set[dev]) {
         PQE_CUDA_TRY(cudaFuncSetAttribute(st::ffn_stream_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)g.smem_bytes));
         PQE_CUDA_TRY(cudaFuncSetAttribute(st::ffn_stream_kernel<5>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                           (int)g.smem_bytes));
-        smem_set = g.smem_bytes;
+        smem_set[dev] = g.smem_bytes;
     }
     // cooperative: all CTAs resident at once (phase 2 of an expert waits for
     // phase-1 work of other CTAs); the attribute also holds when the launch is

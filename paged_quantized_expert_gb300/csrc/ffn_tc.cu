@@ -754,14 +754,14 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
          map_3d(&m2x, xp + L.w2, nx, (uint64_t)H, I, args.slot_stride);
     ok = ok && map_out(&mo1, b.h, (uint64_t)A, (uint64_t)I) && map_out(&mo2, args.out_perm, (uint64_t)A, (uint64_t)H);
     if (!ok) return PQE_ERR_UNSUPPORTED;
-    static bool attr_set = false;
-    static int sms = 0;
-    if (!attr_set) {
+    // the shared-memory opt-in is per device
+    static bool attr_set[PQE_MAX_DEVICES] = {};
+    int dev = 0, sms = 0;
+    const int di = device_info(dev, sms);
+    if (di != PQE_OK) return di;
+    if (!attr_set[dev]) {
         PQE_CUDA_TRY(cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
-        int dev = 0;
-        PQE_CUDA_TRY(cudaGetDevice(&dev));
-        PQE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-        attr_set = true;
+        attr_set[dev] = true;
     }
     // persistent grids: one CTA per SM (or per SM of the share given), at most one per work item
     const int cap = sm_cap > 0 && sm_cap < sms ? sm_cap : sms;

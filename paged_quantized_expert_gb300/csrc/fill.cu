@@ -72,12 +72,9 @@ int slot_fill_batch(const pqe_pool *pool, int n, const int32_t *dest, const void
         PQE_CHECK_ARG(d && host_src[i] && nb > 0 && nb <= pool->slot_stride && nb % 16 == 0);
         PQE_CHECK_ARG(aligned(host_src[i], 16) && aligned(d, 16));
     }
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        PQE_CUDA_TRY(cudaGetDevice(&dev));
-        PQE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    }
+    int dev = 0, sms = 0;
+    const int di = device_info(dev, sms);
+    if (di != PQE_OK) return di;
     for (int i0 = 0; i0 < n; i0 += FILL_MAX) {
         FillBatch b{};
         b.n = (n - i0 < FILL_MAX) ? n - i0 : FILL_MAX;

@@ -301,12 +301,9 @@ int page_table_update_device(void *state, int E, int S, const int32_t *counts, c
 int slot_fill_device(const pqe_pool *pool, const int32_t *miss, int E, const uint64_t *host_pages,
                      const size_t *page_bytes, void *stream) {
     PQE_CHECK_ARG(pool && miss && host_pages && page_bytes && E >= 1 && E <= 1024);
-    static int sms = 0;
-    if (sms == 0) {
-        int dev = 0;
-        PQE_CUDA_TRY(cudaGetDevice(&dev));
-        PQE_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-    }
+    int dev = 0, sms = 0;
+    const int di = device_info(dev, sms);
+    if (di != PQE_OK) return di;
     fill_device_kernel<<<sms, DF_THREADS, sizeof(uint32_t) * (E + 1), as_stream(stream)>>>(
         miss, E, host_pages, page_bytes, static_cast<uint8_t *>(pool->base), static_cast<uint8_t *>(pool->wb_base),
         pool->n_slots, pool->slot_stride);

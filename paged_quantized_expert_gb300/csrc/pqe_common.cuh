@@ -37,6 +37,13 @@ void count_launch();
 
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// The current device and its SM count, cached per device (a process may drive
+// several GPUs; launch attributes such as the dynamic shared-memory opt-in are
+// per device too). PQE_OK, PQE_ERR_CUDA, or PQE_ERR_UNSUPPORTED for a device
+// index at or above PQE_MAX_DEVICES.
+constexpr int PQE_MAX_DEVICES = 64;
+int device_info(int &dev, int &sms);
+
 inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 __host__ __device__ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
