@@ -161,6 +161,11 @@ def _check(fn: str, rc: int):
         raise PqeError(fn, rc)
 
 
+def _nbytes(t) -> int:
+    """Byte size of a buffer tensor (any dtype)."""
+    return t.numel() * t.element_size()
+
+
 def _ptr(t) -> Optional[int]:
     if t is None:
         return None
@@ -358,7 +363,7 @@ def pqe_huff_encode_page(fp8_page: torch.Tensor, H: int, I: int, out: torch.Tens
                          lut2: torch.Tensor) -> int:
     """Host tensors. Returns the compressed size in bytes."""
     n = C.c_size_t(0)
-    _check("pqe_huff_encode_page", lib().pqe_huff_encode_page(_ptr(fp8_page), H, I, _ptr(out), out.numel(),
+    _check("pqe_huff_encode_page", lib().pqe_huff_encode_page(_ptr(fp8_page), H, I, _ptr(out), _nbytes(out),
                                                               C.byref(n), _ptr(lut13), _ptr(lut2)))
     return n.value
 
@@ -382,7 +387,7 @@ def fp8_exp_huff_decode(comp_page, comp_bytes, lut13, lut2, H, I, fp8_page, stat
 def slot_fill_compressed(pool: pqe_pool, dest, pinned_comp, comp_bytes, staging, lut13, lut2, status, stream=None,
                          done_event=None):
     _check("slot_fill_compressed", lib().slot_fill_compressed(
-        C.byref(pool), dest, _ptr(pinned_comp), comp_bytes, _ptr(staging), staging.numel(), _ptr(lut13),
+        C.byref(pool), dest, _ptr(pinned_comp), comp_bytes, _ptr(staging), _nbytes(staging), _ptr(lut13),
         _ptr(lut2), _ptr(status), _stream(stream), _event(done_event)))
 
 
@@ -408,7 +413,7 @@ def pqe_quality_workspace_size(n: int, H: int, I: int) -> int:
 def pqe_expert_quant_error(x, n, page_fp8, page_fp4, H, I, sums, ws, status, stream=None):
     """sums (device float64 [2]) <- (sum ||y4 - y8||^2, sum ||y8||^2) over the n tokens x."""
     _check("pqe_expert_quant_error", lib().pqe_expert_quant_error(_ptr(x), n, _ptr(page_fp8), _ptr(page_fp4), H, I,
-                                                                  _ptr(sums), _ptr(ws), ws.numel(), _ptr(status),
+                                                                  _ptr(sums), _ptr(ws), _nbytes(ws), _ptr(status),
                                                                   _stream(stream)))
 
 
