@@ -204,7 +204,10 @@ PQE_API int moe_permute(const int32_t *topk_ids, int T, int k, int E, int32_t *c
  * current; make that first call before any stream capture. All calls share
  * the one array, so calls that overlap on the GPU (other streams, other host
  * threads) race and corrupt each other's results; issue them in one stream
- * order. Results are identical to moe_permute's. */
+ * order. Results are identical to moe_permute's. The looked-up address is
+ * cached for the life of the process: after cudaDeviceReset (or anything else
+ * that tears down and recreates the device's context) it is stale, and the
+ * call must not be used on that device again. */
 PQE_API size_t moe_permute_static_max_words(void);
 PQE_API int moe_permute_static(const int32_t *topk_ids, int T, int k, int E, int32_t *counts, int32_t *offsets,
                                int32_t *perm_src, int32_t *inv, int32_t *status, void *stream);
@@ -359,39 +362,63 @@ PQE_API int slot_fill_device(const pqe_pool *pool, const int32_t *miss, int E, c
  *   creation order); canonical code values in (length, symbol) order;
  *   each row its own MSB-first bitstream of uint32 words starting on a word
  *   boundary; rows cut into chunks of 64 symbols with a uint16 bit offset per
- *   chunk; raw nibbles two per byte, low nibble = even column.
+ *   chunk (so every chunk must start below bit 65536 of its row: the encoder
+ *   refuses a page where one would not, with PQE_ERR_CAPACITY); raw nibbles
+ *   two per byte, low nibble = even column.
  * Compressed page: a 256-byte header then 256-byte aligned sections:
  *   scales (s13 then s2, fp32), w13 {row_word [2I+1] u32, chunk_bit
  *   [2I*H/64] u16, nibbles [2I*H/2], words}, w2 {row_word [H+1], chunk_bit
  *   [H*I/64], nibbles [H*I/2], words}.
- * Code table: 4096 bytes per matrix, entry for a 12-bit window w = (symbol
- * << 4) | length of the code that prefixes w, 0 if none.
+ * Code table (kept in VRAM, [EP] 表4): 4096 little-endian uint32 entries per
+ * matrix (PQE_HUFF_LUT_BYTES), built from the code lengths; the entry of a
+ * 12-bit window w (the next bits of a stream, MSB first) describes the whole
+ * code words at the front of w, at most 5: bits 0-2 their number n (0 when no
+ * code word prefixes w), bits 3-6 their total length, bits 7-10 the length of
+ * the first, bits 12-31 their symbols, 4 bits each, the first lowest, unused
+ * slots zero. One lookup thus decodes up to 5 symbols.
  * ------------------------------------------------------------------------ */
 
-#define PQE_HUFF_LUT_BYTES 4096
+#define PQE_HUFF_LUT_BYTES 16384
 
 /* Upper bound of a compressed FP8 page for (H, I). */
 PQE_API size_t pqe_huff_page_bound(int H, int I);
 
 /* Host: compress one FP8 page (host bytes, layout above) into out (host,
  * out_cap bytes). Writes the page size to *out_bytes and the two code tables
- * to lut13 / lut2 (host, PQE_HUFF_LUT_BYTES each). */
+ * to lut13 / lut2 (host, PQE_HUFF_LUT_BYTES each). PQE_ERR_CAPACITY when out
+ * is too small or a row's chunk offsets do not fit 16 bits (such a page stays
+ * uncompressed). */
 PQE_API int pqe_huff_encode_page(const uint8_t *fp8_page, int H, int I, void *out, size_t out_cap,
                          size_t *out_bytes, uint8_t *lut13, uint8_t *lut2);
 
 /* Code lengths [16] of a compressed page's two matrices (host page). */
 PQE_API int pqe_huff_page_lengths(const void *comp_page, uint8_t *len13, uint8_t *len2);
 
-/* Host: the code table (PQE_HUFF_LUT_BYTES) of canonical code lengths [16]. */
+/* Host: the code table (PQE_HUFF_LUT_BYTES, layout above) of canonical code
+ * lengths [16]. */
 PQE_API int pqe_huff_build_lut(const uint8_t *lengths, uint8_t *lut);
 
-/* fp8_exp_huff_decode -- GPU decode of one compressed page (device) into an
- * FP8 page (device, e.g. a slot). lut13 / lut2: resident device code tables
- * of that expert. A row that does not decode sets PQE_STATUS_CORRUPT_STREAM;
- * its bytes are then unspecified. comp_bytes bounds every read. */
+/* fp8_exp_huff_decode -- GPU decode of one compressed page (device, 256-byte
+ * aligned) into an FP8 page (device, e.g. a slot, 16-byte aligned). lut13 /
+ * lut2: resident device code tables of that expert (16-byte aligned). A row
+ * that does not decode sets PQE_STATUS_CORRUPT_STREAM; its bytes are then
+ * unspecified. comp_bytes bounds every read. */
 PQE_API int fp8_exp_huff_decode(const void *comp_page, size_t comp_bytes, const uint8_t *lut13,
                         const uint8_t *lut2, int H, int I, uint8_t *fp8_page, int32_t *status,
                         void *stream);
+
+/* fp8_exp_huff_decode_batch -- n pages in one kernel launch (one per 128
+ * pages), all of shape (H, I). Host arrays [n]: comp_pages[i] is a compressed
+ * page in device memory OR in pinned host memory (kernels read pinned memory
+ * directly over the host link, so a host-tier page is pulled and decoded in
+ * the same pass, [EP] 重みの圧縮: decoded on the GPU as it arrives);
+ * comp_bytes[i] bounds its reads; lut13[i], lut2[i] are its device code tables;
+ * fp8_pages[i] its device destination. Every pointer 16-byte aligned; the
+ * destinations must not overlap each other or any source. Status as for
+ * fp8_exp_huff_decode; a corrupt page does not disturb the others. */
+PQE_API int fp8_exp_huff_decode_batch(int n, const void *const *comp_pages, const size_t *comp_bytes,
+                                      const uint8_t *const *lut13, const uint8_t *const *lut2, int H, int I,
+                                      uint8_t *const *fp8_pages, int32_t *status, void *stream);
 
 /* slot_fill_compressed -- H2D copy of a compressed page (pinned) into a device
  * staging buffer, then fp8_exp_huff_decode into slot `dest`, both on
@@ -399,6 +426,18 @@ PQE_API int fp8_exp_huff_decode(const void *comp_page, size_t comp_bytes, const 
 PQE_API int slot_fill_compressed(const pqe_pool *pool, int dest, const void *pinned_comp, size_t comp_bytes,
                          void *staging, size_t staging_bytes, const uint8_t *lut13,
                          const uint8_t *lut2, int32_t *status, void *stream, void *done_event);
+
+/* slot_fill_compressed_batch -- refill n entries of the pool from compressed
+ * host pages without a staging copy: fp8_exp_huff_decode_batch reads each
+ * page (pinned, 16-byte aligned, comp_bytes[i] bytes) over the host link and
+ * writes the decoded FP8 page into entry dest[i]. dest, pinned_comp,
+ * comp_bytes, lut13, lut2 are host arrays [n] (lut pointers: device code
+ * tables). Asynchronous on `stream`; done_event recorded after the last
+ * launch if not NULL. */
+PQE_API int slot_fill_compressed_batch(const pqe_pool *pool, int n, const int32_t *dest,
+                                       const void *const *pinned_comp, const size_t *comp_bytes,
+                                       const uint8_t *const *lut13, const uint8_t *const *lut2, int32_t *status,
+                                       void *stream, void *done_event);
 
 /* ------------------------------------------------------------------------
  * Per-expert bit-width from importance ([PW] 技術的に面白い点: the router's
@@ -459,8 +498,9 @@ PQE_API int64_t pqe_module_batch_size(int E, int k, int H, int I, double hbm_gbs
  * Layer runtime -- one MoE layer over its own slot pool, one call per step.
  * A step: moe_route -> moe_permute -> per-expert counts to the host (the one
  * host synchronisation of a step; the LRU state lives on the host) ->
- * page_table_update -> for each miss slot_fill (or slot_fill_compressed) on
- * the side stream -> the compute stream waits for the refills -> page table
+ * page_table_update -> every miss refilled by one slot_fill_batch (or
+ * slot_fill_compressed_batch) on the side stream -> the compute stream waits
+ * for the refills -> page table
  * to the device -> moe_paged_ffn -> moe_combine. Sources: [EP]
  * 階層ページング and 重みの圧縮; [MG] §3 (transfers on their own stream).
  * ------------------------------------------------------------------------ */
@@ -500,7 +540,8 @@ PQE_API size_t pqe_layer_scratch_bytes(const pqe_layer_config *cfg);
 
 /* host_pages [E]: pinned pointer of each expert's page (compressed page when
  * cfg->compressed), host_page_bytes [E] its size; luts_dev: device code tables
- * [E][2][PQE_HUFF_LUT_BYTES] (w13 then w2), required when compressed;
+ * [E][2][PQE_HUFF_LUT_BYTES] (w13 then w2), required when compressed (host
+ * pages then 16-byte aligned);
  * expert_fmt_dev: device [E] PQE_FMT_* or NULL (all FP8); scratch_dev:
  * device, 256-byte aligned, >= pqe_layer_scratch_bytes(cfg). The layer keeps
  * these pointers (caller-owned) and allocates only small pinned host buffers

@@ -34,7 +34,7 @@ PQE_STATUS_TIMEOUT = 0x8
 
 PQE_FMT_FP8 = 0
 PQE_FMT_MXFP4 = 1
-PQE_HUFF_LUT_BYTES = 4096
+PQE_HUFF_LUT_BYTES = 16384
 
 LIB_PATH = _build.LIB
 
@@ -104,6 +104,8 @@ _SIGS = {
     "pqe_huff_build_lut": (I32, [P, P]),
     "fp8_exp_huff_decode": (I32, [P, SZ, P, P, I32, I32, P, P, P]),
     "slot_fill_compressed": (I32, [C.POINTER(pqe_pool), I32, P, SZ, P, SZ, P, P, P, P, P]),
+    "fp8_exp_huff_decode_batch": (I32, [I32, P, P, P, P, I32, I32, P, P, P]),
+    "slot_fill_compressed_batch": (I32, [C.POINTER(pqe_pool), I32, P, P, P, P, P, P, P, P]),
     "pqe_importance_step": (I32, [P, P, P, I32, I32, I32, C.c_double, C.c_int64, I32, I32, P, P]),
     "pqe_rank_formats": (I32, [P, I32, I32, P]),
     "pqe_module_batch_size": (C.c_int64, [I32, I32, I32, I32, C.c_double, C.c_double, I32]),
@@ -382,6 +384,32 @@ def pqe_huff_build_lut(lengths: torch.Tensor, lut: torch.Tensor):
 def fp8_exp_huff_decode(comp_page, comp_bytes, lut13, lut2, H, I, fp8_page, status, stream=None):
     _check("fp8_exp_huff_decode", lib().fp8_exp_huff_decode(_ptr(comp_page), comp_bytes, _ptr(lut13), _ptr(lut2),
                                                             H, I, _ptr(fp8_page), _ptr(status), _stream(stream)))
+
+
+def _ptr_array(xs):
+    return (C.c_void_p * len(xs))(*[_ptr(x) for x in xs])
+
+
+def fp8_exp_huff_decode_batch(comp_pages, comp_bytes, lut13, lut2, H, I, fp8_pages, status, stream=None):
+    """Lists of n tensors (or addresses): compressed pages (device or pinned host), their sizes, code tables,
+    destinations; one launch per 128 pages."""
+    n = len(comp_pages)
+    cb = (C.c_size_t * n)(*[int(b) for b in comp_bytes])
+    arrs = [_ptr_array(x) for x in (comp_pages, lut13, lut2, fp8_pages)]
+    _check("fp8_exp_huff_decode_batch", lib().fp8_exp_huff_decode_batch(
+        n, C.cast(arrs[0], C.c_void_p), C.cast(cb, C.c_void_p), C.cast(arrs[1], C.c_void_p),
+        C.cast(arrs[2], C.c_void_p), H, I, C.cast(arrs[3], C.c_void_p), _ptr(status), _stream(stream)))
+
+
+def slot_fill_compressed_batch(pool: pqe_pool, dests, pinned_comp, comp_bytes, lut13, lut2, status, stream=None,
+                               done_event=None):
+    n = len(dests)
+    d = (C.c_int32 * n)(*[int(x) for x in dests])
+    cb = (C.c_size_t * n)(*[int(b) for b in comp_bytes])
+    arrs = [_ptr_array(x) for x in (pinned_comp, lut13, lut2)]
+    _check("slot_fill_compressed_batch", lib().slot_fill_compressed_batch(
+        C.byref(pool), n, C.cast(d, C.c_void_p), C.cast(arrs[0], C.c_void_p), C.cast(cb, C.c_void_p),
+        C.cast(arrs[1], C.c_void_p), C.cast(arrs[2], C.c_void_p), _ptr(status), _stream(stream), _event(done_event)))
 
 
 def slot_fill_compressed(pool: pqe_pool, dest, pinned_comp, comp_bytes, staging, lut13, lut2, status, stream=None,

@@ -12,11 +12,14 @@
 // (Larmore & Hirschberg 1990); rows are MSB-first uint32 bitstreams starting on
 // word boundaries, cut into chunks of 64 symbols with uint16 bit offsets.
 //
-// GPU decode: one thread per 64-symbol chunk, both code tables staged in
-// shared memory, 12-bit window lookup per symbol, 64 output bytes written as
-// four 16-byte stores. Every read is bounded by the page size; a bad stream
-// sets PQE_STATUS_CORRUPT_STREAM and the thread stops.
+// Code table (resident in VRAM, built on the host from the code lengths): for
+// every 12-bit window, the whole code words at its front, at most 5, with
+// their symbols and lengths, so one lookup decodes several symbols.
+//
+// GPU decode: a batch of pages per launch, one CTA per block of chunks of one
+// matrix; described with the kernel below.
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <vector>
 
@@ -111,15 +114,35 @@ void canonical_codes(const uint8_t len[16], uint32_t code[16]) {
     for (int s = 0; s < 16; ++s) code[s] = len[s] ? next_code[len[s]]++ : 0;
 }
 
-void build_lut(const uint8_t len[16], uint8_t *lut) {
+// Multi-symbol code table: entry w (a 12-bit window, MSB first) holds
+//   bits 0-2   n, the number of whole code words at the front of w (0..5;
+//              0: no code word prefixes w),
+//   bits 3-6   their total length,
+//   bits 7-10  the length of the first,
+//   bits 12-31 their symbols, 4 bits each, the first lowest (unused: 0).
+void build_lut(const uint8_t len[16], uint8_t *lut_bytes) {
     uint32_t code[16];
     canonical_codes(len, code);
-    std::memset(lut, 0, PQE_HUFF_LUT_BYTES);
+    uint8_t one[1 << HUF_LMAX];  // (symbol << 4) | length of the code word that prefixes a window
+    std::memset(one, 0, sizeof(one));
     for (int s = 0; s < 16; ++s) {
         if (!len[s]) continue;
         const uint32_t lo = code[s] << (HUF_LMAX - len[s]);
         const uint32_t hi = (code[s] + 1) << (HUF_LMAX - len[s]);
-        for (uint32_t w = lo; w < hi; ++w) lut[w] = (uint8_t)((s << 4) | len[s]);
+        for (uint32_t w = lo; w < hi; ++w) one[w] = (uint8_t)((s << 4) | len[s]);
+    }
+    for (uint32_t w = 0; w < (1u << HUF_LMAX); ++w) {
+        uint32_t n = 0, pos = 0, l0 = 0, syms = 0;
+        while (n < 5) {
+            const uint32_t e = one[(w << pos) & ((1u << HUF_LMAX) - 1)], l = e & 15u;
+            if (l == 0 || pos + l > (uint32_t)HUF_LMAX) break;  // no whole code word left in the window
+            if (n == 0) l0 = l;
+            syms |= (e >> 4) << (4 * n);
+            pos += l;
+            ++n;
+        }
+        const uint32_t ent = n ? (n | pos << 3 | l0 << 7 | syms << 12) : 0u;
+        std::memcpy(lut_bytes + 4 * (size_t)w, &ent, 4);  // little-endian u32, as the device reads it
     }
 }
 
@@ -171,14 +194,19 @@ void encode_matrix(const uint8_t *q, int rows, int cols, const uint8_t len[16], 
     row_word[rows] = w;
 }
 
-uint64_t count_words(const uint8_t *q, int rows, int cols, const uint8_t len[16]) {
-    uint64_t words = 0;
+// code words of a matrix; false when a chunk would start at bit 65536 or later
+// of its row (chunk offsets are 16-bit)
+bool count_words(const uint8_t *q, int rows, int cols, const uint8_t len[16], uint64_t *words) {
+    *words = 0;
     for (int r = 0; r < rows; ++r) {
         uint64_t bits = 0;
-        for (int c = 0; c < cols; ++c) bits += len[(q[(size_t)r * cols + c] >> 3) & 15];
-        words += (bits + 31) / 32;
+        for (int c = 0; c < cols; ++c) {
+            if (c % HUF_CHUNK == 0 && bits > 0xFFFFu) return false;
+            bits += len[(q[(size_t)r * cols + c] >> 3) & 15];
+        }
+        *words += (bits + 31) / 32;
     }
-    return words;
+    return true;
 }
 
 void histogram(const uint8_t *q, size_t n, uint64_t freq[16]) {
@@ -189,102 +217,316 @@ void histogram(const uint8_t *q, size_t n, uint64_t freq[16]) {
 }  // namespace
 
 // ---- device: decoder --------------------------------------------------------
+//
+// One launch decodes a batch of pages. A CTA takes one block of at most 512
+// consecutive 64-symbol chunks of one matrix (whole rows), so the grid is
+// pages x blocks per page:
+//   1. it loads the block's code table (16 KiB, resident in VRAM), its row word
+//      offsets, chunk bit offsets and raw-nibble plane (16-byte loads, all
+//      issued before any is used; the source may be device memory or pinned
+//      host memory read over the host link);
+//   2. it stages the block's code words in shared memory (16-byte loads) and
+//      each thread decodes its chunks with a 64-bit bit buffer: one table
+//      lookup yields every whole code word at the front of the 12-bit window
+//      (up to 5), the exponent nibbles collect in a 64-bit accumulator and
+//      leave eight at a time into a shared exponent plane;
+//   3. the exponent plane and the raw nibbles combine into FP8 bytes, written
+//      with coalesced 16-byte stores.
+// Every read is bounded by the page size; a row that does not decode sets
+// PQE_STATUS_CORRUPT_STREAM (its bytes are then unspecified).
+
+constexpr int HD_THREADS = 256;
+constexpr int HD_UNIT_CHUNKS = 2 * HD_THREADS;  // chunks per CTA (two per thread)
+constexpr int HD_SPAN_WORDS = 4096;             // code words staged per pass (16 KiB)
+constexpr int HD_EXP_STRIDE = 9;                // exponent-plane words per chunk: 8 + 1 (bank spread)
+constexpr int HD_LUT_WORDS = PQE_HUFF_LUT_BYTES / 4;
+constexpr int HD_MAX_PAGES = 128;               // pages per launch (kernel parameter block)
+constexpr int HD_RW_WORDS = HD_UNIT_CHUNKS + 4; // row offsets of a block (<= 512 rows + 1)
+
+struct HuffBatch {
+    const uint8_t *comp[HD_MAX_PAGES];
+    const uint32_t *lut13[HD_MAX_PAGES];
+    const uint32_t *lut2[HD_MAX_PAGES];
+    uint8_t *out[HD_MAX_PAGES];
+    uint64_t comp_bytes[HD_MAX_PAGES];
+    int n, H, I;
+    int rows13_unit, rows2_unit;  // rows per CTA
+    int units13, units2;          // CTAs per matrix
+};
+
+constexpr size_t HD_SMEM = sizeof(uint32_t) * (HD_LUT_WORDS + HD_SPAN_WORDS + 8 + HD_UNIT_CHUNKS * HD_EXP_STRIDE +
+                                               HD_RW_WORDS) +
+                           HUF_HEADER + 16;
 
 __device__ __forceinline__ bool in_page(uint64_t off, uint64_t len, uint64_t comp_bytes) {
     return off <= comp_bytes && len <= comp_bytes - off;
 }
 
-__global__ void __launch_bounds__(256) huff_decode_kernel(const uint8_t *__restrict__ comp, uint64_t comp_bytes,
-                                                          const uint8_t *__restrict__ lut13,
-                                                          const uint8_t *__restrict__ lut2, int H, int I,
-                                                          uint8_t *__restrict__ out, int32_t *__restrict__ status) {
-    __shared__ __align__(16) uint8_t lut[2][PQE_HUFF_LUT_BYTES];
-    for (int i = threadIdx.x; i < PQE_HUFF_LUT_BYTES / 16; i += blockDim.x) {
-        reinterpret_cast<uint4 *>(lut[0])[i] = __ldg(reinterpret_cast<const uint4 *>(lut13) + i);
-        reinterpret_cast<uint4 *>(lut[1])[i] = __ldg(reinterpret_cast<const uint4 *>(lut2) + i);
-    }
-    __syncthreads();
-    if (comp_bytes < HUF_HEADER) {
-        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, PQE_STATUS_CORRUPT_STREAM);
-        return;
-    }
-    const HuffHeader hd = *reinterpret_cast<const HuffHeader *>(comp);
-    const PageLayout L = fp8_layout(H, I);
+__device__ bool header_ok(const HuffHeader &hd, uint64_t comp_bytes, int H, int I) {
     const uint64_t n_scale = 2 * (uint64_t)I + H;
     const uint64_t r13 = 2 * (uint64_t)I, r2 = H;
     const uint64_t nc13 = H / HUF_CHUNK, nc2 = I / HUF_CHUNK;
-    bool ok = hd.magic == HUF_MAGIC && hd.version == HUF_VERSION && hd.H == H && hd.I == I &&
-              in_page(hd.off_scales, 4 * n_scale, comp_bytes) &&
-              in_page(hd.m13.off_row_word, 4 * (r13 + 1), comp_bytes) &&
-              in_page(hd.m13.off_chunk_bit, 2 * r13 * nc13, comp_bytes) &&
-              in_page(hd.m13.off_nibbles, r13 * H / 2, comp_bytes) &&
-              hd.m13.n_words < (comp_bytes >> 2) && in_page(hd.m13.off_words, 4 * hd.m13.n_words, comp_bytes) &&
-              in_page(hd.m2.off_row_word, 4 * (r2 + 1), comp_bytes) &&
-              in_page(hd.m2.off_chunk_bit, 2 * r2 * nc2, comp_bytes) &&
-              in_page(hd.m2.off_nibbles, r2 * I / 2, comp_bytes) &&
-              hd.m2.n_words < (comp_bytes >> 2) && in_page(hd.m2.off_words, 4 * hd.m2.n_words, comp_bytes) &&
-              (hd.off_scales % 4) == 0 && (hd.m13.off_row_word % 4) == 0 && (hd.m13.off_chunk_bit % 2) == 0 &&
-              (hd.m13.off_nibbles % 16) == 0 && (hd.m13.off_words % 4) == 0 && (hd.m2.off_row_word % 4) == 0 &&
-              (hd.m2.off_chunk_bit % 2) == 0 && (hd.m2.off_nibbles % 16) == 0 && (hd.m2.off_words % 4) == 0;
-    if (!ok) {
-        if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(status, PQE_STATUS_CORRUPT_STREAM);
+    return hd.magic == HUF_MAGIC && hd.version == HUF_VERSION && hd.H == H && hd.I == I &&
+           in_page(hd.off_scales, 4 * n_scale, comp_bytes) &&
+           in_page(hd.m13.off_row_word, 4 * (r13 + 1), comp_bytes) &&
+           in_page(hd.m13.off_chunk_bit, 2 * r13 * nc13, comp_bytes) &&
+           in_page(hd.m13.off_nibbles, r13 * H / 2, comp_bytes) && hd.m13.n_words < (comp_bytes >> 2) &&
+           in_page(hd.m13.off_words, round_up(4 * hd.m13.n_words, 16), comp_bytes) &&
+           in_page(hd.m2.off_row_word, 4 * (r2 + 1), comp_bytes) &&
+           in_page(hd.m2.off_chunk_bit, 2 * r2 * nc2, comp_bytes) &&
+           in_page(hd.m2.off_nibbles, r2 * I / 2, comp_bytes) && hd.m2.n_words < (comp_bytes >> 2) &&
+           in_page(hd.m2.off_words, round_up(4 * hd.m2.n_words, 16), comp_bytes) && (hd.off_scales % 16) == 0 &&
+           (hd.m13.off_row_word % 4) == 0 && (hd.m13.off_chunk_bit % 2) == 0 && (hd.m13.off_nibbles % 16) == 0 &&
+           (hd.m13.off_words % 16) == 0 && (hd.m2.off_row_word % 4) == 0 && (hd.m2.off_chunk_bit % 2) == 0 &&
+           (hd.m2.off_nibbles % 16) == 0 && (hd.m2.off_words % 16) == 0;
+}
+
+// funnel shift left and byte permute, callable on the host as well (the chunk
+// decoder below is checked there against the encoder)
+__host__ __device__ __forceinline__ uint32_t fshl(uint32_t lo, uint32_t hi, uint32_t sh) {
+#ifdef __CUDA_ARCH__
+    return __funnelshift_l(lo, hi, sh);
+#else
+    sh &= 31u;
+    return sh ? (hi << sh) | (lo >> (32u - sh)) : hi;
+#endif
+}
+
+__host__ __device__ __forceinline__ uint32_t bperm(uint32_t x, uint32_t y, uint32_t sel) {
+#ifdef __CUDA_ARCH__
+    return __byte_perm(x, y, sel);
+#else
+    const uint64_t v = ((uint64_t)y << 32) | x;
+    uint32_t r = 0;
+    for (int i = 0; i < 4; ++i) r |= (uint32_t)((v >> (8 * ((sel >> (4 * i)) & 7u))) & 0xFFu) << (8 * i);
+    return r;
+#endif
+}
+
+// Eight exponent nibbles e and eight raw (sign | mantissa) nibbles r, symbol j
+// in bits 4j..4j+3 of both, to eight E4M3 bytes (symbol j -> byte j).
+__host__ __device__ __forceinline__ uint2 fp8_bytes8(uint32_t e, uint32_t r) {
+    const uint32_t e_ev = e & 0x0F0F0F0Fu, e_od = (e >> 4) & 0x0F0F0F0Fu;
+    const uint32_t r_ev = r & 0x0F0F0F0Fu, r_od = (r >> 4) & 0x0F0F0F0Fu;
+    const uint32_t b_ev = ((r_ev & 0x08080808u) << 4) | (e_ev << 3) | (r_ev & 0x07070707u);
+    const uint32_t b_od = ((r_od & 0x08080808u) << 4) | (e_od << 3) | (r_od & 0x07070707u);
+    return make_uint2(bperm(b_ev, b_od, 0x5140), bperm(b_ev, b_od, 0x7362));
+}
+
+// Decodes the 64 exponents of one chunk into eb[0..7] (eight nibbles per
+// word, first symbol lowest). `word(i)` returns code word i of the row's
+// stream source (the caller clamps i into readable memory); the chunk starts at
+// bit `sb` of word `w0`; `avail` is the number of bits from the chunk start to
+// the end of its row. Returns false for a stream that does not decode.
+template <class Word>
+__host__ __device__ __forceinline__ bool decode_chunk(const uint32_t *__restrict__ lut, Word word, uint32_t w0, uint32_t sb,
+                                             uint32_t avail, uint32_t *__restrict__ eb) {
+    uint32_t idx = w0 + (sb >> 5);
+    const uint32_t sh = sb & 31u;
+    const uint32_t x0 = word(idx), x1 = word(idx + 1);
+    uint32_t hi = fshl(x1, x0, sh), lo = x1 << sh;  // bit buffer, valid bits left-aligned
+    uint32_t nb = 64 - sh;                                        // valid bits in (hi:lo)
+    idx += 2;
+    uint32_t acc_lo = 0, acc_hi = 0, na = 0, o = 0, used = 0;
+    auto take = [&](uint32_t n, uint32_t t, uint32_t syms) {  // n symbols, t bits
+        const uint32_t s4 = na * 4;
+        acc_lo |= syms << s4;
+        acc_hi |= fshl(syms, 0u, s4);
+        na += n;
+        hi = fshl(lo, hi, t);
+        lo <<= t;
+        nb -= t;
+        used += t;
+        if (na >= 8) {
+            eb[o++] = acc_lo;
+            acc_lo = acc_hi;
+            acc_hi = 0;
+            na -= 8;
+        }
+        if (nb < 32) {
+            const uint32_t w = word(idx++);
+            hi |= w >> nb;
+            lo |= w << (32 - nb);
+            nb += 32;
+        }
+    };
+    // every lookup takes all of its (at most 5) symbols while 5 more still fit
+    while (o * 8 + na <= HUF_CHUNK - 5) {
+        const uint32_t ent = lut[hi >> 20];
+        if ((ent & 7u) == 0) return false;
+        take(ent & 7u, (ent >> 3) & 15u, ent >> 12);
+    }
+    // the last few: a lookup with more symbols than needed contributes its first
+    while (o * 8 + na < HUF_CHUNK) {
+        const uint32_t ent = lut[hi >> 20];
+        const uint32_t n = ent & 7u;
+        if (n == 0) return false;
+        if (n <= HUF_CHUNK - (o * 8 + na)) take(n, (ent >> 3) & 15u, ent >> 12);
+        else take(1u, (ent >> 7) & 15u, (ent >> 12) & 15u);
+    }
+    return used <= avail;
+}
+
+__global__ void __launch_bounds__(HD_THREADS, 4) huff_decode_batch_kernel(const __grid_constant__ HuffBatch b,
+                                                                          int32_t *__restrict__ status) {
+    extern __shared__ __align__(16) uint8_t hd_smem[];
+    uint32_t *lut = reinterpret_cast<uint32_t *>(hd_smem);
+    uint32_t *span = lut + HD_LUT_WORDS;
+    uint32_t *expb = span + HD_SPAN_WORDS + 8;
+    uint32_t *rw = expb + HD_UNIT_CHUNKS * HD_EXP_STRIDE;
+    HuffHeader *hdr = reinterpret_cast<HuffHeader *>(rw + HD_RW_WORDS);
+    int *flag = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(hdr) + HUF_HEADER);
+
+    const int tid = threadIdx.x;
+    const int upp = b.units13 + b.units2;
+    const int page = blockIdx.x / upp, u = blockIdx.x % upp;
+    const uint8_t *comp = b.comp[page];
+    const uint64_t cbytes = b.comp_bytes[page];
+    const int H = b.H, I = b.I;
+
+    if (tid < (int)(HUF_HEADER / 16) && cbytes >= HUF_HEADER)
+        reinterpret_cast<uint4 *>(hdr)[tid] = reinterpret_cast<const uint4 *>(comp)[tid];
+    __syncthreads();
+    if (tid == 0) *flag = cbytes >= HUF_HEADER && header_ok(*hdr, cbytes, H, I);
+    __syncthreads();
+    if (!*flag) {
+        if (tid == 0 && u == 0) atomicOr(status, PQE_STATUS_CORRUPT_STREAM);
         return;
     }
-    const uint64_t gid = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    // scales are copied raw
-    if (gid < n_scale) {
-        reinterpret_cast<float *>(out + L.s13)[gid] = reinterpret_cast<const float *>(comp + hd.off_scales)[gid];
+    const bool first = u < b.units13;
+    const int rows = first ? 2 * I : H, cols = first ? H : I, nc = cols / HUF_CHUNK;
+    const int R = first ? b.rows13_unit : b.rows2_unit;
+    const int r0 = (first ? u : u - b.units13) * R;
+    const int nr = min(R, rows - r0);
+    const int nch = nr * nc;
+    const HuffMatrixDesc d = first ? hdr->m13 : hdr->m2;
+    const PageLayout L = fp8_layout(H, I);
+
+    // 1. code table, row offsets, chunk offsets, raw nibbles (registers), scales
+    const uint4 *lut_g = reinterpret_cast<const uint4 *>(first ? b.lut13[page] : b.lut2[page]);
+    for (int i = tid; i < HD_LUT_WORDS / 4; i += HD_THREADS) reinterpret_cast<uint4 *>(lut)[i] = lut_g[i];
+    const uint32_t *rw_g = reinterpret_cast<const uint32_t *>(comp + d.off_row_word) + r0;
+    for (int i = tid; i <= nr; i += HD_THREADS) rw[i] = rw_g[i];
+    const uint16_t *cb_g = reinterpret_cast<const uint16_t *>(comp + d.off_chunk_bit) + (size_t)r0 * nc;
+    const uint32_t cb0 = tid < nch ? cb_g[tid] : 0u;
+    const uint32_t cb1 = tid + HD_THREADS < nch ? cb_g[tid + HD_THREADS] : 0u;
+    const uint4 *nib_g = reinterpret_cast<const uint4 *>(comp + d.off_nibbles + (size_t)r0 * cols / 2);
+    uint4 nib[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int q = tid + HD_THREADS * i;
+        nib[i] = q < 2 * nch ? nib_g[q] : make_uint4(0, 0, 0, 0);
     }
-    const uint64_t n13 = r13 * nc13, n2 = r2 * nc2;
-    if (gid >= n13 + n2) return;
-    const bool first = gid < n13;
-    const HuffMatrixDesc &d = first ? hd.m13 : hd.m2;
-    const uint64_t g = first ? gid : gid - n13;
-    const int cols = first ? H : I;
-    const uint64_t nc = first ? nc13 : nc2;
-    const uint64_t r = g / nc, c = g % nc;
-    const uint8_t *lt = lut[first ? 0 : 1];
-    const uint32_t *row_word = reinterpret_cast<const uint32_t *>(comp + d.off_row_word);
-    const uint32_t *words = reinterpret_cast<const uint32_t *>(comp + d.off_words);
-    const uint32_t w0 = row_word[r], w1 = row_word[r + 1];
-    if (w1 < w0 || w1 > d.n_words) {
-        atomicOr(status, PQE_STATUS_CORRUPT_STREAM);
+    if (u == 0) {
+        const uint4 *sc = reinterpret_cast<const uint4 *>(comp + hdr->off_scales);
+        uint4 *so = reinterpret_cast<uint4 *>(b.out[page] + L.s13);
+        for (int i = tid; i < (2 * I + H) / 4; i += HD_THREADS) so[i] = sc[i];
+    }
+    __syncthreads();
+    // row offsets: ascending, within the stream, and no row longer than the
+    // staging buffer (a row's last chunk starts below bit 65536, as chunk
+    // offsets are 16-bit, so a valid row has fewer than 2100 words)
+    const uint32_t cap = HD_SPAN_WORDS - 8;
+    int bad = 0;
+    for (int i = tid; i < nr; i += HD_THREADS) bad |= rw[i + 1] < rw[i] || rw[i + 1] - rw[i] > cap;
+    if (tid == 0) bad |= rw[nr] > d.n_words;
+    if (__syncthreads_or(bad)) {
+        if (tid == 0) atomicOr(status, PQE_STATUS_CORRUPT_STREAM);
         return;
     }
-    const uint32_t row_bits = (w1 - w0) * 32u;
-    uint32_t pos = reinterpret_cast<const uint16_t *>(comp + d.off_chunk_bit)[g];
-    const uint4 *nibp = reinterpret_cast<const uint4 *>(comp + d.off_nibbles + (r * cols + c * HUF_CHUNK) / 2);
-    const uint4 n0 = nibp[0], n1 = nibp[1];
-    const uint32_t nibw[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
-    uint32_t outw[16];
-    const uint32_t *wr = words + w0;
-    const uint32_t nwr = w1 - w0;
-#pragma unroll 4
-    for (int i = 0; i < HUF_CHUNK; ++i) {
-        if (pos >= row_bits) {
-            atomicOr(status, PQE_STATUS_CORRUPT_STREAM);
-            return;
+
+    // 2. rows in groups whose code words fit the staging buffer
+    bool ok = true;
+    for (int ga = 0; ga < nr;) {
+        int lo = ga + 1, hi = nr;  // largest gb with rw[gb] - rw[ga] <= cap
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (rw[mid] - rw[ga] <= cap) lo = mid;
+            else hi = mid - 1;
         }
-        const uint32_t wi = pos >> 5, sh = pos & 31;
-        const uint64_t two = ((uint64_t)wr[wi] << 32) | (wi + 1 < nwr ? wr[wi + 1] : 0u);
-        const uint32_t win = (uint32_t)(two >> (52 - sh)) & 0xFFFu;
-        const uint32_t ent = lt[win];
-        const uint32_t len = ent & 15u;
-        if (len == 0 || pos + len > row_bits) {
-            atomicOr(status, PQE_STATUS_CORRUPT_STREAM);
-            return;
+        const int gb = lo;
+        const uint64_t byte0 = d.off_words + 4 * (uint64_t)rw[ga];
+        const uint64_t a0 = byte0 & ~(uint64_t)15;
+        const uint32_t dsh = (uint32_t)(byte0 - a0) / 4;
+        const uint64_t a1 = round_up(d.off_words + 4 * (uint64_t)rw[gb], 16);
+        const int nq = (int)((a1 - a0) / 16);
+        for (int i = tid; i < nq; i += HD_THREADS)
+            reinterpret_cast<uint4 *>(span)[i] = *reinterpret_cast<const uint4 *>(comp + a0 + 16 * (uint64_t)i);
+        if (tid < 4) span[4 * nq + tid] = 0;
+        const uint32_t lim = 4 * nq + 3;
+        __syncthreads();
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {
+            const int c = tid + HD_THREADS * j;
+            if (c >= nch) break;
+            const int rr = c / nc;
+            if (rr < ga || rr >= gb) continue;
+            const uint32_t sb = j ? cb1 : cb0;
+            const uint32_t row_bits = 32 * (rw[rr + 1] - rw[rr]);
+            if (sb >= row_bits) {
+                ok = false;
+                continue;
+            }
+            auto word = [&](uint32_t i) { return span[min(i, lim)]; };
+            ok &= decode_chunk(lut, word, dsh + rw[rr] - rw[ga], sb, row_bits - sb,
+                               expb + c * HD_EXP_STRIDE);
         }
-        pos += len;
-        const uint32_t nb = (nibw[i >> 3] >> (4 * (i & 7))) & 15u;
-        const uint32_t byte = ((nb & 8u) << 4) | ((ent >> 4) << 3) | (nb & 7u);
-        if ((i & 3) == 0) outw[i >> 2] = byte;
-        else outw[i >> 2] |= byte << (8 * (i & 3));
+        __syncthreads();
+        ga = gb;
     }
-    uint4 *dst = reinterpret_cast<uint4 *>(out + (first ? L.w13 : L.w2) + r * cols + c * HUF_CHUNK);
-    dst[0] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-    dst[1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
-    dst[2] = make_uint4(outw[8], outw[9], outw[10], outw[11]);
-    dst[3] = make_uint4(outw[12], outw[13], outw[14], outw[15]);
+    if (!ok) atomicOr(status, PQE_STATUS_CORRUPT_STREAM);
+
+    // 3. exponent plane + raw nibbles -> FP8 bytes, 32 per thread and slice
+    uint4 *dst = reinterpret_cast<uint4 *>(b.out[page] + (first ? L.w13 : L.w2) + (size_t)r0 * cols);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int q = tid + HD_THREADS * i;  // 32 symbols: chunk q / 2, half q % 2
+        if (q >= 2 * nch) break;
+        const uint32_t *e = expb + (q >> 1) * HD_EXP_STRIDE + 4 * (q & 1);
+        const uint2 a = fp8_bytes8(e[0], nib[i].x), bb = fp8_bytes8(e[1], nib[i].y);
+        const uint2 c = fp8_bytes8(e[2], nib[i].z), dd = fp8_bytes8(e[3], nib[i].w);
+        dst[2 * q] = make_uint4(a.x, a.y, bb.x, bb.y);
+        dst[2 * q + 1] = make_uint4(c.x, c.y, dd.x, dd.y);
+    }
+}
+
+// launch over n pages (n <= HD_MAX_PAGES per launch)
+int launch_decode_batch(int n, const void *const *comp, const size_t *comp_bytes, const uint8_t *const *lut13,
+                        const uint8_t *const *lut2, int H, int I, uint8_t *const *out, int32_t *status,
+                        cudaStream_t s) {
+    static std::atomic<int> attr_set[PQE_MAX_DEVICES];
+    int dev = 0, sms = 0;
+    const int di = device_info(dev, sms);
+    if (di != PQE_OK) return di;
+    if (!attr_set[dev].load(std::memory_order_relaxed)) {
+        PQE_CUDA_TRY(cudaFuncSetAttribute(huff_decode_batch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)HD_SMEM));
+        attr_set[dev].store(1, std::memory_order_relaxed);
+    }
+    const int nc13 = H / HUF_CHUNK, nc2 = I / HUF_CHUNK;
+    const int R13 = HD_UNIT_CHUNKS / nc13, R2 = HD_UNIT_CHUNKS / nc2;
+    const int u13 = (2 * I + R13 - 1) / R13, u2 = (H + R2 - 1) / R2;
+    for (int i0 = 0; i0 < n; i0 += HD_MAX_PAGES) {
+        HuffBatch b{};
+        b.n = n - i0 < HD_MAX_PAGES ? n - i0 : HD_MAX_PAGES;
+        b.H = H;
+        b.I = I;
+        b.rows13_unit = R13;
+        b.rows2_unit = R2;
+        b.units13 = u13;
+        b.units2 = u2;
+        for (int j = 0; j < b.n; ++j) {
+            b.comp[j] = static_cast<const uint8_t *>(comp[i0 + j]);
+            b.comp_bytes[j] = comp_bytes[i0 + j];
+            b.lut13[j] = reinterpret_cast<const uint32_t *>(lut13[i0 + j]);
+            b.lut2[j] = reinterpret_cast<const uint32_t *>(lut2[i0 + j]);
+            b.out[j] = out[i0 + j];
+        }
+        const unsigned grid = (unsigned)b.n * (unsigned)(u13 + u2);
+        huff_decode_batch_kernel<<<grid, HD_THREADS, HD_SMEM, s>>>(b, status);
+        PQE_LAUNCH_CHECK();
+    }
+    return PQE_OK;
 }
 
 }  // namespace pqe
@@ -322,7 +564,9 @@ int pqe_huff_encode_page(const uint8_t *fp8_page, int H, int I, void *out, size_
     histogram(q13, (size_t)r13 * H, f13);
     histogram(q2, (size_t)r2 * I, f2);
     if (!code_lengths(f13, HUF_LMAX, hd.len13) || !code_lengths(f2, HUF_LMAX, hd.len2)) return PQE_ERR_CORRUPT;
-    const uint64_t nw13 = count_words(q13, r13, H, hd.len13), nw2 = count_words(q2, r2, I, hd.len2);
+    uint64_t nw13 = 0, nw2 = 0;
+    if (!count_words(q13, r13, H, hd.len13, &nw13) || !count_words(q2, r2, I, hd.len2, &nw2))
+        return PQE_ERR_CAPACITY;
     size_t off = HUF_HEADER;
     hd.off_scales = off;
     off += round_up(4 * (2 * (size_t)I + H), 256);
@@ -372,14 +616,22 @@ int fp8_exp_huff_decode(const void *comp_page, size_t comp_bytes, const uint8_t 
                         int I, uint8_t *fp8_page, int32_t *status, void *stream) {
     PQE_CHECK_ARG(comp_page && lut13 && lut2 && fp8_page && status && shape_ok(H, I));
     PQE_CHECK_ARG(aligned(comp_page, 256) && aligned(fp8_page, 16) && aligned(lut13, 16) && aligned(lut2, 16));
-    const uint64_t chunks = (uint64_t)2 * I * (H / HUF_CHUNK) + (uint64_t)H * (I / HUF_CHUNK);
-    const uint64_t n_scale = 2 * (uint64_t)I + H;
-    const uint64_t threads = chunks > n_scale ? chunks : n_scale;
-    const unsigned grid = (unsigned)((threads + 255) / 256);
-    huff_decode_kernel<<<grid, 256, 0, as_stream(stream)>>>(static_cast<const uint8_t *>(comp_page), comp_bytes,
-                                                            lut13, lut2, H, I, fp8_page, status);
-    PQE_LAUNCH_CHECK();
-    return PQE_OK;
+    return launch_decode_batch(1, &comp_page, &comp_bytes, &lut13, &lut2, H, I, &fp8_page, status,
+                               as_stream(stream));
+}
+
+int fp8_exp_huff_decode_batch(int n, const void *const *comp_pages, const size_t *comp_bytes,
+                              const uint8_t *const *lut13, const uint8_t *const *lut2, int H, int I,
+                              uint8_t *const *fp8_pages, int32_t *status, void *stream) {
+    PQE_CHECK_ARG(n >= 0 && status && shape_ok(H, I));
+    if (n == 0) return PQE_OK;
+    PQE_CHECK_ARG(comp_pages && comp_bytes && lut13 && lut2 && fp8_pages);
+    for (int i = 0; i < n; ++i) {
+        PQE_CHECK_ARG(comp_pages[i] && lut13[i] && lut2[i] && fp8_pages[i]);
+        PQE_CHECK_ARG(aligned(comp_pages[i], 16) && aligned(fp8_pages[i], 16) && aligned(lut13[i], 16) &&
+                      aligned(lut2[i], 16));
+    }
+    return launch_decode_batch(n, comp_pages, comp_bytes, lut13, lut2, H, I, fp8_pages, status, as_stream(stream));
 }
 
 int slot_fill_compressed(const pqe_pool *pool, int dest, const void *pinned_comp, size_t comp_bytes, void *staging,
@@ -392,6 +644,26 @@ int slot_fill_compressed(const pqe_pool *pool, int dest, const void *pinned_comp
     PQE_CUDA_TRY(cudaMemcpyAsync(staging, pinned_comp, comp_bytes, cudaMemcpyHostToDevice, s));
     int rc = fp8_exp_huff_decode(staging, comp_bytes, lut13, lut2, pool->H, pool->I, dst, status, stream);
     if (rc != PQE_OK) return rc;
+    if (done_event) PQE_CUDA_TRY(cudaEventRecord(reinterpret_cast<cudaEvent_t>(done_event), s));
+    return PQE_OK;
+}
+
+int slot_fill_compressed_batch(const pqe_pool *pool, int n, const int32_t *dest, const void *const *pinned_comp,
+                               const size_t *comp_bytes, const uint8_t *const *lut13, const uint8_t *const *lut2,
+                               int32_t *status, void *stream, void *done_event) {
+    PQE_CHECK_ARG(pool && n >= 0 && status);
+    auto s = as_stream(stream);
+    if (n > 0) {
+        PQE_CHECK_ARG(dest && pinned_comp && comp_bytes && lut13 && lut2);
+        std::vector<uint8_t *> dst((size_t)n);
+        for (int i = 0; i < n; ++i) {
+            dst[i] = static_cast<uint8_t *>(pqe_pool_slot_addr(pool, dest[i]));
+            PQE_CHECK_ARG(dst[i] && comp_bytes[i] >= HUF_HEADER);
+        }
+        const int rc = fp8_exp_huff_decode_batch(n, pinned_comp, comp_bytes, lut13, lut2, pool->H, pool->I,
+                                                 dst.data(), status, stream);
+        if (rc != PQE_OK) return rc;
+    }
     if (done_event) PQE_CUDA_TRY(cudaEventRecord(reinterpret_cast<cudaEvent_t>(done_event), s));
     return PQE_OK;
 }

@@ -7,8 +7,9 @@
 // Expert-pager article (rand.pepabo.com), "エキスパート重みの階層ページング":
 // per-layer VRAM slots managed LRU, copy-in of a missing expert, working buffer
 // when a step needs more experts than slots; "重みの圧縮": compressed host pages
-// decoded on the GPU after the copy. MoE-Gen summary (aibr.jp), "3.中核となる
-// 技術的要素": host-to-device transfers overlap compute (side stream).
+// decoded on the GPU as they arrive (one pass pulls and decodes every miss).
+// MoE-Gen summary (aibr.jp), "3.中核となる技術的要素": host-to-device transfers
+// overlap compute (side stream).
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -27,7 +28,7 @@ size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
 struct ScratchMap {
     size_t status, topk_ids, topk_w, counts, offsets, perm_src, inv, page_table, perm_ws, ffn_ws, out_perm, x_in,
-        logits_in, y_out, staging, lru, miss, host_pages, page_bytes, total;
+        logits_in, y_out, lru, miss, host_pages, page_bytes, total;
     size_t perm_ws_bytes, ffn_ws_bytes, staging_bytes;
 };
 
@@ -56,8 +57,9 @@ ScratchMap scratch_map(const pqe_layer_config &c) {
     m.x_in = take(sizeof(uint16_t) * (size_t)c.max_T * c.H);
     m.logits_in = take(sizeof(float) * (size_t)c.max_T * c.E);
     m.y_out = take(sizeof(uint16_t) * (size_t)c.max_T * c.H);
+    // compressed refills are decoded straight from the host pages (no staging);
+    // staging_bytes only bounds a compressed page's size
     m.staging_bytes = c.compressed ? pqe_huff_page_bound(c.H, c.I) : 0;
-    m.staging = take(m.staging_bytes);
     if (c.device_pager) {
         m.lru = take(pqe_lru_device_bytes(c.E, c.S));
         m.miss = take(sizeof(int32_t) * (3 * (size_t)c.E + 3));
@@ -92,8 +94,9 @@ struct pqe_layer {
     int32_t *pinned = nullptr;  // counts [E], page table [E], miss expert [E], miss dest [E]
     cudaEvent_t ev_counts = nullptr, ev_fill = nullptr;
     cudaEvent_t ev_ffn_begin = nullptr, ev_ffn_end = nullptr;  // caller's, optional
-    std::vector<const void *> fill_src;  // [E] scratch for slot_fill_batch
+    std::vector<const void *> fill_src;  // [E] scratch for slot_fill_batch / slot_fill_compressed_batch
     std::vector<size_t> fill_bytes;
+    std::vector<const uint8_t *> fill_lut13, fill_lut2;
 
     template <class T>
     T *at(size_t off) const {
@@ -124,7 +127,9 @@ pqe_layer *pqe_layer_create(const pqe_layer_config *cfg, const pqe_pool *pool, c
         if (!cfg->compressed && (reinterpret_cast<uintptr_t>(host_pages[e]) % 16 || host_page_bytes[e] % 16))
             return nullptr;
         if (!cfg->compressed && host_page_bytes[e] > pool->slot_stride) return nullptr;
-        if (cfg->compressed && host_page_bytes[e] > m.staging_bytes) return nullptr;
+        if (cfg->compressed && (host_page_bytes[e] > m.staging_bytes ||
+                                reinterpret_cast<uintptr_t>(host_pages[e]) % 16))
+            return nullptr;
     }
     pqe_layer *L = new (std::nothrow) pqe_layer();
     if (!L) return nullptr;
@@ -134,6 +139,8 @@ pqe_layer *pqe_layer_create(const pqe_layer_config *cfg, const pqe_pool *pool, c
     L->host_bytes.assign(host_page_bytes, host_page_bytes + cfg->E);
     L->fill_src.assign(cfg->E, nullptr);
     L->fill_bytes.assign(cfg->E, 0);
+    L->fill_lut13.assign(cfg->E, nullptr);
+    L->fill_lut2.assign(cfg->E, nullptr);
     L->luts = luts_dev;
     L->expert_fmt = expert_fmt_dev;
     L->scratch = static_cast<uint8_t *>(scratch_dev);
@@ -182,7 +189,8 @@ int pqe_layer_set_host_page(pqe_layer *L, int expert, const void *pinned_page, s
     if (!L->cfg.compressed && (bytes > L->pool.slot_stride || bytes % 16 ||
                                reinterpret_cast<uintptr_t>(pinned_page) % 16))
         return PQE_ERR_INVALID_ARG;
-    if (L->cfg.compressed && bytes > L->map.staging_bytes) return PQE_ERR_INVALID_ARG;
+    if (L->cfg.compressed && (bytes > L->map.staging_bytes || reinterpret_cast<uintptr_t>(pinned_page) % 16))
+        return PQE_ERR_INVALID_ARG;
     L->host_pages[expert] = pinned_page;
     L->host_bytes[expert] = bytes;
     if (L->cfg.device_pager) {
@@ -304,16 +312,19 @@ int pqe_layer_step(pqe_layer *L, const void *x_dev, const float *w_router_dev, f
     local.working_buffer = wb;
     for (int i = 0; i < nm; ++i)
         if (miss_d[i] >= L->pool.n_slots + L->pool.n_wb) return PQE_ERR_CAPACITY;
-    if (c.compressed) {
+    if (c.compressed && nm > 0) {
+        // every miss of the step pulled over the host link and decoded in one pass
         for (int i = 0; i < nm; ++i) {
             const int e = miss_e[i];
-            const uint8_t *l13 = L->luts + (size_t)e * 2 * PQE_HUFF_LUT_BYTES;
-            rc = slot_fill_compressed(&L->pool, miss_d[i], L->host_pages[e], L->host_bytes[e],
-                                      L->at<void>(m.staging), m.staging_bytes, l13, l13 + PQE_HUFF_LUT_BYTES, status,
-                                      side, nullptr);
-            if (rc) return rc;
+            L->fill_src[i] = L->host_pages[e];
+            L->fill_bytes[i] = L->host_bytes[e];
+            L->fill_lut13[i] = L->luts + (size_t)e * 2 * PQE_HUFF_LUT_BYTES;
+            L->fill_lut2[i] = L->fill_lut13[i] + PQE_HUFF_LUT_BYTES;
             local.h2d_bytes += (int64_t)L->host_bytes[e];
         }
+        rc = slot_fill_compressed_batch(&L->pool, nm, miss_d, L->fill_src.data(), L->fill_bytes.data(),
+                                        L->fill_lut13.data(), L->fill_lut2.data(), status, side, nullptr);
+        if (rc) return rc;
     } else if (nm > 0) {
         // every miss of the step in one kernel launch over the host link
         for (int i = 0; i < nm; ++i) {

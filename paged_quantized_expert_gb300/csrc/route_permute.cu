@@ -6,6 +6,8 @@
 // with renormalised softmax gates is used. Permutation: MoE-Gen summary
 // (aibr.jp) "3.中核となる技術的要素", module-based batching: the assignments
 // are grouped into one contiguous batch per expert.
+#include <atomic>
+
 #include "pqe_common.cuh"
 
 namespace pqe {
@@ -332,20 +334,24 @@ __global__ void __launch_bounds__(256) quant_mxfp4_kernel(const uint8_t *__restr
 constexpr size_t PERM_STATIC_WORDS = (size_t)1 << 20;  // 4 MiB of int32 chunk histograms
 static __device__ __align__(256) int32_t g_perm_scratch[PERM_STATIC_WORDS];
 
-constexpr int MAX_DEVICES = 64;
-static int32_t *g_perm_scratch_addr[MAX_DEVICES];
+// One cached address per device. Host threads may make their first call on a
+// device at the same time: each looks the address up and stores the same
+// value, so relaxed atomics suffice (as for the launch caches of device_info).
+static std::atomic<int32_t *> g_perm_scratch_addr[PQE_MAX_DEVICES];
 
 // address of g_perm_scratch on the current device, looked up once per device
 static int perm_static_scratch(int32_t **out) {
     int dev = 0;
     PQE_CUDA_TRY(cudaGetDevice(&dev));
-    if (dev < 0 || dev >= MAX_DEVICES) return PQE_ERR_UNSUPPORTED;
-    if (!g_perm_scratch_addr[dev]) {
-        void *p = nullptr;
-        PQE_CUDA_TRY(cudaGetSymbolAddress(&p, g_perm_scratch));
-        g_perm_scratch_addr[dev] = static_cast<int32_t *>(p);
+    if (dev < 0 || dev >= PQE_MAX_DEVICES) return PQE_ERR_UNSUPPORTED;
+    int32_t *p = g_perm_scratch_addr[dev].load(std::memory_order_relaxed);
+    if (!p) {
+        void *q = nullptr;
+        PQE_CUDA_TRY(cudaGetSymbolAddress(&q, g_perm_scratch));
+        p = static_cast<int32_t *>(q);
+        g_perm_scratch_addr[dev].store(p, std::memory_order_relaxed);
     }
-    *out = g_perm_scratch_addr[dev];
+    *out = p;
     return PQE_OK;
 }
 

@@ -114,10 +114,10 @@ def test_layer_compressed_host_tier(cuda_lib, orc):
     fp8 = pages.pool_mem.view(cfg.E, stride).cpu()
     bound = pqe.pqe_huff_page_bound(cfg.H, cfg.I)
     comp = torch.zeros((cfg.E, bound), dtype=torch.uint8)
-    luts = torch.zeros((cfg.E, 2 * 4096), dtype=torch.uint8)
+    luts = torch.zeros((cfg.E, 2 * pqe.PQE_HUFF_LUT_BYTES), dtype=torch.uint8)
     sizes = []
     for e in range(cfg.E):
-        n = pqe.pqe_huff_encode_page(fp8[e].contiguous(), cfg.H, cfg.I, comp[e], luts[e, :4096], luts[e, 4096:])
+        n = pqe.pqe_huff_encode_page(fp8[e].contiguous(), cfg.H, cfg.I, comp[e], luts[e, :pqe.PQE_HUFF_LUT_BYTES], luts[e, pqe.PQE_HUFF_LUT_BYTES:])
         sizes.append(n)
     host = comp.pin_memory()
     layer = pqe.PagedMoELayer(cfg.E, cfg.H, cfg.I, cfg.k, cfg.S, cfg.E, cfg.T[0], host, sizes, compressed=True,
@@ -319,14 +319,14 @@ def test_layer_large_shapes_compressed(cuda_lib, orc):
     nb = pqe.page_bytes(pqe.PQE_FMT_FP8, H, I)
     bound = pqe.pqe_huff_page_bound(H, I)
     comp = torch.zeros((n_src, bound), dtype=torch.uint8)
-    luts_src = torch.zeros((n_src, 2 * 4096), dtype=torch.uint8)
+    luts_src = torch.zeros((n_src, 2 * pqe.PQE_HUFF_LUT_BYTES), dtype=torch.uint8)
     sizes_src, src_w = [], []
     dev_page = torch.zeros(stride, dtype=torch.uint8, device=DEV)
     for j in range(n_src):
         w13, w2 = synth.expert_weights(cfg, j)
         pqe.pqe_pack_fp8_page(torch.from_numpy(w13).to(DEV), torch.from_numpy(w2).to(DEV), H, I, dev_page)
         page = dev_page[:nb].cpu().contiguous()
-        sizes_src.append(pqe.pqe_huff_encode_page(page, H, I, comp[j], luts_src[j, :4096], luts_src[j, 4096:]))
+        sizes_src.append(pqe.pqe_huff_encode_page(page, H, I, comp[j], luts_src[j, :pqe.PQE_HUFF_LUT_BYTES], luts_src[j, pqe.PQE_HUFF_LUT_BYTES:]))
         q13, s13 = orc.quant_e4m3_rows(w13)
         q2, s2 = orc.quant_e4m3_rows(w2)
         src_w.append((q13, s13, q2, s2))

@@ -38,10 +38,44 @@ def _sections(comp: np.ndarray, H: int, I: int):
 
 def _encode_page(pqe, page: np.ndarray, H: int, I: int):
     out = torch.zeros(pqe.pqe_huff_page_bound(H, I), dtype=torch.uint8)
-    l13 = torch.zeros(4096, dtype=torch.uint8)
-    l2 = torch.zeros(4096, dtype=torch.uint8)
+    l13 = torch.zeros(pqe.PQE_HUFF_LUT_BYTES, dtype=torch.uint8)
+    l2 = torch.zeros(pqe.PQE_HUFF_LUT_BYTES, dtype=torch.uint8)
     n = pqe.pqe_huff_encode_page(torch.from_numpy(page), H, I, out, l13, l2)
     return out[:n].numpy(), l13.numpy(), l2.numpy()
+
+
+def _prefix_symbol(bits: int, nbits: int, lengths, codes):
+    """The symbol whose code word is a prefix of the nbits-bit value `bits`
+    (MSB first), with its length; (None, 0) if none fits."""
+    for s in range(16):
+        L = int(lengths[s])
+        if L and L <= nbits and (bits >> (nbits - L)) == int(codes[s]):
+            return s, L
+    return None, 0
+
+
+def _check_code_table(lut: np.ndarray, lengths, codes):
+    """Every entry holds the whole code words at the front of its 12-bit
+    window (at most 5): n in bits 0-2, their total length in bits 3-6, the first
+    one's length in bits 7-10, the symbols from bit 12 (first lowest, unused
+    slots zero); decoding stops where no whole code word fits the rest."""
+    assert lut.size == 4096
+    for w in range(4096):
+        ent = int(lut[w])
+        n, tot, l0, syms = ent & 7, (ent >> 3) & 15, (ent >> 7) & 15, ent >> 12
+        rest, left, got = w, 12, []
+        while len(got) < 5:
+            s, L = _prefix_symbol(rest, left, lengths, codes)
+            if s is None:
+                break
+            got.append((s, L))
+            left -= L
+            rest &= (1 << left) - 1
+        assert n == len(got), (w, ent, got)
+        assert tot == sum(L for _, L in got)
+        assert l0 == (got[0][1] if got else 0)
+        assert syms == sum(s << (4 * i) for i, (s, _) in enumerate(got))
+        assert (ent >> 11) & 1 == 0
 
 
 def _check_page(orc, pqe, page, H, I):
@@ -56,15 +90,8 @@ def _check_page(orc, pqe, page, H, I):
         assert np.array_equal(sec["chunk_bit" + name], ref["chunk_bit"])
         assert np.array_equal(sec["nibbles" + name], ref["nibbles"])
         assert np.array_equal(sec["words" + name], ref["words"])
-        # code table: every 12-bit window maps to the code that prefixes it
-        codes = orc.huff_codes(ref["lengths"])
-        exp = np.zeros(4096, np.uint8)
-        for s in range(16):
-            L = int(ref["lengths"][s])
-            if L:
-                lo = int(codes[s]) << (12 - L)
-                exp[lo:lo + (1 << (12 - L))] = (s << 4) | L
-        assert np.array_equal(lut, exp)
+        # code table: checked entry by entry against the oracle's canonical codes
+        _check_code_table(lut.view(np.uint32), ref["lengths"], orc.huff_codes(ref["lengths"]))
     assert np.array_equal(sec["scales"], page[lay["s13"]:lay["s13"] + 4 * (2 * I + H)])
     return comp
 
@@ -105,3 +132,19 @@ def test_encoder_matches_oracle_adversarial(orc, kind):
     s2 = np.full(H, 0.5, np.float32)
     page = helpers.fp8_page_host(pqe.page_layout(pqe.PQE_FMT_FP8, H, I), H, I, q13, s13, q2, s2)
     _check_page(orc, pqe, page, H, I)
+
+
+def test_encoder_refuses_rows_beyond_16_bit_chunk_offsets():
+    """Chunk offsets are 16-bit: a row whose chunks would start past bit 65535
+    (here 16384 symbols of ~10-bit codes) is refused, not wrapped."""
+    pqe = _pqe()
+    H, I = 16384, 64
+    g = np.random.default_rng(5)
+    q13 = np.where(g.random((2 * I, H)) < 0.9, 0x38, 0x40).astype(np.uint8)
+    q13[3] = g.permutation(np.repeat(np.arange(8, 16, dtype=np.uint8), H // 8)) << 3
+    q2 = np.full((H, I), 0x38, np.uint8)
+    page = helpers.fp8_page_host(pqe.page_layout(pqe.PQE_FMT_FP8, H, I), H, I, q13, np.ones(2 * I, np.float32), q2,
+                                 np.ones(H, np.float32))
+    with pytest.raises(pqe.PqeError) as ei:
+        _encode_page(pqe, page, H, I)
+    assert ei.value.code == pqe.PQE_ERR_CAPACITY
