@@ -52,8 +52,8 @@ def parse_args():
     ap.add_argument("--no-sweep", action="store_true", help="skip the T=1 and T=8 lines")
     ap.add_argument("--no-batched", action="store_true", help="skip the module-batched (T=16384) measurement")
     ap.add_argument("--batched-steps", type=int, default=6)
-    ap.add_argument("--workload", default="decode", choices=["decode", "batched", "large", "mixed"],
-                    help="batched / large / mixed: only that measurement (for profiling)")
+    ap.add_argument("--workload", default="decode", choices=["decode", "batched", "large", "mixed", "huff"],
+                    help="batched / large / mixed / huff (the decoder alone): only that measurement (for profiling)")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the compressed large-layer (E=512) and mixed-precision (T=4096) measurements")
     ap.add_argument("--pager", default="both", choices=["host", "device", "both"],
@@ -516,6 +516,34 @@ def _timed_steps(torch, layer, x, y, T, logits, steps, stream, side):
     return e0.elapsed_time(e1), [a.elapsed_time(b) for a, b in evs], infos
 
 
+def large_compressed_pages(pqe, torch, device, n_src):
+    """n_src distinct experts of the large layer (E=512, H=2560, I=640) as
+    Huffman-coded pages in pinned host memory, with their code tables."""
+    cfg = synth.WORKLOADS["large"]
+    H, I = cfg.H, cfg.I
+    LB = pqe.PQE_HUFF_LUT_BYTES
+    nb = pqe.page_bytes(pqe.PQE_FMT_FP8, H, I)
+    bound = pqe.pqe_huff_page_bound(H, I)
+    comp = torch.zeros((n_src, bound), dtype=torch.uint8)
+    luts_src = torch.zeros((n_src, 2 * LB), dtype=torch.uint8)
+    sizes_src = []
+    page = torch.zeros(pqe.slot_stride(H, I), dtype=torch.uint8, device=device)
+    for j in range(n_src):
+        w13, w2 = synth.expert_weights(cfg, j)
+        pqe.pqe_pack_fp8_page(torch.from_numpy(w13).to(device), torch.from_numpy(w2).to(device), H, I, page)
+        sizes_src.append(pqe.pqe_huff_encode_page(page[:nb].cpu().contiguous(), H, I, comp[j], luts_src[j, :LB],
+                                                  luts_src[j, LB:]))
+    return comp.pin_memory(), sizes_src, luts_src
+
+
+def run_huff(pqe, torch, device, n_src=32):
+    """The decoder alone on the large layer's pages (for profiling)."""
+    cfg = synth.WORKLOADS["large"]
+    comp, sizes, luts = large_compressed_pages(pqe, torch, device, n_src)
+    nb = pqe.page_bytes(pqe.PQE_FMT_FP8, cfg.H, cfg.I)
+    return huff_decode_rate(pqe, torch, device, comp, sizes, luts, cfg.H, cfg.I, nb)
+
+
 def run_large(pqe, torch, device, steps_t1=64, steps_big=3, n_src=32):
     """Large paged layer with a compressed host tier (E=512, H=2560, I=640, top-8,
     46 LRU slots): every refill copies a Huffman-coded page and decodes it on the
@@ -525,19 +553,8 @@ def run_large(pqe, torch, device, steps_t1=64, steps_big=3, n_src=32):
     bytes moved and decoded per step are those of the full layer."""
     cfg = synth.WORKLOADS["large"]
     E, H, I, k, S = cfg.E, cfg.H, cfg.I, cfg.k, cfg.S
-    stride = pqe.slot_stride(H, I)
     nb = pqe.page_bytes(pqe.PQE_FMT_FP8, H, I)
-    bound = pqe.pqe_huff_page_bound(H, I)
-    comp = torch.zeros((n_src, bound), dtype=torch.uint8)
-    luts_src = torch.zeros((n_src, 2 * pqe.PQE_HUFF_LUT_BYTES), dtype=torch.uint8)
-    sizes_src = []
-    page = torch.zeros(stride, dtype=torch.uint8, device=device)
-    for j in range(n_src):
-        w13, w2 = synth.expert_weights(cfg, j)
-        pqe.pqe_pack_fp8_page(torch.from_numpy(w13).to(device), torch.from_numpy(w2).to(device), H, I, page)
-        sizes_src.append(pqe.pqe_huff_encode_page(page[:nb].cpu().contiguous(), H, I, comp[j], luts_src[j, :pqe.PQE_HUFF_LUT_BYTES],
-                                                  luts_src[j, pqe.PQE_HUFF_LUT_BYTES:]))
-    comp = comp.pin_memory()
+    comp, sizes_src, luts_src = large_compressed_pages(pqe, torch, device, n_src)
     host = [comp[e % n_src] for e in range(E)]
     sizes = [sizes_src[e % n_src] for e in range(E)]
     luts = luts_src[torch.arange(E) % n_src].contiguous().to(device)
@@ -726,17 +743,17 @@ def main():
     device = torch.device("cuda", local)
     pqe.load()
     T, L, K, W = args.T, args.layers, args.steps, max(3, args.warmup)
+    if args.workload in ("large", "mixed", "huff"):
+        res = {"large": run_large, "mixed": run_mixed, "huff": run_huff}[args.workload](pqe, torch, device)
+        if rank == 0:
+            print(json.dumps({args.workload: res}))
+        return 0
     host = expert_pages_host(pqe, torch, device)
     graph_extra = L if args.pager != "host" else 0
     if args.workload == "batched":
         res = run_batched(pqe, torch, device, host, args.batched_steps, ws)
         if rank == 0:
             print(json.dumps({"batched": res}))
-        return 0
-    if args.workload in ("large", "mixed"):
-        res = run_large(pqe, torch, device) if args.workload == "large" else run_mixed(pqe, torch, device)
-        if rank == 0:
-            print(json.dumps({args.workload: res}))
         return 0
     r = Runner(pqe, torch, device, host, L, max(T, 64))
     xs_dev = [torch.from_numpy(synth.activations(CFG, T, s).view(np.int16)).to(device) for s in range(4)]

@@ -372,10 +372,11 @@ PQE_API int slot_fill_device(const pqe_pool *pool, const int32_t *miss, int E, c
  * Code table (kept in VRAM, [EP] 表4): 4096 little-endian uint32 entries per
  * matrix (PQE_HUFF_LUT_BYTES), built from the code lengths; the entry of a
  * 12-bit window w (the next bits of a stream, MSB first) describes the whole
- * code words at the front of w, at most 5: bits 0-2 their number n (0 when no
- * code word prefixes w), bits 3-6 their total length, bits 7-10 the length of
- * the first, bits 12-31 their symbols, 4 bits each, the first lowest, unused
- * slots zero. One lookup thus decodes up to 5 symbols.
+ * code words at the front of w, at most 5: bits 0-3 their total length, bits
+ * 4-6 their number n, bits 7-10 the length of the first, bits 12-31 their
+ * symbols, 4 bits each, the first lowest, unused slots zero. A window that no
+ * code word prefixes reads length 0, n = 1, first length 0 and bit 11 set.
+ * One lookup thus decodes up to 5 symbols.
  * ------------------------------------------------------------------------ */
 
 #define PQE_HUFF_LUT_BYTES 16384

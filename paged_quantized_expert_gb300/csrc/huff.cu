@@ -114,12 +114,15 @@ void canonical_codes(const uint8_t len[16], uint32_t code[16]) {
     for (int s = 0; s < 16; ++s) code[s] = len[s] ? next_code[len[s]]++ : 0;
 }
 
-// Multi-symbol code table: entry w (a 12-bit window, MSB first) holds
-//   bits 0-2   n, the number of whole code words at the front of w (0..5;
-//              0: no code word prefixes w),
-//   bits 3-6   their total length,
-//   bits 7-10  the length of the first,
+// Multi-symbol code table: entry w (a 12-bit window, MSB first) describes the
+// whole code words at the front of w, at most 5:
+//   bits 0-3   t, their total length (0 when no code word prefixes w),
+//   bits 4-6   n, their number (1 when no code word prefixes w),
+//   bits 7-10  the length of the first (0 when none),
+//   bit 11     set when no code word prefixes w (a corrupt stream),
 //   bits 12-31 their symbols, 4 bits each, the first lowest (unused: 0).
+// An invalid window thus yields one symbol and consumes no bits, so a decoder
+// needs no early exit: it finishes its 64 symbols and reports bit 11.
 void build_lut(const uint8_t len[16], uint8_t *lut_bytes) {
     uint32_t code[16];
     canonical_codes(len, code);
@@ -141,7 +144,7 @@ void build_lut(const uint8_t len[16], uint8_t *lut_bytes) {
             pos += l;
             ++n;
         }
-        const uint32_t ent = n ? (n | pos << 3 | l0 << 7 | syms << 12) : 0u;
+        const uint32_t ent = n ? (pos | n << 4 | l0 << 7 | syms << 12) : (1u << 4 | 1u << 11);
         std::memcpy(lut_bytes + 4 * (size_t)w, &ent, 4);  // little-endian u32, as the device reads it
     }
 }
@@ -222,22 +225,28 @@ void histogram(const uint8_t *q, size_t n, uint64_t freq[16]) {
 // consecutive 64-symbol chunks of one matrix (whole rows), so the grid is
 // pages x blocks per page:
 //   1. it loads the block's code table (16 KiB, resident in VRAM), its row word
-//      offsets, chunk bit offsets and raw-nibble plane (16-byte loads, all
-//      issued before any is used; the source may be device memory or pinned
-//      host memory read over the host link);
+//      offsets and chunk bit offsets (the source may be device memory or
+//      pinned host memory read over the host link);
 //   2. it stages the block's code words in shared memory (16-byte loads) and
-//      each thread decodes its chunks with a 64-bit bit buffer: one table
-//      lookup yields every whole code word at the front of the 12-bit window
-//      (up to 5), the exponent nibbles collect in a 64-bit accumulator and
-//      leave eight at a time into a shared exponent plane;
-//   3. the exponent plane and the raw nibbles combine into FP8 bytes, written
-//      with coalesced 16-byte stores.
+//      each thread decodes its two chunks together: one table lookup yields
+//      every whole code word at the front of the 12-bit window (up to 5), the
+//      exponent nibbles collect in a 64-bit accumulator and leave eight at a
+//      time into a shared exponent plane;
+//   3. it loads the raw-nibble plane (16-byte loads) and combines it with the
+//      exponent plane into FP8 bytes, written with coalesced 16-byte stores.
 // Every read is bounded by the page size; a row that does not decode sets
 // PQE_STATUS_CORRUPT_STREAM (its bytes are then unspecified).
 
-constexpr int HD_THREADS = 256;
+#ifndef PQE_HD_THREADS
+#define PQE_HD_THREADS 256
+#endif
+#ifndef PQE_HD_SPAN_WORDS
+#define PQE_HD_SPAN_WORDS 4096
+#endif
+constexpr int HD_THREADS = PQE_HD_THREADS;
 constexpr int HD_UNIT_CHUNKS = 2 * HD_THREADS;  // chunks per CTA (two per thread)
-constexpr int HD_SPAN_WORDS = 4096;             // code words staged per pass (16 KiB)
+constexpr int HD_SPAN_WORDS = PQE_HD_SPAN_WORDS; // code words staged per pass
+constexpr int HD_SPAN_PAD = 32;                 // zero words after them (a chunk reads <= 25 words ahead)
 constexpr int HD_EXP_STRIDE = 9;                // exponent-plane words per chunk: 8 + 1 (bank spread)
 constexpr int HD_LUT_WORDS = PQE_HUFF_LUT_BYTES / 4;
 constexpr int HD_MAX_PAGES = 128;               // pages per launch (kernel parameter block)
@@ -254,7 +263,7 @@ struct HuffBatch {
     int units13, units2;          // CTAs per matrix
 };
 
-constexpr size_t HD_SMEM = sizeof(uint32_t) * (HD_LUT_WORDS + HD_SPAN_WORDS + 8 + HD_UNIT_CHUNKS * HD_EXP_STRIDE +
+constexpr size_t HD_SMEM = sizeof(uint32_t) * (HD_LUT_WORDS + HD_SPAN_WORDS + HD_SPAN_PAD + HD_UNIT_CHUNKS * HD_EXP_STRIDE +
                                                HD_RW_WORDS) +
                            HUF_HEADER + 16;
 
@@ -313,66 +322,80 @@ __host__ __device__ __forceinline__ uint2 fp8_bytes8(uint32_t e, uint32_t r) {
     return make_uint2(bperm(b_ev, b_od, 0x5140), bperm(b_ev, b_od, 0x7362));
 }
 
-// Decodes the 64 exponents of one chunk into eb[0..7] (eight nibbles per
-// word, first symbol lowest). `word(i)` returns code word i of the row's
-// stream source (the caller clamps i into readable memory); the chunk starts at
-// bit `sb` of word `w0`; `avail` is the number of bits from the chunk start to
-// the end of its row. Returns false for a stream that does not decode.
-template <class Word>
-__host__ __device__ __forceinline__ bool decode_chunk(const uint32_t *__restrict__ lut, Word word, uint32_t w0, uint32_t sb,
-                                             uint32_t avail, uint32_t *__restrict__ eb) {
-    uint32_t idx = w0 + (sb >> 5);
-    const uint32_t sh = sb & 31u;
-    const uint32_t x0 = word(idx), x1 = word(idx + 1);
-    uint32_t hi = fshl(x1, x0, sh), lo = x1 << sh;  // bit buffer, valid bits left-aligned
-    uint32_t nb = 64 - sh;                                        // valid bits in (hi:lo)
-    idx += 2;
-    uint32_t acc_lo = 0, acc_hi = 0, na = 0, o = 0, used = 0;
-    auto take = [&](uint32_t n, uint32_t t, uint32_t syms) {  // n symbols, t bits
-        const uint32_t s4 = na * 4;
-        acc_lo |= syms << s4;
-        acc_hi |= fshl(syms, 0u, s4);
-        na += n;
-        hi = fshl(lo, hi, t);
-        lo <<= t;
-        nb -= t;
-        used += t;
-        if (na >= 8) {
-            eb[o++] = acc_lo;
-            acc_lo = acc_hi;
-            acc_hi = 0;
-            na -= 8;
-        }
-        if (nb < 32) {
-            const uint32_t w = word(idx++);
-            hi |= w >> nb;
-            lo |= w << (32 - nb);
-            nb += 32;
-        }
-    };
-    // every lookup takes all of its (at most 5) symbols while 5 more still fit
-    while (o * 8 + na <= HUF_CHUNK - 5) {
-        const uint32_t ent = lut[hi >> 20];
-        if ((ent & 7u) == 0) return false;
-        take(ent & 7u, (ent >> 3) & 15u, ent >> 12);
+// Decoder state of one 64-symbol chunk. span: the row's code words, followed
+// by at least HD_SPAN_PAD readable words (a chunk reads at most 64 * 12 bits
+// past its start); pos: the next bit of span; eb: the chunk's 8 exponent words
+// (eight nibbles each, first symbol lowest). Every step does the same work (no
+// refill or emit branch, which would diverge across the lanes of a warp): the
+// 12-bit window is cut from two span words at the bit position, and an
+// exponent word is stored once complete.
+struct ChunkDec {
+    uint32_t pos, acc_lo, acc_hi;  // next bit; pending exponent nibbles
+    uint32_t na4, o;               // 4 x pending nibbles; exponent words stored
+    uint32_t *eb;
+
+    __host__ __device__ __forceinline__ void init(uint32_t p, uint32_t *e) {
+        pos = p;
+        acc_lo = acc_hi = na4 = o = 0;
+        eb = e;
     }
-    // the last few: a lookup with more symbols than needed contributes its first
-    while (o * 8 + na < HUF_CHUNK) {
-        const uint32_t ent = lut[hi >> 20];
-        const uint32_t n = ent & 7u;
-        if (n == 0) return false;
-        if (n <= HUF_CHUNK - (o * 8 + na)) take(n, (ent >> 3) & 15u, ent >> 12);
-        else take(1u, (ent >> 7) & 15u, (ent >> 12) & 15u);
+    __host__ __device__ __forceinline__ uint32_t window(const uint32_t *__restrict__ lut,
+                                                       const uint32_t *__restrict__ span) const {
+        const uint32_t w = pos >> 5;
+        return lut[fshl(span[w + 1], span[w], pos) >> 20];  // fshl shifts by pos mod 32
     }
-    return used <= avail;
+    __host__ __device__ __forceinline__ void take(uint32_t n4, uint32_t t, uint32_t syms) {
+        pos += t;
+        acc_lo |= syms << na4;
+        acc_hi |= fshl(syms, 0u, na4);
+        na4 += n4;
+        const bool full = na4 >= 32;
+        if (full) eb[o] = acc_lo;
+        o += full;
+        acc_lo = full ? acc_hi : acc_lo;
+        acc_hi = full ? 0u : acc_hi;
+        na4 -= full ? 32u : 0u;
+    }
+    // one lookup taking all of its (at most 5) symbols: while o < 7. An
+    // invalid window consumes no bits, so once met it is met again by every
+    // later lookup: finish() alone checks for it.
+    __host__ __device__ __forceinline__ void step(const uint32_t *__restrict__ lut,
+                                                  const uint32_t *__restrict__ span) {
+        const uint32_t ent = window(lut, span);
+        take((ent >> 2) & 0x1Cu, ent & 15u, ent >> 12);
+    }
+    // the last 8 symbols: a lookup with more than needed contributes its first
+    __host__ __device__ __forceinline__ void finish(const uint32_t *__restrict__ lut,
+                                                    const uint32_t *__restrict__ span, uint32_t &bad) {
+        while (o < 8) {
+            const uint32_t ent = window(lut, span);
+            bad |= ent;
+            const uint32_t n4 = (ent >> 2) & 0x1Cu;
+            if (n4 + na4 <= 32) take(n4, ent & 15u, ent >> 12);
+            else take(4u, (ent >> 7) & 15u, (ent >> 12) & 15u);
+        }
+    }
+};
+
+// Decodes one chunk starting at bit `pos` of span, whose row ends at bit
+// `end`. Returns false for a stream that does not decode.
+__host__ __device__ __forceinline__ bool decode_chunk(const uint32_t *__restrict__ lut,
+                                                      const uint32_t *__restrict__ span, uint32_t pos, uint32_t end,
+                                                      uint32_t *__restrict__ eb) {
+    ChunkDec a;
+    a.init(pos, eb);
+    uint32_t bad = 0;
+    while (a.o < 7) a.step(lut, span);
+    a.finish(lut, span, bad);
+    return !(bad & 0x800u) && a.pos <= end;
 }
 
-__global__ void __launch_bounds__(HD_THREADS, 4) huff_decode_batch_kernel(const __grid_constant__ HuffBatch b,
+__global__ void __launch_bounds__(HD_THREADS, 1024 / HD_THREADS) huff_decode_batch_kernel(const __grid_constant__ HuffBatch b,
                                                                           int32_t *__restrict__ status) {
     extern __shared__ __align__(16) uint8_t hd_smem[];
     uint32_t *lut = reinterpret_cast<uint32_t *>(hd_smem);
     uint32_t *span = lut + HD_LUT_WORDS;
-    uint32_t *expb = span + HD_SPAN_WORDS + 8;
+    uint32_t *expb = span + HD_SPAN_WORDS + HD_SPAN_PAD;
     uint32_t *rw = expb + HD_UNIT_CHUNKS * HD_EXP_STRIDE;
     HuffHeader *hdr = reinterpret_cast<HuffHeader *>(rw + HD_RW_WORDS);
     int *flag = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(hdr) + HUF_HEADER);
@@ -411,7 +434,7 @@ __global__ void __launch_bounds__(HD_THREADS, 4) huff_decode_batch_kernel(const 
     const uint32_t cb0 = tid < nch ? cb_g[tid] : 0u;
     const uint32_t cb1 = tid + HD_THREADS < nch ? cb_g[tid + HD_THREADS] : 0u;
     const uint4 *nib_g = reinterpret_cast<const uint4 *>(comp + d.off_nibbles + (size_t)r0 * cols / 2);
-    uint4 nib[4];
+    uint4 nib[4];  // the raw-nibble plane, loaded now and used after the decode
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int q = tid + HD_THREADS * i;
@@ -452,8 +475,7 @@ __global__ void __launch_bounds__(HD_THREADS, 4) huff_decode_batch_kernel(const 
         const int nq = (int)((a1 - a0) / 16);
         for (int i = tid; i < nq; i += HD_THREADS)
             reinterpret_cast<uint4 *>(span)[i] = *reinterpret_cast<const uint4 *>(comp + a0 + 16 * (uint64_t)i);
-        if (tid < 4) span[4 * nq + tid] = 0;
-        const uint32_t lim = 4 * nq + 3;
+        if (tid < HD_SPAN_PAD) span[4 * nq + tid] = 0;
         __syncthreads();
 #pragma unroll 1
         for (int j = 0; j < 2; ++j) {
@@ -462,14 +484,13 @@ __global__ void __launch_bounds__(HD_THREADS, 4) huff_decode_batch_kernel(const 
             const int rr = c / nc;
             if (rr < ga || rr >= gb) continue;
             const uint32_t sb = j ? cb1 : cb0;
+            const uint32_t row0 = 32 * (dsh + rw[rr] - rw[ga]);  // row start, in bits of span
             const uint32_t row_bits = 32 * (rw[rr + 1] - rw[rr]);
-            if (sb >= row_bits) {
+            if (sb >= row_bits) {  // a chunk that starts past its row
                 ok = false;
                 continue;
             }
-            auto word = [&](uint32_t i) { return span[min(i, lim)]; };
-            ok &= decode_chunk(lut, word, dsh + rw[rr] - rw[ga], sb, row_bits - sb,
-                               expb + c * HD_EXP_STRIDE);
+            ok &= decode_chunk(lut, span, row0 + sb, row0 + row_bits, expb + c * HD_EXP_STRIDE);
         }
         __syncthreads();
         ga = gb;

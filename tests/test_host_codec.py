@@ -56,13 +56,15 @@ def _prefix_symbol(bits: int, nbits: int, lengths, codes):
 
 def _check_code_table(lut: np.ndarray, lengths, codes):
     """Every entry holds the whole code words at the front of its 12-bit
-    window (at most 5): n in bits 0-2, their total length in bits 3-6, the first
-    one's length in bits 7-10, the symbols from bit 12 (first lowest, unused
-    slots zero); decoding stops where no whole code word fits the rest."""
+    window (at most 5): their total length in bits 0-3, their number in bits
+    4-6, the first one's length in bits 7-10, the symbols from bit 12 (first
+    lowest, unused slots zero); decoding stops where no whole code word fits
+    the rest. A window that no code word prefixes reads n = 1, length 0 and
+    bit 11 set."""
     assert lut.size == 4096
     for w in range(4096):
         ent = int(lut[w])
-        n, tot, l0, syms = ent & 7, (ent >> 3) & 15, (ent >> 7) & 15, ent >> 12
+        tot, n, l0, inv, syms = ent & 15, (ent >> 4) & 7, (ent >> 7) & 15, (ent >> 11) & 1, ent >> 12
         rest, left, got = w, 12, []
         while len(got) < 5:
             s, L = _prefix_symbol(rest, left, lengths, codes)
@@ -71,11 +73,13 @@ def _check_code_table(lut: np.ndarray, lengths, codes):
             got.append((s, L))
             left -= L
             rest &= (1 << left) - 1
-        assert n == len(got), (w, ent, got)
+        if not got:
+            assert (tot, n, l0, inv, syms) == (0, 1, 0, 1, 0), (w, ent)
+            continue
+        assert inv == 0 and n == len(got), (w, ent, got)
         assert tot == sum(L for _, L in got)
-        assert l0 == (got[0][1] if got else 0)
+        assert l0 == got[0][1]
         assert syms == sum(s << (4 * i) for i, (s, _) in enumerate(got))
-        assert (ent >> 11) & 1 == 0
 
 
 def _check_page(orc, pqe, page, H, I):
