@@ -52,8 +52,9 @@ def parse_args():
     ap.add_argument("--no-sweep", action="store_true", help="skip the T=1 and T=8 lines")
     ap.add_argument("--no-batched", action="store_true", help="skip the module-batched (T=16384) measurement")
     ap.add_argument("--batched-steps", type=int, default=6)
-    ap.add_argument("--workload", default="decode", choices=["decode", "batched", "large", "mixed", "huff"],
-                    help="batched / large / mixed / huff (the decoder alone): only that measurement (for profiling)")
+    ap.add_argument("--workload", default="decode", choices=["decode", "batched", "large", "mixed", "huff", "ram"],
+                    help="batched / large / mixed / huff (the decoder alone) / ram (the RAM tier): only that "
+                         "measurement (for profiling)")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the compressed large-layer (E=512) and mixed-precision (T=4096) measurements")
     ap.add_argument("--pager", default="both", choices=["host", "device", "both"],
@@ -594,6 +595,91 @@ def run_large(pqe, torch, device, steps_t1=64, steps_big=3, n_src=32):
     return out
 
 
+def run_ram(pqe, torch, device, host, steps=256, L=4, Ts=(1, 8), ram_slots=(256, 128)):
+    """The decode-shaped layer (E=256, H=2048, I=512, top-8, 32 VRAM slots per
+    layer) with its refills served by a host-RAM tier over a paging file
+    (expert-pager article, SSD階層; its Table 2 compares RAM_SLOTS=256 and 128):
+    L layers round-robin, each with its own RAM slots; every page is written
+    once into one paging file, and a RAM miss is read from it by the reader
+    threads (O_DIRECT where the file system allows it). Per RAM_SLOTS and T:
+    whole steps, VRAM misses, file reads and bytes per step, and the refill
+    latency (the step time above the same steps with every page resident in
+    RAM)."""
+    E, H, I, k, S = CFG.E, CFG.H, CFG.I, CFG.k, CFG.S
+    nb = pqe.page_bytes(pqe.PQE_FMT_FP8, H, I)
+    path = os.path.join(tempfile.gettempdir(), f"pqe_paging_{os.getpid()}.bin")
+    t0 = time.perf_counter()
+    offs = pqe.pqe_paging_file_write(path, [host[e] for e in range(E)], [nb] * E)
+    write_s = time.perf_counter() - t0
+    slot = -(-nb // 4096) * 4096
+    wb = pqe.alloc_working_buffer(E, H, I, device)
+    stream = torch.cuda.current_stream(device)
+    side = torch.cuda.Stream(device)
+    out = {"workload": "decode-shaped paged layer (E=256, H=2048, I=512, top-8, CACHE_SLOTS=32) with a host-RAM "
+                       "tier per layer over a paging file of all experts", "layers_round_robin": L,
+           "paging_file_gb": E * slot / 1e9, "paging_file_write_s": write_s, "storage": tempfile.gettempdir()}
+    try:
+        for S_ram in ram_slots:
+            layers, tiers, bufs = [], [], []
+            for _ in range(L):
+                W_ram = max(Ts) * k  # a step misses at most T*k pages in VRAM
+                buf = torch.zeros((S_ram + W_ram) * slot + 4096, dtype=torch.uint8).pin_memory()
+                a = (-buf.data_ptr()) % 4096
+                ram = buf[a:a + (S_ram + W_ram) * slot]
+                tier = pqe.RamTier(path, offs, [nb] * E, S_ram, W_ram, ram, slot, n_threads=8)
+                tier.request([1 if e < S_ram else 0 for e in range(E)])  # start with full RAM slots
+                tier.wait()
+                lay = pqe.PagedMoELayer(E, H, I, k, S, E, max(Ts), host, [nb] * E, working_buffer=wb,
+                                        device=device)
+                lay.attach_ram_tier(tier)
+                layers.append(lay)
+                tiers.append(tier)
+                bufs.append(buf)
+            rec = {}
+            for T in Ts:
+                lg = [torch.from_numpy(l).to(device) for l in make_traces(T, L, 2 * L + steps)]
+                xs = [torch.from_numpy(synth.activations(CFG, T, s).view(np.int16)).to(device) for s in range(2)]
+                y = torch.zeros((T, H), dtype=torch.bfloat16, device=device)
+                for i in range(2 * L):  # warm-up
+                    layers[i % L].step(xs[i % 2], y, T, logits=lg[i], stream=stream, side_stream=side)
+                torch.cuda.synchronize()
+                st0 = [t.state()[3] for t in tiers]
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                misses = reads = 0
+                e0.record(stream)
+                for j in range(steps):
+                    i = 2 * L + j
+                    info = layers[i % L].step(xs[i % 2], y, T, logits=lg[i], stream=stream, side_stream=side)
+                    misses += info.n_miss
+                    reads += info.n_file_read
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ms = e0.elapsed_time(e1) / steps
+                st1 = [t.state()[3] for t in tiers]
+                fbytes = sum(b["bytes"] - a["bytes"] for a, b in zip(st0, st1))
+                rec[f"T={T}"] = {"ms_per_step": ms, "tokens_per_s": T / (ms / 1e3),
+                                 "vram_misses_per_step": misses / steps, "file_reads_per_step": reads / steps,
+                                 "file_mb_per_step": fbytes / steps / 1e6,
+                                 "file_read_gb_per_s": fbytes / (ms * steps / 1e3) / 1e9 if fbytes else 0.0}
+            rec["direct_io"] = tiers[0].state()[3]["direct_io"]
+            out[f"RAM_SLOTS={S_ram}"] = rec
+            for lay in layers:
+                lay.close()
+            for t in tiers:
+                t.close()
+            del bufs
+        full = out.get(f"RAM_SLOTS={max(ram_slots)}")
+        for S_ram in ram_slots:
+            if S_ram != max(ram_slots) and full:
+                for T in Ts:
+                    r = out[f"RAM_SLOTS={S_ram}"][f"T={T}"]
+                    r["refill_latency_ms_per_step"] = r["ms_per_step"] - full[f"T={T}"]["ms_per_step"]
+    finally:
+        os.unlink(path)
+    return out
+
+
 def run_mixed(pqe, torch, device, steps=12):
     """Mixed per-expert precision layer (E=256, H=2048, I=512, top-8, T=4096):
     the top 25% of experts by a seeded importance score keep FP8 pages, the
@@ -750,6 +836,11 @@ def main():
         return 0
     host = expert_pages_host(pqe, torch, device)
     graph_extra = L if args.pager != "host" else 0
+    if args.workload == "ram":
+        res = run_ram(pqe, torch, device, host)
+        if rank == 0:
+            print(json.dumps({"ram": res}))
+        return 0
     if args.workload == "batched":
         res = run_batched(pqe, torch, device, host, args.batched_steps, ws)
         if rank == 0:
@@ -831,11 +922,12 @@ def main():
     if not args.no_batched:
         r.close()
         batched = run_batched(pqe, torch, device, host, args.batched_steps, ws)
-    large = mixed = None
+    large = mixed = ram_tier = None
     if not args.no_extra:
         r.close()
         large = run_large(pqe, torch, device)
         mixed = run_mixed(pqe, torch, device)
+        ram_tier = run_ram(pqe, torch, device, host)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -878,6 +970,7 @@ def main():
             "batched": batched,
             "large": large,
             "mixed": mixed,
+            "ram_tier": ram_tier,
         }
         print(json.dumps(line))
     r.close()

@@ -62,6 +62,7 @@ extern "C" {
 #define PQE_ERR_CORRUPT (-4)
 #define PQE_ERR_TIMEOUT (-5)
 #define PQE_ERR_UNSUPPORTED (-6)
+#define PQE_ERR_IO (-7)
 
 /* bits OR-ed into the device status word */
 #define PQE_STATUS_BAD_EXPERT_ID 0x1  /* a routed id outside [0, E) */
@@ -441,6 +442,74 @@ PQE_API int slot_fill_compressed_batch(const pqe_pool *pool, int n, const int32_
                                        void *stream, void *done_event);
 
 /* ------------------------------------------------------------------------
+ * Host-RAM tier and paging file ([EP] エキスパート重みの階層ページング: each
+ * MoE layer owns slots in VRAM and in host RAM, one expert per slot, both
+ * tiers LRU, slot counts per layer; an expert missing from VRAM is copied from
+ * its RAM slot. [EP] SSD階層: at start-up all experts of all layers are written
+ * into one paging file on SSD; an expert missing from RAM too is read from it
+ * by a host thread into a RAM slot, with O_DIRECT. [EP] 重みの圧縮: the RAM and
+ * SSD tiers may hold compressed pages.)
+ * Reading (the pages say only "LRU"): the RAM tier is accessed by the VRAM
+ * tier's misses; its step is page_table_update's LRU step, with S = RAM
+ * slots, over the set of experts the VRAM tier missed; a step whose set is
+ * larger than S reads the missing pages into W RAM working entries and leaves
+ * the RAM slots as they are. Host only.
+ * ------------------------------------------------------------------------ */
+
+/* Write n pages (host memory, bytes[i] each) into a new paging file at
+ * `path`, each at a 4096-byte aligned offset (offsets[i] out, host) and padded
+ * with zeros to a multiple of 4096 bytes. PQE_ERR_IO on a file error. */
+PQE_API int pqe_paging_file_write(const char *path, int n, const void *const *pages, const size_t *bytes,
+                                  uint64_t *offsets);
+
+typedef struct pqe_ram_tier_config {
+    int32_t E;           /* experts of the layer */
+    int32_t S;           /* RAM slots (RAM_SLOTS) */
+    int32_t W;           /* RAM working entries, for a step that needs more than S pages from RAM */
+    int32_t n_threads;   /* reader threads, 1..64 */
+    int32_t direct_io;   /* 1: read with O_DIRECT where the file system allows it */
+    int32_t pad;
+    uint64_t slot_bytes; /* bytes per RAM slot: a multiple of 4096, >= every page rounded up to 4096 */
+} pqe_ram_tier_config;
+
+typedef struct pqe_ram_tier pqe_ram_tier;
+
+/* The RAM tier of one layer: expert e's page is bytes[e] bytes at offsets[e]
+ * (4096-aligned) of the paging file `path`. ram: pinned host memory of (S + W)
+ * * slot_bytes bytes, 4096-byte aligned, owned by the caller (entry s < S is
+ * RAM slot s, S + w working entry w). Starts the reader threads. NULL on bad
+ * arguments or when the file cannot be opened. */
+PQE_API pqe_ram_tier *pqe_ram_tier_create(const pqe_ram_tier_config *cfg, const char *path,
+                                          const uint64_t *offsets, const size_t *bytes, void *ram);
+/* Stops the reader threads (after the queued reads) and closes the file. */
+PQE_API void pqe_ram_tier_destroy(pqe_ram_tier *t);
+
+/* One RAM-tier step. need [E] (host): nonzero for the experts whose pages are
+ * wanted from RAM this step. Runs the LRU step, queues a file read for every
+ * page not in RAM, and returns without waiting for them. Out (host, [E]):
+ * ram_page[e], the RAM address of e's page (NULL if not needed);
+ * read_queued[e], 1 when that page is being read from the file (valid only
+ * after pqe_ram_tier_wait); *n_read, the pages read; *working, 1 for a
+ * working-entry step. Waits first for the reads of the previous call. A step
+ * needing more working entries than W returns PQE_ERR_CAPACITY. The caller
+ * must not let the GPU read a RAM slot that a later call may refill (the
+ * layer runtime orders its refills before its next step's routing read-back). */
+PQE_API int pqe_ram_tier_request(pqe_ram_tier *t, const int32_t *need, const void **ram_page,
+                                 int32_t *read_queued, int32_t *n_read, int32_t *working);
+
+/* Blocks until every queued read has landed. PQE_ERR_IO if one failed. */
+PQE_API int pqe_ram_tier_wait(pqe_ram_tier *t);
+
+/* LRU state of the RAM slots (see pqe_lru_state) and running totals
+ * stats[4] = pages read, bytes read, working-entry steps, O_DIRECT in use
+ * (0/1). Any output may be NULL. */
+PQE_API int pqe_ram_tier_state(const pqe_ram_tier *t, int32_t *slot_expert, int64_t *last_use, int64_t *step,
+                               int64_t *stats);
+
+/* Bytes of expert e's page (0 for a bad argument). */
+PQE_API size_t pqe_ram_tier_page_bytes(const pqe_ram_tier *t, int expert);
+
+/* ------------------------------------------------------------------------
  * Per-expert bit-width from importance ([PW] 技術的に面白い点: the router's
  * choices estimate each expert's importance; important experts keep more
  * bits). Importance m_e is an exponential moving average of the gate mass
@@ -519,7 +588,7 @@ typedef struct pqe_step_info {
     int32_t n_routed;       /* |U|: experts with a non-empty batch */
     int32_t n_miss;         /* pages copied in by this step */
     int32_t working_buffer; /* 1 when |U| > S */
-    int32_t pad;
+    int32_t n_file_read;    /* pages read from the paging file by the RAM tier (0 without one) */
     int64_t h2d_bytes;      /* bytes of host pages copied by this step */
 } pqe_step_info;
 
@@ -552,6 +621,15 @@ PQE_API pqe_layer *pqe_layer_create(const pqe_layer_config *cfg, const pqe_pool 
                                     const uint8_t *luts_dev, const uint8_t *expert_fmt_dev,
                                     void *scratch_dev, size_t scratch_bytes);
 PQE_API void pqe_layer_destroy(pqe_layer *L);
+
+/* Serve the layer's refills from a RAM tier (host pager only; the tier's E
+ * must equal the layer's, its pages fit the layer's format: FP8 pages of at
+ * most slot_stride bytes, or compressed pages when cfg->compressed). From
+ * then on a VRAM miss is copied from the expert's RAM page instead of
+ * host_pages: the step asks the tier for the step's misses, refills at once
+ * those already in RAM, waits for the file reads, then refills the rest. The
+ * layer does not own the tier; NULL detaches it. */
+PQE_API int pqe_layer_attach_ram_tier(pqe_layer *L, pqe_ram_tier *t);
 
 /* Point expert e at a new host page (e.g. after its format changed) and
  * forget its resident copy, so its next use refills the slot. */

@@ -26,6 +26,7 @@ PQE_ERR_CAPACITY = -3
 PQE_ERR_CORRUPT = -4
 PQE_ERR_TIMEOUT = -5
 PQE_ERR_UNSUPPORTED = -6
+PQE_ERR_IO = -7
 
 PQE_STATUS_BAD_EXPERT_ID = 0x1
 PQE_STATUS_CORRUPT_STREAM = 0x2
@@ -55,7 +56,12 @@ class pqe_layer_config(C.Structure):
 
 class pqe_step_info(C.Structure):
     _fields_ = [("n_routed", C.c_int32), ("n_miss", C.c_int32), ("working_buffer", C.c_int32),
-                ("pad", C.c_int32), ("h2d_bytes", C.c_int64)]
+                ("n_file_read", C.c_int32), ("h2d_bytes", C.c_int64)]
+
+
+class pqe_ram_tier_config(C.Structure):
+    _fields_ = [("E", C.c_int32), ("S", C.c_int32), ("W", C.c_int32), ("n_threads", C.c_int32),
+                ("direct_io", C.c_int32), ("pad", C.c_int32), ("slot_bytes", C.c_uint64)]
 
 
 class pqe_layer_buffers_t(C.Structure):
@@ -130,6 +136,14 @@ _SIGS = {
     "pqe_layer_lru_state": (I32, [P, P, P, P]),
     "pqe_layer_step": (I32, [P, P, P, P, I32, P, P, P, P]),
     "pqe_layer_step_host": (I32, [P, P, P, P, I32, P, P, P, P]),
+    "pqe_layer_attach_ram_tier": (I32, [P, P]),
+    "pqe_paging_file_write": (I32, [C.c_char_p, I32, P, P, P]),
+    "pqe_ram_tier_create": (P, [C.POINTER(pqe_ram_tier_config), C.c_char_p, P, P, P]),
+    "pqe_ram_tier_destroy": (None, [P]),
+    "pqe_ram_tier_request": (I32, [P, P, P, P, P, P]),
+    "pqe_ram_tier_wait": (I32, [P]),
+    "pqe_ram_tier_state": (I32, [P, P, P, P, P]),
+    "pqe_ram_tier_page_bytes": (SZ, [P, I32]),
 }
 
 # every entry point of include/pqe.h
@@ -419,6 +433,77 @@ def slot_fill_compressed(pool: pqe_pool, dest, pinned_comp, comp_bytes, staging,
         _ptr(lut2), _ptr(status), _stream(stream), _event(done_event)))
 
 
+# ---- RAM tier and paging file -----------------------------------------------------
+
+def pqe_paging_file_write(path: str, pages, nbytes) -> list:
+    """Write pages (host tensors / numpy arrays, or addresses) into a paging file; returns their offsets."""
+    n = len(pages)
+    srcs = (C.c_void_p * n)(*[p.ctypes.data if hasattr(p, "ctypes") else _ptr(p) for p in pages])
+    b = (C.c_size_t * n)(*[int(x) for x in nbytes])
+    offs = (C.c_uint64 * n)()
+    _check("pqe_paging_file_write", lib().pqe_paging_file_write(os.fsencode(path), n, C.cast(srcs, C.c_void_p),
+                                                                C.cast(b, C.c_void_p), C.cast(offs, C.c_void_p)))
+    return list(offs)
+
+
+class RamTier:
+    """The host-RAM tier of one layer over a paging file (pqe_ram_tier).
+
+    ``ram`` is host memory of (S + W) * slot_bytes bytes, 4096-byte aligned: a
+    pinned tensor when the GPU reads from it, any aligned buffer otherwise."""
+
+    def __init__(self, path: str, offsets, nbytes, S: int, W: int, ram, slot_bytes: int, n_threads: int = 4,
+                 direct_io: bool = True):
+        E = len(offsets)
+        self.E, self.S, self.W, self.slot_bytes = E, S, W, slot_bytes
+        self.cfg = pqe_ram_tier_config(E, S, W, n_threads, int(bool(direct_io)), 0, slot_bytes)
+        self._ram = ram
+        addr = ram.ctypes.data if hasattr(ram, "ctypes") else _ptr(ram)
+        self.ram_addr = addr
+        offs = (C.c_uint64 * E)(*[int(o) for o in offsets])
+        b = (C.c_size_t * E)(*[int(x) for x in nbytes])
+        self._h = lib().pqe_ram_tier_create(C.byref(self.cfg), os.fsencode(path), C.cast(offs, C.c_void_p),
+                                            C.cast(b, C.c_void_p), addr)
+        if not self._h:
+            raise PqeError("pqe_ram_tier_create", PQE_ERR_INVALID_ARG)
+        self._page = (C.c_void_p * E)()
+        self._queued = (C.c_int32 * E)()
+
+    def close(self):
+        if getattr(self, "_h", None) and _lib is not None:
+            _lib.pqe_ram_tier_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    def request(self, need):
+        """need [E] (nonzero = wanted from RAM) -> (RAM addresses [E] (None if not needed), read_queued [E],
+        n_read, working)."""
+        nd = (C.c_int32 * self.E)(*[int(x) for x in need])
+        nr = C.c_int32(0)
+        wb = C.c_int32(0)
+        _check("pqe_ram_tier_request", lib().pqe_ram_tier_request(self._h, C.cast(nd, C.c_void_p),
+                                                                  C.cast(self._page, C.c_void_p),
+                                                                  C.cast(self._queued, C.c_void_p), C.byref(nr),
+                                                                  C.byref(wb)))
+        return list(self._page), list(self._queued), nr.value, bool(wb.value)
+
+    def wait(self):
+        _check("pqe_ram_tier_wait", lib().pqe_ram_tier_wait(self._h))
+
+    def state(self):
+        se = (C.c_int32 * max(self.S, 1))()
+        lu = (C.c_int64 * max(self.S, 1))()
+        st = C.c_int64(0)
+        stats = (C.c_int64 * 4)()
+        _check("pqe_ram_tier_state", lib().pqe_ram_tier_state(self._h, C.cast(se, C.c_void_p),
+                                                              C.cast(lu, C.c_void_p), C.byref(st),
+                                                              C.cast(stats, C.c_void_p)))
+        return (list(se)[:self.S], list(lu)[:self.S], st.value,
+                {"reads": stats[0], "bytes": stats[1], "working_steps": stats[2], "direct_io": bool(stats[3])})
+
+
 # ---- bit-width assignment ---------------------------------------------------------
 
 def pqe_importance_step(m: torch.Tensor, ids: torch.Tensor, gates: torch.Tensor, T, k, E, alpha, step, every,
@@ -535,6 +620,11 @@ class PagedMoELayer:
             self._h, _ptr(x_host), _ptr(w_router), _ptr(logits_host), T, _ptr(y_host), _stream(stream),
             _stream(side_stream) if side_stream is not None else None, C.byref(self.info)))
         return self.info
+
+    def attach_ram_tier(self, tier: Optional["RamTier"]):
+        """Serve refills from a RAM tier (host pager only); None detaches it."""
+        self._ram_tier = tier
+        _check("pqe_layer_attach_ram_tier", lib().pqe_layer_attach_ram_tier(self._h, tier._h if tier else None))
 
     def set_ffn_events(self, ev_begin, ev_end):
         _check("pqe_layer_set_ffn_events", lib().pqe_layer_set_ffn_events(self._h, _event(ev_begin),

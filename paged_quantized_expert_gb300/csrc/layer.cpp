@@ -12,6 +12,7 @@
 // overlap compute (side stream).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -97,12 +98,39 @@ struct pqe_layer {
     std::vector<const void *> fill_src;  // [E] scratch for slot_fill_batch / slot_fill_compressed_batch
     std::vector<size_t> fill_bytes;
     std::vector<const uint8_t *> fill_lut13, fill_lut2;
+    std::vector<int32_t> fill_dest, fill_expert;
+    // optional RAM tier: the step's misses are served from its RAM pages
+    pqe_ram_tier *ram = nullptr;
+    std::vector<int32_t> ram_need, ram_queued;
+    std::vector<const void *> ram_page;
+    std::vector<size_t> ram_bytes;
 
     template <class T>
     T *at(size_t off) const {
         return reinterpret_cast<T *>(scratch + off);
     }
 };
+
+namespace {
+
+// Refills the n pages described by L->fill_* on `side`: one pull+decode pass
+// for compressed pages, one bulk pull for FP8 pages.
+int refill(pqe_layer *L, int n, cudaStream_t side, int32_t *status) {
+    if (n == 0) return PQE_OK;
+    if (L->cfg.compressed) {
+        for (int i = 0; i < n; ++i) {
+            L->fill_lut13[i] = L->luts + (size_t)L->fill_expert[i] * 2 * PQE_HUFF_LUT_BYTES;
+            L->fill_lut2[i] = L->fill_lut13[i] + PQE_HUFF_LUT_BYTES;
+        }
+        return slot_fill_compressed_batch(&L->pool, n, L->fill_dest.data(), L->fill_src.data(),
+                                          L->fill_bytes.data(), L->fill_lut13.data(), L->fill_lut2.data(), status,
+                                          side, nullptr);
+    }
+    return slot_fill_batch(&L->pool, n, L->fill_dest.data(), L->fill_src.data(), L->fill_bytes.data(), side,
+                           nullptr);
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -141,6 +169,8 @@ pqe_layer *pqe_layer_create(const pqe_layer_config *cfg, const pqe_pool *pool, c
     L->fill_bytes.assign(cfg->E, 0);
     L->fill_lut13.assign(cfg->E, nullptr);
     L->fill_lut2.assign(cfg->E, nullptr);
+    L->fill_dest.assign(cfg->E, 0);
+    L->fill_expert.assign(cfg->E, 0);
     L->luts = luts_dev;
     L->expert_fmt = expert_fmt_dev;
     L->scratch = static_cast<uint8_t *>(scratch_dev);
@@ -182,6 +212,30 @@ void pqe_layer_destroy(pqe_layer *L) {
     if (L->pinned) cudaFreeHost(L->pinned);
     pqe_lru_destroy(L->lru);
     delete L;
+}
+
+int pqe_layer_attach_ram_tier(pqe_layer *L, pqe_ram_tier *t) {
+    if (!L) return PQE_ERR_INVALID_ARG;
+    if (!t) {
+        L->ram = nullptr;
+        return PQE_OK;
+    }
+    if (L->cfg.device_pager) return PQE_ERR_UNSUPPORTED;
+    const int E = L->cfg.E;
+    std::vector<size_t> b(E);
+    for (int e = 0; e < E; ++e) {
+        b[e] = pqe_ram_tier_page_bytes(t, e);
+        if (b[e] == 0) return PQE_ERR_INVALID_ARG;  // the tier has fewer experts than the layer
+        if (!L->cfg.compressed && (b[e] > L->pool.slot_stride || b[e] % 16)) return PQE_ERR_INVALID_ARG;
+        if (L->cfg.compressed && b[e] > L->map.staging_bytes) return PQE_ERR_INVALID_ARG;
+    }
+    if (pqe_ram_tier_page_bytes(t, E) != 0) return PQE_ERR_INVALID_ARG;  // more experts than the layer
+    L->ram_bytes = std::move(b);
+    L->ram_need.assign(E, 0);
+    L->ram_queued.assign(E, 0);
+    L->ram_page.assign(E, nullptr);
+    L->ram = t;
+    return PQE_OK;
 }
 
 int pqe_layer_set_host_page(pqe_layer *L, int expert, const void *pinned_page, size_t bytes) {
@@ -312,28 +366,40 @@ int pqe_layer_step(pqe_layer *L, const void *x_dev, const float *w_router_dev, f
     local.working_buffer = wb;
     for (int i = 0; i < nm; ++i)
         if (miss_d[i] >= L->pool.n_slots + L->pool.n_wb) return PQE_ERR_CAPACITY;
-    if (c.compressed && nm > 0) {
-        // every miss of the step pulled over the host link and decoded in one pass
+    if (L->ram && nm > 0) {
+        // RAM tier: the misses whose pages are in RAM are refilled at once, the
+        // others after the paging-file reads have landed
+        std::fill(L->ram_need.begin(), L->ram_need.end(), 0);
+        for (int i = 0; i < nm; ++i) L->ram_need[miss_e[i]] = 1;
+        int32_t nr = 0, rwb = 0;
+        rc = pqe_ram_tier_request(L->ram, L->ram_need.data(), L->ram_page.data(), L->ram_queued.data(), &nr, &rwb);
+        if (rc) return rc;
+        local.n_file_read = nr;
+        for (int pass = 0; pass < 2; ++pass) {
+            if (pass == 1 && nr > 0 && (rc = pqe_ram_tier_wait(L->ram))) return rc;
+            int n = 0;
+            for (int i = 0; i < nm; ++i) {
+                const int e = miss_e[i];
+                if (L->ram_queued[e] != pass) continue;
+                L->fill_expert[n] = e;
+                L->fill_dest[n] = miss_d[i];
+                L->fill_src[n] = L->ram_page[e];
+                L->fill_bytes[n] = L->ram_bytes[e];
+                ++n;
+            }
+            if ((rc = refill(L, n, side, status))) return rc;
+        }
+        for (int i = 0; i < nm; ++i) local.h2d_bytes += (int64_t)L->ram_bytes[miss_e[i]];
+    } else if (nm > 0) {
         for (int i = 0; i < nm; ++i) {
             const int e = miss_e[i];
+            L->fill_expert[i] = e;
+            L->fill_dest[i] = miss_d[i];
             L->fill_src[i] = L->host_pages[e];
             L->fill_bytes[i] = L->host_bytes[e];
-            L->fill_lut13[i] = L->luts + (size_t)e * 2 * PQE_HUFF_LUT_BYTES;
-            L->fill_lut2[i] = L->fill_lut13[i] + PQE_HUFF_LUT_BYTES;
             local.h2d_bytes += (int64_t)L->host_bytes[e];
         }
-        rc = slot_fill_compressed_batch(&L->pool, nm, miss_d, L->fill_src.data(), L->fill_bytes.data(),
-                                        L->fill_lut13.data(), L->fill_lut2.data(), status, side, nullptr);
-        if (rc) return rc;
-    } else if (nm > 0) {
-        // every miss of the step in one kernel launch over the host link
-        for (int i = 0; i < nm; ++i) {
-            L->fill_src[i] = L->host_pages[miss_e[i]];
-            L->fill_bytes[i] = L->host_bytes[miss_e[i]];
-            local.h2d_bytes += (int64_t)L->host_bytes[miss_e[i]];
-        }
-        rc = slot_fill_batch(&L->pool, nm, miss_d, L->fill_src.data(), L->fill_bytes.data(), side, nullptr);
-        if (rc) return rc;
+        if ((rc = refill(L, nm, side, status))) return rc;
     }
     if (nm > 0 && side != s) {
         ce = cudaEventRecord(L->ev_fill, side);

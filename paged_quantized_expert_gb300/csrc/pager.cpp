@@ -49,6 +49,7 @@ const char *pqe_strerror(int code) {
     case PQE_ERR_CORRUPT: return "corrupt compressed page";
     case PQE_ERR_TIMEOUT: return "timed out";
     case PQE_ERR_UNSUPPORTED: return "unsupported";
+    case PQE_ERR_IO: return "paging file I/O error";
     default: return "unknown error";
     }
 }

@@ -24,7 +24,22 @@ def _host_tier(pqe, pages: Pages):
     return host, nbytes
 
 
-def _run_trace(pqe, orc, cfg, T, steps, S, W, check_every, n_check, side=True, host_api=False, device_pager=False):
+def _ram_tier(pqe, host, nbytes, S_ram, W_ram, path, n_threads=4):
+    """A RAM tier of S_ram slots (+ W_ram working entries) over a paging file
+    holding the host tier's pages; RAM is pinned (the GPU pulls from it)."""
+    E = len(nbytes)
+    offs = pqe.pqe_paging_file_write(path, [host[e] for e in range(E)], nbytes)
+    slot = -(-max(nbytes) // 4096) * 4096
+    buf = torch.zeros((S_ram + W_ram) * slot + 4096, dtype=torch.uint8).pin_memory()
+    a = (-buf.data_ptr()) % 4096
+    ram = buf[a:a + (S_ram + W_ram) * slot]
+    tier = pqe.RamTier(path, offs, nbytes, S_ram, W_ram, ram, slot, n_threads=n_threads)
+    tier._buf = buf
+    return tier
+
+
+def _run_trace(pqe, orc, cfg, T, steps, S, W, check_every, n_check, side=True, host_api=False, device_pager=False,
+               ram_slots=None, ram_wb=0, tmp_path=None):
     # experts the checked tokens of the checked steps use get oracle weights
     tr = synth.RoutingTrace(cfg, T)
     logits_all = [tr.step(s) for s in range(steps)]
@@ -40,6 +55,12 @@ def _run_trace(pqe, orc, cfg, T, steps, S, W, check_every, n_check, side=True, h
     layer = pqe.PagedMoELayer(cfg.E, cfg.H, cfg.I, cfg.k, S, W, T, host, nbytes, expert_fmt=pages.fmt_dev,
                               device_pager=device_pager)
     ref_lru = orc.LRU(cfg.E, S)
+    tier = ref_ram = None
+    if ram_slots is not None:
+        tier = _ram_tier(pqe, host, nbytes, ram_slots, ram_wb, str(tmp_path / "experts.pqe"))
+        layer.attach_ram_tier(tier)
+        ref_ram = orc.LRU(cfg.E, ram_slots)
+        n_file = 0
     stream = torch.cuda.current_stream()
     side_stream = torch.cuda.Stream() if side else None
     y = torch.zeros((T, cfg.H), dtype=torch.bfloat16, device=DEV)
@@ -66,6 +87,15 @@ def _run_trace(pqe, orc, cfg, T, steps, S, W, check_every, n_check, side=True, h
         assert np.array_equal(se.numpy(), se2) and np.array_equal(lu.numpy(), lu2) and st == st2
         if not device_pager:
             assert info.n_miss == len(me) and info.working_buffer == int(wb)
+        if tier is not None:  # the RAM tier: the oracle's LRU with ram_slots, driven by the VRAM misses
+            need = np.zeros(cfg.E, np.int32)
+            need[me] = 1
+            _, r_miss, _, _ = ref_ram.step(need)
+            rse, rlu, rst, _ = tier.state()
+            se3, lu3, st3 = ref_ram.state()
+            assert rse == se3.tolist() and rlu == lu3.tolist() and rst == st3
+            assert info.n_file_read == len(r_miss)
+            n_file += len(r_miss)
         n_wb += int(wb)
         torch.cuda.synchronize()
         if s in checks:
@@ -80,6 +110,9 @@ def _run_trace(pqe, orc, cfg, T, steps, S, W, check_every, n_check, side=True, h
     status = layer.device_view("status", torch.int32, (1,)).item()
     assert status == 0
     layer.close()
+    if tier is not None:
+        assert n_file > 0
+        tier.close()
     return worst, n_wb
 
 
@@ -99,13 +132,33 @@ def test_layer_trace_decode_T64_working_buffer(cuda_lib, orc):
     assert n_wb == 6   # |U| > 32 at T=64 every step
 
 
+def test_layer_ram_tier_decode_T8(cuda_lib, orc, tmp_path):
+    """Pages come from a paging file through 40 RAM slots (of 256 experts) and
+    32 VRAM slots: RAM misses are read from the file, then pulled to VRAM."""
+    cfg = synth.WORKLOADS["decode"]
+    _run_trace(cuda_lib, orc, cfg, T=8, steps=24, S=cfg.S, W=64, check_every=7, n_check=2, ram_slots=40,
+               ram_wb=64, tmp_path=tmp_path)
+
+
+def test_layer_ram_tier_working_entries_T64(cuda_lib, orc, tmp_path):
+    """T=64: ~140 VRAM misses per step against 128 RAM slots, so the RAM tier
+    takes working-entry steps too."""
+    cfg = synth.WORKLOADS["decode"]
+    _run_trace(cuda_lib, orc, cfg, T=64, steps=5, S=cfg.S, W=cfg.E, check_every=4, n_check=2, ram_slots=128,
+               ram_wb=cfg.E, tmp_path=tmp_path)
+
+
 def test_layer_step_host_buffers(cuda_lib, orc):
     cfg = synth.small_config(E=12, H=256, I=128, k=3, T=20, S=5, cid=94, reuse_p=0.5, zipf_s=1.1,
                              router_gemm=False, steps=12)
     _run_trace(cuda_lib, orc, cfg, T=20, steps=12, S=5, W=12, check_every=4, n_check=20, host_api=True)
 
 
-def test_layer_compressed_host_tier(cuda_lib, orc):
+@pytest.mark.parametrize("ram", [False, True])
+def test_layer_compressed_host_tier(cuda_lib, orc, tmp_path, ram):
+    """Compressed pages pulled and decoded into the slots; with `ram`, they
+    come from a paging file through a RAM tier of 4 slots (compressed pages in
+    RAM and in the file, as the article's compressed configurations hold)."""
     pqe = cuda_lib
     cfg = synth.small_config(E=10, H=256, I=128, k=2, T=6, S=3, cid=95, reuse_p=0.5, zipf_s=1.1,
                              router_gemm=False, steps=10)
@@ -122,6 +175,10 @@ def test_layer_compressed_host_tier(cuda_lib, orc):
     host = comp.pin_memory()
     layer = pqe.PagedMoELayer(cfg.E, cfg.H, cfg.I, cfg.k, cfg.S, cfg.E, cfg.T[0], host, sizes, compressed=True,
                               luts=luts.to(DEV), expert_fmt=pages.fmt_dev)
+    tier = None
+    if ram:
+        tier = _ram_tier(pqe, host, sizes, 4, cfg.E, str(tmp_path / "comp.pqe"), n_threads=2)
+        layer.attach_ram_tier(tier)
     tr = synth.RoutingTrace(cfg, 6)
     ref_lru = orc.LRU(cfg.E, cfg.S)
     y = torch.zeros((6, cfg.H), dtype=torch.bfloat16, device=DEV)
@@ -150,6 +207,9 @@ def test_layer_compressed_host_tier(cuda_lib, orc):
             got = layer.pool_mem[slot * stride:slot * stride + lay["bytes"]].cpu()
             assert torch.equal(got, fp8[e, :lay["bytes"]])
     layer.close()
+    if tier is not None:
+        assert tier.state()[3]["reads"] > 0
+        tier.close()
 
 
 def test_layer_capacity_error(cuda_lib, orc):
