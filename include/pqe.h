@@ -86,6 +86,21 @@ PQE_API int pqe_last_cuda_error(void);
 /* Kernels this library has launched in this process (all threads). */
 PQE_API uint64_t pqe_kernel_launches(void);
 
+/* Every wait inside a kernel of this library (on an mbarrier, or on a count
+ * another CTA publishes) is bounded: after `polls` polls it gives up, ORs
+ * PQE_STATUS_TIMEOUT into the call's status word, stops waiting for the rest
+ * of the launch and lets the kernel run to its end, so the call returns and
+ * the CUDA context stays usable (the outputs of that call are then
+ * unspecified). Process-wide, read at each launch; 0 restores the default of
+ * 2^22 polls (a fraction of a second). */
+PQE_API int pqe_set_wait_limit(uint32_t polls);
+
+/* Test hook for the expiry path above, with no GPU fault: adds `bias` to the
+ * count of phase-1 work that phase 2 of every expert in the weight-stream FFN
+ * kernel waits for, so any nonzero bias makes those waits expire. Process-wide,
+ * read at each launch; 0 (the default) in normal use. */
+PQE_API int pqe_test_set_phase2_bias(uint32_t bias);
+
 /* ------------------------------------------------------------------------
  * Expert pages and the slot pool  ([EP] 階層ページング; [PW] page-unit weights)
  *

@@ -84,6 +84,8 @@ _SIGS = {
     "pqe_abi_version": (I32, []),
     "pqe_last_cuda_error": (I32, []),
     "pqe_kernel_launches": (C.c_uint64, []),
+    "pqe_set_wait_limit": (I32, [C.c_uint32]),
+    "pqe_test_set_phase2_bias": (I32, [C.c_uint32]),
     "pqe_layer_set_ffn_events": (I32, [P, P, P]),
     "pqe_page_bytes": (SZ, [I32, I32, I32]),
     "pqe_slot_stride": (SZ, [I32, I32]),
@@ -660,6 +662,16 @@ class PagedMoELayer:
         base = self.scratch.data_ptr()
         off = ptr - base
         return self.scratch[off:off + n * esize].view(dtype).view(*shape)
+
+
+def pqe_set_wait_limit(polls: int):
+    """Polls of every bounded device wait before it gives up (0: the default)."""
+    _check("pqe_set_wait_limit", lib().pqe_set_wait_limit(int(polls)))
+
+
+def pqe_test_set_phase2_bias(bias: int):
+    """Test hook: a nonzero bias makes the weight stream's phase-2 waits expire."""
+    _check("pqe_test_set_phase2_bias", lib().pqe_test_set_phase2_bias(int(bias)))
 
 
 def kernel_launches() -> int:

@@ -531,6 +531,8 @@ int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *of
     args.out_perm = static_cast<uint16_t *>(out_perm);
     args.status = status;
     args.done13 = reinterpret_cast<uint32_t *>(wsb + w.done13);
+    args.wait_limit = wait_limit();
+    args.phase2_bias = phase2_bias();
     if (w.tc && expert_fmt) {  // all-FP8 layers (no format tags) need no copies
         args.xp_base = wsb + w.xp;
         args.xp_list = reinterpret_cast<int32_t *>(wsb + w.xp_list);

@@ -30,6 +30,8 @@ struct FfnArgs {
     int32_t *xp_list;            // [max_xp]: page-table entry of the 4-bit page behind copy i
     int32_t *xp_count;           // [1]: copies used
     int max_xp;
+    uint32_t wait_limit;         // polls of a bounded wait before it gives up
+    uint32_t phase2_bias;        // test hook: added to the phase-2 target (0 in normal use)
 };
 
 // address of page-table entry `slot` (valid: 0 <= slot < n_slots + n_wb)

@@ -58,7 +58,6 @@ constexpr int PAIRS = 8;                  // w13 gate/up row pairs per unit (16 
 constexpr int ROWS2 = 64;                 // w2 rows per unit
 constexpr int NT = 8;                     // tokens per mma column group
 constexpr int NCH_MAX = 5;                // 64-column chunks of K a warp holds at most (H <= 2560, I <= 640)
-constexpr uint32_t WAIT_LIMIT = 1u << 22;
 
 // shared-memory pitch of a weight row of `len` bytes: FP8 rows are read as
 // 16-byte pieces (pitch = 64 mod 128), E2M1 rows as 4-byte pieces (pitch = 16
@@ -130,8 +129,8 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i) {
         uint32_t ok;
         asm volatile(
             "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, "
@@ -482,7 +481,7 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
             for (int i = ua; i < ub; ++i, ++it, rp.next(g.stages), fwd ? up.next(per) : up.prev(per)) {
                 const int s = rp.s;
                 int w_ok = 1;
-                if (lane == 0) w_ok = mbar_wait(bar_empty + 8 * s, rp.ph ^ 1u) ? 1 : 0;
+                if (lane == 0) w_ok = mbar_wait(bar_empty + 8 * s, rp.ph ^ 1u, a.wait_limit) ? 1 : 0;
                 if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
                     ok = false;
                     break;
@@ -543,7 +542,7 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
             if (!ok) atomicOr(a.status, PQE_STATUS_TIMEOUT);
             // the copies issued last have landed before the CTA may exit
             for (int j = (it > g.stages ? it - g.stages : 0); j < it; ++j)
-                mbar_wait(bar_full + 8 * (j % g.stages), (uint32_t)(j / g.stages) & 1u);
+                mbar_wait(bar_full + 8 * (j % g.stages), (uint32_t)(j / g.stages) & 1u, a.wait_limit);
         }
         return;  // the producer warps take no part in the consumer barriers
     }
@@ -568,7 +567,7 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
             const int j = up1.rb * PAIRS + gq;
             for (int tg = 0; tg < f.n; tg += NT, ++rc) {
                 const int nt = min(NT, f.n - tg), sl = rc % RSLOTS;
-                if (!timed_out && !mbar_wait(rfull + 8 * sl, (uint32_t)(rc / RSLOTS) & 1u)) timed_out = true;
+                if (!timed_out && !mbar_wait(rfull + 8 * sl, (uint32_t)(rc / RSLOTS) & 1u, a.wait_limit)) timed_out = true;
                 const float4 *rs = red + sl * CONS * 32;
                 float4 v = rs[lane];
 #pragma unroll
@@ -600,7 +599,7 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
             const bool fp8 = f.fmt == PQE_FMT_FP8;
             for (int tg = 0; tg < f.n; tg += NT, ++rc) {
                 const int nt = min(NT, f.n - tg), sl = rc % RSLOTS;
-                if (!timed_out && !mbar_wait(rfull + 8 * sl, (uint32_t)(rc / RSLOTS) & 1u)) timed_out = true;
+                if (!timed_out && !mbar_wait(rfull + 8 * sl, (uint32_t)(rc / RSLOTS) & 1u, a.wait_limit)) timed_out = true;
                 const float4 *rs = red + sl * CONS * 32;
                 float4 v[4];
 #pragma unroll
@@ -651,7 +650,7 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
     };
     auto hand_off = [&](float s_lo, float s_hi, const float (&acc)[4]) {
         const int sl = rc % RSLOTS;
-        if (!timed_out && !mbar_wait(rfree + 8 * sl, ((uint32_t)(rc / RSLOTS) & 1u) ^ 1u)) timed_out = true;
+        if (!timed_out && !mbar_wait(rfree + 8 * sl, ((uint32_t)(rc / RSLOTS) & 1u) ^ 1u, a.wait_limit)) timed_out = true;
         red[(sl * CONS + cw) * 32 + lane] =
             make_float4(acc[0] * i0 * s_lo, acc[1] * i1 * s_lo, acc[2] * i0 * s_hi, acc[3] * i1 * s_hi);
         mbar_arrive(rfull + 8 * sl);
@@ -672,7 +671,7 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
             const int p0 = f.p0, n = f.n;
             const bool fp8 = f.fmt == PQE_FMT_FP8;
             bool valid = f.valid != 0 && !timed_out;
-            if (!timed_out && !mbar_wait(bar_full + 8 * s, rp.ph)) {
+            if (!timed_out && !mbar_wait(bar_full + 8 * s, rp.ph, a.wait_limit)) {
                 valid = false;
                 timed_out = true;
             }
@@ -732,7 +731,7 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
             const int p0 = f.p0, n = f.n;
             const bool fp8 = f.fmt == PQE_FMT_FP8;
             bool valid = f.valid != 0 && !timed_out;
-            if (!timed_out && !mbar_wait(bar_full + 8 * s, rp.ph)) {
+            if (!timed_out && !mbar_wait(bar_full + 8 * s, rp.ph, a.wait_limit)) {
                 valid = false;
                 timed_out = true;
             }
@@ -750,12 +749,12 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
                 if (valid && ready_a != ua) {
                     // h of this expert: all per13 units x token groups combined (other CTAs included)
-                    const uint32_t target = (uint32_t)per13 * (uint32_t)((n + NT - 1) / NT);
+                    const uint32_t target = (uint32_t)per13 * (uint32_t)((n + NT - 1) / NT) + a.phase2_bias;
                     int ok = 1;
                     if (lane == 0 && !timed_out) {
                         uint32_t i = 0;
                         while (ld_acquire(a.done13 + f.e) < target) {
-                            if (++i > WAIT_LIMIT) {
+                            if (++i > a.wait_limit) {
                                 ok = 0;
                                 break;
                             }

@@ -51,7 +51,6 @@ constexpr int EPI_WARPS = 8;  // two per TMEM lane quarter, each taking half the
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
 constexpr uint32_t ACC_COLS = 256;       // one fp32 accumulator of BM x BN
 constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;  // two: the epilogue of item i overlaps the MMAs of item i+1
-constexpr uint32_t WAIT_LIMIT = 1u << 22;
 constexpr int ROW_CTAS = BM / 8;  // row kernels: CTAs of 8 warps per 128-row tile, one row per warp
 // smem: stages | full[S] empty[S] tfull[2] tempty[2] | tmem base | column scales [2][BN] | store buffers
 constexpr int SMEM_BAR_OFF = STAGES * STAGE_BYTES;
@@ -91,9 +90,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// bounded wait; false after WAIT_LIMIT polls
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+// bounded wait; false after `limit` polls
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if (i > 32) __nanosleep(128);
     }
@@ -182,6 +181,7 @@ struct GemmArgs {
     uint16_t *out;           // bf16 h [A, I] or out_perm [A, H]
     uint32_t *hmax;          // [A] (GEMM1)
     int32_t *status;
+    uint32_t wait_limit;     // polls of a bounded wait before it gives up
 };
 
 // address of the page behind a tile's page-table entry (cache, working buffer or FP8 copy)
@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int zc = w.slot - (reg == 0 ? 0 : (reg == 1 ? a.n_slots : a.n_slots + a.n_wb));
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int s = it % STAGES;
-                    if (!mbar_wait(bar_empty + 8 * s, ((uint32_t)(it / STAGES) & 1u) ^ 1u)) {
+                    if (!mbar_wait(bar_empty + 8 * s, ((uint32_t)(it / STAGES) & 1u) ^ 1u, a.wait_limit)) {
                         ok = false;
                         break;
                     }
@@ -360,7 +360,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!ok) atomicOr(a.status, PQE_STATUS_TIMEOUT);
             // drain: the stages issued last have landed before the CTA may exit
             for (int j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-                mbar_wait(bar_full + 8 * (j % STAGES), (uint32_t)(j / STAGES) & 1u);
+                mbar_wait(bar_full + 8 * (j % STAGES), (uint32_t)(j / STAGES) & 1u, a.wait_limit);
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             bool ok = true;
             for (int i = blockIdx.x; i < n_items && ok; i += G, ++local) {
                 const int b = local & 1;
-                if (!mbar_wait(bar_tempty + 8 * b, ((uint32_t)(local >> 1) & 1u) ^ 1u)) {
+                if (!mbar_wait(bar_tempty + 8 * b, ((uint32_t)(local >> 1) & 1u) ^ 1u, a.wait_limit)) {
                     ok = false;
                     break;
                 }
@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const uint32_t d = tmem + (uint32_t)b * ACC_COLS;
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int s = it % STAGES;
-                    if (!mbar_wait(bar_full + 8 * s, (uint32_t)(it / STAGES) & 1u)) {
+                    if (!mbar_wait(bar_full + 8 * s, (uint32_t)(it / STAGES) & 1u, a.wait_limit)) {
                         ok = false;
                         break;
                     }
@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!ok) atomicOr(a.status, PQE_STATUS_TIMEOUT);
             // every issued MMA has finished before TMEM is released
-            if (local > 0) mbar_wait(bar_tfull + 8 * ((local - 1) & 1), (uint32_t)((local - 1) >> 1) & 1u);
+            if (local > 0) mbar_wait(bar_tfull + 8 * ((local - 1) & 1), (uint32_t)((local - 1) >> 1) & 1u, a.wait_limit);
         }
     } else {
         // ---------------- epilogue: TMEM -> registers -> global ----------------
@@ -421,7 +421,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 asm volatile("prefetch.global.L1 [%0];" ::"l"(pf));
             }
             const float rs = valid ? a.row_scale[p] : 0.0f;
-            if (!epi_all(mbar_wait(bar_tfull + 8 * b, (uint32_t)(local >> 1) & 1u))) {
+            if (!epi_all(mbar_wait(bar_tfull + 8 * b, (uint32_t)(local >> 1) & 1u, a.wait_limit))) {
                 ok = false;
                 if (et == 0) atomicOr(a.status, PQE_STATUS_TIMEOUT);
                 break;
@@ -789,6 +789,7 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     g1.out = b.h;
     g1.hmax = b.hmax;
     g1.status = args.status;
+    g1.wait_limit = args.wait_limit;
     if (args.max_xp > 0) {
         // FP8 copies of the 4-bit pages listed by the schedule (count on the device)
         const long rows = (long)args.max_xp * (2 * I + H);

@@ -17,6 +17,7 @@
 #include <vector>
 
 #include "pqe.h"
+#include "pqe_common.cuh"
 
 namespace pqe {
 
@@ -26,6 +27,14 @@ static std::atomic<uint64_t> g_launches{0};
 void set_last_cuda_error(cudaError_t e) { g_last_cuda = e; }
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+// polls of a bounded device wait before it gives up, and the test bias of the
+// weight stream's phase-2 target (both read at each launch)
+static std::atomic<uint32_t> g_wait_limit{DEFAULT_WAIT_LIMIT};
+static std::atomic<uint32_t> g_phase2_bias{0};
+
+uint32_t wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
+uint32_t phase2_bias() { return g_phase2_bias.load(std::memory_order_relaxed); }
 
 }  // namespace pqe
 
@@ -55,6 +64,16 @@ const char *pqe_strerror(int code) {
 }
 
 int pqe_abi_version(void) { return 1; }
+
+int pqe_set_wait_limit(uint32_t polls) {
+    pqe::g_wait_limit.store(polls ? polls : pqe::DEFAULT_WAIT_LIMIT, std::memory_order_relaxed);
+    return PQE_OK;
+}
+
+int pqe_test_set_phase2_bias(uint32_t bias) {
+    pqe::g_phase2_bias.store(bias, std::memory_order_relaxed);
+    return PQE_OK;
+}
 
 int pqe_last_cuda_error(void) { return (int)pqe::g_last_cuda; }
 

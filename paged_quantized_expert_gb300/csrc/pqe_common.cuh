@@ -37,6 +37,13 @@ void count_launch();
 
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Bounded device waits: polls before a wait gives up (pqe_set_wait_limit), and
+// the test bias added to the weight stream's phase-2 target
+// (pqe_test_set_phase2_bias); both are read on the host at each launch.
+constexpr uint32_t DEFAULT_WAIT_LIMIT = 1u << 22;
+uint32_t wait_limit();
+uint32_t phase2_bias();
+
 // The current device and its SM count, cached per device (a process may drive
 // several GPUs; launch attributes such as the dynamic shared-memory opt-in are
 // per device too). PQE_OK, PQE_ERR_CUDA, or PQE_ERR_UNSUPPORTED for a device
