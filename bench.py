@@ -72,9 +72,51 @@ def peaks():
     return 6800.0, "fallback"
 
 
+_FP8_PEAK = {}
+
+
+def measure_fp8_peak(torch, device, n=8192, reps=10):
+    """Dense e4m3 x e4m3 -> bf16 GEMM through cuBLASLt (torch._scaled_mm),
+    n x n x n, burst: the best of `reps` timed calls after warm-up, with fast
+    and with regular accumulation, whichever is faster. Stored for
+    fp8_peak_tflops(); None when the call is unavailable."""
+    try:
+        a = (torch.randn(n, n, device=device) * 0.1).to(torch.float8_e4m3fn)
+        b = (torch.randn(n, n, device=device) * 0.1).to(torch.float8_e4m3fn)
+        one = torch.ones((), dtype=torch.float32, device=device)
+        best = {}
+        for fast in (True, False):
+            def mm():
+                r = torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16,
+                                     use_fast_accum=fast)
+                return r[0] if isinstance(r, tuple) else r
+            for _ in range(3):
+                mm()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(reps):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record()
+                mm()
+                e1.record()
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1))
+            best[fast] = 2.0 * n ** 3 / (min(ts) / 1e3) / 1e12
+        del a, b
+        _FP8_PEAK["tflops"] = max(best.values())
+        _FP8_PEAK["kind"] = (f"measured: cuBLASLt e4m3 GEMM {n}^3 burst via torch._scaled_mm (best of {reps}; "
+                             f"fast accumulation {best[True]:.0f}, regular {best[False]:.0f} TFLOP/s)")
+    except Exception as ex:  # older torch or no FP8 GEMM: the nominal ratio below is used
+        _FP8_PEAK["error"] = f"{type(ex).__name__}: {ex}"[:200]
+    return _FP8_PEAK
+
+
 def fp8_peak_tflops():
-    """Dense FP8 peak: the measured bf16 cuBLAS rate x the nominal FP8/bf16
-    ratio of 2 (4.5 / 2.25 PFLOP/s), as no FP8 rate is measured."""
+    """Dense FP8 peak: measured in this run (measure_fp8_peak), else the
+    measured bf16 cuBLAS rate x the nominal FP8/bf16 ratio of 2."""
+    if "tflops" in _FP8_PEAK:
+        return _FP8_PEAK["tflops"], _FP8_PEAK["kind"]
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
@@ -257,6 +299,13 @@ class GraphRunner:
 
 def run_graph(pqe, torch, device, host, T, L, logits_dev, xs_dev, warmup, K, ws):
     gr = GraphRunner(pqe, torch, device, host, L, T)
+    # each layer's FFN is bracketed by event nodes in its graph: after the timed
+    # loop they hold the FFN time of that layer's last replay
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+    for (a, b), layer in zip(evs, gr.layers):
+        a.record(gr.stream)
+        b.record(gr.stream)  # creates the events; the graphs record them again
+        layer.set_ffn_events(a, b)
     gr.capture(logits_dev[:L], xs_dev[0])
     for i in range(L, L + warmup):
         gr.step(i, logits_dev[i], xs_dev[i % len(xs_dev)])
@@ -276,6 +325,9 @@ def run_graph(pqe, torch, device, host, T, L, logits_dev, xs_dev, warmup, K, ws)
     ms = e0.elapsed_time(e1)
     stats1 = [l.device_stats() for l in gr.layers]
     d = {k: sum(b[k] - a[k] for a, b in zip(stats0, stats1)) for k in stats0[0]}
+    # the FFN of the last replay of each layer: steps L + warmup + K - L .. - 1
+    last = [L + warmup + K - L + j for j in range(L)]
+    d["ffn_ms_last"] = {i: evs[i % L][0].elapsed_time(evs[i % L][1]) for i in last}
     gr.close()
     return ms, d, launches
 
@@ -324,10 +376,15 @@ def run_timed(r: Runner, T, logits_dev, xs_dev, y, warmup, K, ws, want_ffn=True)
     return ms, wall, infos, ffn_ms, launches
 
 
-# ncu (dram__bytes_read.sum + dram__bytes_write.sum) of every kernel of 10 FFN
-# calls at T=64 (schedule, weight stream, the tensor-core chain), divided by the
-# calls' mean routed experts (142.56): 454.17 MB per call
-FFN_DRAM_BYTES_PER_EXPERT_T64 = 454.17e6 / 142.5625
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum, ncu) of every
+# kernel of one FFN call at T=64, divided by that call's algorithmic bytes;
+# None until a capture of the current kernels is taken
+FFN_DRAM_PER_ALGORITHMIC_BYTE_T64 = None
+
+
+def routed_experts(logits: np.ndarray, k: int) -> int:
+    """Distinct experts in a step's top-k (ties to the lower id, as routed)."""
+    return int(np.unique(np.argsort(-logits, axis=1, kind="stable")[:, :k]).size)
 
 
 def ffn_bytes(n_routed, T):
@@ -453,8 +510,8 @@ def run_batched(pqe, torch, device, host, steps, ws):
     peak, kind = fp8_peak_tflops()
     ffn_ms = float(np.mean(ffn))
     tflops = flops / (ffn_ms / 1e3) / 1e12
-    sweep = batch_sweep(pqe, torch, layer, cfg3, x, y, stream, side, peak)
     layer.close()
+    sweep = batch_sweep(pqe, torch, device, host, cfg3, stream, side, peak)
     return {"workload": "module-batched prefill layer (E=256, H=2048, I=512, top-8, T=16384, CACHE_SLOTS=32, "
                         "working buffer)",
             "tokens_per_s": T * steps / (ms / 1e3), "ms_per_step": ms / steps,
@@ -464,19 +521,28 @@ def run_batched(pqe, torch, device, host, steps, ws):
             "batch_size_sweep": sweep}
 
 
-def batch_sweep(pqe, torch, layer, cfg, x, y, stream, side, peak, Ts=(2048, 4096, 8192, 16384), steps=4):
-    """Module-batch sizing: the FFN of the same layer at several accumulated
-    batch sizes T, beside the knee the library's sizer puts on the roofline."""
+def batch_sweep(pqe, torch, device, host, cfg, stream, side, peak, Ts=(2048, 4096, 8192, 16384, 32768, 65536),
+                steps=4):
+    """Module-batch sizing: the FFN of the module-batched layer at accumulated
+    batch sizes T from 2048 to 65536 (one layer sized for the largest; the
+    token rows of a smaller T are the first T of the largest trace), beside
+    the knee the library's sizer puts on the roofline of the measured
+    ceilings."""
     E, H, I, k = cfg.E, cfg.H, cfg.I, cfg.k
     bw = peaks()[0]
-    out = {"T": [], "ffn_ms": [], "ffn_tflops": [], "ffn_frac_of_fp8_peak": [], "ffn_hbm_gbs": []}
+    Tmax = max(Ts)
     nb = pqe.page_bytes(pqe.PQE_FMT_FP8, H, I)
+    layer = pqe.PagedMoELayer(E, H, I, k, cfg.S, E, Tmax, host, [nb] * E, device=device)
+    tr = synth.RoutingTrace(cfg, Tmax)
+    lg_full = [torch.from_numpy(tr.step(s)).to(device) for s in range(2)]
+    x_full = torch.from_numpy(synth.activations(cfg, Tmax, 0).view(np.int16)).to(device)
+    y_full = torch.zeros((Tmax, H), dtype=torch.bfloat16, device=device)
+    out = {"T": [], "ffn_ms": [], "ffn_tflops": [], "ffn_frac_of_fp8_peak": [], "ffn_hbm_gbs": []}
     for T in Ts:
-        tr = synth.RoutingTrace(cfg, T)
-        logits = [torch.from_numpy(tr.step(s)).to(x.device) for s in range(2)]
-        xs = [x[:T]]
-        layer.step(x[:T], y[:T], T, logits=logits[0], stream=stream, side_stream=side)  # warm-up
-        _, ffn, infos = _timed_steps(torch, layer, xs, y[:T], T, logits, steps, stream, side)
+        logits = [l[:T].contiguous() for l in lg_full]
+        xs = [x_full[:T]]
+        layer.step(xs[0], y_full[:T], T, logits=logits[0], stream=stream, side_stream=side)  # warm-up
+        _, ffn, infos = _timed_steps(torch, layer, xs, y_full[:T], T, logits, steps, stream, side)
         f_ms = float(np.mean(ffn))
         routed = float(np.mean([r for r, _, _ in infos]))
         out["T"].append(T)
@@ -485,11 +551,12 @@ def batch_sweep(pqe, torch, layer, cfg, x, y, stream, side, peak, Ts=(2048, 4096
         out["ffn_tflops"].append(tf)
         out["ffn_frac_of_fp8_peak"].append(tf / peak)
         out["ffn_hbm_gbs"].append((routed * nb + T * H * 2 + T * k * H * 2) / (f_ms / 1e3) / 1e9)
+    layer.close()
     best = max(out["ffn_tflops"])
     out["measured_knee_T"] = next(T for T, tf in zip(out["T"], out["ffn_tflops"]) if tf >= 0.9 * best)
     out["model_knee_T"] = pqe.pqe_module_batch_size(E, k, H, I, bw, peak, 64)
     out["note"] = ("measured_knee_T: the smallest swept T within 90% of the best FFN TFLOP/s; model_knee_T: "
-                   "pqe_module_batch_size on the measured HBM and derived FP8 ceilings")
+                   "pqe_module_batch_size on the measured HBM and FP8 ceilings of this run")
     return out
 
 
@@ -680,20 +747,28 @@ def run_ram(pqe, torch, device, host, steps=256, L=4, Ts=(1, 8), ram_slots=(256,
     return out
 
 
-def run_mixed(pqe, torch, device, steps=12):
-    """Mixed per-expert precision layer (E=256, H=2048, I=512, top-8, T=4096):
-    the top 25% of experts by a seeded importance score keep FP8 pages, the
-    rest hold MXFP4 pages; all pages resident (256 slots). Whole steps and the
-    FFN against both HBM (bytes of the routed pages) and the FP8 peak."""
+def run_mixed(pqe, torch, device, steps=256, every=64):
+    """Mixed per-expert precision layer (E=256, H=2048, I=512, top-8, T=4096),
+    as the PagedWeight commentary's bit-width loop runs it: each expert's
+    importance is an EMA of its gate mass (seeded U(0,1) start, alpha 0.9,
+    updated every step from the step's routing); every `every` steps the
+    experts are re-ranked, the top 25% keep FP8 pages and the rest MXFP4
+    pages; an expert whose format changed gets its new host page and its
+    resident copy is dropped, so its next use refills it through the pager
+    (256 slots: after warm-up every other page stays resident). Reports whole
+    steps, the steps that follow a re-rank (they refill the changed pages),
+    the sets that changed, and the FFN against HBM (bytes of the routed pages
+    in their current format) and the FP8 peak."""
     cfg = synth.WORKLOADS["mixed"]
     E, H, I, k, T = cfg.E, cfg.H, cfg.I, cfg.k, cfg.T[0]
     stride = pqe.slot_stride(H, I)
     n8, n4 = pqe.page_bytes(pqe.PQE_FMT_FP8, H, I), pqe.page_bytes(pqe.PQE_FMT_MXFP4, H, I)
-    m = synth.importance_init(cfg)
-    fmt = np.zeros(E, np.uint8)
     n_hi = E // 4
+    m = synth.importance_init(cfg).astype(np.float64)
+    fmt = np.zeros(E, np.uint8)
     pqe.pqe_rank_formats(torch.from_numpy(m), n_hi, torch.from_numpy(fmt))
-    host = torch.zeros((E, stride), dtype=torch.uint8)
+    host8 = torch.zeros((E, stride), dtype=torch.uint8)
+    host4 = torch.zeros((E, -(-n4 // 256) * 256), dtype=torch.uint8)
     page = torch.zeros(stride, dtype=torch.uint8, device=device)
     p4 = torch.zeros(n4, dtype=torch.uint8, device=device)
     nq = 16  # experts whose two pages feed the quality proxy
@@ -702,48 +777,87 @@ def run_mixed(pqe, torch, device, steps=12):
     for e in range(E):
         w13, w2 = synth.expert_weights(cfg, e)
         pqe.pqe_pack_fp8_page(torch.from_numpy(w13).to(device), torch.from_numpy(w2).to(device), H, I, page)
+        pqe.pqe_pack_mxfp4_page(page, H, I, p4)
         if e < nq:
             q8[e].copy_(page)
-            pqe.pqe_pack_mxfp4_page(page, H, I, q4[e])
-        if fmt[e] == 0:
-            host[e].copy_(page)
-        else:
-            pqe.pqe_pack_mxfp4_page(page, H, I, p4)
-            host[e, :n4].copy_(p4)
-    host = host.pin_memory()
-    sizes = [n8 if fmt[e] == 0 else n4 for e in range(E)]
+            q4[e].copy_(p4)
+        host8[e].copy_(page)
+        host4[e, :n4].copy_(p4)
+    host8, host4 = host8.pin_memory(), host4.pin_memory()
+
+    def host_page(e):
+        return (host8[e], n8) if fmt[e] == pqe.PQE_FMT_FP8 else (host4[e], n4)
+
     fmt_dev = torch.from_numpy(fmt.copy()).to(device)
-    layer = pqe.PagedMoELayer(E, H, I, k, E, 0, T, [host[e] for e in range(E)], sizes, expert_fmt=fmt_dev,
-                              device=device)
+    layer = pqe.PagedMoELayer(E, H, I, k, E, 0, T, [host_page(e)[0] for e in range(E)],
+                              [host_page(e)[1] for e in range(E)], expert_fmt=fmt_dev, device=device)
     stream = torch.cuda.current_stream(device)
     side = torch.cuda.Stream(device)
-    tr = synth.RoutingTrace(cfg, T)
-    logits_np = [tr.step(s) for s in range(4)]
-    logits = [torch.from_numpy(l).to(device) for l in logits_np]
+    tr = synth.RoutingTrace(cfg, T, vectorized=True)
+    warm = 3
+    lg_np = [tr.step(s) for s in range(warm + steps)]
+    logits = [torch.from_numpy(l).to(device) for l in lg_np]
     xs = [torch.from_numpy(synth.activations(cfg, T, s).view(np.int16)).to(device) for s in range(2)]
     y = torch.zeros((T, H), dtype=torch.bfloat16, device=device)
-    for i in range(3):  # warm-up: the first step loads every routed page
-        layer.step(xs[i % 2], y, T, logits=logits[i % 4], stream=stream, side_stream=side)
-    ms, ffn, infos = _timed_steps(torch, layer, xs, y, T, logits, steps, stream, side)
+    ids_h = [torch.zeros(T * k, dtype=torch.int32).pin_memory() for _ in range(2)]
+    g_h = [torch.zeros(T * k, dtype=torch.float32).pin_memory() for _ in range(2)]
+    ids_d = layer.device_view("topk_ids", torch.int32, (T * k,))
+    g_d = layer.device_view("topk_w", torch.float32, (T * k,))
+    for i in range(warm):  # warm-up: the first step loads every routed page
+        layer.step(xs[i % 2], y, T, logits=logits[i], stream=stream, side_stream=side)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ffn = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ffn:
+        a.record(stream)
+        b.record(stream)
+    done = torch.cuda.Event()
+    changed, rerank_at, byts, misses = [], [], [], []
+    ev[0].record(stream)
+    for j in range(steps):
+        i = warm + j
+        layer.set_ffn_events(*ffn[j])
+        info = layer.step(xs[i % 2], y, T, logits=logits[i], stream=stream, side_stream=side)
+        misses.append(info.n_miss)
+        ids_h[j % 2].copy_(ids_d, non_blocking=True)
+        g_h[j % 2].copy_(g_d, non_blocking=True)
+        ev[j + 1].record(stream)
+        done.record(stream)
+        done.synchronize()  # the step's routing on the host for the importance update
+        used = np.unique(ids_h[j % 2].numpy())
+        byts.append(sum(n8 if fmt[e] == pqe.PQE_FMT_FP8 else n4 for e in used) + T * H * 2 + T * k * H * 2)
+        before = fmt.copy()
+        if pqe.pqe_importance_step(torch.from_numpy(m), ids_h[j % 2], g_h[j % 2], T, k, E, 0.9, j, every, n_hi,
+                                   torch.from_numpy(fmt)):
+            moved = np.nonzero(before != fmt)[0]
+            for e in moved:  # new page, resident copy dropped: refilled on its next use
+                pg, nb = host_page(int(e))
+                layer.set_host_page(int(e), pg, nb)
+            fmt_dev.copy_(torch.from_numpy(fmt.copy()), non_blocking=False)
+            changed.append(int(len(moved)))
+            rerank_at.append(j)
+    torch.cuda.synchronize()
+    layer.set_ffn_events(None, None)
     layer.close()
-    ffn_ms = float(np.mean(ffn))
-    # routed bytes per step, from the routing of the logits cycled through
-    byts = []
-    for l in logits_np:
-        ids = np.argsort(-l, axis=1, kind="stable")[:, :k]
-        used = np.unique(ids)
-        byts.append(sum(n8 if fmt[e] == 0 else n4 for e in used) + T * H * 2 + T * k * H * 2)
-    bpstep = float(np.mean([byts[i % 4] for i in range(steps)]))
-    gbs = bpstep / (ffn_ms / 1e3) / 1e9
-    tflops = 6.0 * T * k * H * I / (ffn_ms / 1e3) / 1e12
+    step_ms = [ev[j].elapsed_time(ev[j + 1]) for j in range(steps)]
+    ffn_ms = [a.elapsed_time(b) for a, b in ffn]
+    after = [j + 1 for j in rerank_at if j + 1 < steps]
+    gbs = sum(byts) / (sum(ffn_ms) / 1e3) / 1e9
+    tflops = 6.0 * T * k * H * I * steps / (sum(ffn_ms) / 1e3) / 1e12
     pk, kind = fp8_peak_tflops()
     quality = quality_proxy_rate(pqe, torch, device, cfg, q8, q4, m[:nq])
-    return {"workload": "mixed per-expert precision layer (E=256, H=2048, I=512, top-8, T=4096; top 25% by "
-                        "importance FP8, the rest MXFP4; all pages resident)",
-            "n_fp8_experts": int((fmt == 0).sum()), "tokens_per_s": T * steps / (ms / 1e3), "ms_per_step": ms / steps,
-            "steps": steps, "ffn_ms": ffn_ms, "ffn_hbm_gbs": gbs,
-            "ffn_frac_of_measured_hbm": gbs / peaks()[0],
+    return {"workload": "mixed per-expert precision layer (E=256, H=2048, I=512, top-8, T=4096; importance EMA of "
+                        "the gate mass, re-ranked every 64 steps over 256 steps: top 25% FP8 pages, the rest MXFP4)",
+            "steps": steps, "rerank_every": every, "n_fp8_experts": int((fmt == 0).sum()),
+            "tokens_per_s": T * steps / (sum(step_ms) / 1e3), "ms_per_step": float(np.mean(step_ms)),
+            "ms_per_step_after_rerank": [step_ms[j] for j in after],
+            "misses_after_rerank": [misses[j] for j in after],
+            "ms_per_step_other": float(np.mean([t for j, t in enumerate(step_ms) if j not in after])),
+            "reranked_at_step": rerank_at, "fp8_set_changed": changed,
+            "ffn_ms": float(np.mean(ffn_ms)), "ffn_hbm_gbs": gbs, "ffn_frac_of_measured_hbm": gbs / peaks()[0],
             "ffn_tflops": tflops, "ffn_frac_of_fp8_peak": tflops / pk, "fp8_peak_kind": kind,
+            "note": "each step's routing is read back and folded into the importance EMA on the host before the "
+                    "next step is issued",
             "quality_proxy": quality}
 
 
@@ -829,6 +943,8 @@ def main():
     device = torch.device("cuda", local)
     pqe.load()
     T, L, K, W = args.T, args.layers, args.steps, max(3, args.warmup)
+    if args.workload not in ("huff", "ram"):
+        measure_fp8_peak(torch, device)
     if args.workload in ("large", "mixed", "huff"):
         res = {"large": run_large, "mixed": run_mixed, "huff": run_huff}[args.workload](pqe, torch, device)
         if rank == 0:
@@ -858,7 +974,7 @@ def main():
     clk = clocks.stop()
     ms = max_over_ranks(ws, ms, device)
     host_value, host_ms = ws * T * K / (ms / 1e3), ms / K
-    value, pager_used, graph = host_value, "host", None
+    value, pager_used, graph, graph_ffn = host_value, "host", None, {}
     if args.pager != "host":
         r.close()
         clocks_g = Clocks(local)
@@ -873,17 +989,29 @@ def main():
                  "h2d_gb_per_s": gstats["refill_bytes"] / (gms / 1e3) / 1e9, "clocks": clk_g}
         if args.pager == "device" or gval > host_value:
             value, pager_used, ms, launches, clk = gval, "device", gms, glaunch, clk_g
+            graph_ffn = gstats["ffn_ms_last"]
         r = Runner(pqe, torch, device, host, L, max(T, 64))
 
-    # roofline of the FFN call (w13 + SwiGLU, w2; HBM-bound weight stream)
+    # roofline of the FFN call (w13 + SwiGLU, w2; HBM-bound weight stream), from
+    # the run `value` comes from: the host-pager steps (FFN events of every timed
+    # step), or the device-pager graph replays (event nodes of each layer's last
+    # replay, with those steps' routed experts from their logits)
     peak, peak_kind = peaks()
-    byts = [ffn_bytes(n, T) for (n, _, _, _) in infos]
-    ffn_total_ms = sum(ffn_ms)
+    if pager_used == "device":
+        ffn_steps = sorted(graph_ffn)
+        byts = [ffn_bytes(routed_experts(logits_np[i], CFG.k), T) for i in ffn_steps]
+        ffn_list = [graph_ffn[i] for i in ffn_steps]
+        ffn_source = f"device-pager graph replays (last replay of each of the {L} layers)"
+    else:
+        byts = [ffn_bytes(n, T) for (n, _, _, _) in infos]
+        ffn_list = ffn_ms
+        ffn_source = f"host-pager steps ({K} timed steps)"
+    ffn_total_ms = sum(ffn_list)
     achieved = sum(byts) / (ffn_total_ms / 1e3) / 1e9 if ffn_total_ms > 0 else None
-    # DRAM bytes of one FFN call, from an ncu capture of its kernels at T=64
-    # (profiles/launches_decode_T64.md), per routed expert, times this run's experts
-    traffic = (FFN_DRAM_BYTES_PER_EXPERT_T64 * float(np.mean([n for (n, _, _, _) in infos]))
-               if T == 64 else None)
+    # DRAM bytes of one FFN call: the ratio of an ncu capture of its kernels at
+    # T=64 to that call's algorithmic bytes, times this run's algorithmic bytes
+    traffic = (FFN_DRAM_PER_ALGORITHMIC_BYTE_T64 * float(np.mean(byts))
+               if T == 64 and FFN_DRAM_PER_ALGORITHMIC_BYTE_T64 else None)
 
     # e2e: host buffers through pqe_layer_step_host
     x_h = torch.from_numpy(synth.activations(CFG, T, 0).view(np.int16)).pin_memory()
@@ -960,12 +1088,13 @@ def main():
                          "frac": (achieved / peak) if achieved else None, "traffic": traffic,
                          "kernel": "moe_paged_ffn (w13+SwiGLU and w2 weight streams)",
                          "peak_kind": peak_kind,
-                         "ffn_ms_per_step": ffn_total_ms / K,
+                         "ffn_ms_per_step": ffn_total_ms / len(ffn_list), "ffn_timing": ffn_source,
                          "algorithmic_bytes_per_step": float(np.mean(byts))},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * CFG.H * 2 + T * CFG.E * 4,
                     "d2h_bytes_per_step": T * CFG.H * 2},
             "gpu_launches": int(launches),
+            "fp8_peak": dict(_FP8_PEAK),
             "clocks": clk,
             "batched": batched,
             "large": large,

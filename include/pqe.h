@@ -655,7 +655,9 @@ PQE_API int pqe_layer_buffers(pqe_layer *L, pqe_layer_buffers_t *out);
 
 /* Optional CUDA events (timing-enabled, created by the caller) recorded on
  * the compute stream right before and right after the FFN of the next step;
- * NULL, NULL to stop. For measuring the FFN inside whole steps. */
+ * NULL, NULL to stop. For measuring the FFN inside whole steps. A step
+ * captured into a CUDA graph records them as event nodes, so each replay
+ * records them again. */
 PQE_API int pqe_layer_set_ffn_events(pqe_layer *L, void *ev_begin, void *ev_end);
 
 /* The layer's LRU state (see pqe_lru_state). */

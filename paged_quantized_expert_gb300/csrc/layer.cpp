@@ -113,6 +113,18 @@ struct pqe_layer {
 
 namespace {
 
+// Records one of the caller's FFN timing events on s. Inside a stream capture
+// a plain record only orders streams; an external record becomes an event node
+// that each replay of the graph records, so the FFN inside a replayed step can
+// be timed too.
+cudaError_t record_timing(cudaEvent_t ev, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t ce = cudaStreamIsCapturing(s, &cs);
+    if (ce != cudaSuccess) return ce;
+    return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+                                               : cudaEventRecord(ev, s);
+}
+
 // Refills the n pages described by L->fill_* on `side`: one pull+decode pass
 // for compressed pages, one bulk pull for FP8 pages.
 int refill(pqe_layer *L, int n, cudaStream_t side, int32_t *status) {
@@ -339,11 +351,11 @@ int pqe_layer_step(pqe_layer *L, const void *x_dev, const float *w_router_dev, f
         if (rc) return rc;
         rc = slot_fill_device(&L->pool, miss, c.E, L->at<uint64_t>(m.host_pages), pbytes, stream);
         if (rc) return rc;
-        if (L->ev_ffn_begin && (rc = (cudaEventRecord(L->ev_ffn_begin, s) == cudaSuccess ? 0 : PQE_ERR_CUDA))) return rc;
+        if (L->ev_ffn_begin && (rc = (record_timing(L->ev_ffn_begin, s) == cudaSuccess ? 0 : PQE_ERR_CUDA))) return rc;
         rc = moe_paged_ffn(x_dev, perm_src, offsets, page_table, L->expert_fmt, &L->pool, T, c.k, c.E, out_perm,
                            L->at<void>(m.ffn_ws), m.ffn_ws_bytes, status, stream);
         if (rc) return rc;
-        if (L->ev_ffn_end && (rc = (cudaEventRecord(L->ev_ffn_end, s) == cudaSuccess ? 0 : PQE_ERR_CUDA))) return rc;
+        if (L->ev_ffn_end && (rc = (record_timing(L->ev_ffn_end, s) == cudaSuccess ? 0 : PQE_ERR_CUDA))) return rc;
         rc = moe_combine(out_perm, inv, gates, T, c.k, c.H, y_dev, stream);
         if (rc) return rc;
         if (info) *info = local;
@@ -414,14 +426,14 @@ int pqe_layer_step(pqe_layer *L, const void *x_dev, const float *w_router_dev, f
         pqe::set_last_cuda_error(ce);
         return PQE_ERR_CUDA;
     }
-    if (L->ev_ffn_begin && (ce = cudaEventRecord(L->ev_ffn_begin, s)) != cudaSuccess) {
+    if (L->ev_ffn_begin && (ce = record_timing(L->ev_ffn_begin, s)) != cudaSuccess) {
         pqe::set_last_cuda_error(ce);
         return PQE_ERR_CUDA;
     }
     rc = moe_paged_ffn(x_dev, perm_src, offsets, page_table, L->expert_fmt, &L->pool, T, c.k, c.E, out_perm,
                        L->at<void>(m.ffn_ws), m.ffn_ws_bytes, status, stream);
     if (rc) return rc;
-    if (L->ev_ffn_end && (ce = cudaEventRecord(L->ev_ffn_end, s)) != cudaSuccess) {
+    if (L->ev_ffn_end && (ce = record_timing(L->ev_ffn_end, s)) != cudaSuccess) {
         pqe::set_last_cuda_error(ce);
         return PQE_ERR_CUDA;
     }

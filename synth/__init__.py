@@ -153,11 +153,27 @@ class RoutingTrace:
     their k-th and (k+1)-th largest logits, to exercise the lower-id rule.
     """
 
-    def __init__(self, cfg: LayerConfig, T: int, layer: int = 0):
-        self.cfg, self.T, self.layer = cfg, T, layer
+    def __init__(self, cfg: LayerConfig, T: int, layer: int = 0, vectorized: bool = False):
+        """vectorized: draw the fresh sets of a step all at once (Gumbel top-k:
+        the k largest of log p + Gumbel noise, in descending order, which is
+        the same distribution as k sequential draws without replacement);
+        another random stream than the token-by-token draws, for long traces."""
+        self.cfg, self.T, self.layer, self.vectorized = cfg, T, layer, vectorized
         self._perm = _rng(cfg, 0, _TAG_PERM, layer).permutation(cfg.E)
         self._p = _zipf_probs(cfg.E, cfg.zipf_s) if cfg.zipf_s > 0 else np.full(cfg.E, 1.0 / cfg.E)
         self._prev = None
+
+    def _sets_vectorized(self, g: np.random.Generator) -> np.ndarray:
+        cfg, T = self.cfg, self.T
+        fresh = np.ones(T, bool) if self._prev is None else g.random(T) >= cfg.reuse_p
+        sets = np.empty((T, cfg.k), dtype=np.int64) if self._prev is None else self._prev.copy()
+        n = int(fresh.sum())
+        if n:
+            key = np.log(self._p)[None, :] + g.gumbel(size=(n, cfg.E))
+            top = np.argpartition(-key, cfg.k - 1, axis=1)[:, :cfg.k]
+            order = np.argsort(-np.take_along_axis(key, top, axis=1), axis=1, kind="stable")
+            sets[fresh] = self._perm[np.take_along_axis(top, order, axis=1)]
+        return sets
 
     def _fresh(self, g: np.random.Generator) -> np.ndarray:
         ranks = g.choice(self.cfg.E, size=self.cfg.k, replace=False, p=self._p)
@@ -166,12 +182,15 @@ class RoutingTrace:
     def step(self, s: int) -> np.ndarray:
         cfg, T = self.cfg, self.T
         g = _rng(cfg, s, _TAG_TRACE, T + (self.layer << 20))
-        sets = np.empty((T, cfg.k), dtype=np.int64)
-        for t in range(T):
-            if self._prev is not None and g.random() < cfg.reuse_p:
-                sets[t] = self._prev[t]
-            else:
-                sets[t] = self._fresh(g)
+        if self.vectorized:
+            sets = self._sets_vectorized(g)
+        else:
+            sets = np.empty((T, cfg.k), dtype=np.int64)
+            for t in range(T):
+                if self._prev is not None and g.random() < cfg.reuse_p:
+                    sets[t] = self._prev[t]
+                else:
+                    sets[t] = self._fresh(g)
         self._prev = sets
         logits = g.standard_normal((T, cfg.E), dtype=np.float32)
         bump = np.float32(6.0) - np.float32(0.25) * np.arange(cfg.k, dtype=np.float32)
