@@ -21,9 +21,11 @@ namespace pqe {
 // schedule (one CTA of 1024 threads, one thread per expert, ascending id):
 //   sched[0] = count, sched[1 + a] = experts for the CUDA-core path;
 //   tiles[i] = {expert, first batch row, valid rows, page entry} of the
-//   128-row tiles of experts on the tensor-core path, *n_tiles their count.
+//   128-row tiles of experts on the tensor-core path, those of FP8 pages
+//   first, then those of MXFP4 pages; n_tiles = {all, FP8, MXFP4} counts.
 // An expert goes to the tensor cores when tc_min > 0, its batch has at least
-// tc_min rows, its page is FP8 and its page-table entry is inside the pool.
+// tc_min rows, its page is FP8 or MXFP4 and its page-table entry is inside
+// the pool.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int block_excl_scan(int v, int *warp_tot, int &total) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -66,16 +68,11 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(FfnArgs a, int tc_mi
     if (e < a.E && a.done13) a.done13[e] = 0u;
     const bool valid_page = slot >= 0 && slot < a.n_slots + a.n_wb;
     const bool big = n > 0 && tc_min > 0 && n >= tc_min && valid_page;
-    // 4-bit experts with a large batch get an FP8 copy (while copies last) and the tcgen05 path
+    // large batches take the tcgen05 path: FP8 pages on the FP8 GEMM, MXFP4 pages
+    // on the block-scaled GEMM; everything else (and unknown formats) the weight stream
+    const bool tc8 = big && fmt == PQE_FMT_FP8, tc4 = big && fmt == PQE_FMT_MXFP4;
+    const bool gemv = n > 0 && !tc8 && !tc4;
     int total;
-    const bool want_x = big && fmt == PQE_FMT_MXFP4 && a.max_xp > 0;
-    const int xpos = block_excl_scan(want_x ? 1 : 0, warp_tot, total);
-    const bool tcx = want_x && xpos < a.max_xp;
-    if (tcx) a.xp_list[xpos] = slot;
-    if (threadIdx.x == 0 && a.xp_count) *a.xp_count = min(total, a.max_xp);
-    const bool tc = (big && fmt == PQE_FMT_FP8) || tcx;
-    const int tslot = tcx ? a.n_slots + a.n_wb + xpos : slot;
-    const bool gemv = n > 0 && !tc;
     const int gpos = block_excl_scan(gemv ? 1 : 0, warp_tot, total);
     if (gemv) a.sched[1 + gpos] = e;
     if (threadIdx.x == 0) a.sched[0] = total;
@@ -86,18 +83,24 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(FfnArgs a, int tc_mi
     const int wpos = block_excl_scan(gemv ? wgt : 0, warp_tot, wtot);
     if (gemv) a.wpre[gpos] = wpos;
     if (threadIdx.x == 0) a.wpre[total] = wtot;
-    const int nt = tc ? (n + 127) / 128 : 0;
-    const int tpos = block_excl_scan(nt, warp_tot, total);
+    // tiles of 128 batch rows: the FP8 experts' first, then the MXFP4 experts'
+    int total8, total4;
+    const int nt8 = tc8 ? (n + 127) / 128 : 0, nt4 = tc4 ? (n + 127) / 128 : 0;
+    const int tpos8 = block_excl_scan(nt8, warp_tot, total8);
+    const int tpos4 = block_excl_scan(nt4, warp_tot, total4);
+    const int nt = nt8 + nt4, tpos = tc8 ? tpos8 : total8 + tpos4;
     for (int i = 0; i < nt; ++i) {
         int4 t;
         t.x = e;
         t.y = a.offsets[e] + 128 * i;
         t.z = min(128, n - 128 * i);
-        t.w = tslot;
+        t.w = slot;
         reinterpret_cast<int4 *>(tiles)[tpos + i] = t;
     }
     if (threadIdx.x == 0) {
-        *n_tiles = total;
+        n_tiles[0] = total8 + total4;  // all tiles
+        n_tiles[1] = total8;           // FP8 tiles: [0, total8)
+        n_tiles[2] = total4;           // MXFP4 tiles: [total8, total8 + total4)
     }
 }
 
@@ -408,8 +411,8 @@ int launch_ffn_gemv(const FfnArgs &args, int max_active, cudaStream_t s) {
 
 // workspace carve-up shared by the size query and the call
 struct FfnWs {
-    size_t sched, wpre, tiles, n_tiles, done13, h, xq, sx, hbf, hmax, hq, sh, xp_list, xp_count, xp, total;
-    int max_tiles, max_xp;
+    size_t sched, wpre, tiles, n_tiles, done13, h, xq, sx, hbf, hmax, hq, sh, total;
+    int max_tiles;
     bool tc;
 };
 
@@ -427,7 +430,7 @@ static FfnWs ffn_ws_layout(int T, int k, int E, int H, int I) {
     w.sched = take(sizeof(int32_t) * (E + 1));
     w.wpre = take(sizeof(int32_t) * (E + 1));
     w.tiles = take(sizeof(int32_t) * 4 * (size_t)(w.max_tiles ? w.max_tiles : 1));
-    w.n_tiles = take(sizeof(int32_t));
+    w.n_tiles = take(3 * sizeof(int32_t));
     w.done13 = take(sizeof(uint32_t) * E);
     w.h = take(A * I * sizeof(float));
     if (w.tc) {
@@ -437,12 +440,6 @@ static FfnWs ffn_ws_layout(int T, int k, int E, int H, int I) {
         w.hmax = take(A * sizeof(uint32_t));
         w.hq = take(A * I);
         w.sh = take(A * sizeof(float));
-        // FP8 copies for 4-bit experts with >= TC_MIN_ROWS rows: at most one per such expert
-        const size_t cap = A / TC_MIN_ROWS < (size_t)E ? A / TC_MIN_ROWS : (size_t)E;
-        w.max_xp = (int)cap;
-        w.xp_list = take(sizeof(int32_t) * (cap ? cap : 1));
-        w.xp_count = take(sizeof(int32_t));
-        w.xp = take(cap * pqe_slot_stride(H, I));
     }
     w.total = off;
     return w;
@@ -533,12 +530,6 @@ int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *of
     args.done13 = reinterpret_cast<uint32_t *>(wsb + w.done13);
     args.wait_limit = wait_limit();
     args.phase2_bias = phase2_bias();
-    if (w.tc && expert_fmt) {  // all-FP8 layers (no format tags) need no copies
-        args.xp_base = wsb + w.xp;
-        args.xp_list = reinterpret_cast<int32_t *>(wsb + w.xp_list);
-        args.xp_count = reinterpret_cast<int32_t *>(wsb + w.xp_count);
-        args.max_xp = w.max_xp;
-    }
     const long A = (long)T * k;
     const int max_active = (int)(A < E ? A : E);
     cudaStream_t s = as_stream(stream);

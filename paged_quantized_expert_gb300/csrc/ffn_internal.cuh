@@ -23,13 +23,6 @@ struct FfnArgs {
     uint16_t *out_perm;          // bf16 [T*k, H]
     int32_t *status;
     uint32_t *done13;            // [E] stream kernel: phase-1 units x token groups combined per expert (zeroed by the schedule)
-    // 4-bit pages whose batch takes the tcgen05 path are first rewritten as FP8
-    // pages (power-of-two row scales) into copy i of this region; page-table
-    // entries n_slots + n_wb + i in the tile list address copy i
-    uint8_t *xp_base;            // [max_xp] x slot_stride
-    int32_t *xp_list;            // [max_xp]: page-table entry of the 4-bit page behind copy i
-    int32_t *xp_count;           // [1]: copies used
-    int max_xp;
     uint32_t wait_limit;         // polls of a bounded wait before it gives up
     uint32_t phase2_bias;        // test hook: added to the phase-2 target (0 in normal use)
 };
@@ -44,7 +37,7 @@ __device__ __forceinline__ const uint8_t *page_addr(const FfnArgs &a, int slot) 
 struct TcBuffers {
     long A;
     int32_t *tiles;      // [max_tiles][4]: expert, first batch row, valid rows, page-table entry
-    int32_t *n_tiles;    // [1]
+    int32_t *n_tiles;    // [3]: all tiles, FP8 tiles (first in the list), MXFP4 tiles (after them)
     uint8_t *xq;         // E4M3 [A, H] activations in batch order
     float *sx;           // [A] their row scales
     uint16_t *h;         // bf16 [A, I]

@@ -19,6 +19,20 @@
 // Activations are quantised per row to E4M3 (scale amax / 448) by a gather
 // kernel that also lays the rows out in batch order for TMA.
 //
+// MXFP4 pages (E2M1 weights, one E8M0 scale per 32 along a row) are multiplied
+// as they are, by the block-scaled MMA (kind::mxf8f6f4 with .block_scale): E4M3
+// activations x E2M1 weights, each 32-element K block scaled by a 2^e pair
+// read from TMEM. TMA brings the packed E2M1 rows into 8-bit-footprint smem
+// rows (16 values in the low 8 bytes of each 16-byte chunk, the layout the MMA
+// reads), so the smem tiles and descriptors are those of FP8. Per stage, four
+// scale warps (one per TMEM lane quarter) load the 256 weight rows' E8M0 bytes
+// of the stage's four K blocks and write them into a TMEM ring: row n's word at
+// lane 32q + n % 32 of every quarter q, column SFB + n / 32 (each quarter's MMA
+// datapath reads its own lanes); the activations' scales are all 2^0 (their
+// fp32 row scale stays in the epilogue), at lane m, column SFA + m / 32, and the
+// MMA's scale-factor ids pick the K block's byte. The scale columns take the
+// room of the second accumulator, so MXFP4 items run with one.
+//
 // Persistent CTA (one per SM, or per SM of a given share) over (M tile,
 // N tile) work items, 10 warps: warp 0 issues TMA (one thread), warp 1 owns
 // TMEM and issues the MMAs (one thread), warps 2-9 read the accumulator from
@@ -34,6 +48,8 @@
 // drains what it issued (bounded), frees its TMEM and returns.
 #include <cuda.h>
 
+#include <atomic>
+
 #include "ffn_internal.cuh"
 #include "pqe_common.cuh"
 
@@ -48,7 +64,11 @@ constexpr int A_BYTES = BM * BK;
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_WARPS = 8;  // two per TMEM lane quarter, each taking half the columns
-constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int SF_WARPS = 4;   // MXFP4: one scale warp per TMEM lane quarter
+constexpr int SF_WARP0 = 2 + EPI_WARPS;
+__host__ __device__ constexpr int threads_of(bool fp4) { return 64 + 32 * EPI_WARPS + (fp4 ? 32 * SF_WARPS : 0); }
+constexpr uint32_t SFA_COL = 256;  // MXFP4: activation scales (4 columns)
+constexpr uint32_t SFB_COL = 264;  // MXFP4: weight scales, 8 columns per ring stage
 constexpr uint32_t ACC_COLS = 256;       // one fp32 accumulator of BM x BN
 constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;  // two: the epilogue of item i overlaps the MMAs of item i+1
 constexpr int ROW_CTAS = BM / 8;  // row kernels: CTAs of 8 warps per 128-row tile, one row per warp
@@ -65,6 +85,11 @@ constexpr int SMEM_BYTES = SMEM_EPI_OFF + EPI_WARPS * EPI_NBUF * EPI_BUF + 1024;
 // instruction descriptor, kind::f8f6f4: D f32, A/B E4M3, both K-major, N, M
 constexpr uint32_t IDESC = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(BN >> 3) << 17) |
                            ((uint32_t)(BM >> 4) << 24);
+// instruction descriptor, kind::mxf8f6f4 with block scaling: A E4M3, B E2M1,
+// both K-major, E8M0 scales, N, M; the scale-factor ids (bits 4-5 for B, 29-30
+// for A) select the byte of the scale words, i.e. the K block of the stage
+constexpr uint32_t IDESC_MX = (0u << 7) | (5u << 10) | ((uint32_t)(BN >> 3) << 17) | (1u << 23) |
+                              ((uint32_t)(BM >> 4) << 24);
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -135,6 +160,29 @@ __device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t adesc, uint64_
         : "memory");
 }
 
+// block-scaled MMA on scale words in TMEM (sfa, sfb), K block kb of the stage
+__device__ __forceinline__ void umma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t sfa, uint32_t sfb,
+                                        uint32_t kb, uint32_t accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\ttcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, "
+        "%2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(IDESC_MX | (kb << 4) | (kb << 29)), "r"(sfa), "r"(sfb), "r"(accum)
+        : "memory");
+}
+
+// this warp's 32 TMEM lanes, 4 / 8 consecutive 32-bit columns from taddr
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %1, %1, %1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
@@ -166,37 +214,39 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 
 struct GemmArgs {
     const int32_t *tiles;    // [n][4]: expert, first row p0, valid rows, page-table entry
-    const int32_t *n_tiles;  // device count
+    const int32_t *n_tiles;  // device count of this launch's tiles
+    const int32_t *tile_first;  // device index of this launch's first tile (NULL: 0)
     int n_nt;                // N tiles per M tile
     int n_slots;             // entries below this use the cache map,
-    int n_wb;                // then n_wb working-buffer entries, then FP8 copies of 4-bit pages
+    int n_wb;                // then n_wb working-buffer entries
     int K;                   // reduction length in bytes (H for GEMM1, I for GEMM2)
     int I;                   // GEMM1: up rows start at I
     int out_cols;            // row length of the output (I for h, H for out_perm)
     int swiglu;              // 1: GEMM1 epilogue, 0: GEMM2 epilogue
     const float *row_scale;  // sx or sh [A]
-    const uint8_t *pool_base, *wb_base, *xp_base;
+    const uint8_t *pool_base, *wb_base;
     size_t slot_stride;
-    size_t wscale_off;       // byte offset of the weight row scales in a page (s13 or s2)
+    size_t wscale_off;       // FP8: byte offset of the weight row scales in a page (s13 or s2)
+    size_t sf_off;           // MXFP4: byte offset of the E8M0 block scales in a page (x13 or x2)
+    int sf_row_bytes;        // MXFP4: block-scale bytes per weight row (K / 32)
     uint16_t *out;           // bf16 h [A, I] or out_perm [A, H]
     uint32_t *hmax;          // [A] (GEMM1)
     int32_t *status;
     uint32_t wait_limit;     // polls of a bounded wait before it gives up
 };
 
-// address of the page behind a tile's page-table entry (cache, working buffer or FP8 copy)
+// address of the page behind a tile's page-table entry (cache or working buffer)
 __device__ __forceinline__ const uint8_t *tile_page(const GemmArgs &a, int slot) {
     if (slot < a.n_slots) return a.pool_base + (size_t)slot * a.slot_stride;
-    if (slot < a.n_slots + a.n_wb) return a.wb_base + (size_t)(slot - a.n_slots) * a.slot_stride;
-    return a.xp_base + (size_t)(slot - a.n_slots - a.n_wb) * a.slot_stride;
+    return a.wb_base + (size_t)(slot - a.n_slots) * a.slot_stride;
 }
 
 struct Item {
     int p0, nv, slot, nt, r0, r1;
 };
 
-__device__ __forceinline__ Item item_of(const GemmArgs &a, int i) {
-    const int4 t = reinterpret_cast<const int4 *>(a.tiles)[i / a.n_nt];
+__device__ __forceinline__ Item item_of(const GemmArgs &a, int first, int i) {
+    const int4 t = reinterpret_cast<const int4 *>(a.tiles)[first + i / a.n_nt];
     Item it;
     it.p0 = t.y;
     it.nv = t.z;
@@ -288,11 +338,15 @@ __device__ __forceinline__ bool epi_all(bool v) {
 
 // Persistent: CTA b takes work items b, b + G, b + 2G, ... (item = M tile x N
 // tile; neighbouring CTAs share an M tile, so its activations stay in L2).
-__global__ void __launch_bounds__(THREADS, 1)
+// FP4: the weights are MXFP4 pages (block-scaled MMA, scale warps, one accumulator).
+template <bool FP4>
+__global__ void __launch_bounds__(threads_of(FP4), 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB_cache,
-                   const __grid_constant__ CUtensorMap tmB_wb, const __grid_constant__ CUtensorMap tmB_xp,
-                   const __grid_constant__ CUtensorMap tmOut, const GemmArgs a) {
+                   const __grid_constant__ CUtensorMap tmB_wb, const __grid_constant__ CUtensorMap tmOut,
+                   const GemmArgs a) {
     extern __shared__ uint8_t smem_raw[];
+    constexpr int NBUF = FP4 ? 1 : 2;  // accumulators: the second one's columns hold the scales on the FP4 path
+    const int first = a.tile_first ? *a.tile_first : 0;
     const int n_items = *a.n_tiles * a.n_nt;
     if ((int)blockIdx.x >= n_items) return;
     // 1024-byte alignment for the 128-byte swizzle atoms
@@ -309,7 +363,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_full + 8 * s, FP4 ? 1 + SF_WARPS : 1);  // FP4: the TMA bytes and the scale warps
             mbar_init(bar_empty + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -320,7 +374,6 @@ __global__ void __launch_bounds__(THREADS, 1)
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB_cache)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB_wb)) : "memory");
-        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB_xp)) : "memory");
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -339,11 +392,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             int it = 0;
             bool ok = true;
             for (int i = blockIdx.x; i < n_items && ok; i += G) {
-                const Item w = item_of(a, i);
+                const Item w = item_of(a, first, i);
                 // the region the tile's page lies in, and its index there
-                const int reg = w.slot < a.n_slots ? 0 : (w.slot < a.n_slots + a.n_wb ? 1 : 2);
-                const CUtensorMap *tmB = reg == 0 ? &tmB_cache : (reg == 1 ? &tmB_wb : &tmB_xp);
-                const int zc = w.slot - (reg == 0 ? 0 : (reg == 1 ? a.n_slots : a.n_slots + a.n_wb));
+                const bool cache = w.slot < a.n_slots;
+                const CUtensorMap *tmB = cache ? &tmB_cache : &tmB_wb;
+                const int zc = cache ? w.slot : w.slot - a.n_slots;
                 for (int kb = 0; kb < nk; ++kb, ++it) {
                     const int s = it % STAGES;
                     if (!mbar_wait(bar_empty + 8 * s, ((uint32_t)(it / STAGES) & 1u) ^ 1u, a.wait_limit)) {
@@ -351,7 +404,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     const uint32_t sa = sbase + s * STAGE_BYTES, sb = sa + A_BYTES;
-                    mbar_expect_tx(bar_full + 8 * s, STAGE_BYTES);
+                    // packed E2M1 rows count their global bytes (half the smem footprint)
+                    mbar_expect_tx(bar_full + 8 * s, FP4 ? A_BYTES + B_BYTES / 2 : STAGE_BYTES);
                     tma_load_2d(sa, &tmA, kb * BK, w.p0, bar_full + 8 * s);
                     tma_load_3d(sb, tmB, kb * BK, w.r0, zc, bar_full + 8 * s);
                     tma_load_3d(sb + B_BYTES / 2, tmB, kb * BK, w.r1, zc, bar_full + 8 * s);
@@ -368,8 +422,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             int it = 0, local = 0;
             bool ok = true;
             for (int i = blockIdx.x; i < n_items && ok; i += G, ++local) {
-                const int b = local & 1;
-                if (!mbar_wait(bar_tempty + 8 * b, ((uint32_t)(local >> 1) & 1u) ^ 1u, a.wait_limit)) {
+                const int b = local % NBUF;
+                if (!mbar_wait(bar_tempty + 8 * b, ((uint32_t)(local / NBUF) & 1u) ^ 1u, a.wait_limit)) {
                     ok = false;
                     break;
                 }
@@ -383,17 +437,62 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     tc_fence_after();
                     const uint32_t sa = sbase + s * STAGE_BYTES, sb = sa + A_BYTES;
+                    if constexpr (FP4) {
 #pragma unroll
-                    for (int k = 0; k < BK / 32; ++k)
-                        umma_f8(d, sw128_desc(sa + 32 * k), sw128_desc(sb + 32 * k), (kb | k) != 0);
+                        for (int k = 0; k < BK / 32; ++k)
+                            umma_mx(d, sw128_desc(sa + 32 * k), sw128_desc(sb + 32 * k), tmem + SFA_COL,
+                                    tmem + SFB_COL + 8 * s, (uint32_t)k, (kb | k) != 0);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < BK / 32; ++k)
+                            umma_f8(d, sw128_desc(sa + 32 * k), sw128_desc(sb + 32 * k), (kb | k) != 0);
+                    }
                     umma_commit(bar_empty + 8 * s);
                 }
                 umma_commit(bar_tfull + 8 * b);
             }
             if (!ok) atomicOr(a.status, PQE_STATUS_TIMEOUT);
             // every issued MMA has finished before TMEM is released
-            if (local > 0) mbar_wait(bar_tfull + 8 * ((local - 1) & 1), (uint32_t)((local - 1) >> 1) & 1u, a.wait_limit);
+            if (local > 0)
+                mbar_wait(bar_tfull + 8 * ((local - 1) % NBUF), (uint32_t)((local - 1) / NBUF) & 1u, a.wait_limit);
         }
+    } else if (FP4 && warp >= SF_WARP0) {
+        // ---------------- MXFP4 scale warps: E8M0 block scales -> TMEM ----------------
+        const int q = warp & 3;  // the TMEM lane quarter this warp may access
+        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
+        tmem_st4(tq + SFA_COL, 0x7F7F7F7Fu);  // the activations' block scales: 2^0
+        tmem_st_wait();
+        int it = 0;
+        bool ok = true;
+        for (int i = blockIdx.x; i < n_items && ok; i += G) {
+            const Item w = item_of(a, first, i);
+            const uint8_t *xs = tile_page(a, w.slot) + a.sf_off;
+            for (int kb = 0; kb < nk; ++kb, ++it) {
+                const int s = it % STAGES;
+                // the MMAs that read this stage's scale columns before have finished
+                int e_ok = 1;
+                if (lane == 0) e_ok = mbar_wait(bar_empty + 8 * s, ((uint32_t)(it / STAGES) & 1u) ^ 1u, a.wait_limit);
+                if (!__shfl_sync(0xffffffffu, e_ok, 0)) {
+                    ok = false;
+                    break;
+                }
+                // B row n of the tile: weight row r0 + n (n < 128) or r1 + n - 128; its
+                // four scale bytes of this stage's K blocks form one word
+                uint32_t v[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int n = lane + 32 * c;
+                    const int row = n < 128 ? w.r0 + n : w.r1 + n - 128;
+                    v[c] = __ldg(reinterpret_cast<const uint32_t *>(xs + (size_t)row * a.sf_row_bytes) + kb);
+                }
+                tmem_st8(tq + SFB_COL + 8 * s, v);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_plain(bar_full + 8 * s);
+            }
+        }
+        if (!ok && lane == 0) atomicOr(a.status, PQE_STATUS_TIMEOUT);
     } else {
         // ---------------- epilogue: TMEM -> registers -> global ----------------
         const int q = warp & 3;            // TMEM lane quarter this warp may access
@@ -405,23 +504,25 @@ __global__ void __launch_bounds__(THREADS, 1)
         int local = 0;
         bool ok = true;
         for (int i = blockIdx.x; i < n_items && ok; i += G, ++local) {
-            const Item w = item_of(a, i);
-            const int b = local & 1;
+            const Item w = item_of(a, first, i);
+            const int b = local % NBUF;
             const int p = w.p0 + m;
             const bool valid = m < w.nv;
             // the weight-row (output column) scales of this warp's columns: output
             // column c < 128 is weight row r0 + c, c >= 128 row r1 + c - 128. They are
             // read with broadcast vector loads; fetched to L1 before the accumulator
             // wait, like this lane's row scale
+            // MXFP4 pages have no row scales (their block scales are in the MMA): 1
             const float *wsc = reinterpret_cast<const float *>(tile_page(a, w.slot) + a.wscale_off);
             const float *cs_lo = wsc + w.r0, *cs_hi = wsc + w.r1 - 128;
-            if (lane < 4) {
+            const float4 one4 = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+            if (!FP4 && lane < 4) {
                 const float *pf = a.swiglu ? (lane < 2 ? cs_lo + 64 * half + 32 * lane : cs_hi + 128 + 64 * half + 32 * (lane - 2))
                                            : (half ? cs_hi + 128 : cs_lo) + 32 * lane;
                 asm volatile("prefetch.global.L1 [%0];" ::"l"(pf));
             }
             const float rs = valid ? a.row_scale[p] : 0.0f;
-            if (!epi_all(mbar_wait(bar_tfull + 8 * b, (uint32_t)(local >> 1) & 1u, a.wait_limit))) {
+            if (!epi_all(mbar_wait(bar_tfull + 8 * b, (uint32_t)(local / NBUF) & 1u, a.wait_limit))) {
                 ok = false;
                 if (et == 0) atomicOr(a.status, PQE_STATUS_TIMEOUT);
                 break;
@@ -451,7 +552,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     uint32_t packed[16];
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
-                        const float4 sg = __ldg(cg + j4), su = __ldg(cu + j4);
+                        const float4 sg = FP4 ? one4 : __ldg(cg + j4), su = FP4 ? one4 : __ldg(cu + j4);
 #pragma unroll
                         for (int t = 0; t < 2; ++t) {
                             const int j = 4 * j4 + 2 * t;
@@ -485,7 +586,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const float4 *c4 = reinterpret_cast<const float4 *>(csw + c0);
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
-                        const float4 sc = __ldg(c4 + j4);
+                        const float4 sc = FP4 ? one4 : __ldg(c4 + j4);
                         const float2 s01 = mul2(make_float2(sc.x, sc.y), rs2), s23 = mul2(make_float2(sc.z, sc.w), rs2);
                         const int j = 4 * j4;
                         const float2 v01 = mul2(make_float2(__uint_as_float(d[j]), __uint_as_float(d[j + 1])), s01);
@@ -510,7 +611,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 flush_rows32(ebuf, 2, &tmOut, w.nt * 256 + 128 * half + 64, w.p0 + 32 * q,
                              wrow + w.nt * 256 + 128 * half + 64, a.out_cols, nrows, lane);
             }
-            // this accumulator may be overwritten by the MMAs of item i + 2G
+            // this accumulator may be overwritten by the MMAs of item i + NBUF * G
             tc_fence_before();
             mbar_arrive_plain(bar_tempty + 8 * b);
         }
@@ -614,60 +715,6 @@ __global__ void __launch_bounds__(256) tc_hquant_kernel(const uint16_t *__restri
     }
 }
 
-// ---------------------------------------------------------------------------
-// FP8 copy of a 4-bit page for the tcgen05 path. Row r of w13 or w2 holds
-// E2M1 codes m with E8M0 block scales x_b (value m * 2^(x_b - 127)). With
-// x_max the row's largest block exponent, the copy stores
-// E4M3(m * 2^(x_b - x_max + 6)) and the row scale 2^(x_max - 133): E2M1 values
-// carry at most two significant bits, so every element whose block lies
-// within 14 binades of the row's largest is exact; smaller ones round toward
-// E4M3's subnormals (below 2^-15 of the row's largest element). One warp per
-// row; copies i < *xp_count, page-table entry xp_list[i].
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) tc_expand_fp4_kernel(const FfnArgs a) {
-    const int n_xp = *a.xp_count;
-    const int H = a.H, I = a.I, rows = 2 * I + H;
-    const PageLayout L8 = fp8_layout(H, I), L4 = mxfp4_layout(H, I);
-    const int lane = threadIdx.x & 31;
-    const long total = (long)n_xp * rows;
-    for (long wi = (long)blockIdx.x * 8 + (threadIdx.x >> 5); wi < total; wi += (long)gridDim.x * 8) {
-        const int x = (int)(wi / rows), r = (int)(wi % rows);
-        const uint8_t *src = page_addr(a, a.xp_list[x]);
-        uint8_t *dst = a.xp_base + (size_t)x * a.slot_stride;
-        const bool w13 = r < 2 * I;
-        const int rr = w13 ? r : r - 2 * I, K = w13 ? H : I, nb = K / 32;
-        const uint8_t *q = src + (w13 ? L4.w13 : L4.w2) + (size_t)rr * (K / 2);
-        const uint8_t *xs = src + (w13 ? L4.s13 : L4.s2) + (size_t)rr * nb;
-        uint8_t *o = dst + (w13 ? L8.w13 : L8.w2) + (size_t)rr * K;
-        int xm = 0;
-        for (int b = lane; b < nb; b += 32) xm = max(xm, (int)xs[b]);
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) xm = max(xm, __shfl_xor_sync(0xffffffffu, xm, off));
-        for (int b = lane; b < nb; b += 32) {
-            const float f = ldexpf(1.0f, (int)xs[b] - xm + 6);
-            const uint4 v = *reinterpret_cast<const uint4 *>(q + 16 * b);  // 32 codes
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            uint32_t out[8];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                uint16_t c[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float2 e = e2m1x2_to_f32x2((uint8_t)(w[i] >> (8 * j)));
-                    c[j] = f32x2_to_e4m3x2(e.x * f, e.y * f);
-                }
-                out[2 * i] = (uint32_t)c[0] | ((uint32_t)c[1] << 16);
-                out[2 * i + 1] = (uint32_t)c[2] | ((uint32_t)c[3] << 16);
-            }
-            uint4 *o4 = reinterpret_cast<uint4 *>(o + 32 * b);
-            o4[0] = make_uint4(out[0], out[1], out[2], out[3]);
-            o4[1] = make_uint4(out[4], out[5], out[6], out[7]);
-        }
-        if (lane == 0)
-            reinterpret_cast<float *>(dst + (w13 ? L8.s13 : L8.s2))[rr] = ldexpf(1.0f, xm - 133);
-    }
-}
-
 // ---- host: tensor maps -------------------------------------------------------
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -727,6 +774,23 @@ static bool map_3d(CUtensorMap *m, const void *base, uint64_t slots, uint64_t ro
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D [slots, rows, cols] packed E2M1 (cols values, cols / 2 bytes a row) with a
+// slot stride, box [1, 128, 128 values]: each 16 values land in the low half of
+// a 16-byte smem chunk (the 8-bit footprint the block-scaled MMA reads), 128-byte
+// swizzle. Needs cols % 128 == 0, a 32-byte aligned base, strides % 32 == 0.
+static bool map_3d_fp4(CUtensorMap *m, const void *base, uint64_t slots, uint64_t rows, uint64_t cols,
+                       uint64_t slot_stride) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    cuuint64_t dims[3] = {cols, rows, slots};
+    cuuint64_t strides[2] = {cols / 2, slot_stride};
+    cuuint32_t box[3] = {128, 128, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace tc
 
 bool tc_shape_ok(int H, int I) { return H % 256 == 0 && I % 128 == 0 && H >= 256 && I >= 128; }
@@ -735,8 +799,8 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     using namespace tc;
     const int H = args.H, I = args.I;
     const long A = b.A;
-    CUtensorMap mx, mh, m13c, m13w, m13x, m2c, m2w, m2x, mo1, mo2;
-    const PageLayout L = fp8_layout(H, I);
+    CUtensorMap mx, mh, m13c, m13w, m2c, m2w, f13c, f13w, f2c, f2w, mo1, mo2;
+    const PageLayout L = fp8_layout(H, I), L4 = mxfp4_layout(H, I);
     // the working-buffer / cache maps need a non-empty region to encode; an
     // absent region gets a one-slot map over the other base (never selected)
     const uint8_t *cache = args.n_slots ? args.pool_base : args.wb_base;
@@ -747,21 +811,26 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
               map_3d(&m13w, wb + L.w13, nw, 2 * (uint64_t)I, H, args.slot_stride) &&
               map_3d(&m2c, cache + L.w2, ns, (uint64_t)H, I, args.slot_stride) &&
               map_3d(&m2w, wb + L.w2, nw, (uint64_t)H, I, args.slot_stride);
-    // FP8 copies of 4-bit pages (a one-entry map over the cache when there is no such region)
-    const uint8_t *xp = args.max_xp > 0 ? args.xp_base : cache;
-    const uint64_t nx = args.max_xp > 0 ? (uint64_t)args.max_xp : ns;
-    ok = ok && map_3d(&m13x, xp + L.w13, nx, 2 * (uint64_t)I, H, args.slot_stride) &&
-         map_3d(&m2x, xp + L.w2, nx, (uint64_t)H, I, args.slot_stride);
     ok = ok && map_out(&mo1, b.h, (uint64_t)A, (uint64_t)I) && map_out(&mo2, args.out_perm, (uint64_t)A, (uint64_t)H);
+    // MXFP4 pages, when the layer tags formats
+    const bool fp4 = args.expert_fmt != nullptr;
+    if (fp4)
+        ok = ok && map_3d_fp4(&f13c, cache + L4.w13, ns, 2 * (uint64_t)I, H, args.slot_stride) &&
+             map_3d_fp4(&f13w, wb + L4.w13, nw, 2 * (uint64_t)I, H, args.slot_stride) &&
+             map_3d_fp4(&f2c, cache + L4.w2, ns, (uint64_t)H, I, args.slot_stride) &&
+             map_3d_fp4(&f2w, wb + L4.w2, nw, (uint64_t)H, I, args.slot_stride);
     if (!ok) return PQE_ERR_UNSUPPORTED;
     // the shared-memory opt-in is per device
-    static bool attr_set[PQE_MAX_DEVICES] = {};
+    static std::atomic<int> attr_set[PQE_MAX_DEVICES];
     int dev = 0, sms = 0;
     const int di = device_info(dev, sms);
     if (di != PQE_OK) return di;
-    if (!attr_set[dev]) {
-        PQE_CUDA_TRY(cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES));
-        attr_set[dev] = true;
+    if (!attr_set[dev].load(std::memory_order_relaxed)) {
+        PQE_CUDA_TRY(cudaFuncSetAttribute(tc_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          SMEM_BYTES));
+        PQE_CUDA_TRY(cudaFuncSetAttribute(tc_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          SMEM_BYTES));
+        attr_set[dev].store(1, std::memory_order_relaxed);
     }
     // persistent grids: one CTA per SM (or per SM of the share given), at most one per work item
     const int cap = sm_cap > 0 && sm_cap < sms ? sm_cap : sms;
@@ -770,13 +839,14 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     tc_gather_quant_kernel<<<max_tiles * ROW_CTAS, 256, 0, s>>>(args.x, args.perm_src, args.k, H, b.tiles, b.n_tiles, b.xq,
                                                      b.sx, b.hmax);
     PQE_LAUNCH_CHECK();
+    // GEMM1 over the FP8 tiles (the first n_tiles[1]), then the MXFP4 tiles (the next n_tiles[2])
     GemmArgs g1{};
     g1.tiles = b.tiles;
-    g1.n_tiles = b.n_tiles;
+    g1.n_tiles = b.n_tiles + 1;
+    g1.tile_first = nullptr;
     g1.n_nt = I / 128;
     g1.n_slots = args.n_slots;
     g1.n_wb = args.n_wb;
-    g1.xp_base = args.xp_base;
     g1.K = H;
     g1.I = I;
     g1.out_cols = I;
@@ -786,19 +856,21 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     g1.wb_base = args.wb_base;
     g1.slot_stride = args.slot_stride;
     g1.wscale_off = L.s13;
+    g1.sf_off = L4.s13;
+    g1.sf_row_bytes = H / 32;
     g1.out = b.h;
     g1.hmax = b.hmax;
     g1.status = args.status;
     g1.wait_limit = args.wait_limit;
-    if (args.max_xp > 0) {
-        // FP8 copies of the 4-bit pages listed by the schedule (count on the device)
-        const long rows = (long)args.max_xp * (2 * I + H);
-        const long want = (rows + 7) / 8;
-        tc_expand_fp4_kernel<<<(unsigned)(want < 8L * sms ? want : 8L * sms), 256, 0, s>>>(args);
+    tc_gemm_kernel<false><<<grid1, threads_of(false), SMEM_BYTES, s>>>(mx, m13c, m13w, mo1, g1);
+    PQE_LAUNCH_CHECK();
+    GemmArgs g1x = g1;
+    g1x.n_tiles = b.n_tiles + 2;
+    g1x.tile_first = b.n_tiles + 1;
+    if (fp4) {
+        tc_gemm_kernel<true><<<grid1, threads_of(true), SMEM_BYTES, s>>>(mx, f13c, f13w, mo1, g1x);
         PQE_LAUNCH_CHECK();
     }
-    tc_gemm_kernel<<<grid1, THREADS, SMEM_BYTES, s>>>(mx, m13c, m13w, m13x, mo1, g1);
-    PQE_LAUNCH_CHECK();
     tc_hquant_kernel<<<max_tiles * ROW_CTAS, 256, 0, s>>>(b.h, I, b.tiles, b.n_tiles, b.hmax, b.hq, b.sh);
     PQE_LAUNCH_CHECK();
     GemmArgs g2 = g1;
@@ -808,10 +880,19 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     g2.swiglu = 0;
     g2.row_scale = b.sh;
     g2.wscale_off = L.s2;
+    g2.sf_off = L4.s2;
+    g2.sf_row_bytes = I / 32;
     g2.out = args.out_perm;
     g2.hmax = nullptr;
-    tc_gemm_kernel<<<grid2, THREADS, SMEM_BYTES, s>>>(mh, m2c, m2w, m2x, mo2, g2);
+    tc_gemm_kernel<false><<<grid2, threads_of(false), SMEM_BYTES, s>>>(mh, m2c, m2w, mo2, g2);
     PQE_LAUNCH_CHECK();
+    if (fp4) {
+        GemmArgs g2x = g2;
+        g2x.n_tiles = b.n_tiles + 2;
+        g2x.tile_first = b.n_tiles + 1;
+        tc_gemm_kernel<true><<<grid2, threads_of(true), SMEM_BYTES, s>>>(mh, f2c, f2w, mo2, g2x);
+        PQE_LAUNCH_CHECK();
+    }
     return PQE_OK;
 }
 

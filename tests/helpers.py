@@ -19,9 +19,10 @@ TOL_MAX_OVER_L2 = 2e-2
 # smaller; this bound catches a wrong term that the stated bound would let
 # through.
 TOL_L2_GEMV = 5e-3
-# The tensor-core path (per-expert batches of >= TC_MIN_ROWS rows; 4-bit
-# pages are first copied to FP8 exactly) rounds x and h per row to E4M3 (about 2-3% RMS each); its relative L2
-# error per token stays below 0.1, which a dropped expert term (~1/k) breaks.
+# The tensor-core path (per-expert batches of >= TC_MIN_ROWS rows; MXFP4
+# pages multiplied exactly with their block scales) rounds x and h per row to
+# E4M3 (about 2-3% RMS each); its relative L2 error per token stays below 0.1,
+# which a dropped expert term (~1/k) breaks.
 TOL_L2_TC = 0.1
 TC_MIN_ROWS = 9
 
@@ -30,7 +31,7 @@ def l2_bounds(ids: np.ndarray, tokens, E: int, fp4=(), H: int = 0, I: int = 0) -
     """Per checked token: the L2 bound of the path its experts take."""
     counts = np.bincount(ids.reshape(-1), minlength=E)
     tc_shape = (H % 256 == 0 and I % 128 == 0 and H >= 256 and I >= 128) if H else True
-    # FP8 and 4-bit experts alike (4-bit pages are copied to FP8 for that path)
+    # FP8 and 4-bit experts alike (the block-scaled MMA multiplies MXFP4 pages as they are)
     tc_exp = (counts >= TC_MIN_ROWS) & tc_shape & (ids.size >= TC_MIN_ROWS)
     out = np.full(len(tokens), TOL_L2_GEMV)
     for i, t in enumerate(tokens):

@@ -213,7 +213,7 @@ def test_slot_indirection_and_bad_page(cuda_lib, orc):
     assert np.all(op[rows3] == 0) and np.any(op[np.arange(offsets[0], offsets[1])] != 0)
 
 
-# ---- tensor-core path (batches of >= TC_MIN_ROWS rows on FP8 pages) ----------------------
+# ---- tensor-core path (batches of >= TC_MIN_ROWS rows on FP8 or MXFP4 pages) --------------
 # the per-token L2 bound follows the path (helpers.l2_bounds)
 
 
@@ -243,7 +243,7 @@ def test_mixed_paths_one_call(cuda_lib, orc):
     g = np.random.default_rng(5)
     logits = g.standard_normal((T, E)).astype(np.float32)
     logits[:, 0] += 3.0   # expert 0 in almost every token
-    logits[:, 5] += 3.0   # the 4-bit expert too: its page is copied to FP8 for the tensor-core path
+    logits[:, 5] += 3.0   # the 4-bit expert too: its MXFP4 page on the block-scaled tensor-core path
     res = run_layer(pqe, cfg, T, x, logits_np=logits, fmt_dev=pages.fmt_dev, pool=pages.pool)
     ids, gates = orc.topk_gates(logits, k)
     counts = np.bincount(ids.reshape(-1), minlength=E)
@@ -254,9 +254,9 @@ def test_mixed_paths_one_call(cuda_lib, orc):
 
 @pytest.mark.parametrize("H,I", [(512, 256), (2048, 512)])
 def test_tensor_core_path_4bit_pages(cuda_lib, orc, H, I):
-    # most experts hold MXFP4 pages and batches of ~75 rows: each such page is
-    # rewritten as an FP8 page (power-of-two row scales) and multiplied on the
-    # tensor cores; one FP8 expert and one small 4-bit batch ride along
+    # most experts hold MXFP4 pages and batches of ~75 rows: their E2M1 weights
+    # and E8M0 block scales go straight into the block-scaled MMA; one FP8
+    # expert and one small 4-bit batch (weight stream) ride along
     pqe = cuda_lib
     E, k, T = 8, 2, 300
     cfg = synth.small_config(E=E, H=H, I=I, k=k, T=T, cid=96)
@@ -287,10 +287,12 @@ def tile_cover_tokens(orc, ids, E, k, tile=128):
     return np.unique(perm_src[np.array(rows, np.int64)] // k).astype(np.int32)
 
 
-@pytest.mark.parametrize("wl,T", [("batched", 16384), ("large", 4096)])
+@pytest.mark.parametrize("wl,T", [("batched", 16384), ("large", 4096), ("mixed", 4096)])
 def test_full_size_batched(cuda_lib, orc, wl, T):
-    # the full module-batched and large-layer steps; checked: every token whose
-    # row opens or closes a 128-row tile of some expert's batch
+    # the full module-batched, large-layer and mixed-precision steps (mixed: the
+    # 192 experts outside the top quarter by the seeded importance hold MXFP4
+    # pages, multiplied by the block-scaled MMA); checked: every token whose row
+    # opens or closes a 128-row tile of some expert's batch
     pqe = cuda_lib
     cfg = synth.WORKLOADS[wl]
     logits = synth.routing_logits(cfg, T, 0)
@@ -299,7 +301,13 @@ def test_full_size_batched(cuda_lib, orc, wl, T):
     counts = np.bincount(ids.reshape(-1), minlength=cfg.E)
     assert len(tokens) >= int(np.sum(np.ceil(counts / 128.0)))  # at least one token per tile
     needed = set(ids[tokens].reshape(-1).tolist())
-    pages = Pages(pqe, orc, cfg, needed=needed, seed=cfg.cid)
+    fp4 = set()
+    if wl == "mixed":
+        m = synth.importance_init(cfg)
+        order = np.lexsort((np.arange(cfg.E), -m))  # importance descending, ties to the lower id
+        fp4 = set(order[cfg.E // 4:].tolist())
+        assert sum(counts[e] >= helpers.TC_MIN_ROWS for e in fp4) > 100
+    pages = Pages(pqe, orc, cfg, needed=needed, fp4=fp4, seed=cfg.cid)
     x = synth.activations(cfg, T, 0)
     res = run_layer(pqe, cfg, T, x, logits_np=logits, fmt_dev=pages.fmt_dev, pool=pages.pool)
     assert np.array_equal(res["ids"], ids) and res["status"] == 0
