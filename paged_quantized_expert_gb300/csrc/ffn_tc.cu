@@ -637,13 +637,14 @@ __global__ void __launch_bounds__(256) tc_gather_quant_kernel(const uint16_t *__
                                                               const int32_t *__restrict__ n_tiles,
                                                               uint8_t *__restrict__ xq, float *__restrict__ sx,
                                                               uint32_t *__restrict__ hmax) {
-    // CTA b: tile b / 16, rows 8 (b % 16) .. +7 of it, one per warp
-    const int ti = (int)blockIdx.x / ROW_CTAS;
-    if (ti >= *n_tiles) return;
-    const int4 tile = reinterpret_cast<const int4 *>(tiles)[ti];
+    // unit u: tile u / 16, rows 8 (u % 16) .. +7 of it, one per warp; the grid
+    // strides over the units of the tiles the schedule produced
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m = ((int)blockIdx.x % ROW_CTAS) * 8 + warp;
-    if (m < tile.z) {
+    const int units = *n_tiles * ROW_CTAS;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int4 tile = reinterpret_cast<const int4 *>(tiles)[u / ROW_CTAS];
+        const int m = (u % ROW_CTAS) * 8 + warp;
+        if (m >= tile.z) continue;
         const int p = tile.y + m;
         const int t = perm_src[p] / k;
         const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
@@ -686,12 +687,12 @@ __global__ void __launch_bounds__(256) tc_hquant_kernel(const uint16_t *__restri
                                                         const int32_t *__restrict__ n_tiles,
                                                         const uint32_t *__restrict__ hmax, uint8_t *__restrict__ hq,
                                                         float *__restrict__ sh) {
-    const int ti = (int)blockIdx.x / ROW_CTAS;
-    if (ti >= *n_tiles) return;
-    const int4 tile = reinterpret_cast<const int4 *>(tiles)[ti];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m = ((int)blockIdx.x % ROW_CTAS) * 8 + warp;
-    if (m < tile.z) {
+    const int units = *n_tiles * ROW_CTAS;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int4 tile = reinterpret_cast<const int4 *>(tiles)[u / ROW_CTAS];
+        const int m = (u % ROW_CTAS) * 8 + warp;
+        if (m >= tile.z) continue;
         const int p = tile.y + m;
         const float amax = __uint_as_float(hmax[p]);
         const float s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
@@ -836,7 +837,10 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     const int cap = sm_cap > 0 && sm_cap < sms ? sm_cap : sms;
     const int items1 = max_tiles * (I / 128), items2 = max_tiles * (H / 256);
     const int grid1 = items1 < cap ? items1 : cap, grid2 = items2 < cap ? items2 : cap;
-    tc_gather_quant_kernel<<<max_tiles * ROW_CTAS, 256, 0, s>>>(args.x, args.perm_src, args.k, H, b.tiles, b.n_tiles, b.xq,
+    // row kernels: eight CTAs of 256 threads per SM of the share at most (a full
+    // SM), striding over the row units of the tiles the schedule produced
+    const int row_units = max_tiles * ROW_CTAS, grid_rows = row_units < 8 * cap ? row_units : 8 * cap;
+    tc_gather_quant_kernel<<<grid_rows, 256, 0, s>>>(args.x, args.perm_src, args.k, H, b.tiles, b.n_tiles, b.xq,
                                                      b.sx, b.hmax);
     PQE_LAUNCH_CHECK();
     // GEMM1 over the FP8 tiles (the first n_tiles[1]), then the MXFP4 tiles (the next n_tiles[2])
@@ -871,7 +875,7 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
         tc_gemm_kernel<true><<<grid1, threads_of(true), SMEM_BYTES, s>>>(mx, f13c, f13w, mo1, g1x);
         PQE_LAUNCH_CHECK();
     }
-    tc_hquant_kernel<<<max_tiles * ROW_CTAS, 256, 0, s>>>(b.h, I, b.tiles, b.n_tiles, b.hmax, b.hq, b.sh);
+    tc_hquant_kernel<<<grid_rows, 256, 0, s>>>(b.h, I, b.tiles, b.n_tiles, b.hmax, b.hq, b.sh);
     PQE_LAUNCH_CHECK();
     GemmArgs g2 = g1;
     g2.n_nt = H / 256;
