@@ -411,7 +411,7 @@ int launch_ffn_gemv(const FfnArgs &args, int max_active, cudaStream_t s) {
 
 // workspace carve-up shared by the size query and the call
 struct FfnWs {
-    size_t sched, wpre, tiles, n_tiles, done13, h, xq, sx, hbf, hmax, hq, sh, total;
+    size_t sched, wpre, tiles, n_tiles, done13, h, xt, st, xq, sx, hbf, hmax, hq, sh, total;
     int max_tiles;
     bool tc;
 };
@@ -434,6 +434,8 @@ static FfnWs ffn_ws_layout(int T, int k, int E, int H, int I) {
     w.done13 = take(sizeof(uint32_t) * E);
     w.h = take(A * I * sizeof(float));
     if (w.tc) {
+        w.xt = take((size_t)T * H);
+        w.st = take((size_t)T * sizeof(float));
         w.xq = take(A * H);
         w.sx = take(A * sizeof(float));
         w.hbf = take(A * I * sizeof(uint16_t));
@@ -566,6 +568,8 @@ int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *of
     b.A = A;
     b.tiles = tiles;
     b.n_tiles = n_tiles;
+    b.xt = wsb + w.xt;
+    b.st = reinterpret_cast<float *>(wsb + w.st);
     b.xq = wsb + w.xq;
     b.sx = reinterpret_cast<float *>(wsb + w.sx);
     b.h = reinterpret_cast<uint16_t *>(wsb + w.hbf);

@@ -38,7 +38,9 @@ struct TcBuffers {
     long A;
     int32_t *tiles;      // [max_tiles][4]: expert, first batch row, valid rows, page-table entry
     int32_t *n_tiles;    // [3]: all tiles, FP8 tiles (first in the list), MXFP4 tiles (after them)
-    uint8_t *xq;         // E4M3 [A, H] activations in batch order
+    uint8_t *xt;         // E4M3 [T, H] activations per token
+    float *st;           // [T] their row scales
+    uint8_t *xq;         // E4M3 [A, H] the same rows in batch order
     float *sx;           // [A] their row scales
     uint16_t *h;         // bf16 [A, I]
     uint32_t *hmax;      // [A] row amax of h (fp32 bits)

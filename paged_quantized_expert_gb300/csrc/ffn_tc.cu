@@ -16,8 +16,9 @@
 //   hquant hq[p, :] = E4M3(h[p, :] / sh[p]), sh[p] = hmax[p] / 448
 //   GEMM2  D[128 x 256] = hq[p, :] . W2[n..n+255, :]^T
 //          epilogue: out_perm[p, n..] = D * sh[p] * s2[n] -> bf16
-// Activations are quantised per row to E4M3 (scale amax / 448) by a gather
-// kernel that also lays the rows out in batch order for TMA.
+// Activations are quantised once per token to E4M3 (scale amax / 448); a
+// gather kernel then copies the E4M3 rows into batch order for TMA (a byte
+// copy: each token's row is read from L2, not re-quantised per batch row).
 //
 // MXFP4 pages (E2M1 weights, one E8M0 scale per 32 along a row) are multiplied
 // as they are, by the block-scaled MMA (kind::mxf8f6f4 with .block_scale): E4M3
@@ -627,26 +628,13 @@ __global__ void __launch_bounds__(threads_of(FP4), 1)
 }
 
 // ---------------------------------------------------------------------------
-// gather + quantise: row p of the batch <- E4M3(x[perm_src[p] / k] / sx[p]),
-// sx[p] = amax / 448 (1 for a zero row); one warp per row, rows of TC tiles.
-// Also clears hmax for the rows.
+// quantise: xt[t, :] = E4M3(x[t, :] / st[t]), st[t] = amax / 448 (1 for a zero
+// row); one warp per token, 8 tokens per CTA, the grid striding over the tokens.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) tc_gather_quant_kernel(const uint16_t *__restrict__ x,
-                                                              const int32_t *__restrict__ perm_src, int k, int H,
-                                                              const int32_t *__restrict__ tiles,
-                                                              const int32_t *__restrict__ n_tiles,
-                                                              uint8_t *__restrict__ xq, float *__restrict__ sx,
-                                                              uint32_t *__restrict__ hmax) {
-    // unit u: tile u / 16, rows 8 (u % 16) .. +7 of it, one per warp; the grid
-    // strides over the units of the tiles the schedule produced
+__global__ void __launch_bounds__(256) tc_xquant_kernel(const uint16_t *__restrict__ x, int T, int H,
+                                                        uint8_t *__restrict__ xt, float *__restrict__ st) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int units = *n_tiles * ROW_CTAS;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-        const int4 tile = reinterpret_cast<const int4 *>(tiles)[u / ROW_CTAS];
-        const int m = (u % ROW_CTAS) * 8 + warp;
-        if (m >= tile.z) continue;
-        const int p = tile.y + m;
-        const int t = perm_src[p] / k;
+    for (int t = (int)blockIdx.x * 8 + warp; t < T; t += (int)gridDim.x * 8) {
         const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
         float amax = 0.0f;
         for (int c = lane; c < H / 8; c += 32) {
@@ -672,10 +660,37 @@ __global__ void __launch_bounds__(256) tc_gather_quant_kernel(const uint16_t *__
                                                     __uint_as_float(w[2 * i + 1] & 0xffff0000u) * inv);
                 q[i] = (uint32_t)lo | ((uint32_t)hi << 16);
             }
-            reinterpret_cast<uint2 *>(xq + (size_t)p * H)[c] = make_uint2(q[0], q[1]);
+            reinterpret_cast<uint2 *>(xt + (size_t)t * H)[c] = make_uint2(q[0], q[1]);
         }
+        if (lane == 0) st[t] = s;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// gather: row p of the batch <- xt[perm_src[p] / k], sx[p] = st[that token];
+// one warp per row, rows of TC tiles (unit u: tile u / 16, rows 8 (u % 16) ..
+// +7), the grid striding over the units of the scheduled tiles. Also clears
+// hmax for the rows.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) tc_gather_kernel(const uint8_t *__restrict__ xt, const float *__restrict__ st,
+                                                        const int32_t *__restrict__ perm_src, int k, int H,
+                                                        const int32_t *__restrict__ tiles,
+                                                        const int32_t *__restrict__ n_tiles,
+                                                        uint8_t *__restrict__ xq, float *__restrict__ sx,
+                                                        uint32_t *__restrict__ hmax) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int units = *n_tiles * ROW_CTAS;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int4 tile = reinterpret_cast<const int4 *>(tiles)[u / ROW_CTAS];
+        const int m = (u % ROW_CTAS) * 8 + warp;
+        if (m >= tile.z) continue;
+        const int p = tile.y + m;
+        const int t = __ldg(perm_src + p) / k;
+        const uint4 *src = reinterpret_cast<const uint4 *>(xt + (size_t)t * H);
+        uint4 *dst = reinterpret_cast<uint4 *>(xq + (size_t)p * H);
+        for (int c = lane; c < H / 16; c += 32) dst[c] = __ldg(src + c);
         if (lane == 0) {
-            sx[p] = s;
+            sx[p] = __ldg(st + t);
             hmax[p] = 0u;
         }
     }
@@ -840,8 +855,12 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     // row kernels: eight CTAs of 256 threads per SM of the share at most (a full
     // SM), striding over the row units of the tiles the schedule produced
     const int row_units = max_tiles * ROW_CTAS, grid_rows = row_units < 8 * cap ? row_units : 8 * cap;
-    tc_gather_quant_kernel<<<grid_rows, 256, 0, s>>>(args.x, args.perm_src, args.k, H, b.tiles, b.n_tiles, b.xq,
-                                                     b.sx, b.hmax);
+    const long T = A / args.k, tok_ctas = (T + 7) / 8;
+    tc_xquant_kernel<<<(unsigned)(tok_ctas < 8L * cap ? tok_ctas : 8L * cap), 256, 0, s>>>(args.x, (int)T, H, b.xt,
+                                                                                          b.st);
+    PQE_LAUNCH_CHECK();
+    tc_gather_kernel<<<grid_rows, 256, 0, s>>>(b.xt, b.st, args.perm_src, args.k, H, b.tiles, b.n_tiles, b.xq, b.sx,
+                                               b.hmax);
     PQE_LAUNCH_CHECK();
     // GEMM1 over the FP8 tiles (the first n_tiles[1]), then the MXFP4 tiles (the next n_tiles[2])
     GemmArgs g1{};
