@@ -47,6 +47,16 @@
 // written.
 // Every mbarrier wait is bounded: on expiry the CTA sets PQE_STATUS_TIMEOUT,
 // drains what it issued (bounded), frees its TMEM and returns.
+//
+// The kernels after the first of the chain are launched with programmatic
+// dependent launch: a kernel may be set up while its predecessor runs. One
+// that reads its predecessor's output waits for it (griddepcontrol.wait)
+// before its first read; the MXFP4 GEMM of a phase, which needs nothing from
+// the FP8 GEMM before it, starts as that GEMM's CTAs drain and waits for it
+// only before it exits, so that everything after it still sees both done.
+// A kernel lets its successor launch (griddepcontrol.launch_dependents) only
+// after its own wait, so a successor never starts before the data its
+// predecessor read is complete.
 #include <cuda.h>
 
 #include <atomic>
@@ -93,6 +103,17 @@ constexpr uint32_t IDESC_MX = (0u << 7) | (5u << 10) | ((uint32_t)(BN >> 3) << 1
                               ((uint32_t)(BM >> 4) << 24);
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// programmatic dependent launch: PDL_WAIT_START waits for the predecessor grid
+// before the kernel reads anything, PDL_WAIT_END before it exits (a no-op for
+// a kernel launched without the attribute)
+constexpr int PDL_WAIT_START = 1, PDL_WAIT_END = 2;
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_begin(int pdl) {
+    if (pdl & PDL_WAIT_START) pdl_wait();
+    pdl_trigger();
+}
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -234,6 +255,7 @@ struct GemmArgs {
     uint32_t *hmax;          // [A] (GEMM1)
     int32_t *status;
     uint32_t wait_limit;     // polls of a bounded wait before it gives up
+    int pdl;                 // PDL_WAIT_START / PDL_WAIT_END
 };
 
 // address of the page behind a tile's page-table entry (cache or working buffer)
@@ -349,7 +371,10 @@ __global__ void __launch_bounds__(threads_of(FP4), 1)
     constexpr int NBUF = FP4 ? 1 : 2;  // accumulators: the second one's columns hold the scales on the FP4 path
     const int first = a.tile_first ? *a.tile_first : 0;
     const int n_items = *a.n_tiles * a.n_nt;
-    if ((int)blockIdx.x >= n_items) return;
+    if ((int)blockIdx.x >= n_items) {
+        if (a.pdl) pdl_wait();  // an idle CTA still orders the grid's completion after its predecessor
+        return;
+    }
     // 1024-byte alignment for the 128-byte swizzle atoms
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -386,6 +411,7 @@ __global__ void __launch_bounds__(threads_of(FP4), 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_begin(a.pdl);  // the set-up above may overlap the predecessor; the inputs are read below
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
@@ -625,6 +651,7 @@ __global__ void __launch_bounds__(threads_of(FP4), 1)
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
     }
+    if (a.pdl & PDL_WAIT_END) pdl_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -633,6 +660,7 @@ __global__ void __launch_bounds__(threads_of(FP4), 1)
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) tc_xquant_kernel(const uint16_t *__restrict__ x, int T, int H,
                                                         uint8_t *__restrict__ xt, float *__restrict__ st) {
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int t = (int)blockIdx.x * 8 + warp; t < T; t += (int)gridDim.x * 8) {
         const uint4 *xr = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
@@ -678,6 +706,7 @@ __global__ void __launch_bounds__(256) tc_gather_kernel(const uint8_t *__restric
                                                         const int32_t *__restrict__ n_tiles,
                                                         uint8_t *__restrict__ xq, float *__restrict__ sx,
                                                         uint32_t *__restrict__ hmax) {
+    pdl_begin(PDL_WAIT_START);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int units = *n_tiles * ROW_CTAS;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
@@ -702,6 +731,7 @@ __global__ void __launch_bounds__(256) tc_hquant_kernel(const uint16_t *__restri
                                                         const int32_t *__restrict__ n_tiles,
                                                         const uint32_t *__restrict__ hmax, uint8_t *__restrict__ hq,
                                                         float *__restrict__ sh) {
+    pdl_begin(PDL_WAIT_START);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int units = *n_tiles * ROW_CTAS;
     for (int u = blockIdx.x; u < units; u += gridDim.x) {
@@ -809,6 +839,26 @@ static bool map_3d_fp4(CUtensorMap *m, const void *base, uint64_t slots, uint64_
 
 }  // namespace tc
 
+namespace {
+// a kernel of the chain after the first: programmatic stream serialization
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    PQE_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, args...));
+    count_launch();
+    return PQE_OK;
+}
+}  // namespace
+
 bool tc_shape_ok(int H, int I) { return H % 256 == 0 && I % 128 == 0 && H >= 256 && I >= 128; }
 
 int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaStream_t s, int sm_cap) {
@@ -859,9 +909,10 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     tc_xquant_kernel<<<(unsigned)(tok_ctas < 8L * cap ? tok_ctas : 8L * cap), 256, 0, s>>>(args.x, (int)T, H, b.xt,
                                                                                           b.st);
     PQE_LAUNCH_CHECK();
-    tc_gather_kernel<<<grid_rows, 256, 0, s>>>(b.xt, b.st, args.perm_src, args.k, H, b.tiles, b.n_tiles, b.xq, b.sx,
-                                               b.hmax);
-    PQE_LAUNCH_CHECK();
+    int rc = launch_pdl(tc_gather_kernel, grid_rows, 256, 0, s, (const uint8_t *)b.xt, (const float *)b.st,
+                        args.perm_src, args.k, H, (const int32_t *)b.tiles, (const int32_t *)b.n_tiles, b.xq, b.sx,
+                        b.hmax);
+    if (rc != PQE_OK) return rc;
     // GEMM1 over the FP8 tiles (the first n_tiles[1]), then the MXFP4 tiles (the next n_tiles[2])
     GemmArgs g1{};
     g1.tiles = b.tiles;
@@ -885,17 +936,19 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     g1.hmax = b.hmax;
     g1.status = args.status;
     g1.wait_limit = args.wait_limit;
-    tc_gemm_kernel<false><<<grid1, threads_of(false), SMEM_BYTES, s>>>(mx, m13c, m13w, mo1, g1);
-    PQE_LAUNCH_CHECK();
+    g1.pdl = PDL_WAIT_START;
+    if ((rc = launch_pdl(tc_gemm_kernel<false>, grid1, threads_of(false), SMEM_BYTES, s, mx, m13c, m13w, mo1, g1)))
+        return rc;
+    // the MXFP4 tiles need nothing from the FP8 GEMM: they start as its CTAs drain
     GemmArgs g1x = g1;
     g1x.n_tiles = b.n_tiles + 2;
     g1x.tile_first = b.n_tiles + 1;
-    if (fp4) {
-        tc_gemm_kernel<true><<<grid1, threads_of(true), SMEM_BYTES, s>>>(mx, f13c, f13w, mo1, g1x);
-        PQE_LAUNCH_CHECK();
-    }
-    tc_hquant_kernel<<<grid_rows, 256, 0, s>>>(b.h, I, b.tiles, b.n_tiles, b.hmax, b.hq, b.sh);
-    PQE_LAUNCH_CHECK();
+    g1x.pdl = PDL_WAIT_END;
+    if (fp4 && (rc = launch_pdl(tc_gemm_kernel<true>, grid1, threads_of(true), SMEM_BYTES, s, mx, f13c, f13w, mo1, g1x)))
+        return rc;
+    if ((rc = launch_pdl(tc_hquant_kernel, grid_rows, 256, 0, s, (const uint16_t *)b.h, I, (const int32_t *)b.tiles,
+                         (const int32_t *)b.n_tiles, (const uint32_t *)b.hmax, b.hq, b.sh)))
+        return rc;
     GemmArgs g2 = g1;
     g2.n_nt = H / 256;
     g2.K = I;
@@ -907,14 +960,16 @@ int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaSt
     g2.sf_row_bytes = I / 32;
     g2.out = args.out_perm;
     g2.hmax = nullptr;
-    tc_gemm_kernel<false><<<grid2, threads_of(false), SMEM_BYTES, s>>>(mh, m2c, m2w, mo2, g2);
-    PQE_LAUNCH_CHECK();
+    g2.pdl = PDL_WAIT_START;
+    if ((rc = launch_pdl(tc_gemm_kernel<false>, grid2, threads_of(false), SMEM_BYTES, s, mh, m2c, m2w, mo2, g2)))
+        return rc;
     if (fp4) {
         GemmArgs g2x = g2;
         g2x.n_tiles = b.n_tiles + 2;
         g2x.tile_first = b.n_tiles + 1;
-        tc_gemm_kernel<true><<<grid2, threads_of(true), SMEM_BYTES, s>>>(mh, f2c, f2w, mo2, g2x);
-        PQE_LAUNCH_CHECK();
+        g2x.pdl = PDL_WAIT_END;
+        if ((rc = launch_pdl(tc_gemm_kernel<true>, grid2, threads_of(true), SMEM_BYTES, s, mh, f2c, f2w, mo2, g2x)))
+            return rc;
     }
     return PQE_OK;
 }
