@@ -297,15 +297,18 @@ class GraphRunner:
             l.close()
 
 
-def run_graph(pqe, torch, device, host, T, L, logits_dev, xs_dev, warmup, K, ws):
+def run_graph(pqe, torch, device, host, T, L, logits_dev, xs_dev, warmup, K, ws, ffn_events=False):
+    """Device-pager graph replays. With ffn_events each layer's FFN is bracketed
+    by event nodes in its graph (after the timed loop they hold the FFN time of
+    that layer's last replay). The two nodes add ~11 us to a replayed step, so
+    the headline steps are timed without them and the FFN in a second pass."""
     gr = GraphRunner(pqe, torch, device, host, L, T)
-    # each layer's FFN is bracketed by event nodes in its graph: after the timed
-    # loop they hold the FFN time of that layer's last replay
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
-    for (a, b), layer in zip(evs, gr.layers):
-        a.record(gr.stream)
-        b.record(gr.stream)  # creates the events; the graphs record them again
-        layer.set_ffn_events(a, b)
+    if ffn_events:
+        for (a, b), layer in zip(evs, gr.layers):
+            a.record(gr.stream)
+            b.record(gr.stream)  # creates the events; the graphs record them again
+            layer.set_ffn_events(a, b)
     gr.capture(logits_dev[:L], xs_dev[0])
     for i in range(L, L + warmup):
         gr.step(i, logits_dev[i], xs_dev[i % len(xs_dev)])
@@ -327,7 +330,7 @@ def run_graph(pqe, torch, device, host, T, L, logits_dev, xs_dev, warmup, K, ws)
     d = {k: sum(b[k] - a[k] for a, b in zip(stats0, stats1)) for k in stats0[0]}
     # the FFN of the last replay of each layer: steps L + warmup + K - L .. - 1
     last = [L + warmup + K - L + j for j in range(L)]
-    d["ffn_ms_last"] = {i: evs[i % L][0].elapsed_time(evs[i % L][1]) for i in last}
+    d["ffn_ms_last"] = {i: evs[i % L][0].elapsed_time(evs[i % L][1]) for i in last} if ffn_events else {}
     gr.close()
     return ms, d, launches
 
@@ -990,7 +993,9 @@ def main():
                  "h2d_gb_per_s": gstats["refill_bytes"] / (gms / 1e3) / 1e9, "clocks": clk_g}
         if args.pager == "device" or gval > host_value:
             value, pager_used, ms, launches, clk = gval, "device", gms, glaunch, clk_g
-            graph_ffn = gstats["ffn_ms_last"]
+            # the FFN call's time: a second pass of the same replays with its event nodes
+            graph_ffn = run_graph(pqe, torch, device, host, T, L, logits_dev, xs_dev, W, min(K, 128), ws,
+                                  ffn_events=True)[1]["ffn_ms_last"]
         r = Runner(pqe, torch, device, host, L, max(T, 64))
 
     # roofline of the FFN call (w13 + SwiGLU, w2; HBM-bound weight stream), from
@@ -1042,10 +1047,26 @@ def main():
             ys = torch.zeros((Ts, CFG.H), dtype=torch.bfloat16, device=device)
             ms_s, _, inf_s, ffn_s, _ = run_timed(r, Ts, lg_s, xs_s, ys, W, K, ws)
             b_s = [ffn_bytes(n, Ts) for (n, _, _, _) in inf_s]
-            sweep[f"T={Ts}"] = {"tokens_per_s": ws * Ts * K / (max_over_ranks(ws, ms_s, device) / 1e3),
-                                "ms_per_step": ms_s / K,
-                                "ffn_hbm_gbs": sum(b_s) / (sum(ffn_s) / 1e3) / 1e9 if sum(ffn_s) > 0 else None,
-                                "misses_per_step": float(np.mean([m for (_, m, _, _) in inf_s]))}
+            rec = {"tokens_per_s": ws * Ts * K / (max_over_ranks(ws, ms_s, device) / 1e3),
+                   "ms_per_step": ms_s / K, "pager": "host",
+                   "ffn_hbm_gbs": sum(b_s) / (sum(ffn_s) / 1e3) / 1e9 if sum(ffn_s) > 0 else None,
+                   "misses_per_step": float(np.mean([m for (_, m, _, _) in inf_s]))}
+            if pager_used == "device":
+                # the same pager as the headline: graph replays without, then with, the FFN event nodes
+                r.close()
+                lg_g = [torch.from_numpy(l).to(device) for l in make_traces(Ts, L, W + K + L)]
+                gms_s, gst_s, _ = run_graph(pqe, torch, device, host, Ts, L, lg_g, xs_s, W, K, ws)
+                gms_s = max_over_ranks(ws, gms_s, device)
+                f_s = run_graph(pqe, torch, device, host, Ts, L, lg_g, xs_s, W, min(K, 128), ws,
+                                ffn_events=True)[1]["ffn_ms_last"]
+                fb = [ffn_bytes(routed_experts(lg_g[i].cpu().numpy(), CFG.k), Ts) for i in sorted(f_s)]
+                fm = [f_s[i] for i in sorted(f_s)]
+                rec_host = {k: rec[k] for k in ("tokens_per_s", "ms_per_step", "ffn_hbm_gbs")}
+                rec = {"tokens_per_s": ws * Ts * K / (gms_s / 1e3), "ms_per_step": gms_s / K, "pager": "device",
+                       "ffn_ms": float(np.mean(fm)), "ffn_hbm_gbs": sum(fb) / (sum(fm) / 1e3) / 1e9,
+                       "misses_per_step": gst_s["misses"] / K, "host_pager": rec_host}
+                r = Runner(pqe, torch, device, host, L, max(T, 64))
+            sweep[f"T={Ts}"] = rec
 
     batched = None
     if not args.no_batched:
