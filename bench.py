@@ -249,9 +249,13 @@ class Runner:
 
 
 class GraphRunner:
-    """Device-pager layers, each step captured once into a CUDA graph: a timed
-    step is a copy of that step's logits and x into the graph's input buffers
-    (device to device, 64 KB / 256 KB at T=64) plus one graph replay."""
+    """Device-pager layers replayed from CUDA graphs that each hold a run of up
+    to L consecutive steps (one pass over the layers, layer i % L for step i),
+    every step captured reading its own HBM-resident inputs (that step's
+    logits, one of four x). A timed step is then part of one graph replay,
+    route through combine, with no input copies (in a model the layer's inputs
+    are already in place); a graph is launched once, so its first-launch cost
+    is shared by the steps it holds."""
 
     def __init__(self, pqe, torch, device, host, L, T):
         E, H, I, k, S = CFG.E, CFG.H, CFG.I, CFG.k, CFG.S
@@ -261,47 +265,53 @@ class GraphRunner:
         self.layers = [pqe.PagedMoELayer(E, H, I, k, S, E, T, host, nbytes, working_buffer=self.wb, device=device,
                                          device_pager=True) for _ in range(L)]
         self.stream = torch.cuda.Stream(device)
-        self.x = [torch.zeros((T, H), dtype=torch.int16, device=device) for _ in range(L)]
-        self.lg = [torch.zeros((T, E), dtype=torch.float32, device=device) for _ in range(L)]
         self.y = [torch.zeros((T, H), dtype=torch.bfloat16, device=device) for _ in range(L)]
-        self.graphs = []
-        self.nodes = []
+        self.graphs = []  # (first step, steps, graph, kernel nodes)
 
-    def capture(self, logits0, x0):
+    def capture(self, logits_dev, xs_dev, ranges):
+        """Eager steps 0..L-1 (one per layer), then one graph per run of <= L
+        steps inside each [a, b) of `ranges`."""
         torch = self.torch
+        L = len(self.layers)
         with torch.cuda.stream(self.stream):
             for l, layer in enumerate(self.layers):
-                self.x[l].copy_(x0)
-                self.lg[l].copy_(logits0[l])
-                layer.step(self.x[l], self.y[l], self.T, logits=self.lg[l], stream=self.stream)  # eager warm-up
+                layer.step(xs_dev[l % len(xs_dev)], self.y[l], self.T, logits=logits_dev[l], stream=self.stream)
             torch.cuda.synchronize()
-            for l, layer in enumerate(self.layers):
-                g = torch.cuda.CUDAGraph()
-                n0 = self.pqe.kernel_launches()
-                with torch.cuda.graph(g, stream=self.stream):
-                    layer.step(self.x[l], self.y[l], self.T, logits=self.lg[l], stream=self.stream)
-                # launches recorded during the capture = kernel nodes run by each replay
-                self.nodes.append(self.pqe.kernel_launches() - n0)
-                self.graphs.append(g)
+            for a, b in ranges:
+                for c in range(a, b, L):
+                    n = min(L, b - c)
+                    g = torch.cuda.CUDAGraph()
+                    n0 = self.pqe.kernel_launches()
+                    with torch.cuda.graph(g, stream=self.stream):
+                        for i in range(c, c + n):
+                            self.layers[i % L].step(xs_dev[i % len(xs_dev)], self.y[i % L], self.T,
+                                                    logits=logits_dev[i], stream=self.stream)
+                    # launches recorded during the capture = kernel nodes run by each replay
+                    self.graphs.append((c, n, g, self.pqe.kernel_launches() - n0))
         torch.cuda.synchronize()
 
-    def step(self, i, logits_dev, x_dev):
-        l = i % len(self.layers)
+    def replay(self, a, b):
+        """Replays the graphs of steps [a, b) (a capture range); returns their kernel nodes."""
+        nodes = 0
         with self.torch.cuda.stream(self.stream):
-            self.lg[l].copy_(logits_dev, non_blocking=True)
-            self.x[l].copy_(x_dev, non_blocking=True)
-            self.graphs[l].replay()
+            for c, n, g, k in self.graphs:
+                if a <= c < b:
+                    g.replay()
+                    nodes += k
+        return nodes
 
     def close(self):
+        self.graphs.clear()
         for l in self.layers:
             l.close()
 
 
 def run_graph(pqe, torch, device, host, T, L, logits_dev, xs_dev, warmup, K, ws, ffn_events=False):
-    """Device-pager graph replays. With ffn_events each layer's FFN is bracketed
-    by event nodes in its graph (after the timed loop they hold the FFN time of
-    that layer's last replay). The two nodes add ~11 us to a replayed step, so
-    the headline steps are timed without them and the FFN in a second pass."""
+    """Device-pager graph replays of steps L .. L + warmup + K - 1 (layer i % L).
+    With ffn_events each layer's FFN is bracketed by event nodes in its graphs
+    (after the timed loop they hold the FFN time of that layer's last replay).
+    The two nodes add ~11 us to a replayed step, so the headline steps are
+    timed without them and the FFN in a second pass."""
     gr = GraphRunner(pqe, torch, device, host, L, T)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
     if ffn_events:
@@ -309,19 +319,16 @@ def run_graph(pqe, torch, device, host, T, L, logits_dev, xs_dev, warmup, K, ws,
             a.record(gr.stream)
             b.record(gr.stream)  # creates the events; the graphs record them again
             layer.set_ffn_events(a, b)
-    gr.capture(logits_dev[:L], xs_dev[0])
-    for i in range(L, L + warmup):
-        gr.step(i, logits_dev[i], xs_dev[i % len(xs_dev)])
+    t0 = L + warmup
+    gr.capture(logits_dev, xs_dev, [(L, t0), (t0, t0 + K)])
+    gr.replay(L, t0)
     torch.cuda.synchronize()
     barrier(ws)
     stats0 = [l.device_stats() for l in gr.layers]
-    launches = sum(gr.nodes[(L + warmup + j) % L] for j in range(K))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(gr.stream)
-    for j in range(K):
-        i = L + warmup + j
-        gr.step(i, logits_dev[i], xs_dev[i % len(xs_dev)])
+    launches = gr.replay(t0, t0 + K)
     e1.record(gr.stream)
     torch.cuda.synchronize()
     barrier(ws)

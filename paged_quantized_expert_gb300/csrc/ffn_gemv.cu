@@ -57,6 +57,7 @@ __device__ __forceinline__ int block_excl_scan(int v, int *warp_tot, int &total)
 
 __global__ void __launch_bounds__(1024) ffn_schedule_kernel(FfnArgs a, int tc_min, int32_t *__restrict__ tiles,
                                                             int32_t *__restrict__ n_tiles) {
+    pdl_acquire();  // launched after the previous kernel of the step: wait for its output
     __shared__ int warp_tot[33];
     const int e = threadIdx.x;
     int n = 0, slot = -1, fmt = PQE_FMT_FP8;
@@ -537,8 +538,8 @@ int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *of
     cudaStream_t s = as_stream(stream);
     int32_t *tiles = reinterpret_cast<int32_t *>(wsb + w.tiles);
     int32_t *n_tiles = reinterpret_cast<int32_t *>(wsb + w.n_tiles);
-    ffn_schedule_kernel<<<1, 1024, 0, s>>>(args, w.tc ? TC_MIN_ROWS : 0, tiles, n_tiles);
-    PQE_LAUNCH_CHECK();
+    const int sr = launch_pdl(ffn_schedule_kernel, 1, 1024, 0, s, args, w.tc ? TC_MIN_ROWS : 0, tiles, n_tiles);
+    if (sr != PQE_OK) return sr;
     const bool stream_path = stream_shape_ok(pool->H, pool->I);
     int dev = 0, sms = 0;
     const int di = device_info(dev, sms);

@@ -108,8 +108,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)_
 // before the kernel reads anything, PDL_WAIT_END before it exits (a no-op for
 // a kernel launched without the attribute)
 constexpr int PDL_WAIT_START = 1, PDL_WAIT_END = 2;
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_begin(int pdl) {
     if (pdl & PDL_WAIT_START) pdl_wait();
     pdl_trigger();
@@ -838,26 +836,6 @@ static bool map_3d_fp4(CUtensorMap *m, const void *base, uint64_t slots, uint64_
 }
 
 }  // namespace tc
-
-namespace {
-// a kernel of the chain after the first: programmatic stream serialization
-template <typename... KArgs, typename... Args>
-int launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t s, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(block);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    PQE_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, args...));
-    count_launch();
-    return PQE_OK;
-}
-}  // namespace
 
 bool tc_shape_ok(int H, int I) { return H % 256 == 0 && I % 128 == 0 && H >= 256 && I >= 128; }
 

@@ -113,6 +113,7 @@ constexpr uint32_t DF_SEG = 8192;  // bytes a warp of the refill kernel moves pe
 __global__ void __launch_bounds__(1024) lru_step_kernel(void *state, int E, int S, const int32_t *__restrict__ counts,
                                                         const size_t *__restrict__ page_bytes,
                                                         int32_t *__restrict__ page_table, int32_t *__restrict__ miss) {
+    pdl_acquire();  // launched after the previous kernel of the step: wait for its output
     __shared__ int wtot[33];
     __shared__ uint8_t needed[1024];
     __shared__ int cand_of_rank[1024];
@@ -214,6 +215,7 @@ __global__ void __launch_bounds__(DF_THREADS) fill_device_kernel(const int32_t *
                                                                  uint8_t *__restrict__ base,
                                                                  uint8_t *__restrict__ wb_base, int n_slots,
                                                                  size_t slot_stride) {
+    pdl_acquire();  // launched after the previous kernel of the step: wait for its output
     extern __shared__ uint32_t seg0[];  // [n_miss + 1]
     const int n = miss[0];
     const int32_t *mexp = miss + 2, *mdst = miss + 2 + E, *mseg = miss + 2 + 2 * E;
@@ -293,9 +295,8 @@ int pqe_lru_device_state(const void *state, int E, int S, int32_t *slot_expert, 
 int page_table_update_device(void *state, int E, int S, const int32_t *counts, const size_t *page_bytes,
                              int32_t *page_table, int32_t *miss, void *stream) {
     PQE_CHECK_ARG(state && counts && page_bytes && page_table && miss && E >= 1 && E <= 1024 && S >= 0 && S <= 1024);
-    lru_step_kernel<<<1, 1024, 0, as_stream(stream)>>>(state, E, S, counts, page_bytes, page_table, miss);
-    PQE_LAUNCH_CHECK();
-    return PQE_OK;
+    return launch_pdl(lru_step_kernel, 1, 1024, 0, as_stream(stream), state, E, S, counts, page_bytes, page_table,
+                      miss);
 }
 
 int slot_fill_device(const pqe_pool *pool, const int32_t *miss, int E, const uint64_t *host_pages,
@@ -304,11 +305,9 @@ int slot_fill_device(const pqe_pool *pool, const int32_t *miss, int E, const uin
     int dev = 0, sms = 0;
     const int di = device_info(dev, sms);
     if (di != PQE_OK) return di;
-    fill_device_kernel<<<sms, DF_THREADS, sizeof(uint32_t) * (E + 1), as_stream(stream)>>>(
-        miss, E, host_pages, page_bytes, static_cast<uint8_t *>(pool->base), static_cast<uint8_t *>(pool->wb_base),
-        pool->n_slots, pool->slot_stride);
-    PQE_LAUNCH_CHECK();
-    return PQE_OK;
+    return launch_pdl(fill_device_kernel, sms, DF_THREADS, sizeof(uint32_t) * (E + 1), as_stream(stream), miss, E,
+                      host_pages, page_bytes, static_cast<uint8_t *>(pool->base), static_cast<uint8_t *>(pool->wb_base),
+                      pool->n_slots, pool->slot_stride);
 }
 
 }  // extern "C"

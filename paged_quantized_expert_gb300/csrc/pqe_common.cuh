@@ -37,6 +37,45 @@ void count_launch();
 
 inline cudaStream_t as_stream(void *s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// ---- programmatic dependent launch -------------------------------------------
+// The kernels of a layer step are launched with programmatic stream
+// serialization: a kernel may be set up while the one before it on the stream
+// still runs. pdl_wait() returns once the preceding grid has completed and its
+// writes are visible; pdl_trigger() lets the next kernel be set up. Both are
+// no-ops in a kernel launched without the attribute. pdl_acquire() is the
+// usual pair at the top of a kernel, before its first global access.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_acquire() {
+    pdl_wait();
+    pdl_trigger();
+}
+
+template <class T>
+struct ident {
+    using type = T;
+};
+
+// launch with the programmatic-serialization attribute; the arguments convert
+// to the kernel's parameter types
+template <typename... KArgs>
+int launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+               typename ident<KArgs>::type... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    PQE_CUDA_TRY(cudaLaunchKernelEx(&cfg, kern, args...));
+    count_launch();
+    return PQE_OK;
+}
+
 // Bounded device waits: polls before a wait gives up (pqe_set_wait_limit), and
 // the test bias added to the weight stream's phase-2 target
 // (pqe_test_set_phase2_bias); both are read on the host at each launch.

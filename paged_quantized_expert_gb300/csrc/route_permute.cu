@@ -29,6 +29,7 @@ template <int NV>  // logits held per lane: experts e = lane + 32*i, i < NV
 __global__ void __launch_bounds__(256) route_kernel(const uint16_t *__restrict__ x, const float *__restrict__ w_r,
                                                     float *__restrict__ logits, int T, int H, int E, int k,
                                                     int32_t *__restrict__ ids, float *__restrict__ gates) {
+    pdl_acquire();  // launched after the previous kernel of the step: wait for its output
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -111,6 +112,7 @@ constexpr int PERM_WARP_SPAN = PERM_CHUNK / PERM_WARPS;     // 256 consecutive p
 __global__ void __launch_bounds__(PERM_THREADS) perm_count_kernel(const int32_t *__restrict__ ids, int A, int E,
                                                                    int32_t *__restrict__ hist,
                                                                    int32_t *__restrict__ status) {
+    pdl_acquire();  // launched after the previous kernel of the step: wait for its output
     extern __shared__ int32_t sh[];
     for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
     __syncthreads();
@@ -134,6 +136,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t *__restrict__ h
                                                          int32_t *__restrict__ counts,
                                                          int32_t *__restrict__ offsets,
                                                          int32_t *__restrict__ perm_src) {
+    pdl_acquire();  // launched after the previous kernel of the step: wait for its output
     __shared__ int32_t tot[1024];
     __shared__ int32_t warp_sums[32];
     int e = threadIdx.x;
@@ -188,6 +191,7 @@ __global__ void __launch_bounds__(PERM_THREADS) perm_scatter_kernel(const int32_
                                                                      const int32_t *__restrict__ chunk_base,
                                                                      int32_t *__restrict__ perm_src,
                                                                      int32_t *__restrict__ inv) {
+    pdl_acquire();  // launched after the previous kernel of the step: wait for its output
     extern __shared__ int32_t sh[];  // [PERM_WARPS][E] counts, then bases
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     int32_t *wc = sh + (size_t)w * E;
@@ -244,6 +248,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t *__restrict
                                                       const int32_t *__restrict__ inv,
                                                       const float *__restrict__ gates, int T, int k, int H,
                                                       uint16_t *__restrict__ y) {
+    pdl_acquire();  // launched after the previous kernel of the step: wait for its output
     const int t = blockIdx.x;
     for (int c8 = threadIdx.x; c8 < H / 8; c8 += blockDim.x) {
         float acc[8];
@@ -373,14 +378,9 @@ int moe_route(const void *x_bf16, const float *w_router, float *logits, int T, i
     auto s = as_stream(stream);
     const uint16_t *x = static_cast<const uint16_t *>(x_bf16);
     int nv = (E + 31) / 32;
-    if (nv <= 1) route_kernel<1><<<grid, block, 0, s>>>(x, w_router, logits, T, H, E, k, topk_ids, topk_w);
-    else if (nv <= 2) route_kernel<2><<<grid, block, 0, s>>>(x, w_router, logits, T, H, E, k, topk_ids, topk_w);
-    else if (nv <= 4) route_kernel<4><<<grid, block, 0, s>>>(x, w_router, logits, T, H, E, k, topk_ids, topk_w);
-    else if (nv <= 8) route_kernel<8><<<grid, block, 0, s>>>(x, w_router, logits, T, H, E, k, topk_ids, topk_w);
-    else if (nv <= 16) route_kernel<16><<<grid, block, 0, s>>>(x, w_router, logits, T, H, E, k, topk_ids, topk_w);
-    else route_kernel<32><<<grid, block, 0, s>>>(x, w_router, logits, T, H, E, k, topk_ids, topk_w);
-    PQE_LAUNCH_CHECK();
-    return PQE_OK;
+    auto kern = nv <= 1 ? route_kernel<1> : nv <= 2 ? route_kernel<2> : nv <= 4 ? route_kernel<4>
+              : nv <= 8 ? route_kernel<8> : nv <= 16 ? route_kernel<16> : route_kernel<32>;
+    return launch_pdl(kern, grid, block, 0, s, x, w_router, logits, T, H, E, k, topk_ids, topk_w);
 }
 
 size_t moe_permute_workspace_size(int T, int k, int E) {
@@ -407,16 +407,15 @@ int moe_permute(const int32_t *topk_ids, int T, int k, int E, int32_t *counts, i
     PQE_CHECK_ARG(ws_bytes >= moe_permute_workspace_size(T, k, E) && aligned(ws, 256));
     const int nchunk = (int)((A + PERM_CHUNK - 1) / PERM_CHUNK);
     int32_t *hist = static_cast<int32_t *>(ws);
-    perm_count_kernel<<<nchunk, PERM_THREADS, sizeof(int32_t) * E, s>>>(topk_ids, (int)A, E, hist, status);
-    PQE_LAUNCH_CHECK();
-    perm_scan_kernel<<<1, 1024, 0, s>>>(hist, nchunk, E, (int)A, counts, offsets, perm_src);
-    PQE_LAUNCH_CHECK();
+    int rc = launch_pdl(perm_count_kernel, nchunk, PERM_THREADS, sizeof(int32_t) * E, s, topk_ids, (int)A, E, hist,
+                        status);
+    if (rc != PQE_OK) return rc;
+    if ((rc = launch_pdl(perm_scan_kernel, 1, 1024, 0, s, hist, nchunk, E, (int)A, counts, offsets, perm_src)))
+        return rc;
     size_t smem = sizeof(int32_t) * PERM_WARPS * E;
     if (smem > 48 * 1024) PQE_CUDA_TRY(cudaFuncSetAttribute(perm_scatter_kernel,
                                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    perm_scatter_kernel<<<nchunk, PERM_THREADS, smem, s>>>(topk_ids, (int)A, E, hist, perm_src, inv);
-    PQE_LAUNCH_CHECK();
-    return PQE_OK;
+    return launch_pdl(perm_scatter_kernel, nchunk, PERM_THREADS, smem, s, topk_ids, (int)A, E, hist, perm_src, inv);
 }
 
 size_t moe_permute_static_max_words(void) { return PERM_STATIC_WORDS; }
@@ -442,10 +441,8 @@ int moe_combine(const void *out_perm, const int32_t *inv, const float *topk_w, i
     PQE_CHECK_ARG(out_perm && inv && topk_w && y_bf16);
     PQE_CHECK_ARG(aligned(out_perm, 16) && aligned(y_bf16, 16));
     int threads = H / 8 < 256 ? ((H / 8 + 31) / 32) * 32 : 256;
-    combine_kernel<<<T, threads, 0, as_stream(stream)>>>(static_cast<const uint16_t *>(out_perm), inv, topk_w, T, k,
-                                                         H, static_cast<uint16_t *>(y_bf16));
-    PQE_LAUNCH_CHECK();
-    return PQE_OK;
+    return launch_pdl(combine_kernel, T, threads, 0, as_stream(stream), static_cast<const uint16_t *>(out_perm), inv,
+                      topk_w, T, k, H, static_cast<uint16_t *>(y_bf16));
 }
 
 int pqe_quantize_fp8_rows(const float *w, int rows, int cols, uint8_t *q, float *scale, void *stream) {
