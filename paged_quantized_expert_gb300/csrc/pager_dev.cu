@@ -76,61 +76,74 @@ __global__ void lru_invalidate_kernel(void *state, int E, int S, int e) {
     }
 }
 
-// block-wide exclusive scan of one int per thread (1024 threads)
-__device__ __forceinline__ int scan1024(int x, int *wtot, int &total) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    int incl = x;
+// block-wide exclusive scans of three ints per thread at once (any multiple of
+// 32 threads up to 1024): one pair of barriers for all three
+__device__ __forceinline__ int3 scan3(int3 x, int (*wtot)[33], int3 &total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int3 incl = x;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
+        const int a = __shfl_up_sync(0xffffffffu, incl.x, o), b = __shfl_up_sync(0xffffffffu, incl.y, o),
+                  c = __shfl_up_sync(0xffffffffu, incl.z, o);
+        if (lane >= o) incl = make_int3(incl.x + a, incl.y + b, incl.z + c);
     }
-    if (lane == 31) wtot[w] = incl;
+    if (lane == 31) {
+        wtot[0][w] = incl.x;
+        wtot[1][w] = incl.y;
+        wtot[2][w] = incl.z;
+    }
     __syncthreads();
-    if (w == 0) {
-        const int c = wtot[lane];
+    for (int q = w; q < 3; q += nw) {  // the warp totals of component q, scanned by warp q mod nw
+        const int c = lane < nw ? wtot[q][lane] : 0;
         int ci = c;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int n = __shfl_up_sync(0xffffffffu, ci, o);
             if (lane >= o) ci += n;
         }
-        wtot[lane] = ci - c;
-        if (lane == 31) wtot[32] = ci;
+        wtot[q][lane] = ci - c;
+        if (lane == 31) wtot[q][32] = ci;
     }
     __syncthreads();
-    const int r = wtot[w] + incl - x;
-    total = wtot[32];
-    __syncthreads();
-    return r;
+    total = make_int3(wtot[0][32], wtot[1][32], wtot[2][32]);
+    return make_int3(wtot[0][w] + incl.x - x.x, wtot[1][w] + incl.y - x.y, wtot[2][w] + incl.z - x.z);
 }
 
 constexpr uint32_t DF_SEG = 8192;  // bytes a warp of the refill kernel moves per segment
 
 // miss list layout: [0] n_miss, [1] working-buffer flag, [2 .. 2+E) expert,
 // [2+E .. 2+2E) destination, [2+2E .. 2+3E+1) first refill segment of each miss
-// (prefix over the misses, n_miss + 1 entries)
+// (prefix over the misses, n_miss + 1 entries). One CTA of max(E, S) threads
+// rounded up to a warp: thread t is expert t and slot t.
 __global__ void __launch_bounds__(1024) lru_step_kernel(void *state, int E, int S, const int32_t *__restrict__ counts,
                                                         const size_t *__restrict__ page_bytes,
                                                         int32_t *__restrict__ page_table, int32_t *__restrict__ miss) {
     pdl_acquire();  // launched after the previous kernel of the step: wait for its output
-    __shared__ int wtot[33];
+    __shared__ int wtot[3][33];
     __shared__ uint8_t needed[1024];
     __shared__ int cand_of_rank[1024];
+    __shared__ int s_expert[1024];     // slot -> expert at the start of the step
+    __shared__ int64_t s_last[1024];   // slot -> last use at the start of the step
     LruView v = lru_view(state, E, S);
     const int t = threadIdx.x;
     const int64_t now = v.hdr->step;
     const bool need = t < E && counts[t] > 0;
-    if (t < E) needed[t] = need ? 1 : 0;
-    int nu;
-    scan1024(need ? 1 : 0, wtot, nu);  // (syncs: needed[] visible afterwards)
     const int my_slot = t < E ? v.expert_slot[t] : -1;
     const bool miss_e = need && my_slot < 0;
-    int n_miss;
-    const int mrank = scan1024(miss_e ? 1 : 0, wtot, n_miss);
+    if (t < E) needed[t] = need ? 1 : 0;
+    if (t < S) {
+        s_expert[t] = v.slot_expert[t];
+        s_last[t] = v.last_use[t];
+    }
+    // needed experts, misses, and the misses' refill segments, scanned together
+    // (the barriers inside also make needed[] and the slot copies visible)
+    int3 tot;
+    const int3 pre = scan3(make_int3(need ? 1 : 0, miss_e ? 1 : 0,
+                                     miss_e ? (int)((page_bytes[t] + DF_SEG - 1) / DF_SEG) : 0),
+                           wtot, tot);
+    const int nu = tot.x, n_miss = tot.y, n_seg = tot.z;
+    const int mrank = pre.y, spos = pre.z;
     int32_t *miss_exp = miss + 2, *miss_dst = miss + 2 + E, *miss_seg = miss + 2 + 2 * E;
-    int n_seg;
-    const int spos = scan1024(miss_e ? (int)((page_bytes[t] + DF_SEG - 1) / DF_SEG) : 0, wtot, n_seg);
     if (miss_e) miss_seg[mrank] = spos;
     if (t == 0) miss_seg[n_miss] = n_seg;
     if (nu > S) {
@@ -145,18 +158,17 @@ __global__ void __launch_bounds__(1024) lru_step_kernel(void *state, int E, int 
         int key_class = 2;  // 0 empty, 1 candidate, 2 not a candidate
         int64_t lu = 0;
         if (t < S) {
-            const int held = v.slot_expert[t];
-            lu = v.last_use[t];
+            const int held = s_expert[t];
+            lu = s_last[t];
             key_class = held < 0 ? 0 : (needed[held] ? 2 : 1);
         }
-        __syncthreads();
         int rank = 0;
         if (key_class < 2) {
             for (int s2 = 0; s2 < S; ++s2) {
-                const int held = v.slot_expert[s2];
+                const int held = s_expert[s2];
                 const int c2 = held < 0 ? 0 : (needed[held] ? 2 : 1);
                 if (c2 == 2) continue;
-                const int64_t l2 = v.last_use[s2];
+                const int64_t l2 = s_last[s2];
                 const bool before = c2 < key_class || (c2 == key_class && (c2 == 0 ? s2 < t : (l2 < lu || (l2 == lu && s2 < t))));
                 rank += before ? 1 : 0;
             }
@@ -170,13 +182,9 @@ __global__ void __launch_bounds__(1024) lru_step_kernel(void *state, int E, int 
         } else if (t < E) {
             page_table[t] = -1;
         }
-        int victim = -1, old = -1;
         if (miss_e) {
-            victim = cand_of_rank[mrank];
-            old = v.slot_expert[victim];
-        }
-        __syncthreads();  // every victim's old expert read before any slot is rewritten
-        if (miss_e) {
+            const int victim = cand_of_rank[mrank];
+            const int old = s_expert[victim];
             if (old >= 0) v.expert_slot[old] = -1;
             v.slot_expert[victim] = t;
             v.last_use[victim] = now;
@@ -185,7 +193,7 @@ __global__ void __launch_bounds__(1024) lru_step_kernel(void *state, int E, int 
             miss_dst[mrank] = victim;
         }
         __syncthreads();
-        if (miss_e) v.expert_slot[t] = victim;
+        if (miss_e) v.expert_slot[t] = cand_of_rank[mrank];
     }
     // refill bytes of this step
     long long bytes = miss_e ? (long long)page_bytes[t] : 0;
@@ -295,8 +303,9 @@ int pqe_lru_device_state(const void *state, int E, int S, int32_t *slot_expert, 
 int page_table_update_device(void *state, int E, int S, const int32_t *counts, const size_t *page_bytes,
                              int32_t *page_table, int32_t *miss, void *stream) {
     PQE_CHECK_ARG(state && counts && page_bytes && page_table && miss && E >= 1 && E <= 1024 && S >= 0 && S <= 1024);
-    return launch_pdl(lru_step_kernel, 1, 1024, 0, as_stream(stream), state, E, S, counts, page_bytes, page_table,
-                      miss);
+    const int threads = ((E > S ? E : S) + 31) / 32 * 32;
+    return launch_pdl(lru_step_kernel, 1, threads > 0 ? threads : 32, 0, as_stream(stream), state, E, S, counts,
+                      page_bytes, page_table, miss);
 }
 
 int slot_fill_device(const pqe_pool *pool, const int32_t *miss, int E, const uint64_t *host_pages,

@@ -59,31 +59,52 @@ __global__ void __launch_bounds__(256) route_kernel(const uint16_t *__restrict__
         }
     }
 
-    uint32_t taken = 0;  // bit i: expert lane + 32*i already picked
+    // top-k under `better` (larger value, then lower id): every lane sorts its
+    // NV candidates once (bitonic network in registers, best first), then each
+    // round the best of the 32 lane heads is the next pick and its lane drops
+    // that head. A lane's remaining list is exactly its candidates not yet
+    // picked, so round j picks the best candidate left: the same picks, in the
+    // same order, as scanning every untaken candidate each round.
+    Cand c[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+        const int e = lane + 32 * i;
+        c[i] = e < E ? Cand{lv[i], e} : Cand{-INFINITY, 0x7fffffff};
+    }
+#pragma unroll
+    for (int size = 2; size <= NV; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    // best-first within blocks of `size` whose index bit `size` is 0
+                    const bool desc = (i & size) == 0;
+                    const Cand a = c[i], b = c[j];
+                    const bool swap = desc ? better(b, a) : better(a, b);
+                    c[i] = swap ? b : a;
+                    c[j] = swap ? a : b;
+                }
+            }
     float top0 = 0.0f, sel_v = 0.0f;
     int sel_id = 0;
     for (int j = 0; j < k; ++j) {
-        Cand c{-INFINITY, 0x7fffffff};
-        bool have = false;
-#pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            int e = lane + 32 * i;
-            if (e < E && !((taken >> i) & 1u)) {
-                Cand d{lv[i], e};
-                if (!have || better(d, c)) c = d;
-                have = true;
-            }
-        }
+        Cand w = c[0];
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) {
-            Cand d{__shfl_xor_sync(0xffffffffu, c.v, o), __shfl_xor_sync(0xffffffffu, c.id, o)};
-            if (better(d, c)) c = d;
+            Cand d{__shfl_xor_sync(0xffffffffu, w.v, o), __shfl_xor_sync(0xffffffffu, w.id, o)};
+            if (better(d, w)) w = d;
         }
-        if ((c.id & 31) == lane) taken |= 1u << (c.id >> 5);
-        if (j == 0) top0 = c.v;
+        if ((w.id & 31) == lane) {  // this lane's head was picked: drop it
+#pragma unroll
+            for (int i = 0; i + 1 < NV; ++i) c[i] = c[i + 1];
+            c[NV - 1] = Cand{-INFINITY, 0x7fffffff};
+        }
+        if (j == 0) top0 = w.v;
         if (lane == j) {  // lane j keeps pick j (k <= 32)
-            sel_v = c.v;
-            sel_id = c.id;
+            sel_v = w.v;
+            sel_id = w.id;
         }
     }
     // gates: softmax over the k picked, in pick order
