@@ -57,6 +57,8 @@ def parse_args():
                          "measurement (for profiling)")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the compressed large-layer (E=512) and mixed-precision (T=4096) measurements")
+    ap.add_argument("--overlap-groups", type=int, default=None,
+                    help="device pager: refill groups overlapped with the FFN passes (default by T; 0: none)")
     ap.add_argument("--pager", default="both", choices=["host", "device", "both"],
                     help="host: LRU on the host (one read-back per step); device: LRU on the GPU, each layer's step "
                          "replayed from a CUDA graph; both: measure both, the faster is the headline")
@@ -257,14 +259,16 @@ class GraphRunner:
     are already in place); a graph is launched once, so its first-launch cost
     is shared by the steps it holds."""
 
-    def __init__(self, pqe, torch, device, host, L, T):
+    def __init__(self, pqe, torch, device, host, L, T, overlap_groups=0):
         E, H, I, k, S = CFG.E, CFG.H, CFG.I, CFG.k, CFG.S
         self.pqe, self.torch, self.T = pqe, torch, T
         self.wb = pqe.alloc_working_buffer(E, H, I, device)
         nbytes = [pqe.page_bytes(pqe.PQE_FMT_FP8, H, I)] * E
         self.layers = [pqe.PagedMoELayer(E, H, I, k, S, E, T, host, nbytes, working_buffer=self.wb, device=device,
-                                         device_pager=True) for _ in range(L)]
+                                         device_pager=True, overlap_groups=overlap_groups) for _ in range(L)]
         self.stream = torch.cuda.Stream(device)
+        # the refills of an overlapped step run on this stream, forked and joined inside each step
+        self.side = torch.cuda.Stream(device)
         self.y = [torch.zeros((T, H), dtype=torch.bfloat16, device=device) for _ in range(L)]
         self.graphs = []  # (first step, steps, graph, kernel nodes)
 
@@ -275,7 +279,8 @@ class GraphRunner:
         L = len(self.layers)
         with torch.cuda.stream(self.stream):
             for l, layer in enumerate(self.layers):
-                layer.step(xs_dev[l % len(xs_dev)], self.y[l], self.T, logits=logits_dev[l], stream=self.stream)
+                layer.step(xs_dev[l % len(xs_dev)], self.y[l], self.T, logits=logits_dev[l], stream=self.stream,
+                           side_stream=self.side)
             torch.cuda.synchronize()
             for a, b in ranges:
                 for c in range(a, b, L):
@@ -285,7 +290,7 @@ class GraphRunner:
                     with torch.cuda.graph(g, stream=self.stream):
                         for i in range(c, c + n):
                             self.layers[i % L].step(xs_dev[i % len(xs_dev)], self.y[i % L], self.T,
-                                                    logits=logits_dev[i], stream=self.stream)
+                                                    logits=logits_dev[i], stream=self.stream, side_stream=self.side)
                     # launches recorded during the capture = kernel nodes run by each replay
                     self.graphs.append((c, n, g, self.pqe.kernel_launches() - n0))
         torch.cuda.synchronize()
@@ -306,13 +311,23 @@ class GraphRunner:
             l.close()
 
 
+def overlap_groups_for(T):
+    """Refill groups of an overlapped device-pager step by step size, the best
+    measured on the decode-shaped layer: none at T=1 (the FFN passes' fixed
+    costs outweigh what they hide), 3 at T=8, 5 at T=64 (2282 -> 2233 us)."""
+    return OVERLAP_GROUPS if OVERLAP_GROUPS is not None else (0 if T <= 1 else 3 if T < 32 else 5)
+
+
+OVERLAP_GROUPS = None  # --overlap-groups
+
+
 def run_graph(pqe, torch, device, host, T, L, logits_dev, xs_dev, warmup, K, ws, ffn_events=False):
     """Device-pager graph replays of steps L .. L + warmup + K - 1 (layer i % L).
     With ffn_events each layer's FFN is bracketed by event nodes in its graphs
     (after the timed loop they hold the FFN time of that layer's last replay).
     The two nodes add ~11 us to a replayed step, so the headline steps are
     timed without them and the FFN in a second pass."""
-    gr = GraphRunner(pqe, torch, device, host, L, T)
+    gr = GraphRunner(pqe, torch, device, host, L, T, overlap_groups_for(T))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
     if ffn_events:
         for (a, b), layer in zip(evs, gr.layers):
@@ -943,6 +958,8 @@ def huff_decode_rate(pqe, torch, device, comp_host, sizes, luts_host, H, I, nb, 
 
 def main():
     args = parse_args()
+    global OVERLAP_GROUPS
+    OVERLAP_GROUPS = args.overlap_groups
     ws, rank, local = dist_setup()
     if args.impl == "reference":
         return run_reference(args, ws, rank)
@@ -995,6 +1012,7 @@ def main():
         gms = max_over_ranks(ws, gms, device)
         gval = ws * T * K / (gms / 1e3)
         graph = {"tokens_per_s": gval, "ms_per_step": gms / K, "gpu_launches": int(glaunch),
+                 "overlap_groups": overlap_groups_for(T),
                  "mean_routed_experts": gstats["routed"] / K, "mean_misses": gstats["misses"] / K,
                  "working_buffer_steps": gstats["working_buffer_steps"],
                  "h2d_gb_per_s": gstats["refill_bytes"] / (gms / 1e3) / 1e9, "clocks": clk_g}
@@ -1070,6 +1088,7 @@ def main():
                 fm = [f_s[i] for i in sorted(f_s)]
                 rec_host = {k: rec[k] for k in ("tokens_per_s", "ms_per_step", "ffn_hbm_gbs")}
                 rec = {"tokens_per_s": ws * Ts * K / (gms_s / 1e3), "ms_per_step": gms_s / K, "pager": "device",
+                       "overlap_groups": overlap_groups_for(Ts),
                        "ffn_ms": float(np.mean(fm)), "ffn_hbm_gbs": sum(fb) / (sum(fm) / 1e3) / 1e9,
                        "misses_per_step": gst_s["misses"] / K, "host_pager": rec_host}
                 r = Runner(pqe, torch, device, host, L, max(T, 64))

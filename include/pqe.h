@@ -597,7 +597,16 @@ typedef struct pqe_layer_config {
     int32_t compressed; /* host pages are compressed pages (decoded after the copy) */
     int32_t device_pager; /* 1: LRU state and refills on the GPU, no host synchronisation in a step
                              (uncompressed host pages only) */
+    int32_t overlap_groups; /* device pager with a side stream given to the step: 0 refills every miss,
+                               then runs the FFN once; G >= 1 (at most PQE_MAX_OVERLAP_GROUPS) refills
+                               the misses in G groups on the side stream (a refill kernel on a few SMs)
+                               while the FFN runs in passes on the step's stream: first the experts
+                               already resident, then each group once its pages have landed (transfers
+                               overlapped with compute, MoE-Gen summary, 3.中核となる技術的要素). The
+                               FFN timing events of pqe_layer_set_ffn_events select the single pass. */
 } pqe_layer_config;
+
+#define PQE_MAX_OVERLAP_GROUPS 16
 
 typedef struct pqe_step_info {
     int32_t n_routed;       /* |U|: experts with a non-empty batch */

@@ -51,7 +51,8 @@ class PqeError(RuntimeError):
 
 
 class pqe_layer_config(C.Structure):
-    _fields_ = [(n, C.c_int32) for n in ("E", "H", "I", "k", "S", "W", "max_T", "compressed", "device_pager")]
+    _fields_ = [(n, C.c_int32) for n in ("E", "H", "I", "k", "S", "W", "max_T", "compressed", "device_pager",
+                                         "overlap_groups")]
 
 
 class pqe_step_info(C.Structure):
@@ -564,8 +565,9 @@ class PagedMoELayer:
 
     def __init__(self, E, H, I, k, S, W, max_T, host_pages, host_page_bytes, compressed=False, luts=None,
                  expert_fmt=None, device="cuda", working_buffer: Optional[torch.Tensor] = None,
-                 device_pager=False):
-        self.cfg = pqe_layer_config(E, H, I, k, S, W, max_T, int(bool(compressed)), int(bool(device_pager)))
+                 device_pager=False, overlap_groups=0):
+        self.cfg = pqe_layer_config(E, H, I, k, S, W, max_T, int(bool(compressed)), int(bool(device_pager)),
+                                    int(overlap_groups))
         self.device_pager = bool(device_pager)
         self.E, self.H, self.I, self.k, self.S, self.W, self.max_T = E, H, I, k, S, W, max_T
         self.pool_mem = torch.zeros(max(S, 1) * slot_stride(H, I), dtype=torch.uint8, device=device)

@@ -55,13 +55,29 @@ __device__ __forceinline__ int block_excl_scan(int v, int *warp_tot, int &total)
     return r;
 }
 
+// With a miss list (an overlapped step), only the experts of pass `pass` are
+// scheduled: pass 0 the experts not in the list, pass g + 1 the misses refill
+// group g brings (ranks overlap_group_start(g) .. overlap_group_start(g + 1) - 1).
 __global__ void __launch_bounds__(1024) ffn_schedule_kernel(FfnArgs a, int tc_min, int32_t *__restrict__ tiles,
-                                                            int32_t *__restrict__ n_tiles) {
+                                                            int32_t *__restrict__ n_tiles,
+                                                            const int32_t *__restrict__ miss, int groups, int pass) {
     pdl_acquire();  // launched after the previous kernel of the step: wait for its output
     __shared__ int warp_tot[33];
+    __shared__ int16_t s_pass[1024];
     const int e = threadIdx.x;
+    if (miss) {
+        if (e < a.E) s_pass[e] = 0;
+        __syncthreads();
+        const int nm = miss[0];
+        for (int r = e; r < nm; r += blockDim.x) {
+            int g = 0;
+            while (g + 1 < groups && overlap_group_start(g + 1, groups, nm) <= r) ++g;
+            s_pass[miss[2 + r]] = (int16_t)(1 + g);
+        }
+        __syncthreads();
+    }
     int n = 0, slot = -1, fmt = PQE_FMT_FP8;
-    if (e < a.E) {
+    if (e < a.E && (!miss || s_pass[e] == pass)) {
         n = a.offsets[e + 1] - a.offsets[e];
         slot = a.page_table[e];
         fmt = a.expert_fmt ? (int)a.expert_fmt[e] : PQE_FMT_FP8;
@@ -498,7 +514,20 @@ size_t moe_paged_ffn_workspace_size(int T, int k, int E, int H, int I) {
 int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *offsets, const int32_t *page_table,
                   const uint8_t *expert_fmt, const pqe_pool *pool, int T, int k, int E, void *out_perm, void *ws,
                   size_t ws_bytes, int32_t *status, void *stream) {
+    return pqe::moe_paged_ffn_pass(x_bf16, perm_src, offsets, page_table, expert_fmt, pool, T, k, E, out_perm, ws,
+                                   ws_bytes, status, as_stream(stream), nullptr, 1, 0, 0);
+}
+
+}  // extern "C"
+
+namespace pqe {
+
+int moe_paged_ffn_pass(const void *x_bf16, const int32_t *perm_src, const int32_t *offsets,
+                       const int32_t *page_table, const uint8_t *expert_fmt, const pqe_pool *pool, int T, int k,
+                       int E, void *out_perm, void *ws, size_t ws_bytes, int32_t *status, cudaStream_t s,
+                       const int32_t *miss, int groups, int pass, int reserve_sms) {
     PQE_CHECK_ARG(pool && T >= 0 && k >= 1 && k <= 32 && E >= 1 && E <= 1024 && k <= E);
+    PQE_CHECK_ARG(groups >= 1 && pass >= 0 && pass <= groups && reserve_sms >= 0);
     PQE_CHECK_ARG(shape_ok(pool->H, pool->I));
     if (T == 0) return PQE_OK;
     PQE_CHECK_ARG(x_bf16 && perm_src && offsets && page_table && out_perm && ws && status);
@@ -535,15 +564,17 @@ int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *of
     args.phase2_bias = phase2_bias();
     const long A = (long)T * k;
     const int max_active = (int)(A < E ? A : E);
-    cudaStream_t s = as_stream(stream);
     int32_t *tiles = reinterpret_cast<int32_t *>(wsb + w.tiles);
     int32_t *n_tiles = reinterpret_cast<int32_t *>(wsb + w.n_tiles);
-    const int sr = launch_pdl(ffn_schedule_kernel, 1, 1024, 0, s, args, w.tc ? TC_MIN_ROWS : 0, tiles, n_tiles);
+    const int sr = launch_pdl(ffn_schedule_kernel, 1, 1024, 0, s, args, w.tc ? TC_MIN_ROWS : 0, tiles, n_tiles, miss,
+                              groups, pass);
     if (sr != PQE_OK) return sr;
     const bool stream_path = stream_shape_ok(pool->H, pool->I);
     int dev = 0, sms = 0;
     const int di = device_info(dev, sms);
     if (di != PQE_OK) return di;
+    // SMs left to a refill running beside this pass
+    if (reserve_sms > 0) sms = sms - reserve_sms > 2 * TC_SIDE_SMS + 8 ? sms - reserve_sms : 2 * TC_SIDE_SMS + 8;
     // decode-sized step: the tensor-core batches run beside the weight stream
     const bool side = stream_path && w.tc && A >= TC_MIN_ROWS && A <= (long)DECODE_ROWS_PER_EXPERT * E &&
                       sms > 2 * TC_SIDE_SMS;
@@ -555,7 +586,7 @@ int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *of
     }
     // the stream kernel goes out first: from an idle GPU every host step before it
     // is a gap after the schedule kernel
-    int rc = stream_path ? launch_ffn_stream(args, s, side ? sms - TC_SIDE_SMS : 0)
+    int rc = stream_path ? launch_ffn_stream(args, s, side ? sms - TC_SIDE_SMS : (reserve_sms > 0 ? sms : 0))
                          : launch_ffn_gemv(args, max_active, s);
     if (side) PQE_CUDA_TRY(cudaStreamWaitEvent(ss->s, ss->fork, 0));
     if (rc != PQE_OK || !w.tc) {
@@ -577,7 +608,7 @@ int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *of
     b.hmax = reinterpret_cast<uint32_t *>(wsb + w.hmax);
     b.hq = wsb + w.hq;
     b.sh = reinterpret_cast<float *>(wsb + w.sh);
-    if (!side) return launch_ffn_tc(args, b, w.max_tiles, s);
+    if (!side) return launch_ffn_tc(args, b, w.max_tiles, s, sms);
     rc = launch_ffn_tc(args, b, w.max_tiles, ss->s, TC_SIDE_SMS);
     // the join is recorded even after a failed launch, so the caller's stream never
     // waits on a fork that was left open
@@ -586,4 +617,4 @@ int moe_paged_ffn(const void *x_bf16, const int32_t *perm_src, const int32_t *of
     return rc;
 }
 
-}  // extern "C"
+}  // namespace pqe

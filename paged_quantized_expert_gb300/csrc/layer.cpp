@@ -18,6 +18,7 @@
 #include <vector>
 
 #include "pqe.h"
+#include "pqe_common.cuh"
 
 namespace pqe {
 void set_last_cuda_error(cudaError_t e);
@@ -71,12 +72,19 @@ ScratchMap scratch_map(const pqe_layer_config &c) {
     return m;
 }
 
+// CTAs of the refill kernel in an overlapped step: eight already pull pinned
+// host pages at the host link's rate (measured), the rest of the GPU runs the FFN
+constexpr int OVERLAP_FILL_CTAS = 16;
+
 bool config_ok(const pqe_layer_config *c) {
     if (!c || c->E < 1 || c->E > 1024 || c->k < 1 || c->k > 32 || c->k > c->E || c->S < 0 || c->W < 0 ||
         c->max_T < 1 || (size_t)c->max_T * c->k >= (1u << 30) || pqe_page_bytes(PQE_FMT_FP8, c->H, c->I) == 0)
         return false;
     // the device pager: uncompressed pages, at most 1024 slots, a working buffer for any step
     if (c->device_pager && (c->compressed || c->S > 1024 || c->W < c->E)) return false;
+    if (c->overlap_groups < 0 || c->overlap_groups > PQE_MAX_OVERLAP_GROUPS ||
+        (c->overlap_groups > 0 && !c->device_pager))
+        return false;
     return true;
 }
 
@@ -94,6 +102,7 @@ struct pqe_layer {
     pqe_lru *lru = nullptr;
     int32_t *pinned = nullptr;  // counts [E], page table [E], miss expert [E], miss dest [E]
     cudaEvent_t ev_counts = nullptr, ev_fill = nullptr;
+    cudaEvent_t ev_lru = nullptr, ev_group[PQE_MAX_OVERLAP_GROUPS] = {};  // overlapped device-pager steps
     cudaEvent_t ev_ffn_begin = nullptr, ev_ffn_end = nullptr;  // caller's, optional
     std::vector<const void *> fill_src;  // [E] scratch for slot_fill_batch / slot_fill_compressed_batch
     std::vector<size_t> fill_bytes;
@@ -192,6 +201,11 @@ pqe_layer *pqe_layer_create(const pqe_layer_config *cfg, const pqe_pool *pool, c
                                    cudaHostAllocDefault);
     cudaError_t e2 = cudaEventCreateWithFlags(&L->ev_counts, cudaEventDisableTiming);
     cudaError_t e3 = cudaEventCreateWithFlags(&L->ev_fill, cudaEventDisableTiming);
+    if (e3 == cudaSuccess && cfg->overlap_groups > 0) {
+        e3 = cudaEventCreateWithFlags(&L->ev_lru, cudaEventDisableTiming);
+        for (int g = 0; g < cfg->overlap_groups && e3 == cudaSuccess; ++g)
+            e3 = cudaEventCreateWithFlags(&L->ev_group[g], cudaEventDisableTiming);
+    }
     if (!L->lru || e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) {
         pqe::set_last_cuda_error(e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3));
         pqe_layer_destroy(L);
@@ -221,6 +235,9 @@ void pqe_layer_destroy(pqe_layer *L) {
     if (!L) return;
     if (L->ev_counts) cudaEventDestroy(L->ev_counts);
     if (L->ev_fill) cudaEventDestroy(L->ev_fill);
+    if (L->ev_lru) cudaEventDestroy(L->ev_lru);
+    for (cudaEvent_t e : L->ev_group)
+        if (e) cudaEventDestroy(e);
     if (L->pinned) cudaFreeHost(L->pinned);
     pqe_lru_destroy(L->lru);
     delete L;
@@ -349,6 +366,40 @@ int pqe_layer_step(pqe_layer *L, const void *x_dev, const float *w_router_dev, f
         const size_t *pbytes = L->at<size_t>(m.page_bytes);
         rc = page_table_update_device(L->at<void>(m.lru), c.E, c.S, counts, pbytes, page_table, miss, stream);
         if (rc) return rc;
+        const int G = c.overlap_groups;
+        if (G > 0 && side != s && !L->ev_ffn_begin) {
+            // refills in G groups on the side stream, each by a refill kernel on a few
+            // SMs; the FFN in passes on s: the resident experts first, beside the
+            // refills, then each group's experts once its pages have landed
+            const uint64_t *hp = L->at<uint64_t>(m.host_pages);
+            cudaError_t ce = cudaEventRecord(L->ev_lru, s);
+            if (ce == cudaSuccess) ce = cudaStreamWaitEvent(side, L->ev_lru, 0);
+            for (int g = 0; g < G && ce == cudaSuccess; ++g) {
+                if ((rc = pqe::slot_fill_device_group(&L->pool, miss, c.E, hp, pbytes, g, G, OVERLAP_FILL_CTAS,
+                                                      side)))
+                    return rc;
+                ce = cudaEventRecord(L->ev_group[g], side);
+            }
+            if (ce != cudaSuccess) {
+                pqe::set_last_cuda_error(ce);
+                return PQE_ERR_CUDA;
+            }
+            void *ws = L->at<void>(m.ffn_ws);
+            for (int p = 0; p <= G; ++p) {
+                if (p > 0 && (ce = cudaStreamWaitEvent(s, L->ev_group[p - 1], 0)) != cudaSuccess) {
+                    pqe::set_last_cuda_error(ce);
+                    return PQE_ERR_CUDA;
+                }
+                rc = pqe::moe_paged_ffn_pass(x_dev, perm_src, offsets, page_table, L->expert_fmt, &L->pool, T, c.k,
+                                             c.E, out_perm, ws, m.ffn_ws_bytes, status, s, miss, G, p,
+                                             p < G ? OVERLAP_FILL_CTAS : 0);
+                if (rc) return rc;
+            }
+            rc = moe_combine(out_perm, inv, gates, T, c.k, c.H, y_dev, stream);
+            if (rc) return rc;
+            if (info) *info = local;
+            return PQE_OK;
+        }
         rc = slot_fill_device(&L->pool, miss, c.E, L->at<uint64_t>(m.host_pages), pbytes, stream);
         if (rc) return rc;
         if (L->ev_ffn_begin && (rc = (record_timing(L->ev_ffn_begin, s) == cudaSuccess ? 0 : PQE_ERR_CUDA))) return rc;

@@ -212,7 +212,9 @@ __global__ void __launch_bounds__(1024) lru_step_kernel(void *state, int E, int 
 
 // refill from a device miss list: warps walk 8 KiB segments of the missed
 // pages (one page = ceil(bytes / 8 KiB) segments); pages are located by
-// binary search over the per-miss segment prefix written by the LRU step
+// binary search over the per-miss segment prefix written by the LRU step.
+// Group g of G takes the misses of rank overlap_group_start(g) .. (g + 1) - 1,
+// the grouping the FFN passes of an overlapped step use.
 constexpr int DF_THREADS = 512;
 constexpr int DF_UNROLL = 16;
 static_assert(DF_SEG == 32 * DF_UNROLL * 16, "a warp moves one segment per pass");
@@ -222,17 +224,19 @@ __global__ void __launch_bounds__(DF_THREADS) fill_device_kernel(const int32_t *
                                                                  const size_t *__restrict__ page_bytes,
                                                                  uint8_t *__restrict__ base,
                                                                  uint8_t *__restrict__ wb_base, int n_slots,
-                                                                 size_t slot_stride) {
+                                                                 size_t slot_stride, int group, int groups) {
     pdl_acquire();  // launched after the previous kernel of the step: wait for its output
-    extern __shared__ uint32_t seg0[];  // [n_miss + 1]
-    const int n = miss[0];
-    const int32_t *mexp = miss + 2, *mdst = miss + 2 + E, *mseg = miss + 2 + 2 * E;
+    extern __shared__ uint32_t seg0[];  // [misses of the group + 1]
+    const int n_all = miss[0];
+    const int m0 = overlap_group_start(group, groups, n_all), m1 = overlap_group_start(group + 1, groups, n_all);
+    const int n = m1 - m0;
+    const int32_t *mexp = miss + 2 + m0, *mdst = miss + 2 + E + m0, *mseg = miss + 2 + 2 * E + m0;
     for (int i = threadIdx.x; i <= n; i += blockDim.x) seg0[i] = (uint32_t)mseg[i];
     __syncthreads();
-    const uint32_t total = seg0[n];
+    const uint32_t first = seg0[0], total = seg0[n];
     const int lane = threadIdx.x & 31;
     const uint32_t nwarps = gridDim.x * (DF_THREADS / 32);
-    for (uint32_t seg = blockIdx.x * (DF_THREADS / 32) + (threadIdx.x >> 5); seg < total; seg += nwarps) {
+    for (uint32_t seg = first + blockIdx.x * (DF_THREADS / 32) + (threadIdx.x >> 5); seg < total; seg += nwarps) {
         int lo = 0, hi = n - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
@@ -314,9 +318,21 @@ int slot_fill_device(const pqe_pool *pool, const int32_t *miss, int E, const uin
     int dev = 0, sms = 0;
     const int di = device_info(dev, sms);
     if (di != PQE_OK) return di;
-    return launch_pdl(fill_device_kernel, sms, DF_THREADS, sizeof(uint32_t) * (E + 1), as_stream(stream), miss, E,
-                      host_pages, page_bytes, static_cast<uint8_t *>(pool->base), static_cast<uint8_t *>(pool->wb_base),
-                      pool->n_slots, pool->slot_stride);
+    return slot_fill_device_group(pool, miss, E, host_pages, page_bytes, 0, 1, sms, as_stream(stream));
 }
 
 }  // extern "C"
+
+namespace pqe {
+
+int slot_fill_device_group(const pqe_pool *pool, const int32_t *miss, int E, const uint64_t *host_pages,
+                           const size_t *page_bytes, int group, int groups, int ctas, cudaStream_t s) {
+    if (!pool || !miss || !host_pages || !page_bytes || E < 1 || E > 1024 || groups < 1 || group < 0 ||
+        group >= groups || ctas < 1)
+        return PQE_ERR_INVALID_ARG;
+    return launch_pdl(fill_device_kernel, ctas, DF_THREADS, sizeof(uint32_t) * (E + 1), s, miss, E, host_pages,
+                      page_bytes, static_cast<uint8_t *>(pool->base), static_cast<uint8_t *>(pool->wb_base),
+                      pool->n_slots, pool->slot_stride, group, groups);
+}
+
+}  // namespace pqe

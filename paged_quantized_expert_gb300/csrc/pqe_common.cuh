@@ -51,6 +51,30 @@ __device__ __forceinline__ void pdl_acquire() {
     pdl_trigger();
 }
 
+// ---- internal entry points used by the layer runtime --------------------------
+
+// Refill groups of an overlapped step over n misses: group g of G starts at miss
+// rank n - (n >> g) (halves: 1/2, 1/4, ... of the misses, the last group taking
+// the rest), so the FFN pass left after the last refill is the smallest, while
+// every earlier pass runs beside a refill of at least half its pages.
+__host__ __device__ inline int overlap_group_start(int g, int G, int n) {
+    return g >= G ? n : n - (g < 31 ? (n >> g) : 0);
+}
+
+// refill of group `group` of `groups` of a device miss list (the misses from
+// overlap_group_start(group) on) by a grid of `ctas` CTAs
+int slot_fill_device_group(const pqe_pool *pool, const int32_t *miss, int E, const uint64_t *host_pages,
+                           const size_t *page_bytes, int group, int groups, int ctas, cudaStream_t s);
+
+// moe_paged_ffn restricted to one pass of an overlapped step (miss non-null):
+// pass 0 takes the experts that were resident (not in the miss list), pass
+// g + 1 the misses of refill group g of `groups`; `reserve_sms` SMs are left to
+// a refill running beside it
+int moe_paged_ffn_pass(const void *x_bf16, const int32_t *perm_src, const int32_t *offsets,
+                       const int32_t *page_table, const uint8_t *expert_fmt, const pqe_pool *pool, int T, int k,
+                       int E, void *out_perm, void *ws, size_t ws_bytes, int32_t *status, cudaStream_t s,
+                       const int32_t *miss, int groups, int pass, int reserve_sms);
+
 template <class T>
 struct ident {
     using type = T;

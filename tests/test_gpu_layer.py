@@ -39,7 +39,7 @@ def _ram_tier(pqe, host, nbytes, S_ram, W_ram, path, n_threads=4):
 
 
 def _run_trace(pqe, orc, cfg, T, steps, S, W, check_every, n_check, side=True, host_api=False, device_pager=False,
-               ram_slots=None, ram_wb=0, tmp_path=None):
+               ram_slots=None, ram_wb=0, tmp_path=None, overlap_groups=0):
     # experts the checked tokens of the checked steps use get oracle weights
     tr = synth.RoutingTrace(cfg, T)
     logits_all = [tr.step(s) for s in range(steps)]
@@ -53,7 +53,7 @@ def _run_trace(pqe, orc, cfg, T, steps, S, W, check_every, n_check, side=True, h
     pages = Pages(pqe, orc, cfg, needed=needed, seed=7)
     host, nbytes = _host_tier(pqe, pages)
     layer = pqe.PagedMoELayer(cfg.E, cfg.H, cfg.I, cfg.k, S, W, T, host, nbytes, expert_fmt=pages.fmt_dev,
-                              device_pager=device_pager)
+                              device_pager=device_pager, overlap_groups=overlap_groups)
     ref_lru = orc.LRU(cfg.E, S)
     tier = ref_ram = None
     if ram_slots is not None:
@@ -239,9 +239,28 @@ def test_layer_device_pager_working_buffer(cuda_lib, orc):
     _run_trace(cuda_lib, orc, cfg, T=64, steps=5, S=cfg.S, W=cfg.E, check_every=4, n_check=2, device_pager=True)
 
 
-def test_layer_device_pager_graph_replay(cuda_lib, orc):
+@pytest.mark.parametrize("groups", [1, 3])
+def test_layer_device_pager_overlapped_refills(cuda_lib, orc, groups):
+    # misses refilled in groups on the side stream while the FFN runs in passes
+    # (resident experts first, then each group's): same LRU states as the oracle
+    # and every token of the checked steps within the bounds
+    cfg = synth.WORKLOADS["decode"]
+    _run_trace(cuda_lib, orc, cfg, T=8, steps=30, S=cfg.S, W=cfg.E, check_every=5, n_check=8, device_pager=True,
+               overlap_groups=groups)
+
+
+def test_layer_device_pager_overlapped_working_buffer(cuda_lib, orc):
+    # every routed expert a miss: the resident pass is empty, four refill groups
+    cfg = synth.WORKLOADS["decode"]
+    _run_trace(cuda_lib, orc, cfg, T=64, steps=5, S=cfg.S, W=cfg.E, check_every=2, n_check=8, device_pager=True,
+               overlap_groups=4)
+
+
+@pytest.mark.parametrize("groups", [0, 2])
+def test_layer_device_pager_graph_replay(cuda_lib, orc, groups):
     # with the device pager a whole step has no host synchronisation: capture it
     # once in a CUDA graph and replay it on new inputs copied into its buffers
+    # (groups > 0: the refill groups on a side stream inside the graph)
     pqe = cuda_lib
     cfg = synth.small_config(E=16, H=256, I=128, k=2, T=8, S=4, cid=80, reuse_p=0.5, zipf_s=1.1,
                              router_gemm=False, steps=8)
@@ -249,7 +268,8 @@ def test_layer_device_pager_graph_replay(cuda_lib, orc):
     pages = Pages(pqe, orc, cfg, needed=set(range(cfg.E)), seed=11)
     host, nbytes = _host_tier(pqe, pages)
     layer = pqe.PagedMoELayer(cfg.E, cfg.H, cfg.I, cfg.k, cfg.S, cfg.E, T, host, nbytes, expert_fmt=pages.fmt_dev,
-                              device_pager=True)
+                              device_pager=True, overlap_groups=groups)
+    side = torch.cuda.Stream() if groups else None
     tr = synth.RoutingTrace(cfg, T)
     logits_all = [tr.step(s) for s in range(8)]
     x_buf = torch.zeros((T, cfg.H), dtype=torch.int16, device=DEV)
@@ -258,7 +278,7 @@ def test_layer_device_pager_graph_replay(cuda_lib, orc):
     # step 0 eagerly (also warms up the launch paths), then capture step 1
     x_buf.copy_(torch.from_numpy(synth.activations(cfg, T, 0).view(np.int16)))
     lg_buf.copy_(torch.from_numpy(logits_all[0]))
-    layer.step(x_buf, y, T, logits=lg_buf)
+    layer.step(x_buf, y, T, logits=lg_buf, side_stream=side)
     torch.cuda.synchronize()
     ref_lru = orc.LRU(cfg.E, cfg.S)
     ref_lru.step(np.bincount(orc.topk_gates(logits_all[0], cfg.k)[0].reshape(-1), minlength=cfg.E).astype(np.int32))
@@ -266,7 +286,7 @@ def test_layer_device_pager_graph_replay(cuda_lib, orc):
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(g, stream=stream):
-            layer.step(x_buf, y, T, logits=lg_buf, stream=stream)
+            layer.step(x_buf, y, T, logits=lg_buf, stream=stream, side_stream=side)
     torch.cuda.synchronize()
     # capture did not run the step: the LRU state is still after step 0
     assert layer.lru_state()[2] == 1
