@@ -599,7 +599,7 @@ typedef struct pqe_layer_config {
                              (uncompressed host pages only) */
     int32_t overlap_groups; /* device pager with a side stream given to the step: 0 refills every miss,
                                then runs the FFN once; G >= 1 (at most PQE_MAX_OVERLAP_GROUPS) refills
-                               the misses in G groups on the side stream (a refill kernel on a few SMs)
+                               the misses in G groups on the side stream (a refill kernel on 32 CTAs)
                                while the FFN runs in passes on the step's stream: first the experts
                                already resident, then each group once its pages have landed (transfers
                                overlapped with compute, MoE-Gen summary, 3.中核となる技術的要素). The

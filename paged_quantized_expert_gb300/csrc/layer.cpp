@@ -73,8 +73,9 @@ ScratchMap scratch_map(const pqe_layer_config &c) {
 }
 
 // CTAs of the refill kernel in an overlapped step: eight already pull pinned
-// host pages at the host link's rate (measured), the rest of the GPU runs the FFN
-constexpr int OVERLAP_FILL_CTAS = 16;
+// host pages at the host link's rate alone; beside the FFN passes 32 did best
+// (16 and 64 within 2 us of it at T=64), the rest of the GPU runs the FFN
+constexpr int OVERLAP_FILL_CTAS = 32;
 
 bool config_ok(const pqe_layer_config *c) {
     if (!c || c->E < 1 || c->E > 1024 || c->k < 1 || c->k > 32 || c->k > c->E || c->S < 0 || c->W < 0 ||
