@@ -76,6 +76,10 @@ ScratchMap scratch_map(const pqe_layer_config &c) {
 // host pages at the host link's rate alone; beside the FFN passes 32 did best
 // (16 and 64 within 2 us of it at T=64), the rest of the GPU runs the FFN
 constexpr int OVERLAP_FILL_CTAS = 32;
+// SMs of an FFN pass that runs beside a refill: the passes have slack (each
+// runs under a refill at least half its size), and fewer SMs disturb the
+// refill less (T=64: 2233 us on all but the refill's SMs, 2224 on 48-96)
+constexpr int OVERLAP_FFN_SMS = 64;
 
 bool config_ok(const pqe_layer_config *c) {
     if (!c || c->E < 1 || c->E > 1024 || c->k < 1 || c->k > 32 || c->k > c->E || c->S < 0 || c->W < 0 ||
@@ -386,6 +390,9 @@ int pqe_layer_step(pqe_layer *L, const void *x_dev, const float *w_router_dev, f
                 return PQE_ERR_CUDA;
             }
             void *ws = L->at<void>(m.ffn_ws);
+            int dev = 0, sms = 0;
+            if ((rc = pqe::device_info(dev, sms))) return rc;
+            const int reserve = std::max(OVERLAP_FILL_CTAS, sms - OVERLAP_FFN_SMS);
             for (int p = 0; p <= G; ++p) {
                 if (p > 0 && (ce = cudaStreamWaitEvent(s, L->ev_group[p - 1], 0)) != cudaSuccess) {
                     pqe::set_last_cuda_error(ce);
@@ -393,7 +400,7 @@ int pqe_layer_step(pqe_layer *L, const void *x_dev, const float *w_router_dev, f
                 }
                 rc = pqe::moe_paged_ffn_pass(x_dev, perm_src, offsets, page_table, L->expert_fmt, &L->pool, T, c.k,
                                              c.E, out_perm, ws, m.ffn_ws_bytes, status, s, miss, G, p,
-                                             p < G ? OVERLAP_FILL_CTAS : 0);
+                                             p < G ? reserve : 0);
                 if (rc) return rc;
             }
             rc = moe_combine(out_perm, inv, gates, T, c.k, c.H, y_dev, stream);
