@@ -249,6 +249,39 @@ def test_layer_device_pager_overlapped_refills(cuda_lib, orc, groups):
                overlap_groups=groups)
 
 
+@pytest.mark.parametrize("T,groups", [(8, 3), (64, 5)])
+def test_layer_overlapped_steps_bit_identical(cuda_lib, orc, T, groups):
+    # the passes compute every expert with the same kernels and summation order
+    # as one FFN call: y, the page table and the LRU state equal a plain layer's
+    # bit for bit, step after step
+    pqe = cuda_lib
+    cfg = synth.WORKLOADS["decode"]
+    pages = Pages(pqe, orc, cfg, needed=set(), seed=3)
+    host, nbytes = _host_tier(pqe, pages)
+    tr = synth.RoutingTrace(cfg, T)
+    mk = lambda g: pqe.PagedMoELayer(cfg.E, cfg.H, cfg.I, cfg.k, cfg.S, cfg.E, T, host, nbytes,
+                                     expert_fmt=pages.fmt_dev, device_pager=True, overlap_groups=g)
+    plain, ovl = mk(0), mk(groups)
+    side = torch.cuda.Stream()
+    y0 = torch.zeros((T, cfg.H), dtype=torch.bfloat16, device=DEV)
+    y1 = torch.zeros_like(y0)
+    for s in range(6):
+        x = torch.from_numpy(synth.activations(cfg, T, s).view(np.int16)).to(DEV)
+        lg = torch.from_numpy(tr.step(s)).to(DEV)
+        plain.step(x, y0, T, logits=lg, side_stream=side)
+        ovl.step(x, y1, T, logits=lg, side_stream=side)
+        torch.cuda.synchronize()
+        assert torch.equal(y0.view(torch.int16), y1.view(torch.int16)), s
+        pt0 = plain.device_view("page_table", torch.int32, (cfg.E,)).clone()
+        pt1 = ovl.device_view("page_table", torch.int32, (cfg.E,)).clone()
+        assert torch.equal(pt0, pt1), s
+        a, b = plain.lru_state(), ovl.lru_state()
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]) and a[2] == b[2], s
+    for l in (plain, ovl):
+        assert l.device_view("status", torch.int32, (1,)).item() == 0
+        l.close()
+
+
 def test_layer_device_pager_overlapped_working_buffer(cuda_lib, orc):
     # every routed expert a miss: the resident pass is empty, four refill groups
     cfg = synth.WORKLOADS["decode"]
