@@ -28,6 +28,11 @@
  *     memory; "pinned" means page-locked host memory (cudaHostAlloc).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream). Device calls are asynchronous on it unless stated otherwise.
+ *     Most kernels are launched with programmatic stream serialization, so
+ *     one may be set up while the kernel before it on the stream finishes;
+ *     none reads memory before the kernels whose output it reads have
+ *     completed (griddepcontrol.wait), and none completes before the kernel
+ *     launched before it, so ordering on `stream` is that of plain launches.
  *   - Arguments are checked on the host before any launch; a bad argument
  *     returns PQE_ERR_INVALID_ARG and launches nothing.
  *   - Errors found on the device (an out-of-range expert id, a corrupt
