@@ -436,7 +436,10 @@ struct FfnWs {
 static FfnWs ffn_ws_layout(int T, int k, int E, int H, int I) {
     FfnWs w{};
     const size_t A = (size_t)T * k;
-    w.tc = tc_shape_ok(H, I) && A >= (size_t)TC_MIN_ROWS;
+    // an expert's batch holds at most one row per token (top-k picks distinct
+    // experts), so with fewer than TC_MIN_ROWS tokens no batch reaches the
+    // tensor cores: no tile buffers, no side chain, the weight stream on every SM
+    w.tc = tc_shape_ok(H, I) && T >= TC_MIN_ROWS;
     w.max_tiles = w.tc ? (int)((A + 127) / 128 + (size_t)E) : 0;
     size_t off = 0;
     auto take = [&off](size_t b) {
