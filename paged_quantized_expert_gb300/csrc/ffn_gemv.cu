@@ -18,7 +18,7 @@
 namespace pqe {
 
 // ---------------------------------------------------------------------------
-// schedule (one CTA of 1024 threads, one thread per expert, ascending id):
+// schedule (one CTA, one thread per expert, ascending id):
 //   sched[0] = count, sched[1 + a] = experts for the CUDA-core path;
 //   tiles[i] = {expert, first batch row, valid rows, page entry} of the
 //   128-row tiles of experts on the tensor-core path, those of FP8 pages
@@ -27,32 +27,39 @@ namespace pqe {
 // tc_min rows, its page is FP8 or MXFP4 and its page-table entry is inside
 // the pool.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ int block_excl_scan(int v, int *warp_tot, int &total) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    int incl = v;
+// exclusive scans of four ints per thread at once (blockDim a multiple of 32,
+// at most 1024): one pair of barriers for all four
+__device__ __forceinline__ int4 block_excl_scan4(int4 v, int (*wt)[33], int4 &total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int4 incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += n;
+        const int a = __shfl_up_sync(0xffffffffu, incl.x, o), b = __shfl_up_sync(0xffffffffu, incl.y, o),
+                  c = __shfl_up_sync(0xffffffffu, incl.z, o), d = __shfl_up_sync(0xffffffffu, incl.w, o);
+        if (lane >= o) incl = make_int4(incl.x + a, incl.y + b, incl.z + c, incl.w + d);
     }
-    if (lane == 31) warp_tot[w] = incl;
+    if (lane == 31) {
+        wt[0][w] = incl.x;
+        wt[1][w] = incl.y;
+        wt[2][w] = incl.z;
+        wt[3][w] = incl.w;
+    }
     __syncthreads();
-    if (w == 0) {
-        const int c = warp_tot[lane];
+    for (int q = w; q < 4; q += nw) {  // component q's warp totals, scanned by warp q mod nw
+        const int c = lane < nw ? wt[q][lane] : 0;
         int ci = c;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int n = __shfl_up_sync(0xffffffffu, ci, o);
             if (lane >= o) ci += n;
         }
-        warp_tot[lane] = ci - c;
-        if (lane == 31) warp_tot[32] = ci;
+        wt[q][lane] = ci - c;
+        if (lane == 31) wt[q][32] = ci;
     }
     __syncthreads();
-    const int r = warp_tot[w] + incl - v;
-    total = warp_tot[32];
-    __syncthreads();
-    return r;
+    total = make_int4(wt[0][32], wt[1][32], wt[2][32], wt[3][32]);
+    return make_int4(wt[0][w] + incl.x - v.x, wt[1][w] + incl.y - v.y, wt[2][w] + incl.z - v.z,
+                     wt[3][w] + incl.w - v.w);
 }
 
 // With a miss list (an overlapped step), only the experts of pass `pass` are
@@ -62,7 +69,7 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(FfnArgs a, int tc_mi
                                                             int32_t *__restrict__ n_tiles,
                                                             const int32_t *__restrict__ miss, int groups, int pass) {
     pdl_acquire();  // launched after the previous kernel of the step: wait for its output
-    __shared__ int warp_tot[33];
+    __shared__ int scan_tot[4][33];
     __shared__ int16_t s_pass[1024];
     const int e = threadIdx.x;
     if (miss) {
@@ -89,22 +96,19 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(FfnArgs a, int tc_mi
     // on the block-scaled GEMM; everything else (and unknown formats) the weight stream
     const bool tc8 = big && fmt == PQE_FMT_FP8, tc4 = big && fmt == PQE_FMT_MXFP4;
     const bool gemv = n > 0 && !tc8 && !tc4;
-    int total;
-    const int gpos = block_excl_scan(gemv ? 1 : 0, warp_tot, total);
+    // work weight of a weight-stream expert: its bytes (FP8 4, E2M1 2) plus 3 per
+    // further group of 8 tokens (each repeats the conversion and the mma);
+    // tiles of 128 batch rows: the FP8 experts' first, then the MXFP4 experts'
+    const int wgt = (fmt == PQE_FMT_FP8 ? 4 : 2) + 3 * ((n > 0 ? n - 1 : 0) / 8);
+    const int nt8 = tc8 ? (n + 127) / 128 : 0, nt4 = tc4 ? (n + 127) / 128 : 0;
+    int4 tot;
+    const int4 pre = block_excl_scan4(make_int4(gemv ? 1 : 0, gemv ? wgt : 0, nt8, nt4), scan_tot, tot);
+    const int gpos = pre.x, wpos = pre.y, tpos8 = pre.z, tpos4 = pre.w;
+    const int total = tot.x, wtot = tot.y, total8 = tot.z, total4 = tot.w;
     if (gemv) a.sched[1 + gpos] = e;
     if (threadIdx.x == 0) a.sched[0] = total;
-    // work weight of a weight-stream expert: its bytes (FP8 4, E2M1 2) plus 3 per
-    // further group of 8 tokens (each repeats the conversion and the mma)
-    int wtot;
-    const int wgt = (fmt == PQE_FMT_FP8 ? 4 : 2) + 3 * ((n > 0 ? n - 1 : 0) / 8);
-    const int wpos = block_excl_scan(gemv ? wgt : 0, warp_tot, wtot);
     if (gemv) a.wpre[gpos] = wpos;
     if (threadIdx.x == 0) a.wpre[total] = wtot;
-    // tiles of 128 batch rows: the FP8 experts' first, then the MXFP4 experts'
-    int total8, total4;
-    const int nt8 = tc8 ? (n + 127) / 128 : 0, nt4 = tc4 ? (n + 127) / 128 : 0;
-    const int tpos8 = block_excl_scan(nt8, warp_tot, total8);
-    const int tpos4 = block_excl_scan(nt4, warp_tot, total4);
     const int nt = nt8 + nt4, tpos = tc8 ? tpos8 : total8 + tpos4;
     for (int i = 0; i < nt; ++i) {
         int4 t;
@@ -569,8 +573,8 @@ int moe_paged_ffn_pass(const void *x_bf16, const int32_t *perm_src, const int32_
     const int max_active = (int)(A < E ? A : E);
     int32_t *tiles = reinterpret_cast<int32_t *>(wsb + w.tiles);
     int32_t *n_tiles = reinterpret_cast<int32_t *>(wsb + w.n_tiles);
-    const int sr = launch_pdl(ffn_schedule_kernel, 1, 1024, 0, s, args, w.tc ? TC_MIN_ROWS : 0, tiles, n_tiles, miss,
-                              groups, pass);
+    const int sr = launch_pdl(ffn_schedule_kernel, 1, (E + 31) / 32 * 32, 0, s, args, w.tc ? TC_MIN_ROWS : 0, tiles,
+                              n_tiles, miss, groups, pass);
     if (sr != PQE_OK) return sr;
     const bool stream_path = stream_shape_ok(pool->H, pool->I);
     int dev = 0, sms = 0;
