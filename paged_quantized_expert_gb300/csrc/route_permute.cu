@@ -261,6 +261,103 @@ __global__ void __launch_bounds__(PERM_THREADS) perm_scatter_kernel(const int32_
     }
 }
 
+// One chunk (A <= PERM_CHUNK): the count, scan and scatter above in one CTA,
+// with the same per-warp ranks, so the result is the same, and without the
+// chunk histogram in global memory.
+__global__ void __launch_bounds__(PERM_THREADS) perm_single_kernel(const int32_t *__restrict__ ids, int A, int E,
+                                                                    int32_t *__restrict__ counts,
+                                                                    int32_t *__restrict__ offsets,
+                                                                    int32_t *__restrict__ perm_src,
+                                                                    int32_t *__restrict__ inv,
+                                                                    int32_t *__restrict__ status) {
+    pdl_acquire();  // launched after the previous kernel of the step: wait for its output
+    extern __shared__ int32_t sh[];  // [PERM_WARPS][E] per-warp counts, then bases
+    __shared__ int32_t wsum[PERM_WARPS + 1];
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    int32_t *wc = sh + (size_t)w * E;
+    for (int i = tid; i < PERM_WARPS * E; i += PERM_THREADS) sh[i] = 0;
+    __syncthreads();
+    const int base = w * PERM_WARP_SPAN;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    bool bad = false;
+    // pass 1: per-warp counts
+    for (int r = 0; r < PERM_WARP_SPAN / 32; ++r) {
+        const int f = base + r * 32 + lane;
+        const int e = (f < A) ? __ldg(ids + f) : -1;
+        const bool ok = e >= 0 && e < E;
+        bad |= f < A && !ok;
+        const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : -1);
+        if (ok && (peers & lt_mask) == 0) wc[e] += __popc(peers);
+        __syncwarp();
+    }
+    if (bad) atomicOr(status, PQE_STATUS_BAD_EXPERT_ID);
+    __syncthreads();
+    // totals per expert, their exclusive prefix (thread t takes experts t*ept ..),
+    // and each warp's base per expert
+    const int ept = (E + PERM_THREADS - 1) / PERM_THREADS;
+    int tsum = 0;
+    for (int j = 0; j < ept; ++j) {
+        const int e = tid * ept + j;
+        if (e < E)
+            for (int q = 0; q < PERM_WARPS; ++q) tsum += sh[(size_t)q * E + e];
+    }
+    int incl = tsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) wsum[w] = incl;
+    __syncthreads();
+    if (tid == 0) {
+        int run = 0;
+        for (int q = 0; q < PERM_WARPS; ++q) {
+            const int c = wsum[q];
+            wsum[q] = run;
+            run += c;
+        }
+        wsum[PERM_WARPS] = run;
+    }
+    __syncthreads();
+    int run = wsum[w] + incl - tsum;
+    for (int j = 0; j < ept; ++j) {
+        const int e = tid * ept + j;
+        if (e < E) {
+            offsets[e] = run;
+            const int start = run;
+            for (int q = 0; q < PERM_WARPS; ++q) {
+                const int c = sh[(size_t)q * E + e];
+                sh[(size_t)q * E + e] = run;
+                run += c;
+            }
+            counts[e] = run - start;
+        }
+    }
+    const int valid = wsum[PERM_WARPS];
+    if (tid == 0) offsets[E] = valid;
+    __syncthreads();
+    // pass 2: positions
+    for (int r = 0; r < PERM_WARP_SPAN / 32; ++r) {
+        const int f = base + r * 32 + lane;
+        const int e = (f < A) ? __ldg(ids + f) : -1;
+        const bool ok = e >= 0 && e < E;
+        const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : -1);
+        if (f < A) {
+            if (ok) {
+                const int p = wc[e] + __popc(peers & lt_mask);
+                perm_src[p] = f;
+                inv[f] = p;
+            } else {
+                inv[f] = -1;
+            }
+        }
+        __syncwarp();
+        if (ok && (peers & lt_mask) == 0) wc[e] += __popc(peers);
+        __syncwarp();
+    }
+    for (int p = valid + tid; p < A; p += PERM_THREADS) perm_src[p] = -1;  // only when ids were dropped
+}
+
 // ===========================================================================
 // K8: combine. One CTA per token, each thread 8 columns (16 bytes).
 // ===========================================================================
@@ -427,15 +524,20 @@ int moe_permute(const int32_t *topk_ids, int T, int k, int E, int32_t *counts, i
     PQE_CHECK_ARG(topk_ids && perm_src && inv && ws);
     PQE_CHECK_ARG(ws_bytes >= moe_permute_workspace_size(T, k, E) && aligned(ws, 256));
     const int nchunk = (int)((A + PERM_CHUNK - 1) / PERM_CHUNK);
+    const size_t smem = sizeof(int32_t) * PERM_WARPS * E;
+    if (smem > 48 * 1024) {
+        PQE_CUDA_TRY(cudaFuncSetAttribute(perm_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        PQE_CUDA_TRY(cudaFuncSetAttribute(perm_single_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    }
+    if (nchunk == 1)  // one CTA covers the step: one kernel
+        return launch_pdl(perm_single_kernel, 1, PERM_THREADS, smem, s, topk_ids, (int)A, E, counts, offsets, perm_src,
+                          inv, status);
     int32_t *hist = static_cast<int32_t *>(ws);
     int rc = launch_pdl(perm_count_kernel, nchunk, PERM_THREADS, sizeof(int32_t) * E, s, topk_ids, (int)A, E, hist,
                         status);
     if (rc != PQE_OK) return rc;
     if ((rc = launch_pdl(perm_scan_kernel, 1, 1024, 0, s, hist, nchunk, E, (int)A, counts, offsets, perm_src)))
         return rc;
-    size_t smem = sizeof(int32_t) * PERM_WARPS * E;
-    if (smem > 48 * 1024) PQE_CUDA_TRY(cudaFuncSetAttribute(perm_scatter_kernel,
-                                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
     return launch_pdl(perm_scatter_kernel, nchunk, PERM_THREADS, smem, s, topk_ids, (int)A, E, hist, perm_src, inv);
 }
 
