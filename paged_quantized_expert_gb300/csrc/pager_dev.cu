@@ -124,6 +124,7 @@ __global__ void __launch_bounds__(1024) lru_step_kernel(void *state, int E, int 
     __shared__ int cand_of_rank[1024];
     __shared__ int s_expert[1024];     // slot -> expert at the start of the step
     __shared__ int64_t s_last[1024];   // slot -> last use at the start of the step
+    __shared__ uint8_t s_class[1024];  // slot -> 0 empty, 1 eviction candidate, 2 holds a needed expert
     LruView v = lru_view(state, E, S);
     const int t = threadIdx.x;
     const int64_t now = v.hdr->step;
@@ -161,13 +162,14 @@ __global__ void __launch_bounds__(1024) lru_step_kernel(void *state, int E, int 
             const int held = s_expert[t];
             lu = s_last[t];
             key_class = held < 0 ? 0 : (needed[held] ? 2 : 1);
+            s_class[t] = (uint8_t)key_class;
         }
+        __syncthreads();
         int rank = 0;
         if (key_class < 2) {
+#pragma unroll 4
             for (int s2 = 0; s2 < S; ++s2) {
-                const int held = s_expert[s2];
-                const int c2 = held < 0 ? 0 : (needed[held] ? 2 : 1);
-                if (c2 == 2) continue;
+                const int c2 = s_class[s2];
                 const int64_t l2 = s_last[s2];
                 const bool before = c2 < key_class || (c2 == key_class && (c2 == 0 ? s2 < t : (l2 < lu || (l2 == lu && s2 < t))));
                 rank += before ? 1 : 0;
