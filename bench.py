@@ -654,26 +654,57 @@ def run_large(pqe, torch, device, steps_t1=64, steps_big=3, n_src=32):
     sizes = [sizes_src[e % n_src] for e in range(E)]
     luts = luts_src[torch.arange(E) % n_src].contiguous().to(device)
     big_T = cfg.T[-1]
-    layer = pqe.PagedMoELayer(E, H, I, k, S, E, big_T, host, sizes, compressed=True, luts=luts, device=device)
     stream = torch.cuda.current_stream(device)
     side = torch.cuda.Stream(device)
     out = {"workload": "large paged layer, compressed host tier (E=512, H=2560, I=640, top-8, CACHE_SLOTS=46, "
                        "Huffman-coded FP8 exponents decoded on the GPU after each refill)",
-           "mean_compressed_ratio": float(np.mean(sizes_src)) / nb}
+           "mean_compressed_ratio": float(np.mean(sizes_src)) / nb,
+           "pager": "device (LRU on the GPU; compressed misses pulled and decoded by a kernel reading the "
+                    "step's miss list), eager steps"}
     peak_bw = peaks()[0]
     for T, steps in ((1, steps_t1), (big_T, steps_big)):
+        # no refill groups: the decode of compressed pages needs the SMs the FFN
+        # passes would take (T=4096: 10.38 ms per step plain, 10.77 with 5 groups)
+        groups = OVERLAP_GROUPS if OVERLAP_GROUPS is not None else 0
+        layer = pqe.PagedMoELayer(E, H, I, k, S, E, big_T, host, sizes, compressed=True, luts=luts, device=device,
+                                  device_pager=True, overlap_groups=groups)
         tr = synth.RoutingTrace(cfg, T)
-        n_tr = min(steps + 4, 32)
-        logits = [torch.from_numpy(tr.step(s)).to(device) for s in range(n_tr)]
+        n_tr = min(2 * steps + 4, 64)
+        logits_np = [tr.step(s) for s in range(n_tr)]
+        logits = [torch.from_numpy(l).to(device) for l in logits_np]
         xs = [torch.from_numpy(synth.activations(cfg, T, s % 2).view(np.int16)).to(device) for s in range(2)]
         y = torch.zeros((T, H), dtype=torch.bfloat16, device=device)
+        if T > 1:  # the slots first fill with the experts of small steps, as in a serving run
+            tr1 = synth.RoutingTrace(cfg, 1)
+            x1 = torch.from_numpy(synth.activations(cfg, 1, 0).view(np.int16)).to(device)
+            y1 = torch.zeros((1, H), dtype=torch.bfloat16, device=device)
+            for i in range(24):
+                layer.step(x1, y1, 1, logits=torch.from_numpy(tr1.step(i)).to(device), stream=stream,
+                           side_stream=side)
         for i in range(2):  # warm-up
             layer.step(xs[i % 2], y, T, logits=logits[i % n_tr], stream=stream, side_stream=side)
-        ms, ffn, infos = _timed_steps(torch, layer, xs, y, T, logits, steps, stream, side)
+        torch.cuda.synchronize()
+        st0 = layer.device_stats()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(steps):
+            layer.step(xs[i % 2], y, T, logits=logits[(2 + i) % n_tr], stream=stream, side_stream=side)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        st1 = layer.device_stats()
+        # the FFN call's time: the next steps again with its timing events (one FFN pass per step)
+        ffn_logits = [logits[(2 + steps + i) % n_tr] for i in range(steps)]
+        _, ffn, _ = _timed_steps(torch, layer, xs, y, T, ffn_logits, steps, stream, side)
         ffn_ms = float(np.mean(ffn))
-        routed = float(np.mean([r for r, _, _ in infos]))
+        routed = float(np.mean([routed_experts(logits_np[(2 + steps + i) % n_tr], k) for i in range(steps)]))
+        layer.close()
         rec = {"tokens_per_s": T * steps / (ms / 1e3), "ms_per_step": ms / steps, "steps": steps,
-               "mean_routed_experts": routed, "mean_misses": float(np.mean([m for _, m, _ in infos])),
+               "overlap_groups": groups,
+               "mean_routed_experts": (st1["routed"] - st0["routed"]) / steps,
+               "mean_misses": (st1["misses"] - st0["misses"]) / steps,
+               "h2d_gb_per_s": (st1["refill_bytes"] - st0["refill_bytes"]) / (ms / 1e3) / 1e9,
                "ffn_ms": ffn_ms}
         # both bounds: the routed pages (plus x and out_perm) against HBM, the FLOPs against
         # the FP8 peak; at T=4096 a batch is ~64 rows per expert, below the FP8 ridge (~290)
@@ -684,7 +715,6 @@ def run_large(pqe, torch, device, steps_t1=64, steps_big=3, n_src=32):
                     "ffn_frac_of_fp8_peak": tflops / pk, "fp8_peak_kind": kind,
                     "bound": "hbm" if T * k / max(routed, 1.0) < 290 else "tensor"})
         out["T=%d" % T] = rec
-    layer.close()
     out["huff_decode"] = huff_decode_rate(pqe, torch, device, comp, sizes_src, luts_src, H, I, nb)
     return out
 

@@ -601,7 +601,8 @@ typedef struct pqe_layer_config {
     int32_t max_T;      /* largest token count of a step */
     int32_t compressed; /* host pages are compressed pages (decoded after the copy) */
     int32_t device_pager; /* 1: LRU state and refills on the GPU, no host synchronisation in a step
-                             (uncompressed host pages only) */
+                             (compressed host pages are pulled and decoded by a kernel that reads the
+                             step's miss list on the device) */
     int32_t overlap_groups; /* device pager with a side stream given to the step: 0 refills every miss,
                                then runs the FFN once; G >= 1 (at most PQE_MAX_OVERLAP_GROUPS) refills
                                the misses in G groups on the side stream (a refill kernel on 32 CTAs)

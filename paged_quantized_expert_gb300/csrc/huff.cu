@@ -390,8 +390,18 @@ __host__ __device__ __forceinline__ bool decode_chunk(const uint32_t *__restrict
     return !(bad & 0x800u) && a.pos <= end;
 }
 
-__global__ void __launch_bounds__(HD_THREADS, 1024 / HD_THREADS) huff_decode_batch_kernel(const __grid_constant__ HuffBatch b,
-                                                                          int32_t *__restrict__ status) {
+// geometry of a page's decode blocks (the same for every page of a layer)
+struct HuffGeo {
+    int H, I;
+    int rows13_unit, rows2_unit;  // rows per block
+    int units13, units2;          // blocks per matrix
+};
+
+// One decode block: block u of one page (u < units13: w13 rows, else w2 rows),
+// the compressed page at `comp`, its code tables, the FP8 page out. Every
+// thread of the CTA calls it for the same block.
+__device__ void decode_block(const HuffGeo &b, const uint8_t *comp, uint64_t cbytes, const uint32_t *lut13g,
+                             const uint32_t *lut2g, uint8_t *page_out, int u, int32_t *__restrict__ status) {
     extern __shared__ __align__(16) uint8_t hd_smem[];
     uint32_t *lut = reinterpret_cast<uint32_t *>(hd_smem);
     uint32_t *span = lut + HD_LUT_WORDS;
@@ -401,10 +411,6 @@ __global__ void __launch_bounds__(HD_THREADS, 1024 / HD_THREADS) huff_decode_bat
     int *flag = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(hdr) + HUF_HEADER);
 
     const int tid = threadIdx.x;
-    const int upp = b.units13 + b.units2;
-    const int page = blockIdx.x / upp, u = blockIdx.x % upp;
-    const uint8_t *comp = b.comp[page];
-    const uint64_t cbytes = b.comp_bytes[page];
     const int H = b.H, I = b.I;
 
     if (tid < (int)(HUF_HEADER / 16) && cbytes >= HUF_HEADER)
@@ -426,7 +432,7 @@ __global__ void __launch_bounds__(HD_THREADS, 1024 / HD_THREADS) huff_decode_bat
     const PageLayout L = fp8_layout(H, I);
 
     // 1. code table, row offsets, chunk offsets, raw nibbles (registers), scales
-    const uint4 *lut_g = reinterpret_cast<const uint4 *>(first ? b.lut13[page] : b.lut2[page]);
+    const uint4 *lut_g = reinterpret_cast<const uint4 *>(first ? lut13g : lut2g);
     for (int i = tid; i < HD_LUT_WORDS / 4; i += HD_THREADS) reinterpret_cast<uint4 *>(lut)[i] = lut_g[i];
     const uint32_t *rw_g = reinterpret_cast<const uint32_t *>(comp + d.off_row_word) + r0;
     for (int i = tid; i <= nr; i += HD_THREADS) rw[i] = rw_g[i];
@@ -442,7 +448,7 @@ __global__ void __launch_bounds__(HD_THREADS, 1024 / HD_THREADS) huff_decode_bat
     }
     if (u == 0) {
         const uint4 *sc = reinterpret_cast<const uint4 *>(comp + hdr->off_scales);
-        uint4 *so = reinterpret_cast<uint4 *>(b.out[page] + L.s13);
+        uint4 *so = reinterpret_cast<uint4 *>(page_out + L.s13);
         for (int i = tid; i < (2 * I + H) / 4; i += HD_THREADS) so[i] = sc[i];
     }
     __syncthreads();
@@ -498,7 +504,7 @@ __global__ void __launch_bounds__(HD_THREADS, 1024 / HD_THREADS) huff_decode_bat
     if (!ok) atomicOr(status, PQE_STATUS_CORRUPT_STREAM);
 
     // 3. exponent plane + raw nibbles -> FP8 bytes, 32 per thread and slice
-    uint4 *dst = reinterpret_cast<uint4 *>(b.out[page] + (first ? L.w13 : L.w2) + (size_t)r0 * cols);
+    uint4 *dst = reinterpret_cast<uint4 *>(page_out + (first ? L.w13 : L.w2) + (size_t)r0 * cols);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int q = tid + HD_THREADS * i;  // 32 symbols: chunk q / 2, half q % 2
@@ -511,22 +517,83 @@ __global__ void __launch_bounds__(HD_THREADS, 1024 / HD_THREADS) huff_decode_bat
     }
 }
 
+__global__ void __launch_bounds__(HD_THREADS, 1024 / HD_THREADS) huff_decode_batch_kernel(const __grid_constant__ HuffBatch b,
+                                                                          int32_t *__restrict__ status) {
+    const int upp = b.units13 + b.units2;
+    const int page = blockIdx.x / upp, u = blockIdx.x % upp;
+    const HuffGeo g{b.H, b.I, b.rows13_unit, b.rows2_unit, b.units13, b.units2};
+    decode_block(g, b.comp[page], b.comp_bytes[page], b.lut13[page], b.lut2[page], b.out[page], u, status);
+}
+
+// The misses of a device miss list (layout of the GPU-resident pager: [0] n,
+// [2 .. 2+E) expert, [2+E .. 2+2E) destination entry), those of refill group
+// `group` of `groups`, pulled from their compressed host pages and decoded
+// into their slots: the grid strides over (miss, block) items. Code tables:
+// expert e's at luts + e * 2 * PQE_HUFF_LUT_BYTES (w13, then w2).
+__global__ void __launch_bounds__(HD_THREADS, 1024 / HD_THREADS)
+    huff_decode_device_kernel(const HuffGeo g, const int32_t *__restrict__ miss, int E,
+                              const uint64_t *__restrict__ comp_pages, const size_t *__restrict__ comp_bytes,
+                              const uint8_t *__restrict__ luts, uint8_t *__restrict__ base, uint8_t *__restrict__ wb_base,
+                              int n_slots, size_t slot_stride, int group, int groups, int32_t *__restrict__ status) {
+    pdl_acquire();  // launched after the previous kernel of the step: wait for its output
+    const int n_all = miss[0];
+    const int m0 = overlap_group_start(group, groups, n_all), m1 = overlap_group_start(group + 1, groups, n_all);
+    const int upp = g.units13 + g.units2;
+    const long items = (long)(m1 - m0) * upp;
+    for (long it = blockIdx.x; it < items; it += gridDim.x) {
+        const int i = m0 + (int)(it / upp), u = (int)(it % upp);
+        const int e = miss[2 + i], d = miss[2 + E + i];
+        uint8_t *out = d < n_slots ? base + (size_t)d * slot_stride : wb_base + (size_t)(d - n_slots) * slot_stride;
+        const uint32_t *l13 = reinterpret_cast<const uint32_t *>(luts + (size_t)e * 2 * PQE_HUFF_LUT_BYTES);
+        decode_block(g, reinterpret_cast<const uint8_t *>(comp_pages[e]), comp_bytes[e], l13,
+                     l13 + PQE_HUFF_LUT_BYTES / 4, out, u, status);
+        __syncthreads();  // the block's shared memory is reused by the next item
+    }
+}
+
+// the geometry of the decode blocks of an H x I page
+static HuffGeo huff_geo(int H, int I) {
+    const int nc13 = H / HUF_CHUNK, nc2 = I / HUF_CHUNK;
+    const int R13 = HD_UNIT_CHUNKS / nc13, R2 = HD_UNIT_CHUNKS / nc2;
+    return HuffGeo{H, I, R13, R2, (2 * I + R13 - 1) / R13, (H + R2 - 1) / R2};
+}
+
+static int decode_attr(int dev) {
+    static std::atomic<int> attr_set[PQE_MAX_DEVICES];
+    if (!attr_set[dev].load(std::memory_order_relaxed)) {
+        PQE_CUDA_TRY(cudaFuncSetAttribute(huff_decode_batch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)HD_SMEM));
+        PQE_CUDA_TRY(cudaFuncSetAttribute(huff_decode_device_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)HD_SMEM));
+        attr_set[dev].store(1, std::memory_order_relaxed);
+    }
+    return PQE_OK;
+}
+
+int slot_fill_compressed_device_group(const pqe_pool *pool, const int32_t *miss, int E, const uint64_t *comp_pages,
+                                      const size_t *comp_bytes, const uint8_t *luts, int group, int groups, int ctas,
+                                      int32_t *status, cudaStream_t s) {
+    if (!pool || !miss || !comp_pages || !comp_bytes || !luts || !status || E < 1 || E > 1024 || groups < 1 ||
+        group < 0 || group >= groups || !shape_ok(pool->H, pool->I))
+        return PQE_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    int rc = device_info(dev, sms);
+    if (rc != PQE_OK || (rc = decode_attr(dev)) != PQE_OK) return rc;
+    // the grid strides over the items; by default it fills the GPU (4 decode CTAs per SM)
+    return launch_pdl(huff_decode_device_kernel, ctas > 0 ? ctas : 4 * sms, HD_THREADS, HD_SMEM, s, huff_geo(pool->H, pool->I), miss,
+                      E, comp_pages, comp_bytes, luts, static_cast<uint8_t *>(pool->base),
+                      static_cast<uint8_t *>(pool->wb_base), pool->n_slots, pool->slot_stride, group, groups, status);
+}
+
 // launch over n pages (n <= HD_MAX_PAGES per launch)
 int launch_decode_batch(int n, const void *const *comp, const size_t *comp_bytes, const uint8_t *const *lut13,
                         const uint8_t *const *lut2, int H, int I, uint8_t *const *out, int32_t *status,
                         cudaStream_t s) {
-    static std::atomic<int> attr_set[PQE_MAX_DEVICES];
     int dev = 0, sms = 0;
-    const int di = device_info(dev, sms);
-    if (di != PQE_OK) return di;
-    if (!attr_set[dev].load(std::memory_order_relaxed)) {
-        PQE_CUDA_TRY(cudaFuncSetAttribute(huff_decode_batch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)HD_SMEM));
-        attr_set[dev].store(1, std::memory_order_relaxed);
-    }
-    const int nc13 = H / HUF_CHUNK, nc2 = I / HUF_CHUNK;
-    const int R13 = HD_UNIT_CHUNKS / nc13, R2 = HD_UNIT_CHUNKS / nc2;
-    const int u13 = (2 * I + R13 - 1) / R13, u2 = (H + R2 - 1) / R2;
+    int di = device_info(dev, sms);
+    if (di != PQE_OK || (di = decode_attr(dev)) != PQE_OK) return di;
+    const HuffGeo hg = huff_geo(H, I);
+    const int R13 = hg.rows13_unit, R2 = hg.rows2_unit, u13 = hg.units13, u2 = hg.units2;
     for (int i0 = 0; i0 < n; i0 += HD_MAX_PAGES) {
         HuffBatch b{};
         b.n = n - i0 < HD_MAX_PAGES ? n - i0 : HD_MAX_PAGES;

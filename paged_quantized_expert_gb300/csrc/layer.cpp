@@ -85,8 +85,8 @@ bool config_ok(const pqe_layer_config *c) {
     if (!c || c->E < 1 || c->E > 1024 || c->k < 1 || c->k > 32 || c->k > c->E || c->S < 0 || c->W < 0 ||
         c->max_T < 1 || (size_t)c->max_T * c->k >= (1u << 30) || pqe_page_bytes(PQE_FMT_FP8, c->H, c->I) == 0)
         return false;
-    // the device pager: uncompressed pages, at most 1024 slots, a working buffer for any step
-    if (c->device_pager && (c->compressed || c->S > 1024 || c->W < c->E)) return false;
+    // the device pager: at most 1024 slots, a working buffer for any step
+    if (c->device_pager && (c->S > 1024 || c->W < c->E)) return false;
     if (c->overlap_groups < 0 || c->overlap_groups > PQE_MAX_OVERLAP_GROUPS ||
         (c->overlap_groups > 0 && !c->device_pager))
         return false;
@@ -377,11 +377,21 @@ int pqe_layer_step(pqe_layer *L, const void *x_dev, const float *w_router_dev, f
             // SMs; the FFN in passes on s: the resident experts first, beside the
             // refills, then each group's experts once its pages have landed
             const uint64_t *hp = L->at<uint64_t>(m.host_pages);
+            int dev = 0, sms = 0;
+            if ((rc = pqe::device_info(dev, sms))) return rc;
+            // SMs left to the refills beside the FFN passes: plain pages need 32 CTAs
+            // at the host link's rate, compressed ones are decoded by 4 CTAs on each
+            // SM the passes leave
+            const int reserve = std::max(OVERLAP_FILL_CTAS, sms - OVERLAP_FFN_SMS);
             cudaError_t ce = cudaEventRecord(L->ev_lru, s);
             if (ce == cudaSuccess) ce = cudaStreamWaitEvent(side, L->ev_lru, 0);
             for (int g = 0; g < G && ce == cudaSuccess; ++g) {
-                if ((rc = pqe::slot_fill_device_group(&L->pool, miss, c.E, hp, pbytes, g, G, OVERLAP_FILL_CTAS,
-                                                      side)))
+                // compressed pages: pulled and decoded by 4 decode CTAs on each SM left to the refill
+                if ((rc = c.compressed ? pqe::slot_fill_compressed_device_group(&L->pool, miss, c.E, hp, pbytes,
+                                                                                L->luts, g, G, 4 * reserve, status,
+                                                                                side)
+                                       : pqe::slot_fill_device_group(&L->pool, miss, c.E, hp, pbytes, g, G,
+                                                                     OVERLAP_FILL_CTAS, side)))
                     return rc;
                 ce = cudaEventRecord(L->ev_group[g], side);
             }
@@ -390,9 +400,6 @@ int pqe_layer_step(pqe_layer *L, const void *x_dev, const float *w_router_dev, f
                 return PQE_ERR_CUDA;
             }
             void *ws = L->at<void>(m.ffn_ws);
-            int dev = 0, sms = 0;
-            if ((rc = pqe::device_info(dev, sms))) return rc;
-            const int reserve = std::max(OVERLAP_FILL_CTAS, sms - OVERLAP_FFN_SMS);
             for (int p = 0; p <= G; ++p) {
                 if (p > 0 && (ce = cudaStreamWaitEvent(s, L->ev_group[p - 1], 0)) != cudaSuccess) {
                     pqe::set_last_cuda_error(ce);
@@ -408,7 +415,9 @@ int pqe_layer_step(pqe_layer *L, const void *x_dev, const float *w_router_dev, f
             if (info) *info = local;
             return PQE_OK;
         }
-        rc = slot_fill_device(&L->pool, miss, c.E, L->at<uint64_t>(m.host_pages), pbytes, stream);
+        rc = c.compressed ? pqe::slot_fill_compressed_device_group(&L->pool, miss, c.E, L->at<uint64_t>(m.host_pages),
+                                                                   pbytes, L->luts, 0, 1, 0, status, s)
+                          : slot_fill_device(&L->pool, miss, c.E, L->at<uint64_t>(m.host_pages), pbytes, stream);
         if (rc) return rc;
         if (L->ev_ffn_begin && (rc = (record_timing(L->ev_ffn_begin, s) == cudaSuccess ? 0 : PQE_ERR_CUDA))) return rc;
         rc = moe_paged_ffn(x_dev, perm_src, offsets, page_table, L->expert_fmt, &L->pool, T, c.k, c.E, out_perm,

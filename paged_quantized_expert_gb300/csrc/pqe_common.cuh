@@ -66,6 +66,14 @@ __host__ __device__ inline int overlap_group_start(int g, int G, int n) {
 int slot_fill_device_group(const pqe_pool *pool, const int32_t *miss, int E, const uint64_t *host_pages,
                            const size_t *page_bytes, int group, int groups, int ctas, cudaStream_t s);
 
+// compressed refill of group `group` of `groups` of a device miss list: each
+// miss's compressed host page (comp_pages[e], comp_bytes[e], device arrays) is
+// pulled and decoded into its slot; code tables at luts + e * 2 * LUT bytes;
+// `ctas` decode CTAs (0: four per SM)
+int slot_fill_compressed_device_group(const pqe_pool *pool, const int32_t *miss, int E, const uint64_t *comp_pages,
+                                      const size_t *comp_bytes, const uint8_t *luts, int group, int groups, int ctas,
+                                      int32_t *status, cudaStream_t s);
+
 // moe_paged_ffn restricted to one pass of an overlapped step (miss non-null):
 // pass 0 takes the experts that were resident (not in the miss list), pass
 // g + 1 the misses of refill group g of `groups`; `reserve_sms` SMs are left to

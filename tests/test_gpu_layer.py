@@ -154,11 +154,15 @@ def test_layer_step_host_buffers(cuda_lib, orc):
     _run_trace(cuda_lib, orc, cfg, T=20, steps=12, S=5, W=12, check_every=4, n_check=20, host_api=True)
 
 
-@pytest.mark.parametrize("ram", [False, True])
-def test_layer_compressed_host_tier(cuda_lib, orc, tmp_path, ram):
-    """Compressed pages pulled and decoded into the slots; with `ram`, they
+@pytest.mark.parametrize("mode", ["host", "ram", "device", "device_overlap"])
+def test_layer_compressed_host_tier(cuda_lib, orc, tmp_path, mode):
+    """Compressed pages pulled and decoded into the slots; with "ram", they
     come from a paging file through a RAM tier of 4 slots (compressed pages in
-    RAM and in the file, as the article's compressed configurations hold)."""
+    RAM and in the file, as the article's compressed configurations hold);
+    with "device", the LRU runs on the GPU and a decode kernel reads the step's
+    miss list there (in two overlapped refill groups with "device_overlap")."""
+    ram = mode == "ram"
+    device = mode.startswith("device")
     pqe = cuda_lib
     cfg = synth.small_config(E=10, H=256, I=128, k=2, T=6, S=3, cid=95, reuse_p=0.5, zipf_s=1.1,
                              router_gemm=False, steps=10)
@@ -174,7 +178,8 @@ def test_layer_compressed_host_tier(cuda_lib, orc, tmp_path, ram):
         sizes.append(n)
     host = comp.pin_memory()
     layer = pqe.PagedMoELayer(cfg.E, cfg.H, cfg.I, cfg.k, cfg.S, cfg.E, cfg.T[0], host, sizes, compressed=True,
-                              luts=luts.to(DEV), expert_fmt=pages.fmt_dev)
+                              luts=luts.to(DEV), expert_fmt=pages.fmt_dev, device_pager=device,
+                              overlap_groups=2 if mode == "device_overlap" else 0)
     tier = None
     if ram:
         tier = _ram_tier(pqe, host, sizes, 4, cfg.E, str(tmp_path / "comp.pqe"), n_threads=2)
@@ -193,10 +198,16 @@ def test_layer_compressed_host_tier(cuda_lib, orc, tmp_path, ram):
         ids, g = orc.topk_gates(logits, cfg.k)
         ref_lru.step(np.bincount(ids.reshape(-1), minlength=cfg.E).astype(np.int32))
         torch.cuda.synchronize()
+        if device:  # the GPU-resident LRU against the oracle's, every step
+            se_, lu_, st_ = layer.lru_state()
+            se2, lu2, st2 = ref_lru.state()
+            assert np.array_equal(se_.numpy(), se2) and np.array_equal(lu_.numpy(), lu2) and st_ == st2, s
         ref = orc.moe_ffn(x_np, ids, g, pages.experts, cfg.I)
         st = helpers.error_stats(helpers.bf16_to_f64(y), ref)
         bound = helpers.l2_bounds(ids, np.arange(6), cfg.E, (), cfg.H, cfg.I)
         assert st["max_over_l2"] <= helpers.TOL_MAX_OVER_L2 and np.all(st["l2_per_token"] <= bound), (s, st)
+    if device:
+        total_miss = int(layer.device_stats()["misses"])
     assert total_miss > 0
     assert layer.device_view("status", torch.int32, (1,)).item() == 0
     # the resident slots hold the decoded FP8 pages byte for byte
