@@ -77,6 +77,26 @@ def peaks():
 _FP8_PEAK = {}
 
 
+def measure_h2d_peak(torch, device, nbytes=1 << 30, reps=5):
+    """The host link's ceiling for refills: one pinned-host-to-device copy of
+    1 GiB, best of `reps` (GB/s)."""
+    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    dst.copy_(src, non_blocking=True)
+    torch.cuda.synchronize()
+    best = 0.0
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        best = max(best, nbytes / (a.elapsed_time(b) / 1e3) / 1e9)
+    del src, dst
+    return best
+
+
 def measure_fp8_peak(torch, device, n=8192, reps=10):
     """Dense e4m3 x e4m3 -> bf16 GEMM through cuBLASLt (torch._scaled_mm),
     n x n x n, burst: the best of `reps` timed calls after warm-up, with fast
@@ -1155,6 +1175,8 @@ def main():
     n_routed = [n for (n, _, _, _) in infos]
     misses = [m for (_, m, _, _) in infos]
     h2d = [b for (_, _, _, b) in infos]
+    h2d_step = graph["h2d_gb_per_s"] if pager_used == "device" else sum(h2d) / (ms / 1e3) / 1e9
+    h2d_peak = measure_h2d_peak(torch, device)
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": W,
@@ -1185,6 +1207,13 @@ def main():
                     "api": "pqe_layer_step_host (pinned host x and logits in, pinned host y out, every step)"},
             "gpu_launches": int(launches),
             "fp8_peak": dict(_FP8_PEAK),
+            # the step's refills against the host link: bytes refilled per second of
+            # whole steps, against a plain pinned-host-to-device copy in this run
+            "host_link": {"achieved": h2d_step, "peak": h2d_peak, "unit": "GB/s",
+                          "frac": h2d_step / h2d_peak if h2d_peak else None,
+                          "peak_kind": "measured: one 1 GiB pinned-host-to-device copy (best of 5), this run",
+                          "note": "refill bytes of the timed steps / their whole time: the step is bound by "
+                                  "this link, the FFN running beside the refills"},
             "clocks": clk,
             "batched": batched,
             "large": large,
