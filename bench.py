@@ -280,13 +280,19 @@ class GraphRunner:
     are already in place); a graph is launched once, so its first-launch cost
     is shared by the steps it holds."""
 
-    def __init__(self, pqe, torch, device, host, L, T, overlap_groups=0):
+    def __init__(self, pqe, torch, device, host, L, T, overlap_groups=0, comp=None):
         E, H, I, k, S = CFG.E, CFG.H, CFG.I, CFG.k, CFG.S
         self.pqe, self.torch, self.T = pqe, torch, T
         self.wb = pqe.alloc_working_buffer(E, H, I, device)
         nbytes = [pqe.page_bytes(pqe.PQE_FMT_FP8, H, I)] * E
-        self.layers = [pqe.PagedMoELayer(E, H, I, k, S, E, T, host, nbytes, working_buffer=self.wb, device=device,
-                                         device_pager=True, overlap_groups=overlap_groups) for _ in range(L)]
+        if comp is None:
+            self.layers = [pqe.PagedMoELayer(E, H, I, k, S, E, T, host, nbytes, working_buffer=self.wb, device=device,
+                                             device_pager=True, overlap_groups=overlap_groups) for _ in range(L)]
+        else:  # a compressed host tier: (pinned pages, their sizes, code tables on the device)
+            pages, sizes, luts = comp
+            self.layers = [pqe.PagedMoELayer(E, H, I, k, S, E, T, pages, sizes, compressed=True, luts=luts,
+                                             working_buffer=self.wb, device=device, device_pager=True,
+                                             overlap_groups=overlap_groups) for _ in range(L)]
         self.stream = torch.cuda.Stream(device)
         # the refills of an overlapped step run on this stream, forked and joined inside each step
         self.side = torch.cuda.Stream(device)
@@ -342,13 +348,14 @@ def overlap_groups_for(T):
 OVERLAP_GROUPS = None  # --overlap-groups
 
 
-def run_graph(pqe, torch, device, host, T, L, logits_dev, xs_dev, warmup, K, ws, ffn_events=False):
+def run_graph(pqe, torch, device, host, T, L, logits_dev, xs_dev, warmup, K, ws, ffn_events=False, comp=None,
+              groups=None):
     """Device-pager graph replays of steps L .. L + warmup + K - 1 (layer i % L).
     With ffn_events each layer's FFN is bracketed by event nodes in its graphs
     (after the timed loop they hold the FFN time of that layer's last replay).
     The two nodes add ~11 us to a replayed step, so the headline steps are
     timed without them and the FFN in a second pass."""
-    gr = GraphRunner(pqe, torch, device, host, L, T, overlap_groups_for(T))
+    gr = GraphRunner(pqe, torch, device, host, L, T, overlap_groups_for(T) if groups is None else groups, comp)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
     if ffn_events:
         for (a, b), layer in zip(evs, gr.layers):
@@ -649,6 +656,22 @@ def large_compressed_pages(pqe, torch, device, n_src):
         sizes_src.append(pqe.pqe_huff_encode_page(page[:nb].cpu().contiguous(), H, I, comp[j], luts_src[j, :LB],
                                                   luts_src[j, LB:]))
     return comp.pin_memory(), sizes_src, luts_src
+
+
+def decode_compressed_pages(pqe, torch, host, n_src=32):
+    """The decode-shaped layer's host tier as Huffman-coded pages: n_src distinct
+    experts encoded (expert e uses page e % n_src), pinned, with code tables."""
+    E, H, I = CFG.E, CFG.H, CFG.I
+    LB = pqe.PQE_HUFF_LUT_BYTES
+    nb = pqe.page_bytes(pqe.PQE_FMT_FP8, H, I)
+    bound = pqe.pqe_huff_page_bound(H, I)
+    comp = torch.zeros((n_src, bound), dtype=torch.uint8)
+    luts_src = torch.zeros((n_src, 2 * LB), dtype=torch.uint8)
+    sizes_src = [pqe.pqe_huff_encode_page(host[j, :nb].contiguous(), H, I, comp[j], luts_src[j, :LB],
+                                          luts_src[j, LB:]) for j in range(n_src)]
+    comp = comp.pin_memory()
+    return ([comp[e % n_src] for e in range(E)], [sizes_src[e % n_src] for e in range(E)],
+            luts_src[torch.arange(E) % n_src].contiguous(), float(np.mean(sizes_src)) / nb)
 
 
 def run_huff(pqe, torch, device, n_src=32):
@@ -1155,6 +1178,23 @@ def main():
                 r = Runner(pqe, torch, device, host, L, max(T, 64))
             sweep[f"T={Ts}"] = rec
 
+    # the same decode steps with a compressed host tier (device pager, graph replays):
+    # the link-bound step moves fewer bytes per refill
+    decode_compressed = None
+    if not args.no_extra and pager_used == "device":
+        r.close()
+        pages_c, sizes_c, luts_c, ratio = decode_compressed_pages(pqe, torch, host)
+        cms, cst, _ = run_graph(pqe, torch, device, host, T, L, logits_dev, xs_dev, W, K, ws,
+                                comp=(pages_c, sizes_c, luts_c.to(device)), groups=0)
+        cms = max_over_ranks(ws, cms, device)
+        decode_compressed = {"tokens_per_s": ws * T * K / (cms / 1e3), "ms_per_step": cms / K,
+                             "compressed_over_fp8_bytes": ratio, "mean_misses": cst["misses"] / K,
+                             "h2d_gb_per_s": cst["refill_bytes"] / (cms / 1e3) / 1e9,
+                             "note": "the same workload and routing as the headline with Huffman-coded FP8 "
+                                     "exponents in the host tier (32 distinct encoded pages), each miss pulled "
+                                     "and decoded in one pass; no refill groups"}
+        r = Runner(pqe, torch, device, host, L, max(T, 64))
+
     batched = None
     if not args.no_batched:
         r.close()
@@ -1215,6 +1255,7 @@ def main():
                           "note": "refill bytes of the timed steps / their whole time: the step is bound by "
                                   "this link, the FFN running beside the refills"},
             "clocks": clk,
+            "decode_compressed": decode_compressed,
             "batched": batched,
             "large": large,
             "mixed": mixed,
