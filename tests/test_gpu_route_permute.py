@@ -201,7 +201,10 @@ def test_permute_bit_exact_on_traces(cuda_lib, orc, wl, T):
     assert got[4] == 0
 
 
-@pytest.mark.parametrize("T,k,E", [(2049, 1, 3), (5000, 3, 1024), (257, 32, 1000), (3, 2, 2)])
+# one chunk (a single kernel) up to 2048 assignments: the boundary, E = 1024 (four
+# experts per thread in its scan), one token; then several chunks
+@pytest.mark.parametrize("T,k,E", [(256, 8, 256), (64, 32, 1024), (1, 1, 1024), (2048, 1, 7),
+                                   (2049, 1, 3), (5000, 3, 1024), (257, 32, 1000), (3, 2, 2)])
 def test_permute_bit_exact_random(cuda_lib, orc, T, k, E):
     pqe = cuda_lib
     g = np.random.default_rng(T + E)
@@ -211,11 +214,12 @@ def test_permute_bit_exact_random(cuda_lib, orc, T, k, E):
         assert np.array_equal(a, b)
 
 
-def test_permute_bad_ids_flagged(cuda_lib, orc):
+@pytest.mark.parametrize("E,T", [(16, 300), (1024, 300), (16, 700)])
+def test_permute_bad_ids_flagged(cuda_lib, orc, E, T):
+    # one chunk (T*4 <= 2048) and several (T = 700)
     pqe = cuda_lib
-    E = 16
     g = np.random.default_rng(9)
-    ids = g.integers(0, E, (300, 4)).astype(np.int32)
+    ids = g.integers(0, E, (T, 4)).astype(np.int32)
     ids[5, 1] = -1
     ids[77, 3] = E
     counts, offsets, perm_src, inv, status = _permute(pqe, ids, E)
