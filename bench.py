@@ -62,6 +62,9 @@ def parse_args():
     ap.add_argument("--pager", default="both", choices=["host", "device", "both"],
                     help="host: LRU on the host (one read-back per step); device: LRU on the GPU, each layer's step "
                          "replayed from a CUDA graph; both: measure both, the faster is the headline")
+    ap.add_argument("--stream-kernel", default="auto", choices=["auto", "cuda", "tc"],
+                    help="weight-stream kernel for batches of at most 8 rows: auto (the library's choice), cuda "
+                         "(mma.sync on CUDA cores) or tc (tcgen05 on the tensor cores, all-FP8 layers); for A/B runs")
     return ap.parse_args()
 
 
@@ -1044,6 +1047,7 @@ def main():
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     pqe.load()
+    pqe.pqe_test_set_stream_kernel({"auto": 0, "cuda": 1, "tc": 2}[args.stream_kernel])
     T, L, K, W = args.T, args.layers, args.steps, max(3, args.warmup)
     if args.workload not in ("huff", "ram"):
         measure_fp8_peak(torch, device)

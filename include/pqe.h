@@ -106,6 +106,17 @@ PQE_API int pqe_set_wait_limit(uint32_t polls);
  * read at each launch; 0 (the default) in normal use. */
 PQE_API int pqe_test_set_phase2_bias(uint32_t bias);
 
+/* Test hook: which weight-stream kernel moe_paged_ffn runs for batches of at
+ * most 8 rows. 0 (the default): the tensor-core stream (tcgen05 MMAs on the
+ * page's E4M3 codes, activations as two E4M3 terms) when expert_fmt is NULL
+ * (every page FP8), the shape allows it and the step routes enough experts,
+ * else the CUDA-core stream (mma.sync on f16-converted weights); 1: always the
+ * CUDA-core stream; 2: the tensor-core stream wherever it applies. Both compute
+ * the same layer; the choice changes rounding only, inside the stated
+ * tolerance. Process-wide, read at each launch. PQE_ERR_INVALID_ARG for any
+ * other kind. */
+PQE_API int pqe_test_set_stream_kernel(int kind);
+
 /* ------------------------------------------------------------------------
  * Expert pages and the slot pool  ([EP] 階層ページング; [PW] page-unit weights)
  *

@@ -87,6 +87,7 @@ _SIGS = {
     "pqe_kernel_launches": (C.c_uint64, []),
     "pqe_set_wait_limit": (I32, [C.c_uint32]),
     "pqe_test_set_phase2_bias": (I32, [C.c_uint32]),
+    "pqe_test_set_stream_kernel": (I32, [C.c_int]),
     "pqe_layer_set_ffn_events": (I32, [P, P, P]),
     "pqe_page_bytes": (SZ, [I32, I32, I32]),
     "pqe_slot_stride": (SZ, [I32, I32]),
@@ -674,6 +675,11 @@ def pqe_set_wait_limit(polls: int):
 def pqe_test_set_phase2_bias(bias: int):
     """Test hook: a nonzero bias makes the weight stream's phase-2 waits expire."""
     _check("pqe_test_set_phase2_bias", lib().pqe_test_set_phase2_bias(int(bias)))
+
+
+def pqe_test_set_stream_kernel(kind: int):
+    """Test hook: the weight-stream kernel, 0 default choice, 1 CUDA cores, 2 tensor cores."""
+    _check("pqe_test_set_stream_kernel", lib().pqe_test_set_stream_kernel(int(kind)))
 
 
 def kernel_launches() -> int:

@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(FfnArgs a, int tc_mi
         fmt = a.expert_fmt ? (int)a.expert_fmt[e] : PQE_FMT_FP8;
     }
     if (e < a.E && a.done13) a.done13[e] = 0u;
+    if (e == 0 && a.done13) a.done13[a.E] = 0u;  // the tensor-core stream's grab counter
     const bool valid_page = slot >= 0 && slot < a.n_slots + a.n_wb;
     const bool big = n > 0 && tc_min > 0 && n >= tc_min && valid_page;
     // large batches take the tcgen05 path: FP8 pages on the FP8 GEMM, MXFP4 pages
@@ -455,7 +456,7 @@ static FfnWs ffn_ws_layout(int T, int k, int E, int H, int I) {
     w.wpre = take(sizeof(int32_t) * (E + 1));
     w.tiles = take(sizeof(int32_t) * 4 * (size_t)(w.max_tiles ? w.max_tiles : 1));
     w.n_tiles = take(3 * sizeof(int32_t));
-    w.done13 = take(sizeof(uint32_t) * E);
+    w.done13 = take(sizeof(uint32_t) * (E + 1));
     w.h = take(A * I * sizeof(float));
     if (w.tc) {
         w.xt = take((size_t)T * H);
@@ -582,9 +583,14 @@ int moe_paged_ffn_pass(const void *x_bf16, const int32_t *perm_src, const int32_
     if (di != PQE_OK) return di;
     // SMs left to a refill running beside this pass
     if (reserve_sms > 0) sms = sms - reserve_sms > 2 * TC_SIDE_SMS + 8 ? sms - reserve_sms : 2 * TC_SIDE_SMS + 8;
+    // the tensor-core stream on all-FP8 layers once the step routes enough experts
+    const int kind = stream_kernel_choice();
+    const bool tc_ok = stream_path && expert_fmt == nullptr && stream_tc_shape_ok(pool->H, pool->I);
+    const bool use_tc = tc_ok && (kind == 2 || (kind == 0 && max_active >= STREAM_TC_MIN_EXPERTS));
+    const int side_sms = use_tc ? TC_SIDE_SMS_TC_STREAM : TC_SIDE_SMS;
     // decode-sized step: the tensor-core batches run beside the weight stream
     const bool side = stream_path && w.tc && A >= TC_MIN_ROWS && A <= (long)DECODE_ROWS_PER_EXPERT * E &&
-                      sms > 2 * TC_SIDE_SMS;
+                      sms > 2 * side_sms;
     SideStream *ss = nullptr;
     if (side) {
         const int r = side_stream(dev, ss);
@@ -593,8 +599,13 @@ int moe_paged_ffn_pass(const void *x_bf16, const int32_t *perm_src, const int32_
     }
     // the stream kernel goes out first: from an idle GPU every host step before it
     // is a gap after the schedule kernel
-    int rc = stream_path ? launch_ffn_stream(args, s, side ? sms - TC_SIDE_SMS : (reserve_sms > 0 ? sms : 0))
-                         : launch_ffn_gemv(args, max_active, s);
+    int rc;
+    if (stream_path) {
+        const int grid = side ? sms - side_sms : (reserve_sms > 0 ? sms : 0);
+        rc = use_tc ? launch_ffn_stream_tc(args, s, grid) : launch_ffn_stream(args, s, grid);
+    } else {
+        rc = launch_ffn_gemv(args, max_active, s);
+    }
     if (side) PQE_CUDA_TRY(cudaStreamWaitEvent(ss->s, ss->fork, 0));
     if (rc != PQE_OK || !w.tc) {
         if (side) {  // close the fork
@@ -616,7 +627,7 @@ int moe_paged_ffn_pass(const void *x_bf16, const int32_t *perm_src, const int32_
     b.hq = wsb + w.hq;
     b.sh = reinterpret_cast<float *>(wsb + w.sh);
     if (!side) return launch_ffn_tc(args, b, w.max_tiles, s, sms);
-    rc = launch_ffn_tc(args, b, w.max_tiles, ss->s, TC_SIDE_SMS);
+    rc = launch_ffn_tc(args, b, w.max_tiles, ss->s, side_sms);
     // the join is recorded even after a failed launch, so the caller's stream never
     // waits on a fork that was left open
     PQE_CUDA_TRY(cudaEventRecord(ss->join, ss->s));

@@ -22,7 +22,8 @@ struct FfnArgs {
     float *h;                    // fp32 [T*k, I]
     uint16_t *out_perm;          // bf16 [T*k, H]
     int32_t *status;
-    uint32_t *done13;            // [E] stream kernel: phase-1 units x token groups combined per expert (zeroed by the schedule)
+    uint32_t *done13;            // [E + 1] stream kernels: phase-1 work combined per expert, then the
+                                 // tensor-core stream's grab counter (all zeroed by the schedule)
     uint32_t wait_limit;         // polls of a bounded wait before it gives up
     uint32_t phase2_bias;        // test hook: added to the phase-2 target (0 in normal use)
 };
@@ -62,11 +63,25 @@ constexpr int TC_MIN_ROWS = 9;
 // the step.
 constexpr int TC_SIDE_SMS = 16;
 constexpr int DECODE_ROWS_PER_EXPERT = 4;
+// Beside the tensor-core weight stream the side chain gets more SMs: that
+// stream takes a larger share of HBM per SM, so with 16 the side chain
+// finished last (a T=64 decode step: 97 us against the stream's 89 us; with
+// 24, 77 us against 92 us).
+constexpr int TC_SIDE_SMS_TC_STREAM = 24;
+
+// The weight stream runs on the tensor cores (ffn_stream_tc.cu) when a layer's
+// pages are all FP8 and a step routes at least this many experts: its work
+// items are 128-row tiles of whole K, so fewer experts leave SMs without work,
+// and the CUDA-core stream (16-row units) is then the faster one.
+constexpr int STREAM_TC_MIN_EXPERTS = 32;
 
 bool tc_shape_ok(int H, int I);
 bool stream_shape_ok(int H, int I);
 // grid: CTAs of the persistent stream kernel, 0 = one per SM
 int launch_ffn_stream(const FfnArgs &args, cudaStream_t s, int grid = 0);
+// the same FFN on the tensor cores (tcgen05, FP8 pages only: expert_fmt null)
+bool stream_tc_shape_ok(int H, int I);
+int launch_ffn_stream_tc(const FfnArgs &args, cudaStream_t s, int grid = 0);
 int launch_ffn_gemv(const FfnArgs &args, int max_active, cudaStream_t s);
 // sm_cap: at most this many persistent GEMM CTAs, 0 = one per SM
 int launch_ffn_tc(const FfnArgs &args, const TcBuffers &b, int max_tiles, cudaStream_t s, int sm_cap = 0);

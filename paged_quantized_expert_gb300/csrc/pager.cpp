@@ -32,9 +32,11 @@ void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 // weight stream's phase-2 target (both read at each launch)
 static std::atomic<uint32_t> g_wait_limit{DEFAULT_WAIT_LIMIT};
 static std::atomic<uint32_t> g_phase2_bias{0};
+static std::atomic<int> g_stream_kernel{0};
 
 uint32_t wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
 uint32_t phase2_bias() { return g_phase2_bias.load(std::memory_order_relaxed); }
+int stream_kernel_choice() { return g_stream_kernel.load(std::memory_order_relaxed); }
 
 }  // namespace pqe
 
@@ -72,6 +74,12 @@ int pqe_set_wait_limit(uint32_t polls) {
 
 int pqe_test_set_phase2_bias(uint32_t bias) {
     pqe::g_phase2_bias.store(bias, std::memory_order_relaxed);
+    return PQE_OK;
+}
+
+int pqe_test_set_stream_kernel(int kind) {
+    if (kind < 0 || kind > 2) return PQE_ERR_INVALID_ARG;
+    pqe::g_stream_kernel.store(kind, std::memory_order_relaxed);
     return PQE_OK;
 }
 

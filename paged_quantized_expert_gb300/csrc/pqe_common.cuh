@@ -114,6 +114,10 @@ int launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaS
 constexpr uint32_t DEFAULT_WAIT_LIMIT = 1u << 22;
 uint32_t wait_limit();
 uint32_t phase2_bias();
+// Test hook (pqe_test_set_stream_kernel): which weight-stream kernel the FFN
+// takes, 0 the default choice, 1 the CUDA-core stream, 2 the tensor-core
+// stream where it applies; read on the host at each launch.
+int stream_kernel_choice();
 
 // The current device and its SM count, cached per device (a process may drive
 // several GPUs; launch attributes such as the dynamic shared-memory opt-in are
