@@ -54,7 +54,8 @@
 //              the expert's token rows (x, or h once its phase-1 count is
 //              complete) into a [16 x K] E4M3 tile in the MMA's swizzled
 //              layout, double-buffered; each lane loads its whole share of the
-//              row before it reduces and converts, one round trip per tile
+//              row into registers before the tile's buffer is free, so the
+//              load latency overlaps the MMAs still reading that buffer
 // Every wait is bounded: on expiry PQE_STATUS_TIMEOUT is set, the waiting role
 // stops, the CTA drains the copies and MMAs it issued, frees its TMEM and
 // returns.
@@ -124,9 +125,18 @@ struct Ring {
     }
 };
 
+// bounded wait without sleeping between polls (try_wait itself suspends the
+// thread for a while): a sleeping waiter wakes late, and every wait here is on
+// the stream's critical path; false after `limit` polls
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
 // a ready barrier costs one poll; otherwise the bounded wait
 __device__ __forceinline__ bool mbar_ready(uint32_t bar, uint32_t parity, uint32_t limit) {
-    return mbar_try_wait(bar, parity) || mbar_wait(bar, parity, limit);
+    return mbar_try_wait(bar, parity) || wait_bar(bar, parity, limit);
 }
 
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
@@ -306,7 +316,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     next = (int)gridDim.x + (int)atomicAdd(counter, 1u);
                 }
                 const int qs = q % QN;
-                ok = mbar_wait(bar_qfree + 8 * qs, ((uint32_t)(q / QN) & 1u) ^ 1u, a.wait_limit);
+                ok = wait_bar(bar_qfree + 8 * qs, ((uint32_t)(q / QN) & 1u) ^ 1u, a.wait_limit);
                 if (!ok) {
                     atomicOr(a.status, PQE_STATUS_TIMEOUT);
                     break;
@@ -324,7 +334,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             Ring rp;
             bool ok = true;
             for (int q = 0; ok; ++q) {
-                if (!mbar_wait(bar_qfull + 8 * (q % QN), (uint32_t)(q / QN) & 1u, a.wait_limit)) {
+                if (!wait_bar(bar_qfull + 8 * (q % QN), (uint32_t)(q / QN) & 1u, a.wait_limit)) {
                     ok = false;
                     break;
                 }
@@ -359,7 +369,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!ok) atomicOr(a.status, PQE_STATUS_TIMEOUT);
             // drain: the stages issued last have landed before the CTA may exit
             for (int j = (it > g.stages ? it - g.stages : 0); j < it; ++j)
-                mbar_wait(bar_full + 8 * (j % g.stages), (uint32_t)(j / g.stages) & 1u, a.wait_limit);
+                wait_bar(bar_full + 8 * (j % g.stages), (uint32_t)(j / g.stages) & 1u, a.wait_limit);
         }
     } else if (warp == W_MMA || warp == W_MMA1) {
         // ---------------- MMA issuers ----------------
@@ -373,7 +383,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint64_t adesc0 = sw128_desc(sbase);
             const uint64_t bdesc0 = sw128_desc(sbase + g.act_off);
             for (int q = 0; ok; ++q) {
-                if (!mbar_wait(bar_qfull + 8 * (q % QN), (uint32_t)(q / QN) & 1u, a.wait_limit)) {
+                if (!wait_bar(bar_qfull + 8 * (q % QN), (uint32_t)(q / QN) & 1u, a.wait_limit)) {
                     ok = false;
                     break;
                 }
@@ -381,7 +391,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mbar_arrive_plain(bar_qfree + 8 * (q % QN));
                 if (gr.phase == 0) break;
                 const int buf = q & 1;
-                if (!mbar_wait(bar_afull + 8 * buf, (uint32_t)(q >> 1) & 1u, a.wait_limit)) {
+                if (!wait_bar(bar_afull + 8 * buf, (uint32_t)(q >> 1) & 1u, a.wait_limit)) {
                     ok = false;
                     break;
                 }
@@ -419,7 +429,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!ok) atomicOr(a.status, PQE_STATUS_TIMEOUT);
             // every issued MMA has finished before TMEM is released (also after a wait gave up mid-item)
             umma_commit(bar_drain);
-            mbar_wait(bar_drain, 0u, a.wait_limit);
+            wait_bar(bar_drain, 0u, a.wait_limit);
         }
     } else if (warp < W_ACT0) {
         // ---------------- epilogue: TMEM -> h / out_perm ----------------
@@ -428,7 +438,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         float *xb = reinterpret_cast<float *>(smem + g.xb_off);
         int j = 0;
         for (int q = 0;; ++q) {
-            const bool okq = mbar_wait(bar_qfull + 8 * (q % QN), (uint32_t)(q / QN) & 1u, a.wait_limit);
+            const bool okq = wait_bar(bar_qfull + 8 * (q % QN), (uint32_t)(q / QN) & 1u, a.wait_limit);
             if (!epi_all(okq)) {
                 if (threadIdx.x == 32 * W_EPI0) atomicOr(a.status, PQE_STATUS_TIMEOUT);
                 break;
@@ -449,8 +459,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     srow = __ldg(reinterpret_cast<const float *>(page + (phase == 1 ? L.s13 : L.s2)) + row);
                 }
                 // the activation tile's scales were written before its barrier completed
-                const bool ok = mbar_wait(bar_tfull + 8 * acc, (uint32_t)(j >> 1) & 1u, a.wait_limit) &&
-                                mbar_wait(bar_afull + 8 * buf, (uint32_t)(q >> 1) & 1u, a.wait_limit);
+                const bool ok = wait_bar(bar_tfull + 8 * acc, (uint32_t)(j >> 1) & 1u, a.wait_limit) &&
+                                wait_bar(bar_afull + 8 * buf, (uint32_t)(q >> 1) & 1u, a.wait_limit);
                 if (!epi_all(ok)) {
                     if (threadIdx.x == 32 * W_EPI0) atomicOr(a.status, PQE_STATUS_TIMEOUT);
                     stop = true;
@@ -512,7 +522,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int q = 0;; ++q) {
             const int buf = q & 1;
             int ok = 1;
-            if (lane == 0) ok = mbar_wait(bar_qfull + 8 * (q % QN), (uint32_t)(q / QN) & 1u, a.wait_limit);
+            if (lane == 0) ok = wait_bar(bar_qfull + 8 * (q % QN), (uint32_t)(q / QN) & 1u, a.wait_limit);
             if (!__shfl_sync(0xffffffffu, ok, 0)) {
                 timed_out = true;
                 break;
@@ -522,7 +532,59 @@ __global__ void __launch_bounds__(THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive_plain(bar_qfree + 8 * (q % QN));
             if (f.phase == 0) break;
-            if (lane == 0) ok = mbar_wait(bar_aempty + 8 * buf, ((uint32_t)(q >> 1) & 1u) ^ 1u, a.wait_limit);
+            // this warp's token row into registers before its tile buffer is free:
+            // the loads are in flight while the MMAs finish with the buffer
+            const bool mine = f.valid && aw < f.n;
+            uint4 u[2 * XCH];  // x: bf16 pairs; h: fp32 bits, four per entry
+#pragma unroll
+            for (int i = 0; i < 2 * XCH; ++i) u[i] = make_uint4(0u, 0u, 0u, 0u);
+            if (mine && f.phase == 1) {
+                const int nch = H / 16;
+                const uint4 *xr =
+                    reinterpret_cast<const uint4 *>(a.x + (size_t)(__ldg(a.perm_src + f.p0 + aw) / a.k) * H);
+#pragma unroll
+                for (int i = 0; i < XCH; ++i) {
+                    const int c = lane + 32 * i;
+                    if (c < nch) {
+                        u[2 * i] = __ldg(xr + 2 * c);
+                        u[2 * i + 1] = __ldg(xr + 2 * c + 1);
+                    }
+                }
+            } else if (mine) {
+                // the h row, once all of the expert's phase-1 items are counted
+                const uint32_t target = (uint32_t)per1 * COUNT_PER_ITEM + a.phase2_bias;
+                int hok = 1;
+                if (lane == 0 && !counts_expired) {
+                    uint32_t i = 0;
+                    while (ld_acquire(a.done13 + f.e) < target) {
+                        if (++i > a.wait_limit) {
+                            hok = 0;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, hok, 0)) {
+                    // the tile is built from h as it is, and this warp waits for no later count
+                    if (lane == 0) atomicOr(a.status, PQE_STATUS_TIMEOUT);
+                    counts_expired = true;
+                }
+                const int nch = I / 16;
+                const float4 *hr = reinterpret_cast<const float4 *>(a.h + (size_t)(f.p0 + aw) * I);
+#pragma unroll
+                for (int i = 0; i < HCH; ++i) {
+                    const int c = lane + 32 * i;
+                    if (c < nch) {
+#pragma unroll
+                        for (int b = 0; b < 4; ++b) {
+                            const float4 v = __ldcg(hr + 4 * c + b);
+                            u[4 * i + b] = make_uint4(__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
+                                                      __float_as_uint(v.w));
+                        }
+                    }
+                }
+            }
+            if (lane == 0) ok = wait_bar(bar_aempty + 8 * buf, ((uint32_t)(q >> 1) & 1u) ^ 1u, a.wait_limit);
             if (!__shfl_sync(0xffffffffu, ok, 0)) {
                 timed_out = true;
                 break;
@@ -530,30 +592,22 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint8_t *tile = smem + g.act_off + (size_t)buf * g.act_bytes;
             if (!f.valid) {
                 if (aw == 0 && lane == 0) atomicOr(a.status, PQE_STATUS_BAD_PAGE);
-            } else if (f.phase == 1) {
-                // the x row (bf16) of this warp's token
-                if (aw < f.n) {
-                    const int t = aw, nch = H / 16;
-                    const uint4 *xr =
-                        reinterpret_cast<const uint4 *>(a.x + (size_t)(__ldg(a.perm_src + f.p0 + t) / a.k) * H);
-                    uint4 u[2 * XCH];
+            } else if (mine) {
+                const int t = aw;
+                const bool p1 = f.phase == 1;
+                float amax = 0.0f;
 #pragma unroll
-                    for (int i = 0; i < XCH; ++i) {
-                        const int c = lane + 32 * i;
-                        const bool in = c < nch;
-                        u[2 * i] = in ? __ldg(xr + 2 * c) : make_uint4(0u, 0u, 0u, 0u);
-                        u[2 * i + 1] = in ? __ldg(xr + 2 * c + 1) : make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    float amax = 0.0f;
+                for (int i = 0; i < 2 * XCH; ++i) {
+                    const uint32_t w4[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
 #pragma unroll
-                    for (int i = 0; i < 2 * XCH; ++i) {
-                        const uint32_t w4[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
-#pragma unroll
-                        for (int b = 0; b < 4; ++b)
-                            amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w4[b])), fabsf(bf16_hi(w4[b]))));
-                    }
-                    const float r = act_factor(warp_max(amax));
-                    if (lane == 0) s_ts[buf * NTOK + t] = 1.0f / r;
+                    for (int b = 0; b < 4; ++b)
+                        amax = p1 ? fmaxf(amax, fmaxf(fabsf(bf16_lo(w4[b])), fabsf(bf16_hi(w4[b]))))
+                                  : fmaxf(amax, fabsf(__uint_as_float(w4[b])));
+                }
+                const float r = act_factor(warp_max(amax));
+                if (lane == 0) s_ts[buf * NTOK + t] = 1.0f / r;
+                if (p1) {
+                    const int nch = H / 16;
 #pragma unroll
                     for (int i = 0; i < XCH; ++i) {
                         const int c = lane + 32 * i;
@@ -573,44 +627,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                             *reinterpret_cast<uint4 *>(st + act_chunk(NTOK + t, c & 7)) = lo;
                         }
                     }
-                }
-            } else {
-                // h rows of the expert's tokens (fp32), once all its phase-1 items are counted
-                const uint32_t target = (uint32_t)per1 * COUNT_PER_ITEM + a.phase2_bias;
-                int hok = 1;
-                if (lane == 0 && !counts_expired && aw < f.n) {  // warps without a token write nothing
-                    uint32_t i = 0;
-                    while (ld_acquire(a.done13 + f.e) < target) {
-                        if (++i > a.wait_limit) {
-                            hok = 0;
-                            break;
-                        }
-                        __nanosleep(64);
-                    }
-                }
-                if (!__shfl_sync(0xffffffffu, hok, 0)) {
-                    // the tile is built from h as it is, and this warp waits for no later count
-                    if (lane == 0) atomicOr(a.status, PQE_STATUS_TIMEOUT);
-                    counts_expired = true;
-                }
-                if (aw < f.n) {
-                    const int t = aw, nch = I / 16;
-                    const float4 *hr = reinterpret_cast<const float4 *>(a.h + (size_t)(f.p0 + t) * I);
-                    float4 u[4 * HCH];
-#pragma unroll
-                    for (int i = 0; i < HCH; ++i) {
-                        const int c = lane + 32 * i;
-                        const bool in = c < nch;
-#pragma unroll
-                        for (int b = 0; b < 4; ++b)
-                            u[4 * i + b] = in ? __ldcg(hr + 4 * c + b) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                    }
-                    float amax = 0.0f;
-#pragma unroll
-                    for (int i = 0; i < 4 * HCH; ++i)
-                        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(u[i].x), fabsf(u[i].y)), fmaxf(fabsf(u[i].z), fabsf(u[i].w))));
-                    const float r = act_factor(warp_max(amax));
-                    if (lane == 0) s_ts[buf * NTOK + t] = 1.0f / r;
+                } else {
+                    const int nch = I / 16;
 #pragma unroll
                     for (int i = 0; i < HCH; ++i) {
                         const int c = lane + 32 * i;
@@ -618,10 +636,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                             float v[16];
 #pragma unroll
                             for (int b = 0; b < 4; ++b) {
-                                v[4 * b] = u[4 * i + b].x * r;
-                                v[4 * b + 1] = u[4 * i + b].y * r;
-                                v[4 * b + 2] = u[4 * i + b].z * r;
-                                v[4 * b + 3] = u[4 * i + b].w * r;
+                                v[4 * b] = __uint_as_float(u[4 * i + b].x) * r;
+                                v[4 * b + 1] = __uint_as_float(u[4 * i + b].y) * r;
+                                v[4 * b + 2] = __uint_as_float(u[4 * i + b].z) * r;
+                                v[4 * b + 3] = __uint_as_float(u[4 * i + b].w) * r;
                             }
                             uint4 hi, lo;
                             split16(v, hi, lo);
