@@ -556,6 +556,7 @@ int moe_paged_ffn_pass(const void *x_bf16, const int32_t *perm_src, const int32_
     args.slot_stride = pool->slot_stride;
     args.n_slots = pool->n_slots;
     args.n_wb = pool->n_wb;
+    args.T = T;
     args.k = k;
     args.E = E;
     args.H = pool->H;

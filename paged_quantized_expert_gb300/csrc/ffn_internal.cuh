@@ -16,7 +16,7 @@ struct FfnArgs {
     size_t slot_stride;
     int n_slots;                 // cache slots
     int n_wb;                    // working-buffer entries
-    int k, E, H, I;
+    int T, k, E, H, I;
     int32_t *sched;              // [E+1]: count, then active expert ids
     int32_t *wpre;               // [E+1]: prefix of per-expert work weights over sched (stream kernel)
     float *h;                    // fp32 [T*k, I]

@@ -55,7 +55,9 @@
 //              complete) into a [16 x K] E4M3 tile in the MMA's swizzled
 //              layout, double-buffered; each lane loads its whole share of the
 //              row into registers before the tile's buffer is free, so the
-//              load latency overlaps the MMAs still reading that buffer
+//              load latency overlaps the MMAs still reading that buffer. A step
+//              of at most 8 tokens has all of x and perm_src staged in shared
+//              memory first, so its phase-1 tiles need no global load
 // Every wait is bounded: on expiry PQE_STATUS_TIMEOUT is set, the waiting role
 // stops, the CTA drains the copies and MMAs it issued, frees its TMEM and
 // returns.
@@ -104,6 +106,7 @@ struct Geo {
     uint32_t xb_off;              // [2][64][NTOK] fp32: up-row values for the gate warps
     uint32_t ts_off;              // [2][NTOK] fp32: token scales of each activation tile
     uint32_t q_off;               // Grab [QN]: the queue
+    uint32_t xs_off, xs_bytes;    // steps of at most NTOK tokens: x [T][H] bf16, then perm_src [T k], staged
     uint32_t bar_off, tmem_off, smem_bytes;
 };
 
@@ -200,7 +203,8 @@ __device__ __forceinline__ float act_factor(float amax) {
     return amax > 0.0f ? fminf(448.0f / amax, 0x1p100f) : 1.0f;
 }
 
-// named barriers of the epilogue warps: 1 (all four, AND vote), 3 (all four), 2 (the two gate warps)
+// named barriers of the epilogue warps: 1 (all four, AND vote), 3 (all four), 2 (the two gate warps);
+// 4 is the activation warps' (staging a small step's x)
 __device__ __forceinline__ bool epi_all(bool v) {
     uint32_t r;
     asm volatile(
@@ -519,6 +523,20 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---------------- activation tiles ----------------
         const int aw = warp - W_ACT0;
         bool timed_out = false, counts_expired = false;
+        // a small step: all of x and perm_src into shared memory once (no
+        // dependent global loads behind the weight copies per phase-1 tile)
+        const uint16_t *xsrc = a.x;
+        const int32_t *psrc = a.perm_src;
+        if (g.xs_bytes) {
+            uint4 *xd = reinterpret_cast<uint4 *>(smem + g.xs_off);
+            const int nx = a.T * H / 8, np = a.T * a.k, ta = threadIdx.x - 32 * W_ACT0;
+            for (int i = ta; i < nx; i += 32 * ACT_WARPS) xd[i] = __ldg(reinterpret_cast<const uint4 *>(a.x) + i);
+            int32_t *pd = reinterpret_cast<int32_t *>(smem + g.xs_off + (size_t)a.T * H * 2);
+            for (int i = ta; i < np; i += 32 * ACT_WARPS) pd[i] = __ldg(a.perm_src + i);
+            asm volatile("bar.sync 4, %0;" ::"n"(32 * ACT_WARPS) : "memory");  // the activation warps only (barrier 4)
+            xsrc = reinterpret_cast<const uint16_t *>(xd);
+            psrc = pd;
+        }
         for (int q = 0;; ++q) {
             const int buf = q & 1;
             int ok = 1;
@@ -540,14 +558,13 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int i = 0; i < 2 * XCH; ++i) u[i] = make_uint4(0u, 0u, 0u, 0u);
             if (mine && f.phase == 1) {
                 const int nch = H / 16;
-                const uint4 *xr =
-                    reinterpret_cast<const uint4 *>(a.x + (size_t)(__ldg(a.perm_src + f.p0 + aw) / a.k) * H);
+                const uint4 *xr = reinterpret_cast<const uint4 *>(xsrc + (size_t)(psrc[f.p0 + aw] / a.k) * H);
 #pragma unroll
                 for (int i = 0; i < XCH; ++i) {
                     const int c = lane + 32 * i;
                     if (c < nch) {
-                        u[2 * i] = __ldg(xr + 2 * c);
-                        u[2 * i + 1] = __ldg(xr + 2 * c + 1);
+                        u[2 * i] = xr[2 * c];
+                        u[2 * i + 1] = xr[2 * c + 1];
                     }
                 }
             } else if (mine) {
@@ -700,8 +717,9 @@ static bool map_rows64(CUtensorMap *m, const void *base, uint64_t slots, uint64_
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// shared memory of one CTA
-static bool geometry(int H, int I, Geo &g) {
+// shared memory of one CTA; a step of T <= NTOK tokens (k per token) stages
+// all of x and perm_src once, so that the phase-1 tiles are built on chip
+static bool geometry(int H, int I, int T, int k, Geo &g) {
     if (H / 16 > 32 * XCH || I / 16 > 32 * HCH) return false;  // a row's chunks per activation lane
     const int kmax = (H > I ? H : I) / KSTEP;
     g.act_bytes = (uint32_t)kmax * ACT_STEP;
@@ -709,7 +727,8 @@ static bool geometry(int H, int I, Geo &g) {
     const uint32_t qb = (uint32_t)round_up(sizeof(Grab) * QN, 16);
     const uint32_t bars = 8u * (2 * MAX_STAGES + 9 + 2 * QN);
     const uint32_t tail = 16;
-    const uint32_t fixed = 2 * g.act_bytes + xb + ts + qb + bars + tail;
+    g.xs_bytes = (T >= 1 && T <= NTOK) ? (uint32_t)round_up((size_t)T * H * 2 + (size_t)T * k * 4, 16) : 0u;
+    const uint32_t fixed = 2 * g.act_bytes + xb + ts + qb + g.xs_bytes + bars + tail;
     const uint32_t budget = 227 * 1024 - 1024;  // less the alignment slack
     if (fixed + MIN_STAGES * STAGE_BYTES > budget) return false;
     int stages = (int)((budget - fixed) / STAGE_BYTES);
@@ -719,7 +738,8 @@ static bool geometry(int H, int I, Geo &g) {
     g.xb_off = g.act_off + 2 * g.act_bytes;
     g.ts_off = g.xb_off + xb;
     g.q_off = g.ts_off + ts;
-    g.bar_off = g.q_off + qb;
+    g.xs_off = g.q_off + qb;
+    g.bar_off = g.xs_off + g.xs_bytes;
     g.tmem_off = g.bar_off + bars;
     g.smem_bytes = g.tmem_off + tail + 1024;
     return true;
@@ -729,13 +749,13 @@ static bool geometry(int H, int I, Geo &g) {
 
 bool stream_tc_shape_ok(int H, int I) {
     sw::Geo g;
-    return tc_shape_ok(H, I) && stream_shape_ok(H, I) && sw::geometry(H, I, g);
+    return tc_shape_ok(H, I) && stream_shape_ok(H, I) && sw::geometry(H, I, 0, 1, g);
 }
 
 int launch_ffn_stream_tc(const FfnArgs &args, cudaStream_t s, int grid) {
     using namespace sw;
     Geo g;
-    if (args.expert_fmt != nullptr || !tc_shape_ok(args.H, args.I) || !geometry(args.H, args.I, g))
+    if (args.expert_fmt != nullptr || !tc_shape_ok(args.H, args.I) || !geometry(args.H, args.I, args.T, args.k, g))
         return PQE_ERR_UNSUPPORTED;
     const int H = args.H, I = args.I;
     const PageLayout L = fp8_layout(H, I);
