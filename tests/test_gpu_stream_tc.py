@@ -43,6 +43,10 @@ def _layer(pqe, orc, cfg, T, logits, x=None, needed=None, page_table=None, pool=
     (40, 512, 256, 4, 36),    # batches of 0..8 rows, an expert's items over several CTAs
     (64, 1024, 384, 8, 24),   # K = 1024 in 8 stages; I = 384: six phase-1 items per expert
     (3, 256, 640, 1, 7),      # I > H: the h tile is the longer one
+    # steps of at most 8 tokens: x and perm_src staged in shared memory
+    (9, 256, 128, 2, 8),      # batches of 1..8 rows from a staged x
+    (40, 512, 256, 4, 5),     # an expert's items over several CTAs, staged x
+    (64, 1024, 384, 8, 1),    # one token, eight experts
 ])
 def test_tc_stream_small_layers(tc_stream, orc, E, H, I, k, T):
     pqe = tc_stream
@@ -93,6 +97,33 @@ def test_tc_stream_decode_layer_shapes(tc_stream, orc, T, n_check):
     check_tokens(orc, pages, cfg, x, ids, gates, res, tokens)
 
 
+@pytest.mark.parametrize("T", [3, 16])
+def test_tc_stream_bad_page_staged_and_unstaged(tc_stream, orc, T):
+    # a routed expert whose page-table entry points outside the pool, with x
+    # staged in shared memory (T <= 8) and without: flagged, its rows of
+    # out_perm are zero, the other experts' rows match the oracle
+    pqe = tc_stream
+    E, H, I, k = 6, 256, 128, 2
+    cfg = synth.small_config(E=E, H=H, I=I, k=k, T=T, cid=89)
+    pages = Pages(pqe, orc, cfg, needed=set(range(E)))
+    logits = np.random.default_rng(23 + T).standard_normal((T, E)).astype(np.float32)
+    ids, gates = orc.topk_gates(logits, k)
+    counts = np.bincount(ids.reshape(-1), minlength=E)
+    bad_e = int(np.argmax(counts))
+    pt = np.arange(E, dtype=np.int32)
+    pt[bad_e] = E + 3
+    x = synth.activations(cfg, T)
+    res = run_layer(pqe, cfg, T, x, logits_np=logits, page_table=torch.from_numpy(pt).to(DEV), fmt_dev=None,
+                    pool=pages.pool)
+    assert res["status"] & pqe.PQE_STATUS_BAD_PAGE
+    op = res["out_perm"].float().cpu().numpy()
+    _, offsets, _, _ = orc.permute(ids, E)
+    assert np.all(op[np.arange(offsets[bad_e], offsets[bad_e + 1])] == 0)
+    ok_tokens = np.array([t for t in range(T) if bad_e not in ids[t]], dtype=np.int32)
+    if len(ok_tokens):
+        check_tokens(orc, pages, cfg, x, ids, gates, res, ok_tokens)
+
+
 def test_tc_stream_slot_indirection_and_bad_page(tc_stream, orc):
     # experts in permuted slots of a larger pool; then one routed expert points
     # outside the pool: flagged, its rows of out_perm are zero, the others exact
@@ -123,11 +154,12 @@ def test_tc_stream_slot_indirection_and_bad_page(tc_stream, orc):
     assert np.any(op[np.arange(offsets[0], offsets[1])] != 0)
 
 
-def test_tc_stream_graph_replay_bit_identical(tc_stream, orc):
+@pytest.mark.parametrize("T", [6, 36])
+def test_tc_stream_graph_replay_bit_identical(tc_stream, orc, T):
     # the FFN call eager and replayed from a CUDA graph: the same out_perm bit
-    # for bit (no atomics in the arithmetic, a fixed MMA order)
+    # for bit (no atomics in the arithmetic, a fixed MMA order); T=6 stages x
     pqe = tc_stream
-    E, H, I, k, T = 40, 512, 256, 4, 36
+    E, H, I, k = 40, 512, 256, 4
     cfg = synth.small_config(E=E, H=H, I=I, k=k, T=T, cid=96)
     logits = np.random.default_rng(13).standard_normal((T, E)).astype(np.float32)
     ids, _ = orc.topk_gates(logits, k)
