@@ -83,9 +83,10 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(FfnArgs a, int tc_mi
         }
         __syncthreads();
     }
-    int n = 0, slot = -1, fmt = PQE_FMT_FP8;
+    int n = 0, slot = -1, fmt = PQE_FMT_FP8, p0 = 0;
     if (e < a.E && (!miss || s_pass[e] == pass)) {
-        n = a.offsets[e + 1] - a.offsets[e];
+        p0 = a.offsets[e];
+        n = a.offsets[e + 1] - p0;
         slot = a.page_table[e];
         fmt = a.expert_fmt ? (int)a.expert_fmt[e] : PQE_FMT_FP8;
     }
@@ -106,7 +107,12 @@ __global__ void __launch_bounds__(1024) ffn_schedule_kernel(FfnArgs a, int tc_mi
     const int4 pre = block_excl_scan4(make_int4(gemv ? 1 : 0, gemv ? wgt : 0, nt8, nt4), scan_tot, tot);
     const int gpos = pre.x, wpos = pre.y, tpos8 = pre.z, tpos4 = pre.w;
     const int total = tot.x, wtot = tot.y, total8 = tot.z, total4 = tot.w;
-    if (gemv) a.sched[1 + gpos] = e;
+    if (gemv) {
+        a.sched[1 + gpos] = e;
+        // the stream kernels read the expert's batch and page from here: one
+        // dependent load fewer before their first copies
+        a.info[gpos] = make_int4(e, p0, n, info_pack(slot, fmt));
+    }
     if (threadIdx.x == 0) a.sched[0] = total;
     if (gemv) a.wpre[gpos] = wpos;
     if (threadIdx.x == 0) a.wpre[total] = wtot;
@@ -433,7 +439,7 @@ int launch_ffn_gemv(const FfnArgs &args, int max_active, cudaStream_t s) {
 
 // workspace carve-up shared by the size query and the call
 struct FfnWs {
-    size_t sched, wpre, tiles, n_tiles, done13, h, xt, st, xq, sx, hbf, hmax, hq, sh, total;
+    size_t sched, wpre, tiles, n_tiles, done13, info, h, xt, st, xq, sx, hbf, hmax, hq, sh, total;
     int max_tiles;
     bool tc;
 };
@@ -457,6 +463,7 @@ static FfnWs ffn_ws_layout(int T, int k, int E, int H, int I) {
     w.tiles = take(sizeof(int32_t) * 4 * (size_t)(w.max_tiles ? w.max_tiles : 1));
     w.n_tiles = take(3 * sizeof(int32_t));
     w.done13 = take(sizeof(uint32_t) * (E + 1));
+    w.info = take(sizeof(int4) * (size_t)E);
     w.h = take(A * I * sizeof(float));
     if (w.tc) {
         w.xt = take((size_t)T * H);
@@ -569,6 +576,7 @@ int moe_paged_ffn_pass(const void *x_bf16, const int32_t *perm_src, const int32_
     args.out_perm = static_cast<uint16_t *>(out_perm);
     args.status = status;
     args.done13 = reinterpret_cast<uint32_t *>(wsb + w.done13);
+    args.info = reinterpret_cast<int4 *>(wsb + w.info);
     args.wait_limit = wait_limit();
     args.phase2_bias = phase2_bias();
     const long A = (long)T * k;

@@ -19,6 +19,8 @@ struct FfnArgs {
     int T, k, E, H, I;
     int32_t *sched;              // [E+1]: count, then active expert ids
     int32_t *wpre;               // [E+1]: prefix of per-expert work weights over sched (stream kernel)
+    int4 *info;                  // [E]: per expert of sched, {e, first batch row, batch rows, page entry
+                                 // (24 bits, sign-extended) | format << 24}, written by the schedule
     float *h;                    // fp32 [T*k, I]
     uint16_t *out_perm;          // bf16 [T*k, H]
     int32_t *status;
@@ -27,6 +29,11 @@ struct FfnArgs {
     uint32_t wait_limit;         // polls of a bounded wait before it gives up
     uint32_t phase2_bias;        // test hook: added to the phase-2 target (0 in normal use)
 };
+
+// the schedule's record of an expert's page-table entry and format
+__host__ __device__ __forceinline__ int info_pack(int slot, int fmt) { return (slot & 0x00FFFFFF) | (fmt << 24); }
+__host__ __device__ __forceinline__ int info_slot(int w) { return (int)((unsigned)w << 8) >> 8; }
+__host__ __device__ __forceinline__ int info_fmt(int w) { return (int)((unsigned)w >> 24); }
 
 // address of page-table entry `slot` (valid: 0 <= slot < n_slots + n_wb)
 __device__ __forceinline__ const uint8_t *page_addr(const FfnArgs &a, int slot) {

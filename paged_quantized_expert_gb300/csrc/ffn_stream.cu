@@ -389,12 +389,6 @@ __device__ __forceinline__ void mma_rows_fp4(const uint8_t *rows, uint32_t pitch
     }
 }
 
-__device__ __forceinline__ bool page_ok(const FfnArgs &a, int e, int &slot, int &fmt) {
-    slot = a.page_table[e];
-    fmt = a.expert_fmt ? (int)a.expert_fmt[e] : PQE_FMT_FP8;
-    return slot >= 0 && slot < a.n_slots + a.n_wb && (fmt == PQE_FMT_FP8 || fmt == PQE_FMT_MXFP4);
-}
-
 // Units of the expert list in expert-major order, each expert's units weighted
 // by its work weight w_a = wpre[a+1] - wpre[a]; unit_at maps a position of the
 // weighted line (0 .. wpre[n]*per) to the first unit at or after it.
@@ -436,11 +430,14 @@ __global__ void __launch_bounds__(THREADS, 1) ffn_stream_kernel(const FfnArgs a,
     ExpertInfo *s_info = reinterpret_cast<ExpertInfo *>(s_wpre + g.info_off);  // [n_act]
     for (int i = threadIdx.x; i <= n_act; i += THREADS) s_wpre[i] = __ldg(a.wpre + i);
     for (int i = threadIdx.x; i < n_act; i += THREADS) {
+        const int4 r = __ldg(a.info + i);  // the schedule's record: expert, batch, page
         ExpertInfo f;
-        f.e = __ldg(a.sched + 1 + i);
-        f.p0 = __ldg(a.offsets + f.e);
-        f.n = __ldg(a.offsets + f.e + 1) - f.p0;
-        f.valid = page_ok(a, f.e, f.slot, f.fmt) ? 1 : 0;
+        f.e = r.x;
+        f.p0 = r.y;
+        f.n = r.z;
+        f.slot = info_slot(r.w);
+        f.fmt = info_fmt(r.w);
+        f.valid = f.slot >= 0 && f.slot < a.n_slots + a.n_wb && (f.fmt == PQE_FMT_FP8 || f.fmt == PQE_FMT_MXFP4);
         s_info[i] = f;
     }
     if (threadIdx.x == 0) {

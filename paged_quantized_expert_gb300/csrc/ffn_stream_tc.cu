@@ -218,12 +218,6 @@ __device__ __forceinline__ bool epi_all(bool v) {
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 3, %0;" ::"n"(EPI_WARPS * 32) : "memory"); }
 __device__ __forceinline__ void gate_sync() { asm volatile("bar.sync 2, 64;" ::: "memory"); }
 
-__device__ __forceinline__ bool page_ok(const FfnArgs &a, int e, int &slot) {
-    slot = a.page_table[e];
-    const int fmt = a.expert_fmt ? (int)a.expert_fmt[e] : PQE_FMT_FP8;
-    return slot >= 0 && slot < a.n_slots + a.n_wb && fmt == PQE_FMT_FP8;
-}
-
 __global__ void __launch_bounds__(THREADS, 1)
     ffn_stream_tc_kernel(const __grid_constant__ CUtensorMap m13c, const __grid_constant__ CUtensorMap m13w,
                          const __grid_constant__ CUtensorMap m2c, const __grid_constant__ CUtensorMap m2w,
@@ -312,10 +306,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                         gr.rb0 = (r - i * ng2) * g2;
                         gr.nrb = min(g2, per2 - gr.rb0);
                     }
-                    gr.e = __ldg(a.sched + 1 + i);
-                    gr.p0 = __ldg(a.offsets + gr.e);
-                    gr.n = __ldg(a.offsets + gr.e + 1) - gr.p0;
-                    gr.valid = page_ok(a, gr.e, gr.slot) ? 1 : 0;
+                    const int4 r = __ldg(a.info + i);  // the schedule's record: expert, batch, page
+                    gr.e = r.x;
+                    gr.p0 = r.y;
+                    gr.n = r.z;
+                    gr.slot = info_slot(r.w);
+                    gr.valid = gr.slot >= 0 && gr.slot < a.n_slots + a.n_wb && info_fmt(r.w) == PQE_FMT_FP8;
                     // the grab after this one, taken while this one waits for its entry
                     next = (int)gridDim.x + (int)atomicAdd(counter, 1u);
                 }
