@@ -34,10 +34,11 @@
 // last CTA.
 //
 // One CTA per SM (cooperative launch), sixteen warps:
-//   warp 14    scheduler (one thread): takes the next grab, looks up its
-//              expert, batch and page, and publishes it in a queue of two
-//              entries that every other role reads in order (an entry is
-//              reused once each reader has copied it)
+//   warp 14    scheduler (one thread): takes the next grab, reads its expert,
+//              batch and page from the schedule's record of the expert, and
+//              publishes it in a queue of two entries that every other role
+//              reads in order (an entry is reused once each reader has copied
+//              it)
 //   warp 0     TMA producer (one thread): each stage is 128 weight rows x 128
 //              bytes of K, two [64 rows x 128 B] boxes from the page's 3-D map
 //              [slot, row, k], 128-byte swizzle, into a ring of 16 KB stages
@@ -235,7 +236,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t bar_afull = bar_tempty + 16;           // [2] activation tile written
     const uint32_t bar_aempty = bar_afull + 16;           // [2] activation tile no longer read
     const uint32_t bar_qfull = bar_aempty + 16;           // [QN] queue entry published
-    const uint32_t bar_qfree = bar_qfull + 8 * QN;        // [QN] queue entry read by its last reader
+    const uint32_t bar_qfree = bar_qfull + 8 * QN;        // [QN] queue entry copied by all of its readers
     const uint32_t bar_drain = bar_qfree + 8 * QN;        // every MMA of the CTA finished
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + g.tmem_off);
     Grab *s_q = reinterpret_cast<Grab *>(smem + g.q_off);
