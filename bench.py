@@ -1071,7 +1071,7 @@ def main():
         return 0
     r = Runner(pqe, torch, device, host, L, max(T, 64))
     xs_dev = [torch.from_numpy(synth.activations(CFG, T, s).view(np.int16)).to(device) for s in range(4)]
-    logits_np = make_traces(T, L, W + K + graph_extra)
+    logits_np = make_traces(T, L, max(W, 2 * L) + K + graph_extra)  # the e2e leg warms up on 2 L steps at least
     logits_dev = [torch.from_numpy(l).to(device) for l in logits_np]
     y = torch.zeros((T, CFG.H), dtype=torch.bfloat16, device=device)
 
@@ -1123,17 +1123,21 @@ def main():
     traffic = (FFN_DRAM_PER_ALGORITHMIC_BYTE_T64 * float(np.mean(byts))
                if T == 64 and FFN_DRAM_PER_ALGORITHMIC_BYTE_T64 else None)
 
-    # e2e: host buffers through pqe_layer_step_host (eager calls), on layers with
-    # the headline's pager (and its overlap groups)
+    # e2e: host buffers through pqe_layer_step_host, on layers with the
+    # headline's pager (and its overlap groups); on device-pager layers the call
+    # replays its own cached graph of the step's launches between the copies
     x_h = torch.from_numpy(synth.activations(CFG, T, 0).view(np.int16)).pin_memory()
     y_h = torch.zeros((T, CFG.H), dtype=torch.bfloat16).pin_memory()
     lg_h = [torch.from_numpy(l).pin_memory() for l in logits_np]
     Ke = min(K, 128)
+    We = max(W, 2 * L) if pager_used == "device" else W
     re = r
     if pager_used == "device":
         r.close()
         re = Runner(pqe, torch, device, host, L, max(T, 64), device_pager=True, overlap_groups=overlap_groups_for(T))
-        for i in range(W):
+        re.stream = torch.cuda.Stream(device)  # a created stream, as a caller's would be (capturable)
+        # two calls per layer at least: the second captures the layer's step graph
+        for i in range(We):
             re.layers[i % L].step_host(x_h, y_h, T, logits_host=lg_h[i], stream=re.stream, side_stream=re.side)
     torch.cuda.synchronize()
     barrier(ws)
@@ -1141,7 +1145,7 @@ def main():
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(re.stream)
     for j in range(Ke):
-        i = W + j
+        i = We + j
         re.layers[i % L].step_host(x_h, y_h, T, logits_host=lg_h[i], stream=re.stream, side_stream=re.side)
     e1.record(re.stream)
     torch.cuda.synchronize()
@@ -1249,7 +1253,8 @@ def main():
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": T * CFG.H * 2 + T * CFG.E * 4,
                     "d2h_bytes_per_step": T * CFG.H * 2, "pager": pager_used,
-                    "api": "pqe_layer_step_host (pinned host x and logits in, pinned host y out, every step)"},
+                    "api": "pqe_layer_step_host (pinned host x and logits in, pinned host y out, every step; "
+                           "the call's own step graph on device-pager layers)"},
             "gpu_launches": int(launches),
             "fp8_peak": dict(_FP8_PEAK),
             # the step's refills against the host link: bytes refilled per second of

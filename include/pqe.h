@@ -686,6 +686,10 @@ PQE_API int pqe_layer_buffers(pqe_layer *L, pqe_layer_buffers_t *out);
  * records them again. */
 PQE_API int pqe_layer_set_ffn_events(pqe_layer *L, void *ev_begin, void *ev_end);
 
+/* pqe_layer_step_host's graph replays on (enable != 0, the default) or off
+ * (every call steps eagerly). The layer keeps its graphs until destroyed. */
+PQE_API int pqe_layer_set_step_graphs(pqe_layer *L, int enable);
+
 /* The layer's LRU state (see pqe_lru_state). */
 PQE_API int pqe_layer_lru_state(const pqe_layer *L, int32_t *slot_expert, int64_t *last_use, int64_t *step);
 
@@ -707,7 +711,13 @@ PQE_API int pqe_layer_device_stats(pqe_layer *L, int64_t *stats, int32_t *slot_e
 
 /* The same step on host buffers (pinned for asynchronous copies): x_host bf16
  * [T, H] and logits_host fp32 [T, E] are copied in, y_host bf16 [T, H] is
- * copied out; returns after the stream is synchronised. */
+ * copied out; returns after the stream is synchronised. On a device-pager
+ * layer, a created (non-default) stream and no FFN timing events, the step's
+ * launches between the copies are captured into a CUDA graph on the second
+ * call with the same T, router pointer and stream pairing, and replayed on
+ * later calls (at most 16 shapes kept per layer, the oldest dropped first;
+ * a change of pqe_set_wait_limit or a test hook rebuilds it); the copies and
+ * the synchronisation stay outside the graph. */
 PQE_API int pqe_layer_step_host(pqe_layer *L, const void *x_host, const float *w_router_dev,
                                 const float *logits_host, int T, void *y_host, void *stream,
                                 void *side_stream, pqe_step_info *info);

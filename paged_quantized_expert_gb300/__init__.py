@@ -89,6 +89,7 @@ _SIGS = {
     "pqe_test_set_phase2_bias": (I32, [C.c_uint32]),
     "pqe_test_set_stream_kernel": (I32, [C.c_int]),
     "pqe_layer_set_ffn_events": (I32, [P, P, P]),
+    "pqe_layer_set_step_graphs": (I32, [P, I32]),
     "pqe_page_bytes": (SZ, [I32, I32, I32]),
     "pqe_slot_stride": (SZ, [I32, I32]),
     "pqe_quantize_fp8_rows": (I32, [P, I32, I32, P, P, P]),
@@ -630,6 +631,9 @@ class PagedMoELayer:
         """Serve refills from a RAM tier (host pager only); None detaches it."""
         self._ram_tier = tier
         _check("pqe_layer_attach_ram_tier", lib().pqe_layer_attach_ram_tier(self._h, tier._h if tier else None))
+
+    def set_step_graphs(self, enable):
+        _check("pqe_layer_set_step_graphs", lib().pqe_layer_set_step_graphs(self._h, 1 if enable else 0))
 
     def set_ffn_events(self, ev_begin, ev_end):
         _check("pqe_layer_set_ffn_events", lib().pqe_layer_set_ffn_events(self._h, _event(ev_begin),

@@ -118,6 +118,18 @@ struct pqe_layer {
     std::vector<int32_t> ram_need, ram_queued;
     std::vector<const void *> ram_page;
     std::vector<size_t> ram_bytes;
+    // pqe_layer_step_host on a device-pager layer: the step's launches captured
+    // once per shape and replayed (the first call of a shape runs eagerly)
+    struct StepGraph {
+        int T;
+        const float *w_router;
+        bool overlap;
+        uint64_t gen;
+        int state;  // 0 seen once, 1 exec built, -1 capture failed (eager from then on)
+        cudaGraphExec_t exec;
+    };
+    std::vector<StepGraph> graphs;
+    bool step_graphs = true;
 
     template <class T>
     T *at(size_t off) const {
@@ -244,6 +256,8 @@ void pqe_layer_destroy(pqe_layer *L) {
     for (cudaEvent_t e : L->ev_group)
         if (e) cudaEventDestroy(e);
     if (L->pinned) cudaFreeHost(L->pinned);
+    for (auto &g : L->graphs)
+        if (g.exec) cudaGraphExecDestroy(g.exec);
     pqe_lru_destroy(L->lru);
     delete L;
 }
@@ -323,6 +337,12 @@ int pqe_layer_buffers(pqe_layer *L, pqe_layer_buffers_t *out) {
     out->x_in = L->at<void>(L->map.x_in);
     out->logits_in = L->at<float>(L->map.logits_in);
     out->y_out = L->at<void>(L->map.y_out);
+    return PQE_OK;
+}
+
+int pqe_layer_set_step_graphs(pqe_layer *L, int enable) {
+    if (!L) return PQE_ERR_INVALID_ARG;
+    L->step_graphs = enable != 0;
     return PQE_OK;
 }
 
@@ -511,6 +531,82 @@ int pqe_layer_step(pqe_layer *L, const void *x_dev, const float *w_router_dev, f
     return PQE_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// The launches of one pqe_layer_step for pqe_layer_step_host. A device-pager
+// step decides nothing on the host, so its launches for a given step size,
+// router mode and stream pair are the same every time: they are captured into
+// a CUDA graph on the second call of that shape and replayed from then on.
+// Timing events, the legacy default streams (which cannot be captured) and a
+// changed launch setting (wait limit, test hooks) fall back to the eager step
+// or to a new capture.
+constexpr size_t MAX_STEP_GRAPHS = 16;
+
+int step_host_launches(pqe_layer *L, const void *x_in, const float *w_router, float *lg, int T, void *y,
+                       cudaStream_t s, void *side_stream, pqe_step_info *info) {
+    const bool overlap = side_stream && reinterpret_cast<cudaStream_t>(side_stream) != s;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const bool graphable = L->cfg.device_pager && L->step_graphs && !L->ev_ffn_begin && T > 0 && s &&
+                           s != cudaStreamLegacy && s != cudaStreamPerThread &&
+                           cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone;
+    if (!graphable) return pqe_layer_step(L, x_in, w_router, lg, T, y, s, side_stream, info);
+    const uint64_t gen = pqe::launch_settings_generation();
+    pqe_layer::StepGraph *g = nullptr;
+    for (auto &e : L->graphs)
+        if (e.T == T && e.w_router == w_router && e.overlap == overlap) g = &e;
+    if (g && g->gen != gen) {  // captured under other settings: start again
+        if (g->exec) cudaGraphExecDestroy(g->exec);
+        *g = pqe_layer::StepGraph{T, w_router, overlap, gen, 0, nullptr};
+        return pqe_layer_step(L, x_in, w_router, lg, T, y, s, side_stream, info);
+    }
+    if (!g) {
+        if (L->graphs.size() >= MAX_STEP_GRAPHS) {
+            if (L->graphs.front().exec) cudaGraphExecDestroy(L->graphs.front().exec);
+            L->graphs.erase(L->graphs.begin());
+        }
+        L->graphs.push_back(pqe_layer::StepGraph{T, w_router, overlap, gen, 0, nullptr});
+        return pqe_layer_step(L, x_in, w_router, lg, T, y, s, side_stream, info);
+    }
+    if (g->state < 0) return pqe_layer_step(L, x_in, w_router, lg, T, y, s, side_stream, info);
+    if (g->state == 0) {
+        cudaError_t ce = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+        if (ce != cudaSuccess) {
+            pqe::set_last_cuda_error(ce);
+            return PQE_ERR_CUDA;
+        }
+        const int rc = pqe_layer_step(L, x_in, w_router, lg, T, y, s, side_stream, nullptr);
+        cudaGraph_t graph = nullptr;
+        ce = cudaStreamEndCapture(s, &graph);
+        cudaGraphExec_t exec = nullptr;
+        if (rc == PQE_OK && ce == cudaSuccess) ce = cudaGraphInstantiate(&exec, graph, 0);
+        if (graph) cudaGraphDestroy(graph);
+        if (rc != PQE_OK) {
+            (void)cudaGetLastError();
+            return rc;
+        }
+        if (ce != cudaSuccess) {  // not capturable here: this shape steps eagerly from now on
+            (void)cudaGetLastError();
+            g->state = -1;
+            return pqe_layer_step(L, x_in, w_router, lg, T, y, s, side_stream, info);
+        }
+        g->exec = exec;
+        g->state = 1;
+    }
+    const cudaError_t ce = cudaGraphLaunch(g->exec, s);
+    if (ce != cudaSuccess) {
+        pqe::set_last_cuda_error(ce);
+        return PQE_ERR_CUDA;
+    }
+    if (info) *info = pqe_step_info{};
+    return PQE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 int pqe_layer_step_host(pqe_layer *L, const void *x_host, const float *w_router_dev, const float *logits_host, int T,
                         void *y_host, void *stream, void *side_stream, pqe_step_info *info) {
     if (!L || T < 0 || T > L->cfg.max_T || !x_host || !y_host || (!w_router_dev && !logits_host))
@@ -527,7 +623,7 @@ int pqe_layer_step_host(pqe_layer *L, const void *x_host, const float *w_router_
         pqe::set_last_cuda_error(ce);
         return PQE_ERR_CUDA;
     }
-    int rc = pqe_layer_step(L, x_in, w_router_dev, w_router_dev ? nullptr : lg, T, y, stream, side_stream, info);
+    int rc = step_host_launches(L, x_in, w_router_dev, w_router_dev ? nullptr : lg, T, y, s, side_stream, info);
     if (rc) return rc;
     ce = cudaMemcpyAsync(y_host, y, sizeof(uint16_t) * (size_t)T * c.H, cudaMemcpyDeviceToHost, s);
     if (ce == cudaSuccess) ce = cudaStreamSynchronize(s);

@@ -33,7 +33,11 @@ void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 static std::atomic<uint32_t> g_wait_limit{DEFAULT_WAIT_LIMIT};
 static std::atomic<uint32_t> g_phase2_bias{0};
 static std::atomic<int> g_stream_kernel{0};
+// bumped by every setter above: a captured launch keeps the values it read,
+// so a cached graph of a layer step is rebuilt when this changes
+static std::atomic<uint64_t> g_launch_gen{0};
 
+uint64_t launch_settings_generation() { return g_launch_gen.load(std::memory_order_relaxed); }
 uint32_t wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
 uint32_t phase2_bias() { return g_phase2_bias.load(std::memory_order_relaxed); }
 int stream_kernel_choice() { return g_stream_kernel.load(std::memory_order_relaxed); }
@@ -69,17 +73,20 @@ int pqe_abi_version(void) { return 1; }
 
 int pqe_set_wait_limit(uint32_t polls) {
     pqe::g_wait_limit.store(polls ? polls : pqe::DEFAULT_WAIT_LIMIT, std::memory_order_relaxed);
+    pqe::g_launch_gen.fetch_add(1, std::memory_order_relaxed);
     return PQE_OK;
 }
 
 int pqe_test_set_phase2_bias(uint32_t bias) {
     pqe::g_phase2_bias.store(bias, std::memory_order_relaxed);
+    pqe::g_launch_gen.fetch_add(1, std::memory_order_relaxed);
     return PQE_OK;
 }
 
 int pqe_test_set_stream_kernel(int kind) {
     if (kind < 0 || kind > 2) return PQE_ERR_INVALID_ARG;
     pqe::g_stream_kernel.store(kind, std::memory_order_relaxed);
+    pqe::g_launch_gen.fetch_add(1, std::memory_order_relaxed);
     return PQE_OK;
 }
 

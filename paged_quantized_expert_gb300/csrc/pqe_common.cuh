@@ -118,6 +118,9 @@ uint32_t phase2_bias();
 // takes, 0 the default choice, 1 the CUDA-core stream, 2 the tensor-core
 // stream where it applies; read on the host at each launch.
 int stream_kernel_choice();
+// Changes whenever one of the settings above does (graphs captured before it
+// hold the old values).
+uint64_t launch_settings_generation();
 
 // The current device and its SM count, cached per device (a process may drive
 // several GPUs; launch attributes such as the dynamic shared-memory opt-in are

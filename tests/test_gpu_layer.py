@@ -353,6 +353,66 @@ def test_layer_device_pager_graph_replay(cuda_lib, orc, groups):
     layer.close()
 
 
+@pytest.mark.parametrize("groups", [0, 3])
+def test_layer_step_host_graph_replays(cuda_lib, orc, groups):
+    # pqe_layer_step_host on a device-pager layer replays each step shape from a
+    # graph after its second call: y, the page table and the LRU state equal
+    # those of the same layer stepping eagerly, bit for bit, across step sizes,
+    # a changed wait limit (the graph is captured again) and the oracle's LRU;
+    # replayed calls count no launch of their own
+    pqe = cuda_lib
+    cfg = synth.small_config(E=16, H=256, I=128, k=2, T=8, S=4, cid=81, reuse_p=0.5, zipf_s=1.1,
+                             router_gemm=False, steps=14)
+    pages = Pages(pqe, orc, cfg, needed=set(range(cfg.E)), seed=12)
+    host, nbytes = _host_tier(pqe, pages)
+    mk = lambda: pqe.PagedMoELayer(cfg.E, cfg.H, cfg.I, cfg.k, cfg.S, cfg.E, 8, host, nbytes,
+                                   expert_fmt=pages.fmt_dev, device_pager=True, overlap_groups=groups)
+    graphed, eager = mk(), mk()
+    eager.set_step_graphs(False)
+    stream, side = torch.cuda.Stream(), torch.cuda.Stream()
+    Ts = [8, 8, 8, 5, 8, 5, 5, 8, 8, 3, 5, 8, 8, 8]
+    ref_lru = orc.LRU(cfg.E, cfg.S)
+    y_g = torch.zeros((8, cfg.H), dtype=torch.int16).pin_memory()
+    y_e = torch.zeros_like(y_g).pin_memory()
+    calls = {}  # calls of each step size since the settings last changed
+    try:
+        for s, T in enumerate(Ts):
+            if s == 9:
+                pqe.pqe_set_wait_limit(1 << 23)  # a new setting: shapes are captured again
+                calls = {}
+            tr = synth.RoutingTrace(cfg, T)
+            lg = tr.step(s)
+            x_np = synth.activations(cfg, T, s)
+            x_h = torch.from_numpy(x_np.view(np.int16)).pin_memory()
+            lg_h = torch.from_numpy(lg).pin_memory()
+            n0 = pqe.kernel_launches()
+            graphed.step_host(x_h, y_g, T, logits_host=lg_h, stream=stream, side_stream=side)
+            n_graphed = pqe.kernel_launches() - n0
+            eager.step_host(x_h, y_e, T, logits_host=lg_h, stream=stream, side_stream=side)
+            c = calls.get(T, 0)  # 0: eager, 1: captured and launched, then replays
+            assert (n_graphed == 0) == (c >= 2), (s, T, c, n_graphed)
+            calls[T] = c + 1
+            assert torch.equal(y_g[:T], y_e[:T]), s
+            pt0 = graphed.device_view("page_table", torch.int32, (cfg.E,)).clone()
+            pt1 = eager.device_view("page_table", torch.int32, (cfg.E,)).clone()
+            assert torch.equal(pt0, pt1), s
+            ids, gates = orc.topk_gates(lg, cfg.k)
+            ref_lru.step(np.bincount(ids.reshape(-1), minlength=cfg.E).astype(np.int32))
+            se, lu, st = graphed.lru_state()
+            se2, lu2, st2 = ref_lru.state()
+            assert np.array_equal(se.numpy(), se2) and np.array_equal(lu.numpy(), lu2) and st == st2, s
+            ref = orc.moe_ffn(x_np, ids, gates, pages.experts, cfg.I)
+            y = y_g[:T].view(torch.bfloat16)
+            st_ = helpers.error_stats(helpers.bf16_to_f64(y), ref)
+            bound = helpers.l2_bounds(ids, np.arange(T), cfg.E, (), cfg.H, cfg.I)
+            assert st_["max_over_l2"] <= helpers.TOL_MAX_OVER_L2 and np.all(st_["l2_per_token"] <= bound), (s, st_)
+    finally:
+        pqe.pqe_set_wait_limit(0)
+    for l in (graphed, eager):
+        assert l.device_view("status", torch.int32, (1,)).item() == 0
+        l.close()
+
+
 def test_layer_mixed_precision_reranking(cuda_lib, orc):
     # config-5 behaviour at a small size: every `every` steps the experts are
     # re-ranked by the EMA of their gate mass; the top quarter keep FP8 pages,
