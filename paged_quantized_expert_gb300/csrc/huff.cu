@@ -228,10 +228,12 @@ void histogram(const uint8_t *q, size_t n, uint64_t freq[16]) {
 //      offsets and chunk bit offsets (the source may be device memory or
 //      pinned host memory read over the host link);
 //   2. it stages the block's code words in shared memory (16-byte loads) and
-//      each thread decodes its two chunks together: one table lookup yields
-//      every whole code word at the front of the 12-bit window (up to 5), the
-//      exponent nibbles collect in a 64-bit accumulator and leave eight at a
-//      time into a shared exponent plane;
+//      each thread decodes two chunks: two neighbours of one row as a single
+//      128-symbol run where rows have an even number of chunks, else two
+//      chunks one after the other. One table lookup yields every whole code
+//      word at the front of the 12-bit window (up to 5), the exponent nibbles
+//      collect in a 64-bit accumulator and leave eight at a time into a shared
+//      exponent plane;
 //   3. it loads the raw-nibble plane (16-byte loads) and combines it with the
 //      exponent plane into FP8 bytes, written with coalesced 16-byte stores.
 // Every read is bounded by the page size; a row that does not decode sets
@@ -248,6 +250,8 @@ constexpr int HD_UNIT_CHUNKS = 2 * HD_THREADS;  // chunks per CTA (two per threa
 constexpr int HD_SPAN_WORDS = PQE_HD_SPAN_WORDS; // code words staged per pass
 constexpr int HD_SPAN_PAD = 32;                 // zero words after them (a chunk reads <= 25 words ahead)
 constexpr int HD_EXP_STRIDE = 9;                // exponent-plane words per chunk: 8 + 1 (bank spread)
+constexpr int HD_PAIR_STRIDE = 17;              // per pair of chunks decoded as one run: 16 + 1
+static_assert(HD_THREADS * HD_PAIR_STRIDE <= HD_UNIT_CHUNKS * HD_EXP_STRIDE, "pair plane larger than the chunk plane");
 constexpr int HD_LUT_WORDS = PQE_HUFF_LUT_BYTES / 4;
 constexpr int HD_MAX_PAGES = 128;               // pages per launch (kernel parameter block)
 constexpr int HD_RW_WORDS = HD_UNIT_CHUNKS + 4; // row offsets of a block (<= 512 rows + 1)
@@ -322,10 +326,11 @@ __host__ __device__ __forceinline__ uint2 fp8_bytes8(uint32_t e, uint32_t r) {
     return make_uint2(bperm(b_ev, b_od, 0x5140), bperm(b_ev, b_od, 0x7362));
 }
 
-// Decoder state of one 64-symbol chunk. span: the row's code words, followed
-// by at least HD_SPAN_PAD readable words (a chunk reads at most 64 * 12 bits
-// past its start); pos: the next bit of span; eb: the chunk's 8 exponent words
-// (eight nibbles each, first symbol lowest). Every step does the same work (no
+// Decoder state of a run of 64-symbol chunks that follow each other in one
+// row's code stream. span: the row's code words, followed by at least
+// HD_SPAN_PAD readable words (a chunk reads at most 64 * 12 bits past its
+// start); pos: the next bit of span; eb: the run's exponent words (eight
+// nibbles each, first symbol lowest). Every step does the same work (no
 // refill or emit branch, which would diverge across the lanes of a warp): the
 // 12-bit window is cut from two span words at the bit position, and an
 // exponent word is stored once complete.
@@ -356,18 +361,20 @@ struct ChunkDec {
         acc_hi = full ? 0u : acc_hi;
         na4 -= full ? 32u : 0u;
     }
-    // one lookup taking all of its (at most 5) symbols: while o < 7. An
-    // invalid window consumes no bits, so once met it is met again by every
+    // one lookup taking all of its (at most 5) symbols: while o < words - 1.
+    // An invalid window consumes no bits, so once met it is met again by every
     // later lookup: finish() alone checks for it.
     __host__ __device__ __forceinline__ void step(const uint32_t *__restrict__ lut,
                                                   const uint32_t *__restrict__ span) {
         const uint32_t ent = window(lut, span);
         take((ent >> 2) & 0x1Cu, ent & 15u, ent >> 12);
     }
-    // the last 8 symbols: a lookup with more than needed contributes its first
+    // the last 8 symbols of a run of `words` exponent words: a lookup with more
+    // than needed contributes its first
     __host__ __device__ __forceinline__ void finish(const uint32_t *__restrict__ lut,
-                                                    const uint32_t *__restrict__ span, uint32_t &bad) {
-        while (o < 8) {
+                                                    const uint32_t *__restrict__ span, uint32_t words,
+                                                    uint32_t &bad) {
+        while (o < words) {
             const uint32_t ent = window(lut, span);
             bad |= ent;
             const uint32_t n4 = (ent >> 2) & 0x1Cu;
@@ -377,16 +384,20 @@ struct ChunkDec {
     }
 };
 
-// Decodes one chunk starting at bit `pos` of span, whose row ends at bit
-// `end`. Returns false for a stream that does not decode.
-__host__ __device__ __forceinline__ bool decode_chunk(const uint32_t *__restrict__ lut,
-                                                      const uint32_t *__restrict__ span, uint32_t pos, uint32_t end,
-                                                      uint32_t *__restrict__ eb) {
+// Decodes NCH consecutive chunks of one row (8 NCH exponent words) starting
+// at bit `pos` of span, the row ending at bit `end`. Chunks of a row follow
+// each other in its code stream, so a run needs only its first chunk's offset,
+// and a lookup that crosses from one of its chunks into the next takes all of
+// its symbols. Returns false for a stream that does not decode.
+template <int NCH>
+__host__ __device__ __forceinline__ bool decode_chunks(const uint32_t *__restrict__ lut,
+                                                       const uint32_t *__restrict__ span, uint32_t pos, uint32_t end,
+                                                       uint32_t *__restrict__ eb) {
     ChunkDec a;
     a.init(pos, eb);
     uint32_t bad = 0;
-    while (a.o < 7) a.step(lut, span);
-    a.finish(lut, span, bad);
+    while (a.o < 8 * NCH - 1) a.step(lut, span);
+    a.finish(lut, span, 8 * NCH, bad);
     return !(bad & 0x800u) && a.pos <= end;
 }
 
@@ -436,9 +447,14 @@ __device__ void decode_block(const HuffGeo &b, const uint8_t *comp, uint64_t cby
     for (int i = tid; i < HD_LUT_WORDS / 4; i += HD_THREADS) reinterpret_cast<uint4 *>(lut)[i] = lut_g[i];
     const uint32_t *rw_g = reinterpret_cast<const uint32_t *>(comp + d.off_row_word) + r0;
     for (int i = tid; i <= nr; i += HD_THREADS) rw[i] = rw_g[i];
+    // rows of an even number of chunks: thread t decodes chunks 2t and 2t + 1
+    // as one run (half the lookups that straddle a chunk end, and one loop
+    // whose length varies less across a warp); otherwise chunks t and t + 256
+    const bool pairs = (nc & 1) == 0;
     const uint16_t *cb_g = reinterpret_cast<const uint16_t *>(comp + d.off_chunk_bit) + (size_t)r0 * nc;
-    const uint32_t cb0 = tid < nch ? cb_g[tid] : 0u;
-    const uint32_t cb1 = tid + HD_THREADS < nch ? cb_g[tid + HD_THREADS] : 0u;
+    const int c0 = pairs ? 2 * tid : tid;
+    const uint32_t cb0 = c0 < nch ? cb_g[c0] : 0u;
+    const uint32_t cb1 = !pairs && tid + HD_THREADS < nch ? cb_g[tid + HD_THREADS] : 0u;
     const uint4 *nib_g = reinterpret_cast<const uint4 *>(comp + d.off_nibbles + (size_t)r0 * cols / 2);
     uint4 nib[4];  // the raw-nibble plane, loaded now and used after the decode
 #pragma unroll
@@ -483,20 +499,30 @@ __device__ void decode_block(const HuffGeo &b, const uint8_t *comp, uint64_t cby
             reinterpret_cast<uint4 *>(span)[i] = *reinterpret_cast<const uint4 *>(comp + a0 + 16 * (uint64_t)i);
         if (tid < HD_SPAN_PAD) span[4 * nq + tid] = 0;
         __syncthreads();
-#pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
-            const int c = tid + HD_THREADS * j;
-            if (c >= nch) break;
-            const int rr = c / nc;
-            if (rr < ga || rr >= gb) continue;
-            const uint32_t sb = j ? cb1 : cb0;
-            const uint32_t row0 = 32 * (dsh + rw[rr] - rw[ga]);  // row start, in bits of span
-            const uint32_t row_bits = 32 * (rw[rr + 1] - rw[rr]);
-            if (sb >= row_bits) {  // a chunk that starts past its row
-                ok = false;
-                continue;
+        if (pairs) {
+            const int rr = c0 / nc;
+            if (c0 < nch && rr >= ga && rr < gb) {
+                const uint32_t row0 = 32 * (dsh + rw[rr] - rw[ga]);  // row start, in bits of span
+                const uint32_t row_bits = 32 * (rw[rr + 1] - rw[rr]);
+                if (cb0 >= row_bits) ok = false;  // a chunk that starts past its row
+                else ok &= decode_chunks<2>(lut, span, row0 + cb0, row0 + row_bits, expb + tid * HD_PAIR_STRIDE);
             }
-            ok &= decode_chunk(lut, span, row0 + sb, row0 + row_bits, expb + c * HD_EXP_STRIDE);
+        } else {
+#pragma unroll 1
+            for (int j = 0; j < 2; ++j) {
+                const int c = tid + HD_THREADS * j;
+                if (c >= nch) break;
+                const int rr = c / nc;
+                if (rr < ga || rr >= gb) continue;
+                const uint32_t sb = j ? cb1 : cb0;
+                const uint32_t row0 = 32 * (dsh + rw[rr] - rw[ga]);
+                const uint32_t row_bits = 32 * (rw[rr + 1] - rw[rr]);
+                if (sb >= row_bits) {
+                    ok = false;
+                    continue;
+                }
+                ok &= decode_chunks<1>(lut, span, row0 + sb, row0 + row_bits, expb + c * HD_EXP_STRIDE);
+            }
         }
         __syncthreads();
         ga = gb;
@@ -509,7 +535,8 @@ __device__ void decode_block(const HuffGeo &b, const uint8_t *comp, uint64_t cby
     for (int i = 0; i < 4; ++i) {
         const int q = tid + HD_THREADS * i;  // 32 symbols: chunk q / 2, half q % 2
         if (q >= 2 * nch) break;
-        const uint32_t *e = expb + (q >> 1) * HD_EXP_STRIDE + 4 * (q & 1);
+        const uint32_t *e = expb + (pairs ? (q >> 2) * HD_PAIR_STRIDE + 4 * (q & 3)
+                                          : (q >> 1) * HD_EXP_STRIDE + 4 * (q & 1));
         const uint2 a = fp8_bytes8(e[0], nib[i].x), bb = fp8_bytes8(e[1], nib[i].y);
         const uint2 c = fp8_bytes8(e[2], nib[i].z), dd = fp8_bytes8(e[3], nib[i].w);
         dst[2 * q] = make_uint4(a.x, a.y, bb.x, bb.y);
