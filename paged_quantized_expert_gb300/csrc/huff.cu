@@ -401,6 +401,16 @@ __host__ __device__ __forceinline__ bool decode_chunks(const uint32_t *__restric
     return !(bad & 0x800u) && a.pos <= end;
 }
 
+// 16-byte global -> shared copies that complete asynchronously (no register
+// staging): the code table is requested at block start and lands while the
+// header and the row offsets are read
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(smem_dst)),
+                 "l"(gmem_src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // geometry of a page's decode blocks (the same for every page of a layer)
 struct HuffGeo {
     int H, I;
@@ -423,7 +433,11 @@ __device__ void decode_block(const HuffGeo &b, const uint8_t *comp, uint64_t cby
 
     const int tid = threadIdx.x;
     const int H = b.H, I = b.I;
+    const bool first = u < b.units13;
 
+    // 1. code table (asynchronous), header
+    const uint4 *lut_g = reinterpret_cast<const uint4 *>(first ? lut13g : lut2g);
+    for (int i = tid; i < HD_LUT_WORDS / 4; i += HD_THREADS) cp_async16(reinterpret_cast<uint4 *>(lut) + i, lut_g + i);
     if (tid < (int)(HUF_HEADER / 16) && cbytes >= HUF_HEADER)
         reinterpret_cast<uint4 *>(hdr)[tid] = reinterpret_cast<const uint4 *>(comp)[tid];
     __syncthreads();
@@ -431,9 +445,9 @@ __device__ void decode_block(const HuffGeo &b, const uint8_t *comp, uint64_t cby
     __syncthreads();
     if (!*flag) {
         if (tid == 0 && u == 0) atomicOr(status, PQE_STATUS_CORRUPT_STREAM);
+        cp_async_wait_all();  // the table's copies land before the block's shared memory is reused
         return;
     }
-    const bool first = u < b.units13;
     const int rows = first ? 2 * I : H, cols = first ? H : I, nc = cols / HUF_CHUNK;
     const int R = first ? b.rows13_unit : b.rows2_unit;
     const int r0 = (first ? u : u - b.units13) * R;
@@ -442,9 +456,7 @@ __device__ void decode_block(const HuffGeo &b, const uint8_t *comp, uint64_t cby
     const HuffMatrixDesc d = first ? hdr->m13 : hdr->m2;
     const PageLayout L = fp8_layout(H, I);
 
-    // 1. code table, row offsets, chunk offsets, raw nibbles (registers), scales
-    const uint4 *lut_g = reinterpret_cast<const uint4 *>(first ? lut13g : lut2g);
-    for (int i = tid; i < HD_LUT_WORDS / 4; i += HD_THREADS) reinterpret_cast<uint4 *>(lut)[i] = lut_g[i];
+    // row offsets, chunk offsets, raw nibbles (registers), scales
     const uint32_t *rw_g = reinterpret_cast<const uint32_t *>(comp + d.off_row_word) + r0;
     for (int i = tid; i <= nr; i += HD_THREADS) rw[i] = rw_g[i];
     // rows of an even number of chunks: thread t decodes chunks 2t and 2t + 1
@@ -475,6 +487,7 @@ __device__ void decode_block(const HuffGeo &b, const uint8_t *comp, uint64_t cby
     int bad = 0;
     for (int i = tid; i < nr; i += HD_THREADS) bad |= rw[i + 1] < rw[i] || rw[i + 1] - rw[i] > cap;
     if (tid == 0) bad |= rw[nr] > d.n_words;
+    cp_async_wait_all();  // this thread's table copies; the barriers below publish them
     if (__syncthreads_or(bad)) {
         if (tid == 0) atomicOr(status, PQE_STATUS_CORRUPT_STREAM);
         return;
@@ -496,8 +509,9 @@ __device__ void decode_block(const HuffGeo &b, const uint8_t *comp, uint64_t cby
         const uint64_t a1 = round_up(d.off_words + 4 * (uint64_t)rw[gb], 16);
         const int nq = (int)((a1 - a0) / 16);
         for (int i = tid; i < nq; i += HD_THREADS)
-            reinterpret_cast<uint4 *>(span)[i] = *reinterpret_cast<const uint4 *>(comp + a0 + 16 * (uint64_t)i);
+            cp_async16(reinterpret_cast<uint4 *>(span) + i, comp + a0 + 16 * (uint64_t)i);
         if (tid < HD_SPAN_PAD) span[4 * nq + tid] = 0;
+        cp_async_wait_all();
         __syncthreads();
         if (pairs) {
             const int rr = c0 / nc;
