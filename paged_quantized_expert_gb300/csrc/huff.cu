@@ -467,22 +467,15 @@ __device__ void decode_block(const HuffGeo &b, const uint8_t *comp, uint64_t cby
     const int c0 = pairs ? 2 * tid : tid;
     const uint32_t cb0 = c0 < nch ? cb_g[c0] : 0u;
     const uint32_t cb1 = !pairs && tid + HD_THREADS < nch ? cb_g[tid + HD_THREADS] : 0u;
-    // the raw-nibble plane of the 32-symbol halves of chunks this thread's warp
-    // decodes (half q of chunk q / 2), loaded now and used after the decode: a
-    // warp combines only its own chunks, so no block-wide barrier lies between
-    // its decode and its stores
+    // the 32-symbol halves of the chunks this thread's warp decodes (half q of
+    // chunk q / 2): a warp combines only its own chunks, so no block-wide
+    // barrier lies between its decode and its stores
     const int warp = tid >> 5, lane = tid & 31;
     auto half_of = [&](int i) {
         return (pairs ? 128 * warp + 32 * i : (i < 2 ? 64 * warp + 32 * i : 2 * HD_THREADS + 64 * warp + 32 * (i - 2))) +
                lane;
     };
     const uint4 *nib_g = reinterpret_cast<const uint4 *>(comp + d.off_nibbles + (size_t)r0 * cols / 2);
-    uint4 nib[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int q = half_of(i);
-        nib[i] = q < 2 * nch ? nib_g[q] : make_uint4(0, 0, 0, 0);
-    }
     if (u == 0) {
         const uint4 *sc = reinterpret_cast<const uint4 *>(comp + hdr->off_scales);
         uint4 *so = reinterpret_cast<uint4 *>(page_out + L.s13);
@@ -557,6 +550,12 @@ __device__ void decode_block(const HuffGeo &b, const uint8_t *comp, uint64_t cby
     // 3. exponent plane + raw nibbles -> FP8 bytes, 32 per thread and slice,
     // over the halves of the warp's own chunks (their exponent words are this
     // warp's stores)
+    uint4 nib[4];  // loaded once the warp's decode is done; other warps' decode hides the latency
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int q = half_of(i);
+        nib[i] = q < 2 * nch ? nib_g[q] : make_uint4(0, 0, 0, 0);
+    }
     __syncwarp();
     uint4 *dst = reinterpret_cast<uint4 *>(page_out + (first ? L.w13 : L.w2) + (size_t)r0 * cols);
 #pragma unroll
