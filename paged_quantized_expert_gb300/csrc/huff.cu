@@ -248,7 +248,7 @@ void histogram(const uint8_t *q, size_t n, uint64_t freq[16]) {
 constexpr int HD_THREADS = PQE_HD_THREADS;
 constexpr int HD_UNIT_CHUNKS = 2 * HD_THREADS;  // chunks per CTA (two per thread)
 constexpr int HD_SPAN_WORDS = PQE_HD_SPAN_WORDS; // code words staged per pass
-constexpr int HD_SPAN_PAD = 32;                 // zero words after them (a chunk reads <= 25 words ahead)
+constexpr int HD_SPAN_PAD = 64;                 // zero words after them (a run of two chunks reads <= 49 words ahead)
 constexpr int HD_EXP_STRIDE = 9;                // exponent-plane words per chunk: 8 + 1 (bank spread)
 constexpr int HD_PAIR_STRIDE = 17;              // per pair of chunks decoded as one run: 16 + 1
 static_assert(HD_THREADS * HD_PAIR_STRIDE <= HD_UNIT_CHUNKS * HD_EXP_STRIDE, "pair plane larger than the chunk plane");
@@ -328,8 +328,8 @@ __host__ __device__ __forceinline__ uint2 fp8_bytes8(uint32_t e, uint32_t r) {
 
 // Decoder state of a run of 64-symbol chunks that follow each other in one
 // row's code stream. span: the row's code words, followed by at least
-// HD_SPAN_PAD readable words (a chunk reads at most 64 * 12 bits past its
-// start); pos: the next bit of span; eb: the run's exponent words (eight
+// HD_SPAN_PAD readable words (a run of n chunks reads at most n * 64 * 12 bits
+// past its start, and one word more); pos: the next bit of span; eb: the run's exponent words (eight
 // nibbles each, first symbol lowest). Every step does the same work (no
 // refill or emit branch, which would diverge across the lanes of a warp): the
 // 12-bit window is cut from two span words at the bit position, and an
